@@ -1,0 +1,270 @@
+/*
+ * psg.h -- C ABI of the primitive-op graph hot path on GB300 (sm_103a).
+ *
+ * The library executes the data-parallel kernels of a lazy graph over a closed
+ * set of primitive ops (limn, "The op set": sources, VIEW, NEG EXP LOG SQRT
+ * RECIP CAST, ADD MUL CMPLT, WHERE, SUM MAX, GATHER SCATTER) on tensors laid
+ * out by a View (limn, "Three rules hold it together": shape, strides, offset,
+ * mask).  Five call families:
+ *   psg_elementwise   a fused elementwise chain over Views;
+ *   psg_reduce_rows   SUM/MAX row reductions with fused prologue/epilogue;
+ *   psg_permute       CONTIGUOUS of a permuted View (tiled transpose);
+ *   psg_contract      matmul as a broadcast MUL followed by a SUM over k;
+ *   psg_gather / psg_scatter_add   the indexed ops along dim 0.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory: every pointer argument named as device memory must point to memory
+ *   the CUDA device can address (cudaMalloc / torch CUDA tensors).  The caller
+ *   owns every buffer, workspace and stream; the library allocates no device
+ *   memory, never synchronises, and keeps no mutable global state.
+ * Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every
+ *   call only enqueues work on it and returns.
+ * Errors: host-side validation happens before any launch and returns a
+ *   psg_status; nothing is launched when it is not PSG_OK.  Errors found on the
+ *   device (a GATHER index out of range, a bounded wait that gave up) are
+ *   written as a psg_status code into the caller's `d_status` word (device
+ *   memory, zeroed by the caller) and read after a synchronise.  The library
+ *   never traps.  An unsupported dtype, layout or program returns its own
+ *   code; no call silently runs a different implementation (Tiki, "Compile
+ *   model code": unsupported contracts raise a typed error).
+ * Thread safety: calls may be made from several host threads at once.
+ */
+#ifndef PSG_H
+#define PSG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PSG_OK = 0,
+    PSG_E_INVALID_ARG = 1,          /* null pointer, bad count, shapes that disagree */
+    PSG_E_UNSUPPORTED_DTYPE = 2,    /* dtype combination this call does not implement */
+    PSG_E_UNSUPPORTED_LAYOUT = 3,   /* view layout this call does not implement */
+    PSG_E_OUT_OF_BOUNDS_VIEW = 4,   /* a reachable element lies outside [0, extent) */
+    PSG_E_MISALIGNED = 5,           /* pointer not aligned to its element size */
+    PSG_E_INDEX_OUT_OF_RANGE = 6,   /* device-reported: GATHER/SCATTER index outside [0, V) */
+    PSG_E_TIMEOUT = 7,              /* device-reported: a bounded wait gave up */
+    PSG_E_CUDA = 8,                 /* a CUDA runtime call or launch failed */
+    PSG_E_UNSUPPORTED_PROGRAM = 9,  /* program too long / needs too many live values */
+    PSG_E_WORKSPACE = 10            /* workspace missing or too small */
+} psg_status;
+
+/* The seven dtypes (limn, "The op set", dtype paragraph).  float16/bfloat16
+ * are storage widths: kernels widen them to float32 to compute and reductions
+ * keep float32 running totals, rounding once at the end. */
+typedef enum {
+    PSG_F32 = 0, PSG_BF16 = 1, PSG_F16 = 2, PSG_F64 = 3, PSG_I32 = 4, PSG_I16 = 5, PSG_I8 = 6
+} psg_dtype;
+
+#define PSG_MAX_DIMS 8
+
+/* A View (limn, "Three rules hold it together"): the element with
+ * multi-index (i_0 .. i_{ndim-1}), 0 <= i_d < shape[d], reads
+ *     base[offset + sum_d i_d * strides[d]]
+ * when mask_lo[d] <= i_d < mask_hi[d] for every d, and reads a zero of the
+ * dtype otherwise (a padded read; limn, "Reading the schedule").
+ * Units are elements, not bytes.  strides[d] >= 0 (0 = expand/broadcast; a
+ * step other than 1 has no View behind it, so there are no negative strides).
+ * offset may be negative when masking keeps every reachable read in range.
+ * extent = number of elements in the allocation `base` points to; every
+ * reachable (unmasked) element must lie in [0, extent), or the call returns
+ * PSG_E_OUT_OF_BOUNDS_VIEW.  A View that is written must be injective (no
+ * stride-0 dim of size > 1, no overlapping dims) and unmasked.
+ * ndim 0 is a scalar (one element). */
+typedef struct {
+    int32_t ndim;
+    int32_t dtype; /* psg_dtype */
+    int64_t shape[PSG_MAX_DIMS];
+    int64_t strides[PSG_MAX_DIMS];
+    int64_t offset;
+    int64_t mask_lo[PSG_MAX_DIMS];
+    int64_t mask_hi[PSG_MAX_DIMS];
+    int64_t extent;
+} psg_view;
+
+/* Program nodes.  A program is an array of nodes in topological order; a
+ * node's operands name earlier nodes by index; the last node is the result.
+ * Every node carries the dtype of its value and rounds to it (the per-node
+ * semantics of limn's numpy device).  Operand dtype rules (validated):
+ *   NEG EXP LOG SQRT RECIP: operand dtype == node dtype (EXP LOG SQRT RECIP
+ *       float only);  ADD MUL CMPLT: both operands have the node dtype; CMPLT
+ *       yields 1 or 0 of that dtype (a NaN operand compares false);
+ *   WHERE(a=cond, b=x, c=y): cond any dtype, true when nonzero (NaN is
+ *       nonzero); x, y have the node dtype;
+ *   CAST(a): any dtype -> node dtype (float->float round to nearest even;
+ *       float->int truncates toward zero with NaN -> 0 and saturation to the
+ *       int32 range, then wraps to the width; int->float converts to float32
+ *       and rounds to the width; int->int wraps);
+ *   LOAD(a=input index): the node dtype must equal that input's view dtype;
+ *   CONST: value cval rounded into the node dtype;
+ *   RED(a=stage index): (psg_reduce_rows only) the reduced value of an
+ *       earlier stage, in that stage's dtype.
+ * float64 nodes are not implemented yet (PSG_E_UNSUPPORTED_DTYPE). */
+typedef enum {
+    PSG_OP_LOAD = 0, PSG_OP_CONST = 1, PSG_OP_RED = 2,
+    PSG_OP_NEG = 3, PSG_OP_EXP = 4, PSG_OP_LOG = 5, PSG_OP_SQRT = 6, PSG_OP_RECIP = 7,
+    PSG_OP_CAST = 8, PSG_OP_ADD = 9, PSG_OP_MUL = 10, PSG_OP_CMPLT = 11, PSG_OP_WHERE = 12
+} psg_op;
+
+typedef struct {
+    int32_t op;    /* psg_op */
+    int32_t a, b, c;
+    int32_t dtype; /* psg_dtype of the node's value */
+    int32_t reserved;
+    double cval;   /* PSG_OP_CONST only */
+} psg_node;
+
+#define PSG_MAX_NODES 64
+#define PSG_MAX_INPUTS 8
+
+/* ---------------------------------------------------------------------------
+ * psg_elementwise -- realise a fused elementwise chain (limn, "Reading the
+ * schedule": elementwise work fuses into one kernel; "Backends": one thread
+ * per output cell, here 8 cells per thread with 128-bit loads).
+ *   out[i] = prog(in_0[i], ..., in_{n_in-1}[i])   for every multi-index i of
+ *   out_v's shape.
+ * prog/n_nodes: host memory, 1..PSG_MAX_NODES nodes (no PSG_OP_RED).
+ * in[k]: device pointers; in_v[k]: host array of n_in (<= PSG_MAX_INPUTS)
+ *   views, each with out_v's ndim and shape (broadcasting is a stride-0 dim).
+ * out/out_v: device pointer and its view (unmasked, injective); its dtype must
+ *   equal the last node's dtype.  `out` must not overlap any input unless the
+ *   two views are identical.
+ * Returns PSG_OK or a validation error; the kernel itself cannot fail.
+ * ------------------------------------------------------------------------- */
+psg_status psg_elementwise(const psg_node* prog, int n_nodes, const void* const* in,
+                           const psg_view* in_v, int n_in, void* out, const psg_view* out_v,
+                           void* stream);
+
+/* ---------------------------------------------------------------------------
+ * psg_reduce_rows -- SUM/MAX over the last dim with fused prologue and
+ * epilogue (limn, "Reading the schedule": a reduce is a cut and elementwise
+ * work fuses into it; "Backends": a long reduce splits into partial totals and
+ * a fold; the dtype paragraph: float32 running totals, rounded once).
+ *
+ * Every input view has the iteration shape [R_0 .. R_{d-2}, N]; the last dim
+ * is the reduced one.  Stages run in order; stage s computes, for every row r,
+ *     red_s[r] = fold_{j=0..N-1} prologue_s(r, j)
+ * with SUM (identity 0) or MAX (identity -inf; NaN propagates; +0 wins a tie
+ * with -0).  The fold keeps a float32 total for float dtypes (int32 wrapping
+ * total for ints) and rounds to the stage dtype (the prologue result dtype)
+ * once.  A prologue may read inputs, constants and earlier stages' values
+ * (PSG_OP_RED a=s).  After the stages:
+ *   - if out_v's last dim is N: out[r, j] = epilogue(r, j) per element
+ *     (softmax: two stages, MAX then SUM(EXP(x - m)), epilogue e * RECIP(s));
+ *   - if out_v's last dim is 1 (keepdim) or out_v drops it: out[r] =
+ *     epilogue(r) evaluated once per row, where the epilogue may read only
+ *     constants and stage values; with n_epi == 0 out[r] = red_{last}[r].
+ * The sum of N values deviates from the exact sum by at most
+ * gamma_{N-1} * sum |x_j| in any association order (Litmus, "ToleranceBound",
+ * the reduction_order term), which is the tolerance this call is tested to.
+ * stages: host array of n_stages (1..4) stage descriptors, each pointing to a
+ *   host program.  epilogue: host program or NULL.
+ * d_status: device int32 or NULL (this call reports nothing on the device yet;
+ *   the word is accepted for a uniform signature).
+ * ------------------------------------------------------------------------- */
+typedef enum { PSG_RED_SUM = 0, PSG_RED_MAX = 1 } psg_red_op;
+
+typedef struct {
+    int32_t op;             /* psg_red_op */
+    int32_t n_nodes;
+    const psg_node* prologue;
+} psg_reduce_stage;
+
+psg_status psg_reduce_rows(const psg_reduce_stage* stages, int n_stages, const psg_node* epilogue,
+                           int n_epi, const void* const* in, const psg_view* in_v, int n_in,
+                           void* out, const psg_view* out_v, int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * psg_permute -- CONTIGUOUS(VIEW(permute(perm)) of in): out[i_0..i_{n-1}] =
+ * in[j] with j_{perm[d]} = i_d (limn, "Three rules": permute is a View;
+ * "Reading the schedule": a copy is a cut).  A 2-D transpose takes the tiled
+ * shared-memory path (Tiki, "What works today": swizzled transpose).
+ * perm: host array of in_v->ndim distinct dims.  out_v: shape[d] =
+ * in_v->shape[perm[d]], same dtype, unmasked and injective (contiguous is the
+ * fast path).  Bit-exact: only bytes move.
+ * ------------------------------------------------------------------------- */
+psg_status psg_permute(const void* in, const psg_view* in_v, const int32_t* perm, void* out,
+                       const psg_view* out_v, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * psg_contract -- matmul as MUL of two broadcast Views followed by a SUM over
+ * the last dim (limn, "Reading the schedule": a whole matmul is one kernel and
+ * the (M,N,1) result aliases the (M,N) sink; Luminal IR blog, "Naive Matrix
+ * Multiplication": the broadcast is a stride-0 loop):
+ *     C[b.., m, n] = sum_{k ascending in the reference} Av[b.., m, n, k] * Bv[b.., m, n, k]
+ * Av, Bv: views of rank 3..6 with shape [batch.., M, N, K]; Av's stride along
+ *   N must be 0 and Bv's stride along M must be 0 (A broadcast over n, B over
+ *   m), batch strides are free; unmasked.  Cv: shape [batch.., M, N] (or with
+ *   a trailing 1), injective.
+ * dtypes: A and B both PSG_BF16 (tensor cores, float32 accumulate in TMEM) or
+ *   both PSG_F32 (float32 FMA); C PSG_F32 or PSG_BF16 (rounded once, RNE).
+ * The total deviates from the sequential float32 loop by at most
+ * 2 * gamma_{K-1} * sum_k |a_k b_k| (Litmus, "ToleranceBound").
+ * d_status: device int32 or NULL; receives PSG_E_TIMEOUT if a pipeline wait in
+ *   the tensor-core kernel gave up (the output is then invalid).
+ * ------------------------------------------------------------------------- */
+psg_status psg_contract(const void* A, const psg_view* Av, const void* B, const psg_view* Bv,
+                        void* C, const psg_view* Cv, int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * psg_gather -- GATHER along dim 0 (limn, "The op set"; nn.Embedding is the
+ * use, "nn, optim and checkpoints"):  out[n, ...] = src[idx[n], ...].
+ * sv: view of src with shape [V, ...]; idx: device int32[n]; ov: view of out
+ * with shape [n, ...] (unmasked, injective), same dtype.  An index outside
+ * [0, V) zero-fills its row and writes PSG_E_INDEX_OUT_OF_RANGE to d_status
+ * (device int32, required).
+ * ------------------------------------------------------------------------- */
+psg_status psg_gather(const void* src, const psg_view* sv, const int32_t* idx, int64_t n, void* out,
+                      const psg_view* ov, int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * psg_scatter_add -- SCATTER-add along dim 0 (limn, "The op set"; "Backends":
+ * a scatter's colliding adds stay in order), deterministic:
+ *     for n = 0, 1, .. n-1 in order:  dst[idx[n], ...] += upd[n, ...]
+ * Float destinations keep a float32 running total per cell, starting from the
+ * cell's value, and round into the dtype once; ints wrap.  Colliding rows are
+ * added in ascending n, so two runs give the same bits (no float atomics).
+ * dv: view of dst [V, ...] (contiguous rows); uv: view of upd [n, ...]; both
+ * one dtype (f32, bf16, f16, i32).  An index outside [0, V) skips its row and
+ * writes PSG_E_INDEX_OUT_OF_RANGE to d_status (device int32, required).
+ * workspace: device memory of at least psg_scatter_workspace(n) bytes,
+ *   256-byte aligned, owned by the caller, free for reuse once the stream has
+ *   passed this call.
+ * ------------------------------------------------------------------------- */
+size_t psg_scatter_workspace(int64_t n);
+psg_status psg_scatter_add(void* dst, const psg_view* dv, const int32_t* idx, int64_t n,
+                           const void* upd, const psg_view* uv, void* workspace, size_t ws_bytes,
+                           int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * psg_query_launch -- the launch a call would make, before making it (Tiki,
+ * "The architecture we want": register and shared-memory budgets visible
+ * before launch).  call: one of psg_call; v: the output view the call would
+ * write (for PSG_CALL_CONTRACT: Cv).  Writes grid (blocks), block (threads),
+ * dynamic shared memory bytes and registers per thread of the kernel chosen.
+ * ------------------------------------------------------------------------- */
+typedef enum {
+    PSG_CALL_ELEMENTWISE = 0, PSG_CALL_REDUCE_ROWS = 1, PSG_CALL_PERMUTE = 2,
+    PSG_CALL_CONTRACT_BF16 = 3, PSG_CALL_CONTRACT_F32 = 4, PSG_CALL_GATHER = 5,
+    PSG_CALL_SCATTER_ADD = 6
+} psg_call;
+
+psg_status psg_query_launch(int call, const psg_view* v, int* grid, int* block, int* smem,
+                            int* regs);
+
+/* Human-readable name of a status code (static storage). */
+const char* psg_status_string(int status);
+
+/* Library version string (static storage). */
+const char* psg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSG_H */
