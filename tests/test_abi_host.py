@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/psg.h declares, and refuses bad arguments before any
+launch with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def A():
+    from primitive_sm_graph_gb300 import build
+    build.build()
+    from primitive_sm_graph_gb300 import _abi
+    return _abi
+
+
+def test_exports_every_declared_symbol(A):
+    hdr = open(os.path.join(ROOT, "include", "psg.h")).read()
+    names = set(re.findall(r"^\s*(?:psg_status|size_t|const char\*)\s+(psg_\w+)\s*\(", hdr, re.M))
+    assert {"psg_elementwise", "psg_reduce_rows", "psg_permute", "psg_contract", "psg_gather",
+            "psg_scatter_add", "psg_scatter_workspace", "psg_query_launch",
+            "psg_status_string", "psg_version"} <= names
+    lib = ctypes.CDLL(A.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(A):
+    assert A.status_string(0) == "ok"
+    assert "index" in A.status_string(A.E_INDEX_OUT_OF_RANGE)
+    assert A.status_string(999) == "unknown status"
+    assert "sm_103a" in A.version()
+
+
+def _copy_prog(dt="f32"):
+    from primitive_sm_graph_gb300._abi import node
+    return [node("LOAD", 0, dtype=dt)]
+
+
+def test_elementwise_rejects_bad_arguments(A):
+    out = A.make_view("f32", (4, 4))
+    inp = A.make_view("f32", (4, 4))
+    fake = 0x10000  # never dereferenced: every case below fails validation
+    st = A.psg_elementwise([], [fake], [inp], fake, out, stream=0, check=False)
+    assert st == A.E_INVALID_ARG
+    bad = A.make_view("f32", (4, 4), extent=10)  # reaches element 15
+    assert A.psg_elementwise(_copy_prog(), [fake], [bad], fake, out, stream=0,
+                             check=False) == A.E_OUT_OF_BOUNDS_VIEW
+    shape_mismatch = A.make_view("f32", (4, 5))
+    assert A.psg_elementwise(_copy_prog(), [fake], [shape_mismatch], fake, out, stream=0,
+                             check=False) == A.E_INVALID_ARG
+    f64 = A.make_view("f64", (4, 4))
+    assert A.psg_elementwise([A.node("LOAD", 0, dtype="f64")], [fake], [f64], fake,
+                             A.make_view("f64", (4, 4)), stream=0,
+                             check=False) == A.E_UNSUPPORTED_DTYPE
+    # output must be injective: a stride-0 dim of size 4
+    aliased = A.make_view("f32", (4, 4), strides=(4, 0), extent=16)
+    assert A.psg_elementwise(_copy_prog(), [fake], [inp], fake, aliased, stream=0,
+                             check=False) == A.E_UNSUPPORTED_LAYOUT
+    # misaligned float pointer
+    assert A.psg_elementwise(_copy_prog(), [fake + 2], [inp], fake, out, stream=0,
+                             check=False) == A.E_MISALIGNED
+    # dtype disagreement between LOAD and its input
+    assert A.psg_elementwise(_copy_prog("i32"), [fake], [inp], fake, out, stream=0,
+                             check=False) == A.E_UNSUPPORTED_DTYPE
+    # EXP of an integer
+    i32 = A.make_view("i32", (4, 4))
+    prog = [A.node("LOAD", 0, dtype="i32"), A.node("EXP", 0, dtype="i32")]
+    assert A.psg_elementwise(prog, [fake], [i32], fake, i32, stream=0,
+                             check=False) == A.E_UNSUPPORTED_DTYPE
+    # an operand that names a later node
+    prog = [A.node("ADD", 1, 1), A.node("LOAD", 0)]
+    assert A.psg_elementwise(prog, [fake], [inp], fake, out, stream=0,
+                             check=False) == A.E_INVALID_ARG
+
+
+def test_too_many_live_values_is_refused(A):
+    # seven loads all alive at once, then summed: needs 7 registers (> 6)
+    prog = [A.node("LOAD", k % 2) for k in range(7)]
+    acc = 0
+    for k in range(1, 7):
+        prog.append(A.node("ADD", acc if k == 1 else len(prog) - 1, k))
+    # rewrite so every load stays live until the end: sum pairs late
+    prog = [A.node("LOAD", 0), A.node("LOAD", 1), A.node("EXP", 0), A.node("EXP", 1),
+            A.node("LOG", 0), A.node("LOG", 1), A.node("SQRT", 0),
+            A.node("ADD", 0, 1), A.node("ADD", 7, 2), A.node("ADD", 8, 3), A.node("ADD", 9, 4),
+            A.node("ADD", 10, 5), A.node("ADD", 11, 6)]
+    v = A.make_view("f32", (4, 4))
+    fake = 0x10000
+    assert A.psg_elementwise(prog, [fake, fake], [v, v], fake, v, stream=0,
+                             check=False) == A.E_UNSUPPORTED_PROGRAM
+
+
+def test_permute_rejects_bad_arguments(A):
+    fake = 0x10000
+    iv = A.make_view("f32", (3, 5))
+    ov = A.make_view("f32", (5, 3))
+    assert A.psg_permute(fake, iv, [0, 0], fake, ov, stream=0, check=False) == A.E_INVALID_ARG
+    assert A.psg_permute(fake, iv, [0, 1], fake, ov, stream=0, check=False) == A.E_INVALID_ARG
+    ob = A.make_view("bf16", (5, 3))
+    assert A.psg_permute(fake, iv, [1, 0], fake, ob, stream=0, check=False) == A.E_UNSUPPORTED_DTYPE
