@@ -1,5 +1,7 @@
-// Helpers shared by the entry points (api.cpp and the per-family API files).
+// Helpers shared by the entry points and planners.
 #pragma once
+
+#include <string>
 
 #include "common.h"
 
@@ -7,10 +9,20 @@ namespace psg {
 
 bool ptr_aligned(const void* p, int dt);
 bool same_shape(const psg_view* a, const psg_view* b);
-void fill_operand(Operand& op, const void* ptr, const psg_view* v, const Space& sp,
-                  const int64_t* st, const int64_t* lo, const int64_t* hi, bool masked);
+// Fill a kernel operand from a view and its iteration-space strides/masks;
+// returns its addressing mode (PSG_M_*).
+int fill_operand(PsgOperand& op, const void* ptr, const psg_view* v, const Space& sp,
+                 const int64_t* st, const int64_t* lo, const int64_t* hi, bool masked);
+
+struct EwPlan {
+    PsgEwParams p;
+    int n_in;
+    std::string src;  // full runtime-compiled source
+};
 psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const* in,
                             const psg_view* in_v, int n_in, void* out, const psg_view* out_v,
-                            EwLaunch* L);
+                            EwPlan* P);
+psg_status launch_elementwise(const EwPlan& P, void* stream);
+psg_status query_elementwise(const EwPlan& P, int* grid, int* block, int* smem, int* regs);
 
 }  // namespace psg

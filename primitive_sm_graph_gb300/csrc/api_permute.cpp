@@ -10,7 +10,7 @@ namespace psg {
 
 psg_status plan_permute(const void* in, const psg_view* in_v, const int32_t* perm, void* out,
                         const psg_view* out_v, int* kind, TransposeLaunch* T, CopyLaunch* C,
-                        EwLaunch* E)
+                        EwPlan* E)
 {
     if (!in_v || !out_v) return PSG_E_INVALID_ARG;
     psg_status st = check_view(in_v, false);
@@ -114,7 +114,7 @@ extern "C" psg_status psg_permute(const void* in, const psg_view* in_v, const in
     int kind = 0;
     TransposeLaunch T;
     CopyLaunch C;
-    EwLaunch E;
+    EwPlan E;
     psg_status st = plan_permute(in, in_v, perm, out, out_v, &kind, &T, &C, &E);
     if (st != PSG_OK) return st;
     if (kind == 0) return launch_transpose(T, stream);

@@ -1,0 +1,128 @@
+// psg_elementwise: plan (views -> iteration space -> operand modes), generate
+// the program body, fetch the runtime-specialised kernel, launch it.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "api_internal.h"
+#include "codegen.h"
+#include "jit.h"
+#include "launch_util.cuh"
+
+namespace psg {
+
+namespace {
+constexpr int EW_THREADS = 256;
+
+int group_log2_for(int64_t chunks)
+{
+    int g = 0;
+    while ((1 << g) < chunks && (1 << g) < EW_THREADS) ++g;
+    return g;
+}
+}  // namespace
+
+psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const* in,
+                            const psg_view* in_v, int n_in, void* out, const psg_view* out_v,
+                            EwPlan* P)
+{
+    if (!prog || n_nodes < 1 || n_nodes > PSG_MAX_NODES) return PSG_E_INVALID_ARG;
+    if (n_in < 0 || n_in > PSG_MAX_INPUTS) return PSG_E_INVALID_ARG;
+    if (n_in > 0 && (!in || !in_v)) return PSG_E_INVALID_ARG;
+    if (!out_v) return PSG_E_INVALID_ARG;
+    psg_status st = check_view(out_v, true);
+    if (st != PSG_OK) return st;
+    if (out_v->dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
+    const int64_t n = view_numel(out_v);
+    if (n > 0 && !out) return PSG_E_INVALID_ARG;
+    if (!ptr_aligned(out, out_v->dtype)) return PSG_E_MISALIGNED;
+    const psg_view* views[1 + PSG_MAX_INPUTS];
+    views[0] = out_v;
+    int dts[PSG_MAX_INPUTS];
+    for (int k = 0; k < n_in; ++k) {
+        st = check_view(&in_v[k], false);
+        if (st != PSG_OK) return st;
+        if (!same_shape(&in_v[k], out_v)) return PSG_E_INVALID_ARG;
+        if (in_v[k].dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
+        if (n > 0 && !in[k]) return PSG_E_INVALID_ARG;
+        if (!ptr_aligned(in[k], in_v[k].dtype)) return PSG_E_MISALIGNED;
+        views[1 + k] = &in_v[k];
+        dts[k] = in_v[k].dtype;
+    }
+    std::memset(&P->p, 0, sizeof(P->p));
+    Space sp;
+    int64_t strides[1 + PSG_MAX_INPUTS][MAXD], lo[1 + PSG_MAX_INPUTS][MAXD], hi[1 + PSG_MAX_INPUTS][MAXD];
+    bool masked[1 + PSG_MAX_INPUTS];
+    st = build_space(views, 1 + n_in, false, &sp, strides, lo, hi, masked);
+    if (st != PSG_OK) return st;
+    bool uni[PSG_MAX_INPUTS];
+    int modes[PSG_MAX_INPUTS];
+    for (int k = 0; k < n_in; ++k) {
+        modes[k] = fill_operand(P->p.in[k], in[k], &in_v[k], sp, strides[1 + k], lo[1 + k], hi[1 + k],
+                                masked[1 + k]);
+        uni[k] = modes[k] == PSG_M_UNIFORM;
+    }
+    fill_operand(P->p.out, out, out_v, sp, strides[0], lo[0], hi[0], false);
+    ProgInfo I;
+    st = analyze_program(prog, n_nodes, dts, uni, n_in, nullptr, 0, &I);
+    if (st != PSG_OK) return st;
+    if (I.result_dtype != out_v->dtype) return PSG_E_UNSUPPORTED_DTYPE;
+    P->p.rows = sp.rows;
+    P->p.inner = sp.inner;
+    P->p.chunks = sp.chunks;
+    for (int d = 0; d < MAXD; ++d) P->p.shape[d] = d < sp.nd ? sp.shape[d] : 1;
+    P->p.nd = sp.nd;
+    P->p.group_log2 = group_log2_for(sp.chunks);
+    P->n_in = n_in;
+    // the specialisation: input modes and dtypes, output dtype, the body
+    std::string spec = "constexpr int kNin = " + std::to_string(n_in) + ";\n";
+    std::string m = "constexpr int kInMode[] = {", d = "constexpr int kInDt[] = {";
+    for (int k = 0; k < (n_in > 0 ? n_in : 1); ++k) {
+        m += std::to_string(k < n_in ? modes[k] : 0) + (k + 1 < n_in ? ", " : "");
+        d += std::to_string(k < n_in ? dts[k] : 0) + (k + 1 < n_in ? ", " : "");
+    }
+    spec += m + "};\n" + d + "};\n";
+    spec += "constexpr int kOutDt = " + std::to_string(out_v->dtype) + ";\n";
+    spec += gen_eval(prog, I, "Body");
+    P->src = jit_source(JIT_EW, spec);
+    return PSG_OK;
+}
+
+static psg_status grid_for(const EwPlan& P, cudaKernel_t k, int* grid)
+{
+    const int groups = EW_THREADS >> P.p.group_log2;
+    const int64_t need = (P.p.rows + groups - 1) / groups;
+    const int per_sm = jit_max_blocks_per_sm(k, EW_THREADS, 0);
+    const int64_t cap = (int64_t)num_sms() * per_sm;
+    *grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, cap));
+    return PSG_OK;
+}
+
+psg_status launch_elementwise(const EwPlan& P, void* stream)
+{
+    if (P.p.rows == 0 || P.p.inner == 0) return PSG_OK;
+    cudaKernel_t k;
+    psg_status st = jit_kernel(P.src, "psg_ew", &k);
+    if (st != PSG_OK) return st;
+    int grid;
+    grid_for(P, k, &grid);
+    void* args[] = {(void*)&P.p};
+    if (cudaLaunchKernel((const void*)k, dim3(grid), dim3(EW_THREADS), args, 0, (cudaStream_t)stream) !=
+        cudaSuccess)
+        return PSG_E_CUDA;
+    return PSG_OK;
+}
+
+psg_status query_elementwise(const EwPlan& P, int* grid, int* block, int* smem, int* regs)
+{
+    cudaKernel_t k;
+    psg_status st = jit_kernel(P.src, "psg_ew", &k);
+    if (st != PSG_OK) return st;
+    grid_for(P, k, grid);
+    *block = EW_THREADS;
+    *smem = 0;
+    *regs = jit_regs(k);
+    return PSG_OK;
+}
+
+}  // namespace psg

@@ -1,0 +1,118 @@
+// NVRTC front end and kernel cache of the runtime-specialised kernels.
+#include "jit.h"
+
+#include <nvrtc.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+// kJitParams, kJitPrelude, kJitEw, kJitReduce: the hand-written sources under
+// csrc/jit/, embedded as text by the build
+#include "jit_sources.inc"
+
+namespace psg {
+
+namespace {
+
+std::mutex g_mu;
+
+std::unordered_map<std::string, cudaKernel_t>& cache()
+{
+    static std::unordered_map<std::string, cudaKernel_t> m;
+    return m;
+}
+
+const char* const kOpts[] = {
+    "--gpu-architecture=sm_103a", "-std=c++17", "--fmad=false", "--ftz=false",
+    "--prec-div=true", "--prec-sqrt=true", "-lineinfo", "-default-device",
+};
+
+psg_status compile(const std::string& src, std::vector<char>* cubin, std::string* log)
+{
+    nvrtcProgram prog;
+    if (nvrtcCreateProgram(&prog, src.c_str(), "psg_jit.cu", 0, nullptr, nullptr) != NVRTC_SUCCESS)
+        return PSG_E_CUDA;
+    const nvrtcResult rc = nvrtcCompileProgram(prog, (int)(sizeof(kOpts) / sizeof(kOpts[0])), kOpts);
+    size_t ls = 0;
+    nvrtcGetProgramLogSize(prog, &ls);
+    if (log && ls > 1) {
+        log->resize(ls);
+        nvrtcGetProgramLog(prog, &(*log)[0]);
+    }
+    if (rc != NVRTC_SUCCESS) {
+        if (std::getenv("PSG_JIT_VERBOSE") && log) std::fprintf(stderr, "%s\n%s\n", src.c_str(), log->c_str());
+        nvrtcDestroyProgram(&prog);
+        return PSG_E_CUDA;
+    }
+    if (cubin) {
+        size_t n = 0;
+        nvrtcGetCUBINSize(prog, &n);
+        cubin->resize(n);
+        nvrtcGetCUBIN(prog, cubin->data());
+    }
+    nvrtcDestroyProgram(&prog);
+    return PSG_OK;
+}
+
+}  // namespace
+
+std::string jit_source(JitSkeleton sk, const std::string& spec)
+{
+    std::string s;
+    s.reserve(32768);
+    s += kJitParams;
+    s += "\n";
+    s += kJitPrelude;
+    s += "\n// ---- program-specific part ----\n";
+    s += spec;
+    s += "\n// ---- kernel skeleton ----\n";
+    s += sk == JIT_EW ? kJitEw : kJitReduce;
+    return s;
+}
+
+psg_status jit_compile_only(const std::string& src, std::string* log)
+{
+    if (std::getenv("PSG_JIT_DUMP")) std::fprintf(stderr, "%s\n", src.c_str());
+    return compile(src, nullptr, log);
+}
+
+psg_status jit_kernel(const std::string& src, const char* name, cudaKernel_t* out)
+{
+    std::lock_guard<std::mutex> g(g_mu);
+    auto it = cache().find(src);
+    if (it != cache().end()) {
+        *out = it->second;
+        return PSG_OK;
+    }
+    std::vector<char> cubin;
+    std::string log;
+    psg_status st = compile(src, &cubin, &log);
+    if (st != PSG_OK) return st;
+    cudaLibrary_t lib;
+    if (cudaLibraryLoadData(&lib, cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0) != cudaSuccess)
+        return PSG_E_CUDA;
+    cudaKernel_t k;
+    if (cudaLibraryGetKernel(&k, lib, name) != cudaSuccess) return PSG_E_CUDA;
+    cache().emplace(src, k);
+    *out = k;
+    return PSG_OK;
+}
+
+int jit_max_blocks_per_sm(cudaKernel_t k, int threads, size_t smem)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, (const void*)k, threads, smem) != cudaSuccess) n = 1;
+    return n < 1 ? 1 : n;
+}
+
+int jit_regs(cudaKernel_t k)
+{
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, (const void*)k) != cudaSuccess) return -1;
+    return a.numRegs;
+}
+
+}  // namespace psg

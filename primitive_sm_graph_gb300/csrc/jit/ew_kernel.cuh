@@ -1,0 +1,53 @@
+// Fused elementwise kernel skeleton (runtime-specialised per program).
+//
+// limn ("Backends") runs one thread per output cell; here one thread owns a
+// chunk of PSG_VEC consecutive cells along the innermost dim, so contiguous
+// operands move with 128-bit loads and stores and an expanded (stride-0)
+// operand is read once per chunk.  Row offsets come from one multi-index
+// decomposition per row; within a row the View's index is col * stride.  A
+// block is split into row groups of a power-of-two size so short rows still
+// fill it, and the grid is persistent (a multiple of the SM count).
+//
+// The including source defines kNin, kInMode[], kInDt[], kOutDt and
+// struct Body { template <class C> static void eval(const C&, T (&y)[PSG_VEC]); }.
+
+struct EwCtx {
+    const PsgEwParams& p;
+    const i64 (&roff)[kNin > 0 ? kNin : 1];
+    const bool (&rok)[kNin > 0 ? kNin : 1];
+    i64 col0;
+    int nvalid;
+    template <int K>
+    __device__ __forceinline__ void ldv(typename VT<kInDt[K]>::T (&d)[PSG_VEC]) const
+    {
+        ld_chunk<kInDt[K], kInMode[K]>(p.in[K], roff[K], rok[K], col0, nvalid, d);
+    }
+    template <int K>
+    __device__ __forceinline__ typename VT<kInDt[K]>::T ld1() const
+    {
+        return ld_first<kInDt[K], kInMode[K]>(p.in[K], roff[K], rok[K], col0);
+    }
+};
+
+extern "C" __global__ void __launch_bounds__(256) psg_ew(const __grid_constant__ PsgEwParams p)
+{
+    const int gs = 1 << p.group_log2;
+    const int groups = 256 >> p.group_log2;
+    const int grp = threadIdx.x >> p.group_log2;
+    const int lane = threadIdx.x & (gs - 1);
+    for (i64 row = (i64)blockIdx.x * groups + grp; row < p.rows; row += (i64)gridDim.x * groups) {
+        i64 roff[kNin > 0 ? kNin : 1];
+        bool rok[kNin > 0 ? kNin : 1];
+        i64 ooff;
+        row_offsets<kNin>(p.in, p.out, p.shape, p.nd, row, roff, rok, kInMode, ooff);
+        for (i64 ch = lane; ch < p.chunks; ch += gs) {
+            const i64 col0 = ch * PSG_VEC;
+            const i64 left = p.inner - col0;
+            const int nvalid = left < PSG_VEC ? (int)left : PSG_VEC;
+            const EwCtx c{p, roff, rok, col0, nvalid};
+            typename VT<kOutDt>::T y[PSG_VEC];
+            Body::eval(c, y);
+            st_chunk<kOutDt>(p.out, ooff, col0, nvalid, y);
+        }
+    }
+}

@@ -58,3 +58,13 @@ def dev(t: torch.Tensor) -> torch.Tensor:
 def storage_dtype(name):
     return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "f64": torch.float64,
             "i32": torch.int32, "i16": torch.int16, "i8": torch.int8}[name]
+
+
+def first_mismatches(a: np.ndarray, b: np.ndarray, k=5):
+    """Positions and values of the first k cells whose bits differ (NaN==NaN)."""
+    av = a.reshape(-1)
+    bv = b.reshape(-1)
+    nan_a, nan_b = _isnan_bits(av), _isnan_bits(bv)
+    bad = np.nonzero((av.view(np.uint8).reshape(av.shape + (-1,)) !=
+                      bv.view(np.uint8).reshape(bv.shape + (-1,))).any(axis=-1) & ~(nan_a & nan_b))[0]
+    return [(int(i), av[i], bv[i]) for i in bad[:k]], int(bad.size)

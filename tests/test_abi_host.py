@@ -78,21 +78,48 @@ def test_elementwise_rejects_bad_arguments(A):
                              check=False) == A.E_INVALID_ARG
 
 
-def test_too_many_live_values_is_refused(A):
-    # seven loads all alive at once, then summed: needs 7 registers (> 6)
-    prog = [A.node("LOAD", k % 2) for k in range(7)]
-    acc = 0
-    for k in range(1, 7):
-        prog.append(A.node("ADD", acc if k == 1 else len(prog) - 1, k))
-    # rewrite so every load stays live until the end: sum pairs late
-    prog = [A.node("LOAD", 0), A.node("LOAD", 1), A.node("EXP", 0), A.node("EXP", 1),
-            A.node("LOG", 0), A.node("LOG", 1), A.node("SQRT", 0),
-            A.node("ADD", 0, 1), A.node("ADD", 7, 2), A.node("ADD", 8, 3), A.node("ADD", 9, 4),
-            A.node("ADD", 10, 5), A.node("ADD", 11, 6)]
-    v = A.make_view("f32", (4, 4))
-    fake = 0x10000
-    assert A.psg_elementwise(prog, [fake, fake], [v, v], fake, v, stream=0,
-                             check=False) == A.E_UNSUPPORTED_PROGRAM
+def _compile_hook(A):
+    L = A.lib
+    f = L.psg_internal_compile_elementwise
+    f.argtypes = [ctypes.POINTER(A.psg_node), ctypes.c_int, ctypes.POINTER(A.psg_view), ctypes.c_int,
+                  ctypes.POINTER(A.psg_view), ctypes.c_char_p, ctypes.c_size_t]
+    return f
+
+
+def test_generated_kernels_compile_without_a_gpu(A):
+    """Random programs over every dtype plan and compile (NVRTC, sm_103a)."""
+    import torch
+    f = _compile_hook(A)
+    g = torch.Generator().manual_seed(5)
+    fdt, idt = ["f32", "bf16", "f16"], ["i32", "i16", "i8"]
+    buf = ctypes.create_string_buffer(1 << 16)
+    for case in range(12):
+        pool = fdt if case % 2 == 0 else idt
+        dts = [pool[int(torch.randint(0, 3, (1,), generator=g))] for _ in range(3)]
+        prog = [A.node("LOAD", k, dtype=dts[k]) for k in range(3)]
+        for _ in range(8):
+            i = int(torch.randint(0, len(prog), (1,), generator=g))
+            dt = DT_OF(prog[i])
+            op = ["ADD", "MUL", "CMPLT", "NEG", "CAST", "WHERE"][int(torch.randint(0, 6, (1,), generator=g))]
+            if op == "CAST":
+                t = (fdt + idt)[int(torch.randint(0, 6, (1,), generator=g))]
+                prog.append(A.node("CAST", i, dtype=t))
+            elif op == "NEG":
+                prog.append(A.node("NEG", i, dtype=dt))
+            elif op == "WHERE":
+                prog.append(A.node("WHERE", 0, i, i, dtype=dt))
+            else:
+                prog.append(A.node(op, i, i, dtype=dt))
+        ins = (A.psg_view * 3)(*[A.make_view(d, (7, 33)) for d in dts])
+        out = A.make_view(DT_OF(prog[-1]), (7, 33))
+        arr = (A.psg_node * len(prog))(*prog)
+        st = f(arr, len(prog), ins, 3, ctypes.byref(out), buf, len(buf))
+        assert st == 0, (case, A.STATUS.get(st), buf.value.decode()[:2000])
+
+
+def DT_OF(nd):
+    from primitive_sm_graph_gb300._abi import DTYPE_NAMES
+    return DTYPE_NAMES[nd.dtype]
 
 
 def test_permute_rejects_bad_arguments(A):

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import seeded_inputs as SI
-from helpers import dev, same_bits_nan_equal, storage_dtype, to_np, ulp_dist_f32
+from helpers import dev, first_mismatches, same_bits_nan_equal, storage_dtype, to_np, ulp_dist_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -227,7 +227,8 @@ def _fuzz(A, O, seed, int_mode, transcendental_last, n_cases):
                 assert np.all(np.abs(g64[fin] - r64[fin]) <= rel * np.abs(r64[fin]) + 1e-30), (case, P)
                 assert np.array_equal(np.isnan(g64), np.isnan(r64))
         else:
-            assert same_bits_nan_equal(got, ref.data, not int_mode or out_dt in FLOAT_DT), (case, P)
+            assert same_bits_nan_equal(got, ref.data, not int_mode or out_dt in FLOAT_DT), \
+                (case, P, [x[4] for x in inputs], first_mismatches(got, ref.data))
         ran += 1
     assert ran >= n_cases * 0.7
 
