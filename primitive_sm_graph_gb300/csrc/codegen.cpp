@@ -148,7 +148,8 @@ psg_status analyze_program(const psg_node* nodes, int n, const int* in_dtype, co
     return PSG_OK;
 }
 
-std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string& name)
+std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string& name,
+                     const std::string& prefix)
 {
     const int n = I.n;
     auto ref = [&](int j) {
@@ -219,7 +220,7 @@ std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string
     }
     const std::string rt = ctype(I.result_dtype);
     std::string s;
-    s += "struct " + name + " {\n";
+    s += prefix + "struct " + name + " {\n";
     s += "    template <class C>\n";
     s += "    __device__ __forceinline__ static void eval(const C& c, " + rt + " (&y)[PSG_VEC])\n    {\n";
     s += head;

@@ -28,6 +28,7 @@ psg_status analyze_program(const psg_node* nodes, int n, const int* in_dtype, co
 // C++ source of `struct <name> { template <class C> static void eval(const C& c,
 // T (&y)[PSG_VEC]); }` computing the program for the PSG_VEC lanes of a chunk.
 // C provides ldv<K>(arr), ld1<K>(), redf(s), redi(s).
-std::string gen_eval(const psg_node* nodes, const ProgInfo& info, const std::string& name);
+std::string gen_eval(const psg_node* nodes, const ProgInfo& info, const std::string& name,
+                     const std::string& prefix = "");
 
 }  // namespace psg

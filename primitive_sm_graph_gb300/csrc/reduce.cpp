@@ -1,0 +1,208 @@
+// psg_reduce_rows: validate stages and epilogue, build the iteration space
+// (the reduced axis stays last), choose the team size and whether the row is
+// cached in registers, generate the bodies, launch the specialised kernel.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "api_internal.h"
+#include "codegen.h"
+#include "jit.h"
+#include "launch_util.cuh"
+
+namespace psg {
+
+namespace {
+
+struct RedPlan {
+    PsgRedParams p;
+    int block;
+    std::string src;
+};
+
+std::string int_list(const int* v, int n)
+{
+    std::string s = "{";
+    for (int i = 0; i < (n > 0 ? n : 1); ++i) s += std::to_string(i < n ? v[i] : 0) + (i + 1 < n ? ", " : "");
+    return s + "}";
+}
+
+psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_node* epilogue, int n_epi,
+                       const void* const* in, const psg_view* in_v, int n_in, void* out,
+                       const psg_view* out_v, RedPlan* P)
+{
+    if (!stages || n_stages < 1 || n_stages > MAX_STAGES) return PSG_E_INVALID_ARG;
+    if (n_in < 1 || n_in > PSG_MAX_INPUTS || !in || !in_v || !out_v) return PSG_E_INVALID_ARG;
+    if (n_epi < 0 || (n_epi > 0 && !epilogue)) return PSG_E_INVALID_ARG;
+    const int nd = in_v[0].ndim;
+    if (nd < 1) return PSG_E_INVALID_ARG;
+    psg_status st;
+    int dts[PSG_MAX_INPUTS];
+    for (int k = 0; k < n_in; ++k) {
+        st = check_view(&in_v[k], false);
+        if (st != PSG_OK) return st;
+        if (!same_shape(&in_v[k], &in_v[0])) return PSG_E_INVALID_ARG;
+        if (in_v[k].dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
+        if (view_numel(&in_v[k]) > 0 && !in[k]) return PSG_E_INVALID_ARG;
+        if (!ptr_aligned(in[k], in_v[k].dtype)) return PSG_E_MISALIGNED;
+        dts[k] = in_v[k].dtype;
+    }
+    st = check_view(out_v, true);
+    if (st != PSG_OK) return st;
+    if (out_v->dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
+    if (view_numel(out_v) > 0 && !out) return PSG_E_INVALID_ARG;
+    if (!ptr_aligned(out, out_v->dtype)) return PSG_E_MISALIGNED;
+    const int64_t N = in_v[0].shape[nd - 1];
+    // output form: per element [.., N], or per row [..] / [.., 1]
+    bool per_row;
+    bool lead_match = true;
+    for (int d = 0; d < nd - 1; ++d)
+        if (out_v->ndim > d && out_v->shape[d] != in_v[0].shape[d]) lead_match = false;
+    if (!lead_match) return PSG_E_INVALID_ARG;
+    if (out_v->ndim == nd && out_v->shape[nd - 1] == N) per_row = false;
+    else if (out_v->ndim == nd && out_v->shape[nd - 1] == 1) per_row = true;
+    else if (out_v->ndim == nd - 1) per_row = true;
+    else return PSG_E_INVALID_ARG;
+    // the output as a view over the iteration shape (stride 0 along N when per row)
+    psg_view ov = in_v[0];
+    ov.dtype = out_v->dtype;
+    ov.offset = out_v->offset;
+    ov.extent = out_v->extent;
+    for (int d = 0; d < nd; ++d) {
+        ov.mask_lo[d] = 0;
+        ov.mask_hi[d] = ov.shape[d];
+        ov.strides[d] = d < nd - 1 ? out_v->strides[d] : (per_row ? 0 : out_v->strides[nd - 1]);
+    }
+    const psg_view* views[1 + PSG_MAX_INPUTS];
+    views[0] = &ov;
+    for (int k = 0; k < n_in; ++k) views[1 + k] = &in_v[k];
+    std::memset(&P->p, 0, sizeof(P->p));
+    Space sp;
+    int64_t strides[1 + PSG_MAX_INPUTS][MAXD], lo[1 + PSG_MAX_INPUTS][MAXD], hi[1 + PSG_MAX_INPUTS][MAXD];
+    bool masked[1 + PSG_MAX_INPUTS];
+    st = build_space(views, 1 + n_in, true, &sp, strides, lo, hi, masked);
+    if (st != PSG_OK) return st;
+    bool uni[PSG_MAX_INPUTS];
+    int modes[PSG_MAX_INPUTS];
+    int n_vary = 0;
+    for (int k = 0; k < n_in; ++k) {
+        modes[k] = fill_operand(P->p.in[k], in[k], &in_v[k], sp, strides[1 + k], lo[1 + k], hi[1 + k],
+                                masked[1 + k]);
+        uni[k] = modes[k] == PSG_M_UNIFORM;
+        n_vary += uni[k] ? 0 : 1;
+    }
+    fill_operand(P->p.out, out, &ov, sp, strides[0], lo[0], hi[0], false);
+    // stages
+    std::string bodies;
+    int sop[MAX_STAGES], sdt[MAX_STAGES];
+    for (int s = 0; s < n_stages; ++s) {
+        if (stages[s].op != PSG_RED_SUM && stages[s].op != PSG_RED_MAX) return PSG_E_INVALID_ARG;
+        ProgInfo I;
+        st = analyze_program(stages[s].prologue, stages[s].n_nodes, dts, uni, n_in, sdt, s, &I);
+        if (st != PSG_OK) return st;
+        sop[s] = stages[s].op;
+        sdt[s] = I.result_dtype;
+        bodies += gen_eval(stages[s].prologue, I, "StageBody<" + std::to_string(s) + ">", "template <>\n");
+    }
+    // epilogue (a per-row epilogue may read only constants and stage values)
+    psg_node last_red;
+    std::memset(&last_red, 0, sizeof(last_red));
+    const psg_node* epi = epilogue;
+    if (n_epi == 0) {
+        if (!per_row) return PSG_E_INVALID_ARG;
+        last_red.op = PSG_OP_RED;
+        last_red.a = n_stages - 1;
+        last_red.dtype = sdt[n_stages - 1];
+        epi = &last_red;
+        n_epi = 1;
+    }
+    ProgInfo E;
+    st = per_row ? analyze_program(epi, n_epi, dts, uni, 0, sdt, n_stages, &E)
+                 : analyze_program(epi, n_epi, dts, uni, n_in, sdt, n_stages, &E);
+    if (st != PSG_OK) return st;
+    if (E.result_dtype != out_v->dtype) return PSG_E_UNSUPPORTED_DTYPE;
+    bodies += gen_eval(epi, E, "Epi");
+    // team of T threads per row, chunks per thread cached when they fit
+    int tl = 0;
+    while ((1 << tl) < sp.chunks && tl < 10) ++tl;
+    const int T = 1 << tl;
+    const int64_t ch_per = (sp.chunks + T - 1) / T;
+    const int kch = (ch_per <= 4 && n_vary * ch_per <= 8) ? (int)(ch_per > 0 ? ch_per : 1) : 0;
+    P->block = T > 256 ? T : 256;
+    P->p.rows = sp.rows;
+    P->p.inner = sp.inner;
+    P->p.chunks = sp.chunks;
+    for (int d = 0; d < MAXD; ++d) P->p.shape[d] = d < sp.nd ? sp.shape[d] : 1;
+    P->p.nd = sp.nd;
+    P->p.team_log2 = tl;
+    P->p.out_per_row = per_row ? 1 : 0;
+    std::string spec = "constexpr int kNin = " + std::to_string(n_in) + ";\n";
+    spec += "constexpr int kInMode[] = " + int_list(modes, n_in) + ";\n";
+    spec += "constexpr int kInDt[] = " + int_list(dts, n_in) + ";\n";
+    spec += "constexpr int kOutDt = " + std::to_string(out_v->dtype) + ";\n";
+    spec += "constexpr int kNstages = " + std::to_string(n_stages) + ";\n";
+    spec += "constexpr int kStageOp[] = " + int_list(sop, n_stages) + ";\n";
+    spec += "constexpr int kStageDt[] = " + int_list(sdt, n_stages) + ";\n";
+    spec += "constexpr int kCH = " + std::to_string(kch) + ";\n";
+    spec += "constexpr int kPerRow = " + std::to_string(per_row ? 1 : 0) + ";\n";
+    spec += "template <int S> struct StageBody;\n";
+    spec += bodies;
+    P->src = jit_source(JIT_REDUCE, spec);
+    return PSG_OK;
+}
+
+psg_status grid_for(const RedPlan& P, cudaKernel_t k, int* grid)
+{
+    const int teams = P.block >> P.p.team_log2;
+    const int64_t need = (P.p.rows + teams - 1) / teams;
+    const int per_sm = jit_max_blocks_per_sm(k, P.block, 0);
+    *grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)num_sms() * per_sm));
+    return PSG_OK;
+}
+
+}  // namespace
+
+}  // namespace psg
+
+using namespace psg;
+
+extern "C" psg_status psg_reduce_rows(const psg_reduce_stage* stages, int n_stages, const psg_node* epilogue,
+                                      int n_epi, const void* const* in, const psg_view* in_v, int n_in,
+                                      void* out, const psg_view* out_v, int32_t* d_status, void* stream)
+{
+    (void)d_status;
+    RedPlan P;
+    psg_status st = plan_reduce(stages, n_stages, epilogue, n_epi, in, in_v, n_in, out, out_v, &P);
+    if (st != PSG_OK) return st;
+    if (P.p.rows == 0) return PSG_OK;
+    cudaKernel_t k;
+    st = jit_kernel(P.src, "psg_reduce", &k);
+    if (st != PSG_OK) return st;
+    int grid;
+    grid_for(P, k, &grid);
+    void* args[] = {(void*)&P.p};
+    if (cudaLaunchKernel((const void*)k, dim3(grid), dim3(P.block), args, 0, (cudaStream_t)stream) != cudaSuccess)
+        return PSG_E_CUDA;
+    return PSG_OK;
+}
+
+// Test hook, not part of the ABI: plan a psg_reduce_rows call over dummy
+// pointers and compile its kernel without a GPU.
+extern "C" int psg_internal_compile_reduce(const psg_reduce_stage* stages, int n_stages, const psg_node* epilogue,
+                                           int n_epi, const psg_view* in_v, int n_in, const psg_view* out_v,
+                                           char* log, size_t log_size)
+{
+    const void* fake[PSG_MAX_INPUTS];
+    for (int k = 0; k < PSG_MAX_INPUTS; ++k) fake[k] = (const void*)(uintptr_t)4096;
+    RedPlan P;
+    psg_status st = plan_reduce(stages, n_stages, epilogue, n_epi, fake, in_v, n_in, (void*)(uintptr_t)4096,
+                                out_v, &P);
+    if (st != PSG_OK) return st;
+    std::string l;
+    st = jit_compile_only(P.src, &l);
+    if (log && log_size) {
+        std::strncpy(log, l.c_str(), log_size - 1);
+        log[log_size - 1] = 0;
+    }
+    return st;
+}

@@ -130,3 +130,20 @@ def test_permute_rejects_bad_arguments(A):
     assert A.psg_permute(fake, iv, [0, 1], fake, ov, stream=0, check=False) == A.E_INVALID_ARG
     ob = A.make_view("bf16", (5, 3))
     assert A.psg_permute(fake, iv, [1, 0], fake, ob, stream=0, check=False) == A.E_UNSUPPORTED_DTYPE
+
+
+def test_reduce_rejects_bad_arguments(A):
+    fake = 4096
+    v = A.make_view("f32", (4, 8))
+    bad_out = A.make_view("f32", (3,))
+    st = A.psg_reduce_rows([(A.RED_SUM, [A.node("LOAD", 0)])], None, [fake], [v], fake, bad_out,
+                           stream=0, check=False)
+    assert st == A.E_INVALID_ARG
+    # a per-row epilogue may not read inputs
+    st = A.psg_reduce_rows([(A.RED_SUM, [A.node("LOAD", 0)])], [A.node("LOAD", 0)], [fake], [v], fake,
+                           A.make_view("f32", (4,)), stream=0, check=False)
+    assert st == A.E_INVALID_ARG
+    # a prologue may not read its own stage
+    st = A.psg_reduce_rows([(A.RED_SUM, [A.node("RED", 0)])], None, [fake], [v], fake,
+                           A.make_view("f32", (4,)), stream=0, check=False)
+    assert st == A.E_INVALID_ARG
