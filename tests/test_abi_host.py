@@ -147,3 +147,16 @@ def test_reduce_rejects_bad_arguments(A):
     st = A.psg_reduce_rows([(A.RED_SUM, [A.node("RED", 0)])], None, [fake], [v], fake,
                            A.make_view("f32", (4,)), stream=0, check=False)
     assert st == A.E_INVALID_ARG
+
+
+def test_scatter_workspace_checks(A):
+    fake = 4096
+    dv = A.make_view("f32", (4, 2))
+    uv = A.make_view("f32", (10, 2))
+    need = A.psg_scatter_workspace(10)
+    assert need >= 10 * 8
+    st = A.psg_scatter_add(fake, dv, fake, 10, fake, uv, fake, need - 8, fake, stream=0, check=False)
+    assert st == A.E_WORKSPACE
+    st = A.psg_scatter_add(fake, dv, fake, 10, fake, A.make_view("i8", (10, 2)), fake, need, fake,
+                           stream=0, check=False)
+    assert st == A.E_UNSUPPORTED_DTYPE
