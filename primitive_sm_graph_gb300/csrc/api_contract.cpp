@@ -1,0 +1,193 @@
+// psg_contract: matmul as SUM over the last dim of MUL(Av, Bv).  The roles of
+// the dims come from the Views themselves: Av is broadcast along n (stride 0)
+// and Bv along m, exactly the two stride-0 loops of the broadcast form.
+#include <cstring>
+
+#include "api_internal.h"
+#include "common.h"
+#include "contract.h"
+
+namespace psg {
+
+namespace {
+
+struct Batch {
+    int nb;                       // batch dims kept (after dropping size 1)
+    int64_t shape[MAXD], sa[MAXD], sb[MAXD], sc[MAXD];
+};
+
+// Merge batch dims that are contiguous for A, B and C alike.
+void collapse_batch(Batch& B)
+{
+    int n = 0;
+    for (int d = 0; d < B.nb; ++d) {
+        if (B.shape[d] == 1) continue;
+        if (n > 0 && B.sa[n - 1] == B.sa[d] * B.shape[d] && B.sb[n - 1] == B.sb[d] * B.shape[d] &&
+            B.sc[n - 1] == B.sc[d] * B.shape[d]) {
+            B.shape[n - 1] *= B.shape[d];
+            B.sa[n - 1] = B.sa[d];
+            B.sb[n - 1] = B.sb[d];
+            B.sc[n - 1] = B.sc[d];
+        } else {
+            B.shape[n] = B.shape[d];
+            B.sa[n] = B.sa[d];
+            B.sb[n] = B.sb[d];
+            B.sc[n] = B.sc[d];
+            ++n;
+        }
+    }
+    B.nb = n;
+}
+
+bool al16(const void* p, int64_t off_elems, int es) { return ((uintptr_t)p + (uintptr_t)(off_elems * es)) % 16 == 0; }
+
+}  // namespace
+
+psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, const psg_view* Bv, void* C,
+                         const psg_view* Cv, int32_t* d_status, bool* use_tc, TcOperands* T, SimtParams* S,
+                         Batch* bt)
+{
+    if (!Av || !Bv || !Cv) return PSG_E_INVALID_ARG;
+    const int r = Av->ndim;
+    if (r < 3 || r > 6 || Bv->ndim != r) return PSG_E_INVALID_ARG;
+    psg_status st = check_view(Av, false);
+    if (st != PSG_OK) return st;
+    st = check_view(Bv, false);
+    if (st != PSG_OK) return st;
+    st = check_view(Cv, true);
+    if (st != PSG_OK) return st;
+    if (!same_shape(Av, Bv)) return PSG_E_INVALID_ARG;
+    if (view_has_mask(Av) || view_has_mask(Bv)) return PSG_E_UNSUPPORTED_LAYOUT;
+    const int dm = r - 3, dn = r - 2, dk = r - 1;
+    const int64_t M = Av->shape[dm], N = Av->shape[dn], K = Av->shape[dk];
+    // the broadcast form: A constant along n, B constant along m
+    if ((N > 1 && Av->strides[dn] != 0) || (M > 1 && Bv->strides[dm] != 0)) return PSG_E_UNSUPPORTED_LAYOUT;
+    // C: [batch.., M, N] or [batch.., M, N, 1]
+    const bool kept = Cv->ndim == r;
+    if (!(Cv->ndim == r - 1 || (kept && Cv->shape[r - 1] == 1))) return PSG_E_INVALID_ARG;
+    for (int d = 0; d < r - 1; ++d)
+        if (Cv->shape[d] != Av->shape[d]) return PSG_E_INVALID_ARG;
+    const int adt = Av->dtype, cdt = Cv->dtype;
+    if (Bv->dtype != adt) return PSG_E_UNSUPPORTED_DTYPE;
+    if (adt != PSG_BF16 && adt != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
+    if (cdt != PSG_BF16 && cdt != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
+    const int64_t numel = M * N * K;
+    if (numel > 0 && (!A || !Bp)) return PSG_E_INVALID_ARG;
+    if (M * N > 0 && !C) return PSG_E_INVALID_ARG;
+    if (!ptr_aligned(A, adt) || !ptr_aligned(Bp, adt) || !ptr_aligned(C, cdt)) return PSG_E_MISALIGNED;
+    if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return PSG_E_UNSUPPORTED_LAYOUT;
+    bt->nb = r - 3;
+    for (int d = 0; d < bt->nb; ++d) {
+        bt->shape[d] = Av->shape[d];
+        bt->sa[d] = Av->strides[d];
+        bt->sb[d] = Bv->strides[d];
+        bt->sc[d] = Cv->strides[d];
+    }
+    collapse_batch(*bt);
+    const int64_t a_ms = Av->strides[dm], a_ks = Av->strides[dk];
+    const int64_t b_ns = Bv->strides[dn], b_ks = Bv->strides[dk];
+    const int64_t c_ms = Cv->strides[dm], c_ns = Cv->strides[dn];
+    const int64_t batch = bt->nb == 1 ? bt->shape[0] : 1;
+    // tensor-core path: bf16, one (collapsed) batch dim, TMA-addressable operands
+    bool tc = adt == PSG_BF16 && bt->nb <= 1 && K > 0;
+    auto tma_ok = [&](const void* base, int64_t off, int64_t s_mn, int64_t s_k, int64_t mn, int64_t s_b, bool& kmaj) {
+        if (s_k == 1 && s_mn % 8 == 0 && s_mn >= K) kmaj = true;
+        else if (s_mn == 1 && s_k % 8 == 0 && s_k >= mn) kmaj = false;
+        else return false;
+        if (batch > 1 && (s_b % 8 != 0 || s_b <= 0)) return false;
+        return al16(base, off, 2);
+    };
+    bool akm = true, bkm = true;
+    tc = tc && tma_ok(A, Av->offset, a_ms, a_ks, M, bt->nb ? bt->sa[0] : 0, akm);
+    tc = tc && tma_ok(Bp, Bv->offset, b_ns, b_ks, N, bt->nb ? bt->sb[0] : 0, bkm);
+    *use_tc = tc;
+    if (tc) {
+        std::memset(T, 0, sizeof(*T));
+        T->p.M = (int)M;
+        T->p.N = (int)N;
+        T->p.K = (int)K;
+        T->p.batch = (int)batch;
+        T->p.a_kmajor = akm ? 1 : 0;
+        T->p.b_kmajor = bkm ? 1 : 0;
+        T->p.c_dtype = cdt;
+        T->p.C = C;
+        T->p.status = d_status;
+        T->p.c_offset = Cv->offset;
+        T->p.c_rs = c_ms;
+        T->p.c_cs = c_ns;
+        T->p.c_bs = bt->nb ? bt->sc[0] : 0;
+        T->A = (const char*)A + Av->offset * 2;
+        T->B = (const char*)Bp + Bv->offset * 2;
+        T->a_ms = a_ms;
+        T->a_ks = a_ks;
+        T->a_bs = bt->nb ? bt->sa[0] : 0;
+        T->b_ns = b_ns;
+        T->b_ks = b_ks;
+        T->b_bs = bt->nb ? bt->sb[0] : 0;
+    }
+    std::memset(S, 0, sizeof(*S));
+    S->A = A;
+    S->B = Bp;
+    S->C = C;
+    S->ab_dtype = adt;
+    S->c_dtype = cdt;
+    S->M = M;
+    S->N = N;
+    S->K = K;
+    S->batch = batch;
+    S->a_off = Av->offset;
+    S->a_ms = a_ms;
+    S->a_ks = a_ks;
+    S->a_bs = bt->nb == 1 ? bt->sa[0] : 0;
+    S->b_off = Bv->offset;
+    S->b_ns = b_ns;
+    S->b_ks = b_ks;
+    S->b_bs = bt->nb == 1 ? bt->sb[0] : 0;
+    S->c_off = Cv->offset;
+    S->c_ms = c_ms;
+    S->c_ns = c_ns;
+    S->c_bs = bt->nb == 1 ? bt->sc[0] : 0;
+    return PSG_OK;
+}
+
+}  // namespace psg
+
+using namespace psg;
+
+extern "C" psg_status psg_contract(const void* A, const psg_view* Av, const void* B, const psg_view* Bv, void* C,
+                                   const psg_view* Cv, int32_t* d_status, void* stream)
+{
+    bool tc;
+    TcOperands T;
+    SimtParams S;
+    Batch bt;
+    psg_status st = plan_contract(A, Av, B, Bv, C, Cv, d_status, &tc, &T, &S, &bt);
+    if (st != PSG_OK) return st;
+    if (S.M == 0 || S.N == 0) return PSG_OK;
+    if (S.K == 0) {
+        // an empty SUM is its identity: every cell 0 (through the SIMT kernel)
+        return launch_contract_simt(S, stream);
+    }
+    if (bt.nb <= 1) return tc ? launch_contract_tc(T, stream) : launch_contract_simt(S, stream);
+    // several batch dims that do not merge: one launch per batch index
+    int64_t count = 1;
+    for (int d = 0; d < bt.nb; ++d) count *= bt.shape[d];
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t rem = i, oa = 0, ob = 0, oc = 0;
+        for (int d = bt.nb - 1; d >= 0; --d) {
+            const int64_t x = rem % bt.shape[d];
+            rem /= bt.shape[d];
+            oa += x * bt.sa[d];
+            ob += x * bt.sb[d];
+            oc += x * bt.sc[d];
+        }
+        SimtParams s1 = S;
+        s1.a_off += oa;
+        s1.b_off += ob;
+        s1.c_off += oc;
+        s1.batch = 1;
+        st = launch_contract_simt(s1, stream);
+        if (st != PSG_OK) return st;
+    }
+    return PSG_OK;
+}

@@ -1,0 +1,42 @@
+// Launch descriptors of the MUL+SUM contraction kernels.
+#pragma once
+
+#include "common.h"
+
+namespace psg {
+
+struct TcParams {
+    int M, N, K, batch;
+    int a_kmajor, b_kmajor;     // 1: k stride 1; 0: m (n) stride 1
+    int num_m, num_n, num_k;    // tile counts (filled by the launcher)
+    int c_dtype;
+    void* C;
+    int32_t* status;
+    int64_t c_offset, c_rs, c_cs, c_bs;
+};
+
+struct TcOperands {
+    TcParams p;
+    const void* A;  // at the View's offset
+    const void* B;
+    int64_t a_ms, a_ks, a_bs;   // element strides of A along m, k, batch
+    int64_t b_ns, b_ks, b_bs;
+};
+
+struct SimtParams {
+    const void* A;
+    const void* B;
+    void* C;
+    int32_t ab_dtype, c_dtype;
+    int64_t M, N, K, batch;
+    int64_t a_off, a_ms, a_ks, a_bs;
+    int64_t b_off, b_ns, b_ks, b_bs;
+    int64_t c_off, c_ms, c_ns, c_bs;
+};
+
+psg_status launch_contract_tc(const TcOperands& o, void* stream);
+void query_contract_tc(int64_t tiles, int* grid, int* block, int* smem, int* regs);
+psg_status launch_contract_simt(const SimtParams& p, void* stream);
+void query_contract_simt(const SimtParams& p, int* grid, int* block, int* smem, int* regs);
+
+}  // namespace psg

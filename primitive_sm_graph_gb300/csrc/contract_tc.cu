@@ -1,0 +1,418 @@
+// bf16 MUL+SUM contraction on the 5th-generation tensor cores (sm_103a).
+//
+// C[b, m, n] = sum_k A[b, m, k] * B[b, k, n]: limn lowers a matmul to a
+// broadcast MUL and a SUM over k that fuse into one kernel ("Reading the
+// schedule": a whole matmul is one kernel); the broadcast is the stride-0
+// loop of the Luminal IR blog ("Naive Matrix Multiplication").  Here the
+// MUL+SUM of one 128x256 output tile runs as a chain of
+// tcgen05.mma.cta_group::1.kind::f16 (bf16 inputs, float32 accumulate in
+// TMEM), fed by TMA.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0  TMA producer: one elected lane streams 64-deep K slices of A and
+//           B into a 4-stage shared-memory ring (128B-swizzled tiles);
+//   warp 1  MMA issuer: allocates all 512 TMEM columns (two 128x256 f32
+//           accumulators), one lane issues 4 MMAs (K = 16 each) per stage and
+//           commits the stage back to the producer;
+//   warps 2-5 epilogue: each warp reads its 32 TMEM lanes (rows) with
+//           tcgen05.ld, rounds to the output dtype once and stores, while the
+//           MMA warp fills the other accumulator.
+// Every wait on an mbarrier gives up after about a second: the CTA then sets
+// PSG_E_TIMEOUT in the caller's status word, drains its own copies and MMAs,
+// frees TMEM and returns.  No TMA multicast is used: each CTA loads its own
+// tiles.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "contract.h"
+#include "launch_util.cuh"
+
+namespace psg {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_BYTES = BN * BK * 2;             // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
+constexpr int TMEM_COLS = 512;                   // two 128 x 256 f32 accumulators
+constexpr int THREADS = 192;
+// (8 KB of slack after the barriers keeps every tensor-core operand read inside
+// the allocation even for the widest descriptor stride)
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + 8192;
+constexpr long long WAIT_CYCLES = 2000000000ll;  // about one second
+
+struct Bars {
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase with this parity completed; false when
+// another role gave up or a second passed (then this CTA gives up too).
+__device__ __noinline__ bool bar_wait(uint64_t* b, uint32_t parity, Bars* bars, int32_t* status)
+{
+    const long long t0 = clock64();
+    for (uint32_t i = 0;; ++i) {
+        if (bar_try(b, parity)) return true;
+        if ((i & 63) == 63) {
+            if (*(volatile int32_t*)&bars->abort) return false;
+            if (clock64() - t0 > WAIT_CYCLES) {
+                *(volatile int32_t*)&bars->abort = 1;
+                if (status) atomicCAS(status, 0, (int32_t)PSG_E_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// shared-memory matrix descriptor, 128B swizzle, sm_100 version field
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(dtmem), "l"(ad), "l"(bd), "r"(idesc), "r"(accum));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// tile index -> (batch, m block, n block), grouping 8 m-blocks so the CTAs of
+// one wave share A and B tiles in L2
+__device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& b, int& mb, int& nb)
+{
+    const int per_batch = p.num_m * p.num_n;
+    b = t / per_batch;
+    const int r = t - b * per_batch;
+    const int GM = 8;
+    const int group = r / (GM * p.num_n);
+    const int first_m = group * GM;
+    const int gm = min(GM, p.num_m - first_m);
+    const int rr = r - group * GM * p.num_n;
+    mb = first_m + rr % gm;
+    nb = rr / gm;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CUtensorMap tmap_a,
+                                                      const __grid_constant__ CUtensorMap tmap_b,
+                                                      const __grid_constant__ TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    // swizzled tiles need 1024-byte alignment of their shared-memory address
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Bars* bars = (Bars*)(smem + STAGES * STAGE_BYTES);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int total = p.num_m * p.num_n * p.batch;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            bar_init(&bars->full[s], 1);
+            bar_init(&bars->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            bar_init(&bars->tfull[a], 1);
+            bar_init(&bars->tempty[a], 4);
+        }
+        bar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&bars->tmem_base)), "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t armed = 0, armed_ph = 0;  // per-stage flags / parity of the last arm
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                int b, mb, nb;
+                tile_coords(p, t, b, mb, nb);
+                const int m0 = mb * BM, n0 = nb * BN;
+                for (int kb = 0; kb < p.num_k; ++kb) {
+                    if (!bar_wait(&bars->empty[stage], ph ^ 1u, bars, p.status)) { ok = false; break; }
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    bar_expect_tx(&bars->full[stage], STAGE_BYTES);
+                    const int k0 = kb * BK;
+                    if (p.a_kmajor) {
+                        tma_load_3d(sa, &tmap_a, &bars->full[stage], k0, m0, b);
+                    } else {
+                        tma_load_3d(sa, &tmap_a, &bars->full[stage], m0, k0, b);
+                        tma_load_3d(sa + 8192, &tmap_a, &bars->full[stage], m0 + 64, k0, b);
+                    }
+                    if (p.b_kmajor) {
+                        tma_load_3d(sb, &tmap_b, &bars->full[stage], k0, n0, b);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            tma_load_3d(sb + i * 8192, &tmap_b, &bars->full[stage], n0 + 64 * i, k0, b);
+                    }
+                    armed |= 1u << stage;
+                    armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
+                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                }
+            }
+            // every copy this CTA issued lands before the CTA may exit
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s)) {
+                    const long long t0 = clock64();
+                    while (!bar_try(&bars->full[s], (armed_ph >> s) & 1u) && clock64() - t0 < WAIT_CYCLES) {
+                    }
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            // instruction descriptor: f32 accumulate, bf16 A and B, M = 128, N = 256
+            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((p.a_kmajor ? 0u : 1u) << 15) |
+                                   ((p.b_kmajor ? 0u : 1u) << 16) | ((uint32_t)(BN >> 3) << 17) |
+                                   ((uint32_t)(BM >> 4) << 24);
+            // K-major: 8-row groups 1024 B apart, a K step of 16 is 32 B; MN-major:
+            // 64-wide MN atoms 8 KB apart, 8-row K groups 1024 B apart, a K step of
+            // 16 rows is 2 KB
+            const uint32_t a_lbo = p.a_kmajor ? 16u : 8192u, b_lbo = p.b_kmajor ? 16u : 8192u;
+            const uint32_t a_step = p.a_kmajor ? 2u : 128u, b_step = p.b_kmajor ? 2u : 128u;
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t aph[2] = {0u, 0u};
+            bool ok = true;
+            int local = 0;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
+                const int acc = local & 1;
+                if (!bar_wait(&bars->tempty[acc], aph[acc] ^ 1u, bars, p.status)) break;
+                tc_fence_after();
+                const uint32_t dtm = tmem + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < p.num_k; ++kb) {
+                    if (!bar_wait(&bars->full[stage], ph, bars, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    const uint64_t ad = sdesc(sa, a_lbo, 1024u), bd = sdesc(sb, b_lbo, 1024u);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16(dtm, ad + (uint64_t)(k * a_step), bd + (uint64_t)(k * b_step), idesc,
+                                 (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(&bars->empty[stage]);  // frees the stage when these MMAs finish
+                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(&bars->tfull[acc]);  // accumulator ready for the epilogue
+                aph[acc] ^= 1u;
+            }
+            // every MMA issued by this CTA completes before TMEM is freed
+            mma_commit(&bars->drain);
+            const long long t0 = clock64();
+            while (!bar_try(&bars->drain, 0u) && clock64() - t0 < WAIT_CYCLES) {
+            }
+        }
+    } else {
+        // ---------------- epilogue: TMEM -> registers -> global ----------------
+        const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
+        uint32_t aph[2] = {0u, 0u};
+        int local = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
+            const int acc = local & 1;
+            if (!bar_wait(&bars->tfull[acc], aph[acc], bars, p.status)) break;
+            aph[acc] ^= 1u;
+            tc_fence_after();
+            int b, mb, nb;
+            tile_coords(p, t, b, mb, nb);
+            const int m = mb * BM + q * 32 + lane;
+            const int64_t crow = p.c_offset + (int64_t)b * p.c_bs + (int64_t)m * p.c_rs;
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                __syncwarp();  // tcgen05.ld is warp-collective: reach it converged
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), r);
+                const int n0 = nb * BN + c;
+                if (m < p.M) {
+                    if (p.c_dtype == PSG_BF16) {
+                        __nv_bfloat16* dst = (__nv_bfloat16*)p.C + crow + n0;
+                        if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
+                            uint32_t w[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]),
+                                                                                __uint_as_float(r[2 * j + 1]));
+                                w[j] = *(const uint32_t*)&h;
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                ((uint4*)dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                        } else {
+                            __nv_bfloat16* C = (__nv_bfloat16*)p.C;
+                            for (int j = 0; j < 32; ++j)
+                                if (n0 + j < p.N)
+                                    C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                        }
+                    } else {
+                        float* dst = (float*)p.C + crow + n0;
+                        if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                ((uint4*)dst)[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                        } else {
+                            float* C = (float*)p.C;
+                            for (int j = 0; j < 32; ++j)
+                                if (n0 + j < p.N) C[crow + (int64_t)(n0 + j) * p.c_cs] = __uint_as_float(r[j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&bars->tempty[acc]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    });
+    return fn;
+}
+
+// 3-D tensor map over a bf16 operand: dims {inner, outer, batch}.
+bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t batch, int64_t outer_stride,
+              int64_t batch_stride, uint32_t box_inner, uint32_t box_outer)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)batch};
+    cuuint64_t strides[2] = {(cuuint64_t)(outer_stride * 2), (cuuint64_t)(batch_stride * 2)};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+psg_status launch_contract_tc(const TcOperands& o, void* stream)
+{
+    TcParams p = o.p;
+    if (p.M == 0 || p.N == 0 || p.batch == 0) return PSG_OK;
+    CUtensorMap ma, mb;
+    // batch strides of a single batch are never used; keep them a legal multiple of 16 bytes
+    const int64_t a_bs = p.batch > 1 ? o.a_bs : (p.a_kmajor ? o.a_ms * p.M : o.a_ks * p.K);
+    const int64_t b_bs = p.batch > 1 ? o.b_bs : (p.b_kmajor ? o.b_ns * p.N : o.b_ks * p.K);
+    bool ok = p.a_kmajor ? make_map(&ma, o.A, p.K, p.M, p.batch, o.a_ms, a_bs, 64, 128)
+                         : make_map(&ma, o.A, p.M, p.K, p.batch, o.a_ks, a_bs, 64, 64);
+    ok = ok && (p.b_kmajor ? make_map(&mb, o.B, p.K, p.N, p.batch, o.b_ns, b_bs, 64, 256)
+                           : make_map(&mb, o.B, p.N, p.K, p.batch, o.b_ks, b_bs, 64, 64));
+    if (!ok) return PSG_E_CUDA;
+    p.num_m = (p.M + BM - 1) / BM;
+    p.num_n = (p.N + BN - 1) / BN;
+    p.num_k = (p.K + BK - 1) / BK;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute((const void*)tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return PSG_E_CUDA;
+    const int64_t tiles = (int64_t)p.num_m * p.num_n * p.batch;
+    const int grid = (int)std::min<int64_t>(tiles, num_sms());
+    tc_gemm<<<grid, THREADS, SMEM_BYTES, (cudaStream_t)stream>>>(ma, mb, p);
+    return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
+}
+
+void query_contract_tc(int64_t tiles, int* grid, int* block, int* smem, int* regs)
+{
+    *grid = (int)std::min<int64_t>(tiles, num_sms());
+    *block = THREADS;
+    *smem = SMEM_BYTES;
+    *regs = kernel_regs((const void*)tc_gemm);
+}
+
+}  // namespace psg

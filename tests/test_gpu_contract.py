@@ -1,0 +1,163 @@
+"""GPU parity of psg_contract (matmul as SUM over k of MUL of two broadcast
+Views) against the oracle's naive MUL+SUM loop.
+
+Bar (the reduction-order term of Litmus's ToleranceBound, per output cell):
+  |c - c_ref| <= 2*gamma_{K-1} * sum_k |a_k b_k|           (float32 output)
+  |c - c_ref| <= 2^-7 |c_ref| + 2*gamma_{K-1} * sum|a b|    (bfloat16 output)
+where c_ref is the oracle's float32 total.
+"""
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as SI
+from helpers import dev, gamma, storage_dtype, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    from primitive_sm_graph_gb300 import _abi
+    return _abi
+
+
+def _views(A, dA, dB, M, N, K, a_layout="mk", b_layout="kn", batch=None):
+    """Broadcast Views [batch.., M, N, K] of A and B over their storage."""
+    a_ms, a_ks = (K, 1) if a_layout == "mk" else (1, M)
+    b_ns, b_ks = (1, N) if b_layout == "kn" else (K, 1)
+    shape, sa, sb = [M, N, K], [a_ms, 0, a_ks], [0, b_ns, b_ks]
+    if batch:
+        shape = [batch] + shape
+        sa = [M * K] + sa
+        sb = [K * N] + sb
+    return A.view_of(dA, shape=shape, strides=sa), A.view_of(dB, shape=shape, strides=sb)
+
+
+def _check(got, ref32, mag, K, out_dt):
+    g = got.astype(np.float64)
+    r = ref32.astype(np.float64)
+    tol = 2 * gamma(K - 1) * mag + 1e-30
+    if out_dt == "bf16":
+        tol = tol + 2.0 ** -7 * np.abs(r)
+    bad = np.abs(g - r) > tol
+    assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:3], g[bad][:3], r[bad][:3])
+
+
+def _storage(t, layout):
+    return t if layout in ("mk", "kn") else t.t().contiguous()
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 100), (1, 1, 1), (64, 48, 32), (257, 513, 1000),
+                                   (512, 256, 4096)])
+@pytest.mark.parametrize("out_dt", ["bf16", "f32"])
+def test_bf16_contraction_matches_oracle(A, O, M, N, K, out_dt):
+    a, b = SI.contraction_bf16(M + N + K, M, N, K)
+    ref = O.matmul(O.T(SI.bits(a), "bf16"), O.T(SI.bits(b), "bf16"), "f32").data
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, M, N, K)
+    C = torch.empty((M, N), dtype=storage_dtype(out_dt), device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = O.T(to_np(C.cpu()), out_dt).f64()
+    _check(got, ref, mag, K, out_dt)
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [("mk", "kn"), ("km", "kn"), ("mk", "nk"), ("km", "nk")])
+def test_every_operand_major(A, O, a_layout, b_layout):
+    M, N, K = 300, 520, 200
+    a, b = SI.contraction_bf16(7, M, N, K)
+    ref = O.matmul(O.T(SI.bits(a), "bf16"), O.T(SI.bits(b), "bf16"), "f32").data
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    dA, dB = dev(_storage(a, a_layout)), dev(_storage(b, b_layout))
+    Av, Bv = _views(A, dA, dB, M, N, K, a_layout, b_layout)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), torch.zeros((1,), dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    _check(C.cpu().numpy(), ref, mag, K, "f32")
+
+
+def test_batched_contraction_and_kept_dim(A, O):
+    Bt, M, N, K = 5, 70, 130, 96
+    g = SI.gen(5)
+    a = SI.normal((Bt, M, K), 0, 0.1, g, torch.bfloat16)
+    b = SI.normal((Bt, K, N), 0, 0.1, g, torch.bfloat16)
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, M, N, K, batch=Bt)
+    C = torch.empty((Bt, M, N, 1), dtype=torch.bfloat16, device="cuda")  # the (M,N,1) sink form
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), torch.zeros((1,), dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    got = O.T(to_np(C.cpu()), "bf16").f64().reshape(Bt, M, N)
+    for i in range(Bt):
+        ref = O.matmul(O.T(SI.bits(a[i]), "bf16"), O.T(SI.bits(b[i]), "bf16"), "f32").data
+        mag = (a[i].double().abs() @ b[i].double().abs()).numpy()
+        _check(got[i], ref, mag, K, "bf16")
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 48, 32), (129, 131, 257), (1, 5, 3)])
+def test_f32_contraction_simt(A, O, M, N, K):
+    a, b = SI.contraction_f32(M * N + K, M, N, K)
+    ref = O.matmul(O.T(a.numpy(), "f32"), O.T(b.numpy(), "f32"), "f32").data
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, M, N, K)
+    C = torch.empty((M, N), device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), torch.zeros((1,), dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    _check(C.cpu().numpy(), ref, mag, K, "f32")
+
+
+def test_tiny_graph_literal_shape(A, O):
+    """The tiny graph's 64x32 @ 32x48 float32 contraction through the same call."""
+    a, b = SI.tiny_graph(0)
+    ref = O.matmul_literal(O.T(a.numpy(), "f32"), O.T(b.numpy(), "f32")).data.reshape(64, 48)
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, 64, 48, 32)
+    C = torch.empty((64, 48), device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), None)
+    torch.cuda.synchronize()
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    _check(C.cpu().numpy(), ref, mag, 32, "f32")
+
+
+def _sampled_full(A, O, a, b, out_dt, n_cells, seed):
+    M, K = a.shape
+    N = b.shape[1]
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, M, N, K)
+    C = torch.empty((M, N), dtype=storage_dtype(out_dt), device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    g = np.random.default_rng(seed)
+    ii = g.integers(0, M, n_cells)
+    jj = g.integers(0, N, n_cells)
+    # include the corners and the last tile's edges
+    ii = np.concatenate([ii, [0, M - 1, M - 1, 0]])
+    jj = np.concatenate([jj, [0, N - 1, 0, N - 1]])
+    dt = "bf16" if a.dtype == torch.bfloat16 else "f32"
+    acc, mag = O.matmul_cells(O.T(SI.bits(a), dt), O.T(SI.bits(b), dt), ii, jj)
+    got = O.T(to_np(C.cpu()), out_dt).f64()[ii, jj]
+    _check(got, acc, mag, K, out_dt)
+    return C
+
+
+def test_full_size_bf16_sampled(A, O):
+    a, b = SI.contraction_bf16(0)
+    C = _sampled_full(A, O, a, b, "bf16", 3000, 1)
+    # same bits twice
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, 8192, 8192, 8192)
+    C2 = torch.empty_like(C)
+    A.psg_contract(dA, Av, dB, Bv, C2, A.view_of(C2), None)
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+
+
+def test_full_size_f32_sampled(A, O):
+    a, b = SI.contraction_f32(0)
+    _sampled_full(A, O, a, b, "f32", 2000, 2)
