@@ -242,6 +242,33 @@ psg_status psg_scatter_add(void* dst, const psg_view* dv, const int32_t* idx, in
                            int32_t* d_status, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * psg_scatter_add_static -- the same deterministic SCATTER-add as
+ * psg_scatter_add, for callers that cannot allocate device memory: code that
+ * runs after a memory pool has reserved the whole GPU and hands out no more,
+ * or paths that must not allocate at all (a step being recorded for replay,
+ * a loop with a fixed memory budget).  It takes no workspace; its scratch
+ * (the sort keys) is one fixed array inside this library's device image, of
+ * PSG_SCATTER_STATIC_MAX_N 64-bit keys (8 MiB), which every GPU that loads
+ * the library holds until the process exits.  The pages have no counterpart
+ * to this call.
+ *   - n must be <= PSG_SCATTER_STATIC_MAX_N, else PSG_E_WORKSPACE and nothing
+ *     is launched; the other arguments and errors are those of
+ *     psg_scatter_add.
+ *   - It calls no device allocator of any kind.  The first call on a device
+ *     looks up the array's device address once (with that device current)
+ *     and caches it; make that first call before any stream capture.
+ *   - Every call shares the one array and leaves its keys there; each call
+ *     rewrites every key it reads, so nothing needs clearing between calls.
+ *     Two calls that run on the GPU at the same time (different streams
+ *     without ordering between them) race on the array and give wrong sums:
+ *     order them on one stream.
+ * ------------------------------------------------------------------------- */
+#define PSG_SCATTER_STATIC_MAX_N (1 << 20)
+psg_status psg_scatter_add_static(void* dst, const psg_view* dv, const int32_t* idx, int64_t n,
+                                  const void* upd, const psg_view* uv, int32_t* d_status,
+                                  void* stream);
+
+/* ---------------------------------------------------------------------------
  * psg_query_launch -- the launch a call would make, before making it (Tiki,
  * "The architecture we want": register and shared-memory budgets visible
  * before launch).  call: one of psg_call; v: the output view the call would

@@ -82,6 +82,8 @@ def _load():
     L.psg_scatter_workspace.argtypes = [i64]
     L.psg_scatter_workspace.restype = sz
     L.psg_scatter_add.argtypes = [vp, V, vp, i64, vp, V, vp, sz, vp, vp]
+    L.psg_scatter_add_static.argtypes = [vp, V, vp, i64, vp, V, vp, vp]
+    L.psg_scatter_add_static.restype = i32
     L.psg_query_launch.argtypes = [i32, V, P32, P32, P32, P32]
     L.psg_status_string.argtypes = [i32]
     L.psg_status_string.restype = ctypes.c_char_p
@@ -256,6 +258,20 @@ def psg_scatter_add(dst, dv, idx, n, upd, uv, workspace, ws_bytes, d_status, str
                              _stream(stream))
     if check:
         _check(st, "psg_scatter_add")
+    return st
+
+
+SCATTER_STATIC_MAX_N = 1 << 20
+
+
+def psg_scatter_add_static(dst, dv, idx, n, upd, uv, d_status, stream=None, check=True) -> int:
+    """psg_scatter_add without a workspace: its keys live in a fixed array
+    inside the library (n <= SCATTER_STATIC_MAX_N), for callers that cannot
+    allocate device memory."""
+    st = lib.psg_scatter_add_static(_ptr(dst), ctypes.byref(dv), _ptr(idx), int(n), _ptr(upd),
+                                    ctypes.byref(uv), _ptr(d_status), _stream(stream))
+    if check:
+        _check(st, "psg_scatter_add_static")
     return st
 
 

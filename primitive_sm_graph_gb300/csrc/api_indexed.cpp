@@ -141,4 +141,20 @@ psg_status psg_scatter_add(void* dst, const psg_view* dv, const int32_t* idx, in
     return launch_scatter(L, (unsigned long long*)workspace, stream);
 }
 
+psg_status psg_scatter_add_static(void* dst, const psg_view* dv, const int32_t* idx, int64_t n, const void* upd,
+                                  const psg_view* uv, int32_t* d_status, void* stream)
+{
+    ScatterLaunch L;
+    psg_status st = plan_scatter(dst, dv, idx, n, upd, uv, d_status, &L);
+    if (st != PSG_OK) return st;
+    if (n == 0) return PSG_OK;
+    if (n > PSG_SCATTER_STATIC_MAX_N) return PSG_E_WORKSPACE;
+    unsigned long long* keys = nullptr;
+    st = static_scatter_keys(&keys);
+    if (st != PSG_OK) return st;
+    // every key slot the sort reads is written by this call first, so the
+    // previous call's contents need no clearing
+    return launch_scatter(L, keys, stream);
+}
+
 }  // extern "C"

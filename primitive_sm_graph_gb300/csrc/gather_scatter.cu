@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "gather_scatter.h"
 #include "launch_util.cuh"
@@ -227,7 +228,33 @@ int grid_for(const void* fn, int threads, int64_t work_blocks)
     return (int)std::max<int64_t>(1, std::min<int64_t>(work_blocks, (int64_t)num_sms() * per_sm));
 }
 
+// Fixed scratch for psg_scatter_add_static: the sort keys of one call.  It is
+// part of this library's device image, so every GPU that loads the library
+// holds these 8 MiB until the process exits; the allocating scatter call never
+// touches it.
+__device__ __align__(256) unsigned long long g_static_keys[kStaticScatterKeys];
+
 }  // namespace
+
+// Device address of g_static_keys on the current device.  In host code the
+// array's name only stands in for the symbol, so the address is asked from the
+// runtime once per device (with that device current) and cached.
+psg_status static_scatter_keys(unsigned long long** out)
+{
+    constexpr int MAX_DEV = 64;
+    static std::mutex mu;
+    static unsigned long long* ptrs[MAX_DEV];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return PSG_E_CUDA;
+    std::lock_guard<std::mutex> g(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_keys) != cudaSuccess || !p) return PSG_E_CUDA;
+        ptrs[dev] = (unsigned long long*)p;
+    }
+    *out = ptrs[dev];
+    return PSG_OK;
+}
 
 int64_t scatter_npow2(int64_t n)
 {

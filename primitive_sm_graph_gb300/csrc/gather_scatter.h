@@ -29,7 +29,12 @@ struct ScatterLaunch {
     int64_t upd_offset, upd_rs, upd_cs;
 };
 
+// Capacity of the static key scratch of psg_scatter_add_static (keys, after
+// rounding n up to a power of two).
+constexpr int64_t kStaticScatterKeys = int64_t(1) << 20;
+
 int64_t scatter_npow2(int64_t n);
+psg_status static_scatter_keys(unsigned long long** out);
 psg_status launch_gather(const GatherLaunch& L, void* stream);
 // keys: device scratch of scatter_npow2(n) 64-bit words
 psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void* stream);
