@@ -70,6 +70,7 @@ def lib():
         L.orc_where.argtypes = [i32, vp, i32, vp, vp, vp, i64, i32]
         L.orc_reduce.argtypes = [i32, i32, vp, i64, i64, vp, i32]
         L.orc_matmul.argtypes = [i32, vp, vp, i32, vp, i64, i64, i64, i32]
+        L.orc_matmul_bt.argtypes = [i32, vp, vp, i32, vp, i64, i64, i64, i32]
         L.orc_matmul_cells.argtypes = [i32, vp, vp, i64, i64, i64, vp, vp, i64, vp, vp, i32]
         L.orc_gather_rows.argtypes = [i32, vp, i64, i64, vp, i64, vp]
         L.orc_gather_rows.restype = i64
@@ -248,6 +249,20 @@ def matmul(A: T, B: T, out_dt: str | None = None) -> T:
     out_dt = out_dt or A.dt
     C = np.empty((M, N), _NP[out_dt])
     lib().orc_matmul(_DT[A.dt], _p(A.data), _p(B.data), _DT[out_dt], _p(C), M, N, K, NTHREADS)
+    return T(C, out_dt)
+
+
+def matmul_bt(A: T, BT: T, out_dt: str | None = None) -> T:
+    """:func:`matmul` with B given transposed ([N, K]): the same products in
+    the same k order (so the same bits), walking memory row by row."""
+    M, K = A.shape
+    N, K2 = BT.shape
+    assert K == K2 and A.dt == BT.dt
+    out_dt = out_dt or A.dt
+    C = np.empty((M, N), _NP[out_dt])
+    rc = lib().orc_matmul_bt(_DT[A.dt], _p(A.data), _p(BT.data), _DT[out_dt], _p(C), M, N, K, NTHREADS)
+    if rc != 0:
+        raise TypeError("matmul_bt on %s" % A.dt)
     return T(C, out_dt)
 
 

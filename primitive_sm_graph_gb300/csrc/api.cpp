@@ -95,7 +95,7 @@ extern "C" int psg_internal_compile_elementwise(const psg_node* prog, int n_node
     psg_status st = plan_elementwise(prog, n_nodes, fake, in_v, n_in, (void*)(uintptr_t)4096, out_v, &P);
     if (st != PSG_OK) return st;
     std::string l;
-    st = jit_compile_only(P.src, &l);
+    st = jit_compile_only(jit_source(JIT_EW, P.spec), &l);
     if (log && log_size) {
         std::strncpy(log, l.c_str(), log_size - 1);
         log[log_size - 1] = 0;

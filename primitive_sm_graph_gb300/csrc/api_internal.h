@@ -17,7 +17,7 @@ int fill_operand(PsgOperand& op, const void* ptr, const psg_view* v, const Space
 struct EwPlan {
     PsgEwParams p;
     int n_in;
-    std::string src;  // full runtime-compiled source
+    std::string spec;  // the program-specific part of the runtime-compiled source
 };
 psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const* in,
                             const psg_view* in_v, int n_in, void* out, const psg_view* out_v,

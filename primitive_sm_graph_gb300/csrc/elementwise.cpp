@@ -84,7 +84,7 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
     spec += m + "};\n" + d + "};\n";
     spec += "constexpr int kOutDt = " + std::to_string(out_v->dtype) + ";\n";
     spec += gen_eval(prog, I, "Body");
-    P->src = jit_source(JIT_EW, spec);
+    P->spec = std::move(spec);
     return PSG_OK;
 }
 
@@ -102,7 +102,7 @@ psg_status launch_elementwise(const EwPlan& P, void* stream)
 {
     if (P.p.rows == 0 || P.p.inner == 0) return PSG_OK;
     cudaKernel_t k;
-    psg_status st = jit_kernel(P.src, "psg_ew", &k);
+    psg_status st = jit_kernel(JIT_EW, P.spec, "psg_ew", &k);
     if (st != PSG_OK) return st;
     int grid;
     grid_for(P, k, &grid);
@@ -116,7 +116,7 @@ psg_status launch_elementwise(const EwPlan& P, void* stream)
 psg_status query_elementwise(const EwPlan& P, int* grid, int* block, int* smem, int* regs)
 {
     cudaKernel_t k;
-    psg_status st = jit_kernel(P.src, "psg_ew", &k);
+    psg_status st = jit_kernel(JIT_EW, P.spec, "psg_ew", &k);
     if (st != PSG_OK) return st;
     grid_for(P, k, grid);
     *block = EW_THREADS;

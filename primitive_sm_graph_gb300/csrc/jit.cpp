@@ -79,14 +79,19 @@ psg_status jit_compile_only(const std::string& src, std::string* log)
     return compile(src, nullptr, log);
 }
 
-psg_status jit_kernel(const std::string& src, const char* name, cudaKernel_t* out)
+psg_status jit_kernel(JitSkeleton sk, const std::string& spec, const char* name, cudaKernel_t* out)
 {
+    std::string key;
+    key.reserve(spec.size() + 2);
+    key += (char)('0' + (int)sk);
+    key += spec;
     std::lock_guard<std::mutex> g(g_mu);
-    auto it = cache().find(src);
+    auto it = cache().find(key);
     if (it != cache().end()) {
         *out = it->second;
         return PSG_OK;
     }
+    const std::string src = jit_source(sk, spec);
     std::vector<char> cubin;
     std::string log;
     psg_status st = compile(src, &cubin, &log);
@@ -96,7 +101,7 @@ psg_status jit_kernel(const std::string& src, const char* name, cudaKernel_t* ou
         return PSG_E_CUDA;
     cudaKernel_t k;
     if (cudaLibraryGetKernel(&k, lib, name) != cudaSuccess) return PSG_E_CUDA;
-    cache().emplace(src, k);
+    cache().emplace(std::move(key), k);
     *out = k;
     return PSG_OK;
 }

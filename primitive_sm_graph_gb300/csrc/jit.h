@@ -16,10 +16,11 @@ enum JitSkeleton { JIT_EW = 0, JIT_REDUCE = 1 };
 // Full source: params + prelude + `spec` (constexpr tables and bodies) + skeleton.
 std::string jit_source(JitSkeleton sk, const std::string& spec);
 
-// Compile (or fetch from the cache) and return the kernel named `name`.
-// Returns PSG_E_CUDA on a compile or load failure (the NVRTC log is printed
-// to stderr when PSG_JIT_VERBOSE is set).
-psg_status jit_kernel(const std::string& src, const char* name, cudaKernel_t* out);
+// Compile (or fetch from the cache) the kernel `name` of skeleton `sk`
+// specialised by `spec`.  The cache is keyed by (sk, spec), so a hit costs a
+// hash of the short spec only.  Returns PSG_E_CUDA on a compile or load
+// failure (the NVRTC log is printed to stderr when PSG_JIT_VERBOSE is set).
+psg_status jit_kernel(JitSkeleton sk, const std::string& spec, const char* name, cudaKernel_t* out);
 
 // Compile only (no device needed); for host-side checks of generated code.
 psg_status jit_compile_only(const std::string& src, std::string* log);

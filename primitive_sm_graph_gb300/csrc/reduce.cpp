@@ -17,7 +17,7 @@ namespace {
 struct RedPlan {
     PsgRedParams p;
     int block;
-    std::string src;
+    std::string spec;
 };
 
 std::string int_list(const int* v, int n)
@@ -147,7 +147,7 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     spec += "constexpr int kPerRow = " + std::to_string(per_row ? 1 : 0) + ";\n";
     spec += "template <int S> struct StageBody;\n";
     spec += bodies;
-    P->src = jit_source(JIT_REDUCE, spec);
+    P->spec = std::move(spec);
     return PSG_OK;
 }
 
@@ -161,6 +161,25 @@ psg_status grid_for(const RedPlan& P, cudaKernel_t k, int* grid)
 }
 
 }  // namespace
+
+psg_status query_reduce(const psg_reduce_stage* stages, int n_stages, const psg_node* epi, int n_epi,
+                        const psg_view* in_v, int n_in, const psg_view* out_v, int* grid, int* block,
+                        int* smem, int* regs)
+{
+    const void* fake[PSG_MAX_INPUTS];
+    for (int k = 0; k < PSG_MAX_INPUTS; ++k) fake[k] = (const void*)(uintptr_t)4096;
+    RedPlan P;
+    psg_status st = plan_reduce(stages, n_stages, epi, n_epi, fake, in_v, n_in, (void*)(uintptr_t)4096, out_v, &P);
+    if (st != PSG_OK) return st;
+    cudaKernel_t k;
+    st = jit_kernel(JIT_REDUCE, P.spec, "psg_reduce", &k);
+    if (st != PSG_OK) return st;
+    grid_for(P, k, grid);
+    *block = P.block;
+    *smem = 0;
+    *regs = jit_regs(k);
+    return PSG_OK;
+}
 
 }  // namespace psg
 
@@ -176,7 +195,7 @@ extern "C" psg_status psg_reduce_rows(const psg_reduce_stage* stages, int n_stag
     if (st != PSG_OK) return st;
     if (P.p.rows == 0) return PSG_OK;
     cudaKernel_t k;
-    st = jit_kernel(P.src, "psg_reduce", &k);
+    st = jit_kernel(JIT_REDUCE, P.spec, "psg_reduce", &k);
     if (st != PSG_OK) return st;
     int grid;
     grid_for(P, k, &grid);
@@ -199,7 +218,7 @@ extern "C" int psg_internal_compile_reduce(const psg_reduce_stage* stages, int n
                                 out_v, &P);
     if (st != PSG_OK) return st;
     std::string l;
-    st = jit_compile_only(P.src, &l);
+    st = jit_compile_only(jit_source(JIT_REDUCE, P.spec), &l);
     if (log && log_size) {
         std::strncpy(log, l.c_str(), log_size - 1);
         log[log_size - 1] = 0;

@@ -1,0 +1,1055 @@
+"""Lazy tensors over the closed primitive op set, a scheduler that cuts the
+graph into the library's five kernel calls, and reverse-mode autograd.
+
+The design follows limn ("Architecture", "Reading the schedule"):
+  * Tensor methods never compute; they add nodes.  ``realize()`` runs them.
+  * Composed ops (sub, div, relu, matmul, softmax, rmsnorm, ...) are spelled
+    in the primitives, so the kernels only ever see primitives.
+  * Movement ops compose into Views and cost nothing; a movement of an
+    elementwise value is pushed into that value's operands, so it never forces
+    a copy.
+  * Elementwise work fuses into whatever consumes it; a cut falls where a
+    value must exist in memory: a reduction, a contraction, a gather/scatter,
+    a value used by several consumers.
+  * A SUM over the last axis of MUL(x, y), where x and y are broadcast Views
+    of realized buffers, is a contraction and runs as one psg_contract call
+    (limn: "a whole matmul is one kernel").
+  * Reductions over the same rows fuse into one psg_reduce_rows call with the
+    elementwise work that consumes them as its epilogue (softmax, RMSNorm).
+  * ``backward()`` walks the graph in reverse and builds the gradients as
+    lazy graphs of the same primitives.
+
+Every kernel runs through the C ABI (``_abi``); torch only owns device memory
+and the stream.
+"""
+from __future__ import annotations
+
+import sys
+from math import prod
+
+import torch
+
+from . import _abi as A
+from .tensor_util import torch_dtype
+from .view import View
+
+EW_UNARY = ("NEG", "EXP", "LOG", "SQRT", "RECIP", "CAST")
+EW_BINARY = ("ADD", "MUL", "CMPLT")
+ELEMENTWISE = EW_UNARY + EW_BINARY + ("WHERE", "CONST")
+REDUCE = ("SUM", "MAX")
+FLOATS = ("f32", "bf16", "f16")
+sys.setrecursionlimit(max(sys.getrecursionlimit(), 20000))
+
+
+class Tensor:
+    """A node of the lazy graph.  ``shape`` is the logical shape; ``arg``
+    holds op-specific data; ``_real`` the realized (buffer, View)."""
+
+    __slots__ = ("op", "src", "shape", "dtype", "arg", "requires_grad", "grad", "_real", "_users",
+                 "__weakref__")
+
+    def __init__(self, op, src, shape, dtype, arg=None, requires_grad=False):
+        self.op = op
+        self.src = tuple(src)
+        self.shape = tuple(int(s) for s in shape)
+        self.dtype = dtype
+        self.arg = arg
+        self.requires_grad = requires_grad or any(s.requires_grad for s in self.src)
+        self.grad = None
+        self._real = None
+        self._users = 0
+
+    def __repr__(self):
+        return "Tensor(%s, %s, %s)" % (self.op, self.shape, self.dtype)
+
+    # ---- sources -----------------------------------------------------------
+    @staticmethod
+    def from_torch(t: torch.Tensor, requires_grad=False) -> "Tensor":
+        from .tensor_util import dtype_name
+        t = t.contiguous()
+        x = Tensor("BUF", (), t.shape, dtype_name(t.dtype), requires_grad=requires_grad)
+        x._real = (t, View(t.shape))
+        return x
+
+    @staticmethod
+    def const(value, shape, dtype="f32") -> "Tensor":
+        return Tensor("CONST", (), shape, dtype, arg=float(value))
+
+    @staticmethod
+    def zeros(shape, dtype="f32") -> "Tensor":
+        return Tensor.const(0.0, shape, dtype)
+
+    def numel(self):
+        return prod(self.shape)
+
+    @property
+    def ndim(self):
+        return len(self.shape)
+
+    # ---- elementwise primitives ---------------------------------------------
+    def _un(self, op):
+        if op in ("EXP", "LOG", "SQRT", "RECIP") and self.dtype not in FLOATS:
+            raise TypeError("%s needs a float dtype" % op)
+        return Tensor(op, (self,), self.shape, self.dtype)
+
+    def neg(self): return self._un("NEG")
+    def exp(self): return self._un("EXP")
+    def log(self): return self._un("LOG")
+    def sqrt(self): return self._un("SQRT")
+    def recip(self): return self._un("RECIP")
+
+    def cast(self, dtype):
+        if dtype == self.dtype:
+            return self
+        return Tensor("CAST", (self,), self.shape, dtype)
+
+    def _coerce(self, other):
+        if isinstance(other, Tensor):
+            return other
+        return Tensor.const(other, (), self.dtype)
+
+    def _bin(self, op, other):
+        b = self._coerce(other)
+        a = self
+        if a.dtype != b.dtype:
+            raise TypeError("%s of %s and %s: cast explicitly" % (op, a.dtype, b.dtype))
+        a, b = broadcast(a, b)
+        return Tensor(op, (a, b), a.shape, a.dtype)
+
+    def add(self, o): return self._bin("ADD", o)
+    def mul(self, o): return self._bin("MUL", o)
+    def cmplt(self, o): return self._bin("CMPLT", o)
+
+    def where(self, x, y):
+        """WHERE(self, x, y): self nonzero selects x."""
+        x = x if isinstance(x, Tensor) else Tensor.const(x, (), y.dtype if isinstance(y, Tensor) else "f32")
+        y = y if isinstance(y, Tensor) else Tensor.const(y, (), x.dtype)
+        c, x, y = broadcast(self, x, y)
+        return Tensor("WHERE", (c, x, y), x.shape, x.dtype)
+
+    # composed elementwise ops (limn, "Three rules": composed from primitives)
+    def __add__(self, o): return self.add(o)
+    def __radd__(self, o): return self._coerce(o).add(self)
+    def __mul__(self, o): return self.mul(o)
+    def __rmul__(self, o): return self._coerce(o).mul(self)
+    def __neg__(self): return self.neg()
+    def __sub__(self, o): return self.add(self._coerce(o).neg())
+    def __rsub__(self, o): return self._coerce(o).add(self.neg())
+    def __truediv__(self, o): return self.mul(self._coerce(o).recip())
+    def __lt__(self, o): return self.cmplt(o)
+    def __gt__(self, o): return self._coerce(o).cmplt(self)
+
+    def relu(self):
+        zero = Tensor.const(0.0, (), self.dtype)
+        return zero.cmplt(self).where(self, zero)
+
+    def square(self):
+        return self.mul(self)
+
+    # ---- movement --------------------------------------------------------------
+    def _move(self, kind, arg, shape):
+        return Tensor("MOVE", (self,), shape, self.dtype, arg=(kind, arg))
+
+    def reshape(self, *shape):
+        if len(shape) == 1 and isinstance(shape[0], (tuple, list)):
+            shape = tuple(shape[0])
+        shape = list(shape)
+        if -1 in shape:
+            i = shape.index(-1)
+            shape[i] = self.numel() // max(1, prod(s for s in shape if s != -1))
+        shape = tuple(shape)
+        assert prod(shape) == self.numel(), (self.shape, shape)
+        if shape == self.shape:
+            return self
+        return self._move("reshape", shape, shape)
+
+    def permute(self, *perm):
+        if len(perm) == 1 and isinstance(perm[0], (tuple, list)):
+            perm = tuple(perm[0])
+        if tuple(perm) == tuple(range(self.ndim)):
+            return self
+        return self._move("permute", tuple(perm), [self.shape[p] for p in perm])
+
+    def transpose(self, a=-2, b=-1):
+        p = list(range(self.ndim))
+        p[a], p[b] = p[b], p[a]
+        return self.permute(p)
+
+    @property
+    def T(self):
+        return self.transpose()
+
+    def expand(self, *shape):
+        if len(shape) == 1 and isinstance(shape[0], (tuple, list)):
+            shape = tuple(shape[0])
+        if tuple(shape) == self.shape:
+            return self
+        return self._move("expand", tuple(shape), shape)
+
+    def shrink(self, arg):
+        arg = tuple((int(a), int(b)) for a, b in arg)
+        if all(a == 0 and b == s for (a, b), s in zip(arg, self.shape)):
+            return self
+        return self._move("shrink", arg, [b - a for a, b in arg])
+
+    def pad(self, arg):
+        arg = tuple((int(a), int(b)) for a, b in arg)
+        if all(a == 0 and b == 0 for a, b in arg):
+            return self
+        return self._move("pad", arg, [s + a + b for s, (a, b) in zip(self.shape, arg)])
+
+    def contiguous(self):
+        return Tensor("CONTIG", (self,), self.shape, self.dtype)
+
+    def detach(self):
+        """Cut the gradient path: the value, with no backward through it."""
+        t = Tensor("MOVE", (self,), self.shape, self.dtype, arg=("detach", None))
+        t.requires_grad = False
+        return t
+
+    # ---- reductions --------------------------------------------------------------
+    def _reduce(self, op, axis=-1, keepdim=True):
+        axis = axis % self.ndim
+        if axis != self.ndim - 1:
+            perm = [d for d in range(self.ndim) if d != axis] + [axis]
+            inv = [0] * self.ndim
+            for i, p in enumerate(perm):
+                inv[p] = i
+            r = self.permute(perm)._reduce(op, -1, True).permute(inv)
+        else:
+            r = Tensor(op, (self,), self.shape[:-1] + (1,), self.dtype)
+        if not keepdim:
+            r = r.reshape(tuple(s for d, s in enumerate(self.shape) if d != axis))
+        return r
+
+    def sum(self, axis=-1, keepdim=True): return self._reduce("SUM", axis, keepdim)
+    def max(self, axis=-1, keepdim=True): return self._reduce("MAX", axis, keepdim)
+
+    def mean(self, axis=-1, keepdim=True):
+        n = self.shape[axis]
+        return self.sum(axis, keepdim) * (1.0 / n)
+
+    # ---- indexed -------------------------------------------------------------------
+    def gather(self, idx: "Tensor"):
+        """GATHER along dim 0: out[n, ...] = self[idx[n], ...]."""
+        assert idx.dtype == "i32" and idx.ndim == 1
+        return Tensor("GATHER", (self, idx), (idx.shape[0],) + self.shape[1:], self.dtype)
+
+    def scatter_add(self, idx: "Tensor", upd: "Tensor"):
+        """SCATTER-add along dim 0: self + rows of upd added at idx, in order."""
+        assert idx.dtype == "i32" and upd.shape[1:] == self.shape[1:] and upd.dtype == self.dtype
+        return Tensor("SCATTER", (self, idx, upd), self.shape, self.dtype)
+
+    # ---- composed ops --------------------------------------------------------------
+    def matmul(self, other: "Tensor", out_dtype=None):
+        """a @ b as SUM over k of MUL of two broadcast Views (limn, "Reading
+        the schedule"; Luminal IR blog, "Naive Matrix Multiplication").  Half
+        widths widen to float32 first, so the products are exact and the SUM
+        keeps a float32 total; the result rounds once into out_dtype."""
+        a, b = self, other
+        out_dtype = out_dtype or a.dtype
+        assert a.shape[-1] == b.shape[-2], (a.shape, b.shape)
+        M, K, N = a.shape[-2], a.shape[-1], b.shape[-1]
+        batch = broadcast_shapes(a.shape[:-2], b.shape[:-2])
+        af = a.cast("f32") if a.dtype != "f32" else a
+        bf = b.cast("f32") if b.dtype != "f32" else b
+        af = af.reshape(a.shape[:-2] + (M, 1, K))
+        af = _lead(af, len(batch) + 3).expand(batch + (M, N, K))
+        bf = bf.permute(tuple(range(b.ndim - 2)) + (b.ndim - 1, b.ndim - 2)).reshape(b.shape[:-2] + (1, N, K))
+        bf = _lead(bf, len(batch) + 3).expand(batch + (M, N, K))
+        c = af.mul(bf).sum(-1, keepdim=False)
+        return c.cast(out_dtype)
+
+    __matmul__ = matmul
+
+    def softmax(self, axis=-1):
+        """MAX-shifted softmax: the max is a constant of the gradient (softmax
+        does not depend on the shift)."""
+        m = self.max(axis).detach()
+        e = (self - m).exp()
+        return e / e.sum(axis)
+
+    def log_softmax(self, axis=-1):
+        m = self.max(axis).detach()
+        sh = self - m
+        return sh - sh.exp().sum(axis).log()
+
+    def rmsnorm(self, w: "Tensor", eps=1e-6):
+        """Tiki's RMSNorm target: (xf * rsqrt(mean(xf*xf) + eps) * f32(w)) in
+        x's dtype, with rsqrt = RECIP(SQRT)."""
+        xf = self.cast("f32")
+        inv = ((xf * xf).mean(-1) + eps).sqrt().recip()
+        return (xf * inv * w.cast("f32")).cast(self.dtype)
+
+    # ---- running -----------------------------------------------------------------------
+    def realize(self) -> torch.Tensor:
+        """Run the graph; returns the value as a torch tensor (a strided view
+        of the buffer that holds it)."""
+        return realize_all(self)[0]
+
+    def numpy(self):
+        return self.realize().float().cpu().numpy() if self.dtype == "bf16" else self.realize().cpu().numpy()
+
+    def item(self):
+        return float(self.realize().float().reshape(-1)[0].item())
+
+    def backward(self, grad: "Tensor | None" = None):
+        backward(self, grad)
+
+
+# ---------------------------------------------------------------- helpers -----
+
+def broadcast_shapes(*shapes):
+    n = max(len(s) for s in shapes)
+    out = []
+    for d in range(n):
+        dims = [s[d - (n - len(s))] for s in shapes if d - (n - len(s)) >= 0]
+        m = max(dims)
+        assert all(x in (1, m) for x in dims), shapes
+        out.append(m)
+    return tuple(out)
+
+
+def _lead(t: Tensor, nd: int) -> Tensor:
+    return t.reshape((1,) * (nd - t.ndim) + t.shape) if t.ndim < nd else t
+
+
+def broadcast(*ts):
+    shape = broadcast_shapes(*[t.shape for t in ts])
+    return tuple(_lead(t, len(shape)).expand(shape) for t in ts)
+
+
+def _as_torch(buf: torch.Tensor, v: View, dtype: str) -> torch.Tensor:
+    if v.mask is not None:
+        raise RuntimeError("a masked View has no torch equivalent; realize a contiguous copy")
+    return torch.as_strided(buf, v.shape, v.strides, v.offset)
+
+
+def _inverse(perm):
+    inv = [0] * len(perm)
+    for i, p in enumerate(perm):
+        inv[p] = i
+    return tuple(inv)
+
+
+# ------------------------------------------------------------ executor --------
+
+class Executor:
+    """Cuts the graph into library calls and runs them on the current stream.
+    ``log`` keeps every call it made (kind, details), for inspection."""
+
+    def __init__(self):
+        self.log = []
+        self.status = None
+        self.users = {}
+
+    def prepare(self, roots):
+        """Count, for every unrealized node reachable from roots, how many
+        nodes use it: a computed value with several users is a cut (it is
+        stored once instead of being recomputed in each consumer)."""
+        users, seen, stack = {}, set(), list(roots)
+        while stack:
+            t = stack.pop()
+            if id(t) in seen or t._real is not None:
+                continue
+            seen.add(id(t))
+            for x in t.src:
+                users[id(x)] = users.get(id(x), 0) + 1
+                stack.append(x)
+        self.users = users
+
+    def _shared_heavy(self, x):
+        if self.users.get(id(x), 0) < 2 or x.op == "CONST" or x._real is not None:
+            return False
+        n, red = 0, False
+        stack, seen = [x], set()
+        while stack and n < 4:
+            y = stack.pop()
+            if id(y) in seen or y._real is not None:
+                continue
+            seen.add(id(y))
+            if y.op in REDUCE:
+                red = True
+                continue
+            if y.op in ELEMENTWISE + ("MOVE",):
+                n += y.op != "MOVE"
+                stack.extend(y.src)
+        return red or n >= 4
+
+    def _status(self):
+        if self.status is None or self.status.device != torch.device("cuda", torch.cuda.current_device()):
+            self.status = torch.zeros((1,), dtype=torch.int32, device="cuda")
+        return self.status
+
+    def check_status(self):
+        if self.status is not None:
+            s = int(self.status.item())
+            if s:
+                raise A.PsgError(s, "device")
+
+    def _s(self):
+        return torch.cuda.current_stream().cuda_stream
+
+    @staticmethod
+    def _workspace(nbytes):
+        return torch.empty((max(1, int(nbytes)),), dtype=torch.uint8, device="cuda")
+
+    @staticmethod
+    def _new(shape, dtype):
+        return torch.empty(tuple(shape), dtype=torch_dtype(dtype), device="cuda")
+
+    def _pview(self, buf: torch.Tensor, v: View, dtype: str):
+        return A.make_view(dtype, v.shape, v.strides, v.offset,
+                           None if v.mask is None else list(v.mask), buf.numel())
+
+    # ---- realize ---------------------------------------------------------------
+    def realize(self, t: Tensor):
+        if t._real is not None:
+            return t._real
+        op = t.op
+        if op == "MOVE":
+            r = self._realize_move(t)
+        elif op in ELEMENTWISE:
+            r = self._realize_ew(t)
+        elif op in REDUCE:
+            r = self._realize_reduce(t)
+        elif op == "CONTIG":
+            r = self._copy_contig(*self.realize(t.src[0]), t.dtype)
+        elif op == "GATHER":
+            r = self._realize_gather(t)
+        elif op == "SCATTER":
+            r = self._realize_scatter(t)
+        else:
+            raise RuntimeError("cannot realize %s" % op)
+        t._real = r
+        return r
+
+    def _realize_move(self, t: Tensor):
+        """A movement costs nothing: realize its base, then compose the View
+        (a reshape no View can express copies the base first)."""
+        chain, base = [], t
+        while base.op == "MOVE":
+            chain.append(base.arg)
+            base = base.src[0]
+        buf, v = self.realize(base)
+        return self._apply_moves(buf, v, list(reversed(chain)), base.dtype)
+
+    def _apply_moves(self, buf, v, moves, dtype):
+        for kind, arg in moves:
+            if kind == "detach":
+                continue
+            nv = getattr(v, kind)(arg)
+            if nv is None:  # a reshape no View expresses: copy first
+                buf, v = self._copy_contig(buf, v, dtype)
+                nv = v.reshape(arg)
+            v = nv
+        return buf, v
+
+    def _copy_contig(self, buf, v, dtype):
+        out = self._new(v.shape, dtype)
+        if out.numel():
+            A.psg_permute(buf, self._pview(buf, v, dtype), list(range(len(v.shape))), out,
+                          self._pview(out, View(v.shape), dtype), stream=self._s())
+        self.log.append(("permute", v.shape))
+        return out, View(v.shape)
+
+    # ---- expression lowering (elementwise programs) ---------------------------
+    def _lower(self, root: Tensor, reds=None):
+        """(program nodes, inputs [(buf, View, dtype)]) for root's value.
+        Movements are pushed into elementwise operands; other nodes are
+        realized and become LOAD leaves.  reds maps id(REDUCE node) -> stage
+        index for reductions fused into the same call (read as RED)."""
+        prog, inputs, memo, in_memo = [], [], {}, {}
+        reds = reds or {}
+
+        def leaf(buf, v, dt):
+            key = (buf.data_ptr(), v.key(), dt)
+            if key not in in_memo:
+                if len(inputs) >= A.MAX_INPUTS:
+                    raise _TooBig()
+                in_memo[key] = len(inputs)
+                inputs.append((buf, v, dt))
+            prog.append(A.node("LOAD", in_memo[key], dtype=dt))
+            return len(prog) - 1
+
+        def walk(t: Tensor, moves: tuple):
+            key = (id(t), moves)
+            if key in memo:
+                return memo[key]
+            if len(prog) >= A.MAX_NODES - 2:
+                raise _TooBig()
+            op = t.op
+            if t._real is not None and op != "CONST":
+                # already in memory: a leaf, whatever computed it
+                buf, v = self._apply_moves(*t._real, [m for m in moves], t.dtype)
+                r = leaf(buf, v, t.dtype)
+                memo[key] = r
+                return r
+            # a shared value is a cut, except inside one fused reduction,
+            # whose stages and epilogue recompute it from registers
+            if t is not root and not reds and op in ELEMENTWISE and self._shared_heavy(t):
+                buf, v = self.realize(t)
+                buf, v = self._apply_moves(buf, v, list(moves), t.dtype)
+                r = leaf(buf, v, t.dtype)
+            elif op == "MOVE" and t.arg[0] != "pad":
+                r = walk(t.src[0], (t.arg,) + moves)
+            elif op == "CONST":
+                prog.append(A.node("CONST", dtype=t.dtype, cval=t.arg))
+                r = len(prog) - 1
+            elif op in EW_UNARY and not any(m[0] == "pad" for m in moves):
+                a = walk(t.src[0], moves)
+                prog.append(A.node(op, a, dtype=t.dtype))
+                r = len(prog) - 1
+            elif op in EW_BINARY and not any(m[0] == "pad" for m in moves):
+                a = walk(t.src[0], moves)
+                b = walk(t.src[1], moves)
+                prog.append(A.node(op, a, b, dtype=t.dtype))
+                r = len(prog) - 1
+            elif op == "WHERE" and not any(m[0] == "pad" for m in moves):
+                c = walk(t.src[0], moves)
+                x = walk(t.src[1], moves)
+                y = walk(t.src[2], moves)
+                prog.append(A.node("WHERE", c, x, y, dtype=t.dtype))
+                r = len(prog) - 1
+            elif op in REDUCE and id(t) in reds:
+                prog.append(A.node("RED", reds[id(t)], dtype=t.dtype))
+                r = len(prog) - 1
+            else:
+                buf, v = self.realize(t)
+                buf, v = self._apply_moves(buf, v, [m for m in moves], t.dtype)
+                r = leaf(buf, v, t.dtype)
+            memo[key] = r
+            return r
+
+        walk(root, ())
+        return prog, inputs
+
+    def _realize_ew(self, t: Tensor):
+        # a CAST of a contraction (through movements) rounds inside the
+        # contraction's epilogue
+        base, moves = t, []
+        while base.op == "MOVE" and base.arg[0] != "pad":
+            moves.append(base.arg)
+            base = base.src[0]
+        if base.op == "CAST" and base.dtype in ("bf16", "f32"):
+            x, inner = base.src[0], []
+            while x.op == "MOVE" and x.arg[0] != "pad":
+                inner.append(x.arg)
+                x = x.src[0]
+            if x.op == "SUM" and x._real is None and self._contract_pattern(x):
+                r = self._try_contract(x, (), base.dtype, x.shape)
+                if r is not None:
+                    return self._apply_moves(*r, list(reversed(inner)) + list(reversed(moves)), base.dtype)
+        fused = self._try_fused_reduce(t)
+        if fused is not None:
+            return fused
+        while True:
+            try:
+                prog, inputs = self._lower(t)
+                break
+            except _TooBig:
+                self._split(t)
+        out = self._new(t.shape, t.dtype)
+        if out.numel():
+            A.psg_elementwise(prog, [b for b, _, _ in inputs], [self._pview(b, v, d) for b, v, d in inputs],
+                              out, self._pview(out, View(t.shape), t.dtype), stream=self._s())
+        self.log.append(("elementwise", t.shape, len(prog)))
+        return out, View(t.shape)
+
+    def _split(self, t: Tensor):
+        """A program too large for one call: realize the operand subtree with
+        the most nodes on its own first."""
+        best, size = None, -1
+        stack = [t]
+        seen = set()
+        while stack:
+            x = stack.pop()
+            if id(x) in seen or x._real is not None:
+                continue
+            seen.add(id(x))
+            # only the region this program would cover: elementwise and
+            # movement nodes (anything else is already a leaf of it)
+            if x.op not in ELEMENTWISE and x.op != "MOVE" and x is not t:
+                continue
+            if x is not t and x.op in ELEMENTWISE and x.op != "CONST":
+                n = _count(x)
+                if n > 1 and n > size:
+                    best, size = x, n
+            stack.extend(x.src)
+        if best is None:
+            raise RuntimeError("program cannot be split")
+        self.realize(best)
+
+    # ---- reductions ---------------------------------------------------------------
+    def _collect_reds(self, root: Tensor):
+        """Unrealized reductions reachable from root through elementwise and
+        movement nodes, each with the movements between it and root."""
+        found, seen = {}, set()
+
+        def walk(x, moves):
+            key = (id(x), moves)
+            if x._real is not None or key in seen:
+                return
+            seen.add(key)
+            if x.op == "MOVE":
+                walk(x.src[0], (x.arg,) + moves)
+            elif x.op in ELEMENTWISE:
+                for s in x.src:
+                    walk(s, moves)
+            elif x.op in REDUCE:
+                found.setdefault(id(x), (x, moves))
+        walk(root, ())
+        return found
+
+    def _stage_order(self, reds, row_shape):
+        """Order reductions (and the ones their prologues need) into stages;
+        None if any is not a row reduction over row_shape."""
+        order, state = [], {}
+
+        def visit(r):
+            if state.get(id(r)) == 2:
+                return True
+            if state.get(id(r)) == 1:
+                return False
+            state[id(r)] = 1
+            if r.src[0].shape != row_shape:
+                return False
+            inner = self._collect_reds(r.src[0])
+            for _, (r2, mv) in inner.items():
+                if r2.src[0].shape != row_shape or not _is_row_expand(mv, r2.shape, row_shape):
+                    return False
+                if not visit(r2):
+                    return False
+            state[id(r)] = 2
+            order.append(r)
+            return True
+
+        for r in reds:
+            if not visit(r):
+                return None
+        return order
+
+    def _try_fused_reduce(self, t: Tensor):
+        found = self._collect_reds(t)
+        if not found:
+            return None
+        rows = {r.src[0].shape for r, _ in found.values()}
+        if len(rows) != 1:
+            return None
+        row_shape = rows.pop()
+        per_elem = t.shape == row_shape
+        per_row = t.shape == row_shape[:-1] + (1,)
+        if not (per_elem or per_row):
+            return None
+        for r, mv in found.values():
+            if per_elem and not _is_row_expand(mv, r.shape, row_shape):
+                return None
+            if per_row and any(m[0] != "detach" for m in mv):
+                return None
+        order = self._stage_order([r for r, _ in found.values()], row_shape)
+        if order is None or len(order) > 4:
+            return None
+        if any(self._contract_pattern(r) for r in order):
+            return None
+        try:
+            return self._run_reduce(order, t, per_row)
+        except (_NotFusable, _TooBig):
+            return None
+
+    def _run_reduce(self, order, epi_root, per_row):
+        reds = {}
+        stages, inputs, in_index = [], [], {}
+
+        def merge(prog, ins):
+            # renumber this program's LOADs into the shared input list
+            out = []
+            for nd in prog:
+                if nd.op == A.OPS["LOAD"]:
+                    b, v, d = ins[nd.a]
+                    key = (b.data_ptr(), v.key(), d)
+                    if key not in in_index:
+                        if len(inputs) >= A.MAX_INPUTS:
+                            raise _TooBig()
+                        in_index[key] = len(inputs)
+                        inputs.append((b, v, d))
+                    nd = A.node("LOAD", in_index[key], dtype=d)
+                out.append(nd)
+            return out
+
+        for s, r in enumerate(order):
+            prog, ins = self._lower(r.src[0], reds)
+            stages.append((A.RED_SUM if r.op == "SUM" else A.RED_MAX, merge(prog, ins)))
+            reds[id(r)] = s
+        epi = None
+        if epi_root is not None and not (per_row and epi_root is order[-1]):
+            prog, ins = self._lower(epi_root, reds)
+            if per_row and ins:
+                raise _NotFusable()
+            epi = merge(prog, ins)
+        out_shape = epi_root.shape if epi_root is not None else order[-1].shape
+        out_dt = epi_root.dtype if epi_root is not None else order[-1].dtype
+        out = self._new(out_shape, out_dt)
+        if out.numel():
+            A.psg_reduce_rows(stages, epi, [b for b, _, _ in inputs],
+                              [self._pview(b, v, d) for b, v, d in inputs], out,
+                              self._pview(out, View(out_shape), out_dt), stream=self._s())
+        self.log.append(("reduce_rows", order[0].src[0].shape, len(stages), "per_row" if per_row else "per_elem"))
+        return out, View(out_shape)
+
+    def _realize_reduce(self, t: Tensor):
+        r = self._try_contract(t, (), t.dtype, t.shape)
+        if r is not None:
+            return r
+        order = self._stage_order([t], t.src[0].shape)
+        if order is None or len(order) > 4:
+            # realize the inner reductions first, then this one alone
+            for _, (r2, _) in self._collect_reds(t.src[0]).items():
+                self.realize(r2)
+            order = [t]
+        while True:
+            try:
+                return self._run_reduce(order, t, True)
+            except _TooBig:
+                # a prologue past the call's limits: store its largest
+                # subexpression first (or, failing that, the whole prologue)
+                for r in order:
+                    try:
+                        self._split(r.src[0])
+                        break
+                    except RuntimeError:
+                        continue
+                else:
+                    for r in order:
+                        self.realize(r.src[0])
+                    order = [t]
+
+    # ---- contraction ----------------------------------------------------------------
+    def _contract_pattern(self, r: Tensor):
+        """SUM over the last axis of MUL(x, y) with x, y movements of
+        (widened) non-elementwise values."""
+        if r.op != "SUM":
+            return None
+        m = r.src[0]
+        moves = ()
+        while m.op == "MOVE" and m.arg[0] != "pad":
+            moves = (m.arg,) + moves
+            m = m.src[0]
+        if m.op != "MUL":
+            return None
+        if not any(mv[0] == "expand" for x in m.src for mv in _moves_to_base(x)):
+            return None
+        ops = []
+        for x in m.src:
+            mv = moves
+            widen = None
+            while True:
+                if x.op == "MOVE" and x.arg[0] != "pad":
+                    mv = (x.arg,) + mv
+                    x = x.src[0]
+                elif x.op == "CAST" and x.dtype == "f32" and x.src[0].dtype in ("bf16", "f16"):
+                    widen = x.src[0].dtype
+                    x = x.src[0]
+                else:
+                    break
+            if x.op in ELEMENTWISE and x.op != "CAST":
+                # a computed operand: realize it as its own value first
+                pass
+            ops.append((x, mv, widen))
+        return ops
+
+    def _try_contract(self, r: Tensor, _moves, out_dtype, out_shape):
+        if r.op != "SUM" or r._real is not None:
+            return None
+        pat = self._contract_pattern(r)
+        if pat is None:
+            return None
+        (x, mx, wx), (y, my, wy) = pat
+        dx = wx or x.dtype
+        dy = wy or y.dtype
+        if dx != dy or dx not in ("bf16", "f32"):
+            return None
+        S = r.src[0].shape
+        bx, vx = self._apply_moves(*self.realize(x), list(mx), x.dtype)
+        by, vy = self._apply_moves(*self.realize(y), list(my), y.dtype)
+        if vx.mask is not None or vy.mask is not None:
+            return None
+        L = len(S) - 1
+        Mx, Nx, Bx = [], [], []
+        for a in range(L):
+            if S[a] == 1:
+                continue
+            sx, sy = vx.strides[a], vy.strides[a]
+            if sy == 0 and sx != 0:
+                Mx.append(a)
+            elif sx == 0 and sy != 0:
+                Nx.append(a)
+            elif sx != 0 and sy != 0:
+                Bx.append(a)
+            else:
+                return None
+        if not Mx and not Nx:
+            # no broadcast axis: a plain row reduction with a MUL prologue
+            return None
+        out = self._new(out_shape, out_dtype)
+        # output strides over the leading axes of S (the result shape is S[:-1] + (1,))
+        ostr = View.row_major(S[:-1])
+
+        def merged(axes, views):
+            """One (size, strides per view) for a group of axes, or None."""
+            if not axes:
+                return 1, [0] * len(views)
+            size = S[axes[0]]
+            st = [v[axes[0]] for v in views]
+            for a in axes[1:]:
+                for i, v in enumerate(views):
+                    if st[i] != v[a] * S[a]:
+                        return None
+                size *= S[a]
+                st = [v[a] for v in views]
+            return size, st
+
+        gm = merged(Mx, [vx.strides, ostr])
+        gn = merged(Nx, [vy.strides, ostr])
+        if gm is None or gn is None:
+            return None
+        # batch axes: kept separately when they do not merge (the ABI takes up to 3)
+        gb = merged(Bx, [vx.strides, vy.strides, ostr])
+        if Bx and gb is None:
+            # batch dims that do not merge (e.g. heads split out of a fused
+            # projection): store each operand compactly, so they do
+            bx, vx = self._compact(bx, vx, dx, x.dtype)
+            by, vy = self._compact(by, vy, dy, y.dtype)
+            gm = merged(Mx, [vx.strides, ostr])
+            gn = merged(Nx, [vy.strides, ostr])
+            gb = merged(Bx, [vx.strides, vy.strides, ostr])
+            if gm is None or gn is None or gb is None:
+                return None
+        batch = [(gb[0], gb[1][0], gb[1][1], gb[1][2])] if Bx else []
+        K = S[-1]
+        shape = [b[0] for b in batch] + [gm[0], gn[0], K]
+        sa = [b[1] for b in batch] + [gm[1][0], 0, vx.strides[-1]]
+        sb = [b[2] for b in batch] + [0, gn[1][0], vy.strides[-1]]
+        sc = [b[3] for b in batch] + [gm[1][1], gn[1][1]]
+        Av = A.make_view(dx, shape, sa, vx.offset, None, bx.numel())
+        Bv = A.make_view(dy, shape, sb, vy.offset, None, by.numel())
+        Cv = A.make_view(out_dtype, shape[:-1], sc, 0, None, out.numel())
+        if out.numel():
+            A.psg_contract(bx, Av, by, Bv, out, Cv, self._status(), stream=self._s())
+        self.log.append(("contract", tuple(shape), dx, out_dtype))
+        return out, View(out_shape)
+
+    def _compact(self, buf, v, dt, src_dt):
+        """Copy the cells a broadcast View reads into a row-major buffer and
+        return the same broadcast View over the copy."""
+        zero = [a for a, st in enumerate(v.strides) if st == 0 and v.shape[a] > 1]
+        small = v.shrink([(0, 1) if a in zero else (0, s) for a, s in enumerate(v.shape)])
+        b2, v2 = self._copy_contig(buf, small, src_dt)
+        return b2, v2.expand(v.shape)
+
+    # ---- indexed --------------------------------------------------------------------
+    def _realize_gather(self, t: Tensor):
+        src, idx = t.src
+        bs, vs = self.realize(src)
+        bi, vi = self.realize(idx)
+        if not vi.contiguous():
+            bi, vi = self._copy_contig(bi, vi, "i32")
+        out = self._new(t.shape, t.dtype)
+        n = t.shape[0]
+        A.psg_gather(bs, self._pview(bs, vs, src.dtype), bi, n, out, self._pview(out, View(t.shape), t.dtype),
+                     self._status(), stream=self._s())
+        self.log.append(("gather", t.shape))
+        return out, View(t.shape)
+
+    def _realize_scatter(self, t: Tensor):
+        dst, idx, upd = t.src
+        out, vo = self._copy_contig(*self.realize(dst), dst.dtype)
+        bi, vi = self.realize(idx)
+        if not vi.contiguous():
+            bi, vi = self._copy_contig(bi, vi, "i32")
+        bu, vu = self.realize(upd)
+        n = idx.shape[0]
+        ws = self._workspace(A.psg_scatter_workspace(n))
+        A.psg_scatter_add(out, self._pview(out, vo, t.dtype), bi, n, bu, self._pview(bu, vu, upd.dtype), ws,
+                          ws.numel(), self._status(), stream=self._s())
+        self.log.append(("scatter_add", t.shape, n))
+        return out, vo
+
+
+class _TooBig(Exception):
+    pass
+
+
+class _NotFusable(Exception):
+    pass
+
+
+def _moves_to_base(x):
+    """The movements between x and the first non-movement, non-widening node."""
+    out = []
+    while True:
+        if x.op == "MOVE" and x.arg[0] != "pad":
+            out.append(x.arg)
+            x = x.src[0]
+        elif x.op == "CAST" and x.dtype == "f32" and x.src[0].dtype in ("bf16", "f16"):
+            x = x.src[0]
+        else:
+            return out
+
+
+def _count(t, seen=None):
+    seen = seen if seen is not None else set()
+    if id(t) in seen or t._real is not None or t.op not in ELEMENTWISE + ("MOVE",):
+        return 0
+    seen.add(id(t))
+    return 1 + sum(_count(s, seen) for s in t.src)
+
+
+def _is_row_expand(moves, red_shape, row_shape):
+    """The movements take a [.., 1] row value to [.., N] by expanding the last axis."""
+    mv = [m for m in moves if m[0] != "detach"]
+    if not mv:
+        return red_shape == row_shape
+    v = View(red_shape, [0] * len(red_shape))
+    shape = red_shape
+    for kind, arg in mv:
+        if kind == "expand":
+            shape = tuple(arg)
+        elif kind == "reshape":
+            shape = tuple(arg)
+        else:
+            return False
+    return shape == row_shape and all(m[0] in ("expand", "reshape") for m in mv) and \
+        prod(red_shape) == prod(row_shape[:-1])
+
+
+_EXEC = None
+
+
+def _executor() -> Executor:
+    global _EXEC
+    if _EXEC is None:
+        _EXEC = Executor()
+    return _EXEC
+
+
+def realize_all(*ts):
+    """Realize several values with one schedule (shared subexpressions are
+    computed once) and return them as torch tensors."""
+    ex = _executor()
+    ex.prepare(ts)
+    out = []
+    for t in ts:
+        buf, v = ex.realize(t)
+        if v.mask is not None:
+            buf, v = ex._copy_contig(buf, v, t.dtype)
+        out.append(_as_torch(buf, v, t.dtype))
+    return out
+
+
+# ------------------------------------------------------------ autograd -------
+
+def _toposort(root):
+    order, seen = [], set()
+    stack = [(root, False)]
+    while stack:
+        t, done = stack.pop()
+        if done:
+            order.append(t)
+            continue
+        if id(t) in seen:
+            continue
+        seen.add(id(t))
+        stack.append((t, True))
+        for s in t.src:
+            if s.requires_grad and id(s) not in seen:
+                stack.append((s, False))
+    return order
+
+
+def _sum_to(g: Tensor, shape) -> Tensor:
+    """Undo a broadcast: SUM g over the axes where shape has 1."""
+    if g.shape == tuple(shape):
+        return g
+    nd = len(shape)
+    while g.ndim > nd:
+        g = g.sum(0, keepdim=False)
+    for a in range(nd):
+        if shape[a] == 1 and g.shape[a] != 1:
+            g = g.sum(a, keepdim=True)
+    return g
+
+
+def _vjp(t: Tensor, g: Tensor):
+    op, s = t.op, t.src
+    if op == "ADD":
+        return [(s[0], g), (s[1], g)]
+    if op == "MUL":
+        return [(s[0], g * s[1]), (s[1], g * s[0])]
+    if op == "NEG":
+        return [(s[0], -g)]
+    if op == "EXP":
+        return [(s[0], g * t)]
+    if op == "LOG":
+        return [(s[0], g * s[0].recip())]
+    if op == "SQRT":
+        return [(s[0], g * 0.5 * t.recip())]
+    if op == "RECIP":
+        return [(s[0], -g * (t * t))]
+    if op == "CAST":
+        return [(s[0], g.cast(s[0].dtype))] if s[0].dtype in FLOATS else []
+    if op == "WHERE":
+        z = Tensor.const(0.0, (), g.dtype)
+        return [(s[1], s[0].where(g, z)), (s[2], s[0].where(z, g))]
+    if op == "SUM":
+        return [(s[0], g.expand(s[0].shape))]
+    if op == "MAX":
+        # gradient to the cells equal to the max
+        m = t.expand(s[0].shape)
+        eq = (s[0].cmplt(m).cast("f32") + m.cmplt(s[0]).cast("f32")).cmplt(Tensor.const(0.5, (), "f32"))
+        return [(s[0], eq.where(g.expand(s[0].shape), Tensor.const(0.0, (), g.dtype)))]
+    if op == "MOVE":
+        kind, arg = t.arg
+        src = s[0]
+        if kind == "detach":
+            return []
+        if kind == "reshape":
+            return [(src, g.reshape(src.shape))]
+        if kind == "permute":
+            return [(src, g.permute(_inverse(arg)))]
+        if kind == "expand":
+            return [(src, _sum_to(g, src.shape))]
+        if kind == "shrink":
+            return [(src, g.pad([(a, n - b) for (a, b), n in zip(arg, src.shape)]))]
+        if kind == "pad":
+            return [(src, g.shrink([(a, a + n) for (a, _), n in zip(arg, src.shape)]))]
+    if op == "CONTIG":
+        return [(s[0], g)]
+    if op == "GATHER":
+        return [(s[0], Tensor.zeros(s[0].shape, s[0].dtype).scatter_add(s[1], g))]
+    if op == "SCATTER":
+        return [(s[0], g), (s[2], g.gather(s[1]))]
+    return []
+
+
+def backward(root: Tensor, grad: Tensor | None = None):
+    """Reverse-mode autograd over the lazy graph: every leaf that requires a
+    gradient gets ``.grad``, itself a lazy graph of primitives (limn,
+    "Architecture": the gradients are lazy graphs like everything else)."""
+    if grad is None:
+        assert root.numel() == 1, "backward of a non-scalar needs a gradient"
+        grad = Tensor.const(1.0, root.shape, root.dtype)
+    grads = {id(root): grad}
+    for t in reversed(_toposort(root)):
+        g = grads.pop(id(t), None)
+        if g is None:
+            continue
+        if not t.src:
+            t.grad = g if t.grad is None else t.grad + g
+            continue
+        for src, gs in _vjp(t, g):
+            if not src.requires_grad:
+                continue
+            if gs.shape != src.shape:
+                gs = _sum_to(gs, src.shape)
+            prev = grads.get(id(src))
+            grads[id(src)] = gs if prev is None else prev + gs

@@ -1,0 +1,108 @@
+"""The two graph workloads of the hot path, written only with the lazy
+Tensor API (so every kernel they launch comes from the scheduler):
+
+* ``tiny_graph``: limn's README example at a small size, SUM(relu(A @ B)^2),
+  with the matmul as broadcast MUL + SUM over k;
+* ``gpt_block_loss``: a one-layer byte-level GPT block, forward and the
+  graph its backward builds: embedding GATHER plus a learned position table,
+  pre-norm RMSNorm, causal softmax attention in the composed form (the full
+  T x T scores), a relu MLP, a final RMSNorm, an LM head and the mean
+  next-token cross-entropy.  Weights and activations are bfloat16 at node
+  boundaries; softmax, the logits and the loss are float32.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from .graph import Tensor, backward, realize_all
+
+GPT_WEIGHTS = ("E", "P", "Wqkv", "Wo", "W1", "W2", "Wlm", "g1", "g2", "gf")
+
+
+def tiny_graph(A: Tensor, B: Tensor) -> Tensor:
+    """SUM(relu(A @ B) ** 2) as a scalar [1]."""
+    c = A.matmul(B)
+    return c.relu().square().reshape(1, -1).sum(-1, keepdim=False)
+
+
+def gpt_targets(tok: torch.Tensor, V: int):
+    """Host-side index tables of the loss (data, not arithmetic of the
+    method): row indices r = b*T + t of the positions with a next token
+    (t < T-1) and the flat indices r*V + tok[b, t+1] of their target logits.
+    The last position of each sequence has no target and is dropped."""
+    Bn, T = tok.shape
+    t = np.arange(T - 1)
+    rows = (np.arange(Bn)[:, None] * T + t[None, :]).reshape(-1)
+    tgt = tok[:, 1:].cpu().numpy().reshape(-1)
+    pick = rows * V + tgt
+    return torch.from_numpy(pick.astype(np.int32))
+
+
+def causal_mask(T: int) -> torch.Tensor:
+    """[T, T] float32: 1 where key j <= query i (data for WHERE)."""
+    return torch.tril(torch.ones((T, T), dtype=torch.float32))
+
+
+def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,
+                   pick: torch.Tensor | None = None, mask: torch.Tensor | None = None,
+                   taps: dict | None = None):
+    """Mean next-token cross-entropy of the block on tokens [B, T] (int32,
+    on the device).  w maps GPT_WEIGHTS to Tensors.  Returns the loss node
+    (shape [1], float32).  If taps is a dict, the MLP pre-activation is put
+    there as taps["mlp_pre"] (for inspection)."""
+    Bn, T = tok.shape
+    V, D = w["E"].shape
+    hd = D // H
+    BT = Bn * T
+    dev = tok.device
+    if pick is None:
+        pick = gpt_targets(tok, V).to(dev)
+    if mask is None:
+        mask = causal_mask(T).to(dev)
+    idx = Tensor.from_torch(tok.reshape(-1))
+    h0 = (w["E"].gather(idx).reshape(Bn, T, D) + w["P"].reshape(1, T, D)).reshape(BT, D)
+
+    # attention (pre-norm), composed: scores, causal WHERE, softmax, weighted sum
+    n1 = h0.rmsnorm(w["g1"], eps)
+    qkv = n1.matmul(w["Wqkv"]).reshape(Bn, T, 3, H, hd)
+
+    def head(i):
+        return qkv.shrink(((0, Bn), (0, T), (i, i + 1), (0, H), (0, hd))).reshape(Bn, T, H, hd) \
+                  .permute(0, 2, 1, 3)
+
+    q, k, v = head(0), head(1), head(2)
+    s = q.matmul(k.transpose(-1, -2)).cast("f32") * (1.0 / np.sqrt(hd))
+    s = Tensor.from_torch(mask).where(s, float("-inf"))
+    p = s.softmax(-1).cast("bf16")
+    o = p.matmul(v).permute(0, 2, 1, 3).reshape(BT, D)
+    h1 = h0 + o.matmul(w["Wo"])
+
+    # MLP (pre-norm)
+    n2 = h1.rmsnorm(w["g2"], eps)
+    u = n2.matmul(w["W1"])
+    if taps is not None:
+        taps["mlp_pre"] = u
+    h2 = h1 + u.relu().matmul(w["W2"])
+
+    # head and loss
+    logits = h2.rmsnorm(w["gf"], eps).matmul(w["Wlm"]).cast("f32")
+    lsm = logits.log_softmax(-1)
+    picked = lsm.reshape(BT * V, 1).gather(Tensor.from_torch(pick))
+    n = pick.shape[0]
+    return picked.reshape(1, n).sum(-1, keepdim=False) * (-1.0 / n)
+
+
+def gpt_step(tok: torch.Tensor, weights: dict, H: int, pick=None, mask=None, taps=None):
+    """One forward + backward pass: returns (loss, {name: grad}) as torch
+    tensors.  weights maps GPT_WEIGHTS to device bf16 torch tensors.  With a
+    taps dict, the tapped intermediates come back realized in it too."""
+    w = {k: Tensor.from_torch(weights[k], requires_grad=True) for k in GPT_WEIGHTS}
+    tp = {} if taps is not None else None
+    loss = gpt_block_loss(tok, w, H, pick=pick, mask=mask, taps=tp)
+    backward(loss)
+    names = list(tp) if tp else []
+    outs = realize_all(loss, *[w[k].grad for k in GPT_WEIGHTS], *[tp[k] for k in names])
+    if taps is not None:
+        taps.update(zip(names, outs[1 + len(GPT_WEIGHTS):]))
+    return outs[0], dict(zip(GPT_WEIGHTS, outs[1:1 + len(GPT_WEIGHTS)]))
