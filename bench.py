@@ -9,9 +9,15 @@ The metric is fused-op HBM throughput: algorithmic bytes (every operand byte
 read once and every result byte written once) per second.  L2 is flushed
 (a write of twice the L2 size) before every timed step, outside the events.
 
-Extra rows of the same JSON line time the other hot-path calls on their own
-workloads (row reductions, the MUL+SUM contraction, gather/scatter) when their
-kernels are present, each against its own roofline.
+The "rows" object of the same JSON line times the other hot-path calls on
+their own workloads, each against its own ceiling: softmax over x[4096,1024]
+f32 and RMSNorm over x[8192,4096] bf16 (HBM, L2 flushed), the MUL+SUM
+contraction in bf16 8192^3 (tensor pipe, measured cuBLAS peak) and f32 4096^3
+(FFMA, peak derived from unit counts and clock), the token gather and
+scatter-add of the GPT block, the tiny MUL+SUM graph (eager and CUDA Graph
+replay) and one GPT block forward + backward through the graph layer.
+
+--profile-case NAME runs one workload a few times and exits, for a profiler.
 
 --impl reference runs the plain CPU oracle (the reference implementation of
 the method on these pages) on a bounded sample of the same workload.
@@ -232,6 +238,250 @@ def e2e_steps(step, K, W):
     return ms, h2d, d2h
 
 
+# ------------------------------------------------------ the other rows ----
+
+FP32_LANES_PER_SM = 128   # FFMA lanes per SM (Blackwell SM: 4 partitions x 32)
+
+
+def fp32_alu_peak():
+    """FFMA peak from unit counts and the maximum SM clock: SMs x 128 lanes x
+    2 flop x clock (no measured FFMA figure is on file)."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    mhz = 2070.0
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        mhz = float(json.load(open(p)).get("sm_max_mhz", mhz))
+    return props.multi_processor_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def time_events(fn, iters, warm=3, flush=None):
+    """Median ms of fn() over iters runs, CUDA events on the current stream,
+    each run preceded (outside its events) by an L2 flush when given."""
+    s = torch.cuda.current_stream()
+    for _ in range(warm):
+        if flush is not None:
+            flush.zero_()
+        fn(s.cuda_stream)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn(s.cuda_stream)
+        e1.record(s)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+
+def _hbm_row(name, nbytes, ms, P, extra=None):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    r = {"ms": round(ms, 5), "bytes": nbytes, "achieved": round(gbs, 2), "unit": "GB/s",
+         "bound": "hbm", "peak": P["hbm"], "frac": round(gbs / P["hbm"], 4)}
+    r.update(extra or {})
+    return r
+
+
+class Rows:
+    """One workload per remaining hot-path row, each driven through the C ABI
+    on its own inputs and timed against its own ceiling."""
+
+    def __init__(self, A, P, iters=20):
+        self.A, self.P, self.iters = A, P, iters
+        self.flush = l2_flush_buffer()
+        self.launches = 0
+
+    # C3a: softmax over rows of x[4096,1024] f32
+    def softmax(self):
+        from primitive_sm_graph_gb300 import programs as PR
+        A = self.A
+        x = SI.softmax_input(0).cuda()
+        y = torch.empty_like(x)
+        stages, epi = PR.softmax_rows("f32")
+        vx, vy = A.view_of(x), A.view_of(y)
+        fn = lambda st: A.psg_reduce_rows(stages, epi, [x], [vx], y, vy, stream=st)
+        return fn, lambda ms: _hbm_row("softmax", 2 * x.numel() * 4, ms, self.P,
+                                       {"workload": "softmax rows x[4096,1024] f32"})
+
+    # C3b: RMSNorm x[8192,4096] bf16, w[4096] bf16, eps 1e-6, f32 accumulate
+    def rmsnorm(self):
+        from primitive_sm_graph_gb300 import programs as PR
+        A = self.A
+        xh, wh = SI.rmsnorm_input(0)
+        x, w = xh.cuda(), wh.cuda()
+        y = torch.empty_like(x)
+        R, N = x.shape
+        stages, epi = PR.rmsnorm(N, 1e-6, "bf16")
+        vx, vw, vy = A.view_of(x), A.view_of(w, shape=(R, N), strides=(0, 1)), A.view_of(y)
+        fn = lambda st: A.psg_reduce_rows(stages, epi, [x, w], [vx, vw], y, vy, stream=st)
+        nbytes = 2 * x.numel() * 2 + N * 2
+        return fn, lambda ms: _hbm_row("rmsnorm", nbytes, ms, self.P,
+                                       {"workload": "RMSNorm x[8192,4096] bf16, w[4096], eps 1e-6"})
+
+    def _contract(self, a, b, out_dtype):
+        A = self.A
+        M, K = a.shape
+        N = b.shape[1]
+        va = A.view_of(a, shape=(M, N, K), strides=(K, 0, 1))
+        vb = A.view_of(b, shape=(M, N, K), strides=(0, 1, N))
+        c = torch.empty((M, N), dtype=out_dtype, device="cuda")
+        vc = A.view_of(c)
+        st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+        fn = lambda s: A.psg_contract(a, va, b, vb, c, vc, st, stream=s)
+        return fn, 2.0 * M * N * K
+
+    # C4a: bf16 A,B [8192,8192] -> bf16, f32 accumulate
+    def gemm_bf16(self):
+        a, b = SI.contraction_bf16(0)
+        fn, flops = self._contract(a.cuda(), b.cuda(), torch.bfloat16)
+        pk = self.P["bf16"]
+
+        def fin(ms):
+            tf = flops / (ms * 1e-3) / 1e12
+            return {"ms": round(ms, 5), "flops": flops, "achieved": round(tf, 2), "unit": "TFLOP/s",
+                    "bound": "tensor", "peak": pk, "peak_source": self.P["source"] + " cuBLAS bf16 burst",
+                    "frac": round(tf / pk, 4),
+                    "workload": "bf16 A[8192,8192] @ B[8192,8192] as MUL+SUM, f32 accumulate, bf16 out"}
+        return fn, fin
+
+    # C4b: f32 A,B [4096,4096] -> f32 (FFMA)
+    def gemm_f32(self):
+        a, b = SI.contraction_f32(0)
+        fn, flops = self._contract(a.cuda(), b.cuda(), torch.float32)
+        pk = fp32_alu_peak()
+
+        def fin(ms):
+            tf = flops / (ms * 1e-3) / 1e12
+            return {"ms": round(ms, 5), "flops": flops, "achieved": round(tf, 2), "unit": "TFLOP/s",
+                    "bound": "alu", "peak": round(pk, 2),
+                    "peak_source": "derived: SMs x 128 FFMA lanes x 2 x max SM clock",
+                    "frac": round(tf / pk, 4),
+                    "workload": "f32 A[4096,4096] @ B[4096,4096] as MUL+SUM (FFMA)"}
+        return fn, fin
+
+    # C5 shapes: token embedding gather and its scatter-add backward
+    def gather(self):
+        A = self.A
+        tok, w = SI.gpt_block(0, **SI.GPT_SHAPES)
+        E = w["E"].cuda()
+        idx = tok.reshape(-1).cuda()
+        n = idx.numel()
+        out = torch.empty((n, E.shape[1]), dtype=E.dtype, device="cuda")
+        st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+        vE, vo = A.view_of(E), A.view_of(out)
+        fn = lambda s: A.psg_gather(E, vE, idx, n, out, vo, st, stream=s)
+        nbytes = out.numel() * 2 * 2 + n * 4   # rows read + written, indices
+        return fn, lambda ms: _hbm_row("gather", nbytes, ms, self.P,
+                                       {"workload": "E[256,512] bf16 gathered by 8192 int32 tokens"})
+
+    def scatter(self):
+        A = self.A
+        tok, _ = SI.gpt_block(0, **SI.GPT_SHAPES)
+        idx = tok.reshape(-1).cuda()
+        n = idx.numel()
+        g = SI.gen(1)
+        upd = SI.normal((n, 512), 0.0, 1.0, g, torch.bfloat16).cuda()
+        dst = torch.zeros((256, 512), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty((max(1, A.psg_scatter_workspace(n)),), dtype=torch.uint8, device="cuda")
+        st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+        vd, vu = A.view_of(dst), A.view_of(upd)
+        fn = lambda s: A.psg_scatter_add(dst, vd, idx, n, upd, vu, ws, ws.numel(), st, stream=s)
+        nbytes = upd.numel() * 2 + n * 4 + 2 * dst.numel() * 2
+        return fn, lambda ms: _hbm_row("scatter", nbytes, ms, self.P,
+                                       {"workload": "scatter-add of [8192,512] bf16 rows into [256,512]"})
+
+    def run_kernel_rows(self, names):
+        out = {}
+        for nm in names:
+            fn, fin = getattr(self, nm)()
+            ms = time_events(fn, self.iters, flush=self.flush)
+            self.launches += self.iters
+            out[nm] = fin(ms)
+            del fn
+            torch.cuda.empty_cache()
+        return out
+
+    # C1: the tiny graph, eager realize and CUDA Graph replay
+    def tiny_graph(self):
+        from primitive_sm_graph_gb300 import graph as G
+        from primitive_sm_graph_gb300.workloads import tiny_graph
+        a, b = SI.tiny_graph(0)
+        da, db = a.cuda(), b.cuda()
+
+        def once():
+            return tiny_graph(G.Tensor.from_torch(da), G.Tensor.from_torch(db)).realize()
+        for _ in range(5):
+            once()
+        torch.cuda.synchronize()
+        ex = G._executor()
+        ex.log.clear()
+        once()
+        kernels = len(ex.log)
+        n = 200
+        t0 = time.perf_counter()
+        for _ in range(n):
+            once()
+        torch.cuda.synchronize()
+        eager_us = (time.perf_counter() - t0) / n * 1e6
+        r = {"eager_us_per_realize": round(eager_us, 2), "kernels": kernels,
+             "workload": "SUM(relu(A[64,32] @ B[32,48])^2) f32"}
+        try:
+            gr = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                once()
+            torch.cuda.current_stream().wait_stream(s)
+            with torch.cuda.graph(gr):
+                once()
+            gr.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            r["graph_replay_us"] = round(e0.elapsed_time(e1) / n * 1e3, 3)
+        except Exception as e:  # capture is optional: report why it failed
+            r["graph_replay_us"] = None
+            r["graph_capture_error"] = str(e)[:200]
+        return r
+
+    # C5: one forward + backward of the GPT block through the graph layer
+    def gpt(self, steps=3):
+        from primitive_sm_graph_gb300.workloads import gpt_step
+        tok, w = SI.gpt_block(0, **SI.GPT_SHAPES)
+        dtok = tok.cuda()
+        dw = {k: v.cuda() for k, v in w.items()}
+        H = SI.GPT_SHAPES["H"]
+        gpt_step(dtok, dw, H)          # first call compiles the specialised kernels
+        torch.cuda.synchronize()
+        from primitive_sm_graph_gb300 import graph as G
+        ex = G._executor()
+        ts, kernels = [], 0
+        for _ in range(steps):
+            ex.log.clear()
+            t0 = time.perf_counter()
+            gpt_step(dtok, dw, H)
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+            kernels = len(ex.log)
+        ms = statistics.median(ts) * 1e3
+        # algorithmic flops of the contractions: 8192 tokens x 6,553,600 linear
+        # + 2 x B*H*T*T*hd attention (QK^T and PV), times 3 for fwd + bwd
+        Bn, T, V, D, Hh, F = (SI.GPT_SHAPES[k] for k in ("B", "T", "V", "D", "H", "F"))
+        lin = 2 * Bn * T * (D * 3 * D + D * D + 2 * D * F + D * V)
+        att = 2 * 2 * Bn * Hh * T * T * (D // Hh)
+        flops = 3 * (lin + att)
+        return {"ms_per_step": round(ms, 3), "kernels_per_step": kernels, "flops": flops,
+                "achieved": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "note": "host wall clock per step, graph building and scheduling included",
+                "workload": "1-layer byte GPT fwd+bwd B32 T256 V256 d512 H8 MLP2048 bf16"}
+
+
 # ----------------------------------------------------------- CPU oracle ----
 
 def oracle_sample(threads: int, rows: int = 512):
@@ -291,6 +541,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+KERNEL_ROWS = ["softmax", "rmsnorm", "gemm_bf16", "gemm_f32", "gather", "scatter"]
+ROW_NAMES = KERNEL_ROWS + ["tiny_graph", "gpt"]
+
+
+def profile_case(A, name, iters):
+    """One workload, iters launches, nothing timed: the command a profiler
+    wraps to capture that kernel."""
+    if name in ("chain", "transpose"):
+        step = Step(A)
+        fn = getattr(step, name)
+    else:
+        fn, _ = getattr(Rows(A, peaks()), name)()
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(iters):
+        fn(s)
+    torch.cuda.synchronize()
+    print("profile case", name, "x", iters, "ok", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -298,6 +567,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", default="all",
+                    help="comma list of extra rows to time (softmax,rmsnorm,gemm_bf16,gemm_f32,"
+                         "gather,scatter,tiny_graph,gpt), 'all' or 'none'")
+    ap.add_argument("--profile-case", default=None,
+                    help="run one workload --iters times and exit (for a profiler capture); "
+                         "chain, transpose or a row name")
+    ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -311,6 +587,8 @@ def main():
     B.build()
     from primitive_sm_graph_gb300 import _abi as A
 
+    if args.profile_case:
+        return profile_case(A, args.profile_case, args.iters)
     step = Step(A)
     with Clocks(local) as clk:
         total_ms, chain_ms, tr_ms, wall = timed_steps(step, args.steps, args.warmup, dist)
@@ -348,6 +626,17 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
     }
+    names = ROW_NAMES if args.rows == "all" else [r for r in args.rows.split(",") if r and r != "none"]
+    if names:
+        rows = Rows(A, P)
+        kr = [n for n in names if n in KERNEL_ROWS]
+        line["rows"] = rows.run_kernel_rows(kr)
+        if "tiny_graph" in names:
+            line["rows"]["tiny_graph"] = rows.tiny_graph()
+        if "gpt" in names:
+            line["rows"]["gpt"] = rows.gpt()
+        if "gemm_bf16" in line["rows"]:
+            line["mul_sum_tflops"] = line["rows"]["gemm_bf16"]["achieved"]
     if rank == 0 and not args.no_cpu_baseline:
         cores = cpu_cores()
         sec, nbytes = oracle_sample(cores)

@@ -14,11 +14,30 @@ namespace psg {
 namespace {
 constexpr int EW_THREADS = 256;
 
+constexpr int EW_BLOCKS_PER_SM = 8;  // 2048 resident threads per SM at 256 a block
+
 int group_log2_for(int64_t chunks)
 {
     int g = 0;
     while ((1 << g) < chunks && (1 << g) < EW_THREADS) ++g;
     return g;
+}
+
+// Cut rows into column tiles when there are too few rows to give every
+// resident group of a full wave its own item; a tile is a multiple of the
+// group size, so each thread still walks whole chunks.
+void choose_tiles(int64_t rows, int64_t chunks, int gl, long long* tiles, long long* tile_chunks)
+{
+    const int64_t g = (int64_t)1 << gl;
+    const int64_t want = (int64_t)num_sms() * EW_BLOCKS_PER_SM * (EW_THREADS >> gl);
+    *tiles = 1;
+    *tile_chunks = chunks > 0 ? chunks : 1;
+    if (rows <= 0 || rows >= want || chunks <= g) return;
+    const int64_t per_row = (want + rows - 1) / rows;
+    int64_t tc = (chunks + per_row - 1) / per_row;
+    tc = (tc + g - 1) / g * g;
+    *tile_chunks = tc;
+    *tiles = (chunks + tc - 1) / tc;
 }
 }  // namespace
 
@@ -73,6 +92,7 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
     for (int d = 0; d < MAXD; ++d) P->p.shape[d] = d < sp.nd ? sp.shape[d] : 1;
     P->p.nd = sp.nd;
     P->p.group_log2 = group_log2_for(sp.chunks);
+    choose_tiles(sp.rows, sp.chunks, P->p.group_log2, &P->p.tiles, &P->p.tile_chunks);
     P->n_in = n_in;
     // the specialisation: input modes and dtypes, output dtype, the body
     std::string spec = "constexpr int kNin = " + std::to_string(n_in) + ";\n";
@@ -91,7 +111,7 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
 static psg_status grid_for(const EwPlan& P, cudaKernel_t k, int* grid)
 {
     const int groups = EW_THREADS >> P.p.group_log2;
-    const int64_t need = (P.p.rows + groups - 1) / groups;
+    const int64_t need = (P.p.rows * P.p.tiles + groups - 1) / groups;
     const int per_sm = jit_max_blocks_per_sm(k, EW_THREADS, 0);
     const int64_t cap = (int64_t)num_sms() * per_sm;
     *grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, cap));

@@ -9,9 +9,10 @@
 // serial ("Backends") and its cuda device uses atomics; here the colliding adds
 // happen in ascending n without atomics.  The keys (idx[n] << 32 | n) are
 // unique, so sorting them with a bitonic network gives one order no matter how
-// the sort is scheduled; each run of equal idx is then added by one warp in
-// that order into a float32 total seeded with the destination's value and
-// rounded once (int32 wraps; float64 totals in double).
+// the sort is scheduled; each run of equal idx is then added in that order,
+// one warp per (run, column segment), into a float32 total seeded with the
+// destination's value and rounded once (int32 wraps; float64 totals in
+// double).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -148,77 +149,155 @@ __global__ void bitonic_global(unsigned long long* keys, int64_t npow2, int64_t 
 }
 
 // ---- SCATTER: segmented, ordered accumulation -------------------------------
-template <typename T> struct Acc { typedef float A; };
-template <> struct Acc<double> { typedef double A; };
-template <> struct Acc<int32_t> { typedef int32_t A; };
-
-template <int DT>
-__device__ __forceinline__ float load_f(const void* p, int64_t o)
-{
-    if constexpr (DT == PSG_F32) return __ldg((const float*)p + o);
-    else if constexpr (DT == PSG_BF16) return __uint_as_float(((uint32_t)__ldg((const uint16_t*)p + o)) << 16);
-    else {
-        const uint16_t h = __ldg((const uint16_t*)p + o);
-        float r;
-        asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(h));
-        return r;
+// SV<DT>: the running total's type A (float32 for the float widths, double
+// for float64, uint32 for int32 so it wraps), loads of one cell or one
+// 16-byte vector of cells as A, the add, and the store that rounds once.
+template <int DT> struct SV;
+template <> struct SV<PSG_F32> {
+    typedef float A;
+    static constexpr int ES = 4;
+    static __device__ __forceinline__ A ld(const void* p, int64_t o) { return __ldg((const float*)p + o); }
+    static __device__ __forceinline__ A add(A a, A b) { return __fadd_rn(a, b); }
+    static __device__ __forceinline__ void st(void* p, int64_t o, A v) { ((float*)p)[o] = v; }
+    static __device__ __forceinline__ void unpack(const uint4 u, A (&x)[16 / ES])
+    {
+        x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
     }
-}
-template <int DT>
-__device__ __forceinline__ void store_f(void* p, int64_t o, float v)
-{
-    if constexpr (DT == PSG_F32) ((float*)p)[o] = v;
-    else if constexpr (DT == PSG_BF16) {
+};
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+template <> struct SV<PSG_BF16> {
+    typedef float A;
+    static constexpr int ES = 2;
+    static __device__ __forceinline__ A ld(const void* p, int64_t o)
+    {
+        return __uint_as_float(((uint32_t)__ldg((const uint16_t*)p + o)) << 16);
+    }
+    static __device__ __forceinline__ A add(A a, A b) { return __fadd_rn(a, b); }
+    static __device__ __forceinline__ void st(void* p, int64_t o, A v)
+    {
         uint16_t h;
         asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(v));
         ((uint16_t*)p)[o] = h;
-    } else {
+    }
+    static __device__ __forceinline__ void unpack(const uint4 u, A (&x)[16 / ES])
+    {
+        x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+        x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+    }
+};
+__device__ __forceinline__ float f16_bits(uint16_t h)
+{
+    float r;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(h));
+    return r;
+}
+template <> struct SV<PSG_F16> {
+    typedef float A;
+    static constexpr int ES = 2;
+    static __device__ __forceinline__ A ld(const void* p, int64_t o) { return f16_bits(__ldg((const uint16_t*)p + o)); }
+    static __device__ __forceinline__ A add(A a, A b) { return __fadd_rn(a, b); }
+    static __device__ __forceinline__ void st(void* p, int64_t o, A v)
+    {
         uint16_t h;
         asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(v));
         ((uint16_t*)p)[o] = h;
     }
-}
+    static __device__ __forceinline__ void unpack(const uint4 u, A (&x)[16 / ES])
+    {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = f16_bits((uint16_t)(w[i] & 0xffffu));
+            x[2 * i + 1] = f16_bits((uint16_t)(w[i] >> 16));
+        }
+    }
+};
+template <> struct SV<PSG_F64> {
+    typedef double A;
+    static constexpr int ES = 8;
+    static __device__ __forceinline__ A ld(const void* p, int64_t o) { return __ldg((const double*)p + o); }
+    static __device__ __forceinline__ A add(A a, A b) { return __dadd_rn(a, b); }
+    static __device__ __forceinline__ void st(void* p, int64_t o, A v) { ((double*)p)[o] = v; }
+    static __device__ __forceinline__ void unpack(const uint4 u, A (&x)[16 / ES])
+    {
+        x[0] = __hiloint2double((int)u.y, (int)u.x);
+        x[1] = __hiloint2double((int)u.w, (int)u.z);
+    }
+};
+template <> struct SV<PSG_I32> {
+    typedef uint32_t A;
+    static constexpr int ES = 4;
+    static __device__ __forceinline__ A ld(const void* p, int64_t o) { return __ldg((const uint32_t*)p + o); }
+    static __device__ __forceinline__ A add(A a, A b) { return a + b; }
+    static __device__ __forceinline__ void st(void* p, int64_t o, A v) { ((uint32_t*)p)[o] = v; }
+    static __device__ __forceinline__ void unpack(const uint4 u, A (&x)[16 / ES])
+    {
+        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    }
+};
 
-template <int DT>
+constexpr int SCATTER_UNROLL = 4;  // rows of a run loaded before they are added
+
+// One warp per (run, column segment) item.  A segment is 32 * VPL columns,
+// VPL cells per lane: a 16-byte vector when VEC (every update row contiguous
+// and 16-byte aligned), else one cell.  The run's rows are added in
+// ascending n into a total seeded with the destination's value; loading
+// SCATTER_UNROLL rows ahead of the adds keeps more bytes in flight and
+// leaves the order of the adds, hence the bits, unchanged.
+template <int DT, bool VEC>
 __global__ void __launch_bounds__(256) scatter_accumulate(const __grid_constant__ ScatterLaunch L,
-                                                          const unsigned long long* __restrict__ keys)
+                                                          const unsigned long long* __restrict__ keys,
+                                                          int64_t nseg)
 {
+    typedef SV<DT> S;
+    typedef typename S::A A;
+    constexpr int VPL = VEC ? 16 / S::ES : 1;
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * 8;
-    for (int64_t p = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); p < L.n; p += warps) {
-        const unsigned long long kp = keys[p];
-        const unsigned long long hi = kp >> 32;
-        if (hi == BAD_HI) continue;  // invalid index (or padding)
-        if (p > 0 && (keys[p - 1] >> 32) == hi) continue;  // not the start of a run
+    const int64_t items = L.n * nseg;
+    for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < items; it += warps) {
+        const int64_t p = it / nseg;
+        const int64_t seg = it - p * nseg;
+        const unsigned long long hi = keys[p] >> 32;
+        if (hi == BAD_HI) continue;                          // invalid index (or padding)
+        if (p > 0 && (keys[p - 1] >> 32) == hi) continue;    // not the start of a run
         int64_t end = p + 1;
         while (end < L.n && (keys[end] >> 32) == hi) ++end;
-        const int64_t v = (int64_t)hi;
-        const int64_t drow = L.dst_offset + v * L.dst_rs;
-        for (int64_t c = lane; c < L.D; c += 32) {
-            const int64_t od = drow + c * L.dst_cs;
-            if constexpr (DT == PSG_F64) {
-                double acc = ((const double*)L.dst)[od];
-                for (int64_t q = p; q < end; ++q) {
-                    const int64_t n = (int64_t)(keys[q] & 0xffffffffull);
-                    acc = __dadd_rn(acc, ((const double*)L.upd)[L.upd_offset + n * L.upd_rs + c * L.upd_cs]);
+        const int64_t c0 = (seg * 32 + lane) * VPL;
+        if (c0 >= L.D) continue;
+        const int nv = L.D - c0 < VPL ? (int)(L.D - c0) : VPL;
+        const int64_t drow = L.dst_offset + (int64_t)hi * L.dst_rs;
+        A acc[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) acc[i] = i < nv ? S::ld(L.dst, drow + (c0 + i) * L.dst_cs) : A(0);
+        for (int64_t q = p; q < end; q += SCATTER_UNROLL) {
+            A x[SCATTER_UNROLL][VPL];
+#pragma unroll
+            for (int u = 0; u < SCATTER_UNROLL; ++u) {
+                if (q + u >= end) break;
+                const int64_t n = (int64_t)(keys[q + u] & 0xffffffffull);
+                const int64_t o = L.upd_offset + n * L.upd_rs + c0 * L.upd_cs;
+                if constexpr (VEC) {
+                    if (nv == VPL) {
+                        S::unpack(__ldg((const uint4*)((const char*)L.upd + o * S::ES)), x[u]);
+                        continue;
+                    }
                 }
-                ((double*)L.dst)[od] = acc;
-            } else if constexpr (DT == PSG_I32) {
-                uint32_t acc = ((const uint32_t*)L.dst)[od];
-                for (int64_t q = p; q < end; ++q) {
-                    const int64_t n = (int64_t)(keys[q] & 0xffffffffull);
-                    acc += ((const uint32_t*)L.upd)[L.upd_offset + n * L.upd_rs + c * L.upd_cs];
-                }
-                ((uint32_t*)L.dst)[od] = acc;
-            } else {
-                float acc = load_f<DT>(L.dst, od);
-                for (int64_t q = p; q < end; ++q) {
-                    const int64_t n = (int64_t)(keys[q] & 0xffffffffull);
-                    acc = __fadd_rn(acc, load_f<DT>(L.upd, L.upd_offset + n * L.upd_rs + c * L.upd_cs));
-                }
-                store_f<DT>(L.dst, od, acc);
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) x[u][i] = i < nv ? S::ld(L.upd, o + i * L.upd_cs) : A(0);
+            }
+#pragma unroll
+            for (int u = 0; u < SCATTER_UNROLL; ++u) {
+                if (q + u >= end) break;
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) acc[i] = S::add(acc[i], x[u][i]);
             }
         }
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+            if (i < nv) S::st(L.dst, drow + (c0 + i) * L.dst_cs, acc[i]);
     }
 }
 
@@ -277,6 +356,24 @@ psg_status launch_gather(const GatherLaunch& L, void* stream)
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
+template <int DT>
+static void launch_accumulate(const ScatterLaunch& L, const unsigned long long* keys, cudaStream_t s)
+{
+    constexpr int ES = SV<DT>::ES;
+    const bool vec = L.upd_cs == 1 && ((uintptr_t)L.upd + (uint64_t)L.upd_offset * ES) % 16 == 0 &&
+                     ((uint64_t)L.upd_rs * ES) % 16 == 0;
+    const int64_t seg_cols = 32 * (vec ? 16 / ES : 1);
+    const int64_t nseg = (L.D + seg_cols - 1) / seg_cols;
+    const int64_t blocks = (L.n * nseg + 7) / 8;
+    if (nseg == 0) return;
+    if (vec)
+        scatter_accumulate<DT, true><<<grid_for((const void*)scatter_accumulate<DT, true>, 256, blocks), 256, 0, s>>>(
+            L, keys, nseg);
+    else
+        scatter_accumulate<DT, false><<<grid_for((const void*)scatter_accumulate<DT, false>, 256, blocks), 256, 0,
+                                        s>>>(L, keys, nseg);
+}
+
 psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void* stream)
 {
     if (L.n == 0) return PSG_OK;
@@ -293,23 +390,12 @@ psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void
                 keys, np2, k, j);
         bitonic_local<<<(unsigned)tiles, lthreads, 0, s>>>(keys, np2, k);
     }
-    const int64_t blocks = (L.n + 7) / 8;
     switch (L.dtype) {
-    case PSG_F32:
-        scatter_accumulate<PSG_F32><<<grid_for((const void*)scatter_accumulate<PSG_F32>, 256, blocks), 256, 0, s>>>(L, keys);
-        break;
-    case PSG_BF16:
-        scatter_accumulate<PSG_BF16><<<grid_for((const void*)scatter_accumulate<PSG_BF16>, 256, blocks), 256, 0, s>>>(L, keys);
-        break;
-    case PSG_F16:
-        scatter_accumulate<PSG_F16><<<grid_for((const void*)scatter_accumulate<PSG_F16>, 256, blocks), 256, 0, s>>>(L, keys);
-        break;
-    case PSG_F64:
-        scatter_accumulate<PSG_F64><<<grid_for((const void*)scatter_accumulate<PSG_F64>, 256, blocks), 256, 0, s>>>(L, keys);
-        break;
-    default:
-        scatter_accumulate<PSG_I32><<<grid_for((const void*)scatter_accumulate<PSG_I32>, 256, blocks), 256, 0, s>>>(L, keys);
-        break;
+    case PSG_F32: launch_accumulate<PSG_F32>(L, keys, s); break;
+    case PSG_BF16: launch_accumulate<PSG_BF16>(L, keys, s); break;
+    case PSG_F16: launch_accumulate<PSG_F16>(L, keys, s); break;
+    case PSG_F64: launch_accumulate<PSG_F64>(L, keys, s); break;
+    default: launch_accumulate<PSG_I32>(L, keys, s); break;
     }
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }

@@ -4,9 +4,12 @@
 // chunk of PSG_VEC consecutive cells along the innermost dim, so contiguous
 // operands move with 128-bit loads and stores and an expanded (stride-0)
 // operand is read once per chunk.  Row offsets come from one multi-index
-// decomposition per row; within a row the View's index is col * stride.  A
-// block is split into row groups of a power-of-two size so short rows still
-// fill it, and the grid is persistent (a multiple of the SM count).
+// decomposition per work item; within a row the View's index is col * stride.
+// A block is split into row groups of a power-of-two size so short rows still
+// fill it; long rows are cut into column tiles so that few rows (a fully
+// contiguous space collapses to one) still spread over every SM.  A work item
+// is one (row, tile) pair and the grid is persistent (a multiple of the SM
+// count).
 //
 // The including source defines kNin, kInMode[], kInDt[], kOutDt and
 // struct Body { template <class C> static void eval(const C&, T (&y)[PSG_VEC]); }.
@@ -35,12 +38,16 @@ extern "C" __global__ void __launch_bounds__(256) psg_ew(const __grid_constant__
     const int groups = 256 >> p.group_log2;
     const int grp = threadIdx.x >> p.group_log2;
     const int lane = threadIdx.x & (gs - 1);
-    for (i64 row = (i64)blockIdx.x * groups + grp; row < p.rows; row += (i64)gridDim.x * groups) {
+    const i64 items = p.rows * p.tiles;
+    for (i64 it = (i64)blockIdx.x * groups + grp; it < items; it += (i64)gridDim.x * groups) {
+        const i64 row = p.tiles == 1 ? it : it / p.tiles;
+        const i64 c0 = (it - row * p.tiles) * p.tile_chunks;
+        const i64 c1 = c0 + p.tile_chunks < p.chunks ? c0 + p.tile_chunks : p.chunks;
         i64 roff[kNin > 0 ? kNin : 1];
         bool rok[kNin > 0 ? kNin : 1];
         i64 ooff;
         row_offsets<kNin>(p.in, p.out, p.shape, p.nd, row, roff, rok, kInMode, ooff);
-        for (i64 ch = lane; ch < p.chunks; ch += gs) {
+        for (i64 ch = c0 + lane; ch < c1; ch += gs) {
             const i64 col0 = ch * PSG_VEC;
             const i64 left = p.inner - col0;
             const int nvalid = left < PSG_VEC ? (int)left : PSG_VEC;

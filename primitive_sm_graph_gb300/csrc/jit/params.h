@@ -38,6 +38,8 @@ struct PsgEwParams {
     long long rows;
     long long inner;
     long long chunks;      /* ceil(inner / PSG_VEC) */
+    long long tiles;       /* column tiles per row: work items are (row, tile) */
+    long long tile_chunks; /* chunks per tile (a multiple of the group size) */
     long long shape[PSG_MAXD];
     int nd;
     int group_log2;        /* threads per row group = 1 << group_log2 */

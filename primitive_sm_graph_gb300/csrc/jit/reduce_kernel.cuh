@@ -1,12 +1,12 @@
 // Row reduction skeleton (runtime-specialised per set of stage programs).
 //
-// A team of T = 1 << team_log2 threads owns one row of length N (the last
-// dim; limn, "Reading the schedule": a reduce is a cut and elementwise work
-// fuses into it).  Each thread holds chunks lane, lane+T, ... of PSG_VEC
-// cells.  When the row fits (kCH chunks per thread, kCH > 0) the inputs are
-// loaded once into registers and every stage and the epilogue read them from
-// there, so the row costs one HBM read and one write; otherwise every stage
-// streams the row again.  A stage folds its prologue values per thread, then
+// A team of T = 1 << team_log2 threads (T <= 256, the block size) owns one
+// row of length N (the last dim; limn, "Reading the schedule": a reduce is a
+// cut and elementwise work fuses into it).  Each thread holds chunks lane,
+// lane+T, ... of PSG_VEC cells.  When the row fits (kCH chunks per thread,
+// kCH > 0) the inputs are loaded once into registers and every stage and the
+// epilogue read them from there, so the row costs one HBM read and one
+// write; otherwise every stage streams the row again.  A stage folds its prologue values per thread, then
 // across the warp with shuffles and across the team's warps through shared
 // memory in a fixed order (the same bits every run).  The running total is
 // float32 (int32 for ints) and rounds into the stage dtype once (limn, "The
@@ -129,7 +129,7 @@ __device__ __forceinline__ typename VT<DT>::T team_fold(typename VT<DT>::T v, in
     return v;
 }
 
-extern "C" __global__ void __launch_bounds__(1024) psg_reduce(const __grid_constant__ PsgRedParams p)
+extern "C" __global__ void __launch_bounds__(256) psg_reduce(const __grid_constant__ PsgRedParams p)
 {
     __shared__ u32 sm[32];
     const int T = 1 << p.team_log2;

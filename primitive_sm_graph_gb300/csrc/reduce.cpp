@@ -13,6 +13,10 @@
 namespace psg {
 
 namespace {
+constexpr int RED_THREADS = 256;  // the skeleton's launch bound
+}  // namespace
+
+namespace {
 
 struct RedPlan {
     PsgRedParams p;
@@ -122,13 +126,18 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     if (st != PSG_OK) return st;
     if (E.result_dtype != out_v->dtype) return PSG_E_UNSUPPORTED_DTYPE;
     bodies += gen_eval(epi, E, "Epi");
-    // team of T threads per row, chunks per thread cached when they fit
+    // team of T threads per row.  A thread takes about RED_CHUNKS chunks, so
+    // each issues several 16- or 32-byte loads at once and short rows fold
+    // inside one warp (shuffles only); the row is cached in registers when
+    // its varying inputs fit in RED_CACHE_SLOTS chunk slots per thread.
+    constexpr int RED_CHUNKS = 4, RED_CACHE_SLOTS = 8, RED_MAX_TEAM_LOG2 = 8;
     int tl = 0;
-    while ((1 << tl) < sp.chunks && tl < 10) ++tl;
+    while ((int64_t)RED_CHUNKS << tl < sp.chunks && tl < RED_MAX_TEAM_LOG2) ++tl;
     const int T = 1 << tl;
     const int64_t ch_per = (sp.chunks + T - 1) / T;
-    const int kch = (ch_per <= 4 && n_vary * ch_per <= 8) ? (int)(ch_per > 0 ? ch_per : 1) : 0;
-    P->block = T > 256 ? T : 256;
+    const int vary = n_vary > 0 ? n_vary : 1;
+    const int kch = vary * ch_per <= RED_CACHE_SLOTS ? (int)(ch_per > 0 ? ch_per : 1) : 0;
+    P->block = RED_THREADS;
     P->p.rows = sp.rows;
     P->p.inner = sp.inner;
     P->p.chunks = sp.chunks;
