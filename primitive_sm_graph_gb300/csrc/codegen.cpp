@@ -149,9 +149,27 @@ psg_status analyze_program(const psg_node* nodes, int n, const int* in_dtype, co
 }
 
 std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string& name,
-                     const std::string& prefix)
+                     const std::string& prefix, int stash)
 {
     const int n = I.n;
+    // with a stashed node, liveness restarts from the result with that node
+    // as a leaf: what only fed it is not computed again
+    std::vector<int> live = I.live;
+    if (stash >= 0) {
+        live.assign(n, 0);
+        live[n - 1] = 1;
+        for (int i = n - 1; i >= 0; --i) {
+            if (!live[i] || i == stash) continue;
+            const psg_node& x = nodes[i];
+            switch (x.op) {
+            case PSG_OP_NEG: case PSG_OP_EXP: case PSG_OP_LOG: case PSG_OP_SQRT:
+            case PSG_OP_RECIP: case PSG_OP_CAST: live[x.a] = 1; break;
+            case PSG_OP_ADD: case PSG_OP_MUL: case PSG_OP_CMPLT: live[x.a] = live[x.b] = 1; break;
+            case PSG_OP_WHERE: live[x.a] = live[x.b] = live[x.c] = 1; break;
+            default: break;
+            }
+        }
+    }
     auto ref = [&](int j) {
         const int v = I.val[j];
         return std::string(I.uni[v] ? "u" : "x") + std::to_string(v);
@@ -159,11 +177,15 @@ std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string
     std::string head, uni_part, loop_part;
     std::vector<char> loaded(PSG_MAX_INPUTS, 0);
     for (int i = 0; i < n; ++i) {
-        if (!I.live[i] || I.val[i] != i) continue;
+        if (!live[i] || I.val[i] != i) continue;
         const psg_node& x = nodes[i];
         const int dt = x.dtype;
         const bool isint = dtype_is_int(dt);
         std::string e;
+        if (i == stash) {
+            loop_part += fmt("            const %s x%d = %s;\n", ctype(dt), i, isint ? "c.stashi(v)" : "c.stashf(v)");
+            continue;
+        }
         switch (x.op) {
         case PSG_OP_LOAD:
             if (I.uni[i]) {
@@ -218,16 +240,32 @@ std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string
         if (I.uni[i]) uni_part += "        const " + stmt;
         else loop_part += "            const " + stmt;
     }
+    // uniform values are computed once per row by uni() and handed to eval()
+    // for every chunk of that row
+    std::vector<int> uvals;
+    for (int i = 0; i < n; ++i)
+        if (live[i] && I.val[i] == i && I.uni[i] && i != stash) uvals.push_back(i);
     const std::string rt = ctype(I.result_dtype);
     std::string s;
     s += prefix + "struct " + name + " {\n";
+    s += "    struct U {\n";
+    for (int i : uvals) s += fmt("        %s u%d;\n", ctype(I.dt[i]), i);
+    if (uvals.empty()) s += "        int none;\n";
+    s += "    };\n";
     s += "    template <class C>\n";
-    s += "    __device__ __forceinline__ static void eval(const C& c, " + rt + " (&y)[PSG_VEC])\n    {\n";
-    s += head;
+    s += "    __device__ __forceinline__ static U uni(const C& c)\n    {\n";
     s += uni_part;
+    s += "        U r;\n";
+    for (int i : uvals) s += fmt("        r.u%d = u%d;\n", i, i);
+    if (uvals.empty()) s += "        r.none = 0;\n";
+    s += "        return r;\n    }\n";
+    s += "    template <class C>\n";
+    s += "    __device__ __forceinline__ static void eval(const C& c, const U& u, " + rt + " (&y)[PSG_VEC])\n    {\n";
+    for (int i : uvals) s += fmt("        const %s u%d = u.u%d;\n", ctype(I.dt[i]), i, i);
     if (I.result_uniform) {
         s += fmt("#pragma unroll\n        for (int v = 0; v < PSG_VEC; ++v) y[v] = u%d;\n", I.result);
     } else {
+        s += head;
         s += "#pragma unroll\n        for (int v = 0; v < PSG_VEC; ++v) {\n";
         s += loop_part;
         s += fmt("            y[v] = x%d;\n        }\n", I.result);

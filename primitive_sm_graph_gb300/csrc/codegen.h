@@ -25,10 +25,14 @@ struct ProgInfo {
 psg_status analyze_program(const psg_node* nodes, int n, const int* in_dtype, const bool* in_uniform,
                            int n_in, const int* red_dtype, int n_red, ProgInfo* info);
 
-// C++ source of `struct <name> { template <class C> static void eval(const C& c,
-// T (&y)[PSG_VEC]); }` computing the program for the PSG_VEC lanes of a chunk.
-// C provides ldv<K>(arr), ld1<K>(), redf(s), redi(s).
+// C++ source of `struct <name> { struct U; template <class C> static U uni(const
+// C& c); template <class C> static void eval(const C& c, const U& u, T
+// (&y)[PSG_VEC]); }`: uni() computes the program's uniform values (once per
+// row), eval() the program for the PSG_VEC lanes of a chunk.
+// C provides ldv<K>(arr), ld1<K>(), redf(s), redi(s).  With stash >= 0 the
+// value of node `stash` (non-uniform) is read per lane from c.stashf(v) /
+// c.stashi(v) instead of being computed, and whatever only fed it is dropped.
 std::string gen_eval(const psg_node* nodes, const ProgInfo& info, const std::string& name,
-                     const std::string& prefix = "");
+                     const std::string& prefix = "", int stash = -1);
 
 }  // namespace psg

@@ -103,6 +103,7 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
     }
     spec += m + "};\n" + d + "};\n";
     spec += "constexpr int kOutDt = " + std::to_string(out_v->dtype) + ";\n";
+    spec += std::string("constexpr bool kExact = ") + (sp.inner % PSG_VEC == 0 ? "true" : "false") + ";\n";
     spec += gen_eval(prog, I, "Body");
     P->spec = std::move(spec);
     return PSG_OK;

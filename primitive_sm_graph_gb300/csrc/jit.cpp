@@ -35,13 +35,18 @@ psg_status compile(const std::string& src, std::vector<char>* cubin, std::string
     nvrtcProgram prog;
     if (nvrtcCreateProgram(&prog, src.c_str(), "psg_jit.cu", 0, nullptr, nullptr) != NVRTC_SUCCESS)
         return PSG_E_CUDA;
-    const nvrtcResult rc = nvrtcCompileProgram(prog, (int)(sizeof(kOpts) / sizeof(kOpts[0])), kOpts);
+    // PSG_JIT_PTXAS_V=1 asks ptxas for its resource report (registers,
+    // spills) in the program log
+    std::vector<const char*> opts(kOpts, kOpts + sizeof(kOpts) / sizeof(kOpts[0]));
+    if (std::getenv("PSG_JIT_PTXAS_V")) opts.push_back("--ptxas-options=-v");
+    const nvrtcResult rc = nvrtcCompileProgram(prog, (int)opts.size(), opts.data());
     size_t ls = 0;
     nvrtcGetProgramLogSize(prog, &ls);
     if (log && ls > 1) {
         log->resize(ls);
         nvrtcGetProgramLog(prog, &(*log)[0]);
     }
+    if (rc == NVRTC_SUCCESS && std::getenv("PSG_JIT_PTXAS_V") && log) std::fprintf(stderr, "%s\n", log->c_str());
     if (rc != NVRTC_SUCCESS) {
         if (std::getenv("PSG_JIT_VERBOSE") && log) std::fprintf(stderr, "%s\n%s\n", src.c_str(), log->c_str());
         nvrtcDestroyProgram(&prog);

@@ -11,7 +11,9 @@
 // is one (row, tile) pair and the grid is persistent (a multiple of the SM
 // count).
 //
-// The including source defines kNin, kInMode[], kInDt[], kOutDt and
+// kExact: the row length is a multiple of PSG_VEC, so every chunk is whole.
+//
+// The including source defines kNin, kInMode[], kInDt[], kOutDt, kExact and
 // struct Body { template <class C> static void eval(const C&, T (&y)[PSG_VEC]); }.
 
 struct EwCtx {
@@ -47,13 +49,16 @@ extern "C" __global__ void __launch_bounds__(256) psg_ew(const __grid_constant__
         bool rok[kNin > 0 ? kNin : 1];
         i64 ooff;
         row_offsets<kNin>(p.in, p.out, p.shape, p.nd, row, roff, rok, kInMode, ooff);
+        if (c0 + lane >= c1) continue;
+        const EwCtx cu{p, roff, rok, 0, PSG_VEC};
+        const typename Body::U u = Body::uni(cu);  // the row's uniform values, once
         for (i64 ch = c0 + lane; ch < c1; ch += gs) {
             const i64 col0 = ch * PSG_VEC;
             const i64 left = p.inner - col0;
-            const int nvalid = left < PSG_VEC ? (int)left : PSG_VEC;
+            const int nvalid = kExact || left >= PSG_VEC ? PSG_VEC : (int)left;
             const EwCtx c{p, roff, rok, col0, nvalid};
             typename VT<kOutDt>::T y[PSG_VEC];
-            Body::eval(c, y);
+            Body::eval(c, u, y);
             st_chunk<kOutDt>(p.out, ooff, col0, nvalid, y);
         }
     }

@@ -47,6 +47,9 @@ struct PsgEwParams {
     struct PsgOperand out;
 };
 
+/* device-reported status the generated kernels write (= PSG_E_TIMEOUT) */
+#define PSG_DEV_E_TIMEOUT 7
+
 /* Row reduction: every input has the iteration shape [rows.., N]; the
  * output is [rows.., N] (per-element epilogue) or [rows..] (per-row). */
 struct PsgRedParams {
@@ -58,6 +61,7 @@ struct PsgRedParams {
     int team_log2;         /* threads per row = 1 << team_log2 */
     int out_per_row;       /* 1: one output per row; 0: per element */
     int pad;
+    int* status;           /* device status word (PSG_E_TIMEOUT), may be null */
     struct PsgOperand in[PSG_MAXIN];
     struct PsgOperand out;
 };

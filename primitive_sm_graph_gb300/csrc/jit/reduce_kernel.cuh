@@ -12,8 +12,17 @@
 // float32 (int32 for ints) and rounds into the stage dtype once (limn, "The
 // op set": a reduce keeps its running total in float32).
 //
+// Only inputs that change from row to row are cached (kCacheIn); bfloat16
+// cells are held packed, two to a word.  When the epilogue begins with the
+// whole program of stage kStash, that stage keeps its per-cell values
+// (the stash) and the epilogue reads them instead of computing them again.
+//
+// kExact: every thread's kCH chunks are whole and inside the row, so no
+// chunk needs a range check.
+//
 // The including source defines kNin, kInMode[], kInDt[], kOutDt, kNstages,
-// kStageOp[], kStageDt[], kCH, kPerRow, StageBody<S> and Epi.
+// kStageOp[], kStageDt[], kCH, kExact, kCacheIn[], kStash, kPerRow, the
+// staged-mode constants, StageBody<S> and Epi.
 
 template <int V> struct IC { static constexpr int value = V; };
 template <int J, int N, class F>
@@ -30,12 +39,15 @@ __device__ __forceinline__ void sfor(F& f)
 constexpr int kNinP = kNin > 0 ? kNin : 1;
 constexpr int kCHP = kCH > 0 ? kCH : 1;
 
-// MAX: NaN propagates, +0 beats -0 on a tie, so any order gives the same bits
+// MAX: NaN propagates, +0 beats -0 on a tie, so any order gives the same
+// bits.  max.NaN gives a NaN when either operand is one; operands that
+// compare equal (the only case where +0 and -0 meet) keep a sign bit only
+// when both have it, and equal nonzero operands have equal bits anyway.
 __device__ __forceinline__ float fmax_step(float acc, float x)
 {
-    if (acc != acc) return acc;
-    if (x != x || x > acc || (x == acc && (__float_as_uint(x) >> 31) == 0)) return x;
-    return acc;
+    float m;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(m) : "f"(acc), "f"(x));
+    return acc == x ? __uint_as_float(__float_as_uint(acc) & __float_as_uint(x)) : m;
 }
 
 template <int OP, int DT>
@@ -76,12 +88,84 @@ template <class T> __device__ __forceinline__ T from_bits(u32 b);
 template <> __device__ __forceinline__ float from_bits<float>(u32 b) { return __uint_as_float(b); }
 template <> __device__ __forceinline__ int from_bits<int>(u32 b) { return (int)b; }
 
+// ---- staged rows: shared-memory ring filled by bulk copies ---------------
+__device__ __forceinline__ u32 smem_addr(const void* p) { return (u32)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(unsigned long long* b, u32 count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* b, u32 bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(unsigned long long* b, u32 parity)
+{
+    u32 ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+constexpr long long kWaitCycles = 2000000000ll;  // about one second
+// true when the phase completed; false after about a second (PSG_E_TIMEOUT
+// goes to the status word)
+__device__ __noinline__ bool mbar_wait(unsigned long long* b, u32 parity, int* status)
+{
+    const long long t0 = clock64();
+    for (u32 i = 0;; ++i) {
+        if (mbar_try(b, parity)) return true;
+        if ((i & 63) == 63 && clock64() - t0 > kWaitCycles) {
+            if (status) atomicCAS(status, 0, PSG_DEV_E_TIMEOUT);
+            return false;
+        }
+    }
+}
+// one contiguous global range -> shared memory, completing on mbarrier b
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, u32 bytes, unsigned long long* b)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(b))
+                 : "memory");
+}
+// the PSG_VEC cells at col0 of a staged row segment (16-byte shared loads)
+template <int DT>
+__device__ __forceinline__ void ld_staged(const unsigned char* seg, i64 col0, typename VT<DT>::T (&d)[PSG_VEC])
+{
+    if constexpr (DT == PSG_DT_F32 || DT == PSG_DT_I32) {
+        const uint4* q = (const uint4*)(seg + col0 * 4);
+        const uint4 x = q[0], y = q[1];
+        const u32 w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int v = 0; v < PSG_VEC; ++v) {
+            if constexpr (DT == PSG_DT_F32) d[v] = __uint_as_float(w[v]);
+            else d[v] = (int)w[v];
+        }
+    } else {
+        const uint4 x = *(const uint4*)(seg + col0 * 2);
+        const u32 w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            if constexpr (DT == PSG_DT_BF16) {
+                d[2 * v] = __uint_as_float(w[v] << 16);
+                d[2 * v + 1] = __uint_as_float(w[v] & 0xffff0000u);
+            } else {
+                d[2 * v] = h2f((u16)(w[v] & 0xffffu));
+                d[2 * v + 1] = h2f((u16)(w[v] >> 16));
+            }
+        }
+    }
+}
+
 struct RedCtx {
     const PsgRedParams& p;
     const i64 (&roff)[kNinP];
     const bool (&rok)[kNinP];
     const u32 (&cache)[kNinP][kCHP][PSG_VEC];
+    const u32 (&stash)[kCHP][PSG_VEC];
     const u32 (&red)[PSG_MAXSTAGES];
+    const unsigned char* sb;  // the row's stage in shared memory (staged mode)
     i64 col0;
     int nvalid;
     int j;  // chunk slot (compile-time after unrolling)
@@ -89,7 +173,15 @@ struct RedCtx {
     __device__ __forceinline__ void ldv(typename VT<kInDt[K]>::T (&d)[PSG_VEC]) const
     {
         typedef typename VT<kInDt[K]>::T T;
-        if constexpr (kCH > 0 && kInMode[K] != PSG_M_UNIFORM) {
+        if constexpr (kStaged && kStagedIn[K]) {
+            ld_staged<kInDt[K]>(sb + kSegOff[K], col0, d);
+        } else if constexpr (kCH > 0 && kCacheIn[K] && kInDt[K] == PSG_DT_BF16) {
+#pragma unroll
+            for (int w = 0; w < PSG_VEC / 2; ++w) {
+                d[2 * w] = __uint_as_float(cache[K][j][w] << 16);
+                d[2 * w + 1] = __uint_as_float(cache[K][j][w] & 0xffff0000u);
+            }
+        } else if constexpr (kCH > 0 && kCacheIn[K]) {
 #pragma unroll
             for (int v = 0; v < PSG_VEC; ++v) d[v] = from_bits<T>(cache[K][j][v]);
         } else {
@@ -103,6 +195,8 @@ struct RedCtx {
     }
     __device__ __forceinline__ float redf(int s) const { return __uint_as_float(red[s]); }
     __device__ __forceinline__ int redi(int s) const { return (int)red[s]; }
+    __device__ __forceinline__ float stashf(int v) const { return __uint_as_float(stash[j][v]); }
+    __device__ __forceinline__ int stashi(int v) const { return (int)stash[j][v]; }
 };
 
 // fold v across the team (threads [team*T, team*T + T) of the block)
@@ -129,29 +223,73 @@ __device__ __forceinline__ typename VT<DT>::T team_fold(typename VT<DT>::T v, in
     return v;
 }
 
-extern "C" __global__ void __launch_bounds__(256) psg_reduce(const __grid_constant__ PsgRedParams p)
+extern "C" __global__ void __launch_bounds__(256, kMinBlocks) psg_reduce(const __grid_constant__ PsgRedParams p)
 {
     __shared__ u32 sm[32];
+    extern __shared__ __align__(128) unsigned char dsm[];  // staged mode: barriers, then the ring
     const int T = 1 << p.team_log2;
     const int teams = blockDim.x >> p.team_log2;
     const int team = threadIdx.x >> p.team_log2;
     const int lane = threadIdx.x & (T - 1);
-    // every team of the block runs the same number of iterations, so the
-    // barriers inside team_fold are reached by all threads
-    for (i64 base = (i64)blockIdx.x * teams; base < p.rows; base += (i64)gridDim.x * teams) {
-        const i64 row = base + team;
+    unsigned long long* bars = (unsigned long long*)dsm;  // [teams][kNS]
+    unsigned char* ring = dsm + kBarBytes;                 // [teams][kNS][kStageBytes]
+    if constexpr (kStaged) {
+        if (threadIdx.x < teams * kNS) mbar_init(&bars[threadIdx.x], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        __syncthreads();
+    }
+    // iteration it gives team `team` the row first + it * step + team; every
+    // team of the block runs the same number of iterations, so the barriers
+    // inside team_fold (and the staged ring's) are reached by all threads
+    const i64 step = (i64)gridDim.x * teams;
+    const i64 first = (i64)blockIdx.x * teams;
+    const i64 niter = first < p.rows ? (p.rows - first + step - 1) / step : 0;
+    // staged mode: one lane of the team fills ring slot it % kNS with the
+    // row of iteration it (one bulk copy per staged input)
+    auto issue = [&](i64 it) {
+        const i64 row = first + it * step + team;
+        if (lane != 0 || row >= p.rows) return;
+        i64 ro[kNinP];
+        bool rk[kNinP];
+        i64 oo;
+        row_offsets<kNin>(p.in, p.out, p.shape, p.nd, row, ro, rk, kInMode, oo);
+        const int slot = (int)(it % kNS);
+        unsigned long long* b = &bars[team * kNS + slot];
+        unsigned char* dst = ring + (size_t)(team * kNS + slot) * kStageBytes;
+        // the team's reads of this slot (generic proxy) come before the copy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(b, kTxBytes);
+        auto cp = [&](auto kt) {
+            constexpr int K = decltype(kt)::value;
+            if constexpr (kStagedIn[K])
+                bulk_g2s(dst + kSegOff[K], (const char*)p.in[K].ptr + ro[K] * kInSize[K], kRowBytes[K], b);
+        };
+        sfor<0, kNin>(cp);
+    };
+    if constexpr (kStaged) {
+        for (i64 it = 0; it < kNS - 1 && it < niter; ++it) issue(it);
+    }
+    bool dead = false;  // a staged wait gave up: stop waiting, finish in bounded time
+    for (i64 it = 0; it < niter; ++it) {
+        const i64 row = first + it * step + team;
         const bool active = row < p.rows;
         i64 roff[kNinP];
         bool rok[kNinP];
         i64 ooff = 0;
         if (active) {
-            PsgOperand outp = p.out;
-            row_offsets<kNin>(p.in, outp, p.shape, p.nd, row, roff, rok, kInMode, ooff);
+            row_offsets<kNin>(p.in, p.out, p.shape, p.nd, row, roff, rok, kInMode, ooff);
         } else {
 #pragma unroll
             for (int k = 0; k < kNinP; ++k) { roff[k] = 0; rok[k] = false; }
         }
-        // load the row once when it fits in registers
+        const unsigned char* sb = nullptr;
+        if constexpr (kStaged) {
+            if (it + kNS - 1 < niter) issue(it + kNS - 1);
+            const int slot = (int)(it % kNS);
+            sb = ring + (size_t)(team * kNS + slot) * kStageBytes;
+            if (active && !dead) dead = !mbar_wait(&bars[team * kNS + slot], (u32)((it / kNS) & 1), p.status);
+        }
+        // register-cache mode: load the row once
         u32 cache[kNinP][kCHP][PSG_VEC];
         if constexpr (kCH > 0) {
 #pragma unroll
@@ -159,20 +297,29 @@ extern "C" __global__ void __launch_bounds__(256) psg_reduce(const __grid_consta
                 const i64 ch = lane + (i64)j * T;
                 const i64 col0 = ch * PSG_VEC;
                 const i64 left = p.inner - col0;
-                const int nvalid = !active || left <= 0 ? 0 : left < PSG_VEC ? (int)left : PSG_VEC;
+                const int nvalid = !active ? 0 : kExact ? PSG_VEC : left <= 0 ? 0 : left < PSG_VEC ? (int)left : PSG_VEC;
                 auto ldk = [&](auto kt) {
                     constexpr int K = decltype(kt)::value;
-                    if constexpr (kInMode[K] != PSG_M_UNIFORM) {
+                    if constexpr (kCacheIn[K]) {
                         typename VT<kInDt[K]>::T d[PSG_VEC];
                         if (nvalid > 0) ld_chunk<kInDt[K], kInMode[K]>(p.in[K], roff[K], rok[K], col0, nvalid, d);
+                        if constexpr (kInDt[K] == PSG_DT_BF16) {
 #pragma unroll
-                        for (int v = 0; v < PSG_VEC; ++v) cache[K][j][v] = nvalid > 0 ? as_bits(d[v]) : 0u;
+                            for (int w = 0; w < PSG_VEC / 2; ++w)
+                                cache[K][j][w] = nvalid > 0 ? (__float_as_uint(d[2 * w]) >> 16) |
+                                                                  (__float_as_uint(d[2 * w + 1]) & 0xffff0000u)
+                                                            : 0u;
+                        } else {
+#pragma unroll
+                            for (int v = 0; v < PSG_VEC; ++v) cache[K][j][v] = nvalid > 0 ? as_bits(d[v]) : 0u;
+                        }
                     }
                 };
                 sfor<0, kNin>(ldk);
             }
         }
         u32 red[PSG_MAXSTAGES] = {0u, 0u, 0u, 0u};
+        u32 stash[kCHP][PSG_VEC];
         auto stage = [&](auto st) {
             constexpr int S = decltype(st)::value;
             constexpr int OP = kStageOp[S];
@@ -180,50 +327,64 @@ extern "C" __global__ void __launch_bounds__(256) psg_reduce(const __grid_consta
             typedef Fold<OP, DT> F;
             typename VT<DT>::T acc = F::identity();
             const int nch = kCH > 0 ? kCH : (int)((p.chunks - lane + T - 1) / T);
+            typename StageBody<S>::U u;
+            if (active) {
+                const RedCtx cu{p, roff, rok, cache, stash, red, sb, 0, PSG_VEC, 0};
+                u = StageBody<S>::uni(cu);  // the row's uniform values, once
+            }
 #pragma unroll
             for (int j = 0; j < (kCH > 0 ? kCH : 1); ++j) {
                 for (int jj = (kCH > 0 ? j : 0); jj < (kCH > 0 ? j + 1 : nch); ++jj) {
                     const i64 ch = lane + (i64)jj * T;
                     const i64 col0 = ch * PSG_VEC;
                     const i64 left = p.inner - col0;
-                    if (!active || left <= 0) continue;
-                    const int nvalid = left < PSG_VEC ? (int)left : PSG_VEC;
-                    const RedCtx c{p, roff, rok, cache, red, col0, nvalid, j};
+                    if (!active || (!kExact && left <= 0)) continue;
+                    const int nvalid = kExact ? PSG_VEC : left < PSG_VEC ? (int)left : PSG_VEC;
+                    const RedCtx c{p, roff, rok, cache, stash, red, sb, col0, nvalid, j};
                     typename VT<DT>::T y[PSG_VEC];
-                    StageBody<S>::eval(c, y);
+                    StageBody<S>::eval(c, u, y);
+                    if constexpr (S == kStash) {
+#pragma unroll
+                        for (int v = 0; v < PSG_VEC; ++v) stash[j][v] = as_bits(y[v]);
+                    }
 #pragma unroll
                     for (int v = 0; v < PSG_VEC; ++v)
-                        if (v < nvalid) acc = F::step(acc, y[v]);
+                        if (kExact || v < nvalid) acc = F::step(acc, y[v]);
                 }
             }
             acc = team_fold<OP, DT>(acc, p.team_log2, sm);
             red[S] = as_bits(F::finish(acc));
         };
         sfor<0, kNstages>(stage);
-        if (!active) continue;
-        if constexpr (kPerRow) {
-            if (lane == 0) {
-                const RedCtx c{p, roff, rok, cache, red, 0, 1, 0};
-                typename VT<kOutDt>::T y[PSG_VEC];
-                Epi::eval(c, y);
-                st_cell<kOutDt>((void*)p.out.ptr, ooff, y[0]);
-            }
-        } else {
-            const int nch = kCH > 0 ? kCH : (int)((p.chunks - lane + T - 1) / T);
-#pragma unroll
-            for (int j = 0; j < (kCH > 0 ? kCH : 1); ++j) {
-                for (int jj = (kCH > 0 ? j : 0); jj < (kCH > 0 ? j + 1 : nch); ++jj) {
-                    const i64 ch = lane + (i64)jj * T;
-                    const i64 col0 = ch * PSG_VEC;
-                    const i64 left = p.inner - col0;
-                    if (left <= 0) continue;
-                    const int nvalid = left < PSG_VEC ? (int)left : PSG_VEC;
-                    const RedCtx c{p, roff, rok, cache, red, col0, nvalid, j};
+        if (active) {
+            if constexpr (kPerRow) {
+                if (lane == 0) {
+                    const RedCtx c{p, roff, rok, cache, stash, red, sb, 0, 1, 0};
                     typename VT<kOutDt>::T y[PSG_VEC];
-                    Epi::eval(c, y);
-                    st_chunk<kOutDt>(p.out, ooff, col0, nvalid, y);
+                    Epi::eval(c, Epi::uni(c), y);
+                    st_cell<kOutDt>((void*)p.out.ptr, ooff, y[0]);
+                }
+            } else {
+                const int nch = kCH > 0 ? kCH : (int)((p.chunks - lane + T - 1) / T);
+                const RedCtx cu{p, roff, rok, cache, stash, red, sb, 0, PSG_VEC, 0};
+                const typename Epi::U u = Epi::uni(cu);  // the row's uniform values, once
+#pragma unroll
+                for (int j = 0; j < (kCH > 0 ? kCH : 1); ++j) {
+                    for (int jj = (kCH > 0 ? j : 0); jj < (kCH > 0 ? j + 1 : nch); ++jj) {
+                        const i64 ch = lane + (i64)jj * T;
+                        const i64 col0 = ch * PSG_VEC;
+                        const i64 left = p.inner - col0;
+                        if (!kExact && left <= 0) continue;
+                        const int nvalid = kExact ? PSG_VEC : left < PSG_VEC ? (int)left : PSG_VEC;
+                        const RedCtx c{p, roff, rok, cache, stash, red, sb, col0, nvalid, j};
+                        typename VT<kOutDt>::T y[PSG_VEC];
+                        Epi::eval(c, u, y);
+                        st_chunk<kOutDt>(p.out, ooff, col0, nvalid, y);
+                    }
                 }
             }
         }
+        // staged mode: every thread is done with this slot before it is refilled
+        if constexpr (kStaged) __syncthreads();
     }
 }

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <unordered_map>
+#include <mutex>
 
 #include "api_internal.h"
 #include "codegen.h"
@@ -14,6 +16,7 @@ namespace psg {
 
 namespace {
 constexpr int RED_THREADS = 256;  // the skeleton's launch bound
+static_assert(PSG_DEV_E_TIMEOUT == PSG_E_TIMEOUT, "device status code");
 }  // namespace
 
 namespace {
@@ -21,6 +24,7 @@ namespace {
 struct RedPlan {
     PsgRedParams p;
     int block;
+    int smem;  // dynamic shared memory (staged mode)
     std::string spec;
 };
 
@@ -88,12 +92,10 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     if (st != PSG_OK) return st;
     bool uni[PSG_MAX_INPUTS];
     int modes[PSG_MAX_INPUTS];
-    int n_vary = 0;
     for (int k = 0; k < n_in; ++k) {
         modes[k] = fill_operand(P->p.in[k], in[k], &in_v[k], sp, strides[1 + k], lo[1 + k], hi[1 + k],
                                 masked[1 + k]);
         uni[k] = modes[k] == PSG_M_UNIFORM;
-        n_vary += uni[k] ? 0 : 1;
     }
     fill_operand(P->p.out, out, &ov, sp, strides[0], lo[0], hi[0], false);
     // stages
@@ -125,18 +127,98 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
                  : analyze_program(epi, n_epi, dts, uni, n_in, sdt, n_stages, &E);
     if (st != PSG_OK) return st;
     if (E.result_dtype != out_v->dtype) return PSG_E_UNSUPPORTED_DTYPE;
-    bodies += gen_eval(epi, E, "Epi");
+    // which inputs the register cache holds: those that vary from row to row
+    // (a row-invariant operand, like a norm's weight, stays in L1 and is
+    // read again); bfloat16 rows are held packed, two cells a word
+    int cache_in[PSG_MAX_INPUTS];
+    int words = 0;
+    for (int k = 0; k < n_in; ++k) {
+        bool row_inv = modes[k] != PSG_M_MASKED;
+        for (int d = 0; d + 1 < sp.nd; ++d)
+            if (P->p.in[k].outer_stride[d] != 0) row_inv = false;
+        cache_in[k] = !uni[k] && !row_inv;
+        if (cache_in[k]) words += dts[k] == PSG_BF16 ? PSG_VEC / 2 : PSG_VEC;
+    }
+    // an epilogue that starts with a stage's whole program reuses that
+    // stage's per-cell values (softmax: EXP(x - m) is computed once)
+    int stash = -1;
+    if (!per_row) {
+        for (int s = n_stages - 1; s >= 0 && stash < 0; --s) {
+            const int m = stages[s].n_nodes;
+            if (m > n_epi || E.val[m - 1] != m - 1 || E.uni[m - 1] || !E.live[m - 1]) continue;
+            bool same = true;
+            for (int i = 0; i < m && same; ++i) {
+                const psg_node &x = stages[s].prologue[i], &y = epi[i];
+                same = x.op == y.op && x.a == y.a && x.b == y.b && x.c == y.c && x.dtype == y.dtype &&
+                       std::memcmp(&x.cval, &y.cval, sizeof(double)) == 0;
+            }
+            if (same && m < n_epi) stash = s;
+        }
+    }
     // team of T threads per row.  A thread takes about RED_CHUNKS chunks, so
     // each issues several 16- or 32-byte loads at once and short rows fold
-    // inside one warp (shuffles only); the row is cached in registers when
-    // its varying inputs fit in RED_CACHE_SLOTS chunk slots per thread.
-    constexpr int RED_CHUNKS = 4, RED_CACHE_SLOTS = 8, RED_MAX_TEAM_LOG2 = 8;
+    // inside one warp (shuffles only); the row (and a stash) is cached in
+    // registers when it fits in RED_CACHE_WORDS words per thread.
+    constexpr int RED_CHUNKS = 4, RED_CACHE_WORDS = 64, RED_MAX_TEAM_LOG2 = 8;
     int tl = 0;
     while ((int64_t)RED_CHUNKS << tl < sp.chunks && tl < RED_MAX_TEAM_LOG2) ++tl;
     const int T = 1 << tl;
-    const int64_t ch_per = (sp.chunks + T - 1) / T;
-    const int vary = n_vary > 0 ? n_vary : 1;
-    const int kch = vary * ch_per <= RED_CACHE_SLOTS ? (int)(ch_per > 0 ? ch_per : 1) : 0;
+    const int64_t ch_per = (sp.chunks + T - 1) / T > 0 ? (sp.chunks + T - 1) / T : 1;
+    // staged mode: when every input that changes from row to row is
+    // contiguous, 16-byte aligned at every row start and at least
+    // RED_STAGE_MIN_BYTES a row, the rows come through a shared-memory ring of
+    // kNS slots per team filled by bulk copies (kNS - 1 rows in flight while
+    // the team computes); the stages and the epilogue read them from there.
+    constexpr int RED_STAGED_MAX_CHUNKS = 16, RED_STAGE_MIN_BYTES = 512;
+    constexpr int64_t RED_SMEM_PREF = 110 * 1024, RED_SMEM_MAX = 200 * 1024;
+    const int teams = RED_THREADS >> tl;
+    int staged_in[PSG_MAX_INPUTS] = {0}, seg_off[PSG_MAX_INPUTS] = {0}, row_bytes[PSG_MAX_INPUTS] = {0},
+        in_size[PSG_MAX_INPUTS] = {0};
+    int64_t stage_bytes = 0, tx_bytes = 0;
+    bool staged = ch_per <= RED_STAGED_MAX_CHUNKS && words > 0;
+    for (int k = 0; k < n_in; ++k) {
+        in_size[k] = dtype_size(dts[k]);
+        if (!cache_in[k]) continue;
+        const int es = in_size[k];
+        const bool dt_ok = dts[k] == PSG_F32 || dts[k] == PSG_I32 || dts[k] == PSG_BF16 || dts[k] == PSG_F16;
+        bool ok = dt_ok && modes[k] == PSG_M_CONTIG && P->p.in[k].inner_stride == 1 &&
+                  ((uintptr_t)in[k] + (uint64_t)P->p.in[k].offset * es) % 16 == 0 && (sp.inner * es) % 16 == 0;
+        for (int d = 0; d + 1 < sp.nd && ok; ++d)
+            if (sp.shape[d] > 1 && (P->p.in[k].outer_stride[d] * es) % 16 != 0) ok = false;
+        if (!ok) staged = false;
+        staged_in[k] = 1;
+        seg_off[k] = (int)stage_bytes;
+        row_bytes[k] = (int)(sp.inner * es);
+        stage_bytes += (sp.chunks * PSG_VEC * es + 127) / 128 * 128;
+        tx_bytes += sp.inner * es;
+    }
+    if (tx_bytes < RED_STAGE_MIN_BYTES) staged = false;
+    int ns = 4;
+    const int64_t bar_bytes = ((int64_t)teams * 4 * 8 + 127) / 128 * 128;
+    while (ns > 2 && bar_bytes + teams * ns * stage_bytes > RED_SMEM_PREF) --ns;
+    if (bar_bytes + teams * ns * stage_bytes > RED_SMEM_MAX) staged = false;
+    if (!staged) {
+        for (int k = 0; k < n_in; ++k) staged_in[k] = 0;
+        stage_bytes = tx_bytes = 0;
+        ns = 1;
+    } else {
+        for (int k = 0; k < n_in; ++k) cache_in[k] = 0;  // the ring holds the row
+        words = 0;
+    }
+    P->smem = staged ? (int)(bar_bytes + teams * ns * stage_bytes) : 0;
+    if (stash >= 0 && ch_per * (words + PSG_VEC) > RED_CACHE_WORDS) stash = -1;
+    const int kch = ch_per * words <= RED_CACHE_WORDS || staged ? (int)ch_per : 0;
+    if (kch == 0) stash = -1;
+    const int stash_node = stash >= 0 ? stages[stash].n_nodes - 1 : -1;
+    // resident blocks the launch bound asks registers for: what the ring
+    // leaves room for in staged mode, else 4 (measured best for the softmax
+    // and RMSNorm rows)
+    int min_blocks = 4;
+    if (staged) {
+        min_blocks = (int)((227 * 1024) / (P->smem + 1024));
+        min_blocks = min_blocks < 1 ? 1 : min_blocks > 4 ? 4 : min_blocks;
+    }
+    bodies += gen_eval(epi, E, "Epi", "", stash_node);
     P->block = RED_THREADS;
     P->p.rows = sp.rows;
     P->p.inner = sp.inner;
@@ -153,6 +235,20 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     spec += "constexpr int kStageOp[] = " + int_list(sop, n_stages) + ";\n";
     spec += "constexpr int kStageDt[] = " + int_list(sdt, n_stages) + ";\n";
     spec += "constexpr int kCH = " + std::to_string(kch) + ";\n";
+    spec += "constexpr int kCacheIn[] = " + int_list(cache_in, n_in) + ";\n";
+    spec += "constexpr int kStash = " + std::to_string(stash) + ";\n";
+    spec += "constexpr int kMinBlocks = " + std::to_string(min_blocks) + ";\n";
+    const bool exact = kch > 0 && sp.inner % PSG_VEC == 0 && sp.chunks == (int64_t)kch * T;
+    spec += "constexpr bool kExact = " + std::string(exact ? "true" : "false") + ";\n";
+    spec += "constexpr int kStaged = " + std::to_string(staged ? 1 : 0) + ";\n";
+    spec += "constexpr int kNS = " + std::to_string(ns) + ";\n";
+    spec += "constexpr int kStageBytes = " + std::to_string(stage_bytes) + ";\n";
+    spec += "constexpr int kBarBytes = " + std::to_string(staged ? bar_bytes : 0) + ";\n";
+    spec += "constexpr u32 kTxBytes = " + std::to_string(tx_bytes) + "u;\n";
+    spec += "constexpr int kStagedIn[] = " + int_list(staged_in, n_in) + ";\n";
+    spec += "constexpr int kSegOff[] = " + int_list(seg_off, n_in) + ";\n";
+    spec += "constexpr u32 kRowBytes[] = " + int_list(row_bytes, n_in) + ";\n";
+    spec += "constexpr int kInSize[] = " + int_list(in_size, n_in) + ";\n";
     spec += "constexpr int kPerRow = " + std::to_string(per_row ? 1 : 0) + ";\n";
     spec += "template <int S> struct StageBody;\n";
     spec += bodies;
@@ -164,8 +260,25 @@ psg_status grid_for(const RedPlan& P, cudaKernel_t k, int* grid)
 {
     const int teams = P.block >> P.p.team_log2;
     const int64_t need = (P.p.rows + teams - 1) / teams;
-    const int per_sm = jit_max_blocks_per_sm(k, P.block, 0);
-    *grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)num_sms() * per_sm));
+    const int per_sm = jit_max_blocks_per_sm(k, P.block, (size_t)P.smem);
+    *grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1)));
+    return PSG_OK;
+}
+
+// A staged kernel's ring needs more than the default 48 KB of dynamic shared
+// memory: opt in once per (kernel, device).
+psg_status allow_smem(cudaKernel_t k, int bytes)
+{
+    if (bytes <= 48 * 1024) return PSG_OK;
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> done;
+    const uint64_t key = (uint64_t)(uintptr_t)k ^ ((uint64_t)current_device() << 56);
+    std::lock_guard<std::mutex> g(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return PSG_OK;
+    if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return PSG_E_CUDA;
+    done[key] = bytes;
     return PSG_OK;
 }
 
@@ -183,9 +296,11 @@ psg_status query_reduce(const psg_reduce_stage* stages, int n_stages, const psg_
     cudaKernel_t k;
     st = jit_kernel(JIT_REDUCE, P.spec, "psg_reduce", &k);
     if (st != PSG_OK) return st;
+    st = allow_smem(k, P.smem);
+    if (st != PSG_OK) return st;
     grid_for(P, k, grid);
     *block = P.block;
-    *smem = 0;
+    *smem = P.smem;
     *regs = jit_regs(k);
     return PSG_OK;
 }
@@ -198,18 +313,21 @@ extern "C" psg_status psg_reduce_rows(const psg_reduce_stage* stages, int n_stag
                                       int n_epi, const void* const* in, const psg_view* in_v, int n_in,
                                       void* out, const psg_view* out_v, int32_t* d_status, void* stream)
 {
-    (void)d_status;
     RedPlan P;
     psg_status st = plan_reduce(stages, n_stages, epilogue, n_epi, in, in_v, n_in, out, out_v, &P);
     if (st != PSG_OK) return st;
     if (P.p.rows == 0) return PSG_OK;
+    P.p.status = d_status;
     cudaKernel_t k;
     st = jit_kernel(JIT_REDUCE, P.spec, "psg_reduce", &k);
+    if (st != PSG_OK) return st;
+    st = allow_smem(k, P.smem);
     if (st != PSG_OK) return st;
     int grid;
     grid_for(P, k, &grid);
     void* args[] = {(void*)&P.p};
-    if (cudaLaunchKernel((const void*)k, dim3(grid), dim3(P.block), args, 0, (cudaStream_t)stream) != cudaSuccess)
+    if (cudaLaunchKernel((const void*)k, dim3(grid), dim3(P.block), args, (size_t)P.smem, (cudaStream_t)stream) !=
+        cudaSuccess)
         return PSG_E_CUDA;
     return PSG_OK;
 }

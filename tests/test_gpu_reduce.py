@@ -135,6 +135,37 @@ def test_max_specials_bit_exact(A, O):
     assert np.array_equal(np.nan_to_num(got), np.nan_to_num(ref))
 
 
+@pytest.mark.parametrize("N", [1000, 1024, 4096, 5000])
+def test_max_specials_long_rows(A, O, N):
+    """Signed zeros, NaNs and -inf spread over rows long enough for warp and
+    block folds (and the staged ring): MAX must match the oracle's sign bit
+    and NaN-ness in every row whatever the fold order."""
+    g = SI.gen(N)
+    R = 12
+    x = torch.where(torch.rand((R, N), generator=g) < 0.5, torch.tensor(-0.0), torch.tensor(0.0))
+    x[0] = -0.0                                             # all -0 -> -0
+    x[1] = -0.0
+    x[1, int(torch.randint(0, N, (1,), generator=g))] = 0.0  # a single +0 wins
+    x[2] = float("-inf")                                     # all -inf
+    x[3, int(torch.randint(0, N, (1,), generator=g))] = float("nan")
+    x[4] = -0.0
+    x[4, -1] = float("nan")                                  # NaN in the last cell
+    x[5] = -torch.rand((N,), generator=g) - 1.0              # all negative
+    x[6] = -torch.rand((N,), generator=g) - 1.0
+    x[6, 0] = float("nan")                                   # NaN in the first cell
+    x[7] = float("-inf")
+    x[7, N // 2] = -0.0
+    dx = dev(x)
+    out = torch.empty((R,), device="cuda")
+    A.psg_reduce_rows([(A.RED_MAX, [A.node("LOAD", 0)])], None, [dx], [A.view_of(dx)], out, A.view_of(out))
+    torch.cuda.synchronize()
+    ref = O.reduce_max(O.T(x.numpy(), "f32"), keepdim=False).data
+    got = out.cpu().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.signbit(got[~np.isnan(got)]), np.signbit(ref[~np.isnan(ref)]))
+    assert np.array_equal(np.nan_to_num(got), np.nan_to_num(ref))
+
+
 def test_strided_and_broadcast_inputs(A, O):
     g = SI.gen(9)
     base = SI.normal((300 * 40,), 0, 1, g)
