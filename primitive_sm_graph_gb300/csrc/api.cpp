@@ -36,6 +36,15 @@ int fill_operand(PsgOperand& op, const void* ptr, const psg_view* v, const Space
                                                                                      : PSG_M_STRIDED;
 }
 
+int vec_mode(int mode, const PsgOperand& op, int es, const Space& sp)
+{
+    if (mode != PSG_M_CONTIG || op.inner_stride != 1) return mode;
+    if (((uintptr_t)op.ptr + (uint64_t)op.offset * es) % 16 != 0) return mode;
+    for (int d = 0; d + 1 < sp.nd; ++d)
+        if (sp.shape[d] > 1 && (op.outer_stride[d] * es) % 16 != 0) return mode;
+    return PSG_M_VEC;
+}
+
 bool same_shape(const psg_view* a, const psg_view* b)
 {
     if (a->ndim != b->ndim) return false;

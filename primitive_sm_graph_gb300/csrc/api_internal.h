@@ -13,6 +13,10 @@ bool same_shape(const psg_view* a, const psg_view* b);
 // returns its addressing mode (PSG_M_*).
 int fill_operand(PsgOperand& op, const void* ptr, const psg_view* v, const Space& sp,
                  const int64_t* st, const int64_t* lo, const int64_t* hi, bool masked);
+// PSG_M_VEC in place of PSG_M_CONTIG when the operand's base and every row
+// start are 16-byte aligned (es: element size): the kernels then move whole
+// chunks with vector loads and stores and test nothing at run time.
+int vec_mode(int mode, const PsgOperand& op, int es, const Space& sp);
 
 struct EwPlan {
     PsgEwParams p;

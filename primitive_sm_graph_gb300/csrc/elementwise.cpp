@@ -79,9 +79,11 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
     for (int k = 0; k < n_in; ++k) {
         modes[k] = fill_operand(P->p.in[k], in[k], &in_v[k], sp, strides[1 + k], lo[1 + k], hi[1 + k],
                                 masked[1 + k]);
+        modes[k] = vec_mode(modes[k], P->p.in[k], dtype_size(dts[k]), sp);
         uni[k] = modes[k] == PSG_M_UNIFORM;
     }
-    fill_operand(P->p.out, out, out_v, sp, strides[0], lo[0], hi[0], false);
+    const int out_mode = vec_mode(fill_operand(P->p.out, out, out_v, sp, strides[0], lo[0], hi[0], false),
+                                  P->p.out, dtype_size(out_v->dtype), sp);
     ProgInfo I;
     st = analyze_program(prog, n_nodes, dts, uni, n_in, nullptr, 0, &I);
     if (st != PSG_OK) return st;
@@ -103,6 +105,7 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
     }
     spec += m + "};\n" + d + "};\n";
     spec += "constexpr int kOutDt = " + std::to_string(out_v->dtype) + ";\n";
+    spec += "constexpr int kOutMode = " + std::to_string(out_mode) + ";\n";
     spec += std::string("constexpr bool kExact = ") + (sp.inner % PSG_VEC == 0 ? "true" : "false") + ";\n";
     spec += gen_eval(prog, I, "Body");
     P->spec = std::move(spec);

@@ -59,7 +59,7 @@ extern "C" __global__ void __launch_bounds__(256) psg_ew(const __grid_constant__
             const EwCtx c{p, roff, rok, col0, nvalid};
             typename VT<kOutDt>::T y[PSG_VEC];
             Body::eval(c, u, y);
-            st_chunk<kOutDt>(p.out, ooff, col0, nvalid, y);
+            st_chunk<kOutDt, kOutMode>(p.out, ooff, col0, nvalid, y);
         }
     }
 }

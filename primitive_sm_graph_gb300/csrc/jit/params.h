@@ -23,6 +23,7 @@
 #define PSG_M_CONTIG 1   /* inner stride 1, unmasked: vector loads when aligned */
 #define PSG_M_STRIDED 2  /* any inner stride, unmasked */
 #define PSG_M_MASKED 3   /* masked somewhere: per-cell range checks */
+#define PSG_M_VEC 4      /* contiguous, every row start 16-byte aligned: vector moves only */
 
 struct PsgOperand {
     const void* ptr;

@@ -88,11 +88,11 @@ __device__ __forceinline__ void ld_chunk(const PsgOperand& op, i64 roff, bool ro
         const T x = ld_cell<DT>(op.ptr, roff);
 #pragma unroll
         for (int v = 0; v < PSG_VEC; ++v) d[v] = x;
-    } else if constexpr (MODE == PSG_M_CONTIG) {
+    } else if constexpr (MODE == PSG_M_CONTIG || MODE == PSG_M_VEC) {
         const i64 b = roff + col0;
         if constexpr (DT == PSG_DT_F32 || DT == PSG_DT_I32) {
             const T* q = (const T*)op.ptr + b;
-            if (nvalid == PSG_VEC && (((unsigned long long)q) & 15) == 0) {
+            if (nvalid == PSG_VEC && (MODE == PSG_M_VEC || (((unsigned long long)q) & 15) == 0)) {
                 const uint4 x = __ldg((const uint4*)q), y = __ldg((const uint4*)q + 1);
                 const u32 w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
@@ -104,7 +104,7 @@ __device__ __forceinline__ void ld_chunk(const PsgOperand& op, i64 roff, bool ro
             }
         } else if constexpr (DT == PSG_DT_I8) {
             const signed char* q = (const signed char*)op.ptr + b;
-            if (nvalid == PSG_VEC && (((unsigned long long)q) & 7) == 0) {
+            if (nvalid == PSG_VEC && (MODE == PSG_M_VEC || (((unsigned long long)q) & 7) == 0)) {
                 const uint2 x = __ldg((const uint2*)q);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
@@ -115,7 +115,7 @@ __device__ __forceinline__ void ld_chunk(const PsgOperand& op, i64 roff, bool ro
             }
         } else {
             const u16* q = (const u16*)op.ptr + b;
-            if (nvalid == PSG_VEC && (((unsigned long long)q) & 15) == 0) {
+            if (nvalid == PSG_VEC && (MODE == PSG_M_VEC || (((unsigned long long)q) & 15) == 0)) {
                 const uint4 x = __ldg((const uint4*)q);
                 const u32 w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -164,15 +164,16 @@ __device__ __forceinline__ typename VT<DT>::T ld_first(const PsgOperand& op, i64
 }
 
 // store PSG_VEC cells; vector stores for contiguous, full, aligned runs
-template <int DT>
+// (MODE == PSG_M_VEC: known aligned, nothing is tested)
+template <int DT, int MODE>
 __device__ __forceinline__ void st_chunk(const PsgOperand& op, i64 roff, i64 col0, int nvalid,
                                          const typename VT<DT>::T (&y)[PSG_VEC])
 {
-    if (op.inner_stride == 1 && nvalid == PSG_VEC) {
+    if ((MODE == PSG_M_VEC || op.inner_stride == 1) && nvalid == PSG_VEC) {
         const i64 b = roff + col0;
         if constexpr (DT == PSG_DT_F32 || DT == PSG_DT_I32) {
             u32* q = (u32*)op.ptr + b;
-            if ((((unsigned long long)q) & 15) == 0) {
+            if (MODE == PSG_M_VEC || (((unsigned long long)q) & 15) == 0) {
                 u32 w[8];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
@@ -185,7 +186,7 @@ __device__ __forceinline__ void st_chunk(const PsgOperand& op, i64 roff, i64 col
             }
         } else if constexpr (DT == PSG_DT_BF16 || DT == PSG_DT_F16 || DT == PSG_DT_I16) {
             u16* q = (u16*)op.ptr + b;
-            if ((((unsigned long long)q) & 15) == 0) {
+            if (MODE == PSG_M_VEC || (((unsigned long long)q) & 15) == 0) {
                 u32 w[4];
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {

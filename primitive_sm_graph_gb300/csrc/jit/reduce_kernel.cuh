@@ -379,7 +379,7 @@ extern "C" __global__ void __launch_bounds__(256, kMinBlocks) psg_reduce(const _
                         const RedCtx c{p, roff, rok, cache, stash, red, sb, col0, nvalid, j};
                         typename VT<kOutDt>::T y[PSG_VEC];
                         Epi::eval(c, u, y);
-                        st_chunk<kOutDt>(p.out, ooff, col0, nvalid, y);
+                        st_chunk<kOutDt, kOutMode>(p.out, ooff, col0, nvalid, y);
                     }
                 }
             }

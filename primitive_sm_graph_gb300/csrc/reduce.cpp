@@ -95,9 +95,11 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     for (int k = 0; k < n_in; ++k) {
         modes[k] = fill_operand(P->p.in[k], in[k], &in_v[k], sp, strides[1 + k], lo[1 + k], hi[1 + k],
                                 masked[1 + k]);
+        modes[k] = vec_mode(modes[k], P->p.in[k], dtype_size(dts[k]), sp);
         uni[k] = modes[k] == PSG_M_UNIFORM;
     }
-    fill_operand(P->p.out, out, &ov, sp, strides[0], lo[0], hi[0], false);
+    const int out_mode = vec_mode(fill_operand(P->p.out, out, &ov, sp, strides[0], lo[0], hi[0], false),
+                                  P->p.out, dtype_size(out_v->dtype), sp);
     // stages
     std::string bodies;
     int sop[MAX_STAGES], sdt[MAX_STAGES];
@@ -181,7 +183,7 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
         if (!cache_in[k]) continue;
         const int es = in_size[k];
         const bool dt_ok = dts[k] == PSG_F32 || dts[k] == PSG_I32 || dts[k] == PSG_BF16 || dts[k] == PSG_F16;
-        bool ok = dt_ok && modes[k] == PSG_M_CONTIG && P->p.in[k].inner_stride == 1 &&
+        bool ok = dt_ok && (modes[k] == PSG_M_CONTIG || modes[k] == PSG_M_VEC) && P->p.in[k].inner_stride == 1 &&
                   ((uintptr_t)in[k] + (uint64_t)P->p.in[k].offset * es) % 16 == 0 && (sp.inner * es) % 16 == 0;
         for (int d = 0; d + 1 < sp.nd && ok; ++d)
             if (sp.shape[d] > 1 && (P->p.in[k].outer_stride[d] * es) % 16 != 0) ok = false;
@@ -231,6 +233,7 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     spec += "constexpr int kInMode[] = " + int_list(modes, n_in) + ";\n";
     spec += "constexpr int kInDt[] = " + int_list(dts, n_in) + ";\n";
     spec += "constexpr int kOutDt = " + std::to_string(out_v->dtype) + ";\n";
+    spec += "constexpr int kOutMode = " + std::to_string(out_mode) + ";\n";
     spec += "constexpr int kNstages = " + std::to_string(n_stages) + ";\n";
     spec += "constexpr int kStageOp[] = " + int_list(sop, n_stages) + ";\n";
     spec += "constexpr int kStageDt[] = " + int_list(sdt, n_stages) + ";\n";
