@@ -71,6 +71,14 @@ def barrier(dist):
         dist.barrier()
 
 
+def whole_job_gbs(dist, world: int, bytes_per_rank_step: int, ms_per_step_local: float):
+    """Whole-job throughput of N replicas: every rank processes
+    bytes_per_rank_step per step, the job takes the slowest rank's time.
+    Returns (GB/s over all ranks, max ms per step)."""
+    ms = max_over_ranks(dist, ms_per_step_local)
+    return bytes_per_rank_step * world / (ms * 1e-3) / 1e9, ms
+
+
 def max_over_ranks(dist, x: float) -> float:
     if dist is None:
         return x
@@ -593,9 +601,7 @@ def main():
     with Clocks(local) as clk:
         total_ms, chain_ms, tr_ms, wall = timed_steps(step, args.steps, args.warmup, dist)
     clocks = clk.summary()
-    total_ms = max_over_ranks(dist, total_ms)
-    ms_step = total_ms / args.steps
-    value = STEP_BYTES * world / (ms_step * 1e-3) / 1e9
+    value, ms_step = whole_job_gbs(dist, world, STEP_BYTES, total_ms / args.steps)
     P = peaks()
     # dominant kernel: the one with the larger share of the step
     dom = ("transpose", TRANSPOSE_BYTES, tr_ms) if tr_ms >= chain_ms else ("chain", CHAIN_BYTES, chain_ms)
@@ -605,7 +611,7 @@ def main():
     if os.path.exists(tp):
         traffic = json.load(open(tp)).get(dom[0])
     e2e_ms, h2d, d2h = e2e_steps(step, max(3, args.steps // 4), 2)
-    e2e_gbs = STEP_BYTES * world / (max_over_ranks(dist, e2e_ms) * 1e-3) / 1e9
+    e2e_gbs, _ = whole_job_gbs(dist, world, STEP_BYTES, e2e_ms)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),

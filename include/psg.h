@@ -16,8 +16,13 @@
  * --------------------------------
  * Memory: every pointer argument named as device memory must point to memory
  *   the CUDA device can address (cudaMalloc / torch CUDA tensors).  The caller
- *   owns every buffer, workspace and stream; the library allocates no device
- *   memory, never synchronises, and keeps no mutable global state.
+ *   owns every buffer, workspace and stream; the library never synchronises
+ *   and allocates no device memory at run time.  Its one fixed device array
+ *   is the key scratch of psg_scatter_add_static, part of the library image.
+ * State: psg_elementwise and psg_reduce_rows compile a kernel per distinct
+ *   program (NVRTC, on first use) and keep it in a process-wide cache that
+ *   only grows, guarded by a mutex; per-device attribute caches likewise.
+ *   Nothing else persists between calls.
  * Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every
  *   call only enqueues work on it and returns.
  * Errors: host-side validation happens before any launch and returns a
@@ -143,8 +148,9 @@ psg_status psg_elementwise(const psg_node* prog, int n_nodes, const void* const*
 /* ---------------------------------------------------------------------------
  * psg_reduce_rows -- SUM/MAX over the last dim with fused prologue and
  * epilogue (limn, "Reading the schedule": a reduce is a cut and elementwise
- * work fuses into it; "Backends": a long reduce splits into partial totals and
- * a fold; the dtype paragraph: float32 running totals, rounded once).
+ * work fuses into it; "The op set", the dtype paragraph: float32 running
+ * totals, rounded once).  One team of threads folds each row; a row is not
+ * split across blocks, so very few very long rows use few SMs.
  *
  * Every input view has the iteration shape [R_0 .. R_{d-2}, N]; the last dim
  * is the reduced one.  Stages run in order; stage s computes, for every row r,
@@ -164,8 +170,10 @@ psg_status psg_elementwise(const psg_node* prog, int n_nodes, const void* const*
  * the reduction_order term), which is the tolerance this call is tested to.
  * stages: host array of n_stages (1..4) stage descriptors, each pointing to a
  *   host program.  epilogue: host program or NULL.
- * d_status: device int32 or NULL (this call reports nothing on the device yet;
- *   the word is accepted for a uniform signature).
+ * d_status: device int32 or NULL.  When contiguous rows are staged through
+ *   shared memory by bulk copies, a copy that has not landed after about a
+ *   second makes the kernel write PSG_E_TIMEOUT there, stop waiting and
+ *   finish (its outputs are then undefined).
  * ------------------------------------------------------------------------- */
 typedef enum { PSG_RED_SUM = 0, PSG_RED_MAX = 1 } psg_red_op;
 
