@@ -7,7 +7,8 @@ synthetic input, fully resident in HBM:
   * CONTIGUOUS(permute(1,0)) of x[8192,8192] float32 (the tiled transpose).
 The metric is fused-op HBM throughput: algorithmic bytes (every operand byte
 read once and every result byte written once) per second.  L2 is flushed
-(a write of twice the L2 size) before every timed step, outside the events.
+before every timed step, outside the events: a write of twice the L2 size,
+then a read of twice the L2 size so no dirty flush lines remain.
 
 The "rows" object of the same JSON line times the other hot-path calls on
 their own workloads, each against its own ceiling: softmax over x[4096,1024]
@@ -180,9 +181,25 @@ class Step:
         self.transpose(stream)
 
 
+class L2Flush:
+    """Empties L2 between timed iterations (outside the events): write a
+    buffer of twice the L2 size, then read a second one, so the timed kernel
+    starts with no useful lines in L2 and no dirty lines of the flush itself
+    left to write back while it runs."""
+
+    def __init__(self):
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+        n = int(2 * max(l2, 64 << 20))
+        self.w = torch.empty(n, dtype=torch.uint8, device="cuda")
+        self.r = torch.zeros(n // 4, dtype=torch.int32, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
+
+
 def l2_flush_buffer():
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    return torch.empty(int(2 * max(l2, 64 << 20)), dtype=torch.uint8, device="cuda")
+    return L2Flush()
 
 
 def timed_steps(step, K, W, dist):
@@ -191,7 +208,7 @@ def timed_steps(step, K, W, dist):
     s = torch.cuda.current_stream()
     flush = l2_flush_buffer()
     for _ in range(W):
-        flush.zero_()
+        flush()
         step.run(s.cuda_stream)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
@@ -199,7 +216,7 @@ def timed_steps(step, K, W, dist):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for k in range(K):
-        flush.zero_()
+        flush()
         ev[k][0].record(s)
         step.chain(s.cuda_stream)
         ev[k][1].record(s)
@@ -268,13 +285,13 @@ def time_events(fn, iters, warm=3, flush=None):
     s = torch.cuda.current_stream()
     for _ in range(warm):
         if flush is not None:
-            flush.zero_()
+            flush()
         fn(s.cuda_stream)
     torch.cuda.synchronize()
     ts = []
     for _ in range(iters):
         if flush is not None:
-            flush.zero_()
+            flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         fn(s.cuda_stream)
@@ -619,7 +636,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": "chain y=WHERE(CMPLT(a,b),EXP(a*0.5),LOG(b*b+1)) a[4096,4096] "
                                "b[4096] expanded + permute(1,0) of x[8192,8192] f32",
-                   "bytes_per_step": STEP_BYTES, "l2": "flushed before every step (2x L2 write)",
+                   "bytes_per_step": STEP_BYTES, "l2": "flushed before every step: 2x L2 write then 2x L2 read, outside the events",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": round(achieved, 2),
                      "peak": P["hbm"], "peak_source": P["source"] + " burst copy",
