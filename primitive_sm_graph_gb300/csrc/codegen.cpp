@@ -210,7 +210,7 @@ std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string
         case PSG_OP_NEG:
             e = isint ? wrap(dt, "negi(" + ref(x.a) + ")") : "negf(" + ref(x.a) + ")";
             break;
-        case PSG_OP_EXP: e = wrap(dt, "expf(" + ref(x.a) + ")"); break;
+        case PSG_OP_EXP: e = wrap(dt, "psg_exp(" + ref(x.a) + ")"); break;
         case PSG_OP_LOG: e = wrap(dt, "logf(" + ref(x.a) + ")"); break;
         case PSG_OP_SQRT: e = wrap(dt, "__fsqrt_rn(" + ref(x.a) + ")"); break;
         case PSG_OP_RECIP: e = wrap(dt, "__frcp_rn(" + ref(x.a) + ")"); break;

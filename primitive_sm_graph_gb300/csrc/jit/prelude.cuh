@@ -44,6 +44,33 @@ __device__ __forceinline__ float negf(float x)
 }
 __device__ __forceinline__ int w8(int x) { return (int)(signed char)(x & 0xff); }
 __device__ __forceinline__ int w16(int x) { return (int)(short)(x & 0xffff); }
+// EXP: exp(x) = 2^(x log2 e).  The product x * log2 e is carried as an
+// unevaluated sum t + tl: t = RN(x * L2E_HI), the exact rounding error of
+// that product from one FMA (Dekker's TwoProduct), plus x times the float32
+// remainder of log2 e, so tl holds everything t lost (|tl| <= 2^-16 for any
+// result that is not 0 or inf).  2^t comes from the hardware base-2
+// approximation and 2^tl = 1 + tl ln 2 to first order (the next term is
+// below 2^-33), applied with one FMA.  Results below the normal range are
+// formed 2^64 higher and scaled down once at the end, so they round once
+// into the subnormals; t outside (-160, 128) (0, inf, NaN) takes 2^t as is.
+// No branch.  The error is the base-2 approximation's plus one rounding;
+// the tests hold it to 8 float32 ulps of the C library's expf.
+__device__ __forceinline__ float psg_exp(float x)
+{
+    const float L2E_HI = __uint_as_float(0x3fb8aa3bu);  // log2(e) rounded to float32
+    const float L2E_LO = __uint_as_float(0x32a57060u);  // log2(e) - L2E_HI, rounded
+    const float LN2 = __uint_as_float(0x3f317218u);     // ln 2 rounded to float32
+    const float t = __fmul_rn(x, L2E_HI);
+    const float tl = __fmaf_rn(x, L2E_LO, __fmaf_rn(x, L2E_HI, -t));
+    const bool sub = t < -125.0f;
+    const float ts = sub ? __fadd_rn(t, 64.0f) : t;     // exact: t is a multiple of 2^-17 there
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(ts));
+    const float rc = __fmaf_rn(r, __fmul_rn(tl, LN2), r);
+    const float v = t > -160.0f && t < 128.0f ? rc : r;
+    return sub ? __fmul_rn(v, __uint_as_float(0x1f800000u) /* 2^-64 */) : v;
+}
+
 __device__ __forceinline__ int addi(int a, int b) { return (int)((u32)a + (u32)b); }
 __device__ __forceinline__ int muli(int a, int b) { return (int)((u32)a * (u32)b); }
 __device__ __forceinline__ int negi(int a) { return (int)(0u - (u32)a); }

@@ -6,11 +6,15 @@
 // lane+T, ... of PSG_VEC cells.  When the row fits (kCH chunks per thread,
 // kCH > 0) the inputs are loaded once into registers and every stage and the
 // epilogue read them from there, so the row costs one HBM read and one
-// write; otherwise every stage streams the row again.  A stage folds its prologue values per thread, then
-// across the warp with shuffles and across the team's warps through shared
-// memory in a fixed order (the same bits every run).  The running total is
-// float32 (int32 for ints) and rounds into the stage dtype once (limn, "The
-// op set": a reduce keeps its running total in float32).
+// write; otherwise every stage streams the row again.  A stage folds its
+// prologue values per thread, then across the warp with shuffles and across
+// the team's warps through shared memory in a fixed order (the same bits
+// every run).  Within a thread each
+// of the PSG_VEC lane slots keeps its own running value, so the fold is
+// PSG_VEC short chains and a three-level tree instead of one long chain.
+// The running total is float32 (int32 for ints) and rounds into the stage
+// dtype once (limn, "The op set": a reduce keeps its running total in
+// float32).
 //
 // Only inputs that change from row to row are cached (kCacheIn); bfloat16
 // cells are held packed, two to a word.  When the epilogue begins with the
@@ -40,14 +44,14 @@ constexpr int kNinP = kNin > 0 ? kNin : 1;
 constexpr int kCHP = kCH > 0 ? kCH : 1;
 
 // MAX: NaN propagates, +0 beats -0 on a tie, so any order gives the same
-// bits.  max.NaN gives a NaN when either operand is one; operands that
-// compare equal (the only case where +0 and -0 meet) keep a sign bit only
-// when both have it, and equal nonzero operands have equal bits anyway.
+// bits.  max.NaN gives a NaN when either operand is one and treats -0 as
+// below +0 (checked on this hardware for both operand orders, and by the
+// signed-zero tests across every fold layout).
 __device__ __forceinline__ float fmax_step(float acc, float x)
 {
     float m;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(m) : "f"(acc), "f"(x));
-    return acc == x ? __uint_as_float(__float_as_uint(acc) & __float_as_uint(x)) : m;
+    return m;
 }
 
 template <int OP, int DT>
@@ -325,7 +329,11 @@ extern "C" __global__ void __launch_bounds__(256, kMinBlocks) psg_reduce(const _
             constexpr int OP = kStageOp[S];
             constexpr int DT = kStageDt[S];
             typedef Fold<OP, DT> F;
-            typename VT<DT>::T acc = F::identity();
+            // one running value per lane slot v: PSG_VEC independent chains
+            // (short dependency chains), folded in a fixed tree at the end
+            typename VT<DT>::T accv[PSG_VEC];
+#pragma unroll
+            for (int v = 0; v < PSG_VEC; ++v) accv[v] = F::identity();
             const int nch = kCH > 0 ? kCH : (int)((p.chunks - lane + T - 1) / T);
             typename StageBody<S>::U u;
             if (active) {
@@ -349,10 +357,15 @@ extern "C" __global__ void __launch_bounds__(256, kMinBlocks) psg_reduce(const _
                     }
 #pragma unroll
                     for (int v = 0; v < PSG_VEC; ++v)
-                        if (kExact || v < nvalid) acc = F::step(acc, y[v]);
+                        if (kExact || v < nvalid) accv[v] = F::step(accv[v], y[v]);
                 }
             }
-            acc = team_fold<OP, DT>(acc, p.team_log2, sm);
+#pragma unroll
+            for (int w = PSG_VEC / 2; w > 0; w >>= 1) {
+#pragma unroll
+                for (int v = 0; v < w; ++v) accv[v] = F::step(accv[v], accv[v + w]);
+            }
+            const typename VT<DT>::T acc = team_fold<OP, DT>(accv[0], p.team_log2, sm);
             red[S] = as_bits(F::finish(acc));
         };
         sfor<0, kNstages>(stage);

@@ -260,3 +260,28 @@ def test_rank3_broadcast_and_empty(A, O):
     # an empty output launches nothing and succeeds
     e = torch.empty((0, 7), device="cuda")
     A.psg_elementwise([A.node("LOAD", 0)], [e], [A.view_of(e)], e, A.view_of(e))
+
+
+def test_exp_dense_sweep_within_8_ulp(A, O):
+    """EXP over every 251st float32 bit pattern of [-104, 89] (every binade,
+    overflow to inf, underflow through the subnormals to 0) plus the special
+    values, against the oracle's expf: within 8 float32 ulps, NaN for NaN."""
+    def bits(v):
+        return int(np.array([v], np.float32).view(np.int32)[0])
+    pos = np.arange(0, bits(89.0), 251, dtype=np.int64)
+    neg = np.arange(0, bits(104.0), 251, dtype=np.int64) | np.int64(0x80000000)
+    x = np.concatenate([pos, neg]).astype(np.uint32).view(np.float32)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 88.72283, 88.72284, -87.33654, -87.33655,
+                        -103.97208, -103.97209, 1e-45, -1e-45, 1e30, -1e30, 0.5, -0.5, 1.0, -1.0],
+                       dtype=np.float32)
+    x = np.concatenate([x, special])
+    dx = torch.from_numpy(x).cuda()
+    out = torch.empty_like(dx)
+    v = A.view_of(dx)
+    A.psg_elementwise([A.node("LOAD", 0), A.node("EXP", 0)], [dx], [v], out, A.view_of(out))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    ref = O.exp(O.T(x, "f32")).data
+    d = ulp_dist_f32(got, ref)
+    worst = int(np.argmax(d))
+    assert d.max() <= 8, (float(x[worst]), float(got[worst]), float(ref[worst]), int(d.max()))
