@@ -417,6 +417,16 @@ class Rows:
         return fn, lambda ms: _hbm_row("scatter", nbytes, ms, self.P,
                                        {"workload": "scatter-add of [8192,512] bf16 rows into [256,512]"})
 
+    def copy_ms(self, nbytes):
+        """A device-to-device copy moving the same bytes (half read, half
+        written) in the same harness: the practical ceiling at this size,
+        where launch and ramp costs weigh against the peak copy rate."""
+        src = torch.empty(max(1, nbytes // 2), dtype=torch.uint8, device="cuda")
+        dst = torch.empty_like(src)
+        ms = time_events(lambda s: dst.copy_(src), self.iters, flush=self.flush)
+        del src, dst
+        return ms
+
     def run_kernel_rows(self, names):
         out = {}
         for nm in names:
@@ -426,6 +436,10 @@ class Rows:
             out[nm] = fin(ms)
             del fn
             torch.cuda.empty_cache()
+            if out[nm].get("bound") == "hbm":
+                cms = self.copy_ms(out[nm]["bytes"])
+                out[nm]["copy_same_bytes_ms"] = round(cms, 5)
+                out[nm]["frac_of_copy_same_bytes"] = round(cms / ms, 4)
         return out
 
     # C1: the tiny graph, eager realize and CUDA Graph replay
@@ -452,27 +466,14 @@ class Rows:
         eager_us = (time.perf_counter() - t0) / n * 1e6
         r = {"eager_us_per_realize": round(eager_us, 2), "kernels": kernels,
              "workload": "SUM(relu(A[64,32] @ B[32,48])^2) f32"}
-        try:
-            gr = torch.cuda.CUDAGraph()
-            s = torch.cuda.Stream()
-            s.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.stream(s):
-                once()
-            torch.cuda.current_stream().wait_stream(s)
-            with torch.cuda.graph(gr):
-                once()
-            gr.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(n):
-                gr.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            r["graph_replay_us"] = round(e0.elapsed_time(e1) / n * 1e3, 3)
-        except Exception as e:  # capture is optional: report why it failed
-            r["graph_replay_us"] = None
-            r["graph_capture_error"] = str(e)[:200]
+        rep = G.Replay(lambda x, y: tiny_graph(G.Tensor.from_torch(x), G.Tensor.from_torch(y)).realize(), da, db)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            rep.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        r["graph_replay_us"] = round(e0.elapsed_time(e1) / n * 1e3, 3)
         return r
 
     # C5: one forward + backward of the GPT block through the graph layer
@@ -495,6 +496,21 @@ class Rows:
             ts.append(time.perf_counter() - t0)
             kernels = len(ex.log)
         ms = statistics.median(ts) * 1e3
+        # the same step recorded once and replayed (device time, CUDA events)
+        from primitive_sm_graph_gb300.workloads import GPT_WEIGHTS
+
+        def fwd_bwd(t, *ws):
+            loss, grads = gpt_step(t, dict(zip(GPT_WEIGHTS, ws)), H)
+            return (loss,) + tuple(grads[k] for k in GPT_WEIGHTS)
+        rep = G.Replay(fwd_bwd, dtok, *[dw[k] for k in GPT_WEIGHTS])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        e0.record()
+        for _ in range(reps):
+            rep.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        rms = e0.elapsed_time(e1) / reps
         # algorithmic flops of the contractions: 8192 tokens x 6,553,600 linear
         # + 2 x B*H*T*T*hd attention (QK^T and PV), times 3 for fwd + bwd
         Bn, T, V, D, Hh, F = (SI.GPT_SHAPES[k] for k in ("B", "T", "V", "D", "H", "F"))
@@ -503,7 +519,10 @@ class Rows:
         flops = 3 * (lin + att)
         return {"ms_per_step": round(ms, 3), "kernels_per_step": kernels, "flops": flops,
                 "achieved": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "note": "host wall clock per step, graph building and scheduling included",
+                "replay_ms_per_step": round(rms, 4),
+                "replay_achieved": round(flops / (rms * 1e-3) / 1e12, 3),
+                "note": "ms_per_step: host wall clock, graph building and scheduling included; "
+                        "replay: the recorded step relaunched (CUDA Graph), device time",
                 "workload": "1-layer byte GPT fwd+bwd B32 T256 V256 d512 H8 MLP2048 bf16"}
 
 

@@ -26,22 +26,32 @@ def tiny_graph(A: Tensor, B: Tensor) -> Tensor:
     return c.relu().square().reshape(1, -1).sum(-1, keepdim=False)
 
 
-def gpt_targets(tok: torch.Tensor, V: int):
-    """Host-side index tables of the loss (data, not arithmetic of the
-    method): row indices r = b*T + t of the positions with a next token
-    (t < T-1) and the flat indices r*V + tok[b, t+1] of their target logits.
-    The last position of each sequence has no target and is dropped."""
-    Bn, T = tok.shape
-    t = np.arange(T - 1)
-    rows = (np.arange(Bn)[:, None] * T + t[None, :]).reshape(-1)
-    tgt = tok[:, 1:].cpu().numpy().reshape(-1)
-    pick = rows * V + tgt
-    return torch.from_numpy(pick.astype(np.int32))
-
-
 def causal_mask(T: int) -> torch.Tensor:
     """[T, T] float32: 1 where key j <= query i (data for WHERE)."""
     return torch.tril(torch.ones((T, T), dtype=torch.float32))
+
+
+_STATIC = {}
+
+
+def _static(key, make, device):
+    """Shape-only tables (no data in them) kept on the device, so a recorded
+    step (Replay) reads them from the same place every replay."""
+    k = key + (str(device),)
+    if k not in _STATIC:
+        _STATIC[k] = make().to(device)
+    return _STATIC[k]
+
+
+def target_index(tok: Tensor, V: int, device) -> Tensor:
+    """Flat indices r*V + tok[b, t+1] of the target logits, for positions
+    t < T-1 (r = b*T + t), computed on the device as an int32 ADD of a
+    shape-only table of r*V and the shifted token View."""
+    Bn, T = tok.shape
+    base = _static(("rowbase", Bn, T, V), lambda: torch.from_numpy(
+        ((np.arange(Bn)[:, None] * T + np.arange(T - 1)[None, :]) * V).astype(np.int32)), device)
+    nxt = tok.shrink(((0, Bn), (1, T)))
+    return (Tensor.from_torch(base) + nxt).reshape(Bn * (T - 1))
 
 
 def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,
@@ -55,11 +65,10 @@ def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,
     V, D = w["E"].shape
     hd = D // H
     BT = Bn * T
-    dev = tok.device
-    if pick is None:
-        pick = gpt_targets(tok, V).to(dev)
+    tok_t = Tensor.from_torch(tok)
+    pick_t = target_index(tok_t, V, tok.device) if pick is None else Tensor.from_torch(pick)
     if mask is None:
-        mask = causal_mask(T).to(dev)
+        mask = _static(("causal", T), lambda: causal_mask(T), tok.device)
     idx = Tensor.from_torch(tok.reshape(-1))
     h0 = (w["E"].gather(idx).reshape(Bn, T, D) + w["P"].reshape(1, T, D)).reshape(BT, D)
 
@@ -88,8 +97,8 @@ def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,
     # head and loss
     logits = h2.rmsnorm(w["gf"], eps).matmul(w["Wlm"]).cast("f32")
     lsm = logits.log_softmax(-1)
-    picked = lsm.reshape(BT * V, 1).gather(Tensor.from_torch(pick))
-    n = pick.shape[0]
+    picked = lsm.reshape(BT * V, 1).gather(pick_t)
+    n = pick_t.shape[0]
     return picked.reshape(1, n).sum(-1, keepdim=False) * (-1.0 / n)
 
 
