@@ -266,6 +266,7 @@ def e2e_steps(step, K, W):
 # ------------------------------------------------------ the other rows ----
 
 FP32_LANES_PER_SM = 128   # FFMA lanes per SM (Blackwell SM: 4 partitions x 32)
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 tensor rates
 
 
 def fp32_alu_peak():
@@ -371,19 +372,24 @@ class Rows:
                     "workload": "bf16 A[8192,8192] @ B[8192,8192] as MUL+SUM, f32 accumulate, bf16 out"}
         return fn, fin
 
-    # C4b: f32 A,B [4096,4096] -> f32 (FFMA)
+    # C4b: f32 A,B [4096,4096] -> f32: 3xTF32 on the tensor cores
     def gemm_f32(self):
         a, b = SI.contraction_f32(0)
         fn, flops = self._contract(a.cuda(), b.cuda(), torch.float32)
-        pk = fp32_alu_peak()
+        tf32 = self.P["bf16"] * TF32_PER_BF16
+        ffma = fp32_alu_peak()
 
         def fin(ms):
-            tf = flops / (ms * 1e-3) / 1e12
+            tf = flops / (ms * 1e-3) / 1e12          # float32 MUL+SUM flops per second
+            pipe = 3 * tf                            # TF32 tensor flops issued (three products per term)
             return {"ms": round(ms, 5), "flops": flops, "achieved": round(tf, 2), "unit": "TFLOP/s",
-                    "bound": "alu", "peak": round(pk, 2),
-                    "peak_source": "derived: SMs x 128 FFMA lanes x 2 x max SM clock",
-                    "frac": round(tf / pk, 4),
-                    "workload": "f32 A[4096,4096] @ B[4096,4096] as MUL+SUM (FFMA)"}
+                    "bound": "tensor", "peak": round(tf32 / 3, 2),
+                    "peak_source": "measured cuBLAS bf16 burst x nominal TF32/bf16 ratio (1.1/2.25), "
+                                   "divided by the 3 TF32 products per float32 term",
+                    "frac": round(pipe / tf32, 4),
+                    "tf32_pipe_tflops": round(pipe, 2),
+                    "ffma_ceiling": round(ffma, 2), "vs_ffma_ceiling": round(tf / ffma, 3),
+                    "workload": "f32 A[4096,4096] @ B[4096,4096] as MUL+SUM (3xTF32, f32 accumulate)"}
         return fn, fin
 
     # C5 shapes: token embedding gather and its scatter-add backward

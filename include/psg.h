@@ -282,11 +282,14 @@ psg_status psg_scatter_add_static(void* dst, const psg_view* dv, const int32_t* 
  * before launch).  call: one of psg_call; v: the output view the call would
  * write (for PSG_CALL_CONTRACT: Cv).  Writes grid (blocks), block (threads),
  * dynamic shared memory bytes and registers per thread of the kernel chosen.
+ * A float32 contraction runs on the tensor cores as 3xTF32 when K >= 256
+ * and both operands are TMA-addressable (PSG_CALL_CONTRACT_F32_TENSOR),
+ * else on the FP32 pipes (PSG_CALL_CONTRACT_F32).
  * ------------------------------------------------------------------------- */
 typedef enum {
     PSG_CALL_ELEMENTWISE = 0, PSG_CALL_REDUCE_ROWS = 1, PSG_CALL_PERMUTE = 2,
     PSG_CALL_CONTRACT_BF16 = 3, PSG_CALL_CONTRACT_F32 = 4, PSG_CALL_GATHER = 5,
-    PSG_CALL_SCATTER_ADD = 6
+    PSG_CALL_SCATTER_ADD = 6, PSG_CALL_CONTRACT_F32_TENSOR = 7
 } psg_call;
 
 psg_status psg_query_launch(int call, const psg_view* v, int* grid, int* block, int* smem,

@@ -36,7 +36,7 @@ OPS = {"LOAD": 0, "CONST": 1, "RED": 2, "NEG": 3, "EXP": 4, "LOG": 5, "SQRT": 6,
        "CAST": 8, "ADD": 9, "MUL": 10, "CMPLT": 11, "WHERE": 12}
 RED_SUM, RED_MAX = 0, 1
 CALLS = {"elementwise": 0, "reduce_rows": 1, "permute": 2, "contract_bf16": 3,
-         "contract_f32": 4, "gather": 5, "scatter_add": 6}
+         "contract_f32": 4, "gather": 5, "scatter_add": 6, "contract_f32_tensor": 7}
 
 
 class psg_view(ctypes.Structure):

@@ -88,14 +88,19 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
     const int64_t b_ns = Bv->strides[dn], b_ks = Bv->strides[dk];
     const int64_t c_ms = Cv->strides[dm], c_ns = Cv->strides[dn];
     const int64_t batch = bt->nb == 1 ? bt->shape[0] : 1;
-    // tensor-core path: bf16, one (collapsed) batch dim, TMA-addressable operands
-    bool tc = adt == PSG_BF16 && bt->nb <= 1 && K > 0;
+    // tensor-core paths, one (collapsed) batch dim, TMA-addressable operands:
+    // bf16 (one MMA per term) and float32 with K >= TF32X3_MIN_K (three TF32
+    // MMAs per term; shorter K keeps the exact-product FP32-pipe kernel,
+    // whose only error is the reduction order)
+    constexpr int64_t TF32X3_MIN_K = 256;
+    bool tc = (adt == PSG_BF16 || (adt == PSG_F32 && K >= TF32X3_MIN_K)) && bt->nb <= 1 && K > 0;
+    const int es = dtype_size(adt), q16 = 16 / es;  // elements per 16 bytes
     auto tma_ok = [&](const void* base, int64_t off, int64_t s_mn, int64_t s_k, int64_t mn, int64_t s_b, bool& kmaj) {
-        if (s_k == 1 && s_mn % 8 == 0 && s_mn >= K) kmaj = true;
-        else if (s_mn == 1 && s_k % 8 == 0 && s_k >= mn) kmaj = false;
+        if (s_k == 1 && s_mn % q16 == 0 && s_mn >= K) kmaj = true;
+        else if (s_mn == 1 && s_k % q16 == 0 && s_k >= mn) kmaj = false;
         else return false;
-        if (batch > 1 && (s_b % 8 != 0 || s_b <= 0)) return false;
-        return al16(base, off, 2);
+        if (batch > 1 && (s_b % q16 != 0 || s_b <= 0)) return false;
+        return al16(base, off, es);
     };
     bool akm = true, bkm = true;
     tc = tc && tma_ok(A, Av->offset, a_ms, a_ks, M, bt->nb ? bt->sa[0] : 0, akm);
@@ -116,8 +121,8 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
         T->p.c_rs = c_ms;
         T->p.c_cs = c_ns;
         T->p.c_bs = bt->nb ? bt->sc[0] : 0;
-        T->A = (const char*)A + Av->offset * 2;
-        T->B = (const char*)Bp + Bv->offset * 2;
+        T->A = (const char*)A + Av->offset * es;
+        T->B = (const char*)Bp + Bv->offset * es;
         T->a_ms = a_ms;
         T->a_ks = a_ks;
         T->a_bs = bt->nb ? bt->sa[0] : 0;
@@ -168,7 +173,10 @@ extern "C" psg_status psg_contract(const void* A, const psg_view* Av, const void
         // an empty SUM is its identity: every cell 0 (through the SIMT kernel)
         return launch_contract_simt(S, stream);
     }
-    if (bt.nb <= 1) return tc ? launch_contract_tc(T, stream) : launch_contract_simt(S, stream);
+    if (bt.nb <= 1) {
+        if (!tc) return launch_contract_simt(S, stream);
+        return S.ab_dtype == PSG_BF16 ? launch_contract_tc(T, stream) : launch_contract_tf32(T, stream);
+    }
     // several batch dims that do not merge: one launch per batch index
     int64_t count = 1;
     for (int d = 0; d < bt.nb; ++d) count *= bt.shape[d];

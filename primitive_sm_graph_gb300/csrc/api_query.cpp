@@ -68,6 +68,13 @@ extern "C" psg_status psg_query_launch(int call, const psg_view* v, int* grid, i
         query_contract_tc(tiles, grid, block, smem, regs);
         return PSG_OK;
     }
+    case PSG_CALL_CONTRACT_F32_TENSOR: {
+        if (v->ndim < 2) return PSG_E_INVALID_ARG;
+        int64_t tiles = ((v->shape[v->ndim - 2] + 127) / 128) * ((v->shape[v->ndim - 1] + 127) / 128);
+        for (int d = 0; d < v->ndim - 2; ++d) tiles *= v->shape[d];
+        query_contract_tf32(tiles, grid, block, smem, regs);
+        return PSG_OK;
+    }
     case PSG_CALL_CONTRACT_F32: {
         if (v->ndim < 2) return PSG_E_INVALID_ARG;
         SimtParams p;

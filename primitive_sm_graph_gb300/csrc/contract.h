@@ -36,6 +36,9 @@ struct SimtParams {
 
 psg_status launch_contract_tc(const TcOperands& o, void* stream);
 void query_contract_tc(int64_t tiles, int* grid, int* block, int* smem, int* regs);
+// float32 operands, 3xTF32 on the tensor cores (same operand rules as the bf16 path)
+psg_status launch_contract_tf32(const TcOperands& o, void* stream);
+void query_contract_tf32(int64_t tiles, int* grid, int* block, int* smem, int* regs);
 psg_status launch_contract_simt(const SimtParams& p, void* stream);
 void query_contract_simt(const SimtParams& p, int* grid, int* block, int* smem, int* regs);
 

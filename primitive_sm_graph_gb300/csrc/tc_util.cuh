@@ -1,0 +1,148 @@
+// Device helpers shared by the tensor-core contraction kernels (sm_103a):
+// mbarriers with bounded waits, TMA tile loads, shared-memory matrix
+// descriptors, tcgen05 commit / fences / TMEM loads, and the tensor-map
+// encoder entry point.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "common.h"
+
+namespace psg {
+namespace tcu {
+namespace {  // internal linkage: each kernel file gets its own copy
+
+constexpr long long WAIT_CYCLES = 2000000000ll;  // about one second
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase with this parity completed; false when
+// another role of the CTA gave up (abort set) or a second passed (then this
+// role sets abort and PSG_E_TIMEOUT in the status word).
+__device__ __noinline__ bool bar_wait(uint64_t* b, uint32_t parity, int32_t* abort, int32_t* status)
+{
+    const long long t0 = clock64();
+    for (uint32_t i = 0;; ++i) {
+        if (bar_try(b, parity)) return true;
+        if ((i & 63) == 63) {
+            if (*(volatile int32_t*)abort) return false;
+            if (clock64() - t0 > WAIT_CYCLES) {
+                *(volatile int32_t*)abort = 1;
+                if (status) atomicCAS(status, 0, (int32_t)PSG_E_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// wait for a phase with no abort check (drain paths), at most about a second
+__device__ __forceinline__ void bar_wait_drain(uint64_t* b, uint32_t parity)
+{
+    const long long t0 = clock64();
+    while (!bar_try(b, parity) && clock64() - t0 < WAIT_CYCLES) {
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// shared-memory matrix descriptor, 128B swizzle, sm_100 version field
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// tile index -> (batch, m block, n block), grouping 8 m-blocks so the CTAs of
+// one wave share A and B tiles in L2
+__device__ __forceinline__ void tile_coords(int num_m, int num_n, int t, int& b, int& mb, int& nb)
+{
+    const int per_batch = num_m * num_n;
+    b = t / per_batch;
+    const int r = t - b * per_batch;
+    const int GM = 8;
+    const int group = r / (GM * num_n);
+    const int first_m = group * GM;
+    const int gm = min(GM, num_m - first_m);
+    const int rr = r - group * GM * num_n;
+    mb = first_m + rr % gm;
+    nb = rr / gm;
+}
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    });
+    return fn;
+}
+
+}  // namespace
+}  // namespace tcu
+}  // namespace psg

@@ -161,3 +161,52 @@ def test_full_size_bf16_sampled(A, O):
 def test_full_size_f32_sampled(A, O):
     a, b = SI.contraction_f32(0)
     _sampled_full(A, O, a, b, "f32", 2000, 2)
+
+
+def _f32_tc_case(A, O, M, N, K, a_layout="mk", b_layout="kn", out_dt="f32", seed=0):
+    a, b = SI.contraction_f32(seed + M + 3 * N + 7 * K, M, N, K)
+    ref = O.matmul(O.T(a.numpy(), "f32"), O.T(b.numpy(), "f32"), "f32").data
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    dA, dB = dev(_storage(a, a_layout)), dev(_storage(b, b_layout))
+    Av, Bv = _views(A, dA, dB, M, N, K, a_layout, b_layout)
+    C = torch.empty((M, N), dtype=storage_dtype(out_dt), device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _check(O.T(to_np(C.cpu()), out_dt).f64(), ref, mag, K, out_dt)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 128, 256), (300, 200, 512), (128, 384, 1000), (1, 130, 260)])
+def test_f32_tensor_core_3xtf32(A, O, M, N, K):
+    """float32 with K >= 256 and 16-byte aligned operands: the 3xTF32
+    tensor-core kernel (ragged M, N and K tails), within the SUM bound."""
+    _f32_tc_case(A, O, M, N, K)
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [("mk", "kn"), ("km", "kn"), ("mk", "nk"), ("km", "nk")])
+def test_f32_tensor_core_every_operand_major(A, O, a_layout, b_layout):
+    _f32_tc_case(A, O, 256, 192, 512, a_layout, b_layout)
+
+
+def test_f32_tensor_core_bf16_output_and_batch(A, O):
+    _f32_tc_case(A, O, 200, 256, 384, out_dt="bf16")
+    B_, M, N, K = 3, 128, 128, 256
+    g = SI.gen(77)
+    a = SI.normal((B_, M, K), 0, 1, g)
+    b = SI.normal((B_, K, N), 0, 1, g)
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, M, N, K, batch=B_)
+    C = torch.empty((B_, M, N), device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), None)
+    torch.cuda.synchronize()
+    got = C.cpu().numpy()
+    for i in range(B_):
+        ref = O.matmul(O.T(a[i].numpy(), "f32"), O.T(b[i].numpy(), "f32"), "f32").data
+        mag = (a[i].double().abs() @ b[i].double().abs()).numpy()
+        _check(got[i], ref, mag, K, "f32")
+
+
+def test_f32_tensor_core_launch_query(A):
+    q = A.psg_query_launch("contract_f32_tensor", A.make_view("f32", (4096, 4096)))
+    assert q["block"] == 448 and q["smem"] > 190000 and 1 <= q["grid"] <= 152
