@@ -277,6 +277,36 @@ psg_status psg_scatter_add_static(void* dst, const psg_view* dv, const int32_t* 
                                   void* stream);
 
 /* ---------------------------------------------------------------------------
+ * psg_attention_fwd / psg_attention_bwd -- fused scaled dot-product attention
+ * (limn, "The op set": the fused attention op that saves L = logsumexp for
+ * its backward and a two-pass deterministic backward, in place of the
+ * composed T x T score tensors; Tiki, "Write the attention kernel at the
+ * algorithm level": the FlashAttention backward dS = P * (dO V^T - D)).
+ *
+ * Per batch b and head h, with S = scale * Q K^T and keys j > i hidden from
+ * query i when causal:
+ *     L[b,h,i] = log sum_j exp(S[i,j]),  O = exp(S - L) V;
+ *     D[i] = sum_d dO[i,d] O[i,d],  P = exp(S - L),  dS = P * (dO V^T - D),
+ *     dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
+ * Views: Q, K, V, O, dO, dQ, dK, dV are bf16 [B, T, H, 64] (head dim
+ * contiguous; batch, token and head strides multiples of 8 elements; base
+ * 16-byte aligned; no mask).  T <= 256 (one key block per head); other
+ * shapes return PSG_E_UNSUPPORTED_LAYOUT.  S and dP are float32 sums of exact
+ * bf16 products; P and dS are rounded to bf16 before the second products.
+ * lse: device float32 [B, H, T], written by fwd and read by bwd.  delta:
+ * device float32 [B, H, T] scratch of bwd (caller-owned).  scale > 0.
+ * A bounded wait that gives up writes PSG_E_TIMEOUT into d_status.
+ * ------------------------------------------------------------------------- */
+psg_status psg_attention_fwd(const void* q, const psg_view* qv, const void* k, const psg_view* kv,
+                             const void* v, const psg_view* vv, void* o, const psg_view* ov, float* lse,
+                             float scale, int causal, int32_t* d_status, void* stream);
+psg_status psg_attention_bwd(const void* q, const psg_view* qv, const void* k, const psg_view* kv,
+                             const void* v, const psg_view* vv, const void* o, const psg_view* ov,
+                             const void* dout, const psg_view* dov, const float* lse, float* delta,
+                             void* dq, const psg_view* dqv, void* dk, const psg_view* dkv, void* dv,
+                             const psg_view* dvv, float scale, int causal, int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------------------
  * psg_query_launch -- the launch a call would make, before making it (Tiki,
  * "The architecture we want": register and shared-memory budgets visible
  * before launch).  call: one of psg_call; v: the output view the call would

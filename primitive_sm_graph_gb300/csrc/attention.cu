@@ -1,0 +1,697 @@
+// Fused scaled dot-product attention on the 5th-generation tensor cores
+// (sm_103a), for one key block: T <= 256 keys, head dim 64, bfloat16.
+//
+// limn's fused attention op ("The op set": one node for the whole softmax
+// attention that saves L = logsumexp for its backward, instead of the
+// composed T x T score tensors) and Tiki's FlashAttention target ("Write the
+// attention kernel at the algorithm level").  Per (batch, head, 128-query
+// tile) one CTA:
+//   S = Q K^T           tcgen05.mma.kind::f16, M 128, N 256, K 64 -> TMEM
+//   P = exp(scale S - m) per query row (one thread per row, masked keys 0),
+//       l = its float32 sum, L = m + log l; P rounded to bf16 into shared
+//       memory
+//   O = P V / l         tcgen05.mma, M 128, N 64, K 256 -> TMEM, scaled, bf16
+// K and V arrive as the same TMA box (keys x 64, 128-byte swizzle): the
+// K-major B operand of S = Q K^T and the MN-major B operand of O = P V.
+//
+// Backward (two passes, deterministic: every gradient cell is accumulated by
+// one CTA in a fixed order, no atomics), with D = rowsum(dO * O):
+//   pass K/V (per 128-key tile, over the query tiles):
+//     S^T = K Q^T, P^T = exp(scale S^T - L), dP^T = V dO^T,
+//     dS^T = P^T (dP^T - D), dV = P^T dO, dK = scale dS^T Q
+//   pass Q (per 128-query tile, over the key tiles):
+//     S = Q K^T, P = exp(scale S - L), dP = dO V^T, dS = P (dP - D),
+//     dQ = scale dS K
+// Every mbarrier wait is bounded (about a second; PSG_E_TIMEOUT in the
+// status word, then the CTA drains and frees TMEM).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "attention.h"
+#include "launch_util.cuh"
+#include "tc_util.cuh"
+
+namespace psg {
+
+namespace {
+
+using namespace tcu;
+
+constexpr int QT = 128;                     // queries (or keys) per tile
+constexpr int KB = 256;                     // keys per block (the whole key range)
+constexpr int HD = 64;                      // head dim
+constexpr int ROW_BYTES = HD * 2;           // 128: one swizzle row
+constexpr int Q_BYTES = QT * ROW_BYTES;     // 16 KB
+constexpr int KV_BYTES = KB * ROW_BYTES;    // 32 KB
+constexpr int P_ATOM = QT * 128;            // 16 KB: 128 rows x 64 keys (bf16)
+constexpr int P_BYTES = 4 * P_ATOM;         // 64 KB: 128 rows x 256 keys
+constexpr int FWD_THREADS = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 rows
+constexpr int FWD_SMEM = 1024 + Q_BYTES + 2 * KV_BYTES + P_BYTES + 256 + 1024;
+constexpr int FWD_TMEM = 256;
+
+struct FwdBars {
+    uint64_t full, s_full, p_ready, o_full, drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(dtmem), "l"(ad), "l"(bd), "r"(idesc), "r"(accum));
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+        "[%2];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// byte offset of (row r, column j) in a K-major bf16 tile of 64-column
+// atoms (128 rows x 128 bytes each, 128-byte swizzle): atom j / 64, 16-byte
+// chunk (j % 64) / 8 stored at chunk ^ (r % 8)
+__device__ __forceinline__ uint32_t katom_off(int r, int j)
+{
+    return (uint32_t)((j >> 6) * P_ATOM + r * 128 + ((((j & 63) >> 3) ^ (r & 7)) << 4) + ((j & 7) << 1));
+}
+
+// instruction descriptor: f32 accumulate, bf16 A and B, A K-major
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *(const uint32_t*)&h;
+}
+
+__global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd(const __grid_constant__ CUtensorMap tq,
+                                                           const __grid_constant__ CUtensorMap tk,
+                                                           const __grid_constant__ CUtensorMap tv,
+                                                           const __grid_constant__ AttnParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sq = smem;                       // [128 q][64 d]
+    uint8_t* sk = sq + Q_BYTES;               // [256 keys][64 d]
+    uint8_t* sv = sk + KV_BYTES;              // [256 keys][64 d]
+    uint8_t* sp = sv + KV_BYTES;              // 4 atoms [128 q][64 keys]
+    FwdBars* bars = (FwdBars*)(sp + P_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * QT;
+
+    if (threadIdx.x == 0) {
+        bar_init(&bars->full, 1);
+        bar_init(&bars->s_full, 1);
+        bar_init(&bars->p_ready, 4);
+        bar_init(&bars->o_full, 1);
+        bar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&bars->tmem_base)), "r"(FWD_TMEM));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bar_expect_tx(&bars->full, Q_BYTES + 2 * KV_BYTES);
+            tma_load_4d(sq, &tq, &bars->full, 0, q0, h, b);
+            tma_load_4d(sk, &tk, &bars->full, 0, 0, h, b);
+            tma_load_4d(sv, &tv, &bars->full, 0, 0, h, b);
+            bar_wait_drain(&bars->full, 0u);  // the copies land before this CTA may exit
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = bar_wait(&bars->full, 0u, &bars->abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                // S = Q K^T: A = Q (K-major), B = K (K-major, N = 256 keys); K step 16 = 32 bytes
+                const uint64_t ad = sdesc(smem_u32(sq), 16u, 1024u), bd = sdesc(smem_u32(sk), 16u, 1024u);
+#pragma unroll
+                for (int k = 0; k < HD / 16; ++k)
+                    mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc_bf16(QT, KB, false), k > 0 ? 1u : 0u);
+                mma_commit(&bars->s_full);
+                ok = bar_wait(&bars->p_ready, 0u, &bars->abort, p.status);
+            }
+            if (ok) {
+                tc_fence_after();
+                // O = P V: A = P (K-major atoms of 64 keys), B = V (MN-major: rows = keys,
+                // 8-row groups 1024 B apart; a K step of 16 keys is 2 KB)
+                const uint64_t vd = sdesc(smem_u32(sv), 8192u, 1024u);
+#pragma unroll
+                for (int ks = 0; ks < KB / 16; ++ks) {
+                    const uint64_t pd = sdesc(smem_u32(sp + (ks >> 2) * P_ATOM), 16u, 1024u) + 2u * (ks & 3);
+                    mma_f16(tmem, pd, vd + 128u * ks, idesc_bf16(QT, HD, true), ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->o_full);
+            }
+            mma_commit(&bars->drain);
+            bar_wait_drain(&bars->drain, 0u);
+        }
+    } else {
+        // rows: warps 2-5 own TMEM lanes 32 (warp % 4) .. + 31 = query rows of the tile
+        const int r = 32 * (warp & 3) + lane;
+        const int i = q0 + r;
+        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        // ok stays warp-uniform: the TMEM loads below are warp-collective
+        bool ok = __all_sync(0xffffffffu, bar_wait(&bars->s_full, 0u, &bars->abort, p.status));
+        tc_fence_after();
+        const int kmax = p.causal ? min(i + 1, p.T) : p.T;  // keys 0 .. kmax-1 are visible
+        float m = -INFINITY, l = 0.0f;
+        if (ok) {
+            for (int c = 0; c < KB; c += 32) {
+                uint32_t s[32];
+                __syncwarp();
+                tmem_ld32(trow + (uint32_t)c, s);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (c + j < kmax) m = fmaxf(m, p.scale * __uint_as_float(s[j]));
+            }
+            for (int c = 0; c < KB; c += 32) {
+                uint32_t s[32];
+                __syncwarp();
+                tmem_ld32(trow + (uint32_t)c, s);
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    // l sums the float32 weights (L = m + log l is the row's
+                    // logsumexp); P is rounded to bf16 only as the MMA operand
+                    const float e0 = c + j < kmax ? __expf(p.scale * __uint_as_float(s[j]) - m) : 0.0f;
+                    const float e1 = c + j + 1 < kmax ? __expf(p.scale * __uint_as_float(s[j + 1]) - m) : 0.0f;
+                    l += e0 + e1;
+                    w[j >> 1] = pack_bf16(e0, e1);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *(uint4*)(sp + katom_off(r, c + 8 * u)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                                         w[4 * u + 3]);
+            }
+        }
+        // P (generic-proxy writes) is read by the MMAs (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) bar_arrive(&bars->p_ready);
+        if (ok) ok = __all_sync(0xffffffffu, bar_wait(&bars->o_full, 0u, &bars->abort, p.status));
+        tc_fence_after();
+        if (ok) {
+            uint32_t o[32], o2[32];
+            __syncwarp();  // every lane reaches the collective loads
+            tmem_ld32(trow, o);
+            tmem_ld32(trow + 32u, o2);
+            if (i < p.T) {
+                const float inv = 1.0f / l;
+                p.lse[((int64_t)b * p.H + h) * p.T + i] = m + logf(l);
+                __nv_bfloat16* dst = (__nv_bfloat16*)p.o + p.o_off + (int64_t)b * p.o_sb + (int64_t)i * p.o_st +
+                                     (int64_t)h * p.o_sh;
+                uint32_t w[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    w[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+                    w[16 + j] = pack_bf16(__uint_as_float(o2[2 * j]) * inv, __uint_as_float(o2[2 * j + 1]) * inv);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    ((uint4*)dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(FWD_TMEM));
+}
+
+// ---- backward ---------------------------------------------------------------
+constexpr int T_BYTES = QT * ROW_BYTES;     // 16 KB: a 128-row tile of one operand
+constexpr int G_BYTES = 2 * P_ATOM;         // 32 KB: 128 rows x 128 columns bf16 (two atoms)
+constexpr int BWD_THREADS = 192;
+constexpr int KV_SMEM = 1024 + 4 * T_BYTES + 2 * G_BYTES + 2 * QT * 4 + 256 + 1024;
+// (sized past half the SM's shared memory: with all 512 TMEM columns each,
+// a second resident CTA would only wait in tcgen05.alloc)
+constexpr int Q_SMEM = 120 * 1024;
+static_assert(1024 + 4 * T_BYTES + G_BYTES + 256 <= Q_SMEM, "pass Q shared memory");
+constexpr int BWD_TMEM = 512;
+
+struct BwdBars {
+    uint64_t full, mm1, ready, mm2, drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+// D[b, h, t] = sum_d dO[b, t, h, d] * O[b, t, h, d] (float32 total of exact
+// bf16 products, in ascending d), one warp per row
+__global__ void __launch_bounds__(256) attn_delta(const __grid_constant__ AttnTensor o,
+                                                  const __grid_constant__ AttnTensor dO,
+                                                  const __grid_constant__ AttnParams p)
+{
+    const int64_t rows = (int64_t)p.B * p.T * p.H;
+    const int lane = threadIdx.x & 31;
+    for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += (int64_t)gridDim.x * 8) {
+        const int h = (int)(r % p.H);
+        const int t = (int)((r / p.H) % p.T);
+        const int b = (int)(r / ((int64_t)p.H * p.T));
+        const __nv_bfloat162 x = ((const __nv_bfloat162*)((const __nv_bfloat16*)o.ptr + o.off + b * o.sb + t * o.st +
+                                                          h * o.sh))[lane];
+        const __nv_bfloat162 y = ((const __nv_bfloat162*)((const __nv_bfloat16*)dO.ptr + dO.off + b * dO.sb +
+                                                          t * dO.st + h * dO.sh))[lane];
+        float v = __fadd_rn(__fmul_rn(__low2float(x), __low2float(y)), __fmul_rn(__high2float(x), __high2float(y)));
+        for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane == 0) p.delta[((int64_t)b * p.H + h) * p.T + t] = v;
+    }
+}
+
+// store 64 float32 accumulator columns (scaled) of row `row` as bf16
+__device__ __forceinline__ void store_row64(const AttnTensor& t, int b, int row, int h, const uint32_t (&x)[32],
+                                            const uint32_t (&y)[32], float scale)
+{
+    __nv_bfloat16* dst = (__nv_bfloat16*)t.ptr + t.off + (int64_t)b * t.sb + (int64_t)row * t.st + (int64_t)h * t.sh;
+    uint32_t w[32];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        w[j] = pack_bf16(__uint_as_float(x[2 * j]) * scale, __uint_as_float(x[2 * j + 1]) * scale);
+        w[16 + j] = pack_bf16(__uint_as_float(y[2 * j]) * scale, __uint_as_float(y[2 * j + 1]) * scale);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) ((uint4*)dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+}
+
+// pass K/V: one CTA per (128-key tile, head, batch), over the query tiles
+// that can see its keys.  TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319,
+// dK 320-383.
+__global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kv(const __grid_constant__ CUtensorMap tq,
+                                                              const __grid_constant__ CUtensorMap tk,
+                                                              const __grid_constant__ CUtensorMap tv,
+                                                              const __grid_constant__ CUtensorMap tdo,
+                                                              const __grid_constant__ AttnTensor dk,
+                                                              const __grid_constant__ AttnTensor dv,
+                                                              const __grid_constant__ AttnParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sk = smem;                  // [128 keys][64]
+    uint8_t* sv = sk + T_BYTES;          // [128 keys][64]
+    uint8_t* sq = sv + T_BYTES;          // [128 q][64]
+    uint8_t* sdo = sq + T_BYTES;         // [128 q][64]
+    uint8_t* spt = sdo + T_BYTES;        // P^T: [128 keys][128 q] in two 64-column atoms
+    uint8_t* sdst = spt + G_BYTES;       // dS^T
+    float* sL = (float*)(sdst + G_BYTES);
+    float* sD = sL + QT;
+    BwdBars* bars = (BwdBars*)(sD + QT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int k0 = kt * QT;
+    const int nq = (p.T + QT - 1) / QT;
+    const int qt0 = p.causal ? kt : 0;
+
+    if (threadIdx.x == 0) {
+        bar_init(&bars->full, 1);
+        bar_init(&bars->mm1, 1);
+        bar_init(&bars->ready, 4);
+        bar_init(&bars->mm2, 1);
+        bar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&bars->tmem_base)), "r"(BWD_TMEM));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    bool ok = true;
+    uint32_t ph = 0;
+    for (int qt = qt0; qt < nq; ++qt, ph ^= 1u) {
+        const int q0 = qt * QT;
+        if (warp == 0) {
+            if (lane == 0) {
+                const uint32_t bytes = (qt == qt0 ? 4u : 2u) * T_BYTES;
+                bar_expect_tx(&bars->full, bytes);
+                if (qt == qt0) {
+                    tma_load_4d(sk, &tk, &bars->full, 0, k0, h, b);
+                    tma_load_4d(sv, &tv, &bars->full, 0, k0, h, b);
+                }
+                tma_load_4d(sq, &tq, &bars->full, 0, q0, h, b);
+                tma_load_4d(sdo, &tdo, &bars->full, 0, q0, h, b);
+                bar_wait_drain(&bars->full, ph);
+            }
+        } else if (warp == 1) {
+            if (lane == 0 && ok) {
+                ok = bar_wait(&bars->full, ph, &bars->abort, p.status);
+                if (ok) {
+                    tc_fence_after();
+                    const uint64_t kd = sdesc(smem_u32(sk), 16u, 1024u), vd = sdesc(smem_u32(sv), 16u, 1024u);
+                    const uint64_t qd = sdesc(smem_u32(sq), 16u, 1024u), dod = sdesc(smem_u32(sdo), 16u, 1024u);
+#pragma unroll
+                    for (int k = 0; k < HD / 16; ++k) {
+                        mma_f16(tmem, kd + 2u * k, qd + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
+                        mma_f16(tmem + 128u, vd + 2u * k, dod + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars->mm1);
+                    ok = bar_wait(&bars->ready, ph, &bars->abort, p.status);
+                }
+                if (ok) {
+                    tc_fence_after();
+                    // dV += P^T dO, dK += dS^T Q: B = dO, Q as MN-major (rows = queries)
+                    const uint64_t dob = sdesc(smem_u32(sdo), 8192u, 1024u), qb = sdesc(smem_u32(sq), 8192u, 1024u);
+#pragma unroll
+                    for (int ks = 0; ks < QT / 16; ++ks) {
+                        const uint32_t acc = (qt > qt0 || ks > 0) ? 1u : 0u;
+                        const uint64_t pa = sdesc(smem_u32(spt + (ks >> 2) * P_ATOM), 16u, 1024u) + 2u * (ks & 3);
+                        const uint64_t sa = sdesc(smem_u32(sdst + (ks >> 2) * P_ATOM), 16u, 1024u) + 2u * (ks & 3);
+                        mma_f16(tmem + 256u, pa, dob + 128u * ks, idesc_bf16(QT, HD, true), acc);
+                        mma_f16(tmem + 320u, sa, qb + 128u * ks, idesc_bf16(QT, HD, true), acc);
+                    }
+                }
+                mma_commit(&bars->mm2);  // also when giving up, so the rows never wait long
+            }
+        } else {
+            // rows: key r of the tile; columns: the tile's queries
+            const int r = 32 * (warp & 3) + lane;
+            const int j = k0 + r;
+            const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+            // L and D of the tile's queries, one per thread of the four warps
+            const int c_ = threadIdx.x - 64;
+            {
+                const int i = q0 + c_;
+                sL[c_] = i < p.T ? p.lse[((int64_t)b * p.H + h) * p.T + i] : 0.0f;
+                sD[c_] = i < p.T ? p.delta[((int64_t)b * p.H + h) * p.T + i] : 0.0f;
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four row warps only
+            const bool okw = __all_sync(0xffffffffu, bar_wait(&bars->mm1, ph, &bars->abort, p.status));
+            tc_fence_after();
+            if (okw) {
+                for (int c = 0; c < QT; c += 32) {
+                    uint32_t s[32], dp[32];
+                    __syncwarp();
+                    tmem_ld32(trow + (uint32_t)c, s);
+                    tmem_ld32(trow + 128u + (uint32_t)c, dp);
+                    uint32_t wp[16], ws[16];
+#pragma unroll
+                    for (int u = 0; u < 32; u += 2) {
+                        float pv[2], dsv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int i = q0 + c + u + e;
+                            const bool vis = i < p.T && j < p.T && (!p.causal || j <= i);
+                            const float pe = vis ? __expf(p.scale * __uint_as_float(s[u + e]) - sL[c + u + e]) : 0.0f;
+                            pv[e] = pe;
+                            dsv[e] = pe * (__uint_as_float(dp[u + e]) - sD[c + u + e]);
+                        }
+                        wp[u >> 1] = pack_bf16(pv[0], pv[1]);
+                        ws[u >> 1] = pack_bf16(dsv[0], dsv[1]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        *(uint4*)(spt + katom_off(r, c + 8 * u)) =
+                            make_uint4(wp[4 * u], wp[4 * u + 1], wp[4 * u + 2], wp[4 * u + 3]);
+                        *(uint4*)(sdst + katom_off(r, c + 8 * u)) =
+                            make_uint4(ws[4 * u], ws[4 * u + 1], ws[4 * u + 2], ws[4 * u + 3]);
+                    }
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&bars->ready);
+        }
+        // the dV / dK MMAs of this query tile finish before its tiles are replaced
+        if (!bar_wait(&bars->mm2, ph, &bars->abort, p.status)) ok = false;
+        tc_fence_after();
+        __syncthreads();
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+    }
+    if (warp >= 2) {
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        if (ok && qt0 < nq) {
+            uint32_t x[32], y[32];
+            __syncwarp();
+            tmem_ld32(trow + 256u, x);
+            tmem_ld32(trow + 288u, y);
+            if (k0 + r < p.T) store_row64(dv, b, k0 + r, h, x, y, 1.0f);
+            tmem_ld32(trow + 320u, x);
+            tmem_ld32(trow + 352u, y);
+            if (k0 + r < p.T) store_row64(dk, b, k0 + r, h, x, y, p.scale);
+        } else if (qt0 >= nq) {
+            uint32_t z[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) z[u] = 0u;
+            if (k0 + r < p.T) {
+                store_row64(dv, b, k0 + r, h, z, z, 1.0f);
+                store_row64(dk, b, k0 + r, h, z, z, 1.0f);
+            }
+        }
+    }
+    if (warp == 1 && lane == 0) {
+        mma_commit(&bars->drain);
+        bar_wait_drain(&bars->drain, 0u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BWD_TMEM));
+}
+
+// pass Q: one CTA per (128-query tile, head, batch), over the key tiles it
+// can see.  TMEM columns: S 0-127, dP 128-255, dQ 256-319.
+__global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_q(const __grid_constant__ CUtensorMap tq,
+                                                             const __grid_constant__ CUtensorMap tk,
+                                                             const __grid_constant__ CUtensorMap tv,
+                                                             const __grid_constant__ CUtensorMap tdo,
+                                                             const __grid_constant__ AttnTensor dq,
+                                                             const __grid_constant__ AttnParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sq = smem;                  // [128 q][64]
+    uint8_t* sdo = sq + T_BYTES;         // [128 q][64]
+    uint8_t* sk = sdo + T_BYTES;         // [128 keys][64]
+    uint8_t* sv = sk + T_BYTES;          // [128 keys][64]
+    uint8_t* sds = sv + T_BYTES;         // dS: [128 q][128 keys] in two 64-column atoms
+    BwdBars* bars = (BwdBars*)(sds + G_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * QT;
+    const int nk = (p.T + QT - 1) / QT;
+    const int kt1 = p.causal ? min(qt + 1, nk) : nk;   // key tiles 0 .. kt1-1
+
+    if (threadIdx.x == 0) {
+        bar_init(&bars->full, 1);
+        bar_init(&bars->mm1, 1);
+        bar_init(&bars->ready, 4);
+        bar_init(&bars->mm2, 1);
+        bar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&bars->tmem_base)), "r"(BWD_TMEM));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const int r = 32 * (warp & 3) + lane;      // query row of the tile (row warps)
+    const int i = q0 + r;
+    float Li = 0.0f, Di = 0.0f;
+    if (warp >= 2 && i < p.T) {
+        Li = p.lse[((int64_t)b * p.H + h) * p.T + i];
+        Di = p.delta[((int64_t)b * p.H + h) * p.T + i];
+    }
+    bool ok = true;
+    uint32_t ph = 0;
+    for (int kt = 0; kt < kt1; ++kt, ph ^= 1u) {
+        const int k0 = kt * QT;
+        if (warp == 0) {
+            if (lane == 0) {
+                bar_expect_tx(&bars->full, (kt == 0 ? 4u : 2u) * T_BYTES);
+                if (kt == 0) {
+                    tma_load_4d(sq, &tq, &bars->full, 0, q0, h, b);
+                    tma_load_4d(sdo, &tdo, &bars->full, 0, q0, h, b);
+                }
+                tma_load_4d(sk, &tk, &bars->full, 0, k0, h, b);
+                tma_load_4d(sv, &tv, &bars->full, 0, k0, h, b);
+                bar_wait_drain(&bars->full, ph);
+            }
+        } else if (warp == 1) {
+            if (lane == 0 && ok) {
+                ok = bar_wait(&bars->full, ph, &bars->abort, p.status);
+                if (ok) {
+                    tc_fence_after();
+                    const uint64_t qd = sdesc(smem_u32(sq), 16u, 1024u), dod = sdesc(smem_u32(sdo), 16u, 1024u);
+                    const uint64_t kd = sdesc(smem_u32(sk), 16u, 1024u), vd = sdesc(smem_u32(sv), 16u, 1024u);
+#pragma unroll
+                    for (int k = 0; k < HD / 16; ++k) {
+                        mma_f16(tmem, qd + 2u * k, kd + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
+                        mma_f16(tmem + 128u, dod + 2u * k, vd + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars->mm1);
+                    ok = bar_wait(&bars->ready, ph, &bars->abort, p.status);
+                }
+                if (ok) {
+                    tc_fence_after();
+                    // dQ += dS K: B = K as MN-major (rows = keys)
+                    const uint64_t kb = sdesc(smem_u32(sk), 8192u, 1024u);
+#pragma unroll
+                    for (int ks = 0; ks < QT / 16; ++ks) {
+                        const uint64_t sa = sdesc(smem_u32(sds + (ks >> 2) * P_ATOM), 16u, 1024u) + 2u * (ks & 3);
+                        mma_f16(tmem + 256u, sa, kb + 128u * ks, idesc_bf16(QT, HD, true),
+                                (kt > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&bars->mm2);
+            }
+        } else {
+            const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+            const bool okw = __all_sync(0xffffffffu, bar_wait(&bars->mm1, ph, &bars->abort, p.status));
+            tc_fence_after();
+            if (okw) {
+                for (int c = 0; c < QT; c += 32) {
+                    uint32_t s[32], dp[32];
+                    __syncwarp();
+                    tmem_ld32(trow + (uint32_t)c, s);
+                    tmem_ld32(trow + 128u + (uint32_t)c, dp);
+                    uint32_t ws[16];
+#pragma unroll
+                    for (int u = 0; u < 32; u += 2) {
+                        float dsv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int j = k0 + c + u + e;
+                            const bool vis = i < p.T && j < p.T && (!p.causal || j <= i);
+                            const float pe = vis ? __expf(p.scale * __uint_as_float(s[u + e]) - Li) : 0.0f;
+                            dsv[e] = pe * (__uint_as_float(dp[u + e]) - Di);
+                        }
+                        ws[u >> 1] = pack_bf16(dsv[0], dsv[1]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        *(uint4*)(sds + katom_off(r, c + 8 * u)) =
+                            make_uint4(ws[4 * u], ws[4 * u + 1], ws[4 * u + 2], ws[4 * u + 3]);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&bars->ready);
+        }
+        if (!bar_wait(&bars->mm2, ph, &bars->abort, p.status)) ok = false;
+        tc_fence_after();
+        __syncthreads();
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+    }
+    if (warp >= 2 && ok && kt1 > 0) {
+        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        uint32_t x[32], y[32];
+        __syncwarp();
+        tmem_ld32(trow + 256u, x);
+        tmem_ld32(trow + 288u, y);
+        if (i < p.T) store_row64(dq, b, i, h, x, y, p.scale);
+    }
+    if (warp == 1 && lane == 0) {
+        mma_commit(&bars->drain);
+        bar_wait_drain(&bars->drain, 0u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BWD_TMEM));
+}
+
+// 4-D tensor map over a [B, T, H, 64] bfloat16 operand: dims {64, T, H, B},
+// box {64, rows, 1, 1}, 128-byte swizzle (one 128-byte row per token).
+bool make_map_attn(CUtensorMap* map, const AttnTensor& t, int T, int H, int B, uint32_t rows)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const void* base = (const char*)t.ptr + t.off * 2;
+    cuuint64_t dims[4] = {(cuuint64_t)HD, (cuuint64_t)T, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)(t.st * 2), (cuuint64_t)(t.sh * 2), (cuuint64_t)(t.sb * 2)};
+    cuuint32_t box[4] = {(cuuint32_t)HD, rows, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+psg_status launch_attention_fwd(const AttnTensor& q, const AttnTensor& k, const AttnTensor& v, const AttnParams& p,
+                                void* stream)
+{
+    if (p.B == 0 || p.T == 0 || p.H == 0) return PSG_OK;
+    CUtensorMap mq, mk, mv;
+    if (!make_map_attn(&mq, q, p.T, p.H, p.B, QT) || !make_map_attn(&mk, k, p.T, p.H, p.B, KB) ||
+        !make_map_attn(&mv, v, p.T, p.H, p.B, KB))
+        return PSG_E_CUDA;
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute((const void*)attn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
+    });
+    if (err != cudaSuccess) return PSG_E_CUDA;
+    const dim3 grid((unsigned)((p.T + QT - 1) / QT), (unsigned)p.H, (unsigned)p.B);
+    attn_fwd<<<grid, FWD_THREADS, FWD_SMEM, (cudaStream_t)stream>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
+}
+
+psg_status launch_attention_bwd(const AttnTensor& q, const AttnTensor& k, const AttnTensor& v, const AttnTensor& o,
+                                const AttnTensor& dO, const AttnTensor& dq, const AttnTensor& dk,
+                                const AttnTensor& dv, const AttnParams& p, void* stream)
+{
+    if (p.B == 0 || p.T == 0 || p.H == 0) return PSG_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    CUtensorMap mq, mk, mv, mdo;
+    if (!make_map_attn(&mq, q, p.T, p.H, p.B, QT) || !make_map_attn(&mk, k, p.T, p.H, p.B, QT) ||
+        !make_map_attn(&mv, v, p.T, p.H, p.B, QT) || !make_map_attn(&mdo, dO, p.T, p.H, p.B, QT))
+        return PSG_E_CUDA;
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute((const void*)attn_bwd_kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute((const void*)attn_bwd_q, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM);
+    });
+    if (err != cudaSuccess) return PSG_E_CUDA;
+    const int64_t rows = (int64_t)p.B * p.T * p.H;
+    const int dgrid = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 8);
+    attn_delta<<<dgrid, 256, 0, s>>>(o, dO, p);
+    const unsigned tiles = (unsigned)((p.T + QT - 1) / QT);
+    const dim3 grid(tiles, (unsigned)p.H, (unsigned)p.B);
+    attn_bwd_kv<<<grid, BWD_THREADS, KV_SMEM, s>>>(mq, mk, mv, mdo, dk, dv, p);
+    attn_bwd_q<<<grid, BWD_THREADS, Q_SMEM, s>>>(mq, mk, mv, mdo, dq, p);
+    return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
+}
+
+}  // namespace psg

@@ -1,0 +1,115 @@
+"""GPU parity of the fused attention calls against the attention oracle.
+
+Q, K, V are Views into one packed [B, T, 3, H, 64] bf16 buffer (the GPT
+block's qkv layout).  Bars, from the roundings the kernels make (S and dP
+are float32 sums of exact bf16 products; P and dS round to bf16 before the
+second products; outputs round once to bf16), per cell:
+  O:      |O - O*|   <= 2^-8 * sum_j P*_ij |V_jd|               + 2^-7 |O*|
+  dV:     |dV - dV*| <= 2^-8 * sum_i P*_ij |dO_id|              + 2^-7 |dV*|
+  dQ, dK: |dQ - dQ*| <= 2^-7 * scale * sum_j |P*_ij| (|dP*_ij| + |D*_i|) |K_jd| + 2^-7 |dQ*|
+with * the oracle's float64 values; L within 1e-4 + 2^-16 |L*|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as SI
+from oracle.attention import attention_bwd, attention_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    from primitive_sm_graph_gb300 import _abi
+    return _abi
+
+
+def _heads(x):
+    """[B, T, H, 64] -> [B*H, T, 64] float64."""
+    B, T, H, d = x.shape
+    return x.float().cpu().permute(0, 2, 1, 3).reshape(B * H, T, d).double().numpy()
+
+
+def _setup(A, B, T, H, seed):
+    g = SI.gen(seed)
+    qkv = SI.normal((B, T, 3, H, 64), 0, 1, g, torch.bfloat16).cuda()
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    views = [A.view_of(qkv, shape=(B, T, H, 64), strides=q.stride(), offset=i * H * 64) for i in range(3)]
+    return qkv, (q, k, v), views
+
+
+def _fwd(A, B, T, H, causal, seed):
+    qkv, (q, k, v), (qv, kv, vv) = _setup(A, B, T, H, seed)
+    o = torch.empty((B, T, H, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    scale = 0.125
+    A.psg_attention_fwd(qkv, qv, qkv, kv, qkv, vv, o, A.view_of(o), lse, scale, causal, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return qkv, (q, k, v), (qv, kv, vv), o, lse, scale
+
+
+@pytest.mark.parametrize("B,T,H,causal", [(2, 256, 2, True), (1, 200, 3, True), (2, 64, 1, True),
+                                          (1, 256, 2, False), (1, 130, 1, False)])
+def test_attention_forward_matches_oracle(A, B, T, H, causal):
+    qkv, (q, k, v), _, o, lse, scale = _fwd(A, B, T, H, causal, seed=T + H)
+    Q, K, V = _heads(q), _heads(k), _heads(v)
+    O_ref, L_ref = attention_fwd(Q, K, V, scale, causal)
+    # magnitude of each output cell: sum_j P_ij |V_jd|
+    mag = np.zeros_like(O_ref)
+    vis = np.tril(np.ones((T, T), bool)) if causal else np.ones((T, T), bool)
+    for h in range(Q.shape[0]):
+        P = np.where(vis, np.exp(scale * Q[h] @ K[h].T - L_ref[h][:, None]), 0.0)
+        mag[h] = P @ np.abs(V[h])
+    got = _heads(o)
+    tol = 2.0 ** -8 * mag + 2.0 ** -7 * np.abs(O_ref)
+    bad = np.abs(got - O_ref) > tol
+    assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:3])
+    L = lse.cpu().numpy().reshape(B * H, T)
+    assert np.all(np.abs(L - L_ref) <= 1e-4 + 2.0 ** -16 * np.abs(L_ref))
+
+
+@pytest.mark.parametrize("B,T,H,causal", [(2, 256, 2, True), (1, 200, 3, True), (1, 256, 1, False)])
+def test_attention_backward_matches_oracle(A, B, T, H, causal):
+    qkv, (q, k, v), (qv, kv, vv), o, lse, scale = _fwd(A, B, T, H, causal, seed=7 * T + H)
+    g = SI.gen(99)
+    do = SI.normal((B, T, H, 64), 0, 1, g, torch.bfloat16).cuda()
+    dqkv = torch.empty_like(qkv)
+    dq, dk, dv = dqkv[:, :, 0], dqkv[:, :, 1], dqkv[:, :, 2]
+    dviews = [A.view_of(dqkv, shape=(B, T, H, 64), strides=dq.stride(), offset=i * H * 64) for i in range(3)]
+    delta = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    A.psg_attention_bwd(qkv, qv, qkv, kv, qkv, vv, o, A.view_of(o), do, A.view_of(do), lse, delta,
+                        dqkv, dviews[0], dqkv, dviews[1], dqkv, dviews[2], scale, causal, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    Q, K, V, O, dO = _heads(q), _heads(k), _heads(v), _heads(o), _heads(do)
+    _, L_ref = attention_fwd(Q, K, V, scale, causal)
+    dq_ref, dk_ref, dv_ref = attention_bwd(Q, K, V, O, dO, L_ref, scale, causal)
+    vis = np.tril(np.ones((T, T), bool)) if causal else np.ones((T, T), bool)
+    mq, mk, mv = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for h in range(Q.shape[0]):
+        P = np.where(vis, np.exp(scale * Q[h] @ K[h].T - L_ref[h][:, None]), 0.0)
+        dP = dO[h] @ V[h].T
+        D = (dO[h] * O[h]).sum(1)
+        G = np.abs(P) * (np.abs(dP) + np.abs(D)[:, None])
+        mv[h] = P.T @ np.abs(dO[h])
+        mq[h] = scale * (G @ np.abs(K[h]))
+        mk[h] = scale * (G.T @ np.abs(Q[h]))
+    for name, got, ref, mag, c in (("dv", dv, dv_ref, mv, 2.0 ** -8), ("dq", dq, dq_ref, mq, 2.0 ** -7),
+                                   ("dk", dk, dk_ref, mk, 2.0 ** -7)):
+        g64 = _heads(got)
+        bad = np.abs(g64 - ref) > c * mag + 2.0 ** -7 * np.abs(ref)
+        assert not bad.any(), (name, int(bad.sum()), np.argwhere(bad)[:3])
+
+
+def test_attention_rejects_unsupported_shapes(A):
+    x = torch.empty((1, 300, 1, 64), dtype=torch.bfloat16, device="cuda")
+    v = A.view_of(x)
+    lse = torch.empty((300,), dtype=torch.float32, device="cuda")
+    assert A.psg_attention_fwd(x, v, x, v, x, v, x, v, lse, 0.125, True, check=False) == A.E_UNSUPPORTED_LAYOUT
+    y = torch.empty((1, 16, 1, 32), dtype=torch.bfloat16, device="cuda")
+    w = A.view_of(y)
+    assert A.psg_attention_fwd(y, w, y, w, y, w, y, w, lse, 0.125, True, check=False) == A.E_UNSUPPORTED_LAYOUT
