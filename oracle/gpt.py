@@ -16,7 +16,10 @@ are exact (bfloat16 products fit float32) and its total rounds once into
 `act`.  The softmax max is a constant of the gradient.
 
 The backward is written out by hand, node by node, as the chain rule of the
-forward above.
+forward above.  With attention="fused" the attention is the fused op instead
+of its composition: exact softmax attention (oracle/attention.py, float64)
+between bf16-rounded inputs and a bf16-rounded output, and likewise its
+gradients.
 """
 from __future__ import annotations
 
@@ -46,7 +49,7 @@ def _rows(x: T, n: int) -> T:
 
 class GPTOracle:
     def __init__(self, tok: np.ndarray, w: dict, H: int, act="bf16", acc="f32", eps=1e-6,
-                 relu_mask: np.ndarray | None = None):
+                 relu_mask: np.ndarray | None = None, attention: str = "composed"):
         self.tok = np.asarray(tok, np.int32)
         self.B, self.T = self.tok.shape
         self.w = w                     # name -> oracle T (dtype act)
@@ -60,6 +63,11 @@ class GPTOracle:
         # pre-activations differ by rounding can disagree on units at ~0;
         # handing the other run's mask in compares the rest like for like.
         self.relu_mask = relu_mask
+        # "composed": scores, mask, softmax and the weighted sum as nodes;
+        # "fused": the fused attention op, defined as exact (float64) softmax
+        # attention between act-rounded inputs and an act-rounded output
+        # (the forward and backward of oracle/attention.py)
+        self.attention = attention
 
     # ---- pieces ---------------------------------------------------------------
     def rmsnorm_fwd(self, x: T, g: T):
@@ -132,7 +140,15 @@ class GPTOracle:
         ninf = full((Tn, Tn), -np.inf, acc)
         attn = np.zeros((B, Tn, H, hd), dtype=qkv.data.dtype)
         saved_h = {}
-        for b in range(B):
+        if self.attention == "fused":
+            from .attention import attention_fwd
+            q5 = qkv.f64().reshape(B, Tn, 3, H, hd)
+            heads = [np.ascontiguousarray(q5[:, :, i].transpose(0, 2, 1, 3)).reshape(B * H, Tn, hd)
+                     for i in range(3)]
+            O, Lse = attention_fwd(*heads, 1.0 / np.sqrt(hd), causal=True)
+            o_act = cast(T(O.reshape(B, H, Tn, hd).transpose(0, 2, 1, 3).reshape(B * Tn, D).copy(), "f64"), act)
+            saved_fused = (heads, O, Lse, o_act)
+        for b in range(B if self.attention != "fused" else 0):
             for h in range(H):
                 q = self._head(qkv, 0, b, h)
                 k = self._head(qkv, 1, b, h)
@@ -145,7 +161,7 @@ class GPTOracle:
                 o = _mm(pb, v, act)
                 attn[b, :, h, :] = o.data
                 saved_h[(b, h)] = (q, k, v, sv, pb)
-        o2 = T(attn.reshape(BT, D), act)
+        o2 = T(attn.reshape(BT, D), act) if self.attention != "fused" else o_act
         h1 = add(h0, _mm(o2, w["Wo"], act))
         n2, s2 = self.rmsnorm_fwd(h1, w["g2"])
         u = _mm(n2, w["W1"], act)
@@ -205,7 +221,17 @@ class GPTOracle:
         grads["Wo"] = _mm(_tr(o2), gh1, act)
         go = go2.data.reshape(B, Tn, H, hd)
         gqkv = np.zeros((BT, 3 * D), dtype=qkv.data.dtype)
-        for b in range(B):
+        if self.attention == "fused":
+            from .attention import attention_bwd
+            heads, _, Lse, o_act = saved_fused
+            ohead = o_act.f64().reshape(B, Tn, H, hd).transpose(0, 2, 1, 3).reshape(B * H, Tn, hd)
+            dohead = go2.f64().reshape(B, Tn, H, hd).transpose(0, 2, 1, 3).reshape(B * H, Tn, hd)
+            grads3 = attention_bwd(*heads, ohead, dohead, Lse, 1.0 / np.sqrt(hd), causal=True)
+            g5 = np.zeros((B, Tn, 3, H, hd))
+            for i in range(3):
+                g5[:, :, i] = grads3[i].reshape(B, H, Tn, hd).transpose(0, 2, 1, 3)
+            gqkv = cast(T(g5.reshape(BT, 3 * D), "f64"), act).data
+        for b in range(B if self.attention != "fused" else 0):
             for h in range(H):
                 q, k, v, sv, pb = saved_h[(b, h)]
                 gpv = T(np.ascontiguousarray(go[b, :, h, :]), act)

@@ -45,7 +45,7 @@ class Tensor:
     """A node of the lazy graph.  ``shape`` is the logical shape; ``arg``
     holds op-specific data; ``_real`` the realized (buffer, View)."""
 
-    __slots__ = ("op", "src", "shape", "dtype", "arg", "requires_grad", "grad", "_real", "_users",
+    __slots__ = ("op", "src", "shape", "dtype", "arg", "requires_grad", "grad", "_real", "_users", "_aux",
                  "__weakref__")
 
     def __init__(self, op, src, shape, dtype, arg=None, requires_grad=False):
@@ -58,6 +58,7 @@ class Tensor:
         self.grad = None
         self._real = None
         self._users = 0
+        self._aux = None  # realization-side data another node needs (ATTN: its row logsumexp)
 
     def __repr__(self):
         return "Tensor(%s, %s, %s)" % (self.op, self.shape, self.dtype)
@@ -234,6 +235,15 @@ class Tensor:
         """GATHER along dim 0: out[n, ...] = self[idx[n], ...]."""
         assert idx.dtype == "i32" and idx.ndim == 1
         return Tensor("GATHER", (self, idx), (idx.shape[0],) + self.shape[1:], self.dtype)
+
+    def attention(self, k: "Tensor", v: "Tensor", scale: float, causal: bool = True):
+        """Fused scaled dot-product attention (limn, "The op set": the one
+        fused node in place of the composed T x T scores): self = Q, k, v
+        are bf16 [B, T, H, 64]; returns O [B, T, H, 64] with
+        O = softmax(scale * Q K^T, keys j > i hidden when causal) V per head."""
+        assert self.shape == k.shape == v.shape and len(self.shape) == 4 and self.shape[3] == 64
+        assert self.dtype == k.dtype == v.dtype == "bf16"
+        return Tensor("ATTN", (self, k, v), self.shape, "bf16", arg=(float(scale), bool(causal)))
 
     def scatter_add(self, idx: "Tensor", upd: "Tensor"):
         """SCATTER-add along dim 0: self + rows of upd added at idx, in order."""
@@ -419,6 +429,10 @@ class Executor:
             r = self._realize_gather(t)
         elif op == "SCATTER":
             r = self._realize_scatter(t)
+        elif op == "ATTN":
+            r = self._realize_attn(t)
+        elif op == "ATTN_BWD":
+            r = self._realize_attn_bwd(t)
         else:
             raise RuntimeError("cannot realize %s" % op)
         t._real = r
@@ -847,6 +861,49 @@ class Executor:
         return b2, v2.expand(v.shape)
 
     # ---- indexed --------------------------------------------------------------------
+    def _attn_operand(self, x: Tensor):
+        """(buffer, View) of a [B, T, H, 64] bf16 operand the attention
+        kernels can read with TMA (head dim contiguous, other strides
+        multiples of 8, 16-byte aligned start, no mask); copied first if not."""
+        buf, v = self.realize(x)
+        ok = (v.mask is None and v.strides[3] == 1 and all(st % 8 == 0 for st in v.strides[:3])
+              and (buf.data_ptr() + 2 * v.offset) % 16 == 0)
+        if not ok:
+            buf, v = self._copy_contig(buf, v, x.dtype)
+        return buf, v
+
+    def _realize_attn(self, t: Tensor):
+        q, k, v = t.src
+        scale, causal = t.arg
+        B, T, H, _ = t.shape
+        (bq, vq), (bk, vk), (bv, vv) = (self._attn_operand(x) for x in (q, k, v))
+        out = self._new(t.shape, "bf16")
+        lse = self._new((B, H, T), "f32")
+        A.psg_attention_fwd(bq, self._pview(bq, vq, "bf16"), bk, self._pview(bk, vk, "bf16"), bv,
+                            self._pview(bv, vv, "bf16"), out, self._pview(out, View(t.shape), "bf16"), lse, scale,
+                            causal, self._status(), stream=self._s())
+        t._aux = lse
+        self.log.append(("attention", t.shape))
+        return out, View(t.shape)
+
+    def _realize_attn_bwd(self, t: Tensor):
+        q, k, v, fwd, g = t.src
+        scale, causal = t.arg
+        B, T, H, _ = fwd.shape
+        bo, vo = self.realize(fwd)
+        lse = fwd._aux
+        ops = [self._attn_operand(x) for x in (q, k, v, g)]
+        out = self._new(t.shape, "bf16")                      # [3, B, T, H, 64]: dQ, dK, dV
+        delta = self._new((B, H, T), "f32")
+        gv = [View(t.shape).shrink([(i, i + 1)] + [(0, n) for n in fwd.shape]).reshape(fwd.shape)
+              for i in range(3)]
+        pv = lambda bv: self._pview(bv[0], bv[1], "bf16")
+        A.psg_attention_bwd(ops[0][0], pv(ops[0]), ops[1][0], pv(ops[1]), ops[2][0], pv(ops[2]), bo, pv((bo, vo)),
+                            ops[3][0], pv(ops[3]), lse, delta, out, pv((out, gv[0])), out, pv((out, gv[1])), out,
+                            pv((out, gv[2])), scale, causal, self._status(), stream=self._s())
+        self.log.append(("attention_bwd", fwd.shape))
+        return out, View(t.shape)
+
     def _realize_gather(self, t: Tensor):
         src, idx = t.src
         bs, vs = self.realize(src)
@@ -1066,6 +1123,12 @@ def _vjp(t: Tensor, g: Tensor):
         return [(s[0], Tensor.zeros(s[0].shape, s[0].dtype).scatter_add(s[1], g))]
     if op == "SCATTER":
         return [(s[0], g), (s[2], g.gather(s[1]))]
+    if op == "ATTN":
+        # one node computes dQ, dK, dV together (the two-pass backward)
+        d = Tensor("ATTN_BWD", (s[0], s[1], s[2], t, g.cast("bf16") if g.dtype != "bf16" else g),
+                   (3,) + t.shape, "bf16", arg=t.arg)
+        full = [(0, n) for n in t.shape]
+        return [(s[i], d.shrink([(i, i + 1)] + full).reshape(t.shape)) for i in range(3)]
     return []
 
 

@@ -54,13 +54,21 @@ def target_index(tok: Tensor, V: int, device) -> Tensor:
     return (Tensor.from_torch(base) + nxt).reshape(Bn * (T - 1))
 
 
+def fused_attention_applies(T: int, D: int, H: int) -> bool:
+    """The fused attention op covers head dim 64 and one key block (T <= 256);
+    other shapes use the composed form."""
+    return D // H == 64 and T <= 256
+
+
 def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,
                    pick: torch.Tensor | None = None, mask: torch.Tensor | None = None,
-                   taps: dict | None = None):
+                   taps: dict | None = None, fused_attention: bool = True):
     """Mean next-token cross-entropy of the block on tokens [B, T] (int32,
     on the device).  w maps GPT_WEIGHTS to Tensors.  Returns the loss node
     (shape [1], float32).  If taps is a dict, the MLP pre-activation is put
-    there as taps["mlp_pre"] (for inspection)."""
+    there as taps["mlp_pre"] (for inspection).  fused_attention picks the
+    fused attention op where it applies (head dim 64, T <= 256) over the
+    composed form."""
     Bn, T = tok.shape
     V, D = w["E"].shape
     hd = D // H
@@ -72,19 +80,23 @@ def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,
     idx = Tensor.from_torch(tok.reshape(-1))
     h0 = (w["E"].gather(idx).reshape(Bn, T, D) + w["P"].reshape(1, T, D)).reshape(BT, D)
 
-    # attention (pre-norm), composed: scores, causal WHERE, softmax, weighted sum
+    # attention (pre-norm): the fused op, or composed from scores, causal
+    # WHERE, softmax and the weighted sum
     n1 = h0.rmsnorm(w["g1"], eps)
     qkv = n1.matmul(w["Wqkv"]).reshape(Bn, T, 3, H, hd)
 
     def head(i):
-        return qkv.shrink(((0, Bn), (0, T), (i, i + 1), (0, H), (0, hd))).reshape(Bn, T, H, hd) \
-                  .permute(0, 2, 1, 3)
+        return qkv.shrink(((0, Bn), (0, T), (i, i + 1), (0, H), (0, hd))).reshape(Bn, T, H, hd)
 
     q, k, v = head(0), head(1), head(2)
-    s = q.matmul(k.transpose(-1, -2)).cast("f32") * (1.0 / np.sqrt(hd))
-    s = Tensor.from_torch(mask).where(s, float("-inf"))
-    p = s.softmax(-1).cast("bf16")
-    o = p.matmul(v).permute(0, 2, 1, 3).reshape(BT, D)
+    if fused_attention and fused_attention_applies(T, D, H):
+        o = q.attention(k, v, 1.0 / np.sqrt(hd), causal=True).reshape(BT, D)
+    else:
+        q, k, v = (x.permute(0, 2, 1, 3) for x in (q, k, v))
+        s = q.matmul(k.transpose(-1, -2)).cast("f32") * (1.0 / np.sqrt(hd))
+        s = Tensor.from_torch(mask).where(s, float("-inf"))
+        p = s.softmax(-1).cast("bf16")
+        o = p.matmul(v).permute(0, 2, 1, 3).reshape(BT, D)
     h1 = h0 + o.matmul(w["Wo"])
 
     # MLP (pre-norm)
@@ -102,13 +114,13 @@ def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,
     return picked.reshape(1, n).sum(-1, keepdim=False) * (-1.0 / n)
 
 
-def gpt_step(tok: torch.Tensor, weights: dict, H: int, pick=None, mask=None, taps=None):
+def gpt_step(tok: torch.Tensor, weights: dict, H: int, pick=None, mask=None, taps=None, fused_attention=True):
     """One forward + backward pass: returns (loss, {name: grad}) as torch
     tensors.  weights maps GPT_WEIGHTS to device bf16 torch tensors.  With a
     taps dict, the tapped intermediates come back realized in it too."""
     w = {k: Tensor.from_torch(weights[k], requires_grad=True) for k in GPT_WEIGHTS}
     tp = {} if taps is not None else None
-    loss = gpt_block_loss(tok, w, H, pick=pick, mask=mask, taps=tp)
+    loss = gpt_block_loss(tok, w, H, pick=pick, mask=mask, taps=tp, fused_attention=fused_attention)
     backward(loss)
     names = list(tp) if tp else []
     outs = realize_all(loss, *[w[k].grad for k in GPT_WEIGHTS], *[tp[k] for k in names])

@@ -114,18 +114,19 @@ def _rel_fro(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def _gpt_compare(O, B, T, V, D, H, F, seed, nthreads=None, same_relu_mask=False):
+def _gpt_compare(O, B, T, V, D, H, F, seed, nthreads=None, same_relu_mask=False, fused=True):
     """Loss and every gradient of the GPU block against the oracle's block.
     With same_relu_mask the oracle's backward takes the GPU's MLP activity
     mask (relu is discontinuous at 0: pre-activations that differ only by
     summation order may fall on either side of 0 and switch a unit's whole
     gradient on or off; the forward of both runs is left as is)."""
     import oracle.gpt as OG
-    from primitive_sm_graph_gb300.workloads import GPT_WEIGHTS, gpt_step
+    from primitive_sm_graph_gb300.workloads import GPT_WEIGHTS, fused_attention_applies, gpt_step
     tok, w = SI.gpt_block(seed, B, T, V, D, H, F)
     dev = {k: v.cuda() for k, v in w.items()}
     taps = {}
-    loss, grads = gpt_step(tok.cuda(), dev, H, taps=taps)
+    loss, grads = gpt_step(tok.cuda(), dev, H, taps=taps, fused_attention=fused)
+    mode = "fused" if fused and fused_attention_applies(T, D, H) else "composed"
     torch.cuda.synchronize()
     lg = float(loss.float().cpu()[0])
     assert math.isfinite(lg)
@@ -137,7 +138,7 @@ def _gpt_compare(O, B, T, V, D, H, F, seed, nthreads=None, same_relu_mask=False)
     try:
         ow = {k: O.T(SI.bits(v), "bf16") for k, v in w.items()}
         mask = (taps["mlp_pre"].float() > 0).cpu().numpy() if same_relu_mask else None
-        oloss, ograds = OG.GPTOracle(tok.numpy(), ow, H, relu_mask=mask).run()
+        oloss, ograds = OG.GPTOracle(tok.numpy(), ow, H, relu_mask=mask, attention=mode).run()
     finally:
         O.NTHREADS = old
     assert abs(lg - float(oloss.data[0])) <= 2.0 ** -6 * abs(float(oloss.data[0]))
@@ -151,7 +152,39 @@ def test_gpt_block_small_against_oracle(O):
 
 
 def test_gpt_block_mid_size_against_oracle(O):
-    _gpt_compare(O, B=4, T=64, V=256, D=128, H=2, F=256, seed=4)
+    _gpt_compare(O, B=4, T=64, V=256, D=128, H=2, F=256, seed=4, same_relu_mask=True)
+
+
+def test_gpt_block_composed_attention_against_oracle(O):
+    """The composed attention (scores, mask, softmax, weighted sum as nodes)
+    at head dim 64, against the oracle's composed block."""
+    _gpt_compare(O, B=2, T=128, V=128, D=128, H=2, F=256, seed=5, fused=False, same_relu_mask=True)
+
+
+def test_gpt_block_fused_attention_mid_size(O):
+    _gpt_compare(O, B=2, T=128, V=128, D=128, H=2, F=256, seed=5, same_relu_mask=True)
+
+
+def test_attention_op_forward_and_gradients(G):
+    """Tensor.attention and its VJP against the attention oracle (one call
+    each way, both realized by the fused kernels)."""
+    from oracle.attention import attention_bwd, attention_fwd
+    B, T, H = 2, 96, 2
+    g = SI.gen(12)
+    x = [SI.normal((B, T, H, 64), 0, 1, g, torch.bfloat16) for _ in range(4)]
+    log = _fresh_log(G)
+    q, k, v = (G.Tensor.from_torch(t.cuda(), requires_grad=True) for t in x[:3])
+    o = q.attention(k, v, 0.125)
+    o.backward(G.Tensor.from_torch(x[3].cuda()))
+    out, gq, gk, gv = G.realize_all(o, q.grad, k.grad, v.grad)
+    kinds = [e[0] for e in log]
+    assert kinds.count("attention") == 1 and kinds.count("attention_bwd") == 1, kinds
+    heads = [t.float().permute(0, 2, 1, 3).reshape(B * H, T, 64).double().numpy() for t in x]
+    O_ref, L = attention_fwd(*heads[:3], 0.125)
+    refs = attention_bwd(*heads[:3], O_ref, heads[3], L, 0.125)
+    for got, ref in zip((out, gq, gk, gv), (O_ref,) + tuple(refs)):
+        g64 = got.float().cpu().permute(0, 2, 1, 3).reshape(B * H, T, 64).double().numpy()
+        assert _rel_fro(g64, ref) <= 2.0 ** -7
 
 
 def test_gpt_block_full_size(O):
