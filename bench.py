@@ -433,6 +433,39 @@ class Rows:
         del src, dst
         return ms
 
+    # C5 shapes: the fused attention forward + backward (B32, T256, H8, head dim 64)
+    def attention(self):
+        A = self.A
+        B_, T, H = 32, 256, 8
+        g = SI.gen(5)
+        qkv = SI.normal((B_, T, 3, H, 64), 0, 1, g, torch.bfloat16).cuda()
+        do = SI.normal((B_, T, H, 64), 0, 1, g, torch.bfloat16).cuda()
+        vs = [A.view_of(qkv, shape=(B_, T, H, 64), strides=qkv[:, :, 0].stride(), offset=i * H * 64)
+              for i in range(3)]
+        o = torch.empty((B_, T, H, 64), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B_, H, T), dtype=torch.float32, device="cuda")
+        delta = torch.empty_like(lse)
+        dqkv = torch.empty_like(qkv)
+        dvs = [A.view_of(dqkv, shape=(B_, T, H, 64), strides=dqkv[:, :, 0].stride(), offset=i * H * 64)
+               for i in range(3)]
+        vo, vdo = A.view_of(o), A.view_of(do)
+
+        def fn(s):
+            A.psg_attention_fwd(qkv, vs[0], qkv, vs[1], qkv, vs[2], o, vo, lse, 0.125, True, stream=s)
+            A.psg_attention_bwd(qkv, vs[0], qkv, vs[1], qkv, vs[2], o, vo, do, vdo, lse, delta, dqkv, dvs[0],
+                                dqkv, dvs[1], dqkv, dvs[2], 0.125, True, stream=s)
+        per = 2.0 * B_ * H * T * T * 64       # one T x T x 64 contraction (full square)
+        flops = 7 * per                       # forward: S, O; backward: S, dP, dV, dK, dQ
+        pk = self.P["bf16"]
+
+        def fin(ms):
+            tf = flops / (ms * 1e-3) / 1e12
+            return {"ms": round(ms, 5), "flops": flops, "achieved": round(tf, 2), "unit": "TFLOP/s",
+                    "bound": "tensor", "peak": pk, "frac": round(tf / pk, 4),
+                    "note": "full T x T products counted (the causal half is computed and masked)",
+                    "workload": "fused attention fwd+bwd B32 T256 H8 hd64 causal bf16 (4 launches)"}
+        return fn, fin
+
     def run_kernel_rows(self, names):
         out = {}
         for nm in names:
@@ -591,7 +624,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-KERNEL_ROWS = ["softmax", "rmsnorm", "gemm_bf16", "gemm_f32", "gather", "scatter"]
+KERNEL_ROWS = ["softmax", "rmsnorm", "gemm_bf16", "gemm_f32", "gather", "scatter", "attention"]
 ROW_NAMES = KERNEL_ROWS + ["tiny_graph", "gpt"]
 
 
