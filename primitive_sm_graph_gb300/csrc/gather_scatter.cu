@@ -120,9 +120,10 @@ __global__ void __launch_bounds__(1024) bitonic_local(unsigned long long* keys, 
     const int64_t k1 = kfrom > 0 ? kfrom : m;
     for (int64_t k = k0; k <= k1; k <<= 1) {
         for (int64_t j = (k < m ? k : m) >> 1; j > 0; j >>= 1) {
+            const int jj = (int)j;
             for (int i = t; i < m / 2; i += blockDim.x) {
-                // pair (a, a + j) with a having bit j clear
-                const int a = (int)((i / j) * (2 * j) + (i % j));
+                // pair (a, a + j) with a having bit j clear (j a power of two)
+                const int a = ((i & ~(jj - 1)) << 1) | (i & (jj - 1));
                 const int64_t ga = tile + a;
                 const bool up = (ga & k) == 0;
                 cmp_swap(s[a], s[a + j], up);
@@ -131,6 +132,42 @@ __global__ void __launch_bounds__(1024) bitonic_local(unsigned long long* keys, 
         }
     }
     for (int i = t; i < m; i += blockDim.x) keys[tile + i] = s[i];
+}
+
+// keys and the whole bitonic sort in one block for npow2 <= SMALL_SORT: the
+// keys stay in shared memory for all log2(n) (log2(n) + 1) / 2 steps
+constexpr int SMALL_SORT = 16384;
+constexpr int SMALL_SORT_SMEM = SMALL_SORT * 8;  // 128 KB
+
+__global__ void __launch_bounds__(1024) sort_small(const int32_t* __restrict__ idx, int64_t n, int64_t V, int npow2,
+                                                   unsigned long long* __restrict__ keys, int32_t* status)
+{
+    extern __shared__ unsigned long long sk[];
+    const int t = threadIdx.x;
+    for (int i = t; i < npow2; i += blockDim.x) {
+        unsigned long long k = ~0ull;
+        if (i < n) {
+            const int64_t v = idx[i];
+            if (v >= 0 && v < V) {
+                k = ((unsigned long long)v << 32) | (unsigned long long)i;
+            } else {
+                k = (BAD_HI << 32) | (unsigned long long)i;  // sorts after every valid key
+                report(status, PSG_E_INDEX_OUT_OF_RANGE);
+            }
+        }
+        sk[i] = k;
+    }
+    __syncthreads();
+    for (int k = 2; k <= npow2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = t; i < npow2 / 2; i += blockDim.x) {
+                const int a = ((i & ~(j - 1)) << 1) | (i & (j - 1));
+                cmp_swap(sk[a], sk[a + j], (a & k) == 0);
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = t; i < npow2; i += blockDim.x) keys[i] = sk[i];
 }
 
 // one global step (k, j) with j >= LOCAL_SORT: one thread per pair
@@ -263,8 +300,17 @@ __global__ void __launch_bounds__(256) scatter_accumulate(const __grid_constant_
         const unsigned long long hi = keys[p] >> 32;
         if (hi == BAD_HI) continue;                          // invalid index (or padding)
         if (p > 0 && (keys[p - 1] >> 32) == hi) continue;    // not the start of a run
+        // the run's end, 32 keys at a time (the item is the warp's: converged)
         int64_t end = p + 1;
-        while (end < L.n && (keys[end] >> 32) == hi) ++end;
+        for (;;) {
+            const int64_t q = end + lane;
+            const unsigned same = __ballot_sync(0xffffffffu, q < L.n && (keys[q] >> 32) == hi);
+            if (same != 0xffffffffu) {
+                end += __ffs(~same) - 1;
+                break;
+            }
+            end += 32;
+        }
         const int64_t c0 = (seg * 32 + lane) * VPL;
         if (c0 >= L.D) continue;
         const int nv = L.D - c0 < VPL ? (int)(L.D - c0) : VPL;
@@ -298,6 +344,110 @@ __global__ void __launch_bounds__(256) scatter_accumulate(const __grid_constant_
 #pragma unroll
         for (int i = 0; i < VPL; ++i)
             if (i < nv) S::st(L.dst, drow + (c0 + i) * L.dst_cs, acc[i]);
+    }
+}
+
+// Row-scan SCATTER-add for short update lists (n <= ROWSCAN_MAX_N): no sort.
+// The block stages idx in shared memory; each warp owns one (destination
+// row, column segment) item, lists the update rows n with idx[n] == row in
+// ascending n (ballots over 32 indices at a time), then adds them in that
+// order, ROWSCAN_AHEAD rows loaded ahead of the adds, into a total seeded
+// with the destination's value and rounded once: the same adds in the same
+// order as the sorted path, so the same bits.
+constexpr int ROWSCAN_MAX_N = 16384;
+constexpr int ROWSCAN_LIST = 256;    // listed rows per warp per round
+constexpr int ROWSCAN_AHEAD = 8;
+
+constexpr int ROWSCAN_WARPS = 4;
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(ROWSCAN_WARPS * 32) scatter_rowscan(const __grid_constant__ ScatterLaunch L,
+                                                                      int64_t nseg)
+{
+    typedef SV<DT> S;
+    typedef typename S::A A;
+    constexpr int VPL = VEC ? 16 / S::ES : 1;
+    extern __shared__ int32_t sidx[];                      // [n] then [warps][ROWSCAN_LIST]
+    int32_t* lists = sidx + ((L.n + 3) & ~3ll);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    bool bad = false;
+#pragma unroll 8
+    for (int64_t i = threadIdx.x; i < L.n; i += blockDim.x) {
+        const int32_t v = __ldg(L.idx + i);
+        const bool ok = v >= 0 && v < L.V;
+        bad = bad || !ok;
+        sidx[i] = ok ? v : -1;
+    }
+    if (bad && blockIdx.x == 0) report(L.status, PSG_E_INDEX_OUT_OF_RANGE);
+    __syncthreads();
+    int32_t* list = lists + w * ROWSCAN_LIST;
+    const int64_t items = L.V * nseg;
+    for (int64_t it = (int64_t)blockIdx.x * ROWSCAN_WARPS + w; it < items;
+         it += (int64_t)gridDim.x * ROWSCAN_WARPS) {
+        const int32_t row = (int32_t)(it / nseg);
+        const int64_t seg = it - (int64_t)row * nseg;
+        const int64_t c0 = (seg * 32 + lane) * VPL;
+        const int nv = c0 >= L.D ? 0 : (L.D - c0 < VPL ? (int)(L.D - c0) : VPL);
+        const int64_t drow = L.dst_offset + (int64_t)row * L.dst_rs;
+        A acc[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) acc[i] = i < nv ? S::ld(L.dst, drow + (c0 + i) * L.dst_cs) : A(0);
+        bool touched = false;
+        int64_t base = 0;
+        while (base < L.n) {
+            // phase 1: the next (up to ROWSCAN_LIST) update rows aimed at `row`, ascending
+            int cnt = 0;
+            // four chunks of 32 indices per step: the shared loads go out together
+            for (; base < L.n && cnt <= ROWSCAN_LIST - 128; base += 128) {
+                int32_t v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t q = base + 32 * u + lane;
+                    v[u] = q < L.n ? sidx[q] : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const unsigned m = __ballot_sync(0xffffffffu, v[u] == row);
+                    if (m) {
+                        if (m & (1u << lane))
+                            list[cnt + __popc(m & ((1u << lane) - 1u))] = (int32_t)(base + 32 * u + lane);
+                        cnt += __popc(m);
+                    }
+                }
+            }
+            __syncwarp();
+            // phase 2: add them in order, ROWSCAN_AHEAD rows in flight
+            for (int e = 0; e < cnt; e += ROWSCAN_AHEAD) {
+                A x[ROWSCAN_AHEAD][VPL];
+#pragma unroll
+                for (int u = 0; u < ROWSCAN_AHEAD; ++u) {
+                    if (e + u >= cnt || nv == 0) break;
+                    const int64_t o = L.upd_offset + (int64_t)list[e + u] * L.upd_rs + c0 * L.upd_cs;
+                    if constexpr (VEC) {
+                        if (nv == VPL) {
+                            S::unpack(__ldg((const uint4*)((const char*)L.upd + o * S::ES)), x[u]);
+                            continue;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < VPL; ++i) x[u][i] = i < nv ? S::ld(L.upd, o + i * L.upd_cs) : A(0);
+                }
+#pragma unroll
+                for (int u = 0; u < ROWSCAN_AHEAD; ++u) {
+                    if (e + u >= cnt || nv == 0) break;
+#pragma unroll
+                    for (int i = 0; i < VPL; ++i) acc[i] = S::add(acc[i], x[u][i]);
+                }
+            }
+            touched = touched || cnt > 0;
+            __syncwarp();
+        }
+        // rows nothing lands on keep their bits (no write at all)
+        if (touched) {
+#pragma unroll
+            for (int i = 0; i < VPL; ++i)
+                if (i < nv) S::st(L.dst, drow + (c0 + i) * L.dst_cs, acc[i]);
+        }
     }
 }
 
@@ -374,21 +524,73 @@ static void launch_accumulate(const ScatterLaunch& L, const unsigned long long* 
                                         s>>>(L, keys, nseg);
 }
 
+template <int DT>
+static psg_status launch_rowscan(const ScatterLaunch& L, cudaStream_t s)
+{
+    constexpr int ES = SV<DT>::ES;
+    const bool vec = L.upd_cs == 1 && ((uintptr_t)L.upd + (uint64_t)L.upd_offset * ES) % 16 == 0 &&
+                     ((uint64_t)L.upd_rs * ES) % 16 == 0;
+    const int64_t seg_cols = 32 * (vec ? 16 / ES : 1);
+    const int64_t nseg = (L.D + seg_cols - 1) / seg_cols;
+    if (nseg == 0) return PSG_OK;
+    const size_t smem = (size_t)(((L.n + 3) & ~3ll) + ROWSCAN_WARPS * ROWSCAN_LIST) * 4;
+    const int64_t blocks =
+        std::min<int64_t>((L.V * nseg + ROWSCAN_WARPS - 1) / ROWSCAN_WARPS, (int64_t)num_sms() * 4);
+    static std::once_flag once[2];
+    static cudaError_t err[2] = {cudaSuccess, cudaSuccess};
+    const void* fn = vec ? (const void*)scatter_rowscan<DT, true> : (const void*)scatter_rowscan<DT, false>;
+    std::call_once(once[vec ? 1 : 0], [fn] {
+        err[fn == (const void*)scatter_rowscan<DT, true> ? 1 : 0] =
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    });
+    if (err[vec ? 1 : 0] != cudaSuccess) return PSG_E_CUDA;
+    if (vec) scatter_rowscan<DT, true><<<(unsigned)blocks, ROWSCAN_WARPS * 32, smem, s>>>(L, nseg);
+    else scatter_rowscan<DT, false><<<(unsigned)blocks, ROWSCAN_WARPS * 32, smem, s>>>(L, nseg);
+    return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
+}
+
+// the row scan reads all n indices once per (row, segment) item from shared
+// memory: worth it while V * n stays small against one sort of n keys
+static bool use_rowscan(const ScatterLaunch& L)
+{
+    return L.n <= ROWSCAN_MAX_N && L.V <= 4096 && L.V * L.n <= (int64_t)1 << 24;
+}
+
 psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void* stream)
 {
     if (L.n == 0) return PSG_OK;
     cudaStream_t s = (cudaStream_t)stream;
+    if (use_rowscan(L)) {
+        switch (L.dtype) {
+        case PSG_F32: return launch_rowscan<PSG_F32>(L, s);
+        case PSG_BF16: return launch_rowscan<PSG_BF16>(L, s);
+        case PSG_F16: return launch_rowscan<PSG_F16>(L, s);
+        case PSG_F64: return launch_rowscan<PSG_F64>(L, s);
+        default: return launch_rowscan<PSG_I32>(L, s);
+        }
+    }
     const int64_t np2 = scatter_npow2(L.n);
-    make_keys<<<grid_for((const void*)make_keys, 256, (np2 + 255) / 256), 256, 0, s>>>(L.idx, L.n, L.V, np2,
-                                                                                     keys, L.status);
-    const int64_t tiles = (np2 + LOCAL_SORT - 1) / LOCAL_SORT;
-    const int lthreads = 1024;
-    bitonic_local<<<(unsigned)tiles, lthreads, 0, s>>>(keys, np2, 0);
-    for (int64_t k = 2 * LOCAL_SORT; k <= np2; k <<= 1) {
-        for (int64_t j = k >> 1; j >= LOCAL_SORT; j >>= 1)
-            bitonic_global<<<grid_for((const void*)bitonic_global, 256, (np2 / 2 + 255) / 256), 256, 0, s>>>(
-                keys, np2, k, j);
-        bitonic_local<<<(unsigned)tiles, lthreads, 0, s>>>(keys, np2, k);
+    if (np2 <= SMALL_SORT) {
+        static std::once_flag once;
+        static cudaError_t err = cudaSuccess;
+        std::call_once(once, [] {
+            err = cudaFuncSetAttribute((const void*)sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMALL_SORT_SMEM);
+        });
+        if (err != cudaSuccess) return PSG_E_CUDA;
+        sort_small<<<1, 1024, (size_t)np2 * 8, s>>>(L.idx, L.n, L.V, (int)np2, keys, L.status);
+    } else {
+        make_keys<<<grid_for((const void*)make_keys, 256, (np2 + 255) / 256), 256, 0, s>>>(L.idx, L.n, L.V, np2,
+                                                                                         keys, L.status);
+        const int64_t tiles = (np2 + LOCAL_SORT - 1) / LOCAL_SORT;
+        const int lthreads = 1024;
+        bitonic_local<<<(unsigned)tiles, lthreads, 0, s>>>(keys, np2, 0);
+        for (int64_t k = 2 * LOCAL_SORT; k <= np2; k <<= 1) {
+            for (int64_t j = k >> 1; j >= LOCAL_SORT; j >>= 1)
+                bitonic_global<<<grid_for((const void*)bitonic_global, 256, (np2 / 2 + 255) / 256), 256, 0, s>>>(
+                    keys, np2, k, j);
+            bitonic_local<<<(unsigned)tiles, lthreads, 0, s>>>(keys, np2, k);
+        }
     }
     switch (L.dtype) {
     case PSG_F32: launch_accumulate<PSG_F32>(L, keys, s); break;

@@ -78,7 +78,7 @@ def _scatter(A, dst, idx, upd):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16", "i32", "f64"])
-@pytest.mark.parametrize("case", ["embedding_grad", "single_row", "permutation", "ragged", "large"])
+@pytest.mark.parametrize("case", ["embedding_grad", "single_row", "permutation", "ragged", "large", "long_runs"])
 def test_scatter_add_matches_oracle(A, O, dt, case):
     g = SI.gen(sum(map(ord, dt + case)))
     if case == "embedding_grad":   # [8192, 512] into [256, 512], ~32 collisions per row
@@ -93,8 +93,11 @@ def test_scatter_add_matches_oracle(A, O, dt, case):
     elif case == "ragged":
         V, D, n = 50, 3, 1234
         idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
-    else:                          # past one local sort tile: global bitonic steps
+    elif case == "large":          # past one sorting block: global bitonic steps
         V, D, n = 4000, 2, 20000
+        idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
+    else:                          # runs of ~33,000 equal indices (run ends found 32 keys at a time)
+        V, D, n = 3, 4, 100000
         idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
     dst0 = _vals(g, (V, D), dt)
     upd = _vals(g, (n, D), dt)
