@@ -209,10 +209,16 @@ psg_status psg_permute(const void* in, const psg_view* in_v, const int32_t* perm
  *   N must be 0 and Bv's stride along M must be 0 (A broadcast over n, B over
  *   m), batch strides are free; unmasked.  Cv: shape [batch.., M, N] (or with
  *   a trailing 1), injective.
- * dtypes: A and B both PSG_BF16 (tensor cores, float32 accumulate in TMEM) or
- *   both PSG_F32 (float32 FMA); C PSG_F32 or PSG_BF16 (rounded once, RNE).
+ * dtypes: A and B of one type: PSG_BF16 or PSG_F16 (tensor cores, float32
+ *   accumulate in TMEM, exact products) or PSG_F32 (K >= 256 and 16-byte
+ *   aligned operands: tensor cores as 3xTF32, hi*hi + hi*lo + lo*hi with a
+ *   few 2^-20 relative error per product; otherwise float32 FMA on the FP32
+ *   pipes); C PSG_F32, PSG_BF16 or PSG_F16 (rounded once, RNE).  Operands the
+ *   tensor cores cannot address (strides not 16-byte multiples, several
+ *   batch dims that do not merge) take the FP32-pipe kernel.
  * The total deviates from the sequential float32 loop by at most
- * 2 * gamma_{K-1} * sum_k |a_k b_k| (Litmus, "ToleranceBound").
+ * 2 * gamma_{K-1} * sum_k |a_k b_k| (Litmus, "ToleranceBound"); for the
+ * 3xTF32 path that bound absorbs the product error at the K it is used at.
  * d_status: device int32 or NULL; receives PSG_E_TIMEOUT if a pipeline wait in
  *   the tensor-core kernel gave up (the output is then invalid).
  * ------------------------------------------------------------------------- */

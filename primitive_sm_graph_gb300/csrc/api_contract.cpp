@@ -69,8 +69,8 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
         if (Cv->shape[d] != Av->shape[d]) return PSG_E_INVALID_ARG;
     const int adt = Av->dtype, cdt = Cv->dtype;
     if (Bv->dtype != adt) return PSG_E_UNSUPPORTED_DTYPE;
-    if (adt != PSG_BF16 && adt != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
-    if (cdt != PSG_BF16 && cdt != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
+    if (adt != PSG_BF16 && adt != PSG_F16 && adt != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
+    if (cdt != PSG_BF16 && cdt != PSG_F16 && cdt != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
     const int64_t numel = M * N * K;
     if (numel > 0 && (!A || !Bp)) return PSG_E_INVALID_ARG;
     if (M * N > 0 && !C) return PSG_E_INVALID_ARG;
@@ -93,7 +93,7 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
     // MMAs per term; shorter K keeps the exact-product FP32-pipe kernel,
     // whose only error is the reduction order)
     constexpr int64_t TF32X3_MIN_K = 256;
-    bool tc = (adt == PSG_BF16 || (adt == PSG_F32 && K >= TF32X3_MIN_K)) && bt->nb <= 1 && K > 0;
+    bool tc = (adt == PSG_BF16 || adt == PSG_F16 || (adt == PSG_F32 && K >= TF32X3_MIN_K)) && bt->nb <= 1 && K > 0;
     const int es = dtype_size(adt), q16 = 16 / es;  // elements per 16 bytes
     auto tma_ok = [&](const void* base, int64_t off, int64_t s_mn, int64_t s_k, int64_t mn, int64_t s_b, bool& kmaj) {
         if (s_k == 1 && s_mn % q16 == 0 && s_mn >= K) kmaj = true;
@@ -115,6 +115,7 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
         T->p.a_kmajor = akm ? 1 : 0;
         T->p.b_kmajor = bkm ? 1 : 0;
         T->p.c_dtype = cdt;
+        T->p.ab_dtype = adt;
         T->p.C = C;
         T->p.status = d_status;
         T->p.c_offset = Cv->offset;
@@ -175,7 +176,7 @@ extern "C" psg_status psg_contract(const void* A, const psg_view* Av, const void
     }
     if (bt.nb <= 1) {
         if (!tc) return launch_contract_simt(S, stream);
-        return S.ab_dtype == PSG_BF16 ? launch_contract_tc(T, stream) : launch_contract_tf32(T, stream);
+        return S.ab_dtype == PSG_F32 ? launch_contract_tf32(T, stream) : launch_contract_tc(T, stream);
     }
     // several batch dims that do not merge: one launch per batch index
     int64_t count = 1;

@@ -10,6 +10,7 @@ struct TcParams {
     int a_kmajor, b_kmajor;     // 1: k stride 1; 0: m (n) stride 1
     int num_m, num_n, num_k;    // tile counts (filled by the launcher)
     int c_dtype;
+    int ab_dtype;               // bf16 or f16 (tc_gemm), f32 (tc_gemm_tf32x3)
     void* C;
     int32_t* status;
     int64_t c_offset, c_rs, c_cs, c_bs;

@@ -8,6 +8,7 @@
 // total over k in ascending order (multiply-adds may contract into FMA; the
 // result is bounded by the reduction-order term like any SUM).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "contract.h"
@@ -23,6 +24,7 @@ template <int DT>
 __device__ __forceinline__ float ld(const void* p, int64_t o)
 {
     if constexpr (DT == PSG_F32) return __ldg((const float*)p + o);
+    else if constexpr (DT == PSG_F16) return __half2float(__ldg((const __half*)p + o));
     else return __uint_as_float(((uint32_t)__ldg((const unsigned short*)p + o)) << 16);
 }
 
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(NT) simt_gemm(const __grid_constant__ SimtPara
                 if (n >= p.N) continue;
                 const int64_t o = p.c_off + b * p.c_bs + m * p.c_ms + n * p.c_ns;
                 if (p.c_dtype == PSG_F32) ((float*)p.C)[o] = acc[i][j];
+                else if (p.c_dtype == PSG_F16) ((__half*)p.C)[o] = __float2half_rn(acc[i][j]);
                 else ((__nv_bfloat16*)p.C)[o] = __float2bfloat16_rn(acc[i][j]);
             }
         }
@@ -107,6 +110,7 @@ psg_status launch_contract_simt(const SimtParams& p, void* stream)
     if ((p.N + TN - 1) / TN > 2147483647 || (p.M + TM - 1) / TM > 65535) return PSG_E_UNSUPPORTED_LAYOUT;
     cudaStream_t s = (cudaStream_t)stream;
     if (p.ab_dtype == PSG_F32) simt_gemm<PSG_F32><<<grid_of(p), NT, 0, s>>>(p);
+    else if (p.ab_dtype == PSG_F16) simt_gemm<PSG_F16><<<grid_of(p), NT, 0, s>>>(p);
     else simt_gemm<PSG_BF16><<<grid_of(p), NT, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
@@ -117,7 +121,9 @@ void query_contract_simt(const SimtParams& p, int* grid, int* block, int* smem, 
     *grid = (int)(g.x * g.y * g.z);
     *block = NT;
     *smem = 0;
-    *regs = kernel_regs(p.ab_dtype == PSG_F32 ? (const void*)simt_gemm<PSG_F32> : (const void*)simt_gemm<PSG_BF16>);
+    *regs = kernel_regs(p.ab_dtype == PSG_F32   ? (const void*)simt_gemm<PSG_F32>
+                        : p.ab_dtype == PSG_F16 ? (const void*)simt_gemm<PSG_F16>
+                                                : (const void*)simt_gemm<PSG_BF16>);
 }
 
 }  // namespace psg

@@ -23,6 +23,7 @@
 // tiles.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -143,8 +144,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            // instruction descriptor: f32 accumulate, bf16 A and B, M = 128, N = 256
-            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((p.a_kmajor ? 0u : 1u) << 15) |
+            // instruction descriptor: f32 accumulate, A and B both bf16 (1) or both f16 (0),
+            // M = 128, N = 256
+            const uint32_t ab = p.ab_dtype == PSG_F16 ? 0u : 1u;
+            const uint32_t idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((p.a_kmajor ? 0u : 1u) << 15) |
                                    ((p.b_kmajor ? 0u : 1u) << 16) | ((uint32_t)(BN >> 3) << 17) |
                                    ((uint32_t)(BM >> 4) << 24);
             // K-major: 8-row groups 1024 B apart, a K step of 16 is 32 B; MN-major:
@@ -224,6 +227,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
                                 if (n0 + j < p.N)
                                     C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2bfloat16_rn(__uint_as_float(r[j]));
                         }
+                    } else if (p.c_dtype == PSG_F16) {
+                        __half* C = (__half*)p.C;
+                        for (int j = 0; j < 32; ++j)
+                            if (n0 + j < p.N) C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2half_rn(__uint_as_float(r[j]));
                     } else {
                         float* dst = (float*)p.C + crow + n0;
                         if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
@@ -249,9 +256,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
 }
 
-// 3-D tensor map over a bf16 operand: dims {inner, outer, batch}.
+// 3-D tensor map over a bf16 or f16 operand: dims {inner, outer, batch}.
 bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t batch, int64_t outer_stride,
-              int64_t batch_stride, uint32_t box_inner, uint32_t box_outer)
+              int64_t batch_stride, uint32_t box_inner, uint32_t box_outer, bool f16)
 {
     auto enc = encode_fn();
     if (!enc) return false;
@@ -259,7 +266,8 @@ bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, 
     cuuint64_t strides[2] = {(cuuint64_t)(outer_stride * 2), (cuuint64_t)(batch_stride * 2)};
     cuuint32_t box[3] = {box_inner, box_outer, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+    return enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -274,10 +282,11 @@ psg_status launch_contract_tc(const TcOperands& o, void* stream)
     // batch strides of a single batch are never used; keep them a legal multiple of 16 bytes
     const int64_t a_bs = p.batch > 1 ? o.a_bs : (p.a_kmajor ? o.a_ms * p.M : o.a_ks * p.K);
     const int64_t b_bs = p.batch > 1 ? o.b_bs : (p.b_kmajor ? o.b_ns * p.N : o.b_ks * p.K);
-    bool ok = p.a_kmajor ? make_map(&ma, o.A, p.K, p.M, p.batch, o.a_ms, a_bs, 64, 128)
-                         : make_map(&ma, o.A, p.M, p.K, p.batch, o.a_ks, a_bs, 64, 64);
-    ok = ok && (p.b_kmajor ? make_map(&mb, o.B, p.K, p.N, p.batch, o.b_ns, b_bs, 64, 256)
-                           : make_map(&mb, o.B, p.N, p.K, p.batch, o.b_ks, b_bs, 64, 64));
+    const bool f16 = p.ab_dtype == PSG_F16;
+    bool ok = p.a_kmajor ? make_map(&ma, o.A, p.K, p.M, p.batch, o.a_ms, a_bs, 64, 128, f16)
+                         : make_map(&ma, o.A, p.M, p.K, p.batch, o.a_ks, a_bs, 64, 64, f16);
+    ok = ok && (p.b_kmajor ? make_map(&mb, o.B, p.K, p.N, p.batch, o.b_ns, b_bs, 64, 256, f16)
+                           : make_map(&mb, o.B, p.N, p.K, p.batch, o.b_ks, b_bs, 64, 64, f16));
     if (!ok) return PSG_E_CUDA;
     p.num_m = (p.M + BM - 1) / BM;
     p.num_n = (p.N + BN - 1) / BN;

@@ -27,6 +27,7 @@
 // and returns.  No TMA multicast.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -274,6 +275,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_tf32x3(const __grid_consta
                         for (int j = 0; j < 32; ++j)
                             if (n0 + j < p.N)
                                 C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                    } else if (p.c_dtype == PSG_F16) {
+                        __half* C = (__half*)p.C;
+                        for (int j = 0; j < 32; ++j)
+                            if (n0 + j < p.N) C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2half_rn(__uint_as_float(r[j]));
                     } else {
                         float* dst = (float*)p.C + crow + n0;
                         if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {

@@ -210,3 +210,45 @@ def test_f32_tensor_core_bf16_output_and_batch(A, O):
 def test_f32_tensor_core_launch_query(A):
     q = A.psg_query_launch("contract_f32_tensor", A.make_view("f32", (4096, 4096)))
     assert q["block"] == 448 and q["smem"] > 190000 and 1 <= q["grid"] <= 152
+
+
+@pytest.mark.parametrize("M,N,K,a_layout,b_layout,out_dt", [(256, 256, 128, "mk", "kn", "f32"),
+                                                             (200, 300, 100, "km", "nk", "f16"),
+                                                             (130, 70, 64, "mk", "nk", "bf16")])
+def test_f16_contraction_tensor_cores(A, O, M, N, K, a_layout, b_layout, out_dt):
+    """float16 operands (both f16: the tensor cores take one type for A and
+    B) on the tcgen05 path, within the SUM bound plus the output rounding."""
+    g = SI.gen(M + N + K)
+    s = 1.0 / float(np.sqrt(K))
+    a = SI.normal((M, K), 0.0, s, g).to(torch.float16)
+    b = SI.normal((K, N), 0.0, s, g).to(torch.float16)
+    ref = O.matmul(O.T(a.numpy(), "f16"), O.T(b.numpy(), "f16"), "f32").data
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    dA, dB = dev(_storage(a, a_layout)), dev(_storage(b, b_layout))
+    Av, Bv = _views(A, dA, dB, M, N, K, a_layout, b_layout)
+    C = torch.empty((M, N), dtype=storage_dtype(out_dt), device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), None)
+    torch.cuda.synchronize()
+    got = O.T(to_np(C.cpu()), out_dt).f64()
+    tol = 2 * gamma(K - 1) * mag + 1e-30
+    if out_dt == "bf16":
+        tol = tol + 2.0 ** -7 * np.abs(ref)
+    elif out_dt == "f16":
+        tol = tol + 2.0 ** -10 * np.abs(ref) + 2.0 ** -24
+    assert np.all(np.abs(got - ref) <= tol)
+
+
+def test_f16_contraction_simt_unaligned(A, O):
+    """Rows of odd length (not TMA-addressable): the FP32-pipe kernel."""
+    M, N, K = 33, 17, 45
+    g = SI.gen(3)
+    a = SI.normal((M, K), 0.0, 1.0, g).to(torch.float16)
+    b = SI.normal((K, N), 0.0, 1.0, g).to(torch.float16)
+    ref = O.matmul(O.T(a.numpy(), "f16"), O.T(b.numpy(), "f16"), "f32").data
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, M, N, K)
+    C = torch.empty((M, N), device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), None)
+    torch.cuda.synchronize()
+    assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - ref) <= 2 * gamma(K - 1) * mag + 1e-30)
