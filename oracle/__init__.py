@@ -77,6 +77,8 @@ def lib():
         L.orc_scatter_add_rows.argtypes = [i32, vp, i64, i64, vp, i64, vp]
         L.orc_scatter_add_rows.restype = i64
         L.orc_omp_max_threads.restype = i32
+        fl = ctypes.c_float
+        L.orc_adamw.argtypes = [i32, vp, vp, vp, vp, i64, fl, fl, fl, fl, fl, fl, fl]
         _lib = L
     return _lib
 
@@ -375,6 +377,20 @@ def tiny_graph(A: T, B: T) -> T:
     r = relu(c)
     sq = mul(r, r)
     return reduce_sum(sq.reshape((1, M * N)), keepdim=False).reshape(())
+
+
+def adamw_step(p: T, g: T, m: np.ndarray, v: np.ndarray, lr: float, b1: float, b2: float, eps: float,
+               wd: float, b1t: float, b2t: float):
+    """One AdamW step (decoupled decay) over one tensor in float32, the C
+    loop's operation order; returns (p', m', v').  b1t, b2t: b1^t, b2^t
+    after this step (float32 running products)."""
+    pd = np.ascontiguousarray(p.data).copy()
+    gd = np.ascontiguousarray(g.data)
+    mm = np.ascontiguousarray(m, np.float32).copy()
+    vv = np.ascontiguousarray(v, np.float32).copy()
+    lib().orc_adamw(_DT[p.dt], pd.ctypes.data, gd.ctypes.data, mm.ctypes.data, vv.ctypes.data, pd.size,
+                    lr, b1, b2, eps, wd, b1t, b2t)
+    return T(pd, p.dt), mm, vv
 
 
 def omp_max_threads() -> int:

@@ -506,6 +506,38 @@ int64_t orc_scatter_add_rows(int dt, void* dst, int64_t V, int64_t D, const int3
     return bad;
 }
 
+/* AdamW with decoupled weight decay, one step over one tensor, in float32,
+ * every operation rounded in this order (the reading of limn's optimizer as
+ * an ASSIGN graph; the arithmetic is Loshchilov & Hutter's AdamW in the
+ * order torch.optim.AdamW applies it):
+ *   p1 = p * (1 - lr*wd)
+ *   m' = b1*m + (1-b1)*g          v' = b2*v + (1-b2)*(g*g)
+ *   denom = sqrt(v') / sqrt(1 - b2t) + eps
+ *   p' = p1 - (lr / (1 - b1t)) * (m' / denom)
+ * b1t = b1^t and b2t = b2^t are the running products after this step.
+ * p and g have dtype dt (f32 / bf16 / f16 storage, float32 compute; p'
+ * rounds once into dt); m, v are float32. */
+void orc_adamw(int dt, void* p, const void* g, float* m, float* v, int64_t n, float lr, float b1, float b2,
+               float eps, float wd, float b1t, float b2t)
+{
+    const float decay = 1.0f - lr * wd;
+    const float c1 = 1.0f - b1, c2 = 1.0f - b2;
+    const float bc1 = 1.0f - b1t, bc2s = sqrtf(1.0f - b2t);
+    const float step = lr / bc1;
+    for (int64_t i = 0; i < n; ++i) {
+        const float pi = ld_f(dt, p, i), gi = ld_f(dt, g, i);
+        const float p1 = pi * decay;
+        const float mi = b1 * m[i] + c1 * gi;
+        const float g2 = gi * gi;
+        const float vi = b2 * v[i] + c2 * g2;
+        const float denom = sqrtf(vi) / bc2s + eps;
+        const float upd = mi / denom;
+        st_f(dt, p, i, p1 - step * upd);
+        m[i] = mi;
+        v[i] = vi;
+    }
+}
+
 int orc_omp_max_threads(void)
 {
 #ifdef _OPENMP
