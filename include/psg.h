@@ -313,6 +313,33 @@ psg_status psg_attention_bwd(const void* q, const psg_view* qv, const void* k, c
                              const psg_view* dvv, float scale, int causal, int32_t* d_status, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * psg_adamw_step -- one AdamW step (decoupled weight decay) over a list of
+ * tensors in one launch (limn, "nn, optim and checkpoints": optimizer steps
+ * as ASSIGN graphs over the parameters, beta**t kept on the device).
+ * Per element, in float32, each operation rounded in this order:
+ *     p1 = p * (1 - lr*wd);  m' = b1*m + (1-b1)*g;  v' = b2*v + (1-b2)*(g*g)
+ *     p' = p1 - (lr / (1 - b1^t)) * (m' / (sqrt(v') / sqrt(1 - b2^t) + eps))
+ * where b^t are the running products after this step; p' rounds once into
+ * the parameter dtype (RNE).  tensors: host array of n_tensors entries; p
+ * and g (device) share `dtype` (PSG_F32, PSG_BF16 or PSG_F16); m and v are
+ * float32 device arrays of numel elements, updated in place.  d_beta_pow:
+ * device float32 [2] = {b1^t, b2^t} before the step ({1, 1} at the start);
+ * the call advances it.  Tensors are processed 32 per launch, then one
+ * single-thread launch advances d_beta_pow.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    void* p;            /* parameters (dtype), updated in place */
+    const void* g;      /* gradients (dtype) */
+    float* m;           /* first moment, float32 */
+    float* v;           /* second moment, float32 */
+    int64_t numel;
+} psg_adamw_tensor;
+
+psg_status psg_adamw_step(const psg_adamw_tensor* tensors, int n_tensors, int dtype, float lr, float beta1,
+                          float beta2, float eps, float weight_decay, float* d_beta_pow, int32_t* d_status,
+                          void* stream);
+
+/* ---------------------------------------------------------------------------
  * psg_query_launch -- the launch a call would make, before making it (Tiki,
  * "The architecture we want": register and shared-memory budgets visible
  * before launch).  call: one of psg_call; v: the output view the call would

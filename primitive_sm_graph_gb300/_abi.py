@@ -57,6 +57,11 @@ class psg_reduce_stage(ctypes.Structure):
                 ("prologue", ctypes.POINTER(psg_node))]
 
 
+class psg_adamw_tensor(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_void_p), ("g", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("numel", ctypes.c_int64)]
+
+
 class PsgError(RuntimeError):
     def __init__(self, status: int, call: str):
         self.status = status
@@ -87,13 +92,15 @@ def _load():
     L.psg_query_launch.argtypes = [i32, V, P32, P32, P32, P32]
     fl = ctypes.c_float
     L.psg_attention_fwd.argtypes = [vp, V, vp, V, vp, V, vp, V, vp, fl, i32, vp, vp]
+    L.psg_adamw_step.argtypes = [ctypes.POINTER(psg_adamw_tensor), i32, i32, fl, fl, fl, fl, fl, vp, vp, vp]
     L.psg_attention_bwd.argtypes = [vp, V, vp, V, vp, V, vp, V, vp, V, vp, vp, vp, V, vp, V, vp, V, fl, i32, vp,
                                     vp]
     L.psg_status_string.argtypes = [i32]
     L.psg_status_string.restype = ctypes.c_char_p
     L.psg_version.restype = ctypes.c_char_p
     for f in ("psg_elementwise", "psg_reduce_rows", "psg_permute", "psg_contract", "psg_gather",
-              "psg_scatter_add", "psg_query_launch", "psg_attention_fwd", "psg_attention_bwd"):
+              "psg_scatter_add", "psg_query_launch", "psg_attention_fwd", "psg_attention_bwd",
+              "psg_adamw_step"):
         getattr(L, f).restype = i32
     return L
 
@@ -266,6 +273,24 @@ def psg_attention_bwd(q, qv, k, kv, v, vv, o, ov, do, dov, lse, delta, dq, dqv, 
                                _stream(stream))
     if check:
         _check(st, "psg_attention_bwd")
+    return st
+
+
+def psg_adamw_step(params, grads, ms, vs, lr, beta1, beta2, eps, weight_decay, beta_pow, d_status=None,
+                   stream=None, check=True) -> int:
+    """One AdamW step over lists of torch tensors (params and grads share a
+    dtype; ms, vs float32); beta_pow: float32 device tensor [2]."""
+    n = len(params)
+    arr = (psg_adamw_tensor * max(1, n))()
+    for i, (p, g, m, v) in enumerate(zip(params, grads, ms, vs)):
+        arr[i].p, arr[i].g, arr[i].m, arr[i].v = _ptr(p), _ptr(g), _ptr(m), _ptr(v)
+        arr[i].numel = p.numel()
+    dt = DTYPES[__import__("primitive_sm_graph_gb300.tensor_util", fromlist=["x"]).dtype_name(params[0].dtype)] \
+        if n else 0
+    st = lib.psg_adamw_step(arr, n, dt, float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                            _ptr(beta_pow), _ptr(d_status), _stream(stream))
+    if check:
+        _check(st, "psg_adamw_step")
     return st
 
 
