@@ -550,6 +550,17 @@ class Rows:
         e1.record()
         torch.cuda.synchronize()
         rms = e0.elapsed_time(e1) / reps
+        # a training step: the same plus one AdamW step over the seven weights
+        from primitive_sm_graph_gb300.workloads import AdamW, gpt_train_step
+        tw = {k: v.clone() for k, v in dw.items()}
+        opt = AdamW([tw[k] for k in GPT_WEIGHTS])
+        trep = G.Replay(lambda t: gpt_train_step(t, tw, H, opt), dtok)
+        e0.record()
+        for _ in range(reps):
+            trep.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        tms = e0.elapsed_time(e1) / reps
         # algorithmic flops of the contractions: 8192 tokens x 6,553,600 linear
         # + 2 x B*H*T*T*hd attention (QK^T and PV), times 3 for fwd + bwd
         Bn, T, V, D, Hh, F = (SI.GPT_SHAPES[k] for k in ("B", "T", "V", "D", "H", "F"))
@@ -559,9 +570,11 @@ class Rows:
         return {"ms_per_step": round(ms, 3), "kernels_per_step": kernels, "flops": flops,
                 "achieved": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "replay_ms_per_step": round(rms, 4),
+                "train_replay_ms_per_step": round(tms, 4),
                 "replay_achieved": round(flops / (rms * 1e-3) / 1e12, 3),
                 "note": "ms_per_step: host wall clock, graph building and scheduling included; "
-                        "replay: the recorded step relaunched (CUDA Graph), device time",
+                        "replay: the recorded step relaunched (CUDA Graph), device time; "
+                        "train_replay: forward, backward and one AdamW step (one launch for all weights)",
                 "workload": "1-layer byte GPT fwd+bwd B32 T256 V256 d512 H8 MLP2048 bf16"}
 
 

@@ -127,3 +127,31 @@ def gpt_step(tok: torch.Tensor, weights: dict, H: int, pick=None, mask=None, tap
     if taps is not None:
         taps.update(zip(names, outs[1 + len(GPT_WEIGHTS):]))
     return outs[0], dict(zip(GPT_WEIGHTS, outs[1:1 + len(GPT_WEIGHTS)]))
+
+
+class AdamW:
+    """Decoupled-weight-decay Adam over a fixed list of parameter tensors:
+    float32 moments and the running beta powers live on the device, and a
+    step is one psg_adamw_step call (one launch for all the tensors)."""
+
+    def __init__(self, params, lr=3e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1):
+        from . import _abi as A
+        self._A = A
+        self.params = list(params)
+        self.lr, self.betas, self.eps, self.wd = lr, betas, eps, weight_decay
+        self.m = [torch.zeros(p.numel(), dtype=torch.float32, device=p.device) for p in self.params]
+        self.v = [torch.zeros_like(m) for m in self.m]
+        self.beta_pow = torch.ones(2, dtype=torch.float32, device=self.params[0].device)
+
+    def step(self, grads):
+        self._A.psg_adamw_step(self.params, [g.contiguous() for g in grads], self.m, self.v, self.lr, self.betas[0],
+                               self.betas[1], self.eps, self.wd, self.beta_pow,
+                               stream=torch.cuda.current_stream().cuda_stream)
+
+
+def gpt_train_step(tok: torch.Tensor, weights: dict, H: int, opt: AdamW, fused_attention=True):
+    """Forward, backward and one AdamW step of the block (weights updated in
+    place); returns the loss tensor."""
+    loss, grads = gpt_step(tok, weights, H, fused_attention=fused_attention)
+    opt.step([grads[k] for k in GPT_WEIGHTS])
+    return loss

@@ -59,3 +59,31 @@ def test_gpt_block_step_replay_is_bit_exact(G):
     got2 = rep(*ins2)
     assert all(_same(x, y) for x, y in zip(got2, ref2))
     assert not _same(got2[0], got[0])          # the loss did change with the inputs
+
+
+def test_gpt_train_step_replay_updates_like_eager(G):
+    """Forward, backward and AdamW recorded once: replayed twice from the
+    same start it gives the eager weights bit for bit."""
+    from primitive_sm_graph_gb300.workloads import GPT_WEIGHTS, AdamW, gpt_train_step
+    shapes = dict(B=2, T=16, V=64, D=64, H=2, F=128)
+    tok, w = SI.gpt_block(6, **shapes)
+    dtok = tok.cuda()
+    w_eager = {k: v.cuda() for k, v in w.items()}
+    opt_e = AdamW([w_eager[k] for k in GPT_WEIGHTS], lr=1e-2)
+    for _ in range(2):
+        gpt_train_step(dtok, w_eager, 2, opt_e)
+    w_rep = {k: v.cuda() for k, v in w.items()}
+    opt_r = AdamW([w_rep[k] for k in GPT_WEIGHTS], lr=1e-2)
+    snap = {k: v.clone() for k, v in w_rep.items()}
+    rep = G.Replay(lambda t: gpt_train_step(t, w_rep, 2, opt_r), dtok)
+    # the recording ran the step twice (compile + capture warm-up): restart from the snapshot
+    for k in GPT_WEIGHTS:
+        w_rep[k].copy_(snap[k])
+    for x in opt_r.m + opt_r.v:
+        x.zero_()
+    opt_r.beta_pow.fill_(1.0)
+    for _ in range(2):
+        rep.replay()
+    torch.cuda.synchronize()
+    for k in GPT_WEIGHTS:
+        assert _same(w_rep[k], w_eager[k]), k
