@@ -647,6 +647,13 @@ def profile_case(A, name, iters):
     if name in ("chain", "transpose"):
         step = Step(A)
         fn = getattr(step, name)
+    elif name == "gpt":
+        from primitive_sm_graph_gb300.workloads import gpt_step
+        tok, w = SI.gpt_block(0, **SI.GPT_SHAPES)
+        dtok, dw = tok.cuda(), {k: v.cuda() for k, v in w.items()}
+
+        def fn(_s):
+            gpt_step(dtok, dw, SI.GPT_SHAPES["H"])
     else:
         fn, _ = getattr(Rows(A, peaks()), name)()
     s = torch.cuda.current_stream().cuda_stream
@@ -668,7 +675,7 @@ def main():
                          "gather,scatter,tiny_graph,gpt), 'all' or 'none'")
     ap.add_argument("--profile-case", default=None,
                     help="run one workload --iters times and exit (for a profiler capture); "
-                         "chain, transpose or a row name")
+                         "chain, transpose, gpt (one eager forward + backward) or a row name")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3:

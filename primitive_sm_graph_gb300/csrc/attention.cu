@@ -263,24 +263,39 @@ struct BwdBars {
 };
 
 // D[b, h, t] = sum_d dO[b, t, h, d] * O[b, t, h, d] (float32 total of exact
-// bf16 products, in ascending d), one warp per row
+// bf16 products, folded in a fixed order): 8 lanes per row, 16 bytes of O
+// and dO per lane, a 3-level shuffle fold inside the 8-lane group
 __global__ void __launch_bounds__(256) attn_delta(const __grid_constant__ AttnTensor o,
                                                   const __grid_constant__ AttnTensor dO,
                                                   const __grid_constant__ AttnParams p)
 {
     const int64_t rows = (int64_t)p.B * p.T * p.H;
-    const int lane = threadIdx.x & 31;
-    for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += (int64_t)gridDim.x * 8) {
-        const int h = (int)(r % p.H);
-        const int t = (int)((r / p.H) % p.T);
-        const int b = (int)(r / ((int64_t)p.H * p.T));
-        const __nv_bfloat162 x = ((const __nv_bfloat162*)((const __nv_bfloat16*)o.ptr + o.off + b * o.sb + t * o.st +
-                                                          h * o.sh))[lane];
-        const __nv_bfloat162 y = ((const __nv_bfloat162*)((const __nv_bfloat16*)dO.ptr + dO.off + b * dO.sb +
-                                                          t * dO.st + h * dO.sh))[lane];
-        float v = __fadd_rn(__fmul_rn(__low2float(x), __low2float(y)), __fmul_rn(__high2float(x), __high2float(y)));
-        for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) p.delta[((int64_t)b * p.H + h) * p.T + t] = v;
+    const int sub = threadIdx.x & 7, grp = (threadIdx.x & 31) >> 3;
+    // warp-uniform loop over groups of 4 rows (the shuffles need every lane)
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 4; r0 < rows; r0 += warps * 4) {
+        const int64_t r = r0 + grp;
+        const bool ok = r < rows;
+        float v = 0.0f;
+        int b = 0, t = 0, h = 0;
+        if (ok) {
+            h = (int)(r % p.H);
+            t = (int)((r / p.H) % p.T);
+            b = (int)(r / ((int64_t)p.H * p.T));
+            const uint4 x =
+                ((const uint4*)((const __nv_bfloat16*)o.ptr + o.off + b * o.sb + t * o.st + h * o.sh))[sub];
+            const uint4 y =
+                ((const uint4*)((const __nv_bfloat16*)dO.ptr + dO.off + b * dO.sb + t * dO.st + h * dO.sh))[sub];
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float x0 = __uint_as_float(xs[u] << 16), x1 = __uint_as_float(xs[u] & 0xffff0000u);
+                const float y0 = __uint_as_float(ys[u] << 16), y1 = __uint_as_float(ys[u] & 0xffff0000u);
+                v = __fadd_rn(v, __fadd_rn(__fmul_rn(x0, y0), __fmul_rn(x1, y1)));
+            }
+        }
+        for (int off = 4; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off, 8));
+        if (ok && sub == 0) p.delta[((int64_t)b * p.H + h) * p.T + t] = v;
     }
 }
 
@@ -685,7 +700,7 @@ psg_status launch_attention_bwd(const AttnTensor& q, const AttnTensor& k, const 
     });
     if (err != cudaSuccess) return PSG_E_CUDA;
     const int64_t rows = (int64_t)p.B * p.T * p.H;
-    const int dgrid = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 8);
+    const int dgrid = (int)std::min<int64_t>((rows + 31) / 32, (int64_t)num_sms() * 16);  // 32 rows a block
     attn_delta<<<dgrid, 256, 0, s>>>(o, dO, p);
     const unsigned tiles = (unsigned)((p.T + QT - 1) / QT);
     const dim3 grid(tiles, (unsigned)p.H, (unsigned)p.B);

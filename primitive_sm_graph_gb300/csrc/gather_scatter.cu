@@ -139,12 +139,21 @@ __global__ void __launch_bounds__(1024) bitonic_local(unsigned long long* keys, 
 constexpr int SMALL_SORT = 16384;
 constexpr int SMALL_SORT_SMEM = SMALL_SORT * 8;  // 128 KB
 
+template <int E>
 __global__ void __launch_bounds__(1024) sort_small(const int32_t* __restrict__ idx, int64_t n, int64_t V, int npow2,
                                                    unsigned long long* __restrict__ keys, int32_t* status)
 {
+    // N = 1024 * E keys (padding ~0 sorts last); thread t holds keys
+    // t*E .. t*E+E-1 in registers: a step (k, j) pairs i with i ^ j, inside the
+    // thread for j < E, across lanes (shuffles) for j < 32 E, and through
+    // shared memory above that
     extern __shared__ unsigned long long sk[];
     const int t = threadIdx.x;
-    for (int i = t; i < npow2; i += blockDim.x) {
+    constexpr int N = 1024 * E;
+    unsigned long long r[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int64_t i = (int64_t)t * E + e;
         unsigned long long k = ~0ull;
         if (i < n) {
             const int64_t v = idx[i];
@@ -155,19 +164,43 @@ __global__ void __launch_bounds__(1024) sort_small(const int32_t* __restrict__ i
                 report(status, PSG_E_INDEX_OUT_OF_RANGE);
             }
         }
-        sk[i] = k;
+        r[e] = k;
     }
-    __syncthreads();
-    for (int k = 2; k <= npow2; k <<= 1) {
+    for (int k = 2; k <= N; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = t; i < npow2 / 2; i += blockDim.x) {
-                const int a = ((i & ~(j - 1)) << 1) | (i & (j - 1));
-                cmp_swap(sk[a], sk[a + j], (a & k) == 0);
+            if (j >= 32 * E) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) sk[t * E + e] = r[e];
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = t * E + e;
+                    const unsigned long long q = sk[i ^ j];
+                    const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+                    r[e] = keep_min ? (q < r[e] ? q : r[e]) : (q > r[e] ? q : r[e]);
+                }
+                __syncthreads();
+            } else if (j >= E) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = t * E + e;
+                    const unsigned long long q = __shfl_xor_sync(0xffffffffu, r[e], j / E);
+                    const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+                    r[e] = keep_min ? (q < r[e] ? q : r[e]) : (q > r[e] ? q : r[e]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if (e & j) continue;
+                    const bool up = (((t * E + e) & k) == 0);
+                    cmp_swap(r[e], r[e | j], up);
+                }
             }
-            __syncthreads();
         }
     }
-    for (int i = t; i < npow2; i += blockDim.x) keys[i] = sk[i];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        if (t * E + e < npow2) keys[t * E + e] = r[e];
 }
 
 // one global step (k, j) with j >= LOCAL_SORT: one thread per pair
@@ -574,11 +607,22 @@ psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void
         static std::once_flag once;
         static cudaError_t err = cudaSuccess;
         std::call_once(once, [] {
-            err = cudaFuncSetAttribute((const void*)sort_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMALL_SORT_SMEM);
+            const void* fns[5] = {(const void*)sort_small<1>, (const void*)sort_small<2>, (const void*)sort_small<4>,
+                                  (const void*)sort_small<8>, (const void*)sort_small<16>};
+            for (const void* f : fns)
+                if (err == cudaSuccess)
+                    err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMALL_SORT_SMEM);
         });
         if (err != cudaSuccess) return PSG_E_CUDA;
-        sort_small<<<1, 1024, (size_t)np2 * 8, s>>>(L.idx, L.n, L.V, (int)np2, keys, L.status);
+        const int N = np2 < 1024 ? 1024 : (int)np2;
+        const size_t sm = (size_t)N * 8;
+        switch (N / 1024) {
+        case 1: sort_small<1><<<1, 1024, sm, s>>>(L.idx, L.n, L.V, (int)np2, keys, L.status); break;
+        case 2: sort_small<2><<<1, 1024, sm, s>>>(L.idx, L.n, L.V, (int)np2, keys, L.status); break;
+        case 4: sort_small<4><<<1, 1024, sm, s>>>(L.idx, L.n, L.V, (int)np2, keys, L.status); break;
+        case 8: sort_small<8><<<1, 1024, sm, s>>>(L.idx, L.n, L.V, (int)np2, keys, L.status); break;
+        default: sort_small<16><<<1, 1024, sm, s>>>(L.idx, L.n, L.V, (int)np2, keys, L.status); break;
+        }
     } else {
         make_keys<<<grid_for((const void*)make_keys, 256, (np2 + 255) / 256), 256, 0, s>>>(L.idx, L.n, L.V, np2,
                                                                                          keys, L.status);

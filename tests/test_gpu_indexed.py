@@ -78,7 +78,8 @@ def _scatter(A, dst, idx, upd):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16", "i32", "f64"])
-@pytest.mark.parametrize("case", ["embedding_grad", "single_row", "permutation", "ragged", "large", "long_runs"])
+@pytest.mark.parametrize("case", ["embedding_grad", "single_row", "permutation", "ragged", "large", "long_runs",
+                                  "wide_small", "wide", "wide_max"])
 def test_scatter_add_matches_oracle(A, O, dt, case):
     g = SI.gen(sum(map(ord, dt + case)))
     if case == "embedding_grad":   # [8192, 512] into [256, 512], ~32 collisions per row
@@ -96,8 +97,11 @@ def test_scatter_add_matches_oracle(A, O, dt, case):
     elif case == "large":          # past one sorting block: global bitonic steps
         V, D, n = 4000, 2, 20000
         idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
-    else:                          # runs of ~33,000 equal indices (run ends found 32 keys at a time)
+    elif case == "long_runs":      # runs of ~33,000 equal indices (run ends found 32 keys at a time)
         V, D, n = 3, 4, 100000
+        idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
+    else:                          # many destination rows: the one-block sort (1, 16 keys a thread)
+        V, D, n = {"wide_small": (50000, 3, 700), "wide": (100000, 2, 9000), "wide_max": (60000, 2, 16384)}[case]
         idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
     dst0 = _vals(g, (V, D), dt)
     upd = _vals(g, (n, D), dt)
