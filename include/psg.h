@@ -10,6 +10,7 @@
  *   psg_reduce_rows   SUM/MAX row reductions with fused prologue/epilogue;
  *   psg_permute       CONTIGUOUS of a permuted View (tiled transpose);
  *   psg_contract      matmul as a broadcast MUL followed by a SUM over k;
+ *   psg_contract_ws   the same with a split-K workspace (psg_contract_workspace);
  *   psg_gather / psg_scatter_add   the indexed ops along dim 0.
  *
  * Conventions shared by every call
@@ -224,6 +225,27 @@ psg_status psg_permute(const void* in, const psg_view* in_v, const int32_t* perm
  * ------------------------------------------------------------------------- */
 psg_status psg_contract(const void* A, const psg_view* Av, const void* B, const psg_view* Bv,
                         void* C, const psg_view* Cv, int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * psg_contract_workspace / psg_contract_ws -- psg_contract with a caller
+ * workspace that lets the bf16 / f16 tensor-core kernel split K when the
+ * output has too few 128x256 tiles to occupy the GPU (a weight gradient:
+ * small M x N, long K).  Each split sums its own range of K blocks into a
+ * float32 partial; a second launch adds the partials in split order and
+ * rounds once into C.  The result is deterministic (the split count depends
+ * only on the shapes and the GPU's SM count) and within psg_contract's bound:
+ * it is still a float32 sum of the same K exact products.
+ * psg_contract_workspace: bytes of device workspace psg_contract_ws would use
+ *   for these views (0 when it would not split; also 0 for invalid views).
+ * psg_contract_ws: as psg_contract; workspace: device memory, 16-byte aligned,
+ *   owned by the caller, not read before it is written, free again once the
+ *   stream passes the call.  NULL or fewer than the queried bytes runs the
+ *   unsplit kernel.
+ * ------------------------------------------------------------------------- */
+size_t psg_contract_workspace(const psg_view* Av, const psg_view* Bv, const psg_view* Cv);
+psg_status psg_contract_ws(const void* A, const psg_view* Av, const void* B, const psg_view* Bv,
+                           void* C, const psg_view* Cv, void* workspace, size_t ws_bytes,
+                           int32_t* d_status, void* stream);
 
 /* ---------------------------------------------------------------------------
  * psg_gather -- GATHER along dim 0 (limn, "The op set"; nn.Embedding is the

@@ -83,6 +83,9 @@ def _load():
     L.psg_reduce_rows.argtypes = [S, i32, N, i32, ctypes.POINTER(vp), V, i32, vp, V, vp, vp]
     L.psg_permute.argtypes = [vp, V, P32, vp, V, vp]
     L.psg_contract.argtypes = [vp, V, vp, V, vp, V, vp, vp]
+    L.psg_contract_ws.argtypes = [vp, V, vp, V, vp, V, vp, sz, vp, vp]
+    L.psg_contract_workspace.argtypes = [V, V, V]
+    L.psg_contract_workspace.restype = sz
     L.psg_gather.argtypes = [vp, V, vp, i64, vp, V, vp, vp]
     L.psg_scatter_workspace.argtypes = [i64]
     L.psg_scatter_workspace.restype = sz
@@ -98,7 +101,7 @@ def _load():
     L.psg_status_string.argtypes = [i32]
     L.psg_status_string.restype = ctypes.c_char_p
     L.psg_version.restype = ctypes.c_char_p
-    for f in ("psg_elementwise", "psg_reduce_rows", "psg_permute", "psg_contract", "psg_gather",
+    for f in ("psg_elementwise", "psg_reduce_rows", "psg_permute", "psg_contract", "psg_contract_ws", "psg_gather",
               "psg_scatter_add", "psg_query_launch", "psg_attention_fwd", "psg_attention_bwd",
               "psg_adamw_step"):
         getattr(L, f).restype = i32
@@ -247,6 +250,19 @@ def psg_contract(A, Av, B, Bv, C, Cv, d_status=None, stream=None, check=True) ->
                           ctypes.byref(Cv), _ptr(d_status), _stream(stream))
     if check:
         _check(st, "psg_contract")
+    return st
+
+
+def psg_contract_workspace(Av, Bv, Cv) -> int:
+    """Device bytes psg_contract_ws would use to split K for these views (0: no split)."""
+    return int(lib.psg_contract_workspace(ctypes.byref(Av), ctypes.byref(Bv), ctypes.byref(Cv)))
+
+
+def psg_contract_ws(A, Av, B, Bv, C, Cv, workspace, ws_bytes, d_status=None, stream=None, check=True) -> int:
+    st = lib.psg_contract_ws(_ptr(A), ctypes.byref(Av), _ptr(B), ctypes.byref(Bv), _ptr(C), ctypes.byref(Cv),
+                             _ptr(workspace), int(ws_bytes), _ptr(d_status), _stream(stream))
+    if check:
+        _check(st, "psg_contract_ws")
     return st
 
 

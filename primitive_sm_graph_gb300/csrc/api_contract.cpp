@@ -160,8 +160,10 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
 
 using namespace psg;
 
-extern "C" psg_status psg_contract(const void* A, const psg_view* Av, const void* B, const psg_view* Bv, void* C,
-                                   const psg_view* Cv, int32_t* d_status, void* stream)
+namespace {
+
+psg_status contract_impl(const void* A, const psg_view* Av, const void* B, const psg_view* Bv, void* C,
+                         const psg_view* Cv, void* ws, size_t ws_bytes, int32_t* d_status, void* stream)
 {
     bool tc;
     TcOperands T;
@@ -169,6 +171,8 @@ extern "C" psg_status psg_contract(const void* A, const psg_view* Av, const void
     Batch bt;
     psg_status st = plan_contract(A, Av, B, Bv, C, Cv, d_status, &tc, &T, &S, &bt);
     if (st != PSG_OK) return st;
+    T.ws = ws;
+    T.ws_bytes = ws_bytes;
     if (S.M == 0 || S.N == 0) return PSG_OK;
     if (S.K == 0) {
         // an empty SUM is its identity: every cell 0 (through the SIMT kernel)
@@ -199,4 +203,35 @@ extern "C" psg_status psg_contract(const void* A, const psg_view* Av, const void
         if (st != PSG_OK) return st;
     }
     return PSG_OK;
+}
+
+}  // namespace
+
+extern "C" psg_status psg_contract(const void* A, const psg_view* Av, const void* B, const psg_view* Bv, void* C,
+                                   const psg_view* Cv, int32_t* d_status, void* stream)
+{
+    return contract_impl(A, Av, B, Bv, C, Cv, nullptr, 0, d_status, stream);
+}
+
+extern "C" psg_status psg_contract_ws(const void* A, const psg_view* Av, const void* B, const psg_view* Bv, void* C,
+                                      const psg_view* Cv, void* workspace, size_t ws_bytes, int32_t* d_status,
+                                      void* stream)
+{
+    return contract_impl(A, Av, B, Bv, C, Cv, workspace, ws_bytes, d_status, stream);
+}
+
+extern "C" size_t psg_contract_workspace(const psg_view* Av, const psg_view* Bv, const psg_view* Cv)
+{
+    // shapes and dtypes decide the split; pointers and strides only decide
+    // whether the tensor-core kernel runs at all (if not, nothing is used)
+    if (!Av || !Bv || !Cv || Av->ndim < 3 || Av->ndim > 6 || Bv->ndim != Av->ndim) return 0;
+    if (Av->dtype != Bv->dtype || (Av->dtype != PSG_BF16 && Av->dtype != PSG_F16)) return 0;
+    const int r = Av->ndim;
+    int64_t batch = 1;
+    for (int d = 0; d < r - 3; ++d) batch *= Av->shape[d];
+    const int64_t M = Av->shape[r - 3], N = Av->shape[r - 2], K = Av->shape[r - 1];
+    if (batch <= 0 || M <= 0 || N <= 0 || K <= 0 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return 0;
+    size_t bytes = 0;
+    contract_tc_splits(M, N, K, batch, &bytes);
+    return bytes;
 }

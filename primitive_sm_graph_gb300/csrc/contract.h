@@ -11,6 +11,8 @@ struct TcParams {
     int num_m, num_n, num_k;    // tile counts (filled by the launcher)
     int c_dtype;
     int ab_dtype;               // bf16 or f16 (tc_gemm), f32 (tc_gemm_tf32x3)
+    int splits, kb_per;         // split-K: K-block ranges per tile (1: none)
+    float* ws;                  // split-K partials [splits][batch][M][N] float32
     void* C;
     int32_t* status;
     int64_t c_offset, c_rs, c_cs, c_bs;
@@ -18,6 +20,8 @@ struct TcParams {
 
 struct TcOperands {
     TcParams p;
+    void* ws;                   // caller workspace for split-K partials (may be null)
+    size_t ws_bytes;
     const void* A;  // at the View's offset
     const void* B;
     int64_t a_ms, a_ks, a_bs;   // element strides of A along m, k, batch
@@ -36,6 +40,9 @@ struct SimtParams {
 };
 
 psg_status launch_contract_tc(const TcOperands& o, void* stream);
+// split-K plan of the bf16 / f16 kernel: splits (1 = none) and the
+// workspace bytes they need, for an output of tiles that leaves SMs idle
+int contract_tc_splits(int64_t M, int64_t N, int64_t K, int64_t batch, size_t* bytes);
 void query_contract_tc(int64_t tiles, int* grid, int* block, int* smem, int* regs);
 // float32 operands, 3xTF32 on the tensor cores (same operand rules as the bf16 path)
 psg_status launch_contract_tf32(const TcOperands& o, void* stream);

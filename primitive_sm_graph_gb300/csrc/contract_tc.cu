@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int total = p.num_m * p.num_n * p.batch;
+    const int units = total * p.splits;  // (tile, K range) work units
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -105,11 +106,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
             uint32_t ph = 0;
             uint32_t armed = 0, armed_ph = 0;  // per-stage flags / parity of the last arm
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const int t = u / p.splits, sp = u - t * p.splits;
+                const int kb0 = sp * p.kb_per, kb1 = min(p.num_k, kb0 + p.kb_per);
                 int b, mb, nb;
                 tile_coords(p.num_m, p.num_n, t, b, mb, nb);
                 const int m0 = mb * BM, n0 = nb * BN;
-                for (int kb = 0; kb < p.num_k; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!bar_wait(&bars->empty[stage], ph ^ 1u, &bars->abort, p.status)) { ok = false; break; }
                     uint8_t* sa = smem + stage * STAGE_BYTES;
                     uint8_t* sb = sa + A_BYTES;
@@ -160,12 +163,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
             uint32_t aph[2] = {0u, 0u};
             bool ok = true;
             int local = 0;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+                const int kb0 = (u % p.splits) * p.kb_per, kb1 = min(p.num_k, kb0 + p.kb_per);
                 const int acc = local & 1;
                 if (!bar_wait(&bars->tempty[acc], aph[acc] ^ 1u, &bars->abort, p.status)) break;
                 tc_fence_after();
                 const uint32_t dtm = tmem + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < p.num_k; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!bar_wait(&bars->full[stage], ph, &bars->abort, p.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         mma_bf16(dtm, ad + (uint64_t)(k * a_step), bd + (uint64_t)(k * b_step), idesc,
-                                 (kb | k) != 0 ? 1u : 0u);
+                                 (kb != kb0 || k != 0) ? 1u : 0u);
                     mma_commit(&bars->empty[stage]);  // frees the stage when these MMAs finish
                     if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                 }
@@ -193,7 +197,8 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
         const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
         uint32_t aph[2] = {0u, 0u};
         int local = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+            const int t = u / p.splits, sp = u - t * p.splits;
             const int acc = local & 1;
             if (!bar_wait(&bars->tfull[acc], aph[acc], &bars->abort, p.status)) break;
             aph[acc] ^= 1u;
@@ -207,7 +212,18 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
                 __syncwarp();  // tcgen05.ld is warp-collective: reach it converged
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), r);
                 const int n0 = nb * BN + c;
-                if (m < p.M) {
+                if (m < p.M && p.splits > 1) {
+                    // split-K: this K range's float32 total, summed later in split order
+                    float* dst = p.ws + (((int64_t)sp * p.batch + b) * p.M + m) * p.N + n0;
+                    if (n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            ((uint4*)dst)[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    } else {
+                        for (int j = 0; j < 32; ++j)
+                            if (n0 + j < p.N) dst[j] = __uint_as_float(r[j]);
+                    }
+                } else if (m < p.M) {
                     if (p.c_dtype == PSG_BF16) {
                         __nv_bfloat16* dst = (__nv_bfloat16*)p.C + crow + n0;
                         if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
@@ -256,6 +272,23 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
 }
 
+// C = sum over the splits, in split order, of the float32 partials, rounded
+// once into C's dtype
+__global__ void __launch_bounds__(256) splitk_reduce(const __grid_constant__ TcParams p)
+{
+    const int64_t cells = (int64_t)p.batch * p.M * p.N;
+    const int64_t stride = cells;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < cells; e += (int64_t)gridDim.x * blockDim.x) {
+        float acc = p.ws[e];
+        for (int s = 1; s < p.splits; ++s) acc = __fadd_rn(acc, p.ws[e + s * stride]);
+        const int64_t n = e % p.N, bm = e / p.N, m = bm % p.M, b = bm / p.M;
+        const int64_t o = p.c_offset + b * p.c_bs + m * p.c_rs + n * p.c_cs;
+        if (p.c_dtype == PSG_F32) ((float*)p.C)[o] = acc;
+        else if (p.c_dtype == PSG_F16) ((__half*)p.C)[o] = __float2half_rn(acc);
+        else ((__nv_bfloat16*)p.C)[o] = __float2bfloat16_rn(acc);
+    }
+}
+
 // 3-D tensor map over a bf16 or f16 operand: dims {inner, outer, batch}.
 bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t batch, int64_t outer_stride,
               int64_t batch_stride, uint32_t box_inner, uint32_t box_outer, bool f16)
@@ -274,9 +307,35 @@ bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, 
 
 }  // namespace
 
+int contract_tc_splits(int64_t M, int64_t N, int64_t K, int64_t batch, size_t* bytes)
+{
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN) * batch;
+    const int64_t num_k = (K + BK - 1) / BK;
+    const int64_t sms = num_sms();
+    *bytes = 0;
+    // only when the output's tiles leave most SMs idle and K is long
+    if (tiles * 2 > sms || num_k < 8) return 1;
+    int64_t s = std::min<int64_t>(std::min<int64_t>(sms / tiles, num_k / 4), 16);
+    if (s < 2) return 1;
+    const int64_t per = (num_k + s - 1) / s;
+    s = (num_k + per - 1) / per;  // no empty range
+    *bytes = (size_t)(s * batch * M * N * 4);
+    return (int)s;
+}
+
 psg_status launch_contract_tc(const TcOperands& o, void* stream)
 {
     TcParams p = o.p;
+    p.splits = 1;
+    p.ws = nullptr;
+    if (o.ws) {
+        size_t need = 0;
+        const int s = contract_tc_splits(p.M, p.N, p.K, p.batch, &need);
+        if (s > 1 && need <= o.ws_bytes && ((uintptr_t)o.ws & 15) == 0) {
+            p.splits = s;
+            p.ws = (float*)o.ws;
+        }
+    }
     if (p.M == 0 || p.N == 0 || p.batch == 0) return PSG_OK;
     CUtensorMap ma, mb;
     // batch strides of a single batch are never used; keep them a legal multiple of 16 bytes
@@ -291,15 +350,21 @@ psg_status launch_contract_tc(const TcOperands& o, void* stream)
     p.num_m = (p.M + BM - 1) / BM;
     p.num_n = (p.N + BN - 1) / BN;
     p.num_k = (p.K + BK - 1) / BK;
+    p.kb_per = (p.num_k + p.splits - 1) / p.splits;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute((const void*)tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return PSG_E_CUDA;
-    const int64_t tiles = (int64_t)p.num_m * p.num_n * p.batch;
-    const int grid = (int)std::min<int64_t>(tiles, num_sms());
+    const int64_t units = (int64_t)p.num_m * p.num_n * p.batch * p.splits;
+    const int grid = (int)std::min<int64_t>(units, num_sms());
     tc_gemm<<<grid, THREADS, SMEM_BYTES, (cudaStream_t)stream>>>(ma, mb, p);
+    if (p.splits > 1) {
+        const int64_t cells = (int64_t)p.batch * p.M * p.N;
+        const int rgrid = (int)std::min<int64_t>((cells + 255) / 256, (int64_t)num_sms() * 8);
+        splitk_reduce<<<rgrid, 256, 0, (cudaStream_t)stream>>>(p);
+    }
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 

@@ -848,7 +848,13 @@ class Executor:
         Bv = A.make_view(dy, shape, sb, vy.offset, None, by.numel())
         Cv = A.make_view(out_dtype, shape[:-1], sc, 0, None, out.numel())
         if out.numel():
-            A.psg_contract(bx, Av, by, Bv, out, Cv, self._status(), stream=self._s())
+            need = A.psg_contract_workspace(Av, Bv, Cv)
+            if need:
+                # few output tiles over a long K: the kernel splits K into this workspace
+                ws = self._workspace(need)
+                A.psg_contract_ws(bx, Av, by, Bv, out, Cv, ws, ws.numel(), self._status(), stream=self._s())
+            else:
+                A.psg_contract(bx, Av, by, Bv, out, Cv, self._status(), stream=self._s())
         self.log.append(("contract", tuple(shape), dx, out_dtype))
         return out, View(out_shape)
 

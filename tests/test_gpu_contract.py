@@ -252,3 +252,72 @@ def test_f16_contraction_simt_unaligned(A, O):
     A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), None)
     torch.cuda.synchronize()
     assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - ref) <= 2 * gamma(K - 1) * mag + 1e-30)
+
+
+def _split_case(A, M, N, K, a_layout, b_layout, out_dt, batch, seed):
+    g = SI.gen(seed)
+    s = 1.0 / float(np.sqrt(K))
+    shp_a, shp_b = ((batch, M, K), (batch, K, N)) if batch else ((M, K), (K, N))
+    a = SI.normal(shp_a, 0.0, s, g, torch.bfloat16)
+    b = SI.normal(shp_b, 0.0, s, g, torch.bfloat16)
+    if batch:
+        dA, dB = dev(a), dev(b)
+    else:
+        dA, dB = dev(_storage(a, a_layout)), dev(_storage(b, b_layout))
+    Av, Bv = _views(A, dA, dB, M, N, K, a_layout, b_layout, batch=batch)
+    C = torch.empty(((batch,) if batch else ()) + (M, N), dtype=storage_dtype(out_dt), device="cuda")
+    return a, b, dA, dB, Av, Bv, C
+
+
+@pytest.mark.parametrize("M,N,K,a_layout,b_layout,out_dt,batch", [
+    (256, 512, 4096, "mk", "kn", "f32", None),      # 4 tiles, 16 splits of 4 K blocks
+    (200, 300, 3000, "km", "nk", "bf16", None),     # ragged tiles and a short last split
+    (130, 70, 1000, "mk", "nk", "f32", None),
+    (128, 256, 2048, "mk", "kn", "bf16", 3)])       # batched: 3 tiles
+def test_split_k_matches_oracle(A, O, M, N, K, a_layout, b_layout, out_dt, batch):
+    """Few output tiles over a long K: psg_contract_ws splits K; the result
+    stays within the SUM bound, and is the same bits on every call."""
+    a, b, dA, dB, Av, Bv, C = _split_case(A, M, N, K, a_layout, b_layout, out_dt, batch, M + N + K)
+    need = A.psg_contract_workspace(Av, Bv, A.view_of(C))
+    assert need > 0
+    ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    A.psg_contract_ws(dA, Av, dB, Bv, C, A.view_of(C), ws, need, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    first = C.clone()
+    ws.fill_(0xFF)   # the partials are written before they are read
+    A.psg_contract_ws(dA, Av, dB, Bv, C, A.view_of(C), ws, need, st)
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16 if C.element_size() == 2 else torch.int32),
+                       C.view(torch.int16 if C.element_size() == 2 else torch.int32))
+    got = O.T(to_np(C.cpu()), out_dt).f64()
+    for i in range(batch or 1):
+        ai, bi = (a[i], b[i]) if batch else (a, b)
+        ref = O.matmul(O.T(SI.bits(ai), "bf16"), O.T(SI.bits(bi), "bf16"), "f32").data
+        mag = (ai.double().abs() @ bi.double().abs()).numpy()
+        _check(got[i] if batch else got, ref, mag, K, out_dt)
+
+
+def test_split_k_short_workspace_runs_unsplit(A):
+    """A workspace smaller than the query asks for: the unsplit kernel runs,
+    bit for bit what psg_contract gives."""
+    M, N, K = 256, 256, 2048
+    a, b, dA, dB, Av, Bv, C = _split_case(A, M, N, K, "mk", "kn", "f32", None, 11)
+    need = A.psg_contract_workspace(Av, Bv, A.view_of(C))
+    assert need > 0
+    ref = torch.empty_like(C)
+    A.psg_contract(dA, Av, dB, Bv, ref, A.view_of(ref), None)
+    ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
+    A.psg_contract_ws(dA, Av, dB, Bv, C, A.view_of(C), ws, need - 16, None)
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int32), ref.view(torch.int32))
+
+
+def test_split_k_not_used_for_many_tiles(A):
+    """An output that already fills the GPU with tiles asks for no workspace."""
+    M, N, K = 4096, 4096, 4096
+    Av = A.make_view("bf16", [M, N, K], [K, 0, 1], 0, None, M * K)
+    Bv = A.make_view("bf16", [M, N, K], [0, 1, N], 0, None, K * N)
+    Cv = A.make_view("f32", [M, N], [N, 1], 0, None, M * N)
+    assert A.psg_contract_workspace(Av, Bv, Cv) == 0
