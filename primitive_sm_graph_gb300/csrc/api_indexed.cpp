@@ -125,8 +125,7 @@ psg_status psg_gather(const void* src, const psg_view* sv, const int32_t* idx, i
 
 size_t psg_scatter_workspace(int64_t n)
 {
-    if (n <= 0) return 0;
-    return (size_t)scatter_npow2(n) * sizeof(unsigned long long);
+    return scatter_workspace_bytes(n);
 }
 
 psg_status psg_scatter_add(void* dst, const psg_view* dv, const int32_t* idx, int64_t n, const void* upd,
@@ -137,7 +136,7 @@ psg_status psg_scatter_add(void* dst, const psg_view* dv, const int32_t* idx, in
     psg_status st = plan_scatter(dst, dv, idx, n, upd, uv, d_status, &L);
     if (st != PSG_OK) return st;
     if (n == 0) return PSG_OK;
-    if (!workspace || ws_bytes < psg_scatter_workspace(n) || ((uintptr_t)workspace & 7)) return PSG_E_WORKSPACE;
+    if (!workspace || ws_bytes < psg_scatter_workspace(n) || ((uintptr_t)workspace & 15)) return PSG_E_WORKSPACE;
     return launch_scatter(L, (unsigned long long*)workspace, stream);
 }
 

@@ -29,14 +29,19 @@ struct ScatterLaunch {
     int64_t upd_offset, upd_rs, upd_cs;
 };
 
+// Update lists up to this length are ordered by one block (stable radix sort
+// of the indices in shared memory); longer ones by a multi-block bitonic sort.
+constexpr int64_t kScatterPlanMaxN = 16384;
+
 // Capacity of the static key scratch of psg_scatter_add_static (keys, after
 // rounding n up to a power of two).
 constexpr int64_t kStaticScatterKeys = int64_t(1) << 20;
 
 int64_t scatter_npow2(int64_t n);
+size_t scatter_workspace_bytes(int64_t n);
 psg_status static_scatter_keys(unsigned long long** out);
 psg_status launch_gather(const GatherLaunch& L, void* stream);
-// keys: device scratch of scatter_npow2(n) 64-bit words
+// keys: device scratch of scatter_workspace_bytes(n), 16-byte aligned
 psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void* stream);
 
 }  // namespace psg

@@ -79,7 +79,7 @@ def _scatter(A, dst, idx, upd):
 
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16", "i32", "f64"])
 @pytest.mark.parametrize("case", ["embedding_grad", "single_row", "permutation", "ragged", "large", "long_runs",
-                                  "wide_small", "wide", "wide_max"])
+                                  "wide_small", "wide", "wide_max", "target_pick", "deep_keys", "one_row", "one"])
 def test_scatter_add_matches_oracle(A, O, dt, case):
     g = SI.gen(sum(map(ord, dt + case)))
     if case == "embedding_grad":   # [8192, 512] into [256, 512], ~32 collisions per row
@@ -100,6 +100,19 @@ def test_scatter_add_matches_oracle(A, O, dt, case):
     elif case == "long_runs":      # runs of ~33,000 equal indices (run ends found 32 keys at a time)
         V, D, n = 3, 4, 100000
         idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
+    elif case == "target_pick":    # the cross-entropy pick's gradient: sorted, distinct, one cell a row
+        V, D, n = 2032 * 256, 1, 2032
+        idx = (torch.arange(n, dtype=torch.int32) * 256 + torch.randint(0, 256, (n,), generator=g,
+                                                                          dtype=torch.int32))
+    elif case == "deep_keys":      # 23-bit destinations: six radix passes of the one-block sort
+        V, D, n = 5_000_000, 2, 12000
+        idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
+    elif case == "one_row":        # V = 1: no key bits at all
+        V, D, n = 1, 40, 777
+        idx = torch.zeros((n,), dtype=torch.int32)
+    elif case == "one":
+        V, D, n = 7, 9, 1
+        idx = torch.tensor([3], dtype=torch.int32)
     else:                          # many destination rows: the one-block sort (1, 16 keys a thread)
         V, D, n = {"wide_small": (50000, 3, 700), "wide": (100000, 2, 9000), "wide_max": (60000, 2, 16384)}[case]
         idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
@@ -116,6 +129,44 @@ def test_scatter_add_matches_oracle(A, O, dt, case):
     dst2 = dev(dst0)
     _scatter(A, dst2, idx, upd)
     assert np.array_equal(to_np(dst2.cpu()).view(np.uint8), got.view(np.uint8))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_scatter_padded_update_rows(A, O, dt):
+    """Update rows that are a column slice of wider rows: 16-byte vectors
+    for the full segments, single cells for the ragged last one."""
+    g = SI.gen(21)
+    V, D, W, n = 40, 19, 24, 3000
+    idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
+    dst0 = _vals(g, (V, D), dt)
+    wide = _vals(g, (n, W), dt)
+    dst = dev(dst0)
+    du = dev(wide)
+    uv = A.view_of(du, shape=(n, D), strides=(W, 1))
+    ws = torch.empty((A.psg_scatter_workspace(n),), dtype=torch.uint8, device="cuda")
+    st = _status()
+    A.psg_scatter_add(dst, A.view_of(dst), dev(idx), n, du, uv, ws, ws.numel(), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref, _ = O.scatter_add_rows(O.T(SI.bits(dst0), dt), idx.numpy(), O.T(SI.bits(wide[:, :D].contiguous()), dt))
+    assert np.array_equal(to_np(dst.cpu()).view(np.uint8), ref.data.view(np.uint8))
+
+
+def test_scatter_bad_indices_power_of_two_rows(A, O):
+    """Out-of-range indices equal to V (= 2^8) and negative ones among valid
+    rows: they sort after row 255 and are skipped; the rest is exact."""
+    g = SI.gen(22)
+    V, D, n = 256, 8, 5000
+    idx = torch.randint(0, V, (n,), generator=g, dtype=torch.int32)
+    idx[::97] = V
+    idx[5::131] = -1
+    dst0 = _vals(g, (V, D), "f32")
+    upd = _vals(g, (n, D), "f32")
+    dst = dev(dst0)
+    assert _scatter(A, dst, idx, upd) == A.E_INDEX_OUT_OF_RANGE
+    ref, bad = O.scatter_add_rows(O.T(dst0.numpy(), "f32"), idx.numpy(), O.T(upd.numpy(), "f32"))
+    assert bad > 0
+    assert np.array_equal(dst.cpu().numpy(), ref.data)
 
 
 def test_scatter_bad_indices_are_skipped(A, O):
