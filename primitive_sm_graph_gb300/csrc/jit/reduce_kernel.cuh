@@ -24,6 +24,15 @@
 // kExact: every thread's kCH chunks are whole and inside the row, so no
 // chunk needs a range check.
 //
+// kColumnar: the reduced axis is strided and the rows sit next to each other
+// in memory (a sum over the leading axis of a row-major tensor).  A team is
+// then one thread in each warp of the block (its member index is the warp)
+// and the block's 32 teams are 32 adjacent rows, so one warp's load of a
+// cell index covers 32 adjacent cells.  With kCluster > 1 a thread-block
+// cluster shares the rows: CTA rank c holds members c*M .. c*M + M - 1 and
+// every CTA folds all members' partials, read from each rank's shared
+// memory in rank order, so each gets the same total.
+//
 // The including source defines kNin, kInMode[], kInDt[], kOutDt, kNstages,
 // kStageOp[], kStageDt[], kCH, kExact, kCacheIn[], kStash, kPerRow, the
 // staged-mode constants, StageBody<S> and Epi.
@@ -203,6 +212,54 @@ struct RedCtx {
     __device__ __forceinline__ int stashi(int v) const { return (int)stash[j][v]; }
 };
 
+// ---- columnar teams: fold across warps (and the cluster's CTAs) ----------
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ u32 ld_rank(const u32* p, int rank)
+{
+    u32 a, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+// v: this member's partial for row (threadIdx.x & 31); sm: [M * 32] words,
+// cpart: [32].  Warp 0 folds the CTA's members 0, 1, .. in order; then every
+// thread folds the ranks' CTA totals 0, 1, .. in order: one tree for all.
+template <int OP, int DT>
+__device__ __forceinline__ typename VT<DT>::T col_fold(typename VT<DT>::T v, u32* sm, u32* cpart)
+{
+    typedef Fold<OP, DT> F;
+    typedef typename VT<DT>::T T;
+    constexpr int MM = kBlockThreads / 32;  // members per CTA at the launch bound
+    const int M = blockDim.x >> 5, t = threadIdx.x & 31;
+    sm[(threadIdx.x >> 5) * 32 + t] = as_bits(v);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        u32 part[MM];  // every partial loaded before the first add
+#pragma unroll
+        for (int m = 0; m < MM; ++m) part[m] = m < M ? sm[m * 32 + t] : 0u;
+        T r = from_bits<T>(part[0]);
+#pragma unroll
+        for (int m = 1; m < MM; ++m)
+            if (m < M) r = F::step(r, from_bits<T>(part[m]));
+        cpart[t] = as_bits(r);
+    }
+    if constexpr (kCluster > 1) cluster_sync_all();
+    else __syncthreads();
+    u32 q[kCluster];
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) q[c] = kCluster > 1 ? ld_rank(cpart + t, c) : cpart[t];
+    T r = from_bits<T>(q[0]);
+#pragma unroll
+    for (int c = 1; c < kCluster; ++c) r = F::step(r, from_bits<T>(q[c]));
+    // nobody rewrites sm or cpart (or leaves the cluster) while another still reads them
+    if constexpr (kCluster > 1) cluster_sync_all();
+    else __syncthreads();
+    return r;
+}
+
 // fold v across the team (threads [team*T, team*T + T) of the block)
 template <int OP, int DT>
 __device__ __forceinline__ typename VT<DT>::T team_fold(typename VT<DT>::T v, int team_log2, u32* sm)
@@ -227,14 +284,18 @@ __device__ __forceinline__ typename VT<DT>::T team_fold(typename VT<DT>::T v, in
     return v;
 }
 
-extern "C" __global__ void __launch_bounds__(256, kMinBlocks) psg_reduce(const __grid_constant__ PsgRedParams p)
+extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUSTER_DIMS psg_reduce(
+    const __grid_constant__ PsgRedParams p)
 {
-    __shared__ u32 sm[32];
+    __shared__ u32 sm[kColumnar ? kBlockThreads : 32];
+    __shared__ u32 cpart[kColumnar ? 32 : 1];
     extern __shared__ __align__(128) unsigned char dsm[];  // staged mode: barriers, then the ring
-    const int T = 1 << p.team_log2;
-    const int teams = blockDim.x >> p.team_log2;
-    const int team = threadIdx.x >> p.team_log2;
-    const int lane = threadIdx.x & (T - 1);
+    // members of a team (T), teams of a block, this thread's team and member index (lane)
+    const int T = kColumnar ? (int)(blockDim.x >> 5) * kCluster : 1 << p.team_log2;
+    const int teams = kColumnar ? 32 : (int)(blockDim.x >> p.team_log2);
+    const int team = kColumnar ? (int)(threadIdx.x & 31) : (int)(threadIdx.x >> p.team_log2);
+    const int lane = kColumnar ? (int)(blockIdx.x % kCluster) * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5)
+                               : (int)(threadIdx.x & (T - 1));
     unsigned long long* bars = (unsigned long long*)dsm;  // [teams][kNS]
     unsigned char* ring = dsm + kBarBytes;                 // [teams][kNS][kStageBytes]
     if constexpr (kStaged) {
@@ -245,8 +306,8 @@ extern "C" __global__ void __launch_bounds__(256, kMinBlocks) psg_reduce(const _
     // iteration it gives team `team` the row first + it * step + team; every
     // team of the block runs the same number of iterations, so the barriers
     // inside team_fold (and the staged ring's) are reached by all threads
-    const i64 step = (i64)gridDim.x * teams;
-    const i64 first = (i64)blockIdx.x * teams;
+    const i64 step = (i64)(gridDim.x / kCluster) * teams;
+    const i64 first = (i64)(blockIdx.x / kCluster) * teams;
     const i64 niter = first < p.rows ? (p.rows - first + step - 1) / step : 0;
     // staged mode: one lane of the team fills ring slot it % kNS with the
     // row of iteration it (one bulk copy per staged input)
@@ -340,9 +401,27 @@ extern "C" __global__ void __launch_bounds__(256, kMinBlocks) psg_reduce(const _
                 const RedCtx cu{p, roff, rok, cache, stash, red, sb, 0, PSG_VEC, 0};
                 u = StageBody<S>::uni(cu);  // the row's uniform values, once
             }
+            // streaming: the member's whole chunks first, kStreamUnroll at a
+            // time with no range checks, so their loads can all go out together
+            int jj0 = 0;
+            if constexpr (kCH == 0 && kStreamUnroll > 1) {
+                const i64 whole = p.inner / PSG_VEC;  // chunks entirely inside the row
+                const int nw = active && lane < whole ? (int)((whole - lane + T - 1) / T) : 0;
+                for (; jj0 + kStreamUnroll <= nw; jj0 += kStreamUnroll) {
+#pragma unroll
+                    for (int q = 0; q < kStreamUnroll; ++q) {
+                        const i64 col0 = (lane + (i64)(jj0 + q) * T) * PSG_VEC;
+                        const RedCtx c{p, roff, rok, cache, stash, red, sb, col0, PSG_VEC, 0};
+                        typename VT<DT>::T y[PSG_VEC];
+                        StageBody<S>::eval(c, u, y);
+#pragma unroll
+                        for (int v = 0; v < PSG_VEC; ++v) accv[v] = F::step(accv[v], y[v]);
+                    }
+                }
+            }
 #pragma unroll
             for (int j = 0; j < (kCH > 0 ? kCH : 1); ++j) {
-                for (int jj = (kCH > 0 ? j : 0); jj < (kCH > 0 ? j + 1 : nch); ++jj) {
+                for (int jj = (kCH > 0 ? j : jj0); jj < (kCH > 0 ? j + 1 : nch); ++jj) {
                     const i64 ch = lane + (i64)jj * T;
                     const i64 col0 = ch * PSG_VEC;
                     const i64 left = p.inner - col0;
@@ -365,7 +444,9 @@ extern "C" __global__ void __launch_bounds__(256, kMinBlocks) psg_reduce(const _
 #pragma unroll
                 for (int v = 0; v < w; ++v) accv[v] = F::step(accv[v], accv[v + w]);
             }
-            const typename VT<DT>::T acc = team_fold<OP, DT>(accv[0], p.team_log2, sm);
+            typename VT<DT>::T acc;
+            if constexpr (kColumnar) acc = col_fold<OP, DT>(accv[0], sm, cpart);
+            else acc = team_fold<OP, DT>(accv[0], p.team_log2, sm);
             red[S] = as_bits(F::finish(acc));
         };
         sfor<0, kNstages>(stage);

@@ -15,7 +15,8 @@
 namespace psg {
 
 namespace {
-constexpr int RED_THREADS = 256;  // the skeleton's launch bound
+constexpr int RED_THREADS = 256;      // the skeleton's launch bound (row teams)
+constexpr int RED_COL_THREADS = 512;  // columnar layout: 16 members a CTA
 static_assert(PSG_DEV_E_TIMEOUT == PSG_E_TIMEOUT, "device status code");
 }  // namespace
 
@@ -24,7 +25,8 @@ namespace {
 struct RedPlan {
     PsgRedParams p;
     int block;
-    int smem;  // dynamic shared memory (staged mode)
+    int smem;     // dynamic shared memory (staged mode)
+    int cluster;  // CTAs per cluster (columnar layout), else 1
     std::string spec;
 };
 
@@ -157,6 +159,21 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
             if (same && m < n_epi) stash = s;
         }
     }
+    // columnar layout: the rows are adjacent in memory and the reduced axis
+    // is strided (a sum over a leading axis).  Every input that varies from
+    // row to row must then move by 0 or 1 cell from one row to the next
+    // (the last row dim), one of them by 1; inputs the rows share may be
+    // contiguous along the reduced axis (every lane reads the same cells).
+    bool columnar = sp.nd >= 2 && sp.rows > 1;
+    bool unit_row = false;
+    for (int k = 0; k < n_in && columnar; ++k) {
+        if (uni[k]) continue;
+        const int64_t rs = sp.shape[sp.nd - 2] > 1 ? P->p.in[k].outer_stride[sp.nd - 2] : 0;
+        if (modes[k] == PSG_M_MASKED || (rs != 0 && rs != 1)) columnar = false;
+        if (rs == 1 && modes[k] == PSG_M_STRIDED) unit_row = true;
+        if (rs == 1 && modes[k] != PSG_M_STRIDED) columnar = false;
+    }
+    columnar = columnar && unit_row;
     // team of T threads per row.  A thread takes about RED_CHUNKS chunks, so
     // each issues several 16- or 32-byte loads at once and short rows fold
     // inside one warp (shuffles only); the row (and a stash) is cached in
@@ -177,7 +194,7 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     int staged_in[PSG_MAX_INPUTS] = {0}, seg_off[PSG_MAX_INPUTS] = {0}, row_bytes[PSG_MAX_INPUTS] = {0},
         in_size[PSG_MAX_INPUTS] = {0};
     int64_t stage_bytes = 0, tx_bytes = 0;
-    bool staged = ch_per <= RED_STAGED_MAX_CHUNKS && words > 0;
+    bool staged = ch_per <= RED_STAGED_MAX_CHUNKS && words > 0 && !columnar;
     for (int k = 0; k < n_in; ++k) {
         in_size[k] = dtype_size(dts[k]);
         if (!cache_in[k]) continue;
@@ -209,25 +226,40 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     }
     P->smem = staged ? (int)(bar_bytes + teams * ns * stage_bytes) : 0;
     if (stash >= 0 && ch_per * (words + PSG_VEC) > RED_CACHE_WORDS) stash = -1;
-    const int kch = ch_per * words <= RED_CACHE_WORDS || staged ? (int)ch_per : 0;
+    const int kch = columnar ? 0 : ch_per * words <= RED_CACHE_WORDS || staged ? (int)ch_per : 0;
     if (kch == 0) stash = -1;
     const int stash_node = stash >= 0 ? stages[stash].n_nodes - 1 : -1;
     // resident blocks the launch bound asks registers for: what the ring
     // leaves room for in staged mode, else 4 (measured best for the softmax
     // and RMSNorm rows)
     int min_blocks = 4;
+    if (columnar) min_blocks = 1;  // 512 threads; the unrolled stream keeps its loads in registers
     if (staged) {
         min_blocks = (int)((227 * 1024) / (P->smem + 1024));
         min_blocks = min_blocks < 1 ? 1 : min_blocks > 4 ? 4 : min_blocks;
     }
+    // columnar: 32 rows a block; a cluster of C CTAs shares them when the
+    // row groups alone would leave most SMs idle (C a power of two up to 8,
+    // each of the C * 8 members keeping at least RED_COL_MIN_CHUNKS chunks)
+    constexpr int RED_COL_MIN_CHUNKS = 2;
+    int cluster = 1;
+    const int block = columnar ? RED_COL_THREADS : RED_THREADS;
+    if (columnar) {
+        const int64_t groups = (sp.rows + 31) / 32;
+        const int64_t members = block / 32;
+        while (cluster < 8 && groups * cluster * 2 <= (int64_t)num_sms() &&
+               sp.chunks >= members * cluster * 2 * RED_COL_MIN_CHUNKS)
+            cluster *= 2;
+    }
+    P->cluster = cluster;
     bodies += gen_eval(epi, E, "Epi", "", stash_node);
-    P->block = RED_THREADS;
+    P->block = block;
     P->p.rows = sp.rows;
     P->p.inner = sp.inner;
     P->p.chunks = sp.chunks;
     for (int d = 0; d < MAXD; ++d) P->p.shape[d] = d < sp.nd ? sp.shape[d] : 1;
     P->p.nd = sp.nd;
-    P->p.team_log2 = tl;
+    P->p.team_log2 = columnar ? -1 : tl;  // -1: columnar teams (32 a block)
     P->p.out_per_row = per_row ? 1 : 0;
     std::string spec = "constexpr int kNin = " + std::to_string(n_in) + ";\n";
     spec += "constexpr int kInMode[] = " + int_list(modes, n_in) + ";\n";
@@ -253,6 +285,12 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     spec += "constexpr u32 kRowBytes[] = " + int_list(row_bytes, n_in) + ";\n";
     spec += "constexpr int kInSize[] = " + int_list(in_size, n_in) + ";\n";
     spec += "constexpr int kPerRow = " + std::to_string(per_row ? 1 : 0) + ";\n";
+    spec += "constexpr int kColumnar = " + std::to_string(columnar ? 1 : 0) + ";\n";
+    spec += "constexpr int kBlockThreads = " + std::to_string(block) + ";\n";
+    spec += "constexpr int kCluster = " + std::to_string(cluster) + ";\n";
+    spec += "constexpr int kStreamUnroll = " + std::to_string(columnar ? 4 : 1) + ";\n";
+    spec += cluster > 1 ? "#define PSG_CLUSTER_DIMS __cluster_dims__(" + std::to_string(cluster) + ", 1, 1)\n"
+                        : "#define PSG_CLUSTER_DIMS\n";
     spec += "template <int S> struct StageBody;\n";
     spec += bodies;
     P->spec = std::move(spec);
@@ -261,10 +299,12 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
 
 psg_status grid_for(const RedPlan& P, cudaKernel_t k, int* grid)
 {
-    const int teams = P.block >> P.p.team_log2;
+    const int teams = P.p.team_log2 < 0 ? 32 : P.block >> P.p.team_log2;
     const int64_t need = (P.p.rows + teams - 1) / teams;
     const int per_sm = jit_max_blocks_per_sm(k, P.block, (size_t)P.smem);
-    *grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1)));
+    // whole clusters: every CTA of a cluster walks the same row groups
+    const int64_t cap = std::max<int64_t>(1, (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1) / P.cluster);
+    *grid = (int)(std::max<int64_t>(1, std::min<int64_t>(need, cap)) * P.cluster);
     return PSG_OK;
 }
 

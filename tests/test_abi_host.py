@@ -160,3 +160,48 @@ def test_scatter_workspace_checks(A):
     st = A.psg_scatter_add(fake, dv, fake, 10, fake, A.make_view("i8", (10, 2)), fake, need, fake,
                            stream=0, check=False)
     assert st == A.E_UNSUPPORTED_DTYPE
+
+
+def test_columnar_reductions_compile_without_a_gpu(A):
+    """Reductions over a leading axis (rows adjacent in memory, the reduced
+    axis strided) plan the columnar layout and compile: a weighted column
+    sum reading a per-k vector, and a two-stage softmax over a strided axis
+    with a per-element epilogue."""
+    L = A.lib
+    f = L.psg_internal_compile_reduce
+    f.argtypes = [ctypes.POINTER(A.psg_reduce_stage), ctypes.c_int, ctypes.POINTER(A.psg_node), ctypes.c_int,
+                  ctypes.POINTER(A.psg_view), ctypes.c_int, ctypes.POINTER(A.psg_view), ctypes.c_char_p,
+                  ctypes.c_size_t]
+    buf = ctypes.create_string_buffer(1 << 16)
+    n = A.node
+
+    def run(stages, epi, ins, out):
+        keep = []
+        sarr = (A.psg_reduce_stage * len(stages))()
+        for i, (op, prog) in enumerate(stages):
+            arr = (A.psg_node * len(prog))(*prog)
+            keep.append(arr)
+            sarr[i].op, sarr[i].n_nodes = op, len(prog)
+            sarr[i].prologue = ctypes.cast(arr, ctypes.POINTER(A.psg_node))
+        earr = (A.psg_node * max(1, len(epi)))(*epi)
+        views = (A.psg_view * len(ins))(*ins)
+        return f(sarr, len(stages), earr if epi else None, len(epi), views, len(ins), ctypes.byref(out), buf,
+                 len(buf))
+
+    # dg[c] = sum_r dy[r, c] * x[r, c] * rstd[r]: rows are c (stride 1), k is r (stride 512)
+    R, C = 8192, 512
+    dy = A.make_view("bf16", (C, R), (1, C), 0, None, R * C)
+    x = A.make_view("bf16", (C, R), (1, C), 0, None, R * C)
+    rstd = A.make_view("f32", (C, R), (0, 1), 0, None, R)
+    prog = [n("LOAD", 0, dtype="bf16"), n("LOAD", 1, dtype="bf16"), n("CAST", 0), n("CAST", 1),
+            n("MUL", 2, 3), n("LOAD", 2), n("MUL", 4, 5)]
+    st = run([(A.RED_SUM, prog)], [], [dy, x, rstd], A.make_view("f32", (C,)))
+    assert st == 0, (A.STATUS.get(st), buf.value.decode()[:3000])
+    # softmax over the leading axis of [64, 300]: MAX, then SUM of EXP(x - m), then EXP(x - m) / s
+    v = A.make_view("f32", (300, 64), (1, 300), 0, None, 64 * 300)
+    s1 = [n("LOAD", 0)]
+    s2 = [n("LOAD", 0), n("RED", 0), n("NEG", 1), n("ADD", 0, 2), n("EXP", 3)]
+    epi = s2 + [n("RED", 1), n("RECIP", 5), n("MUL", 4, 6)]
+    st = run([(A.RED_MAX, s1), (A.RED_SUM, s2)], epi, [v], A.make_view("f32", (300, 64), (1, 300), 0, None,
+                                                                         64 * 300))
+    assert st == 0, (A.STATUS.get(st), buf.value.decode()[:3000])

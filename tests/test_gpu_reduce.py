@@ -214,3 +214,98 @@ def test_per_row_epilogue_and_tiny_graph_tail(A, O, PR):
     assert np.all(np.abs(m.cpu().numpy() - mref) <= 2 * gamma(95) * mag + np.spacing(np.abs(mref)))
 
 
+
+
+# ---- reductions over a leading axis (the columnar layout) -------------------
+
+@pytest.mark.parametrize("rows,k,dt", [(512, 8192, "f32"), (512, 4096, "bf16"), (100, 37, "f32"),
+                                       (33, 1000, "bf16"), (1000, 3, "f32")])
+def test_column_sum_weighted(A, O, rows, k, dt):
+    """out[c] = sum_r dy[r, c] * x[r, c] * w[r] over a row-major [k, rows]
+    pair (an RMSNorm weight's gradient): within the SUM bound of the
+    oracle's float32 total of the same products."""
+    g = SI.gen(rows + k)
+    dy = SI.normal((k, rows), 0, 1, g).to(storage_dtype(dt))
+    x = SI.normal((k, rows), 0, 1, g).to(storage_dtype(dt))
+    w = SI.uniform((k,), 0.5, 2.0, g)
+    ddy, dx, dw = dev(dy), dev(x), dev(w)
+    vdy = A.make_view(dt, (rows, k), (1, rows), 0, None, rows * k)
+    vx = A.make_view(dt, (rows, k), (1, rows), 0, None, rows * k)
+    vw = A.make_view("f32", (rows, k), (0, 1), 0, None, k)
+    n = A.node
+    prog = [n("LOAD", 0, dtype=dt), n("LOAD", 1, dtype=dt), n("CAST", 0), n("CAST", 1), n("MUL", 2, 3),
+            n("LOAD", 2), n("MUL", 4, 5)]
+    out = torch.empty((rows,), device="cuda")
+    A.psg_reduce_rows([(A.RED_SUM, prog)], None, [ddy, dx, dw], [vdy, vx, vw], out, A.view_of(out))
+    torch.cuda.synchronize()
+    ody = O.cast(O.view(O.T(SI.bits(dy), dt), (rows, k), (1, rows)), "f32")
+    ox = O.cast(O.view(O.T(SI.bits(x), dt), (rows, k), (1, rows)), "f32")
+    ow = O.view(O.T(w.numpy(), "f32"), (rows, k), (0, 1))
+    prod = O.mul(O.mul(ody, ox), ow)
+    ref = O.reduce_sum(prod, keepdim=False).data.astype(np.float64)
+    mag = np.abs(prod.f64()).sum(axis=-1)
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2 * gamma(k - 1) * mag + 1e-30)
+    # the same bits on a second call
+    out2 = torch.empty_like(out)
+    A.psg_reduce_rows([(A.RED_SUM, prog)], None, [ddy, dx, dw], [vdy, vx, vw], out2, A.view_of(out2))
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
+
+
+@pytest.mark.parametrize("rows,k", [(300, 64), (64, 5000), (40, 1)])
+def test_column_softmax(A, O, PR, rows, k):
+    """Softmax over the leading axis of a row-major [k, rows] tensor, written
+    back in the same layout (two stages and a per-element epilogue)."""
+    g = SI.gen(rows * 3 + k)
+    x = SI.uniform((k, rows), -50.0, 50.0, g)
+    dx = dev(x)
+    y = torch.empty_like(dx)
+    v = A.make_view("f32", (rows, k), (1, rows), 0, None, rows * k)
+    stages, epi = PR.softmax_rows()
+    A.psg_reduce_rows(stages, epi, [dx], [v], y, A.make_view("f32", (rows, k), (1, rows), 0, None, rows * k))
+    torch.cuda.synchronize()
+    _softmax_check(O, x.numpy().T.copy(), y.cpu().numpy().T.copy())
+
+
+@pytest.mark.parametrize("k", [40, 3000, 9000])
+def test_column_max_specials(A, O, k):
+    """MAX over a strided axis with signed zeros, NaNs and -inf, across
+    warps and cluster ranks: bit-exact."""
+    g = SI.gen(k + 1)
+    rows = 96
+    x = torch.where(torch.rand((k, rows), generator=g) < 0.5, torch.tensor(-0.0), torch.tensor(0.0))
+    x[:, 0] = -0.0
+    x[k // 2, 1] = 0.0
+    x[:, 2] = float("-inf")
+    x[k - 1, 3] = float("nan")
+    x[:, 4] = -torch.rand((k,), generator=g) - 1.0
+    x[0, 5] = float("nan")
+    dx = dev(x)
+    out = torch.empty((rows,), device="cuda")
+    v = A.make_view("f32", (rows, k), (1, rows), 0, None, rows * k)
+    A.psg_reduce_rows([(A.RED_MAX, [A.node("LOAD", 0)])], None, [dx], [v], out, A.view_of(out))
+    torch.cuda.synchronize()
+    ref = O.reduce_max(O.view(O.T(x.numpy(), "f32"), (rows, k), (1, rows)), keepdim=False).data
+    got = out.cpu().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.signbit(got[~np.isnan(got)]), np.signbit(ref[~np.isnan(ref)]))
+    assert np.array_equal(np.nan_to_num(got), np.nan_to_num(ref))
+
+
+def test_column_sum_over_batch_of_3d(A, O):
+    """A sum over the batch axis of [B, T, D] (a position embedding's
+    gradient): rows are the (T, D) cells, two row dims."""
+    B, T, D = 8, 40, 96
+    g = SI.gen(77)
+    x = SI.normal((B, T, D), 0, 1, g).to(torch.bfloat16)
+    dx = dev(x)
+    v = A.make_view("bf16", (T, D, B), (D, 1, T * D), 0, None, B * T * D)
+    out = torch.empty((T, D), device="cuda")
+    A.psg_reduce_rows([(A.RED_SUM, [A.node("LOAD", 0, dtype="bf16"), A.node("CAST", 0)])], None, [dx], [v],
+                      out, A.view_of(out))
+    torch.cuda.synchronize()
+    ox = O.cast(O.view(O.T(SI.bits(x), "bf16"), (T, D, B), (D, 1, T * D)), "f32")
+    ref = O.reduce_sum(ox, keepdim=False).data.astype(np.float64)
+    mag = np.abs(ox.f64()).sum(axis=-1)
+    assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - ref) <= 2 * gamma(B - 1) * mag + 1e-30)
