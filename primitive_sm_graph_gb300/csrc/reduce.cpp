@@ -16,7 +16,7 @@ namespace psg {
 
 namespace {
 constexpr int RED_THREADS = 256;      // the skeleton's launch bound (row teams)
-constexpr int RED_COL_THREADS = 512;  // columnar layout: 16 members a CTA
+constexpr int RED_COL_THREADS = 512;  // columnar layout: at most 16 members a CTA
 static_assert(PSG_DEV_E_TIMEOUT == PSG_E_TIMEOUT, "device status code");
 }  // namespace
 
@@ -231,24 +231,27 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     const int stash_node = stash >= 0 ? stages[stash].n_nodes - 1 : -1;
     // resident blocks the launch bound asks registers for: what the ring
     // leaves room for in staged mode, else 4 (measured best for the softmax
-    // and RMSNorm rows)
+    // and RMSNorm rows); columnar, 512 threads an SM, so the unrolled stream
+    // keeps its loads in registers
     int min_blocks = 4;
-    if (columnar) min_blocks = 1;  // 512 threads; the unrolled stream keeps its loads in registers
     if (staged) {
         min_blocks = (int)((227 * 1024) / (P->smem + 1024));
         min_blocks = min_blocks < 1 ? 1 : min_blocks > 4 ? 4 : min_blocks;
     }
-    // columnar: 32 rows a block; a cluster of C CTAs shares them when the
-    // row groups alone would leave most SMs idle (C a power of two up to 8,
-    // each of the C * 8 members keeping at least RED_COL_MIN_CHUNKS chunks)
+    // columnar: 32 rows a CTA and up to 16 members (warps), as many as keep
+    // RED_COL_MIN_CHUNKS chunks each; a cluster of C CTAs (a power of two up
+    // to 8) shares the rows when the row groups alone would leave most SMs
+    // idle and every member still keeps RED_COL_MIN_CHUNKS chunks
     constexpr int RED_COL_MIN_CHUNKS = 2;
+    int col_members = RED_COL_THREADS / 32;
+    while (col_members > 1 && sp.chunks < (int64_t)col_members * RED_COL_MIN_CHUNKS) col_members >>= 1;
+    const int block = columnar ? 32 * col_members : RED_THREADS;
+    if (columnar) min_blocks = std::max(1, 512 / block);
     int cluster = 1;
-    const int block = columnar ? RED_COL_THREADS : RED_THREADS;
     if (columnar) {
         const int64_t groups = (sp.rows + 31) / 32;
-        const int64_t members = block / 32;
         while (cluster < 8 && groups * cluster * 2 <= (int64_t)num_sms() &&
-               sp.chunks >= members * cluster * 2 * RED_COL_MIN_CHUNKS)
+               sp.chunks >= (int64_t)col_members * cluster * 2 * RED_COL_MIN_CHUNKS)
             cluster *= 2;
     }
     P->cluster = cluster;

@@ -245,6 +245,16 @@ class Tensor:
         assert self.dtype == k.dtype == v.dtype == "bf16"
         return Tensor("ATTN", (self, k, v), self.shape, "bf16", arg=(float(scale), bool(causal)))
 
+    def attention_packed(self, scale: float, causal: bool = True):
+        """The fused attention over a packed qkv tensor [B, T, 3, H, 64] bf16
+        (slot 0 Q, 1 K, 2 V: a fused projection's output): returns O
+        [B, T, H, 64].  Its gradient is one tensor in the same packed
+        layout, which the backward kernels write in place (no pad-and-add of
+        dQ, dK, dV back into the packed tensor)."""
+        assert len(self.shape) == 5 and self.shape[2] == 3 and self.shape[4] == 64 and self.dtype == "bf16"
+        B, T, _, H, hd = self.shape
+        return Tensor("ATTN", (self,), (B, T, H, hd), "bf16", arg=(float(scale), bool(causal)))
+
     def scatter_add(self, idx: "Tensor", upd: "Tensor"):
         """SCATTER-add along dim 0: self + rows of upd added at idx, in order."""
         assert idx.dtype == "i32" and upd.shape[1:] == self.shape[1:] and upd.dtype == self.dtype
@@ -878,11 +888,32 @@ class Executor:
             buf, v = self._copy_contig(buf, v, x.dtype)
         return buf, v
 
+    def _attn_slots(self, qkv: Tensor, shape):
+        """(buffer, [View of slot 0, 1, 2]) of a packed [B, T, 3, H, 64]
+        operand, each slot a [B, T, H, 64] View the kernels can read with TMA
+        (the packed tensor is copied contiguous first if a slot is not)."""
+        buf, v = self.realize(qkv)
+        full = [(0, n) for n in qkv.shape]
+
+        def slots(v):
+            return [v.shrink(full[:2] + [(i, i + 1)] + full[3:]).reshape(shape) for i in range(3)]
+
+        vs = slots(v)
+        ok = all(x.mask is None and x.strides[3] == 1 and all(st % 8 == 0 for st in x.strides[:3])
+                 and (buf.data_ptr() + 2 * x.offset) % 16 == 0 for x in vs)
+        if not ok:
+            buf, v = self._copy_contig(buf, v, qkv.dtype)
+            vs = slots(v)
+        return buf, vs
+
     def _realize_attn(self, t: Tensor):
-        q, k, v = t.src
         scale, causal = t.arg
         B, T, H, _ = t.shape
-        (bq, vq), (bk, vk), (bv, vv) = (self._attn_operand(x) for x in (q, k, v))
+        if len(t.src) == 1:  # packed qkv
+            b, (vq, vk, vv) = self._attn_slots(t.src[0], t.shape)
+            bq = bk = bv = b
+        else:
+            (bq, vq), (bk, vk), (bv, vv) = (self._attn_operand(x) for x in t.src)
         out = self._new(t.shape, "bf16")
         lse = self._new((B, H, T), "f32")
         A.psg_attention_fwd(bq, self._pview(bq, vq, "bf16"), bk, self._pview(bk, vk, "bf16"), bv,
@@ -893,16 +924,24 @@ class Executor:
         return out, View(t.shape)
 
     def _realize_attn_bwd(self, t: Tensor):
-        q, k, v, fwd, g = t.src
+        fwd, g = t.src[-2:]
         scale, causal = t.arg
         B, T, H, _ = fwd.shape
         bo, vo = self.realize(fwd)
         lse = fwd._aux
-        ops = [self._attn_operand(x) for x in (q, k, v, g)]
-        out = self._new(t.shape, "bf16")                      # [3, B, T, H, 64]: dQ, dK, dV
+        if len(t.src) == 3:
+            # packed: dQ, dK, dV land in the slots of one [B, T, 3, H, 64] gradient
+            b, vs = self._attn_slots(t.src[0], fwd.shape)
+            ops = [(b, x) for x in vs] + [self._attn_operand(g)]
+            out = self._new(t.shape, "bf16")
+            full = [(0, n) for n in t.shape]
+            gv = [View(t.shape).shrink(full[:2] + [(i, i + 1)] + full[3:]).reshape(fwd.shape) for i in range(3)]
+        else:
+            ops = [self._attn_operand(x) for x in t.src[:3] + (g,)]
+            out = self._new(t.shape, "bf16")                  # [3, B, T, H, 64]: dQ, dK, dV
+            gv = [View(t.shape).shrink([(i, i + 1)] + [(0, n) for n in fwd.shape]).reshape(fwd.shape)
+                  for i in range(3)]
         delta = self._new((B, H, T), "f32")
-        gv = [View(t.shape).shrink([(i, i + 1)] + [(0, n) for n in fwd.shape]).reshape(fwd.shape)
-              for i in range(3)]
         pv = lambda bv: self._pview(bv[0], bv[1], "bf16")
         A.psg_attention_bwd(ops[0][0], pv(ops[0]), ops[1][0], pv(ops[1]), ops[2][0], pv(ops[2]), bo, pv((bo, vo)),
                             ops[3][0], pv(ops[3]), lse, delta, out, pv((out, gv[0])), out, pv((out, gv[1])), out,
@@ -1131,8 +1170,10 @@ def _vjp(t: Tensor, g: Tensor):
         return [(s[0], g), (s[2], g.gather(s[1]))]
     if op == "ATTN":
         # one node computes dQ, dK, dV together (the two-pass backward)
-        d = Tensor("ATTN_BWD", (s[0], s[1], s[2], t, g.cast("bf16") if g.dtype != "bf16" else g),
-                   (3,) + t.shape, "bf16", arg=t.arg)
+        gb = g.cast("bf16") if g.dtype != "bf16" else g
+        if len(s) == 1:  # packed qkv: the gradient in the same packed layout
+            return [(s[0], Tensor("ATTN_BWD", (s[0], t, gb), s[0].shape, "bf16", arg=t.arg))]
+        d = Tensor("ATTN_BWD", (s[0], s[1], s[2], t, gb), (3,) + t.shape, "bf16", arg=t.arg)
         full = [(0, n) for n in t.shape]
         return [(s[i], d.shrink([(i, i + 1)] + full).reshape(t.shape)) for i in range(3)]
     return []

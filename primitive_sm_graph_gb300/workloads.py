@@ -90,7 +90,7 @@ def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,
 
     q, k, v = head(0), head(1), head(2)
     if fused_attention and fused_attention_applies(T, D, H):
-        o = q.attention(k, v, 1.0 / np.sqrt(hd), causal=True).reshape(BT, D)
+        o = qkv.attention_packed(1.0 / np.sqrt(hd), causal=True).reshape(BT, D)
     else:
         q, k, v = (x.permute(0, 2, 1, 3) for x in (q, k, v))
         s = q.matmul(k.transpose(-1, -2)).cast("f32") * (1.0 / np.sqrt(hd))
