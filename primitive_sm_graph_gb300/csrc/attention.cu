@@ -5,14 +5,18 @@
 // attention that saves L = logsumexp for its backward, instead of the
 // composed T x T score tensors) and Tiki's FlashAttention target ("Write the
 // attention kernel at the algorithm level").  Per (batch, head, 128-query
-// tile) one CTA:
-//   S = Q K^T           tcgen05.mma.kind::f16, M 128, N 256, K 64 -> TMEM
-//   P = exp(scale S - m) per query row (one thread per row, masked keys 0),
-//       l = its float32 sum, L = m + log l; P rounded to bf16 into shared
-//       memory
-//   O = P V / l         tcgen05.mma, M 128, N 64, K 256 -> TMEM, scaled, bf16
-// K and V arrive as the same TMA box (keys x 64, 128-byte swizzle): the
-// K-major B operand of S = Q K^T and the MN-major B operand of O = P V.
+// tile) one CTA, two resident a SM:
+//   S = Q K^T           tcgen05.mma.kind::f16, M 128, N <= 256, K 64 -> TMEM
+//   P = exp(scale S - m) per query row (two threads a row, one per half of
+//       the keys; masked keys 0), l = its float32 sum, L = m + log l; P
+//       rounded to bf16 and written back into TMEM over the S columns its
+//       thread has read
+//   O = P V / l         tcgen05.mma with A (= P) from TMEM, M 128, N 64,
+//                       K <= 256 -> TMEM, scaled, bf16
+// With a causal mask a query tile needs keys up to its last query only:
+// the copies and both products stop there.  K and V arrive as the same TMA
+// box (128 keys x 64, 128-byte swizzle): the K-major B operand of S = Q K^T
+// and the MN-major B operand of O = P V.
 //
 // Backward (two passes, deterministic: every gradient cell is accumulated by
 // one CTA in a fixed order, no atomics), with D = rowsum(dO * O):
@@ -50,16 +54,32 @@ constexpr int ROW_BYTES = HD * 2;           // 128: one swizzle row
 constexpr int Q_BYTES = QT * ROW_BYTES;     // 16 KB
 constexpr int KV_BYTES = KB * ROW_BYTES;    // 32 KB
 constexpr int P_ATOM = QT * 128;            // 16 KB: 128 rows x 64 keys (bf16)
-constexpr int P_BYTES = 4 * P_ATOM;         // 64 KB: 128 rows x 256 keys
-constexpr int FWD_THREADS = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 rows
-constexpr int FWD_SMEM = 1024 + Q_BYTES + 2 * KV_BYTES + P_BYTES + 256 + 1024;
+constexpr int FWD_THREADS = 320;            // warp 0 TMA, warp 1 MMA, warps 2-9 two per query row
+constexpr int FWD_SMEM = 1024 + Q_BYTES + 2 * KV_BYTES + 256 + 4 * QT * 4;
 constexpr int FWD_TMEM = 256;
+// TMEM columns: S in [0, 256); P (bf16 pairs) of keys 0..127 at 0, of keys
+// 128..255 at FWD_P1 (each over S its own threads have read); O at FWD_O
+// (S of keys 192..255, read before P is ready)
+constexpr uint32_t FWD_P1 = 128, FWD_O = 192;
 
 struct FwdBars {
     uint64_t full, s_full, p_ready, o_full, drain;
     uint32_t tmem_base;
     int32_t abort;
 };
+
+// tcgen05.mma with the A operand in TMEM (K-major: a row a lane, two bf16 a column)
+__device__ __forceinline__ void mma_f16_ts(uint32_t dtmem, uint32_t atmem, uint64_t bd, uint32_t idesc,
+                                           uint32_t accum)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(dtmem), "r"(atmem), "l"(bd), "r"(idesc), "r"(accum));
+}
+
+// the 8 softmax warps only
+__device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum)
 {
@@ -100,7 +120,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b)
     return *(const uint32_t*)&h;
 }
 
-__global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd(const __grid_constant__ CUtensorMap tq,
+__global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant__ CUtensorMap tq,
                                                            const __grid_constant__ CUtensorMap tk,
                                                            const __grid_constant__ CUtensorMap tv,
                                                            const __grid_constant__ AttnParams p)
@@ -108,18 +128,23 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd(const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sq = smem;                       // [128 q][64 d]
-    uint8_t* sk = sq + Q_BYTES;               // [256 keys][64 d]
+    uint8_t* sk = sq + Q_BYTES;               // [256 keys][64 d], two 128-key boxes
     uint8_t* sv = sk + KV_BYTES;              // [256 keys][64 d]
-    uint8_t* sp = sv + KV_BYTES;              // 4 atoms [128 q][64 keys]
-    FwdBars* bars = (FwdBars*)(sp + P_BYTES);
+    FwdBars* bars = (FwdBars*)(sv + KV_BYTES);
+    float* red_m = (float*)((uint8_t*)bars + 256);  // [2 halves][128 rows]
+    float* red_l = red_m + 2 * QT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int q0 = qt * QT;
+    // keys any query of this tile sees; MMA steps of 16 keys past them read zeros
+    const int kv_end = p.causal ? min(p.T, q0 + QT) : p.T;
+    const int kv_pad = (kv_end + 15) & ~15;
+    const int nkb = (kv_end + QT - 1) / QT;  // 128-key boxes to load (1 or 2)
 
     if (threadIdx.x == 0) {
         bar_init(&bars->full, 1);
         bar_init(&bars->s_full, 1);
-        bar_init(&bars->p_ready, 4);
+        bar_init(&bars->p_ready, 8);
         bar_init(&bars->o_full, 1);
         bar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -137,10 +162,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd(const __grid_constant
 
     if (warp == 0) {
         if (lane == 0) {
-            bar_expect_tx(&bars->full, Q_BYTES + 2 * KV_BYTES);
+            bar_expect_tx(&bars->full, Q_BYTES + 2 * nkb * Q_BYTES);
             tma_load_4d(sq, &tq, &bars->full, 0, q0, h, b);
-            tma_load_4d(sk, &tk, &bars->full, 0, 0, h, b);
-            tma_load_4d(sv, &tv, &bars->full, 0, 0, h, b);
+            for (int kb = 0; kb < nkb; ++kb) {
+                tma_load_4d(sk + kb * Q_BYTES, &tk, &bars->full, 0, kb * QT, h, b);
+                tma_load_4d(sv + kb * Q_BYTES, &tv, &bars->full, 0, kb * QT, h, b);
+            }
             bar_wait_drain(&bars->full, 0u);  // the copies land before this CTA may exit
         }
     } else if (warp == 1) {
@@ -148,23 +175,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd(const __grid_constant
             bool ok = bar_wait(&bars->full, 0u, &bars->abort, p.status);
             if (ok) {
                 tc_fence_after();
-                // S = Q K^T: A = Q (K-major), B = K (K-major, N = 256 keys); K step 16 = 32 bytes
+                // S = Q K^T: A = Q (K-major), B = K (K-major, N = kv_pad keys); K step 16 = 32 bytes
                 const uint64_t ad = sdesc(smem_u32(sq), 16u, 1024u), bd = sdesc(smem_u32(sk), 16u, 1024u);
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k)
-                    mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc_bf16(QT, KB, false), k > 0 ? 1u : 0u);
+                    mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc_bf16(QT, kv_pad, false), k > 0 ? 1u : 0u);
                 mma_commit(&bars->s_full);
                 ok = bar_wait(&bars->p_ready, 0u, &bars->abort, p.status);
             }
             if (ok) {
                 tc_fence_after();
-                // O = P V: A = P (K-major atoms of 64 keys), B = V (MN-major: rows = keys,
-                // 8-row groups 1024 B apart; a K step of 16 keys is 2 KB)
+                // O = P V: A = P from TMEM (8 columns a 16-key step), B = V (MN-major:
+                // rows = keys, 8-row groups 1024 B apart; a 16-key step is 2 KB)
                 const uint64_t vd = sdesc(smem_u32(sv), 8192u, 1024u);
-#pragma unroll
-                for (int ks = 0; ks < KB / 16; ++ks) {
-                    const uint64_t pd = sdesc(smem_u32(sp + (ks >> 2) * P_ATOM), 16u, 1024u) + 2u * (ks & 3);
-                    mma_f16(tmem, pd, vd + 128u * ks, idesc_bf16(QT, HD, true), ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < kv_pad / 16; ++ks) {
+                    const uint32_t pa = tmem + (ks < 8 ? 8u * ks : FWD_P1 + 8u * (ks - 8));
+                    mma_f16_ts(tmem + FWD_O, pa, vd + 128u * ks, idesc_bf16(QT, HD, true), ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&bars->o_full);
             }
@@ -172,17 +198,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd(const __grid_constant
             bar_wait_drain(&bars->drain, 0u);
         }
     } else {
-        // rows: warps 2-5 own TMEM lanes 32 (warp % 4) .. + 31 = query rows of the tile
-        const int r = 32 * (warp & 3) + lane;
+        // rows: warp w owns TMEM lanes 32 (w % 4) .. + 31 (the query rows) and
+        // the keys of half (w - 2) / 4
+        const int half = (warp - 2) >> 2;
+        const int g = warp & 3;
+        const int r = 32 * g + lane;
         const int i = q0 + r;
-        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        // ok stays warp-uniform: the TMEM loads below are warp-collective
+        const uint32_t trow = tmem + ((uint32_t)(32 * g) << 16);
+        const int c_beg = QT * half, c_end = min(c_beg + QT, kv_pad);
+        const uint32_t pcol = half ? FWD_P1 : 0u;
+        // ok stays warp-uniform: the TMEM loads and stores below are warp-collective
         bool ok = __all_sync(0xffffffffu, bar_wait(&bars->s_full, 0u, &bars->abort, p.status));
         tc_fence_after();
         const int kmax = p.causal ? min(i + 1, p.T) : p.T;  // keys 0 .. kmax-1 are visible
-        float m = -INFINITY, l = 0.0f;
+        float m = -INFINITY;
         if (ok) {
-            for (int c = 0; c < KB; c += 32) {
+            for (int c = c_beg; c < c_end; c += 32) {
                 uint32_t s[32];
                 __syncwarp();
                 tmem_ld32(trow + (uint32_t)c, s);
@@ -190,7 +221,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd(const __grid_constant
                 for (int j = 0; j < 32; ++j)
                     if (c + j < kmax) m = fmaxf(m, p.scale * __uint_as_float(s[j]));
             }
-            for (int c = 0; c < KB; c += 32) {
+        }
+        red_m[half * QT + r] = m;
+        rows_sync();
+        m = fmaxf(red_m[r], red_m[QT + r]);  // the row's max, the same in both halves
+        float l = 0.0f;
+        if (ok) {
+            for (int c = c_beg; c < c_end; c += 32) {
                 uint32_t s[32];
                 __syncwarp();
                 tmem_ld32(trow + (uint32_t)c, s);
@@ -201,40 +238,38 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd(const __grid_constant
                     // logsumexp); P is rounded to bf16 only as the MMA operand
                     const float e0 = c + j < kmax ? __expf(p.scale * __uint_as_float(s[j]) - m) : 0.0f;
                     const float e1 = c + j + 1 < kmax ? __expf(p.scale * __uint_as_float(s[j + 1]) - m) : 0.0f;
-                    l += e0 + e1;
+                    l += e0;
+                    l += e1;
                     w[j >> 1] = pack_bf16(e0, e1);
                 }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    *(uint4*)(sp + katom_off(r, c + 8 * u)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                                                                         w[4 * u + 3]);
+                // columns (c - c_beg) / 2 .. + 15 of the half's P: S this thread has read
+                tmem_st16(trow + pcol + (uint32_t)((c - c_beg) >> 1), w);
             }
+            tmem_wait_st();
         }
-        // P (generic-proxy writes) is read by the MMAs (async proxy)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        red_l[half * QT + r] = l;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) bar_arrive(&bars->p_ready);
+        rows_sync();
+        l = red_l[r] + red_l[QT + r];  // first half, then second: one order in both
         if (ok) ok = __all_sync(0xffffffffu, bar_wait(&bars->o_full, 0u, &bars->abort, p.status));
         tc_fence_after();
         if (ok) {
-            uint32_t o[32], o2[32];
-            __syncwarp();  // every lane reaches the collective loads
-            tmem_ld32(trow, o);
-            tmem_ld32(trow + 32u, o2);
+            uint32_t o[32];
+            __syncwarp();  // every lane reaches the collective load
+            tmem_ld32(trow + FWD_O + 32u * half, o);
             if (i < p.T) {
                 const float inv = 1.0f / l;
-                p.lse[((int64_t)b * p.H + h) * p.T + i] = m + logf(l);
+                if (half == 0) p.lse[((int64_t)b * p.H + h) * p.T + i] = m + logf(l);
                 __nv_bfloat16* dst = (__nv_bfloat16*)p.o + p.o_off + (int64_t)b * p.o_sb + (int64_t)i * p.o_st +
-                                     (int64_t)h * p.o_sh;
-                uint32_t w[32];
+                                     (int64_t)h * p.o_sh + 32 * half;
+                uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < 16; ++j)
                     w[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-                    w[16 + j] = pack_bf16(__uint_as_float(o2[2 * j]) * inv, __uint_as_float(o2[2 * j + 1]) * inv);
-                }
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
+                for (int u = 0; u < 4; ++u)
                     ((uint4*)dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
             }
         }
@@ -667,8 +702,8 @@ psg_status launch_attention_fwd(const AttnTensor& q, const AttnTensor& k, const 
 {
     if (p.B == 0 || p.T == 0 || p.H == 0) return PSG_OK;
     CUtensorMap mq, mk, mv;
-    if (!make_map_attn(&mq, q, p.T, p.H, p.B, QT) || !make_map_attn(&mk, k, p.T, p.H, p.B, KB) ||
-        !make_map_attn(&mv, v, p.T, p.H, p.B, KB))
+    if (!make_map_attn(&mq, q, p.T, p.H, p.B, QT) || !make_map_attn(&mk, k, p.T, p.H, p.B, QT) ||
+        !make_map_attn(&mv, v, p.T, p.H, p.B, QT))
         return PSG_E_CUDA;
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
