@@ -53,7 +53,6 @@ constexpr int HD = 64;                      // head dim
 constexpr int ROW_BYTES = HD * 2;           // 128: one swizzle row
 constexpr int Q_BYTES = QT * ROW_BYTES;     // 16 KB
 constexpr int KV_BYTES = KB * ROW_BYTES;    // 32 KB
-constexpr int P_ATOM = QT * 128;            // 16 KB: 128 rows x 64 keys (bf16)
 constexpr int FWD_THREADS = 320;            // warp 0 TMA, warp 1 MMA, warps 2-9 two per query row
 constexpr int FWD_SMEM = 1024 + Q_BYTES + 2 * KV_BYTES + 256 + 4 * QT * 4;
 constexpr int FWD_TMEM = 256;
@@ -97,14 +96,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         "[%2];"
         ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
-}
-
-// byte offset of (row r, column j) in a K-major bf16 tile of 64-column
-// atoms (128 rows x 128 bytes each, 128-byte swizzle): atom j / 64, 16-byte
-// chunk (j % 64) / 8 stored at chunk ^ (r % 8)
-__device__ __forceinline__ uint32_t katom_off(int r, int j)
-{
-    return (uint32_t)((j >> 6) * P_ATOM + r * 128 + ((((j & 63) >> 3) ^ (r & 7)) << 4) + ((j & 7) << 1));
 }
 
 // instruction descriptor: f32 accumulate, bf16 A and B, A K-major
@@ -281,18 +272,30 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
 }
 
 // ---- backward ---------------------------------------------------------------
+// Both passes, one CTA per (128-row tile of its own operands, head, batch),
+// two resident a SM.  The streamed operand tiles (at most two: T <= 256) are
+// all loaded at the start and taken 64 rows (a sub-tile) at a time:
+//   pass K/V (KV): own K, V (rows = keys); streamed Q, dO (columns = queries)
+//     S^T = K Q^T, dP^T = V dO^T, P^T = exp(scale S^T - L), dS^T = P^T (dP^T - D)
+//     dV += P^T dO, dK += dS^T Q            (dK scaled by `scale` at the end)
+//   pass Q: own Q, dO (rows = queries); streamed K, V (columns = keys)
+//     S = Q K^T, dP = dO V^T, P = exp(scale S - L), dS = P (dP - D)
+//     dQ += dS K                            (scaled by `scale` at the end)
+// TMEM columns (256): S 0-63, dP 64-127, dV 128-191, dK or dQ 192-255.  P and
+// dS (bf16 pairs) go back into TMEM over the S and dP columns their own
+// thread has read (half h of the columns at 32 h .. 32 h + 15), and the
+// second products take them as the A operand from TMEM.  Two threads share a
+// row, one per half of the sub-tile's 64 columns; each gradient cell is
+// accumulated by one CTA in a fixed order (no atomics).
 constexpr int T_BYTES = QT * ROW_BYTES;     // 16 KB: a 128-row tile of one operand
-constexpr int G_BYTES = 2 * P_ATOM;         // 32 KB: 128 rows x 128 columns bf16 (two atoms)
-constexpr int BWD_THREADS = 192;
-constexpr int KV_SMEM = 1024 + 4 * T_BYTES + 2 * G_BYTES + 2 * QT * 4 + 256 + 1024;
-// (sized past half the SM's shared memory: with all 512 TMEM columns each,
-// a second resident CTA would only wait in tcgen05.alloc)
-constexpr int Q_SMEM = 120 * 1024;
-static_assert(1024 + 4 * T_BYTES + G_BYTES + 256 <= Q_SMEM, "pass Q shared memory");
-constexpr int BWD_TMEM = 512;
+constexpr int SUB = 64;                     // streamed rows a sub-tile
+constexpr int BWD_THREADS = 320;            // warp 0 TMA, warp 1 MMA, warps 2-9 two per row
+constexpr int BWD_SMEM = 1024 + 6 * T_BYTES + 4 * QT * 4 + 256;
+constexpr int BWD_TMEM = 256;
+constexpr uint32_t BWD_DP = 64, BWD_ACC0 = 128, BWD_ACC1 = 192;
 
 struct BwdBars {
-    uint64_t full, mm1, ready, mm2, drain;
+    uint64_t full[2], mm1, ready, mm2, drain;
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -334,53 +337,53 @@ __global__ void __launch_bounds__(256) attn_delta(const __grid_constant__ AttnTe
     }
 }
 
-// store 64 float32 accumulator columns (scaled) of row `row` as bf16
-__device__ __forceinline__ void store_row64(const AttnTensor& t, int b, int row, int h, const uint32_t (&x)[32],
-                                            const uint32_t (&y)[32], float scale)
+// store 32 float32 accumulator columns (scaled) of row `row` as bf16, at
+// head-dim columns c0 .. c0 + 31
+__device__ __forceinline__ void store_row32(const AttnTensor& t, int b, int row, int h, int c0,
+                                            const uint32_t (&x)[32], float scale)
 {
-    __nv_bfloat16* dst = (__nv_bfloat16*)t.ptr + t.off + (int64_t)b * t.sb + (int64_t)row * t.st + (int64_t)h * t.sh;
-    uint32_t w[32];
+    __nv_bfloat16* dst =
+        (__nv_bfloat16*)t.ptr + t.off + (int64_t)b * t.sb + (int64_t)row * t.st + (int64_t)h * t.sh + c0;
+    uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 16; ++j)
         w[j] = pack_bf16(__uint_as_float(x[2 * j]) * scale, __uint_as_float(x[2 * j + 1]) * scale);
-        w[16 + j] = pack_bf16(__uint_as_float(y[2 * j]) * scale, __uint_as_float(y[2 * j + 1]) * scale);
-    }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) ((uint4*)dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+    for (int u = 0; u < 4; ++u) ((uint4*)dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
 }
 
-// pass K/V: one CTA per (128-key tile, head, batch), over the query tiles
-// that can see its keys.  TMEM columns: S^T 0-127, dP^T 128-255, dV 256-319,
-// dK 320-383.
-__global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kv(const __grid_constant__ CUtensorMap tq,
-                                                              const __grid_constant__ CUtensorMap tk,
-                                                              const __grid_constant__ CUtensorMap tv,
-                                                              const __grid_constant__ CUtensorMap tdo,
-                                                              const __grid_constant__ AttnTensor dk,
-                                                              const __grid_constant__ AttnTensor dv,
-                                                              const __grid_constant__ AttnParams p)
+template <bool KV>
+__global__ void __launch_bounds__(BWD_THREADS, 2) attn_bwd(const __grid_constant__ CUtensorMap tq,
+                                                           const __grid_constant__ CUtensorMap tk,
+                                                           const __grid_constant__ CUtensorMap tv,
+                                                           const __grid_constant__ CUtensorMap tdo,
+                                                           const __grid_constant__ AttnTensor g0,
+                                                           const __grid_constant__ AttnTensor g1,
+                                                           const __grid_constant__ AttnParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* sk = smem;                  // [128 keys][64]
-    uint8_t* sv = sk + T_BYTES;          // [128 keys][64]
-    uint8_t* sq = sv + T_BYTES;          // [128 q][64]
-    uint8_t* sdo = sq + T_BYTES;         // [128 q][64]
-    uint8_t* spt = sdo + T_BYTES;        // P^T: [128 keys][128 q] in two 64-column atoms
-    uint8_t* sdst = spt + G_BYTES;       // dS^T
-    float* sL = (float*)(sdst + G_BYTES);
-    float* sD = sL + QT;
-    BwdBars* bars = (BwdBars*)(sD + QT);
+    uint8_t* own0 = smem;                   // KV: K, Q: Q  [128 rows][64]
+    uint8_t* own1 = own0 + T_BYTES;         // KV: V, Q: dO
+    uint8_t* st0 = own1 + T_BYTES;          // KV: Q, Q: K  [2 tiles][128 rows][64]
+    uint8_t* st1 = st0 + 2 * T_BYTES;       // KV: dO, Q: V
+    float* sL = (float*)(st1 + 2 * T_BYTES);  // KV: L, D of the streamed queries [2 tiles][128]
+    float* sD = sL + 2 * QT;
+    BwdBars* bars = (BwdBars*)(sD + 2 * QT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int k0 = kt * QT;
-    const int nq = (p.T + QT - 1) / QT;
-    const int qt0 = p.causal ? kt : 0;
+    const int ot = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int r0 = ot * QT;  // first own row (key in KV, query in Q)
+    const int ntile = (p.T + QT - 1) / QT;
+    // streamed tiles: KV, the query tiles that see these keys; Q, the key tiles these queries see
+    const int it0 = KV ? (p.causal ? ot : 0) : 0;
+    const int it1 = KV ? ntile : (p.causal ? min(ot + 1, ntile) : ntile);
+    const int nst = 2 * (it1 - it0);  // sub-tiles
 
     if (threadIdx.x == 0) {
-        bar_init(&bars->full, 1);
+        bar_init(&bars->full[0], 1);
+        bar_init(&bars->full[1], 1);
         bar_init(&bars->mm1, 1);
-        bar_init(&bars->ready, 4);
+        bar_init(&bars->ready, 8);
         bar_init(&bars->mm2, 1);
         bar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -395,283 +398,140 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kv(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    bool ok = true;
-    uint32_t ph = 0;
-    for (int qt = qt0; qt < nq; ++qt, ph ^= 1u) {
-        const int q0 = qt * QT;
-        if (warp == 0) {
-            if (lane == 0) {
-                const uint32_t bytes = (qt == qt0 ? 4u : 2u) * T_BYTES;
-                bar_expect_tx(&bars->full, bytes);
-                if (qt == qt0) {
-                    tma_load_4d(sk, &tk, &bars->full, 0, k0, h, b);
-                    tma_load_4d(sv, &tv, &bars->full, 0, k0, h, b);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const CUtensorMap* m_own0 = KV ? &tk : &tq;
+            const CUtensorMap* m_own1 = KV ? &tv : &tdo;
+            const CUtensorMap* m_st0 = KV ? &tq : &tk;
+            const CUtensorMap* m_st1 = KV ? &tdo : &tv;
+            for (int t = it0; t < it1; ++t) {
+                uint64_t* fb = &bars->full[t - it0];
+                bar_expect_tx(fb, (t == it0 ? 4u : 2u) * T_BYTES);
+                if (t == it0) {
+                    tma_load_4d(own0, m_own0, fb, 0, r0, h, b);
+                    tma_load_4d(own1, m_own1, fb, 0, r0, h, b);
                 }
-                tma_load_4d(sq, &tq, &bars->full, 0, q0, h, b);
-                tma_load_4d(sdo, &tdo, &bars->full, 0, q0, h, b);
-                bar_wait_drain(&bars->full, ph);
+                tma_load_4d(st0 + (t - it0) * T_BYTES, m_st0, fb, 0, t * QT, h, b);
+                tma_load_4d(st1 + (t - it0) * T_BYTES, m_st1, fb, 0, t * QT, h, b);
             }
-        } else if (warp == 1) {
-            if (lane == 0 && ok) {
-                ok = bar_wait(&bars->full, ph, &bars->abort, p.status);
-                if (ok) {
-                    tc_fence_after();
-                    const uint64_t kd = sdesc(smem_u32(sk), 16u, 1024u), vd = sdesc(smem_u32(sv), 16u, 1024u);
-                    const uint64_t qd = sdesc(smem_u32(sq), 16u, 1024u), dod = sdesc(smem_u32(sdo), 16u, 1024u);
+            // the copies land before this CTA may exit
+            for (int t = it0; t < it1; ++t) bar_wait_drain(&bars->full[t - it0], 0u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            const uint64_t a0 = sdesc(smem_u32(own0), 16u, 1024u), a1 = sdesc(smem_u32(own1), 16u, 1024u);
+            for (int st = 0; st < nst && ok; ++st) {
+                const int t = st >> 1, s = st & 1;
+                if (s == 0) ok = bar_wait(&bars->full[t], 0u, &bars->abort, p.status);
+                // the previous sub-tile's second products have read P and dS (S and dP columns)
+                if (ok && st > 0) ok = bar_wait(&bars->mm2, (uint32_t)((st - 1) & 1), &bars->abort, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sub = smem_u32(st0 + t * T_BYTES) + (uint32_t)(s * SUB * ROW_BYTES);
+                const uint32_t sub1 = smem_u32(st1 + t * T_BYTES) + (uint32_t)(s * SUB * ROW_BYTES);
+                const uint64_t b0 = sdesc(sub, 16u, 1024u), b1 = sdesc(sub1, 16u, 1024u);
 #pragma unroll
-                    for (int k = 0; k < HD / 16; ++k) {
-                        mma_f16(tmem, kd + 2u * k, qd + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
-                        mma_f16(tmem + 128u, vd + 2u * k, dod + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(&bars->mm1);
-                    ok = bar_wait(&bars->ready, ph, &bars->abort, p.status);
+                for (int k = 0; k < HD / 16; ++k) {
+                    mma_f16(tmem, a0 + 2u * k, b0 + 2u * k, idesc_bf16(QT, SUB, false), k > 0 ? 1u : 0u);
+                    mma_f16(tmem + BWD_DP, a1 + 2u * k, b1 + 2u * k, idesc_bf16(QT, SUB, false), k > 0 ? 1u : 0u);
                 }
-                if (ok) {
-                    tc_fence_after();
-                    // dV += P^T dO, dK += dS^T Q: B = dO, Q as MN-major (rows = queries)
-                    const uint64_t dob = sdesc(smem_u32(sdo), 8192u, 1024u), qb = sdesc(smem_u32(sq), 8192u, 1024u);
+                mma_commit(&bars->mm1);
+                ok = bar_wait(&bars->ready, (uint32_t)(st & 1), &bars->abort, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                // KV: dV += P^T dO_sub, dK += dS^T Q_sub; Q: dQ += dS K_sub.  B MN-major
+                // (rows = the sub-tile's streamed rows; a 16-row K step is 2 KB)
+                const uint64_t n0 = sdesc(sub, 8192u, 1024u), n1 = sdesc(sub1, 8192u, 1024u);
 #pragma unroll
-                    for (int ks = 0; ks < QT / 16; ++ks) {
-                        const uint32_t acc = (qt > qt0 || ks > 0) ? 1u : 0u;
-                        const uint64_t pa = sdesc(smem_u32(spt + (ks >> 2) * P_ATOM), 16u, 1024u) + 2u * (ks & 3);
-                        const uint64_t sa = sdesc(smem_u32(sdst + (ks >> 2) * P_ATOM), 16u, 1024u) + 2u * (ks & 3);
-                        mma_f16(tmem + 256u, pa, dob + 128u * ks, idesc_bf16(QT, HD, true), acc);
-                        mma_f16(tmem + 320u, sa, qb + 128u * ks, idesc_bf16(QT, HD, true), acc);
-                    }
+                for (int ks = 0; ks < SUB / 16; ++ks) {
+                    const uint32_t col = 32u * (ks >> 1) + 8u * (ks & 1);  // half ks / 2, 8 columns a step
+                    const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
+                    if (KV) mma_f16_ts(tmem + BWD_ACC0, tmem + col, n1 + 128u * ks, idesc_bf16(QT, HD, true), acc);
+                    mma_f16_ts(tmem + BWD_ACC1, tmem + BWD_DP + col, n0 + 128u * ks, idesc_bf16(QT, HD, true), acc);
                 }
-                mma_commit(&bars->mm2);  // also when giving up, so the rows never wait long
+                mma_commit(&bars->mm2);
             }
-        } else {
-            // rows: key r of the tile; columns: the tile's queries
-            const int r = 32 * (warp & 3) + lane;
-            const int j = k0 + r;
-            const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-            // L and D of the tile's queries, one per thread of the four warps
-            const int c_ = threadIdx.x - 64;
-            {
-                const int i = q0 + c_;
-                sL[c_] = i < p.T ? p.lse[((int64_t)b * p.H + h) * p.T + i] : 0.0f;
-                sD[c_] = i < p.T ? p.delta[((int64_t)b * p.H + h) * p.T + i] : 0.0f;
+            mma_commit(&bars->drain);
+            bar_wait_drain(&bars->drain, 0u);
+        }
+    } else {
+        // rows: warp w owns TMEM lanes 32 (w % 4) .. + 31 and half (w - 2) / 4 of each sub-tile's columns
+        const int half = (warp - 2) >> 2;
+        const int g = warp & 3;
+        const int r = 32 * g + lane;
+        const int row = r0 + r;  // KV: key j; Q: query i
+        const uint32_t trow = tmem + ((uint32_t)(32 * g) << 16);
+        const int64_t lbase = ((int64_t)b * p.H + h) * p.T;
+        float Lr = 0.0f, Dr = 0.0f;
+        if (KV) {
+            // L and D of every streamed query, for all the row threads
+            const int tid = threadIdx.x - 64;
+            for (int x = tid; x < (it1 - it0) * QT; x += 256) {
+                const int i = it0 * QT + x;
+                sL[x] = i < p.T ? p.lse[lbase + i] : 0.0f;
+                sD[x] = i < p.T ? p.delta[lbase + i] : 0.0f;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four row warps only
-            const bool okw = __all_sync(0xffffffffu, bar_wait(&bars->mm1, ph, &bars->abort, p.status));
+            rows_sync();
+        } else if (row < p.T) {
+            Lr = p.lse[lbase + row];
+            Dr = p.delta[lbase + row];
+        }
+        bool ok = true;
+        for (int st = 0; st < nst; ++st) {
+            const int t = st >> 1, s = st & 1;
+            ok = ok && __all_sync(0xffffffffu, bar_wait(&bars->mm1, (uint32_t)(st & 1), &bars->abort, p.status));
             tc_fence_after();
-            if (okw) {
-                for (int c = 0; c < QT; c += 32) {
-                    uint32_t s[32], dp[32];
-                    __syncwarp();
-                    tmem_ld32(trow + (uint32_t)c, s);
-                    tmem_ld32(trow + 128u + (uint32_t)c, dp);
-                    uint32_t wp[16], ws[16];
+            if (ok) {
 #pragma unroll
-                    for (int u = 0; u < 32; u += 2) {
+                for (int cc = 0; cc < 32; cc += 16) {
+                    uint32_t sv[16], dp[16], wp[8], ws[8];
+                    __syncwarp();
+                    tmem_ld16(trow + 32u * half + cc, sv);
+                    tmem_ld16(trow + BWD_DP + 32u * half + cc, dp);
+#pragma unroll
+                    for (int u = 0; u < 16; u += 2) {
                         float pv[2], dsv[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const int i = q0 + c + u + e;
+                            const int c = SUB * s + 32 * half + cc + u + e;  // streamed row within its tile
+                            const int other = (it0 + t) * QT + c;
+                            const int i = KV ? other : row, j = KV ? row : other;
                             const bool vis = i < p.T && j < p.T && (!p.causal || j <= i);
-                            const float pe = vis ? __expf(p.scale * __uint_as_float(s[u + e]) - sL[c + u + e]) : 0.0f;
+                            const float L = KV ? sL[t * QT + c] : Lr, D = KV ? sD[t * QT + c] : Dr;
+                            const float pe = vis ? __expf(p.scale * __uint_as_float(sv[u + e]) - L) : 0.0f;
                             pv[e] = pe;
-                            dsv[e] = pe * (__uint_as_float(dp[u + e]) - sD[c + u + e]);
+                            dsv[e] = pe * (__uint_as_float(dp[u + e]) - D);
                         }
                         wp[u >> 1] = pack_bf16(pv[0], pv[1]);
                         ws[u >> 1] = pack_bf16(dsv[0], dsv[1]);
                     }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        *(uint4*)(spt + katom_off(r, c + 8 * u)) =
-                            make_uint4(wp[4 * u], wp[4 * u + 1], wp[4 * u + 2], wp[4 * u + 3]);
-                        *(uint4*)(sdst + katom_off(r, c + 8 * u)) =
-                            make_uint4(ws[4 * u], ws[4 * u + 1], ws[4 * u + 2], ws[4 * u + 3]);
-                    }
+                    // over the S and dP columns this thread has just read
+                    if (KV) tmem_st8(trow + 32u * half + (cc >> 1), wp);
+                    tmem_st8(trow + BWD_DP + 32u * half + (cc >> 1), ws);
                 }
+                tmem_wait_st();
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive(&bars->ready);
         }
-        // the dV / dK MMAs of this query tile finish before its tiles are replaced
-        if (!bar_wait(&bars->mm2, ph, &bars->abort, p.status)) ok = false;
+        // the last sub-tile's second products are done: the gradients are complete
+        if (ok && nst > 0)
+            ok = __all_sync(0xffffffffu, bar_wait(&bars->mm2, (uint32_t)((nst - 1) & 1), &bars->abort, p.status));
         tc_fence_after();
-        __syncthreads();
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-    }
-    if (warp >= 2) {
-        const int r = 32 * (warp & 3) + lane;
-        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        if (ok && qt0 < nq) {
-            uint32_t x[32], y[32];
+        if (ok) {
+            // (every tile has at least one streamed tile: nst >= 2 for T >= 1)
+            uint32_t x[32];
             __syncwarp();
-            tmem_ld32(trow + 256u, x);
-            tmem_ld32(trow + 288u, y);
-            if (k0 + r < p.T) store_row64(dv, b, k0 + r, h, x, y, 1.0f);
-            tmem_ld32(trow + 320u, x);
-            tmem_ld32(trow + 352u, y);
-            if (k0 + r < p.T) store_row64(dk, b, k0 + r, h, x, y, p.scale);
-        } else if (qt0 >= nq) {
-            uint32_t z[32];
-#pragma unroll
-            for (int u = 0; u < 32; ++u) z[u] = 0u;
-            if (k0 + r < p.T) {
-                store_row64(dv, b, k0 + r, h, z, z, 1.0f);
-                store_row64(dk, b, k0 + r, h, z, z, 1.0f);
+            if (KV) {
+                tmem_ld32(trow + BWD_ACC0 + 32u * half, x);
+                if (row < p.T) store_row32(g0, b, row, h, 32 * half, x, 1.0f);
             }
+            tmem_ld32(trow + BWD_ACC1 + 32u * half, x);
+            if (row < p.T) store_row32(KV ? g1 : g0, b, row, h, 32 * half, x, p.scale);
         }
-    }
-    if (warp == 1 && lane == 0) {
-        mma_commit(&bars->drain);
-        bar_wait_drain(&bars->drain, 0u);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BWD_TMEM));
-}
-
-// pass Q: one CTA per (128-query tile, head, batch), over the key tiles it
-// can see.  TMEM columns: S 0-127, dP 128-255, dQ 256-319.
-__global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_q(const __grid_constant__ CUtensorMap tq,
-                                                             const __grid_constant__ CUtensorMap tk,
-                                                             const __grid_constant__ CUtensorMap tv,
-                                                             const __grid_constant__ CUtensorMap tdo,
-                                                             const __grid_constant__ AttnTensor dq,
-                                                             const __grid_constant__ AttnParams p)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* sq = smem;                  // [128 q][64]
-    uint8_t* sdo = sq + T_BYTES;         // [128 q][64]
-    uint8_t* sk = sdo + T_BYTES;         // [128 keys][64]
-    uint8_t* sv = sk + T_BYTES;          // [128 keys][64]
-    uint8_t* sds = sv + T_BYTES;         // dS: [128 q][128 keys] in two 64-column atoms
-    BwdBars* bars = (BwdBars*)(sds + G_BYTES);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int q0 = qt * QT;
-    const int nk = (p.T + QT - 1) / QT;
-    const int kt1 = p.causal ? min(qt + 1, nk) : nk;   // key tiles 0 .. kt1-1
-
-    if (threadIdx.x == 0) {
-        bar_init(&bars->full, 1);
-        bar_init(&bars->mm1, 1);
-        bar_init(&bars->ready, 4);
-        bar_init(&bars->mm2, 1);
-        bar_init(&bars->drain, 1);
-        bars->abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(&bars->tmem_base)), "r"(BWD_TMEM));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
-    const int r = 32 * (warp & 3) + lane;      // query row of the tile (row warps)
-    const int i = q0 + r;
-    float Li = 0.0f, Di = 0.0f;
-    if (warp >= 2 && i < p.T) {
-        Li = p.lse[((int64_t)b * p.H + h) * p.T + i];
-        Di = p.delta[((int64_t)b * p.H + h) * p.T + i];
-    }
-    bool ok = true;
-    uint32_t ph = 0;
-    for (int kt = 0; kt < kt1; ++kt, ph ^= 1u) {
-        const int k0 = kt * QT;
-        if (warp == 0) {
-            if (lane == 0) {
-                bar_expect_tx(&bars->full, (kt == 0 ? 4u : 2u) * T_BYTES);
-                if (kt == 0) {
-                    tma_load_4d(sq, &tq, &bars->full, 0, q0, h, b);
-                    tma_load_4d(sdo, &tdo, &bars->full, 0, q0, h, b);
-                }
-                tma_load_4d(sk, &tk, &bars->full, 0, k0, h, b);
-                tma_load_4d(sv, &tv, &bars->full, 0, k0, h, b);
-                bar_wait_drain(&bars->full, ph);
-            }
-        } else if (warp == 1) {
-            if (lane == 0 && ok) {
-                ok = bar_wait(&bars->full, ph, &bars->abort, p.status);
-                if (ok) {
-                    tc_fence_after();
-                    const uint64_t qd = sdesc(smem_u32(sq), 16u, 1024u), dod = sdesc(smem_u32(sdo), 16u, 1024u);
-                    const uint64_t kd = sdesc(smem_u32(sk), 16u, 1024u), vd = sdesc(smem_u32(sv), 16u, 1024u);
-#pragma unroll
-                    for (int k = 0; k < HD / 16; ++k) {
-                        mma_f16(tmem, qd + 2u * k, kd + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
-                        mma_f16(tmem + 128u, dod + 2u * k, vd + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(&bars->mm1);
-                    ok = bar_wait(&bars->ready, ph, &bars->abort, p.status);
-                }
-                if (ok) {
-                    tc_fence_after();
-                    // dQ += dS K: B = K as MN-major (rows = keys)
-                    const uint64_t kb = sdesc(smem_u32(sk), 8192u, 1024u);
-#pragma unroll
-                    for (int ks = 0; ks < QT / 16; ++ks) {
-                        const uint64_t sa = sdesc(smem_u32(sds + (ks >> 2) * P_ATOM), 16u, 1024u) + 2u * (ks & 3);
-                        mma_f16(tmem + 256u, sa, kb + 128u * ks, idesc_bf16(QT, HD, true),
-                                (kt > 0 || ks > 0) ? 1u : 0u);
-                    }
-                }
-                mma_commit(&bars->mm2);
-            }
-        } else {
-            const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-            const bool okw = __all_sync(0xffffffffu, bar_wait(&bars->mm1, ph, &bars->abort, p.status));
-            tc_fence_after();
-            if (okw) {
-                for (int c = 0; c < QT; c += 32) {
-                    uint32_t s[32], dp[32];
-                    __syncwarp();
-                    tmem_ld32(trow + (uint32_t)c, s);
-                    tmem_ld32(trow + 128u + (uint32_t)c, dp);
-                    uint32_t ws[16];
-#pragma unroll
-                    for (int u = 0; u < 32; u += 2) {
-                        float dsv[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int j = k0 + c + u + e;
-                            const bool vis = i < p.T && j < p.T && (!p.causal || j <= i);
-                            const float pe = vis ? __expf(p.scale * __uint_as_float(s[u + e]) - Li) : 0.0f;
-                            dsv[e] = pe * (__uint_as_float(dp[u + e]) - Di);
-                        }
-                        ws[u >> 1] = pack_bf16(dsv[0], dsv[1]);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        *(uint4*)(sds + katom_off(r, c + 8 * u)) =
-                            make_uint4(ws[4 * u], ws[4 * u + 1], ws[4 * u + 2], ws[4 * u + 3]);
-                }
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) bar_arrive(&bars->ready);
-        }
-        if (!bar_wait(&bars->mm2, ph, &bars->abort, p.status)) ok = false;
-        tc_fence_after();
-        __syncthreads();
-        ok = __syncthreads_and(ok);
-        if (!ok) break;
-    }
-    if (warp >= 2 && ok && kt1 > 0) {
-        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        uint32_t x[32], y[32];
-        __syncwarp();
-        tmem_ld32(trow + 256u, x);
-        tmem_ld32(trow + 288u, y);
-        if (i < p.T) store_row64(dq, b, i, h, x, y, p.scale);
-    }
-    if (warp == 1 && lane == 0) {
-        mma_commit(&bars->drain);
-        bar_wait_drain(&bars->drain, 0u);
     }
     tc_fence_before();
     __syncthreads();
@@ -729,9 +589,11 @@ psg_status launch_attention_bwd(const AttnTensor& q, const AttnTensor& k, const 
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute((const void*)attn_bwd_kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
+        err = cudaFuncSetAttribute((const void*)attn_bwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   BWD_SMEM);
         if (err == cudaSuccess)
-            err = cudaFuncSetAttribute((const void*)attn_bwd_q, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM);
+            err = cudaFuncSetAttribute((const void*)attn_bwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       BWD_SMEM);
     });
     if (err != cudaSuccess) return PSG_E_CUDA;
     const int64_t rows = (int64_t)p.B * p.T * p.H;
@@ -739,8 +601,8 @@ psg_status launch_attention_bwd(const AttnTensor& q, const AttnTensor& k, const 
     attn_delta<<<dgrid, 256, 0, s>>>(o, dO, p);
     const unsigned tiles = (unsigned)((p.T + QT - 1) / QT);
     const dim3 grid(tiles, (unsigned)p.H, (unsigned)p.B);
-    attn_bwd_kv<<<grid, BWD_THREADS, KV_SMEM, s>>>(mq, mk, mv, mdo, dk, dv, p);
-    attn_bwd_q<<<grid, BWD_THREADS, Q_SMEM, s>>>(mq, mk, mv, mdo, dq, p);
+    attn_bwd<true><<<grid, BWD_THREADS, BWD_SMEM, s>>>(mq, mk, mv, mdo, dv, dk, p);
+    attn_bwd<false><<<grid, BWD_THREADS, BWD_SMEM, s>>>(mq, mk, mv, mdo, dq, dq, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
