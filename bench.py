@@ -462,7 +462,7 @@ class Rows:
             tf = flops / (ms * 1e-3) / 1e12
             return {"ms": round(ms, 5), "flops": flops, "achieved": round(tf, 2), "unit": "TFLOP/s",
                     "bound": "tensor", "peak": pk, "frac": round(tf / pk, 4),
-                    "note": "full T x T products counted (the causal half is computed and masked)",
+                    "note": "FLOPs of the full T x T products (the kernels skip the key tiles a causal query tile cannot see)",
                     "workload": "fused attention fwd+bwd B32 T256 H8 hd64 causal bf16 (4 launches)"}
         return fn, fin
 

@@ -318,8 +318,8 @@ psg_status psg_scatter_add_static(void* dst, const psg_view* dv, const int32_t* 
  *     dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
  * Views: Q, K, V, O, dO, dQ, dK, dV are bf16 [B, T, H, 64] (head dim
  * contiguous; batch, token and head strides multiples of 8 elements; base
- * 16-byte aligned; no mask).  T <= 256 (one key block per head); other
- * shapes return PSG_E_UNSUPPORTED_LAYOUT.  S and dP are float32 sums of exact
+ * 16-byte aligned; no mask).  T <= 256 (one key block per head), B <= 32767,
+ * H <= 65535; other shapes return PSG_E_UNSUPPORTED_LAYOUT.  S and dP are float32 sums of exact
  * bf16 products; P and dS are rounded to bf16 before the second products.
  * lse: device float32 [B, H, T], written by fwd and read by bwd.  delta:
  * device float32 [B, H, T] scratch of bwd (caller-owned).  scale > 0.

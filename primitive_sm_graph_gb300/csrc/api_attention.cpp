@@ -38,7 +38,8 @@ psg_status attn_common(const psg_view* qv, float scale, int causal, AttnParams* 
     p->B = (int)qv->shape[0];
     p->T = (int)qv->shape[1];
     p->H = (int)qv->shape[2];
-    if (qv->shape[0] > 65535 || qv->shape[2] > 65535) return PSG_E_UNSUPPORTED_LAYOUT;
+    // grid limits: heads on y (65535), 2 B on z (the two backward passes)
+    if (qv->shape[0] > 32767 || qv->shape[2] > 65535) return PSG_E_UNSUPPORTED_LAYOUT;
     if (p->T > 256) return PSG_E_UNSUPPORTED_LAYOUT;  // one key block per head
     if (!(scale > 0.0f) || !(scale < 1e30f)) return PSG_E_INVALID_ARG;
     p->scale = scale;

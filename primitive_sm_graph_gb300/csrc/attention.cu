@@ -353,13 +353,9 @@ __device__ __forceinline__ void store_row32(const AttnTensor& t, int b, int row,
 }
 
 template <bool KV>
-__global__ void __launch_bounds__(BWD_THREADS, 2) attn_bwd(const __grid_constant__ CUtensorMap tq,
-                                                           const __grid_constant__ CUtensorMap tk,
-                                                           const __grid_constant__ CUtensorMap tv,
-                                                           const __grid_constant__ CUtensorMap tdo,
-                                                           const __grid_constant__ AttnTensor g0,
-                                                           const __grid_constant__ AttnTensor g1,
-                                                           const __grid_constant__ AttnParams p)
+__device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                              const CUtensorMap& tdo, const AttnTensor& g0, const AttnTensor& g1,
+                                              const AttnParams& p, int b)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -371,7 +367,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2) attn_bwd(const __grid_constant
     float* sD = sL + 2 * QT;
     BwdBars* bars = (BwdBars*)(sD + 2 * QT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ot = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int ot = blockIdx.x, h = blockIdx.y;
     const int r0 = ot * QT;  // first own row (key in KV, query in Q)
     const int ntile = (p.T + QT - 1) / QT;
     // streamed tiles: KV, the query tiles that see these keys; Q, the key tiles these queries see
@@ -539,6 +535,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 2) attn_bwd(const __grid_constant
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BWD_TMEM));
 }
 
+// both passes in one grid (z < B: pass K/V of batch z, else pass Q of batch
+// z - B), so the two kinds of CTA fill each other's tails
+__global__ void __launch_bounds__(BWD_THREADS, 2) attn_bwd(const __grid_constant__ CUtensorMap tq,
+                                                           const __grid_constant__ CUtensorMap tk,
+                                                           const __grid_constant__ CUtensorMap tv,
+                                                           const __grid_constant__ CUtensorMap tdo,
+                                                           const __grid_constant__ AttnTensor dq,
+                                                           const __grid_constant__ AttnTensor dk,
+                                                           const __grid_constant__ AttnTensor dv,
+                                                           const __grid_constant__ AttnParams p)
+{
+    if ((int)blockIdx.z < p.B) attn_bwd_pass<true>(tq, tk, tv, tdo, dv, dk, p, (int)blockIdx.z);
+    else attn_bwd_pass<false>(tq, tk, tv, tdo, dq, dq, p, (int)blockIdx.z - p.B);
+}
+
 // 4-D tensor map over a [B, T, H, 64] bfloat16 operand: dims {64, T, H, B},
 // box {64, rows, 1, 1}, 128-byte swizzle (one 128-byte row per token).
 bool make_map_attn(CUtensorMap* map, const AttnTensor& t, int T, int H, int B, uint32_t rows)
@@ -589,20 +600,15 @@ psg_status launch_attention_bwd(const AttnTensor& q, const AttnTensor& k, const 
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute((const void*)attn_bwd<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   BWD_SMEM);
-        if (err == cudaSuccess)
-            err = cudaFuncSetAttribute((const void*)attn_bwd<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       BWD_SMEM);
+        err = cudaFuncSetAttribute((const void*)attn_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
     });
     if (err != cudaSuccess) return PSG_E_CUDA;
     const int64_t rows = (int64_t)p.B * p.T * p.H;
     const int dgrid = (int)std::min<int64_t>((rows + 31) / 32, (int64_t)num_sms() * 16);  // 32 rows a block
     attn_delta<<<dgrid, 256, 0, s>>>(o, dO, p);
     const unsigned tiles = (unsigned)((p.T + QT - 1) / QT);
-    const dim3 grid(tiles, (unsigned)p.H, (unsigned)p.B);
-    attn_bwd<true><<<grid, BWD_THREADS, BWD_SMEM, s>>>(mq, mk, mv, mdo, dv, dk, p);
-    attn_bwd<false><<<grid, BWD_THREADS, BWD_SMEM, s>>>(mq, mk, mv, mdo, dq, dq, p);
+    const dim3 grid(tiles, (unsigned)p.H, (unsigned)(2 * p.B));
+    attn_bwd<<<grid, BWD_THREADS, BWD_SMEM, s>>>(mq, mk, mv, mdo, dq, dk, dv, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
