@@ -379,22 +379,24 @@ class Executor:
         self.users = users
 
     def _shared_heavy(self, x):
+        """A value with several users is stored once (a cut) when recomputing
+        it in each consumer costs more than a store and a load: 4 or more
+        elementwise ops above the realized values and reductions it reads
+        (a reduction below is computed once either way: its result is
+        stored, or it runs as a stage of the one fused reduction call)."""
         if self.users.get(id(x), 0) < 2 or x.op == "CONST" or x._real is not None:
             return False
-        n, red = 0, False
+        n = 0
         stack, seen = [x], set()
         while stack and n < 4:
             y = stack.pop()
-            if id(y) in seen or y._real is not None:
+            if id(y) in seen or y._real is not None or y.op in REDUCE:
                 continue
             seen.add(id(y))
-            if y.op in REDUCE:
-                red = True
-                continue
             if y.op in ELEMENTWISE + ("MOVE",):
-                n += y.op != "MOVE"
+                n += y.op not in ("MOVE", "CONST")
                 stack.extend(y.src)
-        return red or n >= 4
+        return n >= 4
 
     def _status(self):
         if self.status is None or self.status.device != torch.device("cuda", torch.cuda.current_device()):
