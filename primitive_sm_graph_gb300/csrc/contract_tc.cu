@@ -313,9 +313,11 @@ int contract_tc_splits(int64_t M, int64_t N, int64_t K, int64_t batch, size_t* b
     const int64_t num_k = (K + BK - 1) / BK;
     const int64_t sms = num_sms();
     *bytes = 0;
-    // only when the output's tiles leave most SMs idle and K is long
-    if (tiles * 2 > sms || num_k < 8) return 1;
-    int64_t s = std::min<int64_t>(std::min<int64_t>(sms / tiles, num_k / 4), 16);
+    // only when the output's tiles leave most SMs idle and K is long enough
+    // (K >= 1024) that each split keeps at least 8 K blocks: the float32
+    // partials then cost little next to the products
+    if (tiles * 2 > sms || num_k < 16) return 1;
+    int64_t s = std::min<int64_t>(std::min<int64_t>(sms / tiles, num_k / 8), 16);
     if (s < 2) return 1;
     const int64_t per = (num_k + s - 1) / s;
     s = (num_k + per - 1) / per;  // no empty range

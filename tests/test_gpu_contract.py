@@ -270,7 +270,7 @@ def _split_case(A, M, N, K, a_layout, b_layout, out_dt, batch, seed):
 
 
 @pytest.mark.parametrize("M,N,K,a_layout,b_layout,out_dt,batch", [
-    (256, 512, 4096, "mk", "kn", "f32", None),      # 4 tiles, 16 splits of 4 K blocks
+    (256, 512, 4096, "mk", "kn", "f32", None),      # 4 tiles, 8 splits of 8 K blocks
     (200, 300, 3000, "km", "nk", "bf16", None),     # ragged tiles and a short last split
     (130, 70, 1000, "mk", "nk", "f32", None),
     (128, 256, 2048, "mk", "kn", "bf16", 3)])       # batched: 3 tiles
