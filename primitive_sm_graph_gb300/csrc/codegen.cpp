@@ -149,7 +149,7 @@ psg_status analyze_program(const psg_node* nodes, int n, const int* in_dtype, co
 }
 
 std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string& name,
-                     const std::string& prefix, int stash)
+                     const std::string& prefix, int stash, bool store_rounds)
 {
     const int n = I.n;
     // with a stashed node, liveness restarts from the result with that node
@@ -181,6 +181,10 @@ std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string
         const psg_node& x = nodes[i];
         const int dt = x.dtype;
         const bool isint = dtype_is_int(dt);
+        // the last node feeds only the store; a half-width store rounds to
+        // nearest-even itself, which gives the same bits as rounding here
+        const bool rounded_by_store = store_rounds && i == n - 1 && (dt == PSG_BF16 || dt == PSG_F16);
+        auto wrap = [&](int d, const std::string& ex) { return rounded_by_store ? ex : psg::wrap(d, ex); };
         std::string e;
         if (i == stash) {
             loop_part += fmt("            const %s x%d = %s;\n", ctype(dt), i, isint ? "c.stashi(v)" : "c.stashf(v)");

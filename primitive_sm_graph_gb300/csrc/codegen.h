@@ -32,7 +32,10 @@ psg_status analyze_program(const psg_node* nodes, int n, const int* in_dtype, co
 // C provides ldv<K>(arr), ld1<K>(), redf(s), redi(s).  With stash >= 0 the
 // value of node `stash` (non-uniform) is read per lane from c.stashf(v) /
 // c.stashi(v) instead of being computed, and whatever only fed it is dropped.
+// With store_rounds the result goes only to a store that rounds float32 to a
+// half width itself (round to nearest even), so a bfloat16/float16 last node
+// is left unrounded; the stored bits are the same.
 std::string gen_eval(const psg_node* nodes, const ProgInfo& info, const std::string& name,
-                     const std::string& prefix = "", int stash = -1);
+                     const std::string& prefix = "", int stash = -1, bool store_rounds = false);
 
 }  // namespace psg

@@ -107,7 +107,7 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
     spec += "constexpr int kOutDt = " + std::to_string(out_v->dtype) + ";\n";
     spec += "constexpr int kOutMode = " + std::to_string(out_mode) + ";\n";
     spec += std::string("constexpr bool kExact = ") + (sp.inner % PSG_VEC == 0 ? "true" : "false") + ";\n";
-    spec += gen_eval(prog, I, "Body");
+    spec += gen_eval(prog, I, "Body", "", -1, true);  // the result only goes to st_chunk
     P->spec = std::move(spec);
     return PSG_OK;
 }

@@ -28,7 +28,7 @@ __device__ __forceinline__ float h2f(u16 h)
     asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(h));
     return r;
 }
-__device__ __forceinline__ u16 f2h(float x)  // x already float16-exact
+__device__ __forceinline__ u16 f2h(float x)  // float32 -> float16 bits (round to nearest even)
 {
     u16 h;
     asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(x));
@@ -97,7 +97,11 @@ template <int DT>
 __device__ __forceinline__ void st_cell(void* p, i64 o, typename VT<DT>::T v)
 {
     if constexpr (DT == PSG_DT_F32) ((float*)p)[o] = v;
-    else if constexpr (DT == PSG_DT_BF16) ((u16*)p)[o] = (u16)(__float_as_uint(v) >> 16);
+    else if constexpr (DT == PSG_DT_BF16) {
+        u16 h;
+        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(v));
+        ((u16*)p)[o] = h;
+    }
     else if constexpr (DT == PSG_DT_F16) ((u16*)p)[o] = f2h(v);
     else if constexpr (DT == PSG_DT_I32) ((int*)p)[o] = v;
     else if constexpr (DT == PSG_DT_I16) ((short*)p)[o] = (short)v;
@@ -217,11 +221,12 @@ __device__ __forceinline__ void st_chunk(const PsgOperand& op, i64 roff, i64 col
                 u32 w[4];
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    u32 lo, hi;
-                    if constexpr (DT == PSG_DT_BF16) { lo = __float_as_uint(y[2 * v]) >> 16; hi = __float_as_uint(y[2 * v + 1]) >> 16; }
-                    else if constexpr (DT == PSG_DT_F16) { lo = f2h(y[2 * v]); hi = f2h(y[2 * v + 1]); }
-                    else { lo = (u32)y[2 * v] & 0xffffu; hi = (u32)y[2 * v + 1] & 0xffffu; }
-                    w[v] = lo | (hi << 16);
+                    // half widths: one round-to-nearest-even conversion per pair
+                    if constexpr (DT == PSG_DT_BF16)
+                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[v]) : "f"(y[2 * v + 1]), "f"(y[2 * v]));
+                    else if constexpr (DT == PSG_DT_F16)
+                        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w[v]) : "f"(y[2 * v + 1]), "f"(y[2 * v]));
+                    else w[v] = ((u32)y[2 * v] & 0xffffu) | ((u32)y[2 * v + 1] << 16);
                 }
                 *(uint4*)q = make_uint4(w[0], w[1], w[2], w[3]);
                 return;

@@ -178,23 +178,23 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     // each issues several 16- or 32-byte loads at once and short rows fold
     // inside one warp (shuffles only); the row (and a stash) is cached in
     // registers when it fits in RED_CACHE_WORDS words per thread.
-    constexpr int RED_CHUNKS = 4, RED_CACHE_WORDS = 64, RED_MAX_TEAM_LOG2 = 8;
+    constexpr int RED_CHUNKS = 4, RED_CHUNKS_WIDE = 8, RED_CACHE_WORDS = 64, RED_MAX_TEAM_LOG2 = 8;
     int tl = 0;
     while ((int64_t)RED_CHUNKS << tl < sp.chunks && tl < RED_MAX_TEAM_LOG2) ++tl;
-    const int T = 1 << tl;
-    const int64_t ch_per = (sp.chunks + T - 1) / T > 0 ? (sp.chunks + T - 1) / T : 1;
     // staged mode: when every input that changes from row to row is
     // contiguous, 16-byte aligned at every row start and at least
     // RED_STAGE_MIN_BYTES a row, the rows come through a shared-memory ring of
     // kNS slots per team filled by bulk copies (kNS - 1 rows in flight while
     // the team computes); the stages and the epilogue read them from there.
     constexpr int RED_STAGED_MAX_CHUNKS = 16, RED_STAGE_MIN_BYTES = 512;
-    constexpr int64_t RED_SMEM_PREF = 110 * 1024, RED_SMEM_MAX = 200 * 1024;
-    const int teams = RED_THREADS >> tl;
+    // the ring is kept near RED_SMEM_PREF a block so that three blocks fit an
+    // SM: more teams in flight beat a deeper ring (RMSNorm: 26.2 us with two
+    // blocks of 3-slot rings, 25.3 us with three blocks of 2-slot rings)
+    constexpr int64_t RED_SMEM_PREF = 72 * 1024, RED_SMEM_MAX = 200 * 1024;
     int staged_in[PSG_MAX_INPUTS] = {0}, seg_off[PSG_MAX_INPUTS] = {0}, row_bytes[PSG_MAX_INPUTS] = {0},
         in_size[PSG_MAX_INPUTS] = {0};
     int64_t stage_bytes = 0, tx_bytes = 0;
-    bool staged = ch_per <= RED_STAGED_MAX_CHUNKS && words > 0 && !columnar;
+    bool staged = words > 0 && !columnar;
     for (int k = 0; k < n_in; ++k) {
         in_size[k] = dtype_size(dts[k]);
         if (!cache_in[k]) continue;
@@ -212,6 +212,22 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
         tx_bytes += sp.inner * es;
     }
     if (tx_bytes < RED_STAGE_MIN_BYTES) staged = false;
+    // a staged row longer than a warp's RED_CHUNKS chunks gives each thread
+    // RED_CHUNKS_WIDE chunks (it reads them from shared memory, so registers
+    // do not grow), and the per-row costs (the fold across warps, the row's
+    // uniform values) are shared by more cells (measured: RMSNorm over 4096
+    // bf16 cells a row, 28.7 us with 128-thread teams of 4 chunks, 25.3 us
+    // with 64-thread teams of 8)
+    if (staged && tl > 5) {
+        int tw = 5;
+        while ((int64_t)RED_CHUNKS_WIDE << tw < sp.chunks && tw < RED_MAX_TEAM_LOG2) ++tw;
+        const int64_t tms = RED_THREADS >> tw;  // its smallest ring must fit, else keep tl
+        if (((tms * 4 * 8 + 127) / 128 * 128) + tms * 2 * stage_bytes <= RED_SMEM_MAX) tl = tw;
+    }
+    const int T = 1 << tl;
+    const int64_t ch_per = (sp.chunks + T - 1) / T > 0 ? (sp.chunks + T - 1) / T : 1;
+    if (ch_per > RED_STAGED_MAX_CHUNKS) staged = false;
+    const int teams = RED_THREADS >> tl;
     int ns = 4;
     const int64_t bar_bytes = ((int64_t)teams * 4 * 8 + 127) / 128 * 128;
     while (ns > 2 && bar_bytes + teams * ns * stage_bytes > RED_SMEM_PREF) --ns;
@@ -255,7 +271,7 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
             cluster *= 2;
     }
     P->cluster = cluster;
-    bodies += gen_eval(epi, E, "Epi", "", stash_node);
+    bodies += gen_eval(epi, E, "Epi", "", stash_node, true);  // the result only goes to a store
     P->block = block;
     P->p.rows = sp.rows;
     P->p.inner = sp.inner;
