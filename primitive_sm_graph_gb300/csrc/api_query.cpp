@@ -63,9 +63,10 @@ extern "C" psg_status psg_query_launch(int call, const psg_view* v, int* grid, i
     }
     case PSG_CALL_CONTRACT_BF16: {
         if (v->ndim < 2) return PSG_E_INVALID_ARG;
-        int64_t tiles = ((v->shape[v->ndim - 2] + 127) / 128) * ((v->shape[v->ndim - 1] + 255) / 256);
+        const int64_t M = v->shape[v->ndim - 2];
+        int64_t tiles = ((M + 127) / 128) * ((v->shape[v->ndim - 1] + 255) / 256);
         for (int d = 0; d < v->ndim - 2; ++d) tiles *= v->shape[d];
-        query_contract_tc(tiles, grid, block, smem, regs);
+        query_contract_tc(M, tiles, grid, block, smem, regs);
         return PSG_OK;
     }
     case PSG_CALL_CONTRACT_F32_TENSOR: {

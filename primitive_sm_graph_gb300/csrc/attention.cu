@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
                                                            const __grid_constant__ CUtensorMap tv,
                                                            const __grid_constant__ AttnParams p)
 {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* sq = smem;                       // [128 q][64 d]
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(256) attn_delta(const __grid_constant__ AttnTe
                                                   const __grid_constant__ AttnTensor dO,
                                                   const __grid_constant__ AttnParams p)
 {
+    pdl_enter();
     const int64_t rows = (int64_t)p.B * p.T * p.H;
     const int sub = threadIdx.x & 7, grp = (threadIdx.x & 31) >> 3;
     // warp-uniform loop over groups of 4 rows (the shuffles need every lane)
@@ -546,6 +548,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 2) attn_bwd(const __grid_constant
                                                            const __grid_constant__ AttnTensor dv,
                                                            const __grid_constant__ AttnParams p)
 {
+    pdl_enter();
     if ((int)blockIdx.z < p.B) attn_bwd_pass<true>(tq, tk, tv, tdo, dv, dk, p, (int)blockIdx.z);
     else attn_bwd_pass<false>(tq, tk, tv, tdo, dq, dq, p, (int)blockIdx.z - p.B);
 }
@@ -583,7 +586,7 @@ psg_status launch_attention_fwd(const AttnTensor& q, const AttnTensor& k, const 
     });
     if (err != cudaSuccess) return PSG_E_CUDA;
     const dim3 grid((unsigned)((p.T + QT - 1) / QT), (unsigned)p.H, (unsigned)p.B);
-    attn_fwd<<<grid, FWD_THREADS, FWD_SMEM, (cudaStream_t)stream>>>(mq, mk, mv, p);
+    launch(attn_fwd, grid, FWD_THREADS, FWD_SMEM, (cudaStream_t)stream, mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
@@ -605,10 +608,10 @@ psg_status launch_attention_bwd(const AttnTensor& q, const AttnTensor& k, const 
     if (err != cudaSuccess) return PSG_E_CUDA;
     const int64_t rows = (int64_t)p.B * p.T * p.H;
     const int dgrid = (int)std::min<int64_t>((rows + 31) / 32, (int64_t)num_sms() * 16);  // 32 rows a block
-    attn_delta<<<dgrid, 256, 0, s>>>(o, dO, p);
+    launch(attn_delta, dgrid, 256, 0, s, o, dO, p);
     const unsigned tiles = (unsigned)((p.T + QT - 1) / QT);
     const dim3 grid(tiles, (unsigned)p.H, (unsigned)(2 * p.B));
-    attn_bwd<<<grid, BWD_THREADS, BWD_SMEM, s>>>(mq, mk, mv, mdo, dq, dk, dv, p);
+    launch(attn_bwd, grid, BWD_THREADS, BWD_SMEM, s, mq, mk, mv, mdo, dq, dk, dv, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 

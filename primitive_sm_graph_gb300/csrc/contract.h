@@ -43,7 +43,9 @@ psg_status launch_contract_tc(const TcOperands& o, void* stream);
 // split-K plan of the bf16 / f16 kernel: splits (1 = none) and the
 // workspace bytes they need, for an output of tiles that leaves SMs idle
 int contract_tc_splits(int64_t M, int64_t N, int64_t K, int64_t batch, size_t* bytes);
-void query_contract_tc(int64_t tiles, int* grid, int* block, int* smem, int* regs);
+// launch shape for an output of M rows in `tiles` 128 x 256 tiles: the CTA-pair
+// kernel (two CTAs a 256 x 256 tile) when M > 128, else the single-CTA one
+void query_contract_tc(int64_t M, int64_t tiles, int* grid, int* block, int* smem, int* regs);
 // float32 operands, 3xTF32 on the tensor cores (same operand rules as the bf16 path)
 psg_status launch_contract_tf32(const TcOperands& o, void* stream);
 void query_contract_tf32(int64_t tiles, int* grid, int* block, int* smem, int* regs);

@@ -31,6 +31,7 @@ __device__ __forceinline__ float ld(const void* p, int64_t o)
 template <int DT>
 __global__ void __launch_bounds__(NT) simt_gemm(const __grid_constant__ SimtParams p)
 {
+    pdl_enter();
     __shared__ float As[TK][TM + 4];
     __shared__ float Bs[TK][TN + 4];
     const int t = threadIdx.x;
@@ -109,9 +110,9 @@ psg_status launch_contract_simt(const SimtParams& p, void* stream)
     if (p.M == 0 || p.N == 0 || p.batch == 0) return PSG_OK;
     if ((p.N + TN - 1) / TN > 2147483647 || (p.M + TM - 1) / TM > 65535) return PSG_E_UNSUPPORTED_LAYOUT;
     cudaStream_t s = (cudaStream_t)stream;
-    if (p.ab_dtype == PSG_F32) simt_gemm<PSG_F32><<<grid_of(p), NT, 0, s>>>(p);
-    else if (p.ab_dtype == PSG_F16) simt_gemm<PSG_F16><<<grid_of(p), NT, 0, s>>>(p);
-    else simt_gemm<PSG_BF16><<<grid_of(p), NT, 0, s>>>(p);
+    if (p.ab_dtype == PSG_F32) launch(simt_gemm<PSG_F32>, grid_of(p), NT, 0, s, p);
+    else if (p.ab_dtype == PSG_F16) launch(simt_gemm<PSG_F16>, grid_of(p), NT, 0, s, p);
+    else launch(simt_gemm<PSG_BF16>, grid_of(p), NT, 0, s, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 

@@ -8,15 +8,16 @@
 // tcgen05.mma.cta_group::1.kind::f16 (bf16 inputs, float32 accumulate in
 // TMEM), fed by TMA.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+// Warp roles (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0  TMA producer: one elected lane streams 64-deep K slices of A and
 //           B into a 4-stage shared-memory ring (128B-swizzled tiles);
 //   warp 1  MMA issuer: allocates all 512 TMEM columns (two 128x256 f32
 //           accumulators), one lane issues 4 MMAs (K = 16 each) per stage and
 //           commits the stage back to the producer;
-//   warps 2-5 epilogue: each warp reads its 32 TMEM lanes (rows) with
-//           tcgen05.ld, rounds to the output dtype once and stores, while the
-//           MMA warp fills the other accumulator.
+//   warps 2-9 epilogue: two warps per 32 TMEM lanes (rows), each taking
+//           128 of the tile's 256 columns; a warp reads 64 columns with two
+//           tcgen05.ld before one wait, rounds to the output dtype once and
+//           stores, while the MMA warp fills the other accumulator.
 // Every wait on an mbarrier gives up after about a second: the CTA then sets
 // PSG_E_TIMEOUT in the caller's status word, drains its own copies and MMAs,
 // frees TMEM and returns.  No TMA multicast is used: each CTA loads its own
@@ -28,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "contract.h"
@@ -45,7 +47,8 @@ constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
 constexpr int TMEM_COLS = 512;                   // two 128 x 256 f32 accumulators
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;                     // warps 2 .. 9
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 // (8 KB of slack after the barriers keeps every tensor-core operand read inside
 // the allocation even for the widest descriptor stride)
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + 8192;
@@ -63,10 +66,64 @@ __device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t ad, uint64_t b
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
         ::"r"(dtmem), "l"(ad), "l"(bd), "r"(idesc), "r"(accum));
 }
+// One TMEM load's 32 columns of row m (n0 = the first column) into C, or, under
+// split-K, into this K range's float32 partials; rows and columns outside C
+// are skipped.
+__device__ __forceinline__ void epi_store32(const TcParams& p, const uint32_t (&r)[32], int m, int64_t crow, int n0,
+                                            int sp, int b)
+{
+    if (m >= p.M) return;
+    if (p.splits > 1) {
+        // split-K: this K range's float32 total, summed later in split order
+        float* dst = p.ws + (((int64_t)sp * p.batch + b) * p.M + m) * p.N + n0;
+        if (n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                ((uint4*)dst)[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        } else {
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < p.N) dst[j] = __uint_as_float(r[j]);
+        }
+    } else if (p.c_dtype == PSG_BF16) {
+        __nv_bfloat16* dst = (__nv_bfloat16*)p.C + crow + n0;
+        if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                w[j] = *(const uint32_t*)&hv;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                ((uint4*)dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        } else {
+            __nv_bfloat16* C = (__nv_bfloat16*)p.C;
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < p.N) C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        }
+    } else if (p.c_dtype == PSG_F16) {
+        __half* C = (__half*)p.C;
+        for (int j = 0; j < 32; ++j)
+            if (n0 + j < p.N) C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2half_rn(__uint_as_float(r[j]));
+    } else {
+        float* dst = (float*)p.C + crow + n0;
+        if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                ((uint4*)dst)[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        } else {
+            float* C = (float*)p.C;
+            for (int j = 0; j < 32; ++j)
+                if (n0 + j < p.N) C[crow + (int64_t)(n0 + j) * p.c_cs] = __uint_as_float(r[j]);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CUtensorMap tmap_a,
                                                       const __grid_constant__ CUtensorMap tmap_b,
                                                       const __grid_constant__ TcParams p)
 {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     // swizzled tiles need 1024-byte alignment of their shared-memory address
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -83,7 +140,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
         }
         for (int a = 0; a < 2; ++a) {
             bar_init(&bars->tfull[a], 1);
-            bar_init(&bars->tempty[a], 4);
+            bar_init(&bars->tempty[a], EPI_WARPS);
         }
         bar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -194,7 +251,10 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
         }
     } else {
         // ---------------- epilogue: TMEM -> registers -> global ----------------
-        const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
+        // a warp may only read TMEM lanes 32 * (warp % 4) .. + 31; warps w and
+        // w + 4 share those rows and split the columns
+        const int q = warp & 3;
+        const int c_lo = ((warp - 2) >> 2) * (BN / 2);
         uint32_t aph[2] = {0u, 0u};
         int local = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
@@ -207,58 +267,18 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
             tile_coords(p.num_m, p.num_n, t, b, mb, nb);
             const int m = mb * BM + q * 32 + lane;
             const int64_t crow = p.c_offset + (int64_t)b * p.c_bs + (int64_t)m * p.c_rs;
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
+            for (int c2 = c_lo; c2 < c_lo + BN / 2; c2 += 64) {
+                uint32_t rr[2][32];
                 __syncwarp();  // tcgen05.ld is warp-collective: reach it converged
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), r);
-                const int n0 = nb * BN + c;
-                if (m < p.M && p.splits > 1) {
-                    // split-K: this K range's float32 total, summed later in split order
-                    float* dst = p.ws + (((int64_t)sp * p.batch + b) * p.M + m) * p.N + n0;
-                    if (n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c2);
+                tmem_ld32_nowait(ta, rr[0]);
+                tmem_ld32_nowait(ta + 32u, rr[1]);
+                tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            ((uint4*)dst)[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                    } else {
-                        for (int j = 0; j < 32; ++j)
-                            if (n0 + j < p.N) dst[j] = __uint_as_float(r[j]);
-                    }
-                } else if (m < p.M) {
-                    if (p.c_dtype == PSG_BF16) {
-                        __nv_bfloat16* dst = (__nv_bfloat16*)p.C + crow + n0;
-                        if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
-                            uint32_t w[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]),
-                                                                                __uint_as_float(r[2 * j + 1]));
-                                w[j] = *(const uint32_t*)&h;
-                            }
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                ((uint4*)dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                        } else {
-                            __nv_bfloat16* C = (__nv_bfloat16*)p.C;
-                            for (int j = 0; j < 32; ++j)
-                                if (n0 + j < p.N)
-                                    C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2bfloat16_rn(__uint_as_float(r[j]));
-                        }
-                    } else if (p.c_dtype == PSG_F16) {
-                        __half* C = (__half*)p.C;
-                        for (int j = 0; j < 32; ++j)
-                            if (n0 + j < p.N) C[crow + (int64_t)(n0 + j) * p.c_cs] = __float2half_rn(__uint_as_float(r[j]));
-                    } else {
-                        float* dst = (float*)p.C + crow + n0;
-                        if (p.c_cs == 1 && n0 + 32 <= p.N && ((uintptr_t)dst & 15) == 0) {
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                ((uint4*)dst)[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                        } else {
-                            float* C = (float*)p.C;
-                            for (int j = 0; j < 32; ++j)
-                                if (n0 + j < p.N) C[crow + (int64_t)(n0 + j) * p.c_cs] = __uint_as_float(r[j]);
-                        }
-                    }
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t (&r)[32] = rr[h];
+                    const int c = c2 + 32 * h;
+                    epi_store32(p, r, m, crow, nb * BN + c, sp, b);
                 }
             }
             tc_fence_before();
@@ -272,10 +292,213 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
 }
 
+// ---- CTA-pair variant: one 256 x 256 tile over two SMs ---------------------
+//
+// A cluster of two CTAs computes a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256): each CTA holds 128 rows of the
+// A slice and 128 columns of the B slice in its own shared memory, and its
+// own 128 rows of the float32 accumulator in its TMEM.  Per 64-deep K slice a
+// CTA loads 32 KB where the single-CTA tile loads 48 KB for the same 128 x 256
+// outputs, so operand traffic from L2 per product drops by a third and the
+// ring holds six stages.  The leader (rank 0) issues every MMA; both CTAs'
+// copies count on the leader's full barrier (cta_group::2 bulk tensor
+// copies), the MMA commits arrive on both CTAs' barriers (multicast), and
+// both CTAs' epilogue warps free an accumulator on the leader's barrier.
+constexpr int P_BM = 256;                              // rows of a pair tile (128 a CTA)
+constexpr int P_HN = BN / 2;                           // columns of B a CTA holds
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;                // 16 KB
+constexpr int P_B_BYTES = P_HN * BK * 2;               // 16 KB
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;   // 32 KB
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 256 + 8192;
+
+struct PairBars {
+    uint64_t full[P_STAGES], empty[P_STAGES], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                              uint32_t accum)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(dtmem), "l"(ad), "l"(bd), "r"(idesc), "r"(accum));
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    tc_gemm2(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+             const __grid_constant__ TcParams p)
+{
+    pdl_enter();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    PairBars* bars = (PairBars*)(smem + P_STAGES * P_STAGE_BYTES);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int cid = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
+    const int total = p.num_m * p.num_n * p.batch;  // num_m counts 256-row blocks here
+    const int units = total * p.splits;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            bar_init(&bars->full[s], 1);
+            bar_init(&bars->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            bar_init(&bars->tfull[a], 1);
+            bar_init(&bars->tempty[a], 2 * EPI_WARPS);
+        }
+        bar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&bars->tmem_base)), "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    // both CTAs' barriers exist and both TMEM allocations are done before any
+    // copy signals the leader or any MMA writes the peer
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs) ----------------
+        if (lane == 0) {
+            const uint32_t full0 = smem_in_rank(&bars->full[0], 0);  // the leader's full barriers
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t armed = 0, armed_ph = 0;
+            bool ok = true;
+            for (int u = cid; u < units && ok; u += ncl) {
+                const int t = u / p.splits, sp = u - t * p.splits;
+                const int kb0 = sp * p.kb_per, kb1 = min(p.num_k, kb0 + p.kb_per);
+                int b, mb, nb;
+                tile_coords(p.num_m, p.num_n, t, b, mb, nb);
+                const int m0 = mb * P_BM + (int)rank * 128, n0 = nb * BN + (int)rank * P_HN;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!bar_wait(&bars->empty[stage], ph ^ 1u, &bars->abort, p.status)) { ok = false; break; }
+                    uint8_t* sa = smem + stage * P_STAGE_BYTES;
+                    uint8_t* sb = sa + P_A_BYTES;
+                    const uint32_t fb = full0 + (uint32_t)(stage * 8);
+                    if (leader) bar_expect_tx(&bars->full[stage], 2 * P_STAGE_BYTES);  // both CTAs' bytes
+                    const int k0 = kb * BK;
+                    if (p.a_kmajor) {
+                        tma_load_3d_pair(sa, &tmap_a, fb, k0, m0, b);
+                    } else {
+                        tma_load_3d_pair(sa, &tmap_a, fb, m0, k0, b);
+                        tma_load_3d_pair(sa + 8192, &tmap_a, fb, m0 + 64, k0, b);
+                    }
+                    if (p.b_kmajor) {
+                        tma_load_3d_pair(sb, &tmap_b, fb, k0, n0, b);
+                    } else {
+                        tma_load_3d_pair(sb, &tmap_b, fb, n0, k0, b);
+                        tma_load_3d_pair(sb + 8192, &tmap_b, fb, n0 + 64, k0, b);
+                    }
+                    armed |= 1u << stage;
+                    armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
+                    if (++stage == P_STAGES) { stage = 0; ph ^= 1u; }
+                }
+            }
+            // the leader's full barriers count both CTAs' copies: once each
+            // armed stage completed, every copy of the pair has landed
+            if (leader)
+                for (int s = 0; s < P_STAGES; ++s)
+                    if (armed & (1u << s)) bar_wait_drain(&bars->full[s], (armed_ph >> s) & 1u);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (leader only) ----------------
+        if (leader && lane == 0) {
+            // f32 accumulate, A and B both bf16 (1) or both f16 (0), M = 256, N = 256
+            const uint32_t ab = p.ab_dtype == PSG_F16 ? 0u : 1u;
+            const uint32_t idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((p.a_kmajor ? 0u : 1u) << 15) |
+                                   ((p.b_kmajor ? 0u : 1u) << 16) | ((uint32_t)(BN >> 3) << 17) |
+                                   ((uint32_t)(P_BM >> 4) << 24);
+            const uint32_t a_lbo = p.a_kmajor ? 16u : 8192u, b_lbo = p.b_kmajor ? 16u : 8192u;
+            const uint32_t a_step = p.a_kmajor ? 2u : 128u, b_step = p.b_kmajor ? 2u : 128u;
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t aph[2] = {0u, 0u};
+            bool ok = true;
+            int local = 0;
+            for (int u = cid; u < units && ok; u += ncl, ++local) {
+                const int kb0 = (u % p.splits) * p.kb_per, kb1 = min(p.num_k, kb0 + p.kb_per);
+                const int acc = local & 1;
+                if (!bar_wait(&bars->tempty[acc], aph[acc] ^ 1u, &bars->abort, p.status)) break;
+                tc_fence_after();
+                const uint32_t dtm = tmem + (uint32_t)(acc * BN);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!bar_wait(&bars->full[stage], ph, &bars->abort, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * P_STAGE_BYTES);
+                    const uint32_t sb = sa + P_A_BYTES;
+                    const uint64_t ad = sdesc(sa, a_lbo, 1024u), bd = sdesc(sb, b_lbo, 1024u);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16_pair(dtm, ad + (uint64_t)(k * a_step), bd + (uint64_t)(k * b_step), idesc,
+                                      (kb != kb0 || k != 0) ? 1u : 0u);
+                    mma_commit_pair(&bars->empty[stage]);  // frees the stage in both CTAs
+                    if (++stage == P_STAGES) { stage = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit_pair(&bars->tfull[acc]);  // both halves of the accumulator are ready
+                aph[acc] ^= 1u;
+            }
+            mma_commit_pair_local(&bars->drain);
+            bar_wait_drain(&bars->drain, 0u);
+        }
+    } else {
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
+        const int q = warp & 3;
+        const int c_lo = ((warp - 2) >> 2) * (BN / 2);
+        const uint32_t tempty0 = smem_in_rank(&bars->tempty[0], 0);
+        uint32_t aph[2] = {0u, 0u};
+        int local = 0;
+        for (int u = cid; u < units; u += ncl, ++local) {
+            const int t = u / p.splits, sp = u - t * p.splits;
+            const int acc = local & 1;
+            if (!bar_wait(&bars->tfull[acc], aph[acc], &bars->abort, p.status)) break;
+            aph[acc] ^= 1u;
+            tc_fence_after();
+            int b, mb, nb;
+            tile_coords(p.num_m, p.num_n, t, b, mb, nb);
+            const int m = mb * P_BM + (int)rank * 128 + q * 32 + lane;
+            const int64_t crow = p.c_offset + (int64_t)b * p.c_bs + (int64_t)m * p.c_rs;
+            for (int c2 = c_lo; c2 < c_lo + BN / 2; c2 += 64) {
+                uint32_t rr[2][32];
+                __syncwarp();
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c2);
+                tmem_ld32_nowait(ta, rr[0]);
+                tmem_ld32_nowait(ta + 32u, rr[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) epi_store32(p, rr[h], m, crow, nb * BN + c2 + 32 * h, sp, b);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
+        }
+    }
+    // the leader's MMAs read this CTA's shared memory and write its TMEM: no
+    // CTA frees either before both are done
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+}
+
 // C = sum over the splits, in split order, of the float32 partials, rounded
 // once into C's dtype
 __global__ void __launch_bounds__(256) splitk_reduce(const __grid_constant__ TcParams p)
 {
+    pdl_enter();
     const int64_t cells = (int64_t)p.batch * p.M * p.N;
     const int64_t stride = cells;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < cells; e += (int64_t)gridDim.x * blockDim.x) {
@@ -325,6 +548,76 @@ int contract_tc_splits(int64_t M, int64_t N, int64_t K, int64_t batch, size_t* b
     return (int)s;
 }
 
+namespace {
+
+// The CTA-pair kernel takes outputs of more than one 128-row block over
+// K >= 1024 (measured on GB300: 8192 x 8192 x 2048 in 170 us against 194 us
+// single-CTA; at K = 512 the two are within a few percent, the single-CTA one
+// ahead).  PSG_GEMM_KERNEL=single or =pair in the environment forces one of
+// them (pair still needs M > 128).
+bool use_pair(const TcParams& p)
+{
+    if (p.M <= BM) return false;
+    const char* f = std::getenv("PSG_GEMM_KERNEL");
+    if (f && f[0] == 's') return false;
+    if (f && f[0] == 'p') return true;
+    return p.K >= 1024;
+}
+
+// clusters of two tc_gemm2 CTAs that fit on the device at once (per device)
+int pair_clusters()
+{
+    constexpr int MAX_DEV = 64;
+    static std::mutex mu;
+    static int cached[MAX_DEV];
+    const int d = current_device();
+    std::lock_guard<std::mutex> g(mu);
+    if (cached[d] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * num_sms());
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = P_SMEM_BYTES;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, (const void*)tc_gemm2, &cfg) != cudaSuccess || n < 1) n = num_sms() / 2;
+        cached[d] = n;
+    }
+    return cached[d];
+}
+
+psg_status launch_pair(const TcOperands& o, TcParams p, int64_t a_bs, int64_t b_bs, void* stream)
+{
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute((const void*)tc_gemm2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        P_SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return PSG_E_CUDA;
+    CUtensorMap ma, mb;
+    const bool f16 = p.ab_dtype == PSG_F16;
+    // a CTA holds 128 rows of A and 128 columns of B per 64-deep K slice
+    bool ok = p.a_kmajor ? make_map(&ma, o.A, p.K, p.M, p.batch, o.a_ms, a_bs, 64, 128, f16)
+                         : make_map(&ma, o.A, p.M, p.K, p.batch, o.a_ks, a_bs, 64, 64, f16);
+    ok = ok && (p.b_kmajor ? make_map(&mb, o.B, p.K, p.N, p.batch, o.b_ns, b_bs, 64, P_HN, f16)
+                           : make_map(&mb, o.B, p.N, p.K, p.batch, o.b_ks, b_bs, 64, 64, f16));
+    if (!ok) return PSG_E_CUDA;
+    p.num_m = (p.M + P_BM - 1) / P_BM;
+    p.num_n = (p.N + BN - 1) / BN;
+    p.num_k = (p.K + BK - 1) / BK;
+    p.kb_per = (p.num_k + p.splits - 1) / p.splits;
+    const int64_t units = (int64_t)p.num_m * p.num_n * p.batch * p.splits;
+    const int clusters = (int)std::min<int64_t>(units, pair_clusters());
+    launch(tc_gemm2, 2 * clusters, THREADS, P_SMEM_BYTES, (cudaStream_t)stream, ma, mb, p);
+    if (p.splits > 1) {
+        const int64_t cells = (int64_t)p.batch * p.M * p.N;
+        const int rgrid = (int)std::min<int64_t>((cells + 255) / 256, (int64_t)num_sms() * 8);
+        launch(splitk_reduce, rgrid, 256, 0, (cudaStream_t)stream, p);
+    }
+    return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
+}
+
+}  // namespace
+
 psg_status launch_contract_tc(const TcOperands& o, void* stream)
 {
     TcParams p = o.p;
@@ -343,6 +636,7 @@ psg_status launch_contract_tc(const TcOperands& o, void* stream)
     // batch strides of a single batch are never used; keep them a legal multiple of 16 bytes
     const int64_t a_bs = p.batch > 1 ? o.a_bs : (p.a_kmajor ? o.a_ms * p.M : o.a_ks * p.K);
     const int64_t b_bs = p.batch > 1 ? o.b_bs : (p.b_kmajor ? o.b_ns * p.N : o.b_ks * p.K);
+    if (use_pair(p)) return launch_pair(o, p, a_bs, b_bs, stream);
     const bool f16 = p.ab_dtype == PSG_F16;
     bool ok = p.a_kmajor ? make_map(&ma, o.A, p.K, p.M, p.batch, o.a_ms, a_bs, 64, 128, f16)
                          : make_map(&ma, o.A, p.M, p.K, p.batch, o.a_ks, a_bs, 64, 64, f16);
@@ -361,17 +655,27 @@ psg_status launch_contract_tc(const TcOperands& o, void* stream)
     if (attr_err != cudaSuccess) return PSG_E_CUDA;
     const int64_t units = (int64_t)p.num_m * p.num_n * p.batch * p.splits;
     const int grid = (int)std::min<int64_t>(units, num_sms());
-    tc_gemm<<<grid, THREADS, SMEM_BYTES, (cudaStream_t)stream>>>(ma, mb, p);
+    launch(tc_gemm, grid, THREADS, SMEM_BYTES, (cudaStream_t)stream, ma, mb, p);
     if (p.splits > 1) {
         const int64_t cells = (int64_t)p.batch * p.M * p.N;
         const int rgrid = (int)std::min<int64_t>((cells + 255) / 256, (int64_t)num_sms() * 8);
-        splitk_reduce<<<rgrid, 256, 0, (cudaStream_t)stream>>>(p);
+        launch(splitk_reduce, rgrid, 256, 0, (cudaStream_t)stream, p);
     }
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
-void query_contract_tc(int64_t tiles, int* grid, int* block, int* smem, int* regs)
+void query_contract_tc(int64_t M, int64_t tiles, int* grid, int* block, int* smem, int* regs)
 {
+    TcParams p = {};
+    p.M = (int)std::min<int64_t>(M, 1 << 30);
+    p.K = 1 << 30;  // the query has no K: report the kernel a long K takes
+    if (use_pair(p)) {
+        *grid = 2 * (int)std::min<int64_t>((tiles + 1) / 2, pair_clusters());
+        *block = THREADS;
+        *smem = P_SMEM_BYTES;
+        *regs = kernel_regs((const void*)tc_gemm2);
+        return;
+    }
     *grid = (int)std::min<int64_t>(tiles, num_sms());
     *block = THREADS;
     *smem = SMEM_BYTES;

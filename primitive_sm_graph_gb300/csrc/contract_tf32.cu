@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm_tf32x3(const __grid_consta
                                                              const __grid_constant__ CUtensorMap tmap_b,
                                                              const __grid_constant__ TcParams p)
 {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     // swizzled tiles need 1024-byte alignment of their shared-memory address
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -347,7 +348,7 @@ psg_status launch_contract_tf32(const TcOperands& o, void* stream)
     if (attr_err != cudaSuccess) return PSG_E_CUDA;
     const int64_t tiles = (int64_t)p.num_m * p.num_n * p.batch;
     const int grid = (int)std::min<int64_t>(tiles, num_sms());
-    tc_gemm_tf32x3<<<grid, THREADS, SMEM_BYTES, (cudaStream_t)stream>>>(ma, mb, p);
+    launch(tc_gemm_tf32x3, grid, THREADS, SMEM_BYTES, (cudaStream_t)stream, ma, mb, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 

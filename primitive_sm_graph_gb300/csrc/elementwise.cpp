@@ -131,9 +131,9 @@ psg_status launch_elementwise(const EwPlan& P, void* stream)
     int grid;
     grid_for(P, k, &grid);
     void* args[] = {(void*)&P.p};
-    if (cudaLaunchKernel((const void*)k, dim3(grid), dim3(EW_THREADS), args, 0, (cudaStream_t)stream) !=
-        cudaSuccess)
-        return PSG_E_CUDA;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config(dim3(grid), dim3(EW_THREADS), 0, (cudaStream_t)stream, attr);
+    if (cudaLaunchKernelExC(&cfg, (const void*)k, args) != cudaSuccess) return PSG_E_CUDA;
     return PSG_OK;
 }
 

@@ -56,6 +56,7 @@ __device__ __forceinline__ void zero_cell(char* d)
 template <int ES>
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherLaunch L)
 {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * 8;
     for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < L.n; r += warps) {
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
 __global__ void make_keys(const int32_t* __restrict__ idx, int64_t n, int64_t V, int64_t npow2,
                           unsigned long long* __restrict__ keys, int32_t* status)
 {
+    pdl_enter();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < npow2;
          i += (int64_t)gridDim.x * blockDim.x) {
         unsigned long long k;
@@ -112,6 +114,7 @@ __device__ __forceinline__ void cmp_swap(unsigned long long& a, unsigned long lo
 // whole local sort; k > LOCAL_SORT: the tail of a global merge stage)
 __global__ void __launch_bounds__(1024) bitonic_local(unsigned long long* keys, int64_t npow2, int64_t kfrom)
 {
+    pdl_enter();
     __shared__ unsigned long long s[LOCAL_SORT];
     const int64_t tile = (int64_t)blockIdx.x * LOCAL_SORT;
     const int t = threadIdx.x;
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(1024) bitonic_local(unsigned long long* keys, 
 // one global step (k, j) with j >= LOCAL_SORT: one thread per pair
 __global__ void bitonic_global(unsigned long long* keys, int64_t npow2, int64_t k, int64_t j)
 {
+    pdl_enter();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < npow2 / 2;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t a = (i / j) * (2 * j) + (i % j);
@@ -254,6 +258,7 @@ __global__ void __launch_bounds__(256) scatter_accumulate(const __grid_constant_
                                                           const unsigned long long* __restrict__ keys,
                                                           int64_t nseg)
 {
+    pdl_enter();
     typedef SV<DT> S;
     typedef typename S::A A;
     constexpr int VPL = VEC ? 16 / S::ES : 1;
@@ -399,6 +404,7 @@ constexpr int PLAN_E = kScatterPlanMaxN / PLAN_THREADS;  // positions a thread o
 __global__ void __launch_bounds__(PLAN_THREADS) scatter_plan(const int32_t* __restrict__ idx, int n, int64_t V,
                                                              PlanOut P, int32_t* status)
 {
+    pdl_enter();
     extern __shared__ uint32_t key[];                        // [kScatterPlanMaxN]
     uint16_t* ord0 = (uint16_t*)(key + kScatterPlanMaxN);   // [kScatterPlanMaxN] x 2
     uint16_t* ord1 = ord0 + kScatterPlanMaxN;
@@ -523,6 +529,7 @@ template <int DT, bool VEC>
 __global__ void __launch_bounds__(256) scatter_runs(const __grid_constant__ ScatterLaunch L, const PlanOut P,
                                                     int64_t nseg)
 {
+    pdl_enter();
     typedef SV<DT> S;
     typedef typename S::A A;
     constexpr int VPL = VEC ? 16 / S::ES : 1;
@@ -647,6 +654,7 @@ template <int DT, bool PAIR>
 __global__ void __launch_bounds__(OWNER_THREADS) scatter_owner(const __grid_constant__ ScatterLaunch L, int64_t ncb,
                                                                int idx16)
 {
+    pdl_enter();
     typedef SV<DT> S;
     typedef typename S::A A;
     constexpr int VPL = PAIR ? 2 : 1;
@@ -761,6 +769,7 @@ constexpr int NARROW_D = 4;
 template <int DT>
 __global__ void __launch_bounds__(256) scatter_runs_narrow(const __grid_constant__ ScatterLaunch L, const PlanOut P)
 {
+    pdl_enter();
     typedef SV<DT> S;
     typedef typename S::A A;
     const int R = P.hdr[0];
@@ -850,10 +859,10 @@ psg_status launch_gather(const GatherLaunch& L, void* stream)
     cudaStream_t s = (cudaStream_t)stream;
     const int64_t blocks = (L.n + 7) / 8;
     switch (L.es) {
-    case 1: gather_kernel<1><<<grid_for((const void*)gather_kernel<1>, 256, blocks), 256, 0, s>>>(L); break;
-    case 2: gather_kernel<2><<<grid_for((const void*)gather_kernel<2>, 256, blocks), 256, 0, s>>>(L); break;
-    case 4: gather_kernel<4><<<grid_for((const void*)gather_kernel<4>, 256, blocks), 256, 0, s>>>(L); break;
-    default: gather_kernel<8><<<grid_for((const void*)gather_kernel<8>, 256, blocks), 256, 0, s>>>(L); break;
+    case 1: launch(gather_kernel<1>, grid_for((const void*)gather_kernel<1>, 256, blocks), 256, 0, s, L); break;
+    case 2: launch(gather_kernel<2>, grid_for((const void*)gather_kernel<2>, 256, blocks), 256, 0, s, L); break;
+    case 4: launch(gather_kernel<4>, grid_for((const void*)gather_kernel<4>, 256, blocks), 256, 0, s, L); break;
+    default: launch(gather_kernel<8>, grid_for((const void*)gather_kernel<8>, 256, blocks), 256, 0, s, L); break;
     }
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
@@ -869,11 +878,9 @@ static void launch_accumulate(const ScatterLaunch& L, const unsigned long long* 
     const int64_t blocks = (L.n * nseg + 7) / 8;
     if (nseg == 0) return;
     if (vec)
-        scatter_accumulate<DT, true><<<grid_for((const void*)scatter_accumulate<DT, true>, 256, blocks), 256, 0, s>>>(
-            L, keys, nseg);
+        launch(scatter_accumulate<DT, true>, grid_for((const void*)scatter_accumulate<DT, true>, 256, blocks), 256, 0, s, L, keys, nseg);
     else
-        scatter_accumulate<DT, false><<<grid_for((const void*)scatter_accumulate<DT, false>, 256, blocks), 256, 0,
-                                        s>>>(L, keys, nseg);
+        launch(scatter_accumulate<DT, false>, grid_for((const void*)scatter_accumulate<DT, false>, 256, blocks), 256, 0, s, L, keys, nseg);
 }
 
 template <int DT>
@@ -887,11 +894,10 @@ static psg_status launch_planned(const ScatterLaunch& L, void* ws, cudaStream_t 
     });
     if (err != cudaSuccess) return PSG_E_CUDA;
     const PlanOut P = plan_layout(ws, L.n);
-    scatter_plan<<<1, PLAN_THREADS, PLAN_SMEM, s>>>(L.idx, (int)L.n, L.V, P, L.status);
+    launch(scatter_plan, 1, PLAN_THREADS, PLAN_SMEM, s, L.idx, (int)L.n, L.V, P, L.status);
     const int64_t runs = std::min<int64_t>(L.n, L.V);  // at most this many runs
     if (L.D <= NARROW_D) {
-        scatter_runs_narrow<DT><<<grid_for((const void*)scatter_runs_narrow<DT>, 256, (runs + 255) / 256), 256, 0,
-                                  s>>>(L, P);
+        launch(scatter_runs_narrow<DT>, grid_for((const void*)scatter_runs_narrow<DT>, 256, (runs + 255) / 256), 256, 0, s, L, P);
         return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
     }
     constexpr int ES = SV<DT>::ES;
@@ -901,9 +907,9 @@ static psg_status launch_planned(const ScatterLaunch& L, void* ws, cudaStream_t 
     const int64_t nseg = (L.D + seg_cols - 1) / seg_cols;
     const int64_t blocks = (runs * nseg + 7) / 8;
     if (vec)
-        scatter_runs<DT, true><<<grid_for((const void*)scatter_runs<DT, true>, 256, blocks), 256, 0, s>>>(L, P, nseg);
+        launch(scatter_runs<DT, true>, grid_for((const void*)scatter_runs<DT, true>, 256, blocks), 256, 0, s, L, P, nseg);
     else
-        scatter_runs<DT, false><<<grid_for((const void*)scatter_runs<DT, false>, 256, blocks), 256, 0, s>>>(L, P,
+        launch(scatter_runs<DT, false>, grid_for((const void*)scatter_runs<DT, false>, 256, blocks), 256, 0, s, L, P,
                                                                                                        nseg);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
@@ -928,8 +934,8 @@ static psg_status launch_owner(const ScatterLaunch& L, cudaStream_t s)
     if (err[pair ? 1 : 0] != cudaSuccess) return PSG_E_CUDA;
     const unsigned blocks = (unsigned)(L.V * ncb);
     const int idx16 = ((uintptr_t)L.idx % 16) == 0 ? 1 : 0;
-    if (pair) scatter_owner<DT, true><<<blocks, OWNER_THREADS, smem, s>>>(L, ncb, idx16);
-    else scatter_owner<DT, false><<<blocks, OWNER_THREADS, smem, s>>>(L, ncb, idx16);
+    if (pair) launch(scatter_owner<DT, true>, blocks, OWNER_THREADS, smem, s, L, ncb, idx16);
+    else launch(scatter_owner<DT, false>, blocks, OWNER_THREADS, smem, s, L, ncb, idx16);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
@@ -957,15 +963,14 @@ psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void
     }
     // longer lists: 64-bit keys (idx << 32 | n) through a bitonic network
     const int64_t np2 = scatter_npow2(L.n);
-    make_keys<<<grid_for((const void*)make_keys, 256, (np2 + 255) / 256), 256, 0, s>>>(L.idx, L.n, L.V, np2, keys,
+    launch(make_keys, grid_for((const void*)make_keys, 256, (np2 + 255) / 256), 256, 0, s, L.idx, L.n, L.V, np2, keys,
                                                                                      L.status);
     const int64_t tiles = (np2 + LOCAL_SORT - 1) / LOCAL_SORT;
-    bitonic_local<<<(unsigned)tiles, 1024, 0, s>>>(keys, np2, 0);
+    launch(bitonic_local, (unsigned)tiles, 1024, 0, s, keys, np2, 0);
     for (int64_t k = 2 * LOCAL_SORT; k <= np2; k <<= 1) {
         for (int64_t j = k >> 1; j >= LOCAL_SORT; j >>= 1)
-            bitonic_global<<<grid_for((const void*)bitonic_global, 256, (np2 / 2 + 255) / 256), 256, 0, s>>>(
-                keys, np2, k, j);
-        bitonic_local<<<(unsigned)tiles, 1024, 0, s>>>(keys, np2, k);
+            launch(bitonic_global, grid_for((const void*)bitonic_global, 256, (np2 / 2 + 255) / 256), 256, 0, s, keys, np2, k, j);
+        launch(bitonic_local, (unsigned)tiles, 1024, 0, s, keys, np2, k);
     }
     switch (L.dtype) {
     case PSG_F32: launch_accumulate<PSG_F32>(L, keys, s); break;

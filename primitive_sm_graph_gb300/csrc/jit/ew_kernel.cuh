@@ -36,6 +36,7 @@ struct EwCtx {
 
 extern "C" __global__ void __launch_bounds__(256) psg_ew(const __grid_constant__ PsgEwParams p)
 {
+    pdl_enter();
     const int gs = 1 << p.group_log2;
     const int groups = 256 >> p.group_log2;
     const int grp = threadIdx.x >> p.group_log2;

@@ -7,6 +7,17 @@ typedef unsigned int u32;
 typedef unsigned short u16;
 typedef long long i64;
 
+// Programmatic dependent launch: wait until the kernel before this one on the
+// stream has finished and its writes are visible, then let the next kernel be
+// scheduled.  First statement of every kernel; the host launches with
+// programmatic stream serialization, so a launch overlaps its predecessor's
+// tail and the data dependency is unchanged.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- per-node rounding -------------------------------------------------
 __device__ __forceinline__ float rbf(float x)  // float32 -> bfloat16 (RNE) -> float32
 {

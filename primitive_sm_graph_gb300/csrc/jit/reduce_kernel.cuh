@@ -287,6 +287,7 @@ __device__ __forceinline__ typename VT<DT>::T team_fold(typename VT<DT>::T v, in
 extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUSTER_DIMS psg_reduce(
     const __grid_constant__ PsgRedParams p)
 {
+    pdl_enter();
     __shared__ u32 sm[kColumnar ? kBlockThreads : 32];
     __shared__ u32 cpart[kColumnar ? 32 : 1];
     extern __shared__ __align__(128) unsigned char dsm[];  // staged mode: barriers, then the ring

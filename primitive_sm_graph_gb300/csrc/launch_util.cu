@@ -2,6 +2,7 @@
 // caches are filled once per (device, kernel) and never change afterwards.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <unordered_map>
 
@@ -68,6 +69,12 @@ int max_blocks_per_sm(const void* fn, int threads, size_t smem)
     std::lock_guard<std::mutex> g(g_mu);
     occ_cache()[key] = n;
     return n;
+}
+
+bool pdl_enabled()
+{
+    static const bool on = std::getenv("PSG_NO_PDL") == nullptr;
+    return on;
 }
 
 int kernel_regs(const void* fn)

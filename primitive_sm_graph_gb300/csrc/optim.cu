@@ -58,6 +58,7 @@ __device__ __forceinline__ void stp(void* p, long long i, float x)
 template <int DT>
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamWLaunch L)
 {
+    pdl_enter();
     // the bias corrections of this step: every thread forms the same values
     const float b1t = __fmul_rn(L.bpow[0], L.b1), b2t = __fmul_rn(L.bpow[1], L.b2);
     const float decay = __fsub_rn(1.0f, __fmul_rn(L.lr, L.wd));
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
 
 __global__ void advance_powers(float* bpow, float b1, float b2)
 {
+    pdl_enter();
     bpow[0] = __fmul_rn(bpow[0], b1);
     bpow[1] = __fmul_rn(bpow[1], b2);
 }
@@ -139,10 +141,10 @@ extern "C" psg_status psg_adamw_step(const psg_adamw_tensor* tensors, int n_tens
         const long long total = L.start[L.count];
         if (total == 0) continue;
         const int grid = (int)std::min<long long>((total + 255) / 256, (long long)num_sms() * 8);
-        if (dtype == PSG_F32) adamw_kernel<PSG_F32><<<grid, 256, 0, s>>>(L);
-        else if (dtype == PSG_BF16) adamw_kernel<PSG_BF16><<<grid, 256, 0, s>>>(L);
-        else adamw_kernel<PSG_F16><<<grid, 256, 0, s>>>(L);
+        if (dtype == PSG_F32) launch(adamw_kernel<PSG_F32>, grid, 256, 0, s, L);
+        else if (dtype == PSG_BF16) launch(adamw_kernel<PSG_BF16>, grid, 256, 0, s, L);
+        else launch(adamw_kernel<PSG_F16>, grid, 256, 0, s, L);
     }
-    advance_powers<<<1, 1, 0, s>>>(d_beta_pow, beta1, beta2);
+    launch(advance_powers, 1, 1, 0, s, d_beta_pow, beta1, beta2);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }

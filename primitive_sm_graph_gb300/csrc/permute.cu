@@ -25,6 +25,7 @@ constexpr int TTHREADS = TX * TY;
 template <typename E>
 __global__ void __launch_bounds__(TTHREADS) transpose_kernel(const __grid_constant__ TransposeLaunch L)
 {
+    pdl_enter();
     __shared__ E tile[TT][TT + 1];
     const E* __restrict__ src = (const E*)L.in;
     E* __restrict__ dst = (E*)L.out;
@@ -84,13 +85,14 @@ void launch_t(const TransposeLaunch& L, cudaStream_t s)
     const int per_sm = max_blocks_per_sm((const void*)transpose_kernel<E>, TTHREADS, 0);
     const int64_t cap = (int64_t)num_sms() * per_sm;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, cap));
-    transpose_kernel<E><<<grid, TTHREADS, 0, s>>>(L);
+    launch(transpose_kernel<E>, grid, TTHREADS, 0, s, L);
 }
 
 // Generic strided copy for layouts the tile does not cover (any dtype):
 // one thread per output cell, the View's index arithmetic per cell.
 __global__ void copy_kernel(const __grid_constant__ CopyLaunch L)
 {
+    pdl_enter();
     const int64_t n = L.numel;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -137,7 +139,7 @@ psg_status launch_copy(const CopyLaunch& L, void* stream)
     const int per_sm = max_blocks_per_sm((const void*)copy_kernel, threads, 0);
     const int64_t need = (L.numel + threads - 1) / threads;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)num_sms() * per_sm));
-    copy_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(L);
+    launch(copy_kernel, grid, threads, 0, (cudaStream_t)stream, L);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 

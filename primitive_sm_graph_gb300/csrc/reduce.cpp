@@ -388,9 +388,10 @@ extern "C" psg_status psg_reduce_rows(const psg_reduce_stage* stages, int n_stag
     int grid;
     grid_for(P, k, &grid);
     void* args[] = {(void*)&P.p};
-    if (cudaLaunchKernel((const void*)k, dim3(grid), dim3(P.block), args, (size_t)P.smem, (cudaStream_t)stream) !=
-        cudaSuccess)
-        return PSG_E_CUDA;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg =
+        launch_config(dim3(grid), dim3(P.block), (size_t)P.smem, (cudaStream_t)stream, attr);
+    if (cudaLaunchKernelExC(&cfg, (const void*)k, args) != cudaSuccess) return PSG_E_CUDA;
     return PSG_OK;
 }
 

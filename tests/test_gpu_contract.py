@@ -321,3 +321,51 @@ def test_split_k_not_used_for_many_tiles(A):
     Bv = A.make_view("bf16", [M, N, K], [0, 1, N], 0, None, K * N)
     Cv = A.make_view("f32", [M, N], [N, 1], 0, None, M * N)
     assert A.psg_contract_workspace(Av, Bv, Cv) == 0
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+@pytest.mark.parametrize("M,N,K,a_layout,b_layout,out_dt", [
+    (300, 520, 200, "mk", "kn", "f32"), (300, 520, 200, "km", "kn", "bf16"),
+    (300, 520, 200, "mk", "nk", "f32"), (300, 520, 200, "km", "nk", "bf16"),
+    (257, 513, 1000, "mk", "kn", "bf16"),   # the second CTA of the last pair reads only zero fill
+    (640, 256, 2048, "km", "nk", "f32")])
+def test_pair_and_single_cta_kernels(A, O, monkeypatch, kernel, M, N, K, a_layout, b_layout, out_dt):
+    """The two bf16 tensor-core kernels (one CTA a 128 x 256 tile; two CTAs a
+    256 x 256 tile) on every operand major and ragged edges, each against the
+    oracle, and the same bits from both."""
+    monkeypatch.setenv("PSG_GEMM_KERNEL", kernel)
+    a, b = SI.contraction_bf16(M * 3 + N + K, M, N, K)
+    ref = O.matmul(O.T(SI.bits(a), "bf16"), O.T(SI.bits(b), "bf16"), "f32").data
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    dA, dB = dev(_storage(a, a_layout)), dev(_storage(b, b_layout))
+    Av, Bv = _views(A, dA, dB, M, N, K, a_layout, b_layout)
+    C = torch.empty((M, N), dtype=storage_dtype(out_dt), device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _check(O.T(to_np(C.cpu()), out_dt).f64(), ref, mag, K, out_dt)
+    # the other kernel sums the same exact products in the same K order
+    monkeypatch.setenv("PSG_GEMM_KERNEL", "single" if kernel == "pair" else "pair")
+    C2 = torch.empty_like(C)
+    A.psg_contract(dA, Av, dB, Bv, C2, A.view_of(C2), st)
+    torch.cuda.synchronize()
+    iv = torch.int16 if C.element_size() == 2 else torch.int32
+    assert torch.equal(C.view(iv), C2.view(iv))
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+def test_pair_and_single_cta_split_k(A, O, monkeypatch, kernel):
+    monkeypatch.setenv("PSG_GEMM_KERNEL", kernel)
+    M, N, K = 384, 512, 4096
+    a, b, dA, dB, Av, Bv, C = _split_case(A, M, N, K, "km", "kn", "bf16", None, 77)
+    need = A.psg_contract_workspace(Av, Bv, A.view_of(C))
+    assert need > 0
+    ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    A.psg_contract_ws(dA, Av, dB, Bv, C, A.view_of(C), ws, need, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = O.matmul(O.T(SI.bits(a), "bf16"), O.T(SI.bits(b), "bf16"), "f32").data
+    mag = (a.double().abs() @ b.double().abs()).numpy()
+    _check(O.T(to_np(C.cpu()), "bf16").f64(), ref, mag, K, "bf16")
