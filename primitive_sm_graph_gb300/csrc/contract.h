@@ -16,6 +16,7 @@ struct TcParams {
     void* C;
     int32_t* status;
     int64_t c_offset, c_rs, c_cs, c_bs;
+    int tma_store;              // 1: the epilogue writes C (or the partials) through a tensor map
 };
 
 struct TcOperands {

@@ -30,6 +30,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "contract.h"
@@ -47,11 +48,14 @@ constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
 constexpr int TMEM_COLS = 512;                   // two 128 x 256 f32 accumulators
-constexpr int EPI_WARPS = 8;                     // warps 2 .. 9
+constexpr int EPI_WARPS = 4;                     // warps 2 .. 5
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-// (8 KB of slack after the barriers keeps every tensor-core operand read inside
-// the allocation even for the widest descriptor stride)
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + 8192;
+// the epilogue stages 32 rows x 128 bytes at a time, two slots a warp; the
+// staging area follows the operand ring (so a tensor-core operand read past
+// the last stage stays inside the allocation), the barriers follow it
+constexpr int EPI_CHUNK = 4096;
+constexpr int STAGING_BYTES = EPI_WARPS * 2 * EPI_CHUNK;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + 256;
 
 struct Bars {
     uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
@@ -119,21 +123,97 @@ __device__ __forceinline__ void epi_store32(const TcParams& p, const uint32_t (&
     }
 }
 
+// One accumulator's rows row0 .. row0 + 31 (this warp's 32 TMEM lanes, tm
+// their first column) over the tile's BN columns, which start at column
+// n_base: 64 columns per pair of TMEM loads, rounded once into the output
+// dtype (float32 partials under split-K).  With p.tma_store every 32 x
+// 128-byte piece is written into one of the warp's two 128B-swizzled staging
+// slots and leaves in one TMA store (the tensor clips rows and columns past
+// its edge); otherwise each lane stores its own row.
+__device__ __forceinline__ void epilogue_rows(const TcParams& p, const CUtensorMap* tmap_c, uint8_t* slots,
+                                              uint32_t& nst, uint32_t tm, int row0, int n_base, int sp, int b,
+                                              int lane)
+{
+    const int m = row0 + lane;
+    const int64_t crow = p.c_offset + (int64_t)b * p.c_bs + (int64_t)m * p.c_rs;
+    const bool f32out = p.splits > 1 || p.c_dtype == PSG_F32;
+    const int z = p.splits > 1 ? sp * p.batch + b : b;
+    for (int c2 = 0; c2 < BN; c2 += 64) {
+        uint32_t rr[2][32];
+        __syncwarp();  // tcgen05.ld is warp-collective: reach it converged
+        tmem_ld32_nowait(tm + (uint32_t)c2, rr[0]);
+        tmem_ld32_nowait(tm + (uint32_t)c2 + 32u, rr[1]);
+        tmem_ld_wait();
+        if (!p.tma_store) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) epi_store32(p, rr[h], m, crow, n_base + c2 + 32 * h, sp, b);
+            continue;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h == 1 && !f32out) break;  // 64 half-width columns fill one 128-byte row
+            uint32_t w[32];
+            if (f32out) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = rr[h][j];
+            } else if (p.c_dtype == PSG_BF16) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[j])
+                        : "f"(__uint_as_float(rr[j >> 4][(2 * j + 1) & 31])), "f"(__uint_as_float(rr[j >> 4][(2 * j) & 31])));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w[j])
+                        : "f"(__uint_as_float(rr[j >> 4][(2 * j + 1) & 31])), "f"(__uint_as_float(rr[j >> 4][(2 * j) & 31])));
+            }
+            uint8_t* slot = slots + (nst & 1u) * EPI_CHUNK;
+            if (nst >= 2) {  // the store that last read this slot is done reading it
+                if (lane == 0) bulk_wait_read1();
+                __syncwarp();
+            }
+            const uint32_t row = smem_u32(slot) + (uint32_t)lane * 128u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                             ::"r"(row + (uint32_t)((u ^ (lane & 7)) << 4)), "r"(w[4 * u]), "r"(w[4 * u + 1]),
+                               "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                             : "memory");
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // a box wholly past the tensor's edge is not issued; the group is
+                // committed either way, so the slot accounting above holds
+                const int x = n_base + c2 + 32 * h;
+                if (row0 < p.M && x < p.N) tma_store_3d(tmap_c, slot, x, row0, z);
+                bulk_commit();
+            }
+            ++nst;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CUtensorMap tmap_a,
                                                       const __grid_constant__ CUtensorMap tmap_b,
+                                                      const __grid_constant__ CUtensorMap tmap_c,
                                                       const __grid_constant__ TcParams p)
 {
-    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     // swizzled tiles need 1024-byte alignment of their shared-memory address
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    Bars* bars = (Bars*)(smem + STAGES * STAGE_BYTES);
+    uint8_t* staging = smem + STAGES * STAGE_BYTES;
+    Bars* bars = (Bars*)(staging + STAGING_BYTES);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int total = p.num_m * p.num_n * p.batch;
     const int units = total * p.splits;  // (tile, K range) work units
 
+    // set-up that touches no global memory runs before the wait on the
+    // previous kernel: barriers, TMEM, the tensor maps' descriptor fetch
     if (threadIdx.x == 0) {
+        prefetch_map(&tmap_a);
+        prefetch_map(&tmap_b);
+        if (p.tma_store) prefetch_map(&tmap_c);
         for (int s = 0; s < STAGES; ++s) {
             bar_init(&bars->full[s], 1);
             bar_init(&bars->empty[s], 1);
@@ -154,6 +234,7 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_enter();
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
@@ -251,10 +332,9 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
         }
     } else {
         // ---------------- epilogue: TMEM -> registers -> global ----------------
-        // a warp may only read TMEM lanes 32 * (warp % 4) .. + 31; warps w and
-        // w + 4 share those rows and split the columns
-        const int q = warp & 3;
-        const int c_lo = ((warp - 2) >> 2) * (BN / 2);
+        const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
+        uint8_t* slots = staging + (warp - 2) * 2 * EPI_CHUNK;
+        uint32_t nst = 0;
         uint32_t aph[2] = {0u, 0u};
         int local = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
@@ -265,26 +345,13 @@ __global__ void __launch_bounds__(THREADS, 1) tc_gemm(const __grid_constant__ CU
             tc_fence_after();
             int b, mb, nb;
             tile_coords(p.num_m, p.num_n, t, b, mb, nb);
-            const int m = mb * BM + q * 32 + lane;
-            const int64_t crow = p.c_offset + (int64_t)b * p.c_bs + (int64_t)m * p.c_rs;
-            for (int c2 = c_lo; c2 < c_lo + BN / 2; c2 += 64) {
-                uint32_t rr[2][32];
-                __syncwarp();  // tcgen05.ld is warp-collective: reach it converged
-                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c2);
-                tmem_ld32_nowait(ta, rr[0]);
-                tmem_ld32_nowait(ta + 32u, rr[1]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t (&r)[32] = rr[h];
-                    const int c = c2 + 32 * h;
-                    epi_store32(p, r, m, crow, nb * BN + c, sp, b);
-                }
-            }
+            epilogue_rows(p, &tmap_c, slots, nst, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN),
+                          mb * BM + q * 32, nb * BN, sp, b, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive(&bars->tempty[acc]);
         }
+        if (lane == 0) bulk_wait_all();  // staged stores done before the CTA's shared memory goes away
     }
     tc_fence_before();
     __syncthreads();
@@ -310,7 +377,7 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = 128 * BK * 2;                // 16 KB
 constexpr int P_B_BYTES = P_HN * BK * 2;               // 16 KB
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;   // 32 KB
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 256 + 8192;
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + STAGING_BYTES + 256;
 
 struct PairBars {
     uint64_t full[P_STAGES], empty[P_STAGES], tfull[2], tempty[2], drain;
@@ -329,12 +396,12 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t dtmem, uint64_t ad, uint6
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_gemm2(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-             const __grid_constant__ TcParams p)
+             const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ TcParams p)
 {
-    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    PairBars* bars = (PairBars*)(smem + P_STAGES * P_STAGE_BYTES);
+    uint8_t* staging = smem + P_STAGES * P_STAGE_BYTES;
+    PairBars* bars = (PairBars*)(staging + STAGING_BYTES);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -344,6 +411,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int units = total * p.splits;
 
     if (threadIdx.x == 0) {
+        prefetch_map(&tmap_a);
+        prefetch_map(&tmap_b);
+        if (p.tma_store) prefetch_map(&tmap_c);
         for (int s = 0; s < P_STAGES; ++s) {
             bar_init(&bars->full[s], 1);
             bar_init(&bars->empty[s], 1);
@@ -366,6 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
+    pdl_enter();  // nothing above touched global memory
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
@@ -456,7 +527,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     } else {
         // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
         const int q = warp & 3;
-        const int c_lo = ((warp - 2) >> 2) * (BN / 2);
+        uint8_t* slots = staging + (warp - 2) * 2 * EPI_CHUNK;
+        uint32_t nst = 0;
         const uint32_t tempty0 = smem_in_rank(&bars->tempty[0], 0);
         uint32_t aph[2] = {0u, 0u};
         int local = 0;
@@ -468,22 +540,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             tc_fence_after();
             int b, mb, nb;
             tile_coords(p.num_m, p.num_n, t, b, mb, nb);
-            const int m = mb * P_BM + (int)rank * 128 + q * 32 + lane;
-            const int64_t crow = p.c_offset + (int64_t)b * p.c_bs + (int64_t)m * p.c_rs;
-            for (int c2 = c_lo; c2 < c_lo + BN / 2; c2 += 64) {
-                uint32_t rr[2][32];
-                __syncwarp();
-                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c2);
-                tmem_ld32_nowait(ta, rr[0]);
-                tmem_ld32_nowait(ta + 32u, rr[1]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) epi_store32(p, rr[h], m, crow, nb * BN + c2 + 32 * h, sp, b);
-            }
+            epilogue_rows(p, &tmap_c, slots, nst, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN),
+                          mb * P_BM + (int)rank * 128 + q * 32, nb * BN, sp, b, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
         }
+        if (lane == 0) bulk_wait_all();
     }
     // the leader's MMAs read this CTA's shared memory and write its TMEM: no
     // CTA frees either before both are done
@@ -528,6 +591,47 @@ bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of the epilogue's destination, 32 rows x 128 bytes a box,
+// 128B-swizzled: C itself, or under split-K the float32 partials
+// [splits][batch][M][N].  Sets p.tma_store; false (direct stores) when C's
+// layout cannot be described (a strided column, a row pitch or base that is
+// not a multiple of 16 bytes).
+void make_out_map(CUtensorMap* map, TcParams& p)
+{
+    p.tma_store = 0;
+    std::memset(map, 0, sizeof(*map));
+    auto enc = encode_fn();
+    if (!enc) return;
+    const bool partials = p.splits > 1;
+    const int es = partials ? 4 : dtype_size(p.c_dtype);
+    const CUtensorMapDataType dt = partials || p.c_dtype == PSG_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : p.c_dtype == PSG_F16          ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const void* base;
+    int64_t rs, bs, nz;
+    if (partials) {
+        base = p.ws;
+        rs = p.N;
+        bs = (int64_t)p.M * p.N;
+        nz = (int64_t)p.splits * p.batch;
+    } else {
+        if (p.c_cs != 1) return;
+        base = (const char*)p.C + p.c_offset * es;
+        rs = p.M > 1 ? p.c_rs : p.N;
+        bs = p.batch > 1 ? p.c_bs : rs * p.M;
+        nz = p.batch;
+    }
+    if (((uintptr_t)base & 15) != 0 || rs < p.N || (rs * es) % 16 != 0 || bs <= 0 || (bs * es) % 16 != 0) return;
+    cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.M, (cuuint64_t)nz};
+    cuuint64_t strides[2] = {(cuuint64_t)(rs * es), (cuuint64_t)(bs * es)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), 32, 1};
+    cuuint32_t ones[3] = {1, 1, 1};
+    if (enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+        p.tma_store = 1;
+}
+
 }  // namespace
 
 int contract_tc_splits(int64_t M, int64_t N, int64_t K, int64_t batch, size_t* bytes)
@@ -551,9 +655,10 @@ int contract_tc_splits(int64_t M, int64_t N, int64_t K, int64_t batch, size_t* b
 namespace {
 
 // The CTA-pair kernel takes outputs of more than one 128-row block over
-// K >= 1024 (measured on GB300: 8192 x 8192 x 2048 in 170 us against 194 us
-// single-CTA; at K = 512 the two are within a few percent, the single-CTA one
-// ahead).  PSG_GEMM_KERNEL=single or =pair in the environment forces one of
+// K >= 1024, or over K >= 512 when the single-CTA tiles make two waves or more
+// (measured on GB300: 8192 x 8192 x 2048 in 164 us against 194 us single-CTA;
+// 8192 x 2048 x 512 in 18.7 us against 20.1 us; 8192 x 512 x 512, one wave,
+// 8.2 us against 7.8 us).  PSG_GEMM_KERNEL=single or =pair in the environment forces one of
 // them (pair still needs M > 128).
 bool use_pair(const TcParams& p)
 {
@@ -561,7 +666,8 @@ bool use_pair(const TcParams& p)
     const char* f = std::getenv("PSG_GEMM_KERNEL");
     if (f && f[0] == 's') return false;
     if (f && f[0] == 'p') return true;
-    return p.K >= 1024;
+    const int64_t tiles = (int64_t)((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN) * p.batch;
+    return p.K >= 1024 || (p.K >= 512 && tiles >= 2 * (int64_t)num_sms());
 }
 
 // clusters of two tc_gemm2 CTAs that fit on the device at once (per device)
@@ -605,9 +711,11 @@ psg_status launch_pair(const TcOperands& o, TcParams p, int64_t a_bs, int64_t b_
     p.num_n = (p.N + BN - 1) / BN;
     p.num_k = (p.K + BK - 1) / BK;
     p.kb_per = (p.num_k + p.splits - 1) / p.splits;
+    CUtensorMap mc;
+    make_out_map(&mc, p);
     const int64_t units = (int64_t)p.num_m * p.num_n * p.batch * p.splits;
     const int clusters = (int)std::min<int64_t>(units, pair_clusters());
-    launch(tc_gemm2, 2 * clusters, THREADS, P_SMEM_BYTES, (cudaStream_t)stream, ma, mb, p);
+    launch(tc_gemm2, 2 * clusters, THREADS, P_SMEM_BYTES, (cudaStream_t)stream, ma, mb, mc, p);
     if (p.splits > 1) {
         const int64_t cells = (int64_t)p.batch * p.M * p.N;
         const int rgrid = (int)std::min<int64_t>((cells + 255) / 256, (int64_t)num_sms() * 8);
@@ -653,9 +761,11 @@ psg_status launch_contract_tc(const TcOperands& o, void* stream)
         attr_err = cudaFuncSetAttribute((const void*)tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return PSG_E_CUDA;
+    CUtensorMap mc;
+    make_out_map(&mc, p);
     const int64_t units = (int64_t)p.num_m * p.num_n * p.batch * p.splits;
     const int grid = (int)std::min<int64_t>(units, num_sms());
-    launch(tc_gemm, grid, THREADS, SMEM_BYTES, (cudaStream_t)stream, ma, mb, p);
+    launch(tc_gemm, grid, THREADS, SMEM_BYTES, (cudaStream_t)stream, ma, mb, mc, p);
     if (p.splits > 1) {
         const int64_t cells = (int64_t)p.batch * p.M * p.N;
         const int rgrid = (int)std::min<int64_t>((cells + 255) / 256, (int64_t)num_sms() * 8);
