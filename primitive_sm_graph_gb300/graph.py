@@ -362,12 +362,14 @@ class Executor:
         self.log = []
         self.status = None
         self.users = {}
+        self.user_nodes = {}
+        self.narrow = {}
 
     def prepare(self, roots):
         """Count, for every unrealized node reachable from roots, how many
         nodes use it: a computed value with several users is a cut (it is
         stored once instead of being recomputed in each consumer)."""
-        users, seen, stack = {}, set(), list(roots)
+        users, nodes, seen, stack = {}, {}, set(), list(roots)
         while stack:
             t = stack.pop()
             if id(t) in seen or t._real is not None:
@@ -375,8 +377,61 @@ class Executor:
             seen.add(id(t))
             for x in t.src:
                 users[id(x)] = users.get(id(x), 0) + 1
+                nodes.setdefault(id(x), []).append(t)
                 stack.append(x)
         self.users = users
+        self.user_nodes = nodes
+        self.narrow = {}
+
+    def _only_cast_to(self, x, dt, depth=0):
+        """True when every use of x (through movements) is a CAST to dt."""
+        us = self.user_nodes.get(id(x))
+        if not us or depth > 8:
+            return False
+        for u in us:
+            if u.op == "CAST" and u.dtype == dt:
+                continue
+            if u.op == "MOVE" and u.arg[0] not in ("pad", "detach") and self._only_cast_to(u, dt, depth + 1):
+                continue
+            return False
+        return True
+
+    def _narrowable(self, t):
+        """(contraction node, movements) when t is a CAST to a half width of
+        an unrealized contraction whose every use is that CAST (see
+        _narrow_contraction), else None; realizes nothing."""
+        if t.op != "CAST" or t.dtype not in ("bf16", "f16"):
+            return None
+        x, inner = t.src[0], []
+        while x.op == "MOVE" and x.arg[0] not in ("pad", "detach"):
+            inner.append(x.arg)
+            x = x.src[0]
+        if x.op != "SUM" or x.dtype != "f32":
+            return None
+        if (id(x), t.dtype) in self.narrow:
+            return x, inner
+        if x._real is not None or not self._contract_pattern(x) or not self._only_cast_to(x, t.dtype):
+            return None
+        return x, inner
+
+    def _narrow_contraction(self, t):
+        """For t = CAST to a half width of an unrealized contraction (through
+        movements) whose every use is that same CAST: the contraction stored
+        once in the half width ((buf, View) for t), else None.  Its epilogue
+        rounds the float32 total to nearest even, the bits a CAST of the
+        float32 result gives, and the float32 tensor is never written."""
+        nx = self._narrowable(t)
+        if nx is None:
+            return None
+        x, inner = nx
+        key = (id(x), t.dtype)
+        if key not in self.narrow:
+            r = self._try_contract(x, (), t.dtype, x.shape)
+            if r is None:
+                return None
+            self.narrow[key] = r
+        buf, v = self.narrow[key]
+        return self._apply_moves(buf, v, list(reversed(inner)), t.dtype)
 
     def _shared_heavy(self, x):
         """A value with several users is stored once (a cut) when recomputing
@@ -511,6 +566,12 @@ class Executor:
                 r = leaf(buf, v, t.dtype)
                 memo[key] = r
                 return r
+            nr = self._narrow_contraction(t) if op == "CAST" and not any(m[0] == "pad" for m in moves) else None
+            if nr is not None:
+                buf, v = self._apply_moves(*nr, list(moves), t.dtype)
+                r = leaf(buf, v, t.dtype)
+                memo[key] = r
+                return r
             # a shared value is a cut, except inside one fused reduction,
             # whose stages and epilogue recompute it from registers
             if t is not root and not reds and op in ELEMENTWISE and self._shared_heavy(t):
@@ -557,6 +618,9 @@ class Executor:
         while base.op == "MOVE" and base.arg[0] != "pad":
             moves.append(base.arg)
             base = base.src[0]
+        nr = self._narrow_contraction(base)
+        if nr is not None:
+            return self._apply_moves(*nr, list(reversed(moves)), base.dtype)
         if base.op == "CAST" and base.dtype in ("bf16", "f32"):
             x, inner = base.src[0], []
             while x.op == "MOVE" and x.arg[0] != "pad":
@@ -619,6 +683,8 @@ class Executor:
             seen.add(key)
             if x.op == "MOVE":
                 walk(x.src[0], (x.arg,) + moves)
+            elif x.op == "CAST" and self._narrowable(x) is not None:
+                return  # read from the contraction stored in the half width
             elif x.op in ELEMENTWISE:
                 for s in x.src:
                     walk(s, moves)
