@@ -260,6 +260,172 @@ __device__ __forceinline__ typename VT<DT>::T col_fold(typename VT<DT>::T v, u32
     return r;
 }
 
+// ---- kColVec: columnar rows eight to a thread ------------------------------
+// A thread's PSG_VEC lanes are eight adjacent rows (the cells next to each
+// other in memory), and a chunk is one index r of the reduced axis: an input
+// that moves with the row is read as one 16-byte (32-byte for float32) vector
+// at r, an input that does not is read once and shared by the lanes.  A warp
+// holds kVecRT row threads (kVecRT * 8 rows) by 32 / kVecRT slots of the
+// reduced axis; the members of a row group are those slots over the CTA's
+// warps and the cluster's CTAs.  One stage, one output per row.
+constexpr int kVecRS = 32 / kVecRT;
+
+template <int DT>
+__device__ __forceinline__ void ld_rowvec(const void* p, i64 o, typename VT<DT>::T (&d)[PSG_VEC])
+{
+    if constexpr (DT == PSG_DT_F32) {
+        const uint4* q = (const uint4*)((const float*)p + o);
+        const uint4 a = __ldg(q), b = __ldg(q + 1);
+        const u32 w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int v = 0; v < PSG_VEC; ++v) d[v] = __uint_as_float(w[v]);
+    } else {
+        const uint4 a = __ldg((const uint4*)((const u16*)p + o));
+        const u32 w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            if constexpr (DT == PSG_DT_BF16) {
+                d[2 * v] = __uint_as_float(w[v] << 16);
+                d[2 * v + 1] = __uint_as_float(w[v] & 0xffff0000u);
+            } else {
+                d[2 * v] = h2f((u16)(w[v] & 0xffffu));
+                d[2 * v + 1] = h2f((u16)(w[v] >> 16));
+            }
+        }
+    }
+}
+
+struct VecCtx {
+    const PsgRedParams& p;
+    const i64 (&roff)[kNinP];  // each input's offset at the thread's first row, r = 0
+    i64 r;
+    const u32* red;
+    template <int K>
+    __device__ __forceinline__ void ldv(typename VT<kInDt[K]>::T (&d)[PSG_VEC]) const
+    {
+        const i64 o = roff[K] + r * p.in[K].inner_stride;
+        if constexpr (kVecRow[K]) {
+            ld_rowvec<kInDt[K]>(p.in[K].ptr, o, d);
+        } else {
+            const typename VT<kInDt[K]>::T x = ld_cell<kInDt[K]>(p.in[K].ptr, o);
+#pragma unroll
+            for (int v = 0; v < PSG_VEC; ++v) d[v] = x;
+        }
+    }
+    template <int K>
+    __device__ __forceinline__ typename VT<kInDt[K]>::T ld1() const
+    {
+        return ld_cell<kInDt[K]>(p.in[K].ptr, roff[K]);
+    }
+    __device__ __forceinline__ float redf(int s) const { return __uint_as_float(red[s]); }
+    __device__ __forceinline__ int redi(int s) const { return (int)red[s]; }
+    __device__ __forceinline__ float stashf(int) const { return 0.0f; }
+    __device__ __forceinline__ int stashi(int) const { return 0; }
+};
+
+// fold: [warps][kVecRT][PSG_VEC] words; cpart: [kVecRT][PSG_VEC] = 32 words
+__device__ __forceinline__ void colvec_body(const PsgRedParams& p, u32* fold, u32* cpart)
+{
+    typedef Fold<kStageOp[0], kStageDt[0]> F;
+    typedef typename VT<kStageDt[0]>::T T;
+    const int warp = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int rt = l % kVecRT, rs = l / kVecRT;
+    const int W = blockDim.x >> 5;
+    const int rank = kCluster > 1 ? (int)(blockIdx.x % kCluster) : 0;
+    const i64 member = ((i64)rank * W + warp) * kVecRS + rs;
+    const i64 TM = (i64)kCluster * W * kVecRS;  // members of a row group
+    const i64 rows_cta = (i64)kVecRT * PSG_VEC;
+    const i64 groups = (p.rows + rows_cta - 1) / rows_cta;
+    const u32 nored[PSG_MAXSTAGES] = {0u, 0u, 0u, 0u};
+    for (i64 g = blockIdx.x / kCluster; g < groups; g += gridDim.x / kCluster) {
+        const i64 j0 = g * rows_cta + (i64)rt * PSG_VEC;
+        const bool active = j0 < p.rows;  // rows come in whole groups of PSG_VEC
+        i64 roff[kNinP];
+        bool rok[kNinP];
+        i64 ooff = 0;
+        if (active) {
+            row_offsets<kNin>(p.in, p.out, p.shape, p.nd, j0, roff, rok, kInMode, ooff);
+        } else {
+#pragma unroll
+            for (int k = 0; k < kNinP; ++k) roff[k] = 0;
+        }
+        T accv[PSG_VEC];
+#pragma unroll
+        for (int v = 0; v < PSG_VEC; ++v) accv[v] = F::identity();
+        if (active) {
+            const VecCtx cu{p, roff, 0, nored};
+            const typename StageBody<0>::U u = StageBody<0>::uni(cu);
+            i64 r = member;
+            // four reduced indices at a time: their loads all go out together
+            for (; r + 3 * TM < p.inner; r += 4 * TM) {
+                T y[4][PSG_VEC];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const VecCtx c{p, roff, r + q * TM, nored};
+                    StageBody<0>::eval(c, u, y[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int v = 0; v < PSG_VEC; ++v) accv[v] = F::step(accv[v], y[q][v]);
+            }
+            for (; r < p.inner; r += TM) {
+                const VecCtx c{p, roff, r, nored};
+                T y[PSG_VEC];
+                StageBody<0>::eval(c, u, y);
+#pragma unroll
+                for (int v = 0; v < PSG_VEC; ++v) accv[v] = F::step(accv[v], y[v]);
+            }
+        }
+        // one fixed tree, the same bits on every run: the warp's slots by
+        // shuffles (xor 4, 8, 16), then the CTA's warps in order, then the
+        // cluster's CTAs in rank order; lane rt * PSG_VEC + v of warp 0 owns
+        // row j0(rt) + v from the second level on
+#pragma unroll
+        for (int off = kVecRT; off < 32; off <<= 1)
+#pragma unroll
+            for (int v = 0; v < PSG_VEC; ++v)
+                accv[v] = F::step(accv[v], from_bits<T>(__shfl_xor_sync(0xffffffffu, as_bits(accv[v]), off, 32)));
+        if (rs == 0) {
+#pragma unroll
+            for (int v = 0; v < PSG_VEC; ++v) fold[(warp * kVecRT + rt) * PSG_VEC + v] = as_bits(accv[v]);
+        }
+        __syncthreads();
+        constexpr int MW = kBlockThreads / 32;  // warps at the launch bound
+        if (warp == 0) {
+            u32 part[MW];  // every warp's partial loaded before the first add
+#pragma unroll
+            for (int m = 0; m < MW; ++m) part[m] = m < W ? fold[m * 32 + l] : 0u;
+            T a = from_bits<T>(part[0]);
+#pragma unroll
+            for (int m = 1; m < MW; ++m)
+                if (m < W) a = F::step(a, from_bits<T>(part[m]));
+            cpart[l] = as_bits(a);
+        }
+        if constexpr (kCluster > 1) cluster_sync_all();
+        else __syncthreads();
+        const int ort = l / PSG_VEC, ov = l % PSG_VEC;  // the row this lane of warp 0 finishes
+        const i64 oj = g * rows_cta + (i64)ort * PSG_VEC + ov;
+        if (rank == 0 && warp == 0 && oj < p.rows) {
+            T a = from_bits<T>(kCluster > 1 ? ld_rank(cpart + l, 0) : cpart[l]);
+#pragma unroll
+            for (int c = 1; c < kCluster; ++c) a = F::step(a, from_bits<T>(ld_rank(cpart + l, c)));
+            const u32 red1[PSG_MAXSTAGES] = {as_bits(F::finish(a)), 0u, 0u, 0u};
+            i64 ro2[kNinP];
+            bool rk2[kNinP];
+            i64 oo2 = 0;
+            row_offsets<kNin>(p.in, p.out, p.shape, p.nd, oj, ro2, rk2, kInMode, oo2);
+            const VecCtx ce{p, ro2, 0, red1};
+            typename VT<kOutDt>::T y[PSG_VEC];
+            Epi::eval(ce, Epi::uni(ce), y);
+            st_cell<kOutDt>((void*)p.out.ptr, oo2, y[0]);
+        }
+        // nobody rewrites fold or cpart while another CTA of the cluster reads them
+        if constexpr (kCluster > 1) cluster_sync_all();
+        else __syncthreads();
+    }
+}
+
 // fold v across the team (threads [team*T, team*T + T) of the block)
 template <int OP, int DT>
 __device__ __forceinline__ typename VT<DT>::T team_fold(typename VT<DT>::T v, int team_log2, u32* sm)
@@ -290,6 +456,10 @@ extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUS
     pdl_enter();
     __shared__ u32 sm[kColumnar ? kBlockThreads : 32];
     __shared__ u32 cpart[kColumnar ? 32 : 1];
+    if constexpr (kColVec) {
+        colvec_body(p, sm, cpart);
+        return;
+    }
     extern __shared__ __align__(128) unsigned char dsm[];  // staged mode: barriers, then the ring
     // members of a team (T), teams of a block, this thread's team and member index (lane)
     const int T = kColumnar ? (int)(blockDim.x >> 5) * kCluster : 1 << p.team_log2;

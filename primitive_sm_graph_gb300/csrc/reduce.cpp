@@ -261,13 +261,43 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     constexpr int RED_COL_MIN_CHUNKS = 2;
     int col_members = RED_COL_THREADS / 32;
     while (col_members > 1 && sp.chunks < (int64_t)col_members * RED_COL_MIN_CHUNKS) col_members >>= 1;
+    // vectorised columnar layout (kColVec): one stage, one output per row,
+    // two row dims at most collapsed to one, rows in whole groups of PSG_VEC,
+    // and every input float-typed and either moving one cell a row (read as
+    // aligned 16-byte vectors of PSG_VEC rows) or not moving with the row at
+    // all (read once for the PSG_VEC rows).  Then a thread holds eight rows:
+    // for the GPT block's RMSNorm weight gradients (512 sums of 8192 rows,
+    // three inputs) one load moves 16 or 32 bytes instead of 2 or 4.
+    constexpr int VEC_RT = 4;  // row threads a warp: 32 rows a CTA, 8 slots of the reduced axis a warp
+    int vec_row[PSG_MAX_INPUTS] = {0};
+    bool colvec = columnar && n_stages == 1 && per_row && sp.nd == 2 && sp.rows % PSG_VEC == 0;
+    for (int k = 0; k < n_in && colvec; ++k) {
+        const int es = dtype_size(dts[k]);
+        if (dts[k] != PSG_F32 && dts[k] != PSG_BF16 && dts[k] != PSG_F16) colvec = false;
+        const int64_t rs = P->p.in[k].outer_stride[0];
+        if (rs == 1) {
+            vec_row[k] = 1;
+            if (uni[k] || ((uintptr_t)in[k] + (uint64_t)P->p.in[k].offset * es) % 16 != 0 ||
+                (P->p.in[k].inner_stride * es) % 16 != 0)
+                colvec = false;
+        } else if (rs != 0) {
+            colvec = false;
+        }
+    }
+    if (colvec) {
+        col_members = RED_COL_THREADS / 32;
+        while (col_members > 1 && sp.inner < (int64_t)col_members * (32 / VEC_RT) * 2) col_members >>= 1;
+    }
     const int block = columnar ? 32 * col_members : RED_THREADS;
     if (columnar) min_blocks = std::max(1, 512 / block);
     int cluster = 1;
     if (columnar) {
         const int64_t groups = (sp.rows + 31) / 32;
-        while (cluster < 8 && groups * cluster * 2 <= (int64_t)num_sms() &&
-               sp.chunks >= (int64_t)col_members * cluster * 2 * RED_COL_MIN_CHUNKS)
+        auto deep_enough = [&](int c) {  // every member still keeps two cells (chunks) of the reduced axis
+            return colvec ? sp.inner >= (int64_t)col_members * (32 / VEC_RT) * c * 2
+                          : sp.chunks >= (int64_t)col_members * c * 2 * RED_COL_MIN_CHUNKS;
+        };
+        while (cluster < 8 && groups * cluster * 2 <= (int64_t)num_sms() && deep_enough(cluster))
             cluster *= 2;
     }
     P->cluster = cluster;
@@ -305,6 +335,9 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     spec += "constexpr int kInSize[] = " + int_list(in_size, n_in) + ";\n";
     spec += "constexpr int kPerRow = " + std::to_string(per_row ? 1 : 0) + ";\n";
     spec += "constexpr int kColumnar = " + std::to_string(columnar ? 1 : 0) + ";\n";
+    spec += "constexpr int kColVec = " + std::to_string(colvec ? 1 : 0) + ";\n";
+    spec += "constexpr int kVecRT = " + std::to_string(VEC_RT) + ";\n";
+    spec += "constexpr int kVecRow[] = " + int_list(vec_row, n_in) + ";\n";
     spec += "constexpr int kBlockThreads = " + std::to_string(block) + ";\n";
     spec += "constexpr int kCluster = " + std::to_string(cluster) + ";\n";
     spec += "constexpr int kStreamUnroll = " + std::to_string(columnar ? 4 : 1) + ";\n";

@@ -364,6 +364,7 @@ class Executor:
         self.users = {}
         self.user_nodes = {}
         self.narrow = {}
+        self.copies = {}
 
     def prepare(self, roots):
         """Count, for every unrealized node reachable from roots, how many
@@ -382,6 +383,7 @@ class Executor:
         self.users = users
         self.user_nodes = nodes
         self.narrow = {}
+        self.copies = {}
 
     def _only_cast_to(self, x, dt, depth=0):
         """True when every use of x (through movements) is a CAST to dt."""
@@ -526,8 +528,18 @@ class Executor:
             v = nv
         return buf, v
 
-    def _copy_contig(self, buf, v, dtype):
+    def _copy_contig(self, buf, v, dtype, fresh=False):
+        # the same cells of the same buffer are copied once per schedule (an
+        # expanded table reshaped for several consumers, say); the entry holds
+        # the source, so its memory cannot be reused under the key meanwhile.
+        # fresh: a copy of its own, for a caller that writes into it
+        key = (buf.data_ptr(), v.key(), dtype)
+        hit = None if fresh else self.copies.get(key)
+        if hit is not None and hit[0] is buf:
+            return hit[1], View(v.shape)
         out = self._new(v.shape, dtype)
+        if not fresh:
+            self.copies[key] = (buf, out)
         if out.numel():
             A.psg_permute(buf, self._pview(buf, v, dtype), list(range(len(v.shape))), out,
                           self._pview(out, View(v.shape), dtype), stream=self._s())
@@ -1032,7 +1044,7 @@ class Executor:
 
     def _realize_scatter(self, t: Tensor):
         dst, idx, upd = t.src
-        out, vo = self._copy_contig(*self.realize(dst), dst.dtype)
+        out, vo = self._copy_contig(*self.realize(dst), dst.dtype, fresh=True)  # scatter-added in place
         bi, vi = self.realize(idx)
         if not vi.contiguous():
             bi, vi = self._copy_contig(bi, vi, "i32")
@@ -1111,7 +1123,7 @@ def realize_all(*ts):
     for t in ts:
         buf, v = ex.realize(t)
         if v.mask is not None:
-            buf, v = ex._copy_contig(buf, v, t.dtype)
+            buf, v = ex._copy_contig(buf, v, t.dtype, fresh=True)
         out.append(_as_torch(buf, v, t.dtype))
     return out
 

@@ -219,7 +219,8 @@ def test_per_row_epilogue_and_tiny_graph_tail(A, O, PR):
 # ---- reductions over a leading axis (the columnar layout) -------------------
 
 @pytest.mark.parametrize("rows,k,dt", [(512, 8192, "f32"), (512, 4096, "bf16"), (100, 37, "f32"),
-                                       (33, 1000, "bf16"), (1000, 3, "f32")])
+                                       (33, 1000, "bf16"), (1000, 3, "f32"),
+                                       (40, 777, "bf16"), (8, 20000, "f32"), (2056, 300, "bf16")])
 def test_column_sum_weighted(A, O, rows, k, dt):
     """out[c] = sum_r dy[r, c] * x[r, c] * w[r] over a row-major [k, rows]
     pair (an RMSNorm weight's gradient): within the SUM bound of the
