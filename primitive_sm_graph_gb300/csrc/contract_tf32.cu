@@ -89,28 +89,39 @@ __device__ __forceinline__ void convert_tile(const float* __restrict__ raw, uint
                                              int ct)
 {
     constexpr int NT = CONV_WARPS * 32;
+    constexpr int NJ = (128 * 8) / NT;
+    // explicit shared-memory loads and stores (the tiles are shared memory;
+    // a generic access would take the slower generic path), every load of
+    // the thread issued before the first split
+    const uint32_t rs = smem_u32(raw), hs = smem_u32(hi_t), ls = smem_u32(lo_t);
+    float x[NJ][4];
 #pragma unroll
-    for (int j = 0; j < (128 * 8) / NT; ++j) {
+    for (int j = 0; j < NJ; ++j) {
         const int i = ct + NT * j;
-        int r, c;
-        float x[4];
         if (kmajor) {
-            r = i >> 3;
-            c = i & 7;
-            const float4 v = *(const float4*)(raw + r * BKF + c * 4);
-            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(x[j][0]), "=f"(x[j][1]), "=f"(x[j][2]), "=f"(x[j][3])
+                         : "r"(rs + (uint32_t)(((i >> 3) * BKF + (i & 7) * 4) * 4)));
         } else {
-            r = i & 127;
-            c = i >> 7;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) x[q] = raw[(c * 4 + q) * 128 + r];
+            for (int q = 0; q < 4; ++q)
+                asm volatile("ld.shared.f32 %0, [%1];"
+                             : "=f"(x[j][q])
+                             : "r"(rs + (uint32_t)((((i >> 7) * 4 + q) * 128 + (i & 127)) * 4)));
         }
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        const int i = ct + NT * j;
+        const int r = kmajor ? i >> 3 : i & 127, c = kmajor ? i & 7 : i >> 7;
         float h[4], l[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) split1(x[q], h[q], l[q]);
-        const int off = r * 128 + ((c ^ (r & 7)) << 4);
-        *(float4*)(hi_t + off) = make_float4(h[0], h[1], h[2], h[3]);
-        *(float4*)(lo_t + off) = make_float4(l[0], l[1], l[2], l[3]);
+        for (int q = 0; q < 4; ++q) split1(x[j][q], h[q], l[q]);
+        const uint32_t off = (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(hs + off), "f"(h[0]), "f"(h[1]), "f"(h[2]), "f"(h[3])
+                     : "memory");
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ls + off), "f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3])
+                     : "memory");
     }
 }
 
