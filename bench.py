@@ -573,6 +573,26 @@ class Rows:
         e1.record()
         torch.cuda.synchronize()
         r["graph_replay_us"] = round(e0.elapsed_time(e1) / n * 1e3, 3)
+        # device time per realize: 20 realizes recorded in one CUDA Graph, so
+        # the host's graph-launch call is paid once per 20 (one replay above is
+        # bounded by that call)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            once()
+        torch.cuda.current_stream().wait_stream(side)
+        g20 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g20):
+            for _ in range(20):
+                once()
+        g20.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(10):
+            g20.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        r["graph_device_us"] = round(e0.elapsed_time(e1) / 200 * 1e3, 3)
         return r
 
     # C5: one forward + backward of the GPT block through the graph layer
