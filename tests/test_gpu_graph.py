@@ -195,3 +195,55 @@ def test_gpt_block_full_size(O):
     import os
     lg, errs = _gpt_compare(O, **SI.GPT_SHAPES, seed=0, nthreads=os.cpu_count(), same_relu_mask=True)
     assert abs(lg - math.log(256)) < 0.5, lg
+
+
+def test_gpt_step_contractions_write_half_width(G):
+    """Every contraction of the GPT block step is read only through a CAST to
+    bfloat16, so each one is stored in bfloat16 by its own epilogue (no
+    float32 contraction output, and no contraction computed twice)."""
+    from primitive_sm_graph_gb300.workloads import gpt_step
+    tok, w = SI.gpt_block(6, 2, 64, 128, 128, 2, 256)
+    dev = {k: v.cuda() for k, v in w.items()}
+    log = _fresh_log(G)
+    gpt_step(tok.cuda(), dev, 2)
+    torch.cuda.synchronize()
+    cons = [e for e in log if e[0] == "contract"]
+    assert len(cons) == 15, cons        # 5 forward, 5 input gradients, 5 weight gradients
+    assert all(e[3] == "bf16" for e in cons), cons
+
+
+_PDL_SCRIPT = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+import seeded_inputs as SI
+from primitive_sm_graph_gb300.workloads import gpt_step, GPT_WEIGHTS
+tok, w = SI.gpt_block(7, 4, 128, 256, 128, 2, 256)
+loss, grads = gpt_step(tok.cuda(), {k: v.cuda() for k, v in w.items()}, 2)
+torch.cuda.synchronize()
+torch.save({"loss": loss.cpu(), **{k: grads[k].cpu() for k in GPT_WEIGHTS}}, sys.argv[2])
+"""
+
+
+def test_gpt_step_same_bits_without_dependent_launches(tmp_path):
+    """Every kernel waits on griddepcontrol.wait before it touches memory, so
+    letting launches overlap their predecessor's tail changes no result: the
+    GPT block step gives the same bits with programmatic stream
+    serialization on (the default) and off (PSG_NO_PDL), each in a process
+    of its own."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for off in (False, True):
+        env = dict(os.environ)
+        env.pop("PSG_NO_PDL", None)
+        if off:
+            env["PSG_NO_PDL"] = "1"
+        f = str(tmp_path / ("nopdl.pt" if off else "pdl.pt"))
+        subprocess.run([sys.executable, "-c", _PDL_SCRIPT, root, f], check=True, env=env, timeout=600)
+        outs.append(torch.load(f))
+    for k in outs[0]:
+        a, b = outs[0][k], outs[1][k]
+        iv = torch.int16 if a.element_size() == 2 else torch.int32
+        assert torch.equal(a.view(iv), b.view(iv)), k
