@@ -17,6 +17,7 @@ struct TcParams {
     int32_t* status;
     int64_t c_offset, c_rs, c_cs, c_bs;
     int tma_store;              // 1: the epilogue writes C (or the partials) through a tensor map
+    int reduce_quad;            // split-K reduce: 1 when C's rows take 4-cell vector moves
 };
 
 struct TcOperands {

@@ -558,13 +558,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 // C = sum over the splits, in split order, of the float32 partials, rounded
-// once into C's dtype
+// once into C's dtype.  With p.reduce_quad (every row of C contiguous and
+// 4-cell aligned: N % 4 == 0, unit column stride, 16-byte aligned partials)
+// a thread adds four adjacent cells with 16-byte loads and divides its index
+// once per four cells.
 __global__ void __launch_bounds__(256) splitk_reduce(const __grid_constant__ TcParams p)
 {
     pdl_enter();
     const int64_t cells = (int64_t)p.batch * p.M * p.N;
     const int64_t stride = cells;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < cells; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    if (p.reduce_quad) {
+        const int64_t nq = p.N / 4, quads = cells / 4;
+        for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < quads; q += step) {
+            const int64_t bm = q / nq;
+            const int64_t n = (q - bm * nq) * 4, e = q * 4;
+            float4 acc = *(const float4*)(p.ws + e);
+            for (int s = 1; s < p.splits; ++s) {
+                const float4 v = *(const float4*)(p.ws + e + s * stride);
+                acc.x = __fadd_rn(acc.x, v.x);
+                acc.y = __fadd_rn(acc.y, v.y);
+                acc.z = __fadd_rn(acc.z, v.z);
+                acc.w = __fadd_rn(acc.w, v.w);
+            }
+            const int64_t m = bm % p.M, b = bm / p.M;
+            const int64_t o = p.c_offset + b * p.c_bs + m * p.c_rs + n;
+            if (p.c_dtype == PSG_F32) {
+                *(float4*)((float*)p.C + o) = acc;
+            } else if (p.c_dtype == PSG_F16) {
+                const __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+                *(uint2*)((__half*)p.C + o) = make_uint2(*(const uint32_t*)&lo, *(const uint32_t*)&hi);
+            } else {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+                *(uint2*)((__nv_bfloat16*)p.C + o) = make_uint2(*(const uint32_t*)&lo, *(const uint32_t*)&hi);
+            }
+        }
+        return;
+    }
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < cells; e += step) {
         float acc = p.ws[e];
         for (int s = 1; s < p.splits; ++s) acc = __fadd_rn(acc, p.ws[e + s * stride]);
         const int64_t n = e % p.N, bm = e / p.N, m = bm % p.M, b = bm / p.M;
@@ -573,6 +604,20 @@ __global__ void __launch_bounds__(256) splitk_reduce(const __grid_constant__ TcP
         else if (p.c_dtype == PSG_F16) ((__half*)p.C)[o] = __float2half_rn(acc);
         else ((__nv_bfloat16*)p.C)[o] = __float2bfloat16_rn(acc);
     }
+}
+
+// launch of splitk_reduce: the quad path when C's rows allow it
+void launch_splitk_reduce(TcParams p, void* stream)
+{
+    const int es = dtype_size(p.c_dtype);
+    const bool quad = p.N % 4 == 0 && p.c_cs == 1 && ((uintptr_t)p.ws & 15) == 0 &&
+                      (((uintptr_t)p.C + (uint64_t)p.c_offset * es) % (4 * es)) == 0 && (p.c_rs * es) % (4 * es) == 0 &&
+                      (p.batch == 1 || (p.c_bs * es) % (4 * es) == 0);
+    p.reduce_quad = quad ? 1 : 0;
+    const int64_t cells = (int64_t)p.batch * p.M * p.N;
+    const int64_t work = quad ? cells / 4 : cells;
+    const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, (int64_t)num_sms() * 8));
+    launch(splitk_reduce, rgrid, 256, 0, (cudaStream_t)stream, p);
 }
 
 // 3-D tensor map over a bf16 or f16 operand: dims {inner, outer, batch}.
@@ -716,11 +761,7 @@ psg_status launch_pair(const TcOperands& o, TcParams p, int64_t a_bs, int64_t b_
     const int64_t units = (int64_t)p.num_m * p.num_n * p.batch * p.splits;
     const int clusters = (int)std::min<int64_t>(units, pair_clusters());
     launch(tc_gemm2, 2 * clusters, THREADS, P_SMEM_BYTES, (cudaStream_t)stream, ma, mb, mc, p);
-    if (p.splits > 1) {
-        const int64_t cells = (int64_t)p.batch * p.M * p.N;
-        const int rgrid = (int)std::min<int64_t>((cells + 255) / 256, (int64_t)num_sms() * 8);
-        launch(splitk_reduce, rgrid, 256, 0, (cudaStream_t)stream, p);
-    }
+    if (p.splits > 1) launch_splitk_reduce(p, stream);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
@@ -766,11 +807,7 @@ psg_status launch_contract_tc(const TcOperands& o, void* stream)
     const int64_t units = (int64_t)p.num_m * p.num_n * p.batch * p.splits;
     const int grid = (int)std::min<int64_t>(units, num_sms());
     launch(tc_gemm, grid, THREADS, SMEM_BYTES, (cudaStream_t)stream, ma, mb, mc, p);
-    if (p.splits > 1) {
-        const int64_t cells = (int64_t)p.batch * p.M * p.N;
-        const int rgrid = (int)std::min<int64_t>((cells + 255) / 256, (int64_t)num_sms() * 8);
-        launch(splitk_reduce, rgrid, 256, 0, (cudaStream_t)stream, p);
-    }
+    if (p.splits > 1) launch_splitk_reduce(p, stream);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
