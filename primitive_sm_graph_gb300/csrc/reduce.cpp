@@ -224,6 +224,15 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
         const int64_t tms = RED_THREADS >> tw;  // its smallest ring must fit, else keep tl
         if (((tms * 4 * 8 + 127) / 128 * 128) + tms * 2 * stage_bytes <= RED_SMEM_MAX) tl = tw;
     }
+    // a staged row set too wide for a 2-slot ring per team at this team size
+    // (many inputs a row): larger teams, fewer of them a block, until the ring
+    // fits RED_SMEM_PREF or a team has one chunk a thread.  (Measured on the
+    // GPT block's 4-stage RMSNorm backward, 7 inputs over 512-cell rows:
+    // without this the rows streamed from global memory once per stage.)
+    auto bar_for = [](int64_t tms) { return (tms * 4 * 8 + 127) / 128 * 128; };
+    while (staged && tl < RED_MAX_TEAM_LOG2 && ((int64_t)1 << tl) < sp.chunks &&
+           bar_for(RED_THREADS >> tl) + (int64_t)(RED_THREADS >> tl) * 2 * stage_bytes > RED_SMEM_PREF)
+        ++tl;
     const int T = 1 << tl;
     const int64_t ch_per = (sp.chunks + T - 1) / T > 0 ? (sp.chunks + T - 1) / T : 1;
     if (ch_per > RED_STAGED_MAX_CHUNKS) staged = false;
