@@ -1044,7 +1044,17 @@ class Executor:
 
     def _realize_scatter(self, t: Tensor):
         dst, idx, upd = t.src
-        out, vo = self._copy_contig(*self.realize(dst), dst.dtype, fresh=True)  # scatter-added in place
+        out = None
+        if (dst._real is None and self.users.get(id(dst), 0) == 1 and dst.op in ELEMENTWISE
+                and self._narrowable(dst) is None):  # a narrowed contraction's buffer may be shared
+            # a value computed for this scatter alone (a zero-filled gradient
+            # buffer, say): scatter into its own fresh buffer, no copy
+            buf, vd = self.realize(dst)
+            if vd.mask is None and vd.offset == 0 and vd.contiguous():
+                out, vo = buf, vd
+                dst._real = None  # the buffer now holds the scatter's result, not dst's value
+        if out is None:
+            out, vo = self._copy_contig(*self.realize(dst), dst.dtype, fresh=True)  # scatter-added in place
         bi, vi = self.realize(idx)
         if not vi.contiguous():
             bi, vi = self._copy_contig(bi, vi, "i32")
