@@ -733,7 +733,35 @@ class Executor:
                 return None
         return order
 
+    def _store_shared_row_values(self, t: Tensor):
+        """Per-row values inside t's expression (shape [.., 1], computed from
+        reductions) that are shared and heavy and also used outside t (a
+        norm's 1/rms, read again by the backward) are stored first, so the
+        fused call reads them instead of recomputing them, and the other
+        users do not recompute the reduction either."""
+        inner, order, seen = {}, [], set()
+        stack = [t]
+        while stack:
+            x = stack.pop()
+            if id(x) in seen or x._real is not None:
+                continue
+            seen.add(id(x))
+            order.append(x)
+            if x.op in ELEMENTWISE or (x.op == "MOVE" and x.arg[0] != "pad"):
+                for y in x.src:
+                    inner[id(y)] = inner.get(id(y), 0) + 1
+                    stack.append(y)
+        for x in order:
+            if (x is not t and x.op in ELEMENTWISE and x._real is None and len(x.shape) >= 1 and x.shape[-1] == 1
+                    and self.users.get(id(x), 0) > inner.get(id(x), 0) and self._shared_heavy(x)
+                    and self._collect_reds(x)):
+                self.realize(x)
+
     def _try_fused_reduce(self, t: Tensor):
+        found = self._collect_reds(t)
+        if not found:
+            return None
+        self._store_shared_row_values(t)
         found = self._collect_reds(t)
         if not found:
             return None
