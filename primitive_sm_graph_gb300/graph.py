@@ -770,13 +770,16 @@ class Executor:
             return None
         row_shape = rows.pop()
         per_elem = t.shape == row_shape
-        per_row = t.shape == row_shape[:-1] + (1,)
+        # one value per row: [.., 1], or any shape of that many cells that
+        # the per-row values reach through movements that keep the row-major
+        # order (a reshape, a permute of size-1 dims), so cell i is row i
+        per_row = not per_elem and prod(t.shape) == prod(row_shape[:-1])
         if not (per_elem or per_row):
             return None
         for r, mv in found.values():
             if per_elem and not _is_row_expand(mv, r.shape, row_shape):
                 return None
-            if per_row and any(m[0] != "detach" for m in mv):
+            if per_row and not _keeps_row_order(mv, r.shape, t.shape):
                 return None
         order = self._stage_order([r for r, _ in found.values()], row_shape)
         if order is None or len(order) > 4:
@@ -1093,6 +1096,21 @@ class Executor:
                           ws.numel(), self._status(), stream=self._s())
         self.log.append(("scatter_add", t.shape, n))
         return out, vo
+
+
+def _keeps_row_order(moves, shape, out_shape) -> bool:
+    """True when the movements take a contiguous View of `shape` to a
+    contiguous View of `out_shape` (cell i stays cell i)."""
+    v = View(tuple(shape))
+    for kind, arg in moves:
+        if kind == "detach":
+            continue
+        if kind not in ("reshape", "permute"):
+            return False
+        v = getattr(v, kind)(arg)
+        if v is None:
+            return False
+    return tuple(v.shape) == tuple(out_shape) and v.contiguous()
 
 
 class _TooBig(Exception):
