@@ -3,8 +3,9 @@
 // The tiled-matmul shape of limn's cuda device ("Backends": a block per
 // output tile, both operands staged through shared memory, a patch of cells
 // per thread in registers, the reduce axis walked in order).  Block tile
-// 128x128, K slices of 8, 256 threads with an 8x8 register patch each; the
-// View's strides are honoured for any layout.  Each output is one float32
+// 128x128, K slices of 16 (a short K, the case this kernel serves, takes
+// few waits for its loads), 256 threads with an 8x8 register patch each;
+// the View's strides are honoured for any layout.  Each output is one float32
 // total over k in ascending order (multiply-adds may contract into FMA; the
 // result is bounded by the reduction-order term like any SUM).
 #include <cuda_bf16.h>
@@ -18,7 +19,7 @@ namespace psg {
 
 namespace {
 
-constexpr int TM = 128, TN = 128, TK = 8, NT = 256;
+constexpr int TM = 128, TN = 128, TK = 16, NT = 256;
 
 template <int DT>
 __device__ __forceinline__ float ld(const void* p, int64_t o)
