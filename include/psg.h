@@ -35,6 +35,13 @@
  *   code; no call silently runs a different implementation (Tiki, "Compile
  *   model code": unsupported contracts raise a typed error).
  * Thread safety: calls may be made from several host threads at once.
+ * Launches: every kernel is launched with programmatic stream serialization
+ *   and waits (griddepcontrol.wait) for the kernel before it on the stream
+ *   before touching memory, so a launch overlaps only its predecessor's tail;
+ *   results are the same bits either way.  Environment: PSG_NO_PDL (any
+ *   value, read once) launches without the attribute; PSG_GEMM_KERNEL=single
+ *   or =pair picks the bf16/f16 contraction kernel (single CTA or CTA pair)
+ *   where both apply.
  */
 #ifndef PSG_H
 #define PSG_H
