@@ -215,15 +215,26 @@ psg_status psg_permute(const void* in, const psg_view* in_v, const int32_t* perm
  *     C[b.., m, n] = sum_{k ascending in the reference} Av[b.., m, n, k] * Bv[b.., m, n, k]
  * Av, Bv: views of rank 3..6 with shape [batch.., M, N, K]; Av's stride along
  *   N must be 0 and Bv's stride along M must be 0 (A broadcast over n, B over
- *   m), batch strides are free; unmasked.  Cv: shape [batch.., M, N] (or with
- *   a trailing 1), injective.
+ *   m), batch strides are free.  Cv: shape [batch.., M, N] (or with a
+ *   trailing 1), injective.
+ * Masks (padded operands) are allowed on Av and Bv: a masked element is a
+ *   zero factor.  A's mask along m and k and B's along n and k zero the
+ *   loaded factor (so 0 * inf is NaN, as in the broadcast product); a mask
+ *   across the other operand's broadcast axis (A's along n, B's along m) or
+ *   along a batch dim writes the cell 0, which is the sum of its zero
+ *   products whenever the other operand is finite.  Masked operands take the
+ *   FP32-pipe kernel (a masked batch dim: one launch per batch index).
  * dtypes: A and B of one type: PSG_BF16 or PSG_F16 (tensor cores, float32
  *   accumulate in TMEM, exact products) or PSG_F32 (K >= 256 and 16-byte
  *   aligned operands: tensor cores as 3xTF32, hi*hi + hi*lo + lo*hi with a
  *   few 2^-20 relative error per product; otherwise float32 FMA on the FP32
- *   pipes); C PSG_F32, PSG_BF16 or PSG_F16 (rounded once, RNE).  Operands the
+ *   pipes); C PSG_F32, PSG_BF16 or PSG_F16 (rounded once, RNE).  PSG_F64
+ *   operands sum in float64 in k order into a PSG_F64 C.  PSG_I32 / PSG_I16 /
+ *   PSG_I8 operands sum in uint32 with wraparound into an integer C of any
+ *   of those widths (stored modulo 2^width: the ints wrap).  Operands the
  *   tensor cores cannot address (strides not 16-byte multiples, several
- *   batch dims that do not merge) take the FP32-pipe kernel.
+ *   batch dims that do not merge) take the FP32-pipe kernel.  Any other
+ *   dtype pairing returns PSG_E_UNSUPPORTED_DTYPE.
  * The total deviates from the sequential float32 loop by at most
  * 2 * gamma_{K-1} * sum_k |a_k b_k| (Litmus, "ToleranceBound"); for the
  * 3xTF32 path that bound absorbs the product error at the K it is used at.

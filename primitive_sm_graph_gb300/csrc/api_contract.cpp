@@ -1,6 +1,7 @@
 // psg_contract: matmul as SUM over the last dim of MUL(Av, Bv).  The roles of
 // the dims come from the Views themselves: Av is broadcast along n (stride 0)
 // and Bv along m, exactly the two stride-0 loops of the broadcast form.
+#include <algorithm>
 #include <cstring>
 
 #include "api_internal.h"
@@ -14,7 +15,28 @@ namespace {
 struct Batch {
     int nb;                       // batch dims kept (after dropping size 1)
     int64_t shape[MAXD], sa[MAXD], sb[MAXD], sc[MAXD];
+    bool masked;                  // a batch dim is masked: every dim kept, one launch per index
+    int64_t lo[MAXD], hi[MAXD];   // the window both operands read along each batch dim
 };
+
+// [lo, hi): the indices of dim d a View reads (its mask clipped to the shape)
+void window(const psg_view* v, int d, int64_t& lo, int64_t& hi)
+{
+    lo = std::max<int64_t>(v->mask_lo[d], 0);
+    hi = std::min<int64_t>(v->mask_hi[d], v->shape[d]);
+    if (hi < lo) hi = lo;
+}
+
+// true when some dim's window is empty: the View reads nothing at all
+bool reads_nothing(const psg_view* v)
+{
+    for (int d = 0; d < v->ndim; ++d) {
+        int64_t lo, hi;
+        window(v, d, lo, hi);
+        if (hi == lo) return true;
+    }
+    return false;
+}
 
 // Merge batch dims that are contiguous for A, B and C alike.
 void collapse_batch(Batch& B)
@@ -57,7 +79,7 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
     st = check_view(Cv, true);
     if (st != PSG_OK) return st;
     if (!same_shape(Av, Bv)) return PSG_E_INVALID_ARG;
-    if (view_has_mask(Av) || view_has_mask(Bv)) return PSG_E_UNSUPPORTED_LAYOUT;
+    const bool masked = view_has_mask(Av) || view_has_mask(Bv);
     const int dm = r - 3, dn = r - 2, dk = r - 1;
     const int64_t M = Av->shape[dm], N = Av->shape[dn], K = Av->shape[dk];
     // the broadcast form: A constant along n, B constant along m
@@ -69,21 +91,32 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
         if (Cv->shape[d] != Av->shape[d]) return PSG_E_INVALID_ARG;
     const int adt = Av->dtype, cdt = Cv->dtype;
     if (Bv->dtype != adt) return PSG_E_UNSUPPORTED_DTYPE;
-    if (adt != PSG_BF16 && adt != PSG_F16 && adt != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
-    if (cdt != PSG_BF16 && cdt != PSG_F16 && cdt != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
+    auto is_float = [](int t) { return t == PSG_BF16 || t == PSG_F16 || t == PSG_F32; };
+    auto is_int = [](int t) { return t == PSG_I32 || t == PSG_I16 || t == PSG_I8; };
+    // float32-accumulated floats store to any of them; float64 to float64;
+    // the integers (uint32 wraparound total) to any integer width
+    if (!((is_float(adt) && is_float(cdt)) || (adt == PSG_F64 && cdt == PSG_F64) || (is_int(adt) && is_int(cdt))))
+        return PSG_E_UNSUPPORTED_DTYPE;
     const int64_t numel = M * N * K;
     if (numel > 0 && (!A || !Bp)) return PSG_E_INVALID_ARG;
     if (M * N > 0 && !C) return PSG_E_INVALID_ARG;
     if (!ptr_aligned(A, adt) || !ptr_aligned(Bp, adt) || !ptr_aligned(C, cdt)) return PSG_E_MISALIGNED;
     if (M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return PSG_E_UNSUPPORTED_LAYOUT;
     bt->nb = r - 3;
+    bt->masked = false;
     for (int d = 0; d < bt->nb; ++d) {
         bt->shape[d] = Av->shape[d];
         bt->sa[d] = Av->strides[d];
         bt->sb[d] = Bv->strides[d];
         bt->sc[d] = Cv->strides[d];
+        int64_t alo, ahi, blo, bhi;
+        window(Av, d, alo, ahi);
+        window(Bv, d, blo, bhi);
+        bt->lo[d] = std::max(alo, blo);
+        bt->hi[d] = std::max(bt->lo[d], std::min(ahi, bhi));
+        if (bt->lo[d] > 0 || bt->hi[d] < bt->shape[d]) bt->masked = true;
     }
-    collapse_batch(*bt);
+    if (!bt->masked) collapse_batch(*bt);
     const int64_t a_ms = Av->strides[dm], a_ks = Av->strides[dk];
     const int64_t b_ns = Bv->strides[dn], b_ks = Bv->strides[dk];
     const int64_t c_ms = Cv->strides[dm], c_ns = Cv->strides[dn];
@@ -93,7 +126,8 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
     // MMAs per term; shorter K keeps the exact-product FP32-pipe kernel,
     // whose only error is the reduction order)
     constexpr int64_t TF32X3_MIN_K = 256;
-    bool tc = (adt == PSG_BF16 || adt == PSG_F16 || (adt == PSG_F32 && K >= TF32X3_MIN_K)) && bt->nb <= 1 && K > 0;
+    bool tc = (adt == PSG_BF16 || adt == PSG_F16 || (adt == PSG_F32 && K >= TF32X3_MIN_K)) && bt->nb <= 1 && K > 0 &&
+              !masked;
     const int es = dtype_size(adt), q16 = 16 / es;  // elements per 16 bytes
     auto tma_ok = [&](const void* base, int64_t off, int64_t s_mn, int64_t s_k, int64_t mn, int64_t s_b, bool& kmaj) {
         if (s_k == 1 && s_mn % q16 == 0 && s_mn >= K) kmaj = true;
@@ -153,6 +187,17 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
     S->c_ms = c_ms;
     S->c_ns = c_ns;
     S->c_bs = bt->nb == 1 ? bt->sc[0] : 0;
+    // read windows and the window of cells that are not zero by a mask
+    window(Av, dm, S->a_mlo, S->a_mhi);
+    window(Av, dk, S->a_klo, S->a_khi);
+    window(Bv, dn, S->b_nlo, S->b_nhi);
+    window(Bv, dk, S->b_klo, S->b_khi);
+    window(Bv, dm, S->c_mlo, S->c_mhi);
+    window(Av, dn, S->c_nlo, S->c_nhi);
+    // a View with an empty window along any dim reads nothing (and its
+    // offset is unchecked): it loads no element at all
+    if (reads_nothing(Av)) S->a_mlo = S->a_mhi = 0;
+    if (reads_nothing(Bv)) S->b_nlo = S->b_nhi = 0;
     return PSG_OK;
 }
 
@@ -174,27 +219,28 @@ psg_status contract_impl(const void* A, const psg_view* Av, const void* B, const
     T.ws = ws;
     T.ws_bytes = ws_bytes;
     if (S.M == 0 || S.N == 0) return PSG_OK;
-    if (S.K == 0) {
-        // an empty SUM is its identity: every cell 0 (through the SIMT kernel)
-        return launch_contract_simt(S, stream);
-    }
-    if (bt.nb <= 1) {
+    // (an empty SUM, K == 0, is its identity: every cell 0 through the SIMT kernel)
+    if (bt.nb <= 1 && !bt.masked) {
         if (!tc) return launch_contract_simt(S, stream);
         return S.ab_dtype == PSG_F32 ? launch_contract_tf32(T, stream) : launch_contract_tc(T, stream);
     }
-    // several batch dims that do not merge: one launch per batch index
+    // several batch dims that do not merge, or a masked batch dim: one launch
+    // per batch index (an index outside a batch window reads nothing, writes 0)
     int64_t count = 1;
     for (int d = 0; d < bt.nb; ++d) count *= bt.shape[d];
     for (int64_t i = 0; i < count; ++i) {
         int64_t rem = i, oa = 0, ob = 0, oc = 0;
+        bool inside = true;
         for (int d = bt.nb - 1; d >= 0; --d) {
             const int64_t x = rem % bt.shape[d];
             rem /= bt.shape[d];
             oa += x * bt.sa[d];
             ob += x * bt.sb[d];
             oc += x * bt.sc[d];
+            inside = inside && (!bt.masked || (x >= bt.lo[d] && x < bt.hi[d]));
         }
         SimtParams s1 = S;
+        if (!inside) s1.a_mlo = s1.a_mhi = s1.b_nlo = s1.b_nhi = s1.c_mlo = s1.c_mhi = 0;
         s1.a_off += oa;
         s1.b_off += ob;
         s1.c_off += oc;

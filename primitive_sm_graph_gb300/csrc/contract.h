@@ -39,6 +39,12 @@ struct SimtParams {
     int64_t a_off, a_ms, a_ks, a_bs;
     int64_t b_off, b_ns, b_ks, b_bs;
     int64_t c_off, c_ms, c_ns, c_bs;
+    // read windows (masks clipped to the shape; empty when the operand reads
+    // nothing): A along m and k, B along n and k; cells outside the c window
+    // (B's m mask, A's n mask, a batch mask) are written 0
+    int64_t a_mlo, a_mhi, a_klo, a_khi;
+    int64_t b_nlo, b_nhi, b_klo, b_khi;
+    int64_t c_mlo, c_mhi, c_nlo, c_nhi;
 };
 
 psg_status launch_contract_tc(const TcOperands& o, void* stream);

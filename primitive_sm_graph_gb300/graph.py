@@ -265,14 +265,17 @@ class Tensor:
         """a @ b as SUM over k of MUL of two broadcast Views (limn, "Reading
         the schedule"; Luminal IR blog, "Naive Matrix Multiplication").  Half
         widths widen to float32 first, so the products are exact and the SUM
-        keeps a float32 total; the result rounds once into out_dtype."""
+        keeps a float32 total; the result rounds once into out_dtype.  Two
+        float64 or two same-width integer operands keep their dtype (the
+        integers wrap)."""
         a, b = self, other
         out_dtype = out_dtype or a.dtype
         assert a.shape[-1] == b.shape[-2], (a.shape, b.shape)
         M, K, N = a.shape[-2], a.shape[-1], b.shape[-1]
         batch = broadcast_shapes(a.shape[:-2], b.shape[:-2])
-        af = a.cast("f32") if a.dtype != "f32" else a
-        bf = b.cast("f32") if b.dtype != "f32" else b
+        keep = a.dtype == b.dtype and a.dtype in ("f64", "i32", "i16", "i8")
+        af = a.cast("f32") if a.dtype != "f32" and not keep else a
+        bf = b.cast("f32") if b.dtype != "f32" and not keep else b
         af = af.reshape(a.shape[:-2] + (M, 1, K))
         af = _lead(af, len(batch) + 3).expand(batch + (M, N, K))
         bf = bf.permute(tuple(range(b.ndim - 2)) + (b.ndim - 1, b.ndim - 2)).reshape(b.shape[:-2] + (1, N, K))
@@ -353,6 +356,18 @@ def _inverse(perm):
 
 
 # ------------------------------------------------------------ executor --------
+
+_FLOATS32 = ("bf16", "f16", "f32")
+_INTS = ("i32", "i16", "i8")
+
+
+def _contract_dtypes(ab, c):
+    """The operand / result dtype pairs psg_contract takes: float32-summed
+    floats into any of them, float64 into float64, the integers (wrapping
+    uint32 total) into any integer width."""
+    return ((ab in _FLOATS32 and c in _FLOATS32) or (ab == "f64" and c == "f64")
+            or (ab in _INTS and c in _INTS))
+
 
 class Executor:
     """Cuts the graph into library calls and runs them on the current stream.
@@ -901,7 +916,7 @@ class Executor:
         (x, mx, wx), (y, my, wy) = pat
         dx = wx or x.dtype
         dy = wy or y.dtype
-        if dx != dy or dx not in ("bf16", "f32"):
+        if dx != dy or not _contract_dtypes(dx, out_dtype):
             return None
         S = r.src[0].shape
         bx, vx = self._apply_moves(*self.realize(x), list(mx), x.dtype)
