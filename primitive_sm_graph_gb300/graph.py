@@ -243,6 +243,8 @@ class Tensor:
         O = softmax(scale * Q K^T, keys j > i hidden when causal) V per head."""
         assert self.shape == k.shape == v.shape and len(self.shape) == 4 and self.shape[3] == 64
         assert self.dtype == k.dtype == v.dtype == "bf16"
+        if self.shape[1] > ATTN_MAX_T:
+            return _composed_attention(self, k, v, scale, causal)
         return Tensor("ATTN", (self, k, v), self.shape, "bf16", arg=(float(scale), bool(causal)))
 
     def attention_packed(self, scale: float, causal: bool = True):
@@ -253,6 +255,10 @@ class Tensor:
         dQ, dK, dV back into the packed tensor)."""
         assert len(self.shape) == 5 and self.shape[2] == 3 and self.shape[4] == 64 and self.dtype == "bf16"
         B, T, _, H, hd = self.shape
+        if T > ATTN_MAX_T:
+            q, k, v = (self.shrink(((0, B), (0, T), (i, i + 1), (0, H), (0, hd))).reshape(B, T, H, hd)
+                       for i in range(3))
+            return _composed_attention(q, k, v, scale, causal)
         return Tensor("ATTN", (self,), (B, T, H, hd), "bf16", arg=(float(scale), bool(causal)))
 
     def scatter_add(self, idx: "Tensor", upd: "Tensor"):
@@ -356,6 +362,29 @@ def _inverse(perm):
 
 
 # ------------------------------------------------------------ executor --------
+
+# keys the fused attention kernels hold in one block; longer sequences take
+# the composed form below
+ATTN_MAX_T = 256
+
+
+def _composed_attention(q, k, v, scale, causal):
+    """softmax(scale * Q K^T, keys j > i hidden when causal) V per head as
+    the composed graph (limn, "The op set": the T x T scores the fused node
+    avoids): one contraction for the scores, one fused row reduction for the
+    softmax, one contraction for P V.  The scores and weights are float32, P
+    rounds to bf16 as the second product's operand (as in the fused kernel),
+    and a hidden key gets a bias of -2^100, whose weight exp underflows to
+    exactly 0 (every causal row keeps its own key)."""
+    B, T, H, hd = q.shape
+    qh, kh, vh = (x.permute(0, 2, 1, 3) for x in (q, k, v))  # [B, H, T, hd]
+    s = qh.matmul(kh.permute(0, 1, 3, 2), "f32") * float(scale)
+    if causal:
+        hide = torch.triu(torch.full((T, T), -2.0 ** 100, dtype=torch.float32), diagonal=1)
+        s = s + Tensor.from_torch(hide.to("cuda"))
+    p = s.softmax(-1).cast("bf16")
+    return p.matmul(vh, "bf16").permute(0, 2, 1, 3)
+
 
 _FLOATS32 = ("bf16", "f16", "f32")
 _INTS = ("i32", "i16", "i8")

@@ -113,3 +113,44 @@ def test_attention_rejects_unsupported_shapes(A):
     y = torch.empty((1, 16, 1, 32), dtype=torch.bfloat16, device="cuda")
     w = A.view_of(y)
     assert A.psg_attention_fwd(y, w, y, w, y, w, y, w, lse, 0.125, True, check=False) == A.E_UNSUPPORTED_LAYOUT
+
+
+@pytest.mark.parametrize("T,causal", [(384, True), (300, False)])
+def test_long_sequence_attention_composes(T, causal):
+    """Past one key block (T > 256) the graph's attention is the composed
+    form (score contraction, fused softmax, P V contraction); forward and the
+    three gradients meet the same bars as the fused kernels."""
+    from primitive_sm_graph_gb300 import graph as G
+    B, H, scale = 1, 2, 0.125
+    g = SI.gen(T)
+    qkv = SI.normal((B, T, 3, H, 64), 0, 1, g, torch.bfloat16)
+    do = SI.normal((B, T, H, 64), 0, 1, g, torch.bfloat16)
+    ex = G._executor()
+    ex.log.clear()
+    x = G.Tensor.from_torch(qkv.cuda(), requires_grad=True)
+    o = x.attention_packed(scale, causal)
+    o.backward(G.Tensor.from_torch(do.cuda()))
+    o_t, dx = G.realize_all(o, x.grad)
+    assert not any(e[0].startswith("attention") for e in ex.log) and any(e[0] == "contract" for e in ex.log)
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    Q, K, V, dO = _heads(q), _heads(k), _heads(v), _heads(do)
+    O_ref, L_ref = attention_fwd(Q, K, V, scale, causal)
+    dq_ref, dk_ref, dv_ref = attention_bwd(Q, K, V, O_ref, dO, L_ref, scale, causal)
+    vis = np.tril(np.ones((T, T), bool)) if causal else np.ones((T, T), bool)
+    mo, mq, mk, mv = (np.zeros_like(Q) for _ in range(4))
+    for h in range(Q.shape[0]):
+        P = np.where(vis, np.exp(scale * Q[h] @ K[h].T - L_ref[h][:, None]), 0.0)
+        mo[h] = P @ np.abs(V[h])
+        dP = dO[h] @ V[h].T
+        D = (dO[h] * O_ref[h]).sum(1)
+        Gm = np.abs(P) * (np.abs(dP) + np.abs(D)[:, None])
+        mv[h] = P.T @ np.abs(dO[h])
+        mq[h] = scale * (Gm @ np.abs(K[h]))
+        mk[h] = scale * (Gm.T @ np.abs(Q[h]))
+    dxc = dx.cpu()
+    for name, got, ref, mag, c in (("o", o_t.cpu(), O_ref, mo, 2.0 ** -8), ("dv", dxc[:, :, 2], dv_ref, mv, 2.0 ** -8),
+                                   ("dq", dxc[:, :, 0], dq_ref, mq, 2.0 ** -7),
+                                   ("dk", dxc[:, :, 1], dk_ref, mk, 2.0 ** -7)):
+        g64 = _heads(got)
+        bad = np.abs(g64 - ref) > c * mag + 2.0 ** -7 * np.abs(ref)
+        assert not bad.any(), (name, int(bad.sum()), np.argwhere(bad)[:3])
