@@ -239,23 +239,23 @@ class Tensor:
     def attention(self, k: "Tensor", v: "Tensor", scale: float, causal: bool = True):
         """Fused scaled dot-product attention (limn, "The op set": the one
         fused node in place of the composed T x T scores): self = Q, k, v
-        are bf16 [B, T, H, 64]; returns O [B, T, H, 64] with
+        are bf16 [B, T, H, hd]; returns O [B, T, H, hd] with
         O = softmax(scale * Q K^T, keys j > i hidden when causal) V per head."""
-        assert self.shape == k.shape == v.shape and len(self.shape) == 4 and self.shape[3] == 64
+        assert self.shape == k.shape == v.shape and len(self.shape) == 4
         assert self.dtype == k.dtype == v.dtype == "bf16"
-        if self.shape[1] > ATTN_MAX_T:
+        if self.shape[1] > ATTN_MAX_T or self.shape[3] != ATTN_HD:
             return _composed_attention(self, k, v, scale, causal)
         return Tensor("ATTN", (self, k, v), self.shape, "bf16", arg=(float(scale), bool(causal)))
 
     def attention_packed(self, scale: float, causal: bool = True):
-        """The fused attention over a packed qkv tensor [B, T, 3, H, 64] bf16
+        """The fused attention over a packed qkv tensor [B, T, 3, H, hd] bf16
         (slot 0 Q, 1 K, 2 V: a fused projection's output): returns O
-        [B, T, H, 64].  Its gradient is one tensor in the same packed
+        [B, T, H, hd].  Its gradient is one tensor in the same packed
         layout, which the backward kernels write in place (no pad-and-add of
         dQ, dK, dV back into the packed tensor)."""
-        assert len(self.shape) == 5 and self.shape[2] == 3 and self.shape[4] == 64 and self.dtype == "bf16"
+        assert len(self.shape) == 5 and self.shape[2] == 3 and self.dtype == "bf16"
         B, T, _, H, hd = self.shape
-        if T > ATTN_MAX_T:
+        if T > ATTN_MAX_T or hd != ATTN_HD:
             q, k, v = (self.shrink(((0, B), (0, T), (i, i + 1), (0, H), (0, hd))).reshape(B, T, H, hd)
                        for i in range(3))
             return _composed_attention(q, k, v, scale, causal)
@@ -363,9 +363,10 @@ def _inverse(perm):
 
 # ------------------------------------------------------------ executor --------
 
-# keys the fused attention kernels hold in one block; longer sequences take
-# the composed form below
+# keys the fused attention kernels hold in one block, and their head dim;
+# longer sequences and other head dims take the composed form below
 ATTN_MAX_T = 256
+ATTN_HD = 64
 
 
 def _composed_attention(q, k, v, scale, causal):

@@ -115,16 +115,17 @@ def test_attention_rejects_unsupported_shapes(A):
     assert A.psg_attention_fwd(y, w, y, w, y, w, y, w, lse, 0.125, True, check=False) == A.E_UNSUPPORTED_LAYOUT
 
 
-@pytest.mark.parametrize("T,causal", [(384, True), (300, False)])
-def test_long_sequence_attention_composes(T, causal):
-    """Past one key block (T > 256) the graph's attention is the composed
-    form (score contraction, fused softmax, P V contraction); forward and the
-    three gradients meet the same bars as the fused kernels."""
+@pytest.mark.parametrize("T,hd,causal", [(384, 64, True), (300, 64, False), (130, 32, True), (96, 128, False)])
+def test_long_sequence_attention_composes(T, hd, causal):
+    """Past one key block (T > 256), or at a head dim other than 64, the
+    graph's attention is the composed form (score contraction, fused
+    softmax, P V contraction); forward and the three gradients meet the same
+    bars as the fused kernels."""
     from primitive_sm_graph_gb300 import graph as G
-    B, H, scale = 1, 2, 0.125
-    g = SI.gen(T)
-    qkv = SI.normal((B, T, 3, H, 64), 0, 1, g, torch.bfloat16)
-    do = SI.normal((B, T, H, 64), 0, 1, g, torch.bfloat16)
+    B, H, scale = 1, 2, hd ** -0.5
+    g = SI.gen(T + hd)
+    qkv = SI.normal((B, T, 3, H, hd), 0, 1, g, torch.bfloat16)
+    do = SI.normal((B, T, H, hd), 0, 1, g, torch.bfloat16)
     ex = G._executor()
     ex.log.clear()
     x = G.Tensor.from_torch(qkv.cuda(), requires_grad=True)
