@@ -382,6 +382,37 @@ def test_integer_matmul_exact(O):
     np.testing.assert_array_equal(C, A.astype(np.int64) @ B.astype(np.int64))
 
 
+def test_integer_matmul_wraps_modulo_the_width(O):
+    """Full-range int32 operands: every product and the total wrap modulo
+    2^32 (limn, "Three rules hold it together": integers wrap), and a
+    narrower output keeps the low bits.  numpy's uint64 matmul wraps modulo
+    2^64, which reduces to the same residues."""
+    g = np.random.default_rng(13)
+    A = g.integers(-2**31, 2**31, (6, 11), dtype=np.int64).astype(np.int32)
+    B = g.integers(-2**31, 2**31, (11, 5), dtype=np.int64).astype(np.int32)
+    exact = A.astype(np.int64).astype(np.uint64) @ B.astype(np.int64).astype(np.uint64)
+    np.testing.assert_array_equal(O.matmul(O.T(A, "i32"), O.T(B, "i32"), "i32").data,
+                                  exact.astype(np.uint32).view(np.int32))
+    np.testing.assert_array_equal(O.matmul(O.T(A, "i32"), O.T(B, "i32"), "i8").data,
+                                  (exact & np.uint64(0xff)).astype(np.uint8).view(np.int8))
+    A16 = g.integers(-2**15, 2**15, (4, 7), dtype=np.int64).astype(np.int16)
+    B16 = g.integers(-2**15, 2**15, (7, 3), dtype=np.int64).astype(np.int16)
+    e16 = A16.astype(np.int64).astype(np.uint64) @ B16.astype(np.int64).astype(np.uint64)
+    np.testing.assert_array_equal(O.matmul(O.T(A16, "i16"), O.T(B16, "i16"), "i16").data,
+                                  (e16 & np.uint64(0xffff)).astype(np.uint16).view(np.int16))
+
+
+def test_float64_matmul_exact_on_small_integers(O):
+    """Small-integer float64 operands: every product and partial sum is an
+    exact double, so the oracle's float64 loop must equal the exact integer
+    product (a transposed operand or a dropped term would not)."""
+    g = np.random.default_rng(14)
+    A = g.integers(-1000, 1000, (7, 13)).astype(np.float64)
+    B = g.integers(-1000, 1000, (13, 9)).astype(np.float64)
+    got = O.matmul(O.T(A, "f64"), O.T(B, "f64")).data
+    np.testing.assert_array_equal(got, (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64))
+
+
 # ------------------------------------------------------- composed ops ------
 
 def test_softmax_lemmas_r1_r2_and_row_sums(O):
