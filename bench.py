@@ -295,6 +295,7 @@ def e2e_steps(step, K, W):
 # ------------------------------------------------------ the other rows ----
 
 FP32_LANES_PER_SM = 128   # FFMA lanes per SM (Blackwell SM: 4 partitions x 32)
+IMAD_PER_FFMA = 0.5       # integer multiply-adds issue at half the FFMA rate
 TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 tensor rates
 
 
@@ -419,6 +420,21 @@ class Rows:
                     "tf32_pipe_tflops": round(pipe, 2),
                     "ffma_ceiling": round(ffma, 2), "vs_ffma_ceiling": round(tf / ffma, 3),
                     "workload": "f32 A[4096,4096] @ B[4096,4096] as MUL+SUM (3xTF32, f32 accumulate)"}
+        return fn, fin
+
+    # integer MUL+SUM on the integer pipes: int8 operands, wrapping int32 total
+    def gemm_i8(self):
+        a, b = SI.contraction_i8(0)
+        fn, ops = self._contract(a.cuda(), b.cuda(), torch.int32)
+        pk = fp32_alu_peak() * IMAD_PER_FFMA
+
+        def fin(ms):
+            t = ops / (ms * 1e-3) / 1e12
+            return {"ms": round(ms, 5), "ops": ops, "achieved": round(t, 2), "unit": "TOP/s", "bound": "alu",
+                    "peak": round(pk, 2),
+                    "peak_source": "derived: SMs x 64 IMAD lanes (half the FFMA lanes) x 2 ops x max SM clock",
+                    "frac": round(t / pk, 4),
+                    "workload": "int8 A[2048,2048] @ B[2048,2048] as MUL+SUM, uint32 wraparound total, int32 out"}
         return fn, fin
 
     # C5 shapes: token embedding gather and its scatter-add backward
@@ -746,7 +762,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-KERNEL_ROWS = ["softmax", "rmsnorm", "gemm_bf16", "gemm_f32", "gather", "scatter", "attention"]
+KERNEL_ROWS = ["softmax", "rmsnorm", "gemm_bf16", "gemm_f32", "gemm_i8", "gather", "scatter", "attention"]
 ROW_NAMES = KERNEL_ROWS + ["tiny_graph", "gpt"]
 
 
@@ -780,7 +796,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", default="all",
-                    help="comma list of extra rows to time (softmax,rmsnorm,gemm_bf16,gemm_f32,"
+                    help="comma list of extra rows to time (softmax,rmsnorm,gemm_bf16,gemm_f32,gemm_i8,"
                          "gather,scatter,tiny_graph,gpt), 'all' or 'none'")
     ap.add_argument("--profile-case", default=None,
                     help="run one workload --iters times and exit (for a profiler capture); "

@@ -79,6 +79,14 @@ def contraction_f32(seed=0, M=4096, N=4096, K=4096):
     return normal((M, K), 0.0, 1.0, g), normal((K, N), 0.0, 1.0, g)
 
 
+def contraction_i8(seed=0, M=2048, N=2048, K=2048):
+    """A[M,K], B[K,N] int8 uniform over [-128, 127], A drawn first."""
+    g = gen(seed)
+    a = torch.randint(-128, 128, (M, K), generator=g, dtype=torch.int64).to(torch.int8)
+    b = torch.randint(-128, 128, (K, N), generator=g, dtype=torch.int64).to(torch.int8)
+    return a, b
+
+
 GPT_SHAPES = dict(B=32, T=256, V=256, D=512, H=8, F=2048)
 
 

@@ -198,3 +198,21 @@ def test_graph_matmul_of_every_dtype_is_one_contraction(O, dt):
         _close(c.numpy(), ref, np.abs(a.numpy()) @ np.abs(b.numpy()), K, 2.0 ** -53)
     else:
         np.testing.assert_array_equal(c.numpy(), O.matmul(O.T(a.numpy(), dt), O.T(b.numpy(), dt)).data)
+
+
+def test_full_size_int8_contraction_sampled_rows(A, O):
+    """The bench's int8 [2048, 2048] @ [2048, 2048] -> int32 contraction in
+    its own launch configuration: sampled rows bit-exact against the
+    oracle's integer loop over those rows."""
+    a, b = SI.contraction_i8(0)
+    M, K = a.shape
+    N = b.shape[1]
+    da, db = a.cuda(), b.cuda()
+    va = A.view_of(da, shape=(M, N, K), strides=(K, 0, 1))
+    vb = A.view_of(db, shape=(M, N, K), strides=(0, 1, N))
+    c = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    A.psg_contract(da, va, db, vb, c, A.view_of(c), None, stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 1000, 2047])
+    ref = O.matmul(O.T(a.numpy()[rows], "i8"), O.T(b.numpy(), "i8"), "i32").data
+    np.testing.assert_array_equal(c.cpu().numpy()[rows], ref)
