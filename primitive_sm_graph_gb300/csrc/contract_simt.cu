@@ -64,7 +64,10 @@ __device__ __forceinline__ void st(const SimtParams& p, int64_t o, uint32_t v)
     else ((uint8_t*)p.C)[o] = (uint8_t)(v & 0xffu);
 }
 
-template <int DT>
+// MASKED: the read windows and the cell window are applied; otherwise the
+// operands are read in full (the windows are the whole shape) and the
+// bounds are the tile edges alone
+template <int DT, bool MASKED>
 __global__ void __launch_bounds__(NT) simt_gemm(const __grid_constant__ SimtParams p)
 {
     pdl_enter();
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(NT) simt_gemm(const __grid_constant__ SimtPara
                 int mm, kk;
                 if (p.a_ks == 1) { mm = idx / TK; kk = idx % TK; } else { kk = idx / TM; mm = idx % TM; }
                 const int64_t m = m0 + mm, k = k0 + kk;
-                As[kk][mm] = (m >= p.a_mlo && m < p.a_mhi && k >= p.a_klo && k < p.a_khi)
+                As[kk][mm] = (MASKED ? (m >= p.a_mlo && m < p.a_mhi && k >= p.a_klo && k < p.a_khi) : (m < p.M && k < p.K))
                                  ? ld<DT>(p.A, ab + m * p.a_ms + k * p.a_ks)
                                  : Acc(0);
             }
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(NT) simt_gemm(const __grid_constant__ SimtPara
                 int nn, kk;
                 if (p.b_ks == 1) { nn = idx / TK; kk = idx % TK; } else { kk = idx / TN; nn = idx % TN; }
                 const int64_t n = n0 + nn, k = k0 + kk;
-                Bs[kk][nn] = (n >= p.b_nlo && n < p.b_nhi && k >= p.b_klo && k < p.b_khi)
+                Bs[kk][nn] = (MASKED ? (n >= p.b_nlo && n < p.b_nhi && k >= p.b_klo && k < p.b_khi) : (n < p.N && k < p.K))
                                  ? ld<DT>(p.B, bb + n * p.b_ns + k * p.b_ks)
                                  : Acc(0);
             }
@@ -125,12 +128,12 @@ __global__ void __launch_bounds__(NT) simt_gemm(const __grid_constant__ SimtPara
         for (int i = 0; i < 8; ++i) {
             const int64_t m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
             if (m >= p.M) continue;
-            const bool mk = m >= p.c_mlo && m < p.c_mhi;
+            const bool mk = !MASKED || (m >= p.c_mlo && m < p.c_mhi);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int64_t n = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
                 if (n >= p.N) continue;
-                const bool keep = mk && n >= p.c_nlo && n < p.c_nhi;
+                const bool keep = mk && (!MASKED || (n >= p.c_nlo && n < p.c_nhi));
                 st(p, p.c_off + b * p.c_bs + m * p.c_ms + n * p.c_ns, keep ? acc[i][j] : Acc(0));
             }
         }
@@ -143,18 +146,42 @@ dim3 grid_of(const SimtParams& p)
     return dim3((unsigned)((p.N + TN - 1) / TN), (unsigned)((p.M + TM - 1) / TM), (unsigned)gz);
 }
 
+// true when a window is narrower than the shape (a mask is in effect)
+bool masked(const SimtParams& p)
+{
+    return p.a_mlo != 0 || p.a_mhi != p.M || p.a_klo != 0 || p.a_khi != p.K || p.b_nlo != 0 || p.b_nhi != p.N ||
+           p.b_klo != 0 || p.b_khi != p.K || p.c_mlo != 0 || p.c_mhi != p.M || p.c_nlo != 0 || p.c_nhi != p.N;
+}
+
+template <bool MK>
 const void* kernel_of(int dt)
 {
     switch (dt) {
-    case PSG_F32: return (const void*)simt_gemm<PSG_F32>;
-    case PSG_BF16: return (const void*)simt_gemm<PSG_BF16>;
-    case PSG_F16: return (const void*)simt_gemm<PSG_F16>;
-    case PSG_F64: return (const void*)simt_gemm<PSG_F64>;
-    case PSG_I32: return (const void*)simt_gemm<PSG_I32>;
-    case PSG_I16: return (const void*)simt_gemm<PSG_I16>;
-    case PSG_I8: return (const void*)simt_gemm<PSG_I8>;
+    case PSG_F32: return (const void*)simt_gemm<PSG_F32, MK>;
+    case PSG_BF16: return (const void*)simt_gemm<PSG_BF16, MK>;
+    case PSG_F16: return (const void*)simt_gemm<PSG_F16, MK>;
+    case PSG_F64: return (const void*)simt_gemm<PSG_F64, MK>;
+    case PSG_I32: return (const void*)simt_gemm<PSG_I32, MK>;
+    case PSG_I16: return (const void*)simt_gemm<PSG_I16, MK>;
+    case PSG_I8: return (const void*)simt_gemm<PSG_I8, MK>;
     }
     return nullptr;
+}
+
+template <bool MK>
+psg_status launch_typed(const SimtParams& p, dim3 g, cudaStream_t s)
+{
+    switch (p.ab_dtype) {
+    case PSG_F32: launch(simt_gemm<PSG_F32, MK>, g, NT, 0, s, p); break;
+    case PSG_BF16: launch(simt_gemm<PSG_BF16, MK>, g, NT, 0, s, p); break;
+    case PSG_F16: launch(simt_gemm<PSG_F16, MK>, g, NT, 0, s, p); break;
+    case PSG_F64: launch(simt_gemm<PSG_F64, MK>, g, NT, 0, s, p); break;
+    case PSG_I32: launch(simt_gemm<PSG_I32, MK>, g, NT, 0, s, p); break;
+    case PSG_I16: launch(simt_gemm<PSG_I16, MK>, g, NT, 0, s, p); break;
+    case PSG_I8: launch(simt_gemm<PSG_I8, MK>, g, NT, 0, s, p); break;
+    default: return PSG_E_UNSUPPORTED_DTYPE;
+    }
+    return PSG_OK;
 }
 
 }  // namespace
@@ -164,17 +191,8 @@ psg_status launch_contract_simt(const SimtParams& p, void* stream)
     if (p.M == 0 || p.N == 0 || p.batch == 0) return PSG_OK;
     if ((p.N + TN - 1) / TN > 2147483647 || (p.M + TM - 1) / TM > 65535) return PSG_E_UNSUPPORTED_LAYOUT;
     cudaStream_t s = (cudaStream_t)stream;
-    const dim3 g = grid_of(p);
-    switch (p.ab_dtype) {
-    case PSG_F32: launch(simt_gemm<PSG_F32>, g, NT, 0, s, p); break;
-    case PSG_BF16: launch(simt_gemm<PSG_BF16>, g, NT, 0, s, p); break;
-    case PSG_F16: launch(simt_gemm<PSG_F16>, g, NT, 0, s, p); break;
-    case PSG_F64: launch(simt_gemm<PSG_F64>, g, NT, 0, s, p); break;
-    case PSG_I32: launch(simt_gemm<PSG_I32>, g, NT, 0, s, p); break;
-    case PSG_I16: launch(simt_gemm<PSG_I16>, g, NT, 0, s, p); break;
-    case PSG_I8: launch(simt_gemm<PSG_I8>, g, NT, 0, s, p); break;
-    default: return PSG_E_UNSUPPORTED_DTYPE;
-    }
+    const psg_status st = masked(p) ? launch_typed<true>(p, grid_of(p), s) : launch_typed<false>(p, grid_of(p), s);
+    if (st != PSG_OK) return st;
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
@@ -184,7 +202,7 @@ void query_contract_simt(const SimtParams& p, int* grid, int* block, int* smem, 
     *grid = (int)(g.x * g.y * g.z);
     *block = NT;
     *smem = 0;
-    const void* f = kernel_of(p.ab_dtype);
+    const void* f = masked(p) ? kernel_of<true>(p.ab_dtype) : kernel_of<false>(p.ab_dtype);
     *regs = f ? kernel_regs(f) : 0;
 }
 
