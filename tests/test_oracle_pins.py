@@ -564,3 +564,72 @@ def test_scatter_add_bf16_rounds_once(O):
     upd = O.tensor(np.full((256, 1), 2.0 ** -9), "bf16")
     out, _ = O.scatter_add_rows(dst, np.zeros(256, np.int32), upd)
     assert out.f64()[0, 0] == 1.5
+
+
+def test_matmul_bt_float_path_equals_fused_loop_and_exact_values(O):
+    """The transposed-operand loop (the one the GPT oracle uses) against the
+    plain loop and against exact values.  Its products and k order are those
+    of the naive loop (Luminal IR blog, "Naive Matrix Multiplication"), so
+    both give the same bits for float32, bfloat16 and float16 operands and
+    every output dtype; on small-integer operands every product and partial
+    sum is an exact float32, so the result equals the exact integer product
+    (a transposed operand, a dropped term or a wrong index would not)."""
+    g = np.random.default_rng(21)
+    for (M, K, N) in ((3, 7, 5), (1, 1, 1), (17, 130, 9), (2, 513, 33)):
+        A64 = g.standard_normal((M, K))
+        B64 = g.standard_normal((K, N))
+        for dt in ("f32", "bf16", "f16"):
+            a = O.tensor(A64, dt)
+            b = O.tensor(B64, dt)
+            bt = O.transpose(b)
+            for out in ("f32", "bf16", "f16"):
+                ref = O.matmul(a, b, out).data
+                got = O.matmul_bt(a, bt, out).data
+                assert got.tobytes() == ref.tobytes(), (M, K, N, dt, out)
+        Ai = g.integers(-60, 60, (M, K))
+        Bi = g.integers(-60, 60, (K, N))
+        exact = (Ai @ Bi).astype(np.float64)
+        for dt in ("f32", "bf16", "f16"):
+            got = O.matmul_bt(O.tensor(Ai, dt), O.T(O.tensor(Bi.T.copy(), dt).data, dt), "f32").data
+            np.testing.assert_array_equal(got.astype(np.float64), exact)
+    # a non-square case with rows and columns told apart: C[i, j] = sum_k
+    # A[i, k] * B[k, j], never A[j, k] or B[j, k]
+    A = f32([[1, 2, 3], [4, 5, 6]])
+    B = f32([[1, 0], [0, 10], [100, 0]])
+    got = O.matmul_bt(O.T(A, "f32"), O.T(B.T.copy(), "f32"), "f32").data
+    np.testing.assert_array_equal(got, f32([[301, 20], [604, 50]]))
+
+
+def test_cast_f16_round_to_nearest_even(O):
+    """float32 -> float16 matches numpy's conversion (IEEE round to nearest
+    even) on a wide random sweep and on hand-worked cases: ties to even,
+    overflow to inf at the halfway point above the largest finite half,
+    the subnormal range and its ties; float16 -> float32 is exact."""
+    g = SI.gen(22)
+    x = torch.cat([torch.randn(20000, generator=g) * 300,
+                   torch.randn(4000, generator=g) * 1e-5,
+                   torch.randn(2000, generator=g) * 5e4]).numpy().astype(np.float32)
+    got = O.cast(O.T(x, "f32"), "f16").data
+    with np.errstate(over="ignore"):  # values past 65520 overflow to inf on both sides
+        want = x.astype(np.float16)
+    np.testing.assert_array_equal(got.view(np.uint16), want.view(np.uint16))
+    cases = {
+        1.0 + 2 ** -11: 1.0,                    # halfway between 1 and 1 + 2^-10 -> even (1)
+        1.0 + 3 * 2 ** -11: 1.0 + 2 ** -9,      # halfway -> even (1 + 2^-9)
+        -(1.0 + 2 ** -11): -1.0,
+        65504.0: 65504.0,                       # largest finite half
+        65519.0: 65504.0,                       # below the halfway point
+        65520.0: np.inf,                        # halfway to 65536 rounds to even: inf
+        2.0 ** -25: 0.0,                        # half the smallest subnormal -> even (0)
+        3 * 2.0 ** -25: 2.0 ** -23,             # 1.5 subnormal steps -> even (2 steps)
+        2.0 ** -24: 2.0 ** -24,                 # smallest subnormal is exact
+        -0.0: -0.0,
+    }
+    src = f32(list(cases.keys()))
+    out = O.cast(O.T(src, "f32"), "f16").data
+    for s, o, want in zip(src, out, cases.values()):
+        assert float(o) == want and np.signbit(o) == np.signbit(np.float16(want)), (float(s), float(o), want)
+    nan = O.cast(O.T(f32([np.nan]), "f32"), "f16").data
+    assert np.isnan(nan[0])
+    back = O.cast(O.T(got, "f16"), "f32").data
+    np.testing.assert_array_equal(back, got.astype(np.float32))
