@@ -68,3 +68,41 @@ def first_mismatches(a: np.ndarray, b: np.ndarray, k=5):
     bad = np.nonzero((av.view(np.uint8).reshape(av.shape + (-1,)) !=
                       bv.view(np.uint8).reshape(bv.shape + (-1,))).any(axis=-1) & ~(nan_a & nan_b))[0]
     return [(int(i), av[i], bv[i]) for i in bad[:k]], int(bad.size)
+
+
+def _visible(T, causal):
+    return np.tril(np.ones((T, T), bool)) if causal else np.ones((T, T), bool)
+
+
+def attention_fwd_bounds(Q, K, V, O_ref, L_ref, scale, causal):
+    """Per-cell bound on the fused forward's output O (heads [BH, T, d],
+    float64 oracle values): S is a float32 sum of exact bf16 products, P
+    rounds to bf16 before P V, and O rounds once to bf16:
+        |O - O*| <= 2^-8 * sum_j P*_ij |V_jd| + 2^-7 |O*|."""
+    vis = _visible(Q.shape[1], causal)
+    mag = np.zeros_like(O_ref)
+    for h in range(Q.shape[0]):
+        P = np.where(vis, np.exp(scale * Q[h] @ K[h].T - L_ref[h][:, None]), 0.0)
+        mag[h] = P @ np.abs(V[h])
+    return 2.0 ** -8 * mag + 2.0 ** -7 * np.abs(O_ref)
+
+
+def attention_bwd_bounds(Q, K, V, O, dO, L, scale, causal, refs):
+    """Per-cell bounds on the fused backward's (dQ, dK, dV) against the
+    float64 oracle values refs = (dQ*, dK*, dV*): P and dS round to bf16
+    before the second products and every output rounds once to bf16:
+        dV:     2^-8 * sum_i P_ij |dO_id|                          + 2^-7 |dV*|
+        dQ, dK: 2^-7 * scale * sum_j P_ij (|dP_ij| + |D_i|) |K_jd|   + 2^-7 |dQ*|."""
+    vis = _visible(Q.shape[1], causal)
+    mq, mk, mv = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for h in range(Q.shape[0]):
+        P = np.where(vis, np.exp(scale * Q[h] @ K[h].T - L[h][:, None]), 0.0)
+        dP = dO[h] @ V[h].T
+        D = (dO[h] * O[h]).sum(1)
+        G = np.abs(P) * (np.abs(dP) + np.abs(D)[:, None])
+        mv[h] = P.T @ np.abs(dO[h])
+        mq[h] = scale * (G @ np.abs(K[h]))
+        mk[h] = scale * (G.T @ np.abs(Q[h]))
+    dq, dk, dv = refs
+    return (2.0 ** -7 * mq + 2.0 ** -7 * np.abs(dq), 2.0 ** -7 * mk + 2.0 ** -7 * np.abs(dk),
+            2.0 ** -8 * mv + 2.0 ** -7 * np.abs(dv))
