@@ -608,8 +608,18 @@ class Rows:
             once()
         torch.cuda.synchronize()
         eager_us = (time.perf_counter() - t0) / n * 1e6
-        r = {"eager_us_per_realize": round(eager_us, 2), "kernels": kernels,
-             "workload": "SUM(relu(A[64,32] @ B[32,48])^2) f32"}
+        # the same with the plan cache off: every realize schedules afresh
+        G.PLAN_CACHE = False
+        try:
+            t0 = time.perf_counter()
+            for _ in range(n):
+                once()
+            torch.cuda.synchronize()
+            fresh_us = (time.perf_counter() - t0) / n * 1e6
+        finally:
+            G.PLAN_CACHE = True
+        r = {"eager_us_per_realize": round(eager_us, 2), "eager_unplanned_us_per_realize": round(fresh_us, 2),
+             "kernels": kernels, "workload": "SUM(relu(A[64,32] @ B[32,48])^2) f32"}
         rep = G.Replay(lambda x, y: tiny_graph(G.Tensor.from_torch(x), G.Tensor.from_torch(y)).realize(), da, db)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -660,6 +670,15 @@ class Rows:
             ts.append(time.perf_counter() - t0)
             kernels = len(ex.log)
         ms = statistics.median(ts) * 1e3
+        # the same with the plan cache off: the step scheduled afresh
+        G.PLAN_CACHE = False
+        try:
+            t0 = time.perf_counter()
+            gpt_step(dtok, dw, H)
+            torch.cuda.synchronize()
+            fresh_ms = (time.perf_counter() - t0) * 1e3
+        finally:
+            G.PLAN_CACHE = True
         # the same step recorded once and replayed (device time, CUDA events)
         from primitive_sm_graph_gb300.workloads import GPT_WEIGHTS
 
@@ -692,12 +711,14 @@ class Rows:
         lin = 2 * Bn * T * (D * 3 * D + D * D + 2 * D * F + D * V)
         att = 2 * 2 * Bn * Hh * T * T * (D // Hh)
         flops = 3 * (lin + att)
-        return {"ms_per_step": round(ms, 3), "kernels_per_step": kernels, "flops": flops,
+        return {"ms_per_step": round(ms, 3), "unplanned_ms_per_step": round(fresh_ms, 3),
+                "kernels_per_step": kernels, "flops": flops,
                 "achieved": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "replay_ms_per_step": round(rms, 4),
                 "train_replay_ms_per_step": round(tms, 4),
                 "replay_achieved": round(flops / (rms * 1e-3) / 1e12, 3),
-                "note": "ms_per_step: host wall clock, graph building and scheduling included; "
+                "note": "ms_per_step: host wall clock, graph building included, the schedule replayed "
+                        "from the plan cache (unplanned_ms_per_step: scheduled afresh); "
                         "replay: the recorded step relaunched (CUDA Graph), device time; "
                         "train_replay: forward, backward and one AdamW step (one launch for all weights)",
                 "workload": "1-layer byte GPT fwd+bwd B32 T256 V256 d512 H8 MLP2048 bf16"}
@@ -723,6 +744,37 @@ def oracle_sample(threads: int, rows: int = 512):
     sec = time.perf_counter() - t0
     nbytes = rows * 4096 * 4 * 2 + rows * 4 + rows * 2 * 8192 * 4 * 2
     return sec, nbytes
+
+
+def oracle_rows(threads: int):
+    """The oracle on a bounded sample of each other row's workload (the
+    first rows of each input), OpenMP over output rows: {row: (seconds,
+    units of the row's metric, unit, sample)}."""
+    import oracle as O
+    O.build()
+    O.NTHREADS = threads
+    out = {}
+    x = SI.softmax_input(0)[:256]
+    xs = O.T(x.numpy(), "f32")
+    t0 = time.perf_counter()
+    O.softmax_rows(xs)
+    out["softmax"] = (time.perf_counter() - t0, 256 * 1024 * 8, "GB/s", "256 of 4096 rows")
+    xr, wr = SI.rmsnorm_input(0)
+    xo, wo = O.T(SI.bits(xr[:128]), "bf16"), O.T(SI.bits(wr), "bf16")
+    t0 = time.perf_counter()
+    O.rmsnorm(xo, wo)
+    out["rmsnorm"] = (time.perf_counter() - t0, 128 * 4096 * 4, "GB/s", "128 of 8192 rows")
+    a, b = SI.contraction_bf16(0)
+    ao, bt = O.T(SI.bits(a[:32]), "bf16"), O.transpose(O.T(SI.bits(b), "bf16"))
+    t0 = time.perf_counter()
+    O.matmul_bt(ao, bt, "bf16")
+    out["gemm_bf16"] = (time.perf_counter() - t0, 2 * 32 * 8192 * 8192, "TFLOP/s", "32 of 8192 rows of C")
+    a, b = SI.contraction_f32(0)
+    ao, bt = O.T(a[:32].numpy(), "f32"), O.transpose(O.T(b.numpy(), "f32"))
+    t0 = time.perf_counter()
+    O.matmul_bt(ao, bt, "f32")
+    out["gemm_f32"] = (time.perf_counter() - t0, 2 * 32 * 4096 * 4096, "TFLOP/s", "32 of 4096 rows of C")
+    return out
 
 
 def cpu_cores():
@@ -866,9 +918,17 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         cores = cpu_cores()
         sec, nbytes = oracle_sample(cores)
+        sec1, nbytes1 = oracle_sample(1, rows=64)  # one thread: the serial loops the team splits
+        rows_cpu = {}
+        for name, (s, units, unit, sample) in oracle_rows(cores).items():
+            scale = 1e9 if unit == "GB/s" else 1e12
+            rows_cpu[name] = {"value": round(units / s / scale, 6), "unit": unit, "sample": sample}
         line["cpu_baseline"] = {"value": round(nbytes / sec / 1e9, 4), "unit": "GB/s",
                                 "cores": cores, "kind": "oracle",
-                                "sample": "512 of 4096 chain rows + a 1024x8192 transpose slab"}
+                                "sample": "512 of 4096 chain rows + a 1024x8192 transpose slab",
+                                "serial": {"value": round(nbytes1 / sec1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                           "sample": "64 of 4096 chain rows + a 128x8192 transpose slab"},
+                                "rows": rows_cpu}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -9,7 +9,8 @@
  *   psg_elementwise   a fused elementwise chain over Views;
  *   psg_reduce_rows   SUM/MAX row reductions with fused prologue/epilogue;
  *   psg_permute       CONTIGUOUS of a permuted View (tiled transpose);
- *   psg_contract      matmul as a broadcast MUL followed by a SUM over k;
+ *   psg_contract      matmul as a broadcast MUL followed by a SUM over k,
+ *                     with an optional fused elementwise epilogue;
  *   psg_contract_ws   the same with a split-K workspace (psg_contract_workspace);
  *   psg_gather / psg_scatter_add   the indexed ops along dim 0.
  *
@@ -116,12 +117,15 @@ typedef struct {
  *   LOAD(a=input index): the node dtype must equal that input's view dtype;
  *   CONST: value cval rounded into the node dtype;
  *   RED(a=stage index): (psg_reduce_rows only) the reduced value of an
- *       earlier stage, in that stage's dtype.
+ *       earlier stage, in that stage's dtype;
+ *   ACC: (psg_contract's epilogue only) the cell's float32 total, the SUM
+ *       over k before any rounding into C; node dtype PSG_F32.
  * float64 nodes are not implemented yet (PSG_E_UNSUPPORTED_DTYPE). */
 typedef enum {
     PSG_OP_LOAD = 0, PSG_OP_CONST = 1, PSG_OP_RED = 2,
     PSG_OP_NEG = 3, PSG_OP_EXP = 4, PSG_OP_LOG = 5, PSG_OP_SQRT = 6, PSG_OP_RECIP = 7,
-    PSG_OP_CAST = 8, PSG_OP_ADD = 9, PSG_OP_MUL = 10, PSG_OP_CMPLT = 11, PSG_OP_WHERE = 12
+    PSG_OP_CAST = 8, PSG_OP_ADD = 9, PSG_OP_MUL = 10, PSG_OP_CMPLT = 11, PSG_OP_WHERE = 12,
+    PSG_OP_ACC = 13
 } psg_op;
 
 typedef struct {
@@ -238,11 +242,35 @@ psg_status psg_permute(const void* in, const psg_view* in_v, const int32_t* perm
  * The total deviates from the sequential float32 loop by at most
  * 2 * gamma_{K-1} * sum_k |a_k b_k| (Litmus, "ToleranceBound"); for the
  * 3xTF32 path that bound absorbs the product error at the K it is used at.
+ * epilogue: NULL (or n_nodes == 0) stores each total rounded once into C.
+ *   Otherwise every cell of C is the epilogue program's value at that cell
+ *   (limn, "Reading the schedule": elementwise work fuses into the kernel
+ *   that produces its operand, so a residual add, a ReLU or a cast after the
+ *   contraction costs no trip through memory):
+ *       C[b.., m, n] = prog(ACC = the cell's float32 total,
+ *                           LOAD k = epilogue->in[k] read through in_v[k] at (b.., m, n))
+ *   Each node rounds into its own dtype as in psg_elementwise; the last
+ *   node's dtype must be C's.  The epilogue runs in the bf16 / f16 tensor-
+ *   core kernel only (A and B bf16 or f16, TMA-addressable, batch dims that
+ *   merge for every operand): any other contraction with an epilogue
+ *   returns PSG_E_UNSUPPORTED_LAYOUT, as does a masked epilogue input.
+ *   The first call with a new program compiles its kernel (NVRTC, cached
+ *   for the process, as psg_elementwise does).  C may be an epilogue input
+ *   only through an identical View (an in-place update).
  * d_status: device int32 or NULL; receives PSG_E_TIMEOUT if a pipeline wait in
  *   the tensor-core kernel gave up (the output is then invalid).
  * ------------------------------------------------------------------------- */
+typedef struct {
+    const psg_node* prog;      /* host program, 1..PSG_MAX_NODES nodes (ACC, LOAD, CONST and elementwise ops) */
+    int32_t n_nodes;
+    int32_t n_in;              /* 0..PSG_MAX_INPUTS */
+    const void* const* in;     /* host array of n_in device pointers */
+    const psg_view* in_v;      /* host array of n_in views, each of C's shape, unmasked */
+} psg_epilogue;
+
 psg_status psg_contract(const void* A, const psg_view* Av, const void* B, const psg_view* Bv,
-                        void* C, const psg_view* Cv, int32_t* d_status, void* stream);
+                        void* C, const psg_view* Cv, const psg_epilogue* epilogue, int32_t* d_status,
+                        void* stream);
 
 /* ---------------------------------------------------------------------------
  * psg_contract_workspace / psg_contract_ws -- psg_contract with a caller
@@ -258,12 +286,12 @@ psg_status psg_contract(const void* A, const psg_view* Av, const void* B, const 
  * psg_contract_ws: as psg_contract; workspace: device memory, 16-byte aligned,
  *   owned by the caller, not read before it is written, free again once the
  *   stream passes the call.  NULL or fewer than the queried bytes runs the
- *   unsplit kernel.
+ *   unsplit kernel, and so does a call with an epilogue program.
  * ------------------------------------------------------------------------- */
 size_t psg_contract_workspace(const psg_view* Av, const psg_view* Bv, const psg_view* Cv);
 psg_status psg_contract_ws(const void* A, const psg_view* Av, const void* B, const psg_view* Bv,
-                           void* C, const psg_view* Cv, void* workspace, size_t ws_bytes,
-                           int32_t* d_status, void* stream);
+                           void* C, const psg_view* Cv, const psg_epilogue* epilogue, void* workspace,
+                           size_t ws_bytes, int32_t* d_status, void* stream);
 
 /* ---------------------------------------------------------------------------
  * psg_gather -- GATHER along dim 0 (limn, "The op set"; nn.Embedding is the

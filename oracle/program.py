@@ -4,9 +4,10 @@ TEST INFRASTRUCTURE ONLY (see oracle/__init__.py): only the tests, the smoke
 check and the bench's CPU legs use it, and it imports nothing of the CUDA
 library.  A call is described in plain Python data:
 
-  node   (op, a, b, c, dtype, cval) with op one of LOAD CONST RED NEG EXP LOG
-         SQRT RECIP CAST ADD MUL CMPLT WHERE: a postfix program whose operands
-         name earlier nodes by index and whose last node is the result;
+  node   (op, a, b, c, dtype, cval) with op one of LOAD CONST RED ACC NEG EXP
+         LOG SQRT RECIP CAST ADD MUL CMPLT WHERE: a postfix program whose
+         operands name earlier nodes by index and whose last node is the
+         result;
   load   an oracle tensor already read through its View (:func:`read`), at
          the call's iteration shape.
 
@@ -33,7 +34,8 @@ import numpy as np
 from . import (_NP, T, add, cast, cmplt, exp, full, log, matmul_bt, mul, neg, recip, reduce_max, reduce_sum, sqrt,
                view, where)
 
-OPS = ("LOAD", "CONST", "RED", "NEG", "EXP", "LOG", "SQRT", "RECIP", "CAST", "ADD", "MUL", "CMPLT", "WHERE")
+OPS = ("LOAD", "CONST", "RED", "ACC", "NEG", "EXP", "LOG", "SQRT", "RECIP", "CAST", "ADD", "MUL", "CMPLT",
+       "WHERE")
 _UNARY = {"NEG": neg, "EXP": exp, "LOG": log, "SQRT": sqrt, "RECIP": recip}
 _BINARY = {"ADD": add, "MUL": mul, "CMPLT": cmplt}
 
@@ -57,11 +59,12 @@ def _expand(x: T, shape) -> T:
     return view(T(flat, x.dt), (rows, n), (1, 0)).reshape(shape)
 
 
-def program(nodes, loads, shape, reds=(), hook=None) -> T:
+def program(nodes, loads, shape, reds=(), hook=None, acc=None) -> T:
     """Evaluate a postfix program node by node over ``shape``.  loads[k] is
     input k read through its View at ``shape``; reds[s] is stage s's reduced
     value (shape [rows, 1]), broadcast over the row wherever a RED node reads
-    it.  Returns the last node's value."""
+    it; acc is the float32 value an ACC node reads (a contraction's totals,
+    shape ``shape``).  Returns the last node's value."""
     shape = tuple(int(s) for s in shape)
     vals = []
     for i, (op, a, b, c, dt, cval) in enumerate(nodes):
@@ -77,6 +80,10 @@ def program(nodes, loads, shape, reds=(), hook=None) -> T:
             x = _expand(reds[a], shape)
             if x.dt != dt:
                 raise TypeError("RED %d: node dtype %s, stage dtype %s" % (a, dt, x.dt))
+        elif op == "ACC":
+            if acc is None or acc.dt != "f32" or dt != "f32":
+                raise TypeError("ACC reads a float32 contraction total")
+            x = acc if acc.shape == shape else acc.reshape(shape)
         elif op in _UNARY:
             x = _UNARY[op](vals[a])
         elif op == "CAST":
@@ -145,3 +152,14 @@ def contract(a: T, bt: T, out_dt: str) -> T:
     for z in range(Z):
         out[z] = matmul_bt(T(a.data[z], a.dt), T(bt.data[z], bt.dt), out_dt).data
     return T(out, out_dt)
+
+
+def contract_epilogue(a: T, bt: T, nodes, loads, hook=None) -> T:
+    """A contraction whose cells go through an epilogue program: ACC is each
+    cell's float32 total (:func:`contract` before any rounding), LOAD k the
+    epilogue's input k at the same cell (loads: [Z, M, N] tensors).  The
+    elementwise program then runs node by node over [Z, M, N] (limn,
+    "Reading the schedule": elementwise work fused into the kernel that
+    produces its operand computes what the separate nodes compute)."""
+    tot = contract(a, bt, "f32")
+    return program(nodes, loads, tot.shape, hook=hook, acc=tot)

@@ -33,7 +33,7 @@ DTYPE_SIZE = {"f32": 4, "bf16": 2, "f16": 2, "f64": 8, "i32": 4, "i16": 2, "i8":
 
 # psg_op
 OPS = {"LOAD": 0, "CONST": 1, "RED": 2, "NEG": 3, "EXP": 4, "LOG": 5, "SQRT": 6, "RECIP": 7,
-       "CAST": 8, "ADD": 9, "MUL": 10, "CMPLT": 11, "WHERE": 12}
+       "CAST": 8, "ADD": 9, "MUL": 10, "CMPLT": 11, "WHERE": 12, "ACC": 13}
 RED_SUM, RED_MAX = 0, 1
 CALLS = {"elementwise": 0, "reduce_rows": 1, "permute": 2, "contract_bf16": 3,
          "contract_f32": 4, "gather": 5, "scatter_add": 6, "contract_f32_tensor": 7}
@@ -55,6 +55,11 @@ class psg_node(ctypes.Structure):
 class psg_reduce_stage(ctypes.Structure):
     _fields_ = [("op", ctypes.c_int32), ("n_nodes", ctypes.c_int32),
                 ("prologue", ctypes.POINTER(psg_node))]
+
+
+class psg_epilogue(ctypes.Structure):
+    _fields_ = [("prog", ctypes.POINTER(psg_node)), ("n_nodes", ctypes.c_int32), ("n_in", ctypes.c_int32),
+                ("in_", ctypes.POINTER(ctypes.c_void_p)), ("in_v", ctypes.POINTER(psg_view))]
 
 
 class psg_adamw_tensor(ctypes.Structure):
@@ -82,8 +87,9 @@ def _load():
     L.psg_elementwise.argtypes = [N, i32, ctypes.POINTER(vp), V, i32, vp, V, vp]
     L.psg_reduce_rows.argtypes = [S, i32, N, i32, ctypes.POINTER(vp), V, i32, vp, V, vp, vp]
     L.psg_permute.argtypes = [vp, V, P32, vp, V, vp]
-    L.psg_contract.argtypes = [vp, V, vp, V, vp, V, vp, vp]
-    L.psg_contract_ws.argtypes = [vp, V, vp, V, vp, V, vp, sz, vp, vp]
+    E = ctypes.POINTER(psg_epilogue)
+    L.psg_contract.argtypes = [vp, V, vp, V, vp, V, E, vp, vp]
+    L.psg_contract_ws.argtypes = [vp, V, vp, V, vp, V, E, vp, sz, vp, vp]
     L.psg_contract_workspace.argtypes = [V, V, V]
     L.psg_contract_workspace.restype = sz
     L.psg_gather.argtypes = [vp, V, vp, i64, vp, V, vp, vp]
@@ -245,9 +251,28 @@ def psg_permute(inp, in_view, perm, out, out_view, stream=None, check=True) -> i
     return st
 
 
-def psg_contract(A, Av, B, Bv, C, Cv, d_status=None, stream=None, check=True) -> int:
+def _epilogue(epilogue):
+    """psg_epilogue from (program nodes, input buffers, input views), or a
+    NULL pointer for None; returns (pointer, objects to keep alive)."""
+    if not epilogue or not epilogue[0]:
+        return None, ()
+    prog, ins, views = epilogue
+    arr, n = _nodes(prog)
+    ptrs = (ctypes.c_void_p * max(1, len(ins)))(*[_ptr(x) for x in ins])
+    vs = _views(views)
+    e = psg_epilogue(ctypes.cast(arr, ctypes.POINTER(psg_node)), n, len(ins), ctypes.cast(ptrs, ctypes.POINTER(
+        ctypes.c_void_p)), ctypes.cast(vs, ctypes.POINTER(psg_view)))
+    return ctypes.byref(e), (e, arr, ptrs, vs)
+
+
+def psg_contract(A, Av, B, Bv, C, Cv, d_status=None, stream=None, check=True, epilogue=None) -> int:
+    """epilogue: None, or (program nodes, input buffers, input views): C is
+    then the program's value at each cell, with ACC the cell's float32
+    total."""
+    ep, keep = _epilogue(epilogue)
     st = lib.psg_contract(_ptr(A), ctypes.byref(Av), _ptr(B), ctypes.byref(Bv), _ptr(C),
-                          ctypes.byref(Cv), _ptr(d_status), _stream(stream))
+                          ctypes.byref(Cv), ep, _ptr(d_status), _stream(stream))
+    del keep
     if check:
         _check(st, "psg_contract")
     return st
@@ -258,9 +283,12 @@ def psg_contract_workspace(Av, Bv, Cv) -> int:
     return int(lib.psg_contract_workspace(ctypes.byref(Av), ctypes.byref(Bv), ctypes.byref(Cv)))
 
 
-def psg_contract_ws(A, Av, B, Bv, C, Cv, workspace, ws_bytes, d_status=None, stream=None, check=True) -> int:
-    st = lib.psg_contract_ws(_ptr(A), ctypes.byref(Av), _ptr(B), ctypes.byref(Bv), _ptr(C), ctypes.byref(Cv),
+def psg_contract_ws(A, Av, B, Bv, C, Cv, workspace, ws_bytes, d_status=None, stream=None, check=True,
+                    epilogue=None) -> int:
+    ep, keep = _epilogue(epilogue)
+    st = lib.psg_contract_ws(_ptr(A), ctypes.byref(Av), _ptr(B), ctypes.byref(Bv), _ptr(C), ctypes.byref(Cv), ep,
                              _ptr(workspace), int(ws_bytes), _ptr(d_status), _stream(stream))
+    del keep
     if check:
         _check(st, "psg_contract_ws")
     return st

@@ -5,8 +5,10 @@
 #include <cstring>
 
 #include "api_internal.h"
+#include "codegen.h"
 #include "common.h"
 #include "contract.h"
+#include "jit.h"
 
 namespace psg {
 
@@ -63,11 +65,94 @@ void collapse_batch(Batch& B)
 
 bool al16(const void* p, int64_t off_elems, int es) { return ((uintptr_t)p + (uintptr_t)(off_elems * es)) % 16 == 0; }
 
+// The fused epilogue of the tensor-core path: validates the program and its
+// inputs against C, fills the kernel's operand descriptors and writes the
+// spec pieces.  dm, dn: the dims of m and n in C's index space; nb_dims:
+// C's leading (batch) dims, which must merge into one stride for every input
+// as they did for A, B and C.
+psg_status plan_epilogue(const psg_epilogue* E, const psg_view* Cv, int dm, int dn, int nb_dims, int64_t batch,
+                         TcParams& p, EpiSpec& spec)
+{
+    const int n = E->n_nodes, nin = E->n_in;
+    if (!E->prog || n < 1 || n > PSG_MAX_NODES || nin < 0 || nin > PSG_MAX_INPUTS || nin > PSG_TC_MAX_EPI_IN)
+        return PSG_E_INVALID_ARG;
+    if (nin > 0 && (!E->in || !E->in_v)) return PSG_E_INVALID_ARG;
+    // ACC becomes the stashed value: the first ACC node reads it, any later
+    // one is a no-op CAST of the first
+    std::vector<psg_node> nodes(E->prog, E->prog + n);
+    int acc = -1;
+    for (int i = 0; i < n; ++i) {
+        psg_node& x = nodes[i];
+        if (x.op == PSG_OP_LOAD && (x.a < 0 || x.a >= nin)) return PSG_E_INVALID_ARG;
+        if (x.op == PSG_OP_RED) return PSG_E_INVALID_ARG;
+        if (x.dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
+        if (x.op != PSG_OP_ACC) continue;
+        if (x.dtype != PSG_F32) return PSG_E_UNSUPPORTED_DTYPE;
+        if (acc < 0) {
+            acc = i;
+            x.op = PSG_OP_LOAD;
+            x.a = nin;
+        } else {
+            x.op = PSG_OP_CAST;
+            x.a = acc;
+        }
+    }
+    int dts[PSG_MAX_INPUTS + 1];
+    bool uni[PSG_MAX_INPUTS + 1];
+    int modes[PSG_TC_MAX_EPI_IN] = {};
+    const int64_t M = Cv->shape[dm], N = Cv->shape[dn];
+    for (int k = 0; k < nin; ++k) {
+        const psg_view* v = &E->in_v[k];
+        if (v->ndim != Cv->ndim || !same_shape(v, Cv)) return PSG_E_INVALID_ARG;
+        if (!dtype_valid(v->dtype) || v->dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
+        if (view_has_mask(v)) return PSG_E_UNSUPPORTED_LAYOUT;
+        psg_status st = check_view(v, false);
+        if (st != PSG_OK) return st;
+        if (M * N * batch > 0 && !E->in[k]) return PSG_E_INVALID_ARG;
+        if (!ptr_aligned(E->in[k], v->dtype)) return PSG_E_MISALIGNED;
+        // the batch dims that are not 1 merge into one stride, as for A, B and C
+        int64_t sb = 0;
+        int last = -1;
+        for (int d = 0; d < nb_dims; ++d) {
+            if (v->shape[d] == 1) continue;
+            if (last >= 0 && v->strides[last] != v->strides[d] * v->shape[d]) return PSG_E_UNSUPPORTED_LAYOUT;
+            last = d;
+            sb = v->strides[d];
+        }
+        const int es = dtype_size(v->dtype);
+        TcEpiOperand& o = p.epi[k];
+        o.ptr = (const char*)E->in[k] + v->offset * es;
+        o.sb = sb;
+        o.sm = M > 1 ? v->strides[dm] : 0;
+        o.sn = N > 1 ? v->strides[dn] : 0;
+        const bool al = ((uintptr_t)o.ptr % 16) == 0 && (o.sm * es) % 16 == 0 && (batch <= 1 || (o.sb * es) % 16 == 0);
+        modes[k] = o.sn == 0 ? 0 : (o.sn == 1 && al && dtype_is_float(v->dtype)) ? 1 : 2;  // EPI_ROW / VEC / STRIDED
+        dts[k] = v->dtype;
+        uni[k] = o.sn == 0;
+    }
+    dts[nin] = PSG_F32;
+    uni[nin] = false;
+    ProgInfo I;
+    psg_status st = analyze_program(nodes.data(), n, dts, uni, nin + 1, nullptr, 0, &I);
+    if (st != PSG_OK) return st;
+    if (I.result_dtype != Cv->dtype) return PSG_E_UNSUPPORTED_DTYPE;
+    p.n_epi = nin;
+    std::string dl = "constexpr int kEpiDt[8] = {", ml = "constexpr int kEpiMode[8] = {";
+    for (int k = 0; k < 8; ++k) {
+        dl += std::to_string(k < nin ? dts[k] : 0) + (k < 7 ? ", " : "};\n");
+        ml += std::to_string(k < nin ? modes[k] : 0) + (k < 7 ? ", " : "};\n");
+    }
+    spec.tables = dl + ml;
+    // a half-width C is rounded by the store itself (the same bits)
+    spec.prog = gen_eval(nodes.data(), I, "EpiProg", "", acc, Cv->dtype != PSG_F32);
+    return PSG_OK;
+}
+
 }  // namespace
 
 psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, const psg_view* Bv, void* C,
-                         const psg_view* Cv, int32_t* d_status, bool* use_tc, TcOperands* T, SimtParams* S,
-                         Batch* bt)
+                         const psg_view* Cv, const psg_epilogue* epi, EpiSpec* espec, int32_t* d_status,
+                         bool* use_tc, TcOperands* T, SimtParams* S, Batch* bt)
 {
     if (!Av || !Bv || !Cv) return PSG_E_INVALID_ARG;
     const int r = Av->ndim;
@@ -140,6 +225,12 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
     tc = tc && tma_ok(A, Av->offset, a_ms, a_ks, M, bt->nb ? bt->sa[0] : 0, akm);
     tc = tc && tma_ok(Bp, Bv->offset, b_ns, b_ks, N, bt->nb ? bt->sb[0] : 0, bkm);
     *use_tc = tc;
+    const bool has_epi = epi && epi->n_nodes > 0;
+    if (has_epi) {
+        // the epilogue runs in the bf16 / f16 tensor-core kernel only
+        if (!tc || adt == PSG_F32 || bt->masked || bt->nb > 1) return PSG_E_UNSUPPORTED_LAYOUT;
+        if (!is_float(cdt)) return PSG_E_UNSUPPORTED_DTYPE;
+    }
     if (tc) {
         std::memset(T, 0, sizeof(*T));
         T->p.M = (int)M;
@@ -164,6 +255,11 @@ psg_status plan_contract(const void* A, const psg_view* Av, const void* Bp, cons
         T->b_ns = b_ns;
         T->b_ks = b_ks;
         T->b_bs = bt->nb ? bt->sb[0] : 0;
+        if (has_epi) {
+            st = plan_epilogue(epi, Cv, dm, dn, r - 3, batch, T->p, *espec);
+            if (st != PSG_OK) return st;
+            T->epi = espec;
+        }
     }
     std::memset(S, 0, sizeof(*S));
     S->A = A;
@@ -208,16 +304,20 @@ using namespace psg;
 namespace {
 
 psg_status contract_impl(const void* A, const psg_view* Av, const void* B, const psg_view* Bv, void* C,
-                         const psg_view* Cv, void* ws, size_t ws_bytes, int32_t* d_status, void* stream)
+                         const psg_view* Cv, const psg_epilogue* epi, void* ws, size_t ws_bytes, int32_t* d_status,
+                         void* stream)
 {
     bool tc;
     TcOperands T;
     SimtParams S;
     Batch bt;
-    psg_status st = plan_contract(A, Av, B, Bv, C, Cv, d_status, &tc, &T, &S, &bt);
+    EpiSpec espec;
+    psg_status st = plan_contract(A, Av, B, Bv, C, Cv, epi, &espec, d_status, &tc, &T, &S, &bt);
     if (st != PSG_OK) return st;
-    T.ws = ws;
-    T.ws_bytes = ws_bytes;
+    // a fused epilogue needs the whole total of a cell in one place: no split K
+    const bool has_epi = epi && epi->n_nodes > 0;
+    T.ws = has_epi ? nullptr : ws;
+    T.ws_bytes = has_epi ? 0 : ws_bytes;
     if (S.M == 0 || S.N == 0) return PSG_OK;
     // (an empty SUM, K == 0, is its identity: every cell 0 through the SIMT kernel)
     if (bt.nb <= 1 && !bt.masked) {
@@ -254,16 +354,16 @@ psg_status contract_impl(const void* A, const psg_view* Av, const void* B, const
 }  // namespace
 
 extern "C" psg_status psg_contract(const void* A, const psg_view* Av, const void* B, const psg_view* Bv, void* C,
-                                   const psg_view* Cv, int32_t* d_status, void* stream)
+                                   const psg_view* Cv, const psg_epilogue* epilogue, int32_t* d_status, void* stream)
 {
-    return contract_impl(A, Av, B, Bv, C, Cv, nullptr, 0, d_status, stream);
+    return contract_impl(A, Av, B, Bv, C, Cv, epilogue, nullptr, 0, d_status, stream);
 }
 
 extern "C" psg_status psg_contract_ws(const void* A, const psg_view* Av, const void* B, const psg_view* Bv, void* C,
-                                      const psg_view* Cv, void* workspace, size_t ws_bytes, int32_t* d_status,
-                                      void* stream)
+                                      const psg_view* Cv, const psg_epilogue* epilogue, void* workspace,
+                                      size_t ws_bytes, int32_t* d_status, void* stream)
 {
-    return contract_impl(A, Av, B, Bv, C, Cv, workspace, ws_bytes, d_status, stream);
+    return contract_impl(A, Av, B, Bv, C, Cv, epilogue, workspace, ws_bytes, d_status, stream);
 }
 
 extern "C" size_t psg_contract_workspace(const psg_view* Av, const psg_view* Bv, const psg_view* Cv)
@@ -280,4 +380,32 @@ extern "C" size_t psg_contract_workspace(const psg_view* Av, const psg_view* Bv,
     size_t bytes = 0;
     contract_tc_splits(M, N, K, batch, &bytes);
     return bytes;
+}
+
+// Test hook, not part of the ABI: plan a psg_contract call with an epilogue
+// over dummy pointers and compile both variants of its kernel (single CTA
+// and CTA pair) without a GPU.
+extern "C" int psg_internal_compile_contract_epilogue(const psg_view* Av, const psg_view* Bv, const psg_view* Cv,
+                                                      const psg_epilogue* epi, char* log, size_t log_size)
+{
+    const void* fake[PSG_MAX_INPUTS];
+    for (int k = 0; k < PSG_MAX_INPUTS; ++k) fake[k] = (const void*)(uintptr_t)4096;
+    psg_epilogue e = *epi;
+    e.in = fake;
+    bool tc;
+    TcOperands T;
+    SimtParams S;
+    Batch bt;
+    EpiSpec espec;
+    const void* p = (const void*)(uintptr_t)4096;
+    psg_status st = plan_contract(p, Av, p, Bv, (void*)p, Cv, &e, &espec, nullptr, &tc, &T, &S, &bt);
+    if (st != PSG_OK) return st;
+    std::string l;
+    for (int pair = 0; pair < 2 && st == PSG_OK; ++pair)
+        st = jit_compile_only(jit_source(JIT_GEMM, epi_spec_source(espec, pair != 0)), &l);
+    if (log && log_size) {
+        std::strncpy(log, l.c_str(), log_size - 1);
+        log[log_size - 1] = 0;
+    }
+    return st;
 }

@@ -579,12 +579,7 @@ psg_status launch_attention_fwd(const AttnTensor& q, const AttnTensor& k, const 
     if (!make_map_attn(&mq, q, p.T, p.H, p.B, QT) || !make_map_attn(&mk, k, p.T, p.H, p.B, QT) ||
         !make_map_attn(&mv, v, p.T, p.H, p.B, QT))
         return PSG_E_CUDA;
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute((const void*)attn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
-    });
-    if (err != cudaSuccess) return PSG_E_CUDA;
+    if (set_max_dynamic_smem((const void*)attn_fwd, FWD_SMEM) != cudaSuccess) return PSG_E_CUDA;
     const dim3 grid((unsigned)((p.T + QT - 1) / QT), (unsigned)p.H, (unsigned)p.B);
     launch(attn_fwd, grid, FWD_THREADS, FWD_SMEM, (cudaStream_t)stream, mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
@@ -600,12 +595,7 @@ psg_status launch_attention_bwd(const AttnTensor& q, const AttnTensor& k, const 
     if (!make_map_attn(&mq, q, p.T, p.H, p.B, QT) || !make_map_attn(&mk, k, p.T, p.H, p.B, QT) ||
         !make_map_attn(&mv, v, p.T, p.H, p.B, QT) || !make_map_attn(&mdo, dO, p.T, p.H, p.B, QT))
         return PSG_E_CUDA;
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute((const void*)attn_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
-    });
-    if (err != cudaSuccess) return PSG_E_CUDA;
+    if (set_max_dynamic_smem((const void*)attn_bwd, BWD_SMEM) != cudaSuccess) return PSG_E_CUDA;
     const int64_t rows = (int64_t)p.B * p.T * p.H;
     const int dgrid = (int)std::min<int64_t>((rows + 31) / 32, (int64_t)num_sms() * 16);  // 32 rows a block
     launch(attn_delta, dgrid, 256, 0, s, o, dO, p);

@@ -52,7 +52,7 @@ std::string fmt(const char* f, ...)
     return buf;
 }
 
-const char* ctype(int dt) { return dtype_is_int(dt) ? "int" : "float"; }
+const char* ctype(int dt) { return dtype_is_int(dt) ? "int" : dt == PSG_F64 ? "double" : "float"; }
 
 // round a 32-bit value expression into dtype dt
 std::string wrap(int dt, const std::string& e)
@@ -80,7 +80,6 @@ psg_status analyze_program(const psg_node* nodes, int n, const int* in_dtype, co
     for (int i = 0; i < n; ++i) {
         const psg_node& x = nodes[i];
         if (!dtype_valid(x.dtype)) return PSG_E_UNSUPPORTED_DTYPE;
-        if (x.dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
         I->dt[i] = x.dtype;
         I->val[i] = i;
         auto opnd = [&](int k) { return k >= 0 && k < i; };
@@ -104,7 +103,7 @@ psg_status analyze_program(const psg_node* nodes, int n, const int* in_dtype, co
             break;
         case PSG_OP_EXP: case PSG_OP_LOG: case PSG_OP_SQRT: case PSG_OP_RECIP:
             if (!opnd(x.a) || I->dt[x.a] != x.dtype) return PSG_E_INVALID_ARG;
-            if (!dtype_is_float(x.dtype)) return PSG_E_UNSUPPORTED_DTYPE;
+            if (!dtype_is_float(x.dtype) && x.dtype != PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
             I->uni[i] = I->uni[x.a];
             break;
         case PSG_OP_CAST: {
@@ -204,6 +203,12 @@ std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string
             }
             break;
         case PSG_OP_CONST: {
+            if (dt == PSG_F64) {
+                uint64_t b64;
+                std::memcpy(&b64, &x.cval, 8);
+                e = fmt("__longlong_as_double(0x%016llxll)", (unsigned long long)b64);
+                break;
+            }
             const uint32_t b = const_bits(x.cval, dt);
             e = isint ? fmt("(int)%d", (int32_t)b) : fmt("__uint_as_float(0x%08xu)", b);
             break;
@@ -212,31 +217,45 @@ std::string gen_eval(const psg_node* nodes, const ProgInfo& I, const std::string
             e = fmt(isint ? "c.redi(%d)" : "c.redf(%d)", x.a);
             break;
         case PSG_OP_NEG:
-            e = isint ? wrap(dt, "negi(" + ref(x.a) + ")") : "negf(" + ref(x.a) + ")";
+            e = isint ? wrap(dt, "negi(" + ref(x.a) + ")") : (dt == PSG_F64 ? "negd(" : "negf(") + ref(x.a) + ")";
             break;
-        case PSG_OP_EXP: e = wrap(dt, "psg_exp(" + ref(x.a) + ")"); break;
-        case PSG_OP_LOG: e = wrap(dt, "logf(" + ref(x.a) + ")"); break;
-        case PSG_OP_SQRT: e = wrap(dt, "__fsqrt_rn(" + ref(x.a) + ")"); break;
-        case PSG_OP_RECIP: e = wrap(dt, "__frcp_rn(" + ref(x.a) + ")"); break;
+        // float64 nodes compute natively in double (limn, "The op set", the
+        // dtype paragraph): the C library's exp and log, correctly rounded
+        // sqrt, reciprocal, add and multiply
+        case PSG_OP_EXP: e = dt == PSG_F64 ? "exp(" + ref(x.a) + ")" : wrap(dt, "psg_exp(" + ref(x.a) + ")"); break;
+        case PSG_OP_LOG: e = dt == PSG_F64 ? "log(" + ref(x.a) + ")" : wrap(dt, "logf(" + ref(x.a) + ")"); break;
+        case PSG_OP_SQRT:
+            e = dt == PSG_F64 ? "__dsqrt_rn(" + ref(x.a) + ")" : wrap(dt, "__fsqrt_rn(" + ref(x.a) + ")");
+            break;
+        case PSG_OP_RECIP:
+            e = dt == PSG_F64 ? "__drcp_rn(" + ref(x.a) + ")" : wrap(dt, "__frcp_rn(" + ref(x.a) + ")");
+            break;
         case PSG_OP_CAST: {
             const int s = I.dt[x.a];
-            if (dtype_is_float(s) && dtype_is_int(dt)) e = wrap(dt, "__float2int_rz(" + ref(x.a) + ")");
+            // float64 to a narrower float rounds to float32 first, then (for a
+            // half width) to the half width, as the oracle's CAST does
+            if (s == PSG_F64 && dtype_is_int(dt)) e = wrap(dt, "__double2int_rz(" + ref(x.a) + ")");
+            else if (s == PSG_F64 && dt != PSG_F64) e = wrap(dt, "__double2float_rn(" + ref(x.a) + ")");
+            else if (dtype_is_int(s) && dt == PSG_F64) e = "__int2double_rn(" + ref(x.a) + ")";
+            else if (dt == PSG_F64) e = "(double)" + ref(x.a);
+            else if (dtype_is_float(s) && dtype_is_int(dt)) e = wrap(dt, "__float2int_rz(" + ref(x.a) + ")");
             else if (dtype_is_int(s) && dtype_is_float(dt)) e = wrap(dt, "__int2float_rn(" + ref(x.a) + ")");
             else e = wrap(dt, ref(x.a));
             break;
         }
         case PSG_OP_ADD:
-            e = wrap(dt, (isint ? "addi(" : "__fadd_rn(") + ref(x.a) + ", " + ref(x.b) + ")");
+            e = wrap(dt, (isint ? "addi(" : dt == PSG_F64 ? "__dadd_rn(" : "__fadd_rn(") + ref(x.a) + ", " + ref(x.b) + ")");
             break;
         case PSG_OP_MUL:
-            e = wrap(dt, (isint ? "muli(" : "__fmul_rn(") + ref(x.a) + ", " + ref(x.b) + ")");
+            e = wrap(dt, (isint ? "muli(" : dt == PSG_F64 ? "__dmul_rn(" : "__fmul_rn(") + ref(x.a) + ", " + ref(x.b) + ")");
             break;
         case PSG_OP_CMPLT:
-            e = "(" + ref(x.a) + " < " + ref(x.b) + (isint ? " ? 1 : 0)" : " ? 1.0f : 0.0f)");
+            e = "(" + ref(x.a) + " < " + ref(x.b) + (isint ? " ? 1 : 0)" : dt == PSG_F64 ? " ? 1.0 : 0.0)" : " ? 1.0f : 0.0f)");
             break;
         case PSG_OP_WHERE: {
-            const bool cint = dtype_is_int(I.dt[x.a]);
-            e = "((" + ref(x.a) + (cint ? " != 0" : " != 0.0f") + ") ? " + ref(x.b) + " : " + ref(x.c) + ")";
+            const int cdt = I.dt[x.a];
+            const bool cint = dtype_is_int(cdt);
+            e = "((" + ref(x.a) + (cint ? " != 0" : cdt == PSG_F64 ? " != 0.0" : " != 0.0f") + ") ? " + ref(x.b) + " : " + ref(x.c) + ")";
             break;
         }
         }

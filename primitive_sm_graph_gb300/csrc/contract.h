@@ -1,27 +1,24 @@
 // Launch descriptors of the MUL+SUM contraction kernels.
 #pragma once
 
+#include <string>
+
 #include "common.h"
 
 namespace psg {
 
-struct TcParams {
-    int M, N, K, batch;
-    int a_kmajor, b_kmajor;     // 1: k stride 1; 0: m (n) stride 1
-    int num_m, num_n, num_k;    // tile counts (filled by the launcher)
-    int c_dtype;
-    int ab_dtype;               // bf16 or f16 (tc_gemm), f32 (tc_gemm_tf32x3)
-    int splits, kb_per;         // split-K: K-block ranges per tile (1: none)
-    float* ws;                  // split-K partials [splits][batch][M][N] float32
-    void* C;
-    int32_t* status;
-    int64_t c_offset, c_rs, c_cs, c_bs;
-    int tma_store;              // 1: the epilogue writes C (or the partials) through a tensor map
-    int reduce_quad;            // split-K reduce: 1 when C's rows take 4-cell vector moves
+#include "jit/gemm_params.h"
+
+// The runtime-compiled part of a contraction with a fused epilogue: the
+// operand tables and the program body (gen_eval's EpiProg) of the spec; the
+// launcher adds the kernel entry point of the variant it runs.
+struct EpiSpec {
+    std::string tables, prog;
 };
 
 struct TcOperands {
     TcParams p;
+    const EpiSpec* epi;         // fused epilogue program, or null
     void* ws;                   // caller workspace for split-K partials (may be null)
     size_t ws_bytes;
     const void* A;  // at the View's offset
@@ -48,6 +45,9 @@ struct SimtParams {
 };
 
 psg_status launch_contract_tc(const TcOperands& o, void* stream);
+// the JIT_GEMM spec of a fused epilogue for the single-CTA (pair false) or
+// CTA-pair kernel
+std::string epi_spec_source(const EpiSpec& e, bool pair);
 // split-K plan of the bf16 / f16 kernel: splits (1 = none) and the
 // workspace bytes they need, for an output of tiles that leaves SMs idle
 int contract_tc_splits(int64_t M, int64_t N, int64_t K, int64_t batch, size_t* bytes);

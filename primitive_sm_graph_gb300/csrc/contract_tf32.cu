@@ -350,13 +350,7 @@ psg_status launch_contract_tf32(const TcOperands& o, void* stream)
     p.num_m = (p.M + BM - 1) / BM;
     p.num_n = (p.N + BN - 1) / BN;
     p.num_k = (p.K + BKF - 1) / BKF;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute((const void*)tc_gemm_tf32x3, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return PSG_E_CUDA;
+    if (set_max_dynamic_smem((const void*)tc_gemm_tf32x3, SMEM_BYTES) != cudaSuccess) return PSG_E_CUDA;
     const int64_t tiles = (int64_t)p.num_m * p.num_n * p.batch;
     const int grid = (int)std::min<int64_t>(tiles, num_sms());
     launch(tc_gemm_tf32x3, grid, THREADS, SMEM_BYTES, (cudaStream_t)stream, ma, mb, p);

@@ -51,7 +51,6 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
     if (!out_v) return PSG_E_INVALID_ARG;
     psg_status st = check_view(out_v, true);
     if (st != PSG_OK) return st;
-    if (out_v->dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
     const int64_t n = view_numel(out_v);
     if (n > 0 && !out) return PSG_E_INVALID_ARG;
     if (!ptr_aligned(out, out_v->dtype)) return PSG_E_MISALIGNED;
@@ -62,7 +61,6 @@ psg_status plan_elementwise(const psg_node* prog, int n_nodes, const void* const
         st = check_view(&in_v[k], false);
         if (st != PSG_OK) return st;
         if (!same_shape(&in_v[k], out_v)) return PSG_E_INVALID_ARG;
-        if (in_v[k].dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
         if (n > 0 && !in[k]) return PSG_E_INVALID_ARG;
         if (!ptr_aligned(in[k], in_v[k].dtype)) return PSG_E_MISALIGNED;
         views[1 + k] = &in_v[k];

@@ -886,13 +886,7 @@ static void launch_accumulate(const ScatterLaunch& L, const unsigned long long* 
 template <int DT>
 static psg_status launch_planned(const ScatterLaunch& L, void* ws, cudaStream_t s)
 {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute((const void*)scatter_plan, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   PLAN_SMEM);
-    });
-    if (err != cudaSuccess) return PSG_E_CUDA;
+    if (set_max_dynamic_smem((const void*)scatter_plan, PLAN_SMEM) != cudaSuccess) return PSG_E_CUDA;
     const PlanOut P = plan_layout(ws, L.n);
     launch(scatter_plan, 1, PLAN_THREADS, PLAN_SMEM, s, L.idx, (int)L.n, L.V, P, L.status);
     const int64_t runs = std::min<int64_t>(L.n, L.V);  // at most this many runs
@@ -924,14 +918,8 @@ static psg_status launch_owner(const ScatterLaunch& L, cudaStream_t s)
     const int64_t ncb = (L.D + chunk - 1) / chunk;
     if (ncb == 0) return PSG_OK;
     const size_t smem = (size_t)L.n * 4;
-    static std::once_flag once[2];
-    static cudaError_t err[2] = {cudaSuccess, cudaSuccess};
     const void* fn = pair ? (const void*)scatter_owner<DT, true> : (const void*)scatter_owner<DT, false>;
-    std::call_once(once[pair ? 1 : 0], [fn, pair] {
-        err[pair ? 1 : 0] =
-            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScatterPlanMaxN * 4);
-    });
-    if (err[pair ? 1 : 0] != cudaSuccess) return PSG_E_CUDA;
+    if (set_max_dynamic_smem(fn, (int)kScatterPlanMaxN * 4) != cudaSuccess) return PSG_E_CUDA;
     const unsigned blocks = (unsigned)(L.V * ncb);
     const int idx16 = ((uintptr_t)L.idx % 16) == 0 ? 1 : 0;
     if (pair) launch(scatter_owner<DT, true>, blocks, OWNER_THREADS, smem, s, L, ncb, idx16);

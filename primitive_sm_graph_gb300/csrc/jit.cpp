@@ -64,13 +64,38 @@ psg_status compile(const std::string& src, std::vector<char>* cubin, std::string
 
 }  // namespace
 
+// what NVRTC lacks for the tensor-core skeleton: the fixed-width integer
+// types and the 128-byte tensor map the host encodes (an opaque blob)
+const char* const kGemmPreamble =
+    "typedef unsigned char uint8_t;\ntypedef unsigned short uint16_t;\ntypedef unsigned int uint32_t;\n"
+    "typedef int int32_t;\ntypedef unsigned long long uint64_t;\ntypedef long long int64_t;\n"
+    "typedef unsigned long long uintptr_t;\n"
+    "struct __align__(64) CUtensorMap { unsigned long long opaque[16]; };\n";
+
 std::string jit_source(JitSkeleton sk, const std::string& spec)
 {
     std::string s;
-    s.reserve(32768);
+    s.reserve(65536);
     s += kJitParams;
     s += "\n";
     s += kJitPrelude;
+    if (sk == JIT_GEMM) {
+        const size_t cut = spec.find('\x01');
+        s += "\n";
+        s += kGemmPreamble;
+        s += kJitGemmParams;
+        s += "\n";
+        s += kJitTcDevice;
+        s += "\n";
+        s += kJitGemmBody;
+        s += "\n// ---- operand tables ----\n";
+        s += spec.substr(0, cut);
+        s += "\n";
+        s += kJitGemmEpi;
+        s += "\n// ---- epilogue program and entry point ----\n";
+        s += cut == std::string::npos ? std::string() : spec.substr(cut + 1);
+        return s;
+    }
     s += "\n// ---- program-specific part ----\n";
     s += spec;
     s += "\n// ---- kernel skeleton ----\n";

@@ -11,9 +11,12 @@
 
 namespace psg {
 
-enum JitSkeleton { JIT_EW = 0, JIT_REDUCE = 1 };
+enum JitSkeleton { JIT_EW = 0, JIT_REDUCE = 1, JIT_GEMM = 2 };
 
 // Full source: params + prelude + `spec` (constexpr tables and bodies) + skeleton.
+// JIT_GEMM: the tensor-core contraction with a fused epilogue; `spec` is the
+// operand tables, a '\x01', then the program body and the kernel entry point,
+// around the skeleton's device helpers, kernel bodies and epilogue context.
 std::string jit_source(JitSkeleton sk, const std::string& spec);
 
 // Compile (or fetch from the cache) the kernel `name` of skeleton `sk`

@@ -63,6 +63,9 @@ struct PsgRedParams {
     int out_per_row;       /* 1: one output per row; 0: per element */
     int pad;
     int* status;           /* device status word (PSG_E_TIMEOUT), may be null */
+    long long wait_cycles; /* bound of each staged-ring wait, in SM clock cycles */
+    int skip_first_copy;   /* test hook: 1 leaves every team's first ring slot unfilled */
+    int pad2;
     struct PsgOperand in[PSG_MAXIN];
     struct PsgOperand out;
 };

@@ -53,6 +53,11 @@ __device__ __forceinline__ float negf(float x)
     asm("xor.b32 %0, %1, 0x80000000;" : "=r"(r) : "r"(__float_as_uint(x)));
     return __uint_as_float(r);
 }
+// NEG of a float64: the sign bit flipped
+__device__ __forceinline__ double negd(double x)
+{
+    return __longlong_as_double(__double_as_longlong(x) ^ (long long)0x8000000000000000ull);
+}
 __device__ __forceinline__ int w8(int x) { return (int)(signed char)(x & 0xff); }
 __device__ __forceinline__ int w16(int x) { return (int)(short)(x & 0xffff); }
 // EXP: exp(x) = 2^(x log2 e).  The product x * log2 e is carried as an
@@ -88,6 +93,7 @@ __device__ __forceinline__ int negi(int a) { return (int)(0u - (u32)a); }
 
 // ---- value type of a dtype ----------------------------------------------
 template <int DT> struct VT { typedef float T; };
+template <> struct VT<PSG_DT_F64> { typedef double T; };
 template <> struct VT<PSG_DT_I32> { typedef int T; };
 template <> struct VT<PSG_DT_I16> { typedef int T; };
 template <> struct VT<PSG_DT_I8> { typedef int T; };
@@ -97,6 +103,7 @@ template <int DT>
 __device__ __forceinline__ typename VT<DT>::T ld_cell(const void* p, i64 o)
 {
     if constexpr (DT == PSG_DT_F32) return __ldg((const float*)p + o);
+    else if constexpr (DT == PSG_DT_F64) return __ldg((const double*)p + o);
     else if constexpr (DT == PSG_DT_BF16) return __uint_as_float(((u32)__ldg((const u16*)p + o)) << 16);
     else if constexpr (DT == PSG_DT_F16) return h2f(__ldg((const u16*)p + o));
     else if constexpr (DT == PSG_DT_I32) return __ldg((const int*)p + o);
@@ -108,6 +115,7 @@ template <int DT>
 __device__ __forceinline__ void st_cell(void* p, i64 o, typename VT<DT>::T v)
 {
     if constexpr (DT == PSG_DT_F32) ((float*)p)[o] = v;
+    else if constexpr (DT == PSG_DT_F64) ((double*)p)[o] = v;
     else if constexpr (DT == PSG_DT_BF16) {
         u16 h;
         asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(v));
@@ -141,6 +149,17 @@ __device__ __forceinline__ void ld_chunk(const PsgOperand& op, i64 roff, bool ro
                 for (int v = 0; v < PSG_VEC; ++v) {
                     if constexpr (DT == PSG_DT_F32) d[v] = __uint_as_float(w[v]);
                     else d[v] = (int)w[v];
+                }
+                return;
+            }
+        } else if constexpr (DT == PSG_DT_F64) {
+            const double* q = (const double*)op.ptr + b;
+            if (nvalid == PSG_VEC && (MODE == PSG_M_VEC || (((unsigned long long)q) & 15) == 0)) {
+#pragma unroll
+                for (int u = 0; u < PSG_VEC / 2; ++u) {
+                    const double2 x = __ldg((const double2*)q + u);
+                    d[2 * u] = x.x;
+                    d[2 * u + 1] = x.y;
                 }
                 return;
             }
@@ -224,6 +243,13 @@ __device__ __forceinline__ void st_chunk(const PsgOperand& op, i64 roff, i64 col
                 }
                 ((uint4*)q)[0] = make_uint4(w[0], w[1], w[2], w[3]);
                 ((uint4*)q)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                return;
+            }
+        } else if constexpr (DT == PSG_DT_F64) {
+            double* q = (double*)op.ptr + b;
+            if (MODE == PSG_M_VEC || (((unsigned long long)q) & 15) == 0) {
+#pragma unroll
+                for (int u = 0; u < PSG_VEC / 2; ++u) ((double2*)q)[u] = make_double2(y[2 * u], y[2 * u + 1]);
                 return;
             }
         } else if constexpr (DT == PSG_DT_BF16 || DT == PSG_DT_F16 || DT == PSG_DT_I16) {

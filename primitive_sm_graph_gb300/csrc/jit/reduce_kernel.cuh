@@ -122,14 +122,14 @@ __device__ __forceinline__ bool mbar_try(unsigned long long* b, u32 parity)
     return ok != 0;
 }
 constexpr long long kWaitCycles = 2000000000ll;  // about one second
-// true when the phase completed; false after about a second (PSG_E_TIMEOUT
-// goes to the status word)
-__device__ __noinline__ bool mbar_wait(unsigned long long* b, u32 parity, int* status)
+// true when the phase completed; false once `limit` cycles have passed
+// (PSG_E_TIMEOUT goes to the status word)
+__device__ __noinline__ bool mbar_wait(unsigned long long* b, u32 parity, int* status, long long limit)
 {
     const long long t0 = clock64();
     for (u32 i = 0;; ++i) {
         if (mbar_try(b, parity)) return true;
-        if ((i & 63) == 63 && clock64() - t0 > kWaitCycles) {
+        if ((i & 7) == 7 && clock64() - t0 > limit) {
             if (status) atomicCAS(status, 0, PSG_DEV_E_TIMEOUT);
             return false;
         }
@@ -480,11 +480,18 @@ extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUS
     const i64 step = (i64)(gridDim.x / kCluster) * teams;
     const i64 first = (i64)(blockIdx.x / kCluster) * teams;
     const i64 niter = first < p.rows ? (p.rows - first + step - 1) / step : 0;
+    // a staged wait gave up: this thread stops waiting (and, as the team's
+    // issuing lane, stops filling the ring) and the kernel ends in bounded time
+    bool dead = false;
+    // ring slots lane 0 has filled, and the phase parity of each one's last
+    // fill: every copy the team issued lands before the kernel may exit
+    u32 armed = 0, armed_ph = 0;
     // staged mode: one lane of the team fills ring slot it % kNS with the
     // row of iteration it (one bulk copy per staged input)
     auto issue = [&](i64 it) {
         const i64 row = first + it * step + team;
-        if (lane != 0 || row >= p.rows) return;
+        if (lane != 0 || row >= p.rows || dead) return;
+        if (p.skip_first_copy && it == 0) return;  // test hook: a slot nothing fills
         i64 ro[kNinP];
         bool rk[kNinP];
         i64 oo;
@@ -495,6 +502,8 @@ extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUS
         // the team's reads of this slot (generic proxy) come before the copy
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_expect_tx(b, kTxBytes);
+        armed |= 1u << slot;
+        armed_ph = (armed_ph & ~(1u << slot)) | ((u32)((it / kNS) & 1) << slot);
         auto cp = [&](auto kt) {
             constexpr int K = decltype(kt)::value;
             if constexpr (kStagedIn[K])
@@ -505,7 +514,6 @@ extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUS
     if constexpr (kStaged) {
         for (i64 it = 0; it < kNS - 1 && it < niter; ++it) issue(it);
     }
-    bool dead = false;  // a staged wait gave up: stop waiting, finish in bounded time
     for (i64 it = 0; it < niter; ++it) {
         const i64 row = first + it * step + team;
         const bool active = row < p.rows;
@@ -523,7 +531,8 @@ extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUS
             if (it + kNS - 1 < niter) issue(it + kNS - 1);
             const int slot = (int)(it % kNS);
             sb = ring + (size_t)(team * kNS + slot) * kStageBytes;
-            if (active && !dead) dead = !mbar_wait(&bars[team * kNS + slot], (u32)((it / kNS) & 1), p.status);
+            if (active && !dead)
+                dead = !mbar_wait(&bars[team * kNS + slot], (u32)((it / kNS) & 1), p.status, p.wait_cycles);
         }
         // register-cache mode: load the row once
         u32 cache[kNinP][kCHP][PSG_VEC];
@@ -651,5 +660,18 @@ extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUS
         }
         // staged mode: every thread is done with this slot before it is refilled
         if constexpr (kStaged) __syncthreads();
+    }
+    // staged mode: the last fill of every slot has landed before the block's
+    // shared memory goes away (at once when every wait succeeded; after a
+    // wait gave up, the copies still in flight are waited for, bounded)
+    if constexpr (kStaged) {
+        if (lane == 0) {
+            for (int s = 0; s < kNS; ++s) {
+                if (!(armed & (1u << s))) continue;
+                const long long t0 = clock64();
+                while (!mbar_try(&bars[team * kNS + s], (armed_ph >> s) & 1u) && clock64() - t0 < kWaitCycles) {
+                }
+            }
+        }
     }
 }

@@ -20,6 +20,11 @@ std::unordered_map<uint64_t, int>& occ_cache()
     static std::unordered_map<uint64_t, int> m;
     return m;
 }
+std::unordered_map<uint64_t, cudaError_t>& smem_attr_cache()
+{
+    static std::unordered_map<uint64_t, cudaError_t> m;
+    return m;
+}
 }  // namespace
 
 int current_device()
@@ -69,6 +74,18 @@ int max_blocks_per_sm(const void* fn, int threads, size_t smem)
     std::lock_guard<std::mutex> g(g_mu);
     occ_cache()[key] = n;
     return n;
+}
+
+cudaError_t set_max_dynamic_smem(const void* fn, int bytes)
+{
+    const int d = current_device();
+    const uint64_t key = ((uint64_t)(uintptr_t)fn * 2654435761ull) ^ ((uint64_t)d << 56) ^ (uint64_t)(uint32_t)bytes;
+    std::lock_guard<std::mutex> g(g_mu);
+    auto it = smem_attr_cache().find(key);
+    if (it != smem_attr_cache().end()) return it->second;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    smem_attr_cache()[key] = e;
+    return e;
 }
 
 bool pdl_enabled()

@@ -15,6 +15,10 @@ int num_sms();                                                 // of the current
 int max_blocks_per_sm(const void* fn, int threads, size_t smem);  // occupancy, >= 1
 int kernel_regs(const void* fn);
 size_t l2_bytes();
+// cudaFuncSetAttribute(fn, MaxDynamicSharedMemorySize, bytes) on the current
+// device, made once per (device, kernel, bytes) and remembered; the attribute
+// belongs to a device, so a process that drives several GPUs sets it on each
+cudaError_t set_max_dynamic_smem(const void* fn, int bytes);
 
 // Programmatic dependent launch.  Every kernel of this library begins with
 // pdl_enter(): griddepcontrol.wait holds it until the kernel before it on the

@@ -3,6 +3,7 @@
 // cached in registers, generate the bodies, launch the specialised kernel.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <unordered_map>
 #include <mutex>
@@ -102,6 +103,13 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     }
     const int out_mode = vec_mode(fill_operand(P->p.out, out, &ov, sp, strides[0], lo[0], hi[0], false),
                                   P->p.out, dtype_size(out_v->dtype), sp);
+    // float64 nodes run in psg_elementwise only: the row kernels keep 32-bit
+    // running totals and register caches
+    for (int s = 0; s < n_stages; ++s)
+        for (int i = 0; i < stages[s].n_nodes && stages[s].prologue; ++i)
+            if (stages[s].prologue[i].dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
+    for (int i = 0; i < n_epi; ++i)
+        if (epilogue[i].dtype == PSG_F64) return PSG_E_UNSUPPORTED_DTYPE;
     // stages
     std::string bodies;
     int sop[MAX_STAGES], sdt[MAX_STAGES];
@@ -422,6 +430,17 @@ extern "C" psg_status psg_reduce_rows(const psg_reduce_stage* stages, int n_stag
     if (st != PSG_OK) return st;
     if (P.p.rows == 0) return PSG_OK;
     P.p.status = d_status;
+    P.p.wait_cycles = 2000000000ll;  // about a second at the SM clock
+    P.p.skip_first_copy = 0;
+    // Test hook, not part of the ABI: PSG_TEST_RING_TIMEOUT=1 (read at each
+    // call) leaves the first ring slot of every staged team unfilled and
+    // bounds each wait by about a millisecond, so that the wait gives up,
+    // PSG_E_TIMEOUT reaches d_status and the kernel still ends after its
+    // copies in flight have landed.
+    if (const char* t = std::getenv("PSG_TEST_RING_TIMEOUT"); t && t[0] == '1') {
+        P.p.wait_cycles = 2000000ll;
+        P.p.skip_first_copy = 1;
+    }
     cudaKernel_t k;
     st = jit_kernel(JIT_REDUCE, P.spec, "psg_reduce", &k);
     if (st != PSG_OK) return st;

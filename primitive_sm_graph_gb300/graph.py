@@ -24,6 +24,7 @@ and the stream.
 """
 from __future__ import annotations
 
+import os
 import sys
 from math import prod
 
@@ -405,11 +406,13 @@ class Executor:
 
     def __init__(self):
         self.log = []
+        self.rec = None    # the plan being recorded (see realize_all), or None
         self.status = None
         self.users = {}
         self.user_nodes = {}
         self.narrow = {}
         self.copies = {}
+        self.epi_cut = {}
 
     def prepare(self, roots):
         """Count, for every unrealized node reachable from roots, how many
@@ -429,6 +432,7 @@ class Executor:
         self.user_nodes = nodes
         self.narrow = {}
         self.copies = {}
+        self.epi_cut = {}
 
     def _only_cast_to(self, x, dt, depth=0):
         """True when every use of x (through movements) is a CAST to dt."""
@@ -488,6 +492,15 @@ class Executor:
         stored, or it runs as a stage of the one fused reduction call)."""
         if self.users.get(id(x), 0) < 2 or x.op == "CONST" or x._real is not None:
             return False
+        # a shared value computed from a contraction is stored once, by the
+        # contraction's own epilogue, instead of being recomputed from the
+        # contraction's stored result in each consumer
+        k = id(x)
+        if k not in self.epi_cut:
+            self.epi_cut[k] = False  # (a cycle of this question answers no)
+            self.epi_cut[k] = x.op in ELEMENTWISE and self._epilogue_contraction(x) is not None
+        if self.epi_cut[k]:
+            return True
         n = 0
         stack, seen = [x], set()
         while stack and n < 4:
@@ -514,13 +527,32 @@ class Executor:
     def _s(self):
         return torch.cuda.current_stream().cuda_stream
 
-    @staticmethod
-    def _workspace(nbytes):
-        return torch.empty((max(1, int(nbytes)),), dtype=torch.uint8, device="cuda")
+    def _workspace(self, nbytes):
+        ws = torch.empty((max(1, int(nbytes)),), dtype=torch.uint8, device="cuda")
+        if self.rec is not None:
+            self.rec.alloc(ws, ((max(1, int(nbytes)),), torch.uint8))
+        return ws
 
-    @staticmethod
-    def _new(shape, dtype):
-        return torch.empty(tuple(shape), dtype=torch_dtype(dtype), device="cuda")
+    def _new(self, shape, dtype):
+        t = torch.empty(tuple(shape), dtype=torch_dtype(dtype), device="cuda")
+        if self.rec is not None:
+            self.rec.alloc(t, (tuple(shape), torch_dtype(dtype)))
+        return t
+
+    def _lib(self, name):
+        """The binding's call `name`; while a plan is recorded, a wrapper
+        that also records the call when it succeeds."""
+        f = getattr(A, name)
+        rec = self.rec
+        if rec is None:
+            return f
+
+        def call(*args, **kw):
+            st = f(*args, **kw)
+            if st == A.OK:
+                rec.call(name, args, kw)
+            return st
+        return call
 
     def _pview(self, buf: torch.Tensor, v: View, dtype: str):
         return A.make_view(dtype, v.shape, v.strides, v.offset,
@@ -586,17 +618,19 @@ class Executor:
         if not fresh:
             self.copies[key] = (buf, out)
         if out.numel():
-            A.psg_permute(buf, self._pview(buf, v, dtype), list(range(len(v.shape))), out,
+            self._lib("psg_permute")(buf, self._pview(buf, v, dtype), list(range(len(v.shape))), out,
                           self._pview(out, View(v.shape), dtype), stream=self._s())
         self.log.append(("permute", v.shape))
         return out, View(v.shape)
 
     # ---- expression lowering (elementwise programs) ---------------------------
-    def _lower(self, root: Tensor, reds=None):
+    def _lower(self, root: Tensor, reds=None, acc=None):
         """(program nodes, inputs [(buf, View, dtype)]) for root's value.
         Movements are pushed into elementwise operands; other nodes are
         realized and become LOAD leaves.  reds maps id(REDUCE node) -> stage
-        index for reductions fused into the same call (read as RED)."""
+        index for reductions fused into the same call (read as RED).  acc:
+        the contraction node (or its CAST) whose value a fused contraction
+        epilogue reads as ACC (and rounds with a CAST node)."""
         prog, inputs, memo, in_memo = [], [], {}, {}
         reds = reds or {}
 
@@ -617,6 +651,13 @@ class Executor:
             if len(prog) >= A.MAX_NODES - 2:
                 raise _TooBig()
             op = t.op
+            if acc is not None and t is acc and not moves:
+                # the contraction's float32 total, rounded as its CAST rounds
+                prog.append(A.node("ACC", dtype="f32"))
+                if t.op == "CAST" and t.dtype != "f32":
+                    prog.append(A.node("CAST", len(prog) - 1, dtype=t.dtype))
+                memo[key] = len(prog) - 1
+                return len(prog) - 1
             if t._real is not None and op != "CONST":
                 # already in memory: a leaf, whatever computed it
                 buf, v = self._apply_moves(*t._real, [m for m in moves], t.dtype)
@@ -687,6 +728,9 @@ class Executor:
                 r = self._try_contract(x, (), base.dtype, x.shape)
                 if r is not None:
                     return self._apply_moves(*r, list(reversed(inner)) + list(reversed(moves)), base.dtype)
+        fused = self._try_contract_epilogue(t)
+        if fused is not None:
+            return fused
         fused = self._try_fused_reduce(t)
         if fused is not None:
             return fused
@@ -698,10 +742,130 @@ class Executor:
                 self._split(t)
         out = self._new(t.shape, t.dtype)
         if out.numel():
-            A.psg_elementwise(prog, [b for b, _, _ in inputs], [self._pview(b, v, d) for b, v, d in inputs],
+            self._lib("psg_elementwise")(prog, [b for b, _, _ in inputs], [self._pview(b, v, d) for b, v, d in inputs],
                               out, self._pview(out, View(t.shape), t.dtype), stream=self._s())
         self.log.append(("elementwise", t.shape, len(prog)))
         return out, View(t.shape)
+
+    @staticmethod
+    def _unit_moves(x: Tensor):
+        """The node below a chain of movements that only add, drop or move
+        dims of size 1 (the cells keep their order and their index along
+        every other dim), starting at x; x itself when there is none."""
+        while x.op == "MOVE" and x._real is None:
+            kind, arg = x.arg[0], x.arg[1]
+            src = x.src[0]
+            if kind == "reshape":
+                if [s for s in src.shape if s != 1] != [s for s in x.shape if s != 1]:
+                    break
+            elif kind == "permute":
+                big = [p for p in arg if src.shape[p] != 1]
+                if big != sorted(big):
+                    break
+            else:
+                break
+            x = src
+        return x
+
+    def _pending_contraction(self, s: Tensor):
+        """True for a contraction not computed yet in any width."""
+        return (s._real is None and not any((id(s), d) in self.narrow for d in ("bf16", "f16"))
+                and self._contract_pattern(s) is not None)
+
+    def _epilogue_contraction(self, t: Tensor):
+        """(top, SUM node) of the one unrealized contraction that t's
+        elementwise program reads directly, through a CAST to a half width or
+        as its float32 value, with at most unit-dim movements between (top:
+        the node the program reads, a CAST or the float32 value), when every
+        use of it lies inside that program; else None."""
+        found, region, seen, stack = [], {}, set(), [t]
+        while stack:
+            x = stack.pop()
+            if id(x) in seen or x._real is not None:
+                continue
+            seen.add(id(x))
+            if x is not t and x.op in ELEMENTWISE and self._shared_heavy(x):
+                continue  # stored on its own: a leaf of this program
+            if x.op == "CAST" and x.dtype in ("bf16", "f16"):
+                s = self._unit_moves(x.src[0])
+                if s.op == "SUM" and self._pending_contraction(s):
+                    found.append((x, s))
+                    continue
+            s = self._unit_moves(x)
+            if s.op == "SUM" and s.dtype == "f32" and self._pending_contraction(s):
+                found.append((x, s))
+                continue
+            if x.op in REDUCE:
+                return None  # a row reduction: the fused reduction path takes it
+            if x.op in ELEMENTWISE:
+                region[id(x)] = x
+                stack.extend(x.src)
+        if len(found) != 1:
+            return None
+        top, s = found[0]
+        if top is t or any(id(u) not in region for u in self.user_nodes.get(id(top), [])):
+            return None
+        # no value computed from the contraction below t is read from outside
+        # this program (else that reader would need the contraction again)
+        dep = {id(top): True}
+
+        def depends(x):
+            if id(x) not in dep:
+                dep[id(x)] = False
+                dep[id(x)] = id(x) in region and any(depends(y) for y in x.src)
+            return dep[id(x)]
+        for i, x in region.items():
+            if x is not t and depends(x) and any(id(u) not in region for u in self.user_nodes.get(i, [])):
+                return None
+        # the nodes between top and the SUM feed nothing else
+        y = top.src[0] if top.op == "CAST" else top
+        while y is not s:
+            if self.users.get(id(y), 0) != 1:
+                return None
+            y = y.src[0]
+        if self.users.get(id(s), 0) != 1:
+            return None
+        # a program of nothing but roundings is the contraction's own store
+        if not any(x.op not in ("CAST", "CONST") for x in region.values()):
+            return None
+        out_shape = tuple(s.shape[:-1]) if s.shape and s.shape[-1] == 1 else tuple(s.shape)
+        if [d for d in t.shape if d != 1] != [d for d in out_shape if d != 1]:
+            return None
+        (x, _, wx), (y, _, wy) = self._contract_pattern(s)
+        if (wx or x.dtype) not in ("bf16", "f16") or (wy or y.dtype) != (wx or x.dtype):
+            return None
+        return top, s
+
+    def _try_contract_epilogue(self, t: Tensor):
+        """An elementwise value computed from one contraction (a residual add,
+        a ReLU, a cast): the contraction's kernel computes it in its epilogue
+        (psg_contract's epilogue program, ACC the float32 total), so the
+        contraction's result never goes through memory (limn, "Reading the
+        schedule": elementwise work fuses into the kernel that produces its
+        operand).  None when t is not of that form or the call cannot take
+        it (then t is computed the ordinary way)."""
+        if t.op not in ELEMENTWISE or t.op == "CONST" or t.dtype not in ("f32", "bf16", "f16"):
+            return None
+        hit = self._epilogue_contraction(t)
+        if hit is None:
+            return None
+        top, s = hit
+        try:
+            prog, inputs = self._lower(t, acc=top)
+        except _TooBig:
+            return None
+        S = s.src[0].shape
+        conv = []
+        for b, v, d in inputs:
+            v2 = v.reshape(tuple(S[:-1])) if v.mask is None else None
+            if v2 is None:
+                return None
+            conv.append((b, v2, d))
+        r = self._try_contract(s, (), t.dtype, tuple(S[:-1]), epilogue=(prog, conv))
+        if r is None:
+            return None
+        buf, v = r
+        return buf, v.reshape(t.shape)
 
     def _split(self, t: Tensor):
         """A program too large for one call: realize the operand subtree with
@@ -870,7 +1034,7 @@ class Executor:
         out_dt = epi_root.dtype if epi_root is not None else order[-1].dtype
         out = self._new(out_shape, out_dt)
         if out.numel():
-            A.psg_reduce_rows(stages, epi, [b for b, _, _ in inputs],
+            self._lib("psg_reduce_rows")(stages, epi, [b for b, _, _ in inputs],
                               [self._pview(b, v, d) for b, v, d in inputs], out,
                               self._pview(out, View(out_shape), out_dt), stream=self._s())
         self.log.append(("reduce_rows", order[0].src[0].shape, len(stages), "per_row" if per_row else "per_elem"))
@@ -937,7 +1101,10 @@ class Executor:
             ops.append((x, mv, widen))
         return ops
 
-    def _try_contract(self, r: Tensor, _moves, out_dtype, out_shape):
+    def _try_contract(self, r: Tensor, _moves, out_dtype, out_shape, epilogue=None):
+        """r, a contraction, as one psg_contract call writing out_dtype; with
+        epilogue = (program, inputs [(buf, View, dtype)] over r's shape) the
+        call's epilogue program computes the stored value from the total."""
         if r.op != "SUM" or r._real is not None:
             return None
         pat = self._contract_pattern(r)
@@ -988,12 +1155,15 @@ class Executor:
                 st = [v[a] for v in views]
             return size, st
 
-        gm = merged(Mx, [vx.strides, ostr])
-        gn = merged(Nx, [vy.strides, ostr])
+        estr = [v.strides for _, v, _ in epilogue[1]] if epilogue else []
+        gm = merged(Mx, [vx.strides, ostr] + estr)
+        gn = merged(Nx, [vy.strides, ostr] + estr)
         if gm is None or gn is None:
             return None
         # batch axes: kept separately when they do not merge (the ABI takes up to 3)
-        gb = merged(Bx, [vx.strides, vy.strides, ostr])
+        gb = merged(Bx, [vx.strides, vy.strides, ostr] + estr)
+        if Bx and gb is None and epilogue:
+            return None
         if Bx and gb is None:
             # batch dims that do not merge (e.g. heads split out of a fused
             # projection): store each operand compactly, so they do
@@ -1013,14 +1183,27 @@ class Executor:
         Av = A.make_view(dx, shape, sa, vx.offset, None, bx.numel())
         Bv = A.make_view(dy, shape, sb, vy.offset, None, by.numel())
         Cv = A.make_view(out_dtype, shape[:-1], sc, 0, None, out.numel())
+        if epilogue:
+            prog, inputs = epilogue
+            ev = [A.make_view(d, shape[:-1], [gb[1][3 + k]] * bool(Bx) + [gm[1][2 + k], gn[1][2 + k]], v.offset,
+                              None, b.numel()) for k, (b, v, d) in enumerate(inputs)]
+            if out.numel():
+                st = self._lib("psg_contract")(bx, Av, by, Bv, out, Cv, self._status(), stream=self._s(), check=False,
+                                    epilogue=(prog, [b for b, _, _ in inputs], ev))
+                if st == A.E_UNSUPPORTED_LAYOUT:
+                    return None  # not a tensor-core contraction: computed the ordinary way
+                if st != A.OK:
+                    raise A.PsgError(st, "psg_contract")
+            self.log.append(("contract", tuple(shape), dx, out_dtype, len(prog)))
+            return out, View(out_shape)
         if out.numel():
             need = A.psg_contract_workspace(Av, Bv, Cv)
             if need:
                 # few output tiles over a long K: the kernel splits K into this workspace
                 ws = self._workspace(need)
-                A.psg_contract_ws(bx, Av, by, Bv, out, Cv, ws, ws.numel(), self._status(), stream=self._s())
+                self._lib("psg_contract_ws")(bx, Av, by, Bv, out, Cv, ws, ws.numel(), self._status(), stream=self._s())
             else:
-                A.psg_contract(bx, Av, by, Bv, out, Cv, self._status(), stream=self._s())
+                self._lib("psg_contract")(bx, Av, by, Bv, out, Cv, self._status(), stream=self._s())
         self.log.append(("contract", tuple(shape), dx, out_dtype))
         return out, View(out_shape)
 
@@ -1072,7 +1255,7 @@ class Executor:
             (bq, vq), (bk, vk), (bv, vv) = (self._attn_operand(x) for x in t.src)
         out = self._new(t.shape, "bf16")
         lse = self._new((B, H, T), "f32")
-        A.psg_attention_fwd(bq, self._pview(bq, vq, "bf16"), bk, self._pview(bk, vk, "bf16"), bv,
+        self._lib("psg_attention_fwd")(bq, self._pview(bq, vq, "bf16"), bk, self._pview(bk, vk, "bf16"), bv,
                             self._pview(bv, vv, "bf16"), out, self._pview(out, View(t.shape), "bf16"), lse, scale,
                             causal, self._status(), stream=self._s())
         t._aux = lse
@@ -1099,7 +1282,7 @@ class Executor:
                   for i in range(3)]
         delta = self._new((B, H, T), "f32")
         pv = lambda bv: self._pview(bv[0], bv[1], "bf16")
-        A.psg_attention_bwd(ops[0][0], pv(ops[0]), ops[1][0], pv(ops[1]), ops[2][0], pv(ops[2]), bo, pv((bo, vo)),
+        self._lib("psg_attention_bwd")(ops[0][0], pv(ops[0]), ops[1][0], pv(ops[1]), ops[2][0], pv(ops[2]), bo, pv((bo, vo)),
                             ops[3][0], pv(ops[3]), lse, delta, out, pv((out, gv[0])), out, pv((out, gv[1])), out,
                             pv((out, gv[2])), scale, causal, self._status(), stream=self._s())
         self.log.append(("attention_bwd", fwd.shape))
@@ -1113,7 +1296,7 @@ class Executor:
             bi, vi = self._copy_contig(bi, vi, "i32")
         out = self._new(t.shape, t.dtype)
         n = t.shape[0]
-        A.psg_gather(bs, self._pview(bs, vs, src.dtype), bi, n, out, self._pview(out, View(t.shape), t.dtype),
+        self._lib("psg_gather")(bs, self._pview(bs, vs, src.dtype), bi, n, out, self._pview(out, View(t.shape), t.dtype),
                      self._status(), stream=self._s())
         self.log.append(("gather", t.shape))
         return out, View(t.shape)
@@ -1137,7 +1320,7 @@ class Executor:
         bu, vu = self.realize(upd)
         n = idx.shape[0]
         ws = self._workspace(A.psg_scatter_workspace(n))
-        A.psg_scatter_add(out, self._pview(out, vo, t.dtype), bi, n, bu, self._pview(bu, vu, upd.dtype), ws,
+        self._lib("psg_scatter_add")(out, self._pview(out, vo, t.dtype), bi, n, bu, self._pview(bu, vu, upd.dtype), ws,
                           ws.numel(), self._status(), stream=self._s())
         self.log.append(("scatter_add", t.shape, n))
         return out, vo
@@ -1215,17 +1398,138 @@ def _executor() -> Executor:
     return _EXEC
 
 
+class _Ref:
+    """A buffer argument of a recorded call: a leaf of the graph, a buffer
+    the schedule allocated, the status word or the current stream."""
+    __slots__ = ("kind", "i")
+
+    def __init__(self, kind, i=0):
+        self.kind, self.i = kind, i
+
+
+class _Plan:
+    """The library calls one graph structure was realized into, recorded
+    once (limn, "Reading the schedule": the compiled devices cache execution
+    plans by graph structure).  Replaying it rebinds the buffers and makes
+    the same calls: no scheduling, lowering or program building."""
+
+    def __init__(self, ex, leaves):
+        self.refs = {id(b): _Ref("leaf", i) for i, b in reversed(list(enumerate(leaves)))}
+        self.refs[id(ex._status())] = _Ref("status")
+        self.allocs, self.keep, self.calls, self.outs, self.log = [], [], [], [], []
+        self.ok = True
+
+    def alloc(self, t, spec):
+        self.refs[id(t)] = _Ref("tmp", len(self.allocs))
+        self.allocs.append(spec)
+        self.keep.append(t)
+
+    def sym(self, x, key=None):
+        if key == "stream":
+            return _Ref("stream")
+        if isinstance(x, torch.Tensor):
+            r = self.refs.get(id(x))
+            if r is None:
+                self.ok = False  # a buffer from elsewhere: this schedule is not recorded
+            return r
+        if isinstance(x, (list, tuple)):
+            return type(x)(self.sym(y) for y in x)
+        return x
+
+    def call(self, name, args, kw):
+        self.calls.append((name, self.sym(args), {k: self.sym(v, k) for k, v in kw.items()}))
+
+    def run(self, ex, leaves, roots):
+        status, stream = ex._status(), ex._s()
+        tmps = [torch.empty(shape, dtype=dt, device=status.device) for shape, dt in self.allocs]
+
+        def val(x):
+            if isinstance(x, _Ref):
+                return (leaves[x.i] if x.kind == "leaf" else tmps[x.i] if x.kind == "tmp"
+                        else status if x.kind == "status" else stream)
+            if isinstance(x, (list, tuple)):
+                return type(x)(val(y) for y in x)
+            return x
+        for name, args, kw in self.calls:
+            getattr(A, name)(*val(args), **{k: val(v) for k, v in kw.items()})
+        ex.log.extend(self.log)
+        out = []
+        for t, (ref, v, dt) in zip(roots, self.outs):
+            buf = val(ref)
+            t._real = (buf, v)
+            out.append(_as_torch(buf, v, dt))
+        return out
+
+
+#: graph structure -> recorded plan; PLAN_CACHE = False (or PSG_NO_PLAN_CACHE
+#: in the environment) schedules every realization afresh
+_PLANS = {}
+PLAN_CACHE = os.environ.get("PSG_NO_PLAN_CACHE") is None
+_PLAN_LIMIT = 256
+
+
+def _structure(roots):
+    """(key, leaf buffers) of the unrealized graph under roots: every node's
+    op, dtype, shape, argument and operands by position, every leaf's
+    layout, size, alignment and aliasing; equal keys schedule alike."""
+    index, items, leaves, first_ptr = {}, [], [], {}
+    stack = [(r, False) for r in reversed(roots)]
+    while stack:
+        t, done = stack.pop()
+        if id(t) in index:
+            continue
+        if t._real is not None:
+            buf, v = t._real
+            p = buf.data_ptr()
+            aux = getattr(t, "_aux", None)
+            items.append(("L", t.dtype, t.shape, v.key(), str(buf.dtype), buf.numel(), p % 256,
+                          first_ptr.setdefault(p, len(leaves)), aux is not None))
+            leaves.append(buf)
+            if aux is not None:
+                leaves.append(aux)
+            index[id(t)] = len(items) - 1
+            continue
+        if not done:
+            stack.append((t, True))
+            stack.extend((s, False) for s in reversed(t.src) if id(s) not in index)
+            continue
+        items.append((t.op, t.dtype, t.shape, repr(t.arg), tuple(index[id(s)] for s in t.src)))
+        index[id(t)] = len(items) - 1
+    return (tuple(items), tuple(index[id(r)] for r in roots)), leaves
+
+
 def realize_all(*ts):
     """Realize several values with one schedule (shared subexpressions are
-    computed once) and return them as torch tensors."""
+    computed once) and return them as torch tensors.  The schedule of a
+    graph structure seen before is replayed from the plan cache."""
     ex = _executor()
+    key = leaves = None
+    if PLAN_CACHE:
+        key, leaves = _structure(ts)
+        plan = _PLANS.get(key)
+        if plan is not None:
+            return plan.run(ex, leaves, ts)
     ex.prepare(ts)
-    out = []
-    for t in ts:
-        buf, v = ex.realize(t)
-        if v.mask is not None:
-            buf, v = ex._copy_contig(buf, v, t.dtype, fresh=True)
-        out.append(_as_torch(buf, v, t.dtype))
+    rec = _Plan(ex, leaves) if key is not None else None
+    ex.rec = rec
+    n0 = len(ex.log)
+    try:
+        out = []
+        for t in ts:
+            buf, v = ex.realize(t)
+            if v.mask is not None:
+                buf, v = ex._copy_contig(buf, v, t.dtype, fresh=True)
+            out.append(_as_torch(buf, v, t.dtype))
+            if rec is not None:
+                rec.outs.append((rec.sym(buf), v, t.dtype))
+    finally:
+        ex.rec = None
+    if rec is not None and rec.ok:
+        rec.log = ex.log[n0:]
+        rec.keep = []
+        if len(_PLANS) >= _PLAN_LIMIT:
+            _PLANS.pop(next(iter(_PLANS)))
+        _PLANS[key] = rec
     return out
 
 

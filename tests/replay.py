@@ -16,7 +16,8 @@ by node):
 * Contractions: |c - c*| <= (1 + 2^-8) * 2 gamma_{K-1} sum_k |a_k b_k|
   + 2^-8 |c*| for a bfloat16 output (2^-11 for float16), with c* the oracle's
   float32 total: the reduction-order bound (Litmus, "ToleranceBound") plus
-  one rounding into the narrow output.
+  one rounding into the narrow output.  With a fused epilogue program, the
+  hull rule below, with the total itself the value moved by that bound.
 * Row reductions, and elementwise programs with EXP or LOG: the oracle runs
   the call again with every value that may legitimately differ moved to
   either edge of its allowance, and the GPU cell must lie in the hull of
@@ -266,6 +267,68 @@ def movable_items(stages, epi, stage_dts):
     return items
 
 
+def check_contract(O, P, rec, a3, b3, K, got, out_dt, epi=None):
+    """A contraction's cells got ([Z, M, N] oracle tensor of the GPU's C)
+    against the oracle's naive loop over the same operands a3 [Z, M, K] and
+    b3 [Z, N, K]; epi: None, or (epilogue nodes, its inputs read at
+    [Z, M, N]) for a fused epilogue program."""
+    acc = "f64" if a3.dt == "f64" else ("i32" if a3.dt.startswith("i") else "f32")
+    if acc == "i32":
+        raise NotImplementedError("integer contractions are checked by their own tests")
+    ref = P.contract(a3, b3, acc)
+    r = ref.f64()
+    mag = np.abs(a3.f64()) @ np.abs(b3.f64()).transpose(0, 2, 1)
+    move = (1 + 2.0 ** -8) * 2 * gamma(K - 1) * mag
+    if a3.dt == "f32":
+        move = move + 2.0 ** -18 * mag  # three-term TF32 products: a few 2^-20 each
+    if epi is not None:
+        nodes, loads = epi
+        items = ["acc"] + [("epilogue", i) for i, n in enumerate(nodes) if n[0] in ("EXP", "LOG")]
+
+        def run(signs):
+            s = signs["acc"]
+            total = O.T(_round_out_f32(r + s * move, s), "f32")
+
+            def hook(kind, i, x):
+                d = signs.get(("epilogue", i))
+                return step_units(x, d, 8 if x.dt == "f32" else 1) if d else x
+            return P.program(nodes, loads, total.shape, hook=hook, acc=total)
+        plain = P.program(nodes, loads, ref.shape, acc=ref)
+        check_hull(rec, got, plain, perturbed_runs(O, run, items), out_dt)
+        rec.note = (rec.note + " epilogue %d nodes" % len(nodes)).strip()
+        return
+    g = got.f64()
+    tol = move
+    if out_dt == "bf16":
+        tol = tol + 2.0 ** -8 * np.abs(r) + 2.0 ** -133
+    elif out_dt == "f16":
+        tol = tol + 2.0 ** -11 * np.abs(r) + 2.0 ** -25
+    else:
+        tol = tol + 2.0 ** -149
+    err = np.abs(g - r)
+    ok = err <= tol
+    ok |= np.isnan(g) & np.isnan(r)
+    rec.cells = ok.size
+    rec.bad = int((~ok).sum())
+    rec.worst = float(np.max(np.where(np.isfinite(err), err / tol, 0.0))) if ok.size else 0.0
+    if rec.bad:
+        i = np.unravel_index(int(np.argmax(~ok)), ok.shape)
+        rec.note = "first bad cell %s: got %r, oracle %r, tol %r" % (i, g[i], r[i], tol[i])
+
+
+def read_epilogue(O, P, A, epilogue, dims):
+    """(nodes, inputs read at [Z, M, N]) of an epilogue argument, or None."""
+    if not epilogue or not epilogue[0]:
+        return None
+    prog, ins, views = epilogue
+    Z, M, N, _ = dims
+    loads = []
+    for b, v in zip(ins, views):
+        x = read_view(O, P, A, b, v)
+        loads.append(O.T(x.data.reshape(Z, M, N), x.dt))
+    return ndesc(A, prog), loads
+
+
 # -------------------------------------------------------------- replayer ---
 
 class Replayer:
@@ -382,45 +445,23 @@ class Replayer:
         b3 = O.T(b3.data.reshape(Z, N, K), bdt)
         return a3, b3, (Z, M, N, K)
 
-    def _contract_check(self, rec, a3, b3, dims, Cb, Cv):
+    def _contract_check(self, rec, a3, b3, dims, Cb, Cv, epi=None):
         A, O, P = self.A, self.O, self.P
         Z, M, N, K = dims
         cdt, csh, cst, coff, _ = vdesc(A, Cv)
-        acc = "f64" if a3.dt == "f64" else ("i32" if a3.dt.startswith("i") else "f32")
-        if acc == "i32":
-            raise NotImplementedError("integer contractions are checked by their own tests")
-        ref = P.contract(a3, b3, acc)
-        got = P.read(snap(Cb, cdt, Cv.extent), cdt, csh, cst, coff).f64().reshape(Z, M, N)
-        r = ref.f64()
-        mag = np.abs(a3.f64()) @ np.abs(b3.f64()).transpose(0, 2, 1)
-        tol = (1 + 2.0 ** -8) * 2 * gamma(K - 1) * mag
-        if a3.dt == "f32":
-            tol = tol + 2.0 ** -18 * mag  # three-term TF32 products: a few 2^-20 each
-        if cdt == "bf16":
-            tol = tol + 2.0 ** -8 * np.abs(r) + 2.0 ** -133
-        elif cdt == "f16":
-            tol = tol + 2.0 ** -11 * np.abs(r) + 2.0 ** -25
-        else:
-            tol = tol + 2.0 ** -149
-        err = np.abs(got - r)
-        ok = err <= tol
-        ok |= np.isnan(got) & np.isnan(r)
-        rec.cells = ok.size
-        rec.bad = int((~ok).sum())
-        rec.worst = float(np.max(np.where(np.isfinite(err), err / tol, 0.0))) if ok.size else 0.0
-        if rec.bad:
-            i = np.unravel_index(int(np.argmax(~ok)), ok.shape)
-            rec.note = "first bad cell %s: got %r, oracle %r, tol %r" % (i, got[i], r[i], tol[i])
+        got = P.read(snap(Cb, cdt, Cv.extent), cdt, csh, cst, coff)
+        check_contract(O, P, rec, a3, b3, K, O.T(got.data.reshape(Z, M, N), cdt), cdt, epi)
 
     def _contract(self, f):
         def w(Ab, Av, Bb, Bv, Cb, Cv, *a, **k):
             self.sync()
             rec = self._rec("contract", "")
             a3, b3, dims = self._contract_common(rec, Ab, Av, Bb, Bv, Cb, Cv)
+            epi = read_epilogue(self.O, self.P, self.A, k.get("epilogue"), dims)
             st = f(Ab, Av, Bb, Bv, Cb, Cv, *a, **k)
             self.sync()
             rec.desc = "Z%d M%d N%d K%d -> %s" % (dims + (self.A.DTYPE_NAMES[Cv.dtype],))
-            self._contract_check(rec, a3, b3, dims, Cb, Cv)
+            self._contract_check(rec, a3, b3, dims, Cb, Cv, epi)
             return st
         return w
 
@@ -429,10 +470,11 @@ class Replayer:
             self.sync()
             rec = self._rec("contract_ws", "")
             a3, b3, dims = self._contract_common(rec, Ab, Av, Bb, Bv, Cb, Cv)
+            epi = read_epilogue(self.O, self.P, self.A, k.get("epilogue"), dims)
             st = f(Ab, Av, Bb, Bv, Cb, Cv, ws, ws_bytes, *a, **k)
             self.sync()
             rec.desc = "Z%d M%d N%d K%d -> %s (split K)" % (dims + (self.A.DTYPE_NAMES[Cv.dtype],))
-            self._contract_check(rec, a3, b3, dims, Cb, Cv)
+            self._contract_check(rec, a3, b3, dims, Cb, Cv, epi)
             return st
         return w
 

@@ -53,9 +53,9 @@ def test_elementwise_rejects_bad_arguments(A):
     shape_mismatch = A.make_view("f32", (4, 5))
     assert A.psg_elementwise(_copy_prog(), [fake], [shape_mismatch], fake, out, stream=0,
                              check=False) == A.E_INVALID_ARG
+    # a float64 load into a float32 result without a CAST: the dtype rules refuse it
     f64 = A.make_view("f64", (4, 4))
-    assert A.psg_elementwise([A.node("LOAD", 0, dtype="f64")], [fake], [f64], fake,
-                             A.make_view("f64", (4, 4)), stream=0,
+    assert A.psg_elementwise([A.node("LOAD", 0, dtype="f64")], [fake], [f64], fake, out, stream=0,
                              check=False) == A.E_UNSUPPORTED_DTYPE
     # output must be injective: a stride-0 dim of size 4
     aliased = A.make_view("f32", (4, 4), strides=(4, 0), extent=16)
@@ -205,3 +205,60 @@ def test_columnar_reductions_compile_without_a_gpu(A):
     st = run([(A.RED_MAX, s1), (A.RED_SUM, s2)], epi, [v], A.make_view("f32", (300, 64), (1, 300), 0, None,
                                                                          64 * 300))
     assert st == 0, (A.STATUS.get(st), buf.value.decode()[:3000])
+    # staged rows (contiguous, 16-byte aligned, >= 512 bytes a row): the
+    # shared-memory ring with its bounded waits and final drain compiles
+    v = A.make_view("f32", (300, 1024))
+    st = run([(A.RED_MAX, s1), (A.RED_SUM, s2)], epi, [v], A.make_view("f32", (300, 1024)))
+    assert st == 0, (A.STATUS.get(st), buf.value.decode()[:3000])
+
+
+def test_contraction_epilogue_kernels_compile_without_a_gpu(A):
+    """A contraction with a fused epilogue program (ACC cast to bf16 plus a
+    bf16 residual, then a ReLU) plans and compiles both tensor-core kernels
+    (single CTA and CTA pair) through NVRTC; a program that reads a missing
+    input is refused before any compile."""
+    L = A.lib
+    f = L.psg_internal_compile_contract_epilogue
+    V = ctypes.POINTER(A.psg_view)
+    f.argtypes = [V, V, V, ctypes.POINTER(A.psg_epilogue), ctypes.c_char_p, ctypes.c_size_t]
+    M, N, K = 1024, 512, 512
+    Av = A.make_view("bf16", (M, N, K), (K, 0, 1), 0, None, M * K)
+    Bv = A.make_view("bf16", (M, N, K), (0, 1, N), 0, None, K * N)
+    Cv = A.make_view("bf16", (M, N))
+    n = A.node
+    prog = [n("ACC"), n("CAST", 0, dtype="bf16"), n("LOAD", 0, dtype="bf16"), n("ADD", 1, 2, dtype="bf16"),
+            n("CONST", dtype="bf16"), n("CMPLT", 4, 3, dtype="bf16"), n("WHERE", 5, 3, 4, dtype="bf16")]
+    arr = (A.psg_node * len(prog))(*prog)
+    views = (A.psg_view * 1)(A.make_view("bf16", (M, N)))
+    e = A.psg_epilogue(ctypes.cast(arr, ctypes.POINTER(A.psg_node)), len(prog), 1, None,
+                       ctypes.cast(views, V))
+    buf = ctypes.create_string_buffer(1 << 16)
+    st = f(ctypes.byref(Av), ctypes.byref(Bv), ctypes.byref(Cv), ctypes.byref(e), buf, len(buf))
+    assert st == 0, (A.STATUS.get(st), buf.value.decode()[:3000])
+    bad = (A.psg_node * 1)(n("LOAD", 1, dtype="bf16"))
+    e2 = A.psg_epilogue(ctypes.cast(bad, ctypes.POINTER(A.psg_node)), 1, 1, None, ctypes.cast(views, V))
+    assert f(ctypes.byref(Av), ctypes.byref(Bv), ctypes.byref(Cv), ctypes.byref(e2), buf, len(buf)) == \
+        A.E_INVALID_ARG
+
+
+def test_float64_programs_compile_and_rows_refuse_them(A):
+    """float64 nodes (limn, "The op set": float64 computes natively) compile
+    in psg_elementwise with every op and every CAST to and from float64; the
+    row reductions, which keep 32-bit totals, refuse a float64 node."""
+    f = _compile_hook(A)
+    buf = ctypes.create_string_buffer(1 << 16)
+    n = A.node
+    prog = [n("LOAD", 0, dtype="f64"), n("LOAD", 1, dtype="f32"), n("CAST", 1, dtype="f64"),
+            n("ADD", 0, 2, dtype="f64"), n("MUL", 3, 0, dtype="f64"), n("NEG", 4, dtype="f64"),
+            n("EXP", 5, dtype="f64"), n("LOG", 6, dtype="f64"), n("SQRT", 0, dtype="f64"),
+            n("RECIP", 8, dtype="f64"), n("CMPLT", 7, 9, dtype="f64"), n("CONST", dtype="f64", cval=0.1),
+            n("WHERE", 10, 9, 11, dtype="f64"), n("CAST", 12, dtype="bf16"), n("CAST", 13, dtype="f64"),
+            n("CAST", 14, dtype="i32"), n("CAST", 15, dtype="f64")]
+    views = (A.psg_view * 2)(A.make_view("f64", (37, 301)), A.make_view("f32", (37, 301)))
+    arr = (A.psg_node * len(prog))(*prog)
+    st = f(arr, len(prog), views, 2, ctypes.byref(A.make_view("f64", (37, 301))), buf, len(buf))
+    assert st == 0, (A.STATUS.get(st), buf.value.decode()[:3000])
+    rv = A.make_view("f64", (8, 100))
+    st = A.psg_reduce_rows([(A.RED_SUM, [n("LOAD", 0, dtype="f64")])], None, [4096], [rv], 4096,
+                           A.make_view("f64", (8,)), stream=0, check=False)
+    assert st == A.E_UNSUPPORTED_DTYPE

@@ -6,6 +6,8 @@ Bar (the reduction-order term of Litmus's ToleranceBound, per output cell):
   |c - c_ref| <= 2^-7 |c_ref| + 2*gamma_{K-1} * sum|a b|    (bfloat16 output)
 where c_ref is the oracle's float32 total.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -161,6 +163,53 @@ def test_full_size_bf16_sampled(A, O):
 def test_full_size_f32_sampled(A, O):
     a, b = SI.contraction_f32(0)
     _sampled_full(A, O, a, b, "f32", 2000, 2)
+
+
+def _host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _full_matrix(A, O, a, b, out_dt):
+    """Every cell of the workload's product against the oracle's naive loop
+    (float32 totals, k ascending), run on all the host's cores; the bound per
+    cell is the one above, with sum |a b| from a float64 product of the
+    magnitudes."""
+    M, K = a.shape
+    N = b.shape[1]
+    dA, dB = dev(a), dev(b)
+    Av, Bv = _views(A, dA, dB, M, N, K)
+    C = torch.empty((M, N), dtype=storage_dtype(out_dt), device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    A.psg_contract(dA, Av, dB, Bv, C, A.view_of(C), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = O.T(to_np(C.cpu()), out_dt).f64()
+    del C, dA, dB
+    dt = "bf16" if a.dtype == torch.bfloat16 else "f32"
+    old = O.NTHREADS
+    O.NTHREADS = _host_threads()
+    try:
+        ref = O.matmul_bt(O.T(SI.bits(a), dt), O.transpose(O.T(SI.bits(b), dt)), "f32").data
+    finally:
+        O.NTHREADS = old
+    mag = np.abs(a.double().numpy()) @ np.abs(b.double().numpy())
+    _check(got, ref, mag, K, out_dt)
+
+
+def test_full_size_bf16_every_cell(A, O):
+    """C4a at its full size (8192^3, bf16 in, bf16 out): all 67,108,864 cells."""
+    a, b = SI.contraction_bf16(0)
+    _full_matrix(A, O, a, b, "bf16")
+
+
+def test_full_size_f32_every_cell(A, O):
+    """C4b at its full size (4096^3 float32, 3xTF32 on the tensor cores): all
+    16,777,216 cells."""
+    a, b = SI.contraction_f32(0)
+    _full_matrix(A, O, a, b, "f32")
 
 
 def _f32_tc_case(A, O, M, N, K, a_layout="mk", b_layout="kn", out_dt="f32", seed=0):

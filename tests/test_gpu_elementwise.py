@@ -109,10 +109,10 @@ def _make_inputs(g, shape, dts):
     return out
 
 
-def _random_program(g, n_in, in_dts, int_mode, n_ops, transcendental_last):
+def _random_program(g, n_in, in_dts, int_mode, n_ops, transcendental_last, pool=None):
     """A random DAG as (op, args, dtype) in topological order."""
     P = [("LOAD", (k,), in_dts[k]) for k in range(n_in)]
-    dts_pool = INT_DT if int_mode else FLOAT_DT
+    dts_pool = pool or (INT_DT if int_mode else FLOAT_DT)
 
     def pick(pred=None):
         cands = [i for i in range(len(P)) if pred is None or pred(P[i][2])]
@@ -130,7 +130,7 @@ def _random_program(g, n_in, in_dts, int_mode, n_ops, transcendental_last):
             op = unary[int(torch.randint(0, len(unary), (1,), generator=g))]
             i = pick()
             if op == "CAST":
-                dt = dts_pool[int(torch.randint(0, 3, (1,), generator=g))]
+                dt = dts_pool[int(torch.randint(0, len(dts_pool), (1,), generator=g))]
                 if not int_mode and float(torch.rand(1, generator=g)) < 0.2:
                     dt = "i32"
                 P.append(("CAST", (i,), dt))
@@ -154,7 +154,7 @@ def _random_program(g, n_in, in_dts, int_mode, n_ops, transcendental_last):
             P.append(("WHERE", (c, x, y), P[x][2]))
     last = len(P) - 1
     if transcendental_last:
-        if P[last][2] not in FLOAT_DT:
+        if P[last][2] not in (pool or FLOAT_DT):
             P.append(("CAST", (last,), "f32"))
             last += 1
         P.append((["EXP", "LOG"][int(torch.randint(0, 2, (1,), generator=g))], (last,), P[last][2]))
@@ -191,18 +191,18 @@ def _oracle_eval(O, P, inputs, shape):
     return vals[-1]
 
 
-def _fuzz(A, O, seed, int_mode, transcendental_last, n_cases):
+def _fuzz(A, O, seed, int_mode, transcendental_last, n_cases, pool=None):
     g = SI.gen(seed)
     ran = 0
     for case in range(n_cases):
         R = int(torch.randint(1, 40, (1,), generator=g))
         C = int(torch.randint(1, 300, (1,), generator=g))
         n_in = int(torch.randint(1, 4, (1,), generator=g))
-        pool = INT_DT if int_mode else FLOAT_DT
-        in_dts = [pool[int(torch.randint(0, 3, (1,), generator=g))] for _ in range(n_in)]
+        dpool = pool or (INT_DT if int_mode else FLOAT_DT)
+        in_dts = [dpool[int(torch.randint(0, len(dpool), (1,), generator=g))] for _ in range(n_in)]
         inputs = _make_inputs(g, (R, C), in_dts)
         P = _random_program(g, n_in, in_dts, int_mode, int(torch.randint(2, 10, (1,), generator=g)),
-                            transcendental_last)
+                            transcendental_last, pool)
         prog = _to_psg(A, P)
         dins = [dev(x[0]) for x in inputs]
         views = [A.view_of(d, shape=x[1], strides=x[2], offset=x[3], mask=x[4])
@@ -217,7 +217,15 @@ def _fuzz(A, O, seed, int_mode, transcendental_last, n_cases):
         ref = _oracle_eval(O, P, inputs, (R, C))
         got = to_np(out.cpu())
         if transcendental_last:
-            if out_dt == "f32":
+            if out_dt == "f64":
+                # float64 EXP / LOG: CUDA's and the C library's are both within
+                # an ulp or so of the exact value; 4 float64 ulps bound them
+                g64, r64 = got.astype(np.float64), ref.data.astype(np.float64)
+                fin = np.isfinite(r64)
+                assert np.all(np.abs(g64[fin] - r64[fin]) <= 4 * np.spacing(np.abs(r64[fin]))), (case, P)
+                assert np.array_equal(np.isnan(g64), np.isnan(r64)) and np.array_equal(g64[~fin & ~np.isnan(r64)],
+                                                                                        r64[~fin & ~np.isnan(r64)])
+            elif out_dt == "f32":
                 assert ulp_dist_f32(got, ref.data).max() <= 8, (case, P)
             else:  # a narrow float result: within one unit of its own rounding
                 g64 = O.T(got, out_dt).f64()
@@ -243,6 +251,15 @@ def test_random_int_programs_bit_exact(A, O):
 
 def test_random_programs_ending_in_exp_or_log(A, O):
     _fuzz(A, O, seed=13, int_mode=False, transcendental_last=True, n_cases=80)
+
+
+def test_random_float64_programs(A, O):
+    """float64 nodes (limn, "The op set": float64 computes natively at its own
+    width) mixed with float32 inputs and CASTs both ways: programs of
+    correctly rounded nodes give the oracle's bits; a final EXP or LOG in
+    float64 is within 4 float64 ulps of the C library's."""
+    _fuzz(A, O, seed=14, int_mode=False, transcendental_last=False, n_cases=80, pool=("f64", "f32"))
+    _fuzz(A, O, seed=15, int_mode=False, transcendental_last=True, n_cases=60, pool=("f64", "f32"))
 
 
 def test_rank3_broadcast_and_empty(A, O):

@@ -284,7 +284,11 @@ def test_gpt_block_full_size(O):
 def test_gpt_step_contractions_write_half_width(G):
     """Every contraction of the GPT block step is read only through a CAST to
     bfloat16, so each one is stored in bfloat16 by its own epilogue (no
-    float32 contraction output, and no contraction computed twice)."""
+    float32 contraction output, and no contraction computed twice), unless
+    an elementwise consumer runs in its epilogue: the two residual adds of
+    the forward and the ReLU mask of the MLP's backward are computed by the
+    contraction that produces their operand (psg_contract's epilogue
+    program), whose value then never goes through memory."""
     from primitive_sm_graph_gb300.workloads import gpt_step
     tok, w = SI.gpt_block(6, 2, 64, 128, 128, 2, 256)
     dev = {k: v.cuda() for k, v in w.items()}
@@ -293,7 +297,9 @@ def test_gpt_step_contractions_write_half_width(G):
     torch.cuda.synchronize()
     cons = [e for e in log if e[0] == "contract"]
     assert len(cons) == 15, cons        # 5 forward, 5 input gradients, 5 weight gradients
-    assert all(e[3] == "bf16" for e in cons), cons
+    fused = [e for e in cons if len(e) > 4]
+    assert len(fused) == 3, cons
+    assert all(e[3] == "bf16" for e in cons if len(e) == 4), cons
 
 
 _PDL_SCRIPT = r"""

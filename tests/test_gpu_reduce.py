@@ -310,3 +310,27 @@ def test_column_sum_over_batch_of_3d(A, O):
     ref = O.reduce_sum(ox, keepdim=False).data.astype(np.float64)
     mag = np.abs(ox.f64()).sum(axis=-1)
     assert np.all(np.abs(out.cpu().numpy().astype(np.float64) - ref) <= 2 * gamma(B - 1) * mag + 1e-30)
+
+
+def test_staged_wait_gives_up_with_timeout_status_then_recovers(A, O, PR, monkeypatch):
+    """The staged ring's bounded wait, made to run out.  The library's test
+    hook PSG_TEST_RING_TIMEOUT=1 leaves every team's first ring slot unfilled
+    (a phase nothing completes) and bounds each wait by about a millisecond:
+    the waits give up, PSG_E_TIMEOUT reaches the status word, and the kernel
+    still ends, after the copies it did issue have landed, with the context
+    usable.  The same call without the hook is then correct again."""
+    x = SI.softmax_input(7, 600, 1024)  # 4 KB rows: the staged ring
+    dx = dev(x)
+    y = torch.empty_like(dx)
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    stages, epi = PR.softmax_rows()
+    monkeypatch.setenv("PSG_TEST_RING_TIMEOUT", "1")
+    A.psg_reduce_rows(stages, epi, [dx], [A.view_of(dx)], y, A.view_of(y), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == A.E_TIMEOUT
+    monkeypatch.delenv("PSG_TEST_RING_TIMEOUT")
+    st.zero_()
+    A.psg_reduce_rows(stages, epi, [dx], [A.view_of(dx)], y, A.view_of(y), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _softmax_check(O, x.numpy(), y.cpu().numpy())

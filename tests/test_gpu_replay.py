@@ -87,3 +87,47 @@ def test_gpt_train_step_replay_updates_like_eager(G):
     torch.cuda.synchronize()
     for k in GPT_WEIGHTS:
         assert _same(w_rep[k], w_eager[k]), k
+
+
+def test_plan_cache_replays_the_same_calls_bit_for_bit(G):
+    """The plan cache (limn, "Reading the schedule": execution plans cached
+    by graph structure): a graph whose structure was realized before replays
+    the recorded calls with its own buffers, skipping the scheduler.  The
+    GPT block step and the tiny graph give the same bits through a recorded
+    plan, through the plan on new inputs, and with the cache off (scheduled
+    afresh); the hit makes the same calls (the executor's log)."""
+    from primitive_sm_graph_gb300.workloads import GPT_WEIGHTS, gpt_step, tiny_graph
+    shapes = dict(B=2, T=64, V=128, D=128, H=2, F=256)
+    tok, w = SI.gpt_block(8, **shapes)
+    dtok, dw = tok.cuda(), {k: v.cuda() for k, v in w.items()}
+    ex = G._executor()
+    old = G.PLAN_CACHE
+    try:
+        G.PLAN_CACHE = True
+        ex.log.clear()
+        first = gpt_step(dtok, dw, 2)
+        log_first = list(ex.log)
+        n_plans = len(G._PLANS)
+        ex.log.clear()
+        hit = gpt_step(dtok, dw, 2)
+        assert len(G._PLANS) == n_plans and ex.log == log_first
+        G.PLAN_CACHE = False
+        fresh = gpt_step(dtok, dw, 2)
+        for a, b, c in [(first[0], hit[0], fresh[0])] + [(first[1][k], hit[1][k], fresh[1][k]) for k in GPT_WEIGHTS]:
+            assert _same(a, b) and _same(a, c)
+        # other inputs through the recorded plan
+        G.PLAN_CACHE = True
+        tok2, w2 = SI.gpt_block(9, **shapes)
+        d2 = {k: v.cuda() for k, v in w2.items()}
+        via_plan = gpt_step(tok2.cuda(), d2, 2)
+        G.PLAN_CACHE = False
+        fresh2 = gpt_step(tok2.cuda(), d2, 2)
+        assert _same(via_plan[0], fresh2[0]) and not _same(via_plan[0], first[0])
+        assert all(_same(via_plan[1][k], fresh2[1][k]) for k in GPT_WEIGHTS)
+        G.PLAN_CACHE = True
+        a, b = (t.cuda() for t in SI.tiny_graph(0))
+        r1 = tiny_graph(G.Tensor.from_torch(a), G.Tensor.from_torch(b)).realize().clone()
+        r2 = tiny_graph(G.Tensor.from_torch(a), G.Tensor.from_torch(b)).realize()
+        assert _same(r1, r2)
+    finally:
+        G.PLAN_CACHE = old

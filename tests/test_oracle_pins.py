@@ -633,3 +633,42 @@ def test_cast_f16_round_to_nearest_even(O):
     assert np.isnan(nan[0])
     back = O.cast(O.T(got, "f16"), "f32").data
     np.testing.assert_array_equal(back, got.astype(np.float32))
+
+
+def test_float64_nodes_against_exact_values(O):
+    """float64 nodes compute in double: ADD, MUL exact on small integers,
+    SQRT and RECIP correctly rounded (exact rationals), EXP and LOG within
+    one float64 ulp of 40-digit values (sympy, an independent
+    arbitrary-precision evaluation), NEG flips the sign, CMPLT/WHERE as for
+    float32, CAST to float32 rounds to nearest."""
+    sympy = pytest.importorskip("sympy")
+    g = np.random.default_rng(31)
+    a = g.integers(-10**6, 10**6, 200).astype(np.float64)
+    b = g.integers(-10**6, 10**6, 200).astype(np.float64)
+    A, B = O.T(a, "f64"), O.T(b, "f64")
+    np.testing.assert_array_equal(O.add(A, B).data, a + b)
+    np.testing.assert_array_equal(O.mul(A, B).data, a * b)
+    np.testing.assert_array_equal(O.neg(A).data, -a)
+    x = np.abs(g.standard_normal(50)) * 10 + 1e-3
+    X = O.T(x, "f64")
+    for xi, si, ri in zip(x, O.sqrt(X).data, O.recip(X).data):
+        fx = Fraction(float(xi))
+        # the correctly rounded square root: the nearest double, checked by
+        # the exact squares of its neighbours
+        below, above = np.nextafter(si, -np.inf), np.nextafter(si, np.inf)
+        assert abs(Fraction(float(si)) ** 2 - fx) <= min(abs(Fraction(float(below)) ** 2 - fx),
+                                                         abs(Fraction(float(above)) ** 2 - fx))
+        err = abs(Fraction(1) / fx - Fraction(float(ri)))
+        assert err <= abs(Fraction(1) / fx - Fraction(float(np.nextafter(ri, np.inf))))
+        assert err <= abs(Fraction(1) / fx - Fraction(float(np.nextafter(ri, -np.inf))))
+    y = g.uniform(-20, 20, 40)
+    for yi, ei in zip(y, O.exp(O.T(y, "f64")).data):
+        exact = float(sympy.exp(sympy.Float(float(yi), 60)).evalf(40))
+        assert abs(ei - exact) <= np.spacing(exact)
+    for xi, li in zip(x, O.log(X).data):
+        exact = float(sympy.log(sympy.Float(float(xi), 60)).evalf(40))
+        assert abs(li - exact) <= np.spacing(abs(exact))
+    c = O.cmplt(O.T(np.array([1.0, np.nan, 2.0]), "f64"), O.T(np.array([2.0, 1.0, np.nan]), "f64")).data
+    assert list(c) == [1.0, 0.0, 0.0]
+    v = np.array([1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, 1e300], np.float64)
+    np.testing.assert_array_equal(O.cast(O.T(v, "f64"), "f32").data, v.astype(np.float32))

@@ -109,3 +109,23 @@ def test_contract_equals_naive_loop_per_batch(O, P):
         assert got.data[z].tobytes() == ref.data.tobytes()
     with pytest.raises(ValueError):
         P.contract(O.T(A, "f32"), O.T(B, "f32"), "f32")
+
+
+def test_contract_epilogue_equals_matmul_then_elementwise(O, P):
+    """ACC + residual, cast and relu through the evaluator give the bits of
+    the separate nodes: the float32 matmul, its CAST, the ADD, the WHERE."""
+    g = np.random.default_rng(6)
+    A = O.tensor(g.standard_normal((2, 7, 33)), "bf16")
+    B = O.tensor(g.standard_normal((2, 33, 5)), "bf16")
+    R = O.tensor(g.standard_normal((2, 7, 5)), "bf16")
+    bt = O.T(np.ascontiguousarray(B.data.transpose(0, 2, 1)), "bf16")
+    prog = [N("ACC"), N("CAST", 0, dt="bf16"), N("LOAD", 0, dt="bf16"), N("ADD", 1, 2, dt="bf16"),
+            N("CONST", dt="bf16"), N("CMPLT", 4, 3, dt="bf16"), N("WHERE", 5, 3, 4, dt="bf16")]
+    got = P.contract_epilogue(A, bt, prog, [R])
+    for z in range(2):
+        c = O.matmul(O.T(A.data[z], "bf16"), O.T(B.data[z], "bf16"), "f32")
+        h = O.add(O.cast(c, "bf16"), O.T(R.data[z], "bf16"))
+        ref = O.relu(h)
+        assert got.data[z].tobytes() == ref.data.tobytes()
+    with pytest.raises(TypeError):
+        P.program([N("ACC")], [], (2, 2))
