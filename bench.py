@@ -296,7 +296,34 @@ def e2e_steps(step, K, W):
 
 FP32_LANES_PER_SM = 128   # FFMA lanes per SM (Blackwell SM: 4 partitions x 32)
 IMAD_PER_FFMA = 0.5       # integer multiply-adds issue at half the FFMA rate
-TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 tensor rates
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 tensor rates (the fallback when cuBLAS TF32 cannot be timed)
+
+
+def cublas_tf32_tflops(n=8192, reps=5):
+    """Dense TF32 tensor rate of cuBLAS on this GPU: a float32 n^3 matmul with
+    TF32 allowed, best of `reps` after warm-up (the ceiling the 3xTF32
+    contraction issues its products against)."""
+    old = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        g = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn((n, n), device="cuda", generator=g)
+        b = torch.randn((n, n), device="cuda", generator=g)
+        for _ in range(3):
+            a @ b
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            a @ b
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
 
 
 def fp32_alu_peak():
@@ -406,7 +433,12 @@ class Rows:
     def gemm_f32(self):
         a, b = SI.contraction_f32(0)
         fn, flops = self._contract(a.cuda(), b.cuda(), torch.float32)
-        tf32 = self.P["bf16"] * TF32_PER_BF16
+        try:
+            tf32 = cublas_tf32_tflops()
+            src = "measured here: cuBLAS float32 8192^3 with TF32 allowed (best of 5)"
+        except Exception:
+            tf32 = self.P["bf16"] * TF32_PER_BF16
+            src = "measured cuBLAS bf16 burst x nominal TF32/bf16 ratio (1.1/2.25)"
         ffma = fp32_alu_peak()
 
         def fin(ms):
@@ -414,8 +446,8 @@ class Rows:
             pipe = 3 * tf                            # TF32 tensor flops issued (three products per term)
             return {"ms": round(ms, 5), "flops": flops, "achieved": round(tf, 2), "unit": "TFLOP/s",
                     "bound": "tensor", "peak": round(tf32 / 3, 2),
-                    "peak_source": "measured cuBLAS bf16 burst x nominal TF32/bf16 ratio (1.1/2.25), "
-                                   "divided by the 3 TF32 products per float32 term",
+                    "peak_source": src + ", divided by the 3 TF32 products per float32 term",
+                    "tf32_ceiling_tflops": round(tf32, 2),
                     "frac": round(pipe / tf32, 4),
                     "tf32_pipe_tflops": round(pipe, 2),
                     "ffma_ceiling": round(ffma, 2), "vs_ffma_ceiling": round(tf / ffma, 3),
@@ -499,7 +531,11 @@ class Rows:
             A.psg_attention_fwd(qkv, vs[0], qkv, vs[1], qkv, vs[2], o, vo, lse, 0.125, True, stream=s)
             A.psg_attention_bwd(qkv, vs[0], qkv, vs[1], qkv, vs[2], o, vo, do, vdo, lse, delta, dqkv, dvs[0],
                                 dqkv, dvs[1], dqkv, dvs[2], 0.125, True, stream=s)
-        per = 2.0 * B_ * H * T * T * 64       # one T x T x 64 contraction (full square)
+        return fn, self._attn_fin(B_, T, H, "fused attention fwd+bwd B32 T256 H8 hd64 causal bf16 (4 launches)")
+
+    def _attn_fin(self, B_, T, H, workload):
+        # the products' visible cells only: a causal row i has i + 1 keys
+        per = 2.0 * B_ * H * 64 * (T * (T + 1) / 2)
         flops = 7 * per                       # forward: S, O; backward: S, dP, dV, dK, dQ
         pk = self.P["bf16"]
 
@@ -507,9 +543,33 @@ class Rows:
             tf = flops / (ms * 1e-3) / 1e12
             return {"ms": round(ms, 5), "flops": flops, "achieved": round(tf, 2), "unit": "TFLOP/s",
                     "bound": "tensor", "peak": pk, "frac": round(tf / pk, 4),
-                    "note": "FLOPs of the full T x T products (the kernels skip the key tiles a causal query tile cannot see)",
-                    "workload": "fused attention fwd+bwd B32 T256 H8 hd64 causal bf16 (4 launches)"}
-        return fn, fin
+                    "note": "FLOPs of the causal products' visible cells (T(T+1)/2 per head), 7 products",
+                    "workload": workload}
+        return fin
+
+    # fused attention past one key block: the running softmax over 128-key blocks
+    def attention_long(self):
+        A = self.A
+        B_, T, H = 2, 4096, 8
+        g = SI.gen(6)
+        qkv = SI.normal((B_, T, 3, H, 64), 0, 1, g, torch.bfloat16).cuda()
+        do = SI.normal((B_, T, H, 64), 0, 1, g, torch.bfloat16).cuda()
+        vs = [A.view_of(qkv, shape=(B_, T, H, 64), strides=qkv[:, :, 0].stride(), offset=i * H * 64)
+              for i in range(3)]
+        o = torch.empty((B_, T, H, 64), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B_, H, T), dtype=torch.float32, device="cuda")
+        delta = torch.empty_like(lse)
+        dqkv = torch.empty_like(qkv)
+        dvs = [A.view_of(dqkv, shape=(B_, T, H, 64), strides=dqkv[:, :, 0].stride(), offset=i * H * 64)
+               for i in range(3)]
+        vo, vdo = A.view_of(o), A.view_of(do)
+
+        def fn(s):
+            A.psg_attention_fwd(qkv, vs[0], qkv, vs[1], qkv, vs[2], o, vo, lse, 0.125, True, stream=s)
+            A.psg_attention_bwd(qkv, vs[0], qkv, vs[1], qkv, vs[2], o, vo, do, vdo, lse, delta, dqkv, dvs[0],
+                                dqkv, dvs[1], dqkv, dvs[2], 0.125, True, stream=s)
+        return fn, self._attn_fin(B_, T, H, "fused attention fwd+bwd B2 T4096 H8 hd64 causal bf16, "
+                                            "32 key blocks (4 launches)")
 
     def stream_ms(self, nm, pairs=8, rounds=4):
         """Device ms per launch of row nm in steady state: a CUDA Graph of
@@ -814,7 +874,8 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-KERNEL_ROWS = ["softmax", "rmsnorm", "gemm_bf16", "gemm_f32", "gemm_i8", "gather", "scatter", "attention"]
+KERNEL_ROWS = ["softmax", "rmsnorm", "gemm_bf16", "gemm_f32", "gemm_i8", "gather", "scatter", "attention",
+               "attention_long"]
 ROW_NAMES = KERNEL_ROWS + ["tiny_graph", "gpt"]
 
 
@@ -849,7 +910,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", default="all",
                     help="comma list of extra rows to time (softmax,rmsnorm,gemm_bf16,gemm_f32,gemm_i8,"
-                         "gather,scatter,tiny_graph,gpt), 'all' or 'none'")
+                         "gather,scatter,attention,attention_long,tiny_graph,gpt), 'all' or 'none'")
     ap.add_argument("--profile-case", default=None,
                     help="run one workload --iters times and exit (for a profiler capture); "
                          "chain, transpose, gpt (one eager forward + backward) or a row name")

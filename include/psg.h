@@ -120,7 +120,9 @@ typedef struct {
  *       earlier stage, in that stage's dtype;
  *   ACC: (psg_contract's epilogue only) the cell's float32 total, the SUM
  *       over k before any rounding into C; node dtype PSG_F32.
- * float64 nodes are not implemented yet (PSG_E_UNSUPPORTED_DTYPE). */
+ * float64 nodes (PSG_F64, every op above) run in psg_elementwise, each
+ * rounded to double; psg_reduce_rows and psg_contract's epilogue refuse them
+ * (PSG_E_UNSUPPORTED_DTYPE). */
 typedef enum {
     PSG_OP_LOAD = 0, PSG_OP_CONST = 1, PSG_OP_RED = 2,
     PSG_OP_NEG = 3, PSG_OP_EXP = 4, PSG_OP_LOG = 5, PSG_OP_SQRT = 6, PSG_OP_RECIP = 7,
@@ -312,7 +314,9 @@ psg_status psg_gather(const void* src, const psg_view* sv, const int32_t* idx, i
  * cell's value, and round into the dtype once; ints wrap.  Colliding rows are
  * added in ascending n, so two runs give the same bits (no float atomics).
  * dv: view of dst [V, ...] (contiguous rows); uv: view of upd [n, ...]; both
- * one dtype (f32, bf16, f16, i32).  An index outside [0, V) skips its row and
+ * one dtype, any of the seven (f64 keeps a float64 total; i32, i16 and i8
+ * add in 32-bit wrapping arithmetic and keep the low bits, which is the
+ * wrap of the width).  An index outside [0, V) skips its row and
  * writes PSG_E_INDEX_OUT_OF_RANGE to d_status (device int32, required).
  * workspace: device memory of at least psg_scatter_workspace(n) bytes,
  *   256-byte aligned, owned by the caller, free for reuse once the stream has
@@ -354,31 +358,39 @@ psg_status psg_scatter_add_static(void* dst, const psg_view* dv, const int32_t* 
  * psg_attention_fwd / psg_attention_bwd -- fused scaled dot-product attention
  * (limn, "The op set": the fused attention op that saves L = logsumexp for
  * its backward and a two-pass deterministic backward, in place of the
- * composed T x T score tensors; Tiki, "Write the attention kernel at the
- * algorithm level": the FlashAttention backward dS = P * (dO V^T - D)).
+ * composed T x T score tensors; masking is a flag per key that composes with
+ * causal; Tiki, "Write the attention kernel at the algorithm level": the
+ * running max, denominator and weighted sum, and the FlashAttention backward
+ * dS = P * (dO V^T - D)).
  *
- * Per batch b and head h, with S = scale * Q K^T and keys j > i hidden from
- * query i when causal:
- *     L[b,h,i] = log sum_j exp(S[i,j]),  O = exp(S - L) V;
- *     D[i] = sum_d dO[i,d] O[i,d],  P = exp(S - L),  dS = P * (dO V^T - D),
- *     dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
+ * Per batch b and head h, with S = scale * Q K^T and key j visible to query
+ * i unless j > i (causal) or key_mask[b, j] == 0:
+ *     L[b,h,i] = log sum_{visible j} exp(S[i,j]),  O = exp(S - L) V over the
+ *     visible keys (a query with no visible key: O = 0, L = -inf);
+ *     D[i] = sum_d dO[i,d] O[i,d],  P = exp(S - L) (0 where hidden),
+ *     dS = P * (dO V^T - D),  dV = P^T dO,  dQ = scale * dS K,
+ *     dK = scale * dS^T Q.
  * Views: Q, K, V, O, dO, dQ, dK, dV are bf16 [B, T, H, 64] (head dim
  * contiguous; batch, token and head strides multiples of 8 elements; base
- * 16-byte aligned; no mask).  T <= 256 (one key block per head), B <= 32767,
- * H <= 65535; other shapes return PSG_E_UNSUPPORTED_LAYOUT.  S and dP are float32 sums of exact
- * bf16 products; P and dS are rounded to bf16 before the second products.
- * lse: device float32 [B, H, T], written by fwd and read by bwd.  delta:
- * device float32 [B, H, T] scratch of bwd (caller-owned).  scale > 0.
- * A bounded wait that gives up writes PSG_E_TIMEOUT into d_status.
+ * 16-byte aligned; no mask).  B <= 32767, H <= 65535, T <= 2^24; other
+ * shapes return PSG_E_UNSUPPORTED_LAYOUT.  T <= 256 keys take one key block
+ * per head; longer sequences walk 128-key blocks with a running max and sum.
+ * key_mask: device bytes [B, T] (row-major; nonzero = visible) or NULL (every
+ * key visible).  S and dP are float32 sums of exact bf16 products; P and dS
+ * are rounded to bf16 before the second products.  lse: device float32
+ * [B, H, T], written by fwd and read by bwd.  delta: device float32 [B, H, T]
+ * scratch of bwd (caller-owned).  scale > 0.  A bounded wait that gives up
+ * writes PSG_E_TIMEOUT into d_status.
  * ------------------------------------------------------------------------- */
 psg_status psg_attention_fwd(const void* q, const psg_view* qv, const void* k, const psg_view* kv,
                              const void* v, const psg_view* vv, void* o, const psg_view* ov, float* lse,
-                             float scale, int causal, int32_t* d_status, void* stream);
+                             float scale, int causal, const uint8_t* key_mask, int32_t* d_status, void* stream);
 psg_status psg_attention_bwd(const void* q, const psg_view* qv, const void* k, const psg_view* kv,
                              const void* v, const psg_view* vv, const void* o, const psg_view* ov,
                              const void* dout, const psg_view* dov, const float* lse, float* delta,
                              void* dq, const psg_view* dqv, void* dk, const psg_view* dkv, void* dv,
-                             const psg_view* dvv, float scale, int causal, int32_t* d_status, void* stream);
+                             const psg_view* dvv, float scale, int causal, const uint8_t* key_mask,
+                             int32_t* d_status, void* stream);
 
 /* ---------------------------------------------------------------------------
  * psg_adamw_step -- one AdamW step (decoupled weight decay) over a list of

@@ -100,10 +100,10 @@ def _load():
     L.psg_scatter_add_static.restype = i32
     L.psg_query_launch.argtypes = [i32, V, P32, P32, P32, P32]
     fl = ctypes.c_float
-    L.psg_attention_fwd.argtypes = [vp, V, vp, V, vp, V, vp, V, vp, fl, i32, vp, vp]
+    L.psg_attention_fwd.argtypes = [vp, V, vp, V, vp, V, vp, V, vp, fl, i32, vp, vp, vp]
     L.psg_adamw_step.argtypes = [ctypes.POINTER(psg_adamw_tensor), i32, i32, fl, fl, fl, fl, fl, vp, vp, vp]
     L.psg_attention_bwd.argtypes = [vp, V, vp, V, vp, V, vp, V, vp, V, vp, vp, vp, V, vp, V, vp, V, fl, i32, vp,
-                                    vp]
+                                    vp, vp]
     L.psg_status_string.argtypes = [i32]
     L.psg_status_string.restype = ctypes.c_char_p
     L.psg_version.restype = ctypes.c_char_p
@@ -295,26 +295,28 @@ def psg_contract_ws(A, Av, B, Bv, C, Cv, workspace, ws_bytes, d_status=None, str
 
 
 def psg_attention_fwd(q, qv, k, kv, v, vv, o, ov, lse, scale, causal=True, d_status=None, stream=None,
-                      check=True) -> int:
+                      check=True, key_mask=None) -> int:
     """Fused attention forward over [B, T, H, 64] bf16 views; lse: float32
-    [B, H, T] device buffer (written)."""
+    [B, H, T] device buffer (written); key_mask: None or a device byte
+    tensor [B, T] (nonzero: the key is visible)."""
     st = lib.psg_attention_fwd(_ptr(q), ctypes.byref(qv), _ptr(k), ctypes.byref(kv), _ptr(v), ctypes.byref(vv),
                                _ptr(o), ctypes.byref(ov), _ptr(lse), float(scale), 1 if causal else 0,
-                               _ptr(d_status), _stream(stream))
+                               _ptr(key_mask), _ptr(d_status), _stream(stream))
     if check:
         _check(st, "psg_attention_fwd")
     return st
 
 
 def psg_attention_bwd(q, qv, k, kv, v, vv, o, ov, do, dov, lse, delta, dq, dqv, dk, dkv, dv, dvv, scale,
-                      causal=True, d_status=None, stream=None, check=True) -> int:
+                      causal=True, d_status=None, stream=None, check=True, key_mask=None) -> int:
     """Fused attention backward: dQ, dK, dV (bf16 [B, T, H, 64] views) from
-    dO and the forward's O and lse; delta: float32 [B, H, T] scratch."""
+    dO and the forward's O and lse; delta: float32 [B, H, T] scratch;
+    key_mask as for the forward."""
     st = lib.psg_attention_bwd(_ptr(q), ctypes.byref(qv), _ptr(k), ctypes.byref(kv), _ptr(v), ctypes.byref(vv),
                                _ptr(o), ctypes.byref(ov), _ptr(do), ctypes.byref(dov), _ptr(lse), _ptr(delta),
                                _ptr(dq), ctypes.byref(dqv), _ptr(dk), ctypes.byref(dkv), _ptr(dv),
-                               ctypes.byref(dvv), float(scale), 1 if causal else 0, _ptr(d_status),
-                               _stream(stream))
+                               ctypes.byref(dvv), float(scale), 1 if causal else 0, _ptr(key_mask),
+                               _ptr(d_status), _stream(stream))
     if check:
         _check(st, "psg_attention_bwd")
     return st

@@ -40,7 +40,7 @@ psg_status attn_common(const psg_view* qv, float scale, int causal, AttnParams* 
     p->H = (int)qv->shape[2];
     // grid limits: heads on y (65535), 2 B on z (the two backward passes)
     if (qv->shape[0] > 32767 || qv->shape[2] > 65535) return PSG_E_UNSUPPORTED_LAYOUT;
-    if (p->T > 256) return PSG_E_UNSUPPORTED_LAYOUT;  // one key block per head
+    if (qv->shape[1] > (1 << 24)) return PSG_E_UNSUPPORTED_LAYOUT;
     if (!(scale > 0.0f) || !(scale < 1e30f)) return PSG_E_INVALID_ARG;
     p->scale = scale;
     p->causal = causal ? 1 : 0;
@@ -54,11 +54,14 @@ using namespace psg;
 
 extern "C" psg_status psg_attention_fwd(const void* q, const psg_view* qv, const void* k, const psg_view* kv,
                                         const void* v, const psg_view* vv, void* o, const psg_view* ov, float* lse,
-                                        float scale, int causal, int32_t* d_status, void* stream)
+                                        float scale, int causal, const uint8_t* key_mask, int32_t* d_status,
+                                        void* stream)
 {
     AttnParams p;
     psg_status st = attn_common(qv, scale, causal, &p);
     if (st != PSG_OK) return st;
+    p.kmask = key_mask;
+    p.km_sb = p.T;
     AttnTensor tq, tk, tv, to;
     if ((st = attn_view(q, qv, false, p.B, p.T, p.H, &tq)) != PSG_OK) return st;
     if ((st = attn_view(k, kv, false, p.B, p.T, p.H, &tk)) != PSG_OK) return st;
@@ -80,12 +83,14 @@ extern "C" psg_status psg_attention_bwd(const void* q, const psg_view* qv, const
                                         const void* v, const psg_view* vv, const void* o, const psg_view* ov,
                                         const void* dout, const psg_view* dov, const float* lse, float* delta,
                                         void* dq, const psg_view* dqv, void* dk, const psg_view* dkv, void* dv,
-                                        const psg_view* dvv, float scale, int causal, int32_t* d_status,
-                                        void* stream)
+                                        const psg_view* dvv, float scale, int causal, const uint8_t* key_mask,
+                                        int32_t* d_status, void* stream)
 {
     AttnParams p;
     psg_status st = attn_common(qv, scale, causal, &p);
     if (st != PSG_OK) return st;
+    p.kmask = key_mask;
+    p.km_sb = p.T;
     AttnTensor tq, tk, tv, to, tdo, tdq, tdk, tdv;
     if ((st = attn_view(q, qv, false, p.B, p.T, p.H, &tq)) != PSG_OK) return st;
     if ((st = attn_view(k, kv, false, p.B, p.T, p.H, &tk)) != PSG_OK) return st;

@@ -86,8 +86,7 @@ psg_status plan_scatter(void* dst, const psg_view* dv, const int32_t* idx, int64
     if (dv->ndim < 1 || !rest_shape_equal(dv, uv) || uv->shape[0] != n) return PSG_E_INVALID_ARG;
     if (dv->dtype != uv->dtype) return PSG_E_UNSUPPORTED_DTYPE;
     const int dt = dv->dtype;
-    if (dt != PSG_F32 && dt != PSG_BF16 && dt != PSG_F16 && dt != PSG_F64 && dt != PSG_I32)
-        return PSG_E_UNSUPPORTED_DTYPE;
+    if (!dtype_valid(dt)) return PSG_E_UNSUPPORTED_DTYPE;
     if (view_has_mask(uv)) return PSG_E_UNSUPPORTED_LAYOUT;
     std::memset(L, 0, sizeof(*L));
     int64_t D2;

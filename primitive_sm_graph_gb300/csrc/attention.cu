@@ -80,6 +80,13 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t dtmem, uint32_t atmem, uint6
 // the 8 softmax warps only
 __device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// key j of batch b is not hidden by the per-key mask (limn, "The op set":
+// masking is a flag per key that composes with causal)
+__device__ __forceinline__ bool key_on(const AttnParams& p, int b, int j)
+{
+    return !p.kmask || p.kmask[(int64_t)b * p.km_sb + j] != 0;
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum)
 {
     asm volatile(
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
                 tmem_ld32(trow + (uint32_t)c, s);
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (c + j < kmax) m = fmaxf(m, p.scale * __uint_as_float(s[j]));
+                    if (c + j < kmax && key_on(p, b, c + j)) m = fmaxf(m, p.scale * __uint_as_float(s[j]));
             }
         }
         red_m[half * QT + r] = m;
@@ -228,8 +235,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
                 for (int j = 0; j < 32; j += 2) {
                     // l sums the float32 weights (L = m + log l is the row's
                     // logsumexp); P is rounded to bf16 only as the MMA operand
-                    const float e0 = c + j < kmax ? __expf(p.scale * __uint_as_float(s[j]) - m) : 0.0f;
-                    const float e1 = c + j + 1 < kmax ? __expf(p.scale * __uint_as_float(s[j + 1]) - m) : 0.0f;
+                    const bool v0 = c + j < kmax && key_on(p, b, c + j), v1 = c + j + 1 < kmax && key_on(p, b, c + j + 1);
+                    const float e0 = v0 ? __expf(p.scale * __uint_as_float(s[j]) - m) : 0.0f;
+                    const float e1 = v1 ? __expf(p.scale * __uint_as_float(s[j + 1]) - m) : 0.0f;
                     l += e0;
                     l += e1;
                     w[j >> 1] = pack_bf16(e0, e1);
@@ -252,8 +260,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
             __syncwarp();  // every lane reaches the collective load
             tmem_ld32(trow + FWD_O + 32u * half, o);
             if (i < p.T) {
-                const float inv = 1.0f / l;
-                if (half == 0) p.lse[((int64_t)b * p.H + h) * p.T + i] = m + logf(l);
+                // a query that sees no key at all (every key masked): O = 0, L = -inf
+                const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+                if (half == 0) p.lse[((int64_t)b * p.H + h) * p.T + i] = l > 0.0f ? m + logf(l) : -INFINITY;
                 __nv_bfloat16* dst = (__nv_bfloat16*)p.o + p.o_off + (int64_t)b * p.o_sb + (int64_t)i * p.o_st +
                                      (int64_t)h * p.o_sh + 32 * half;
                 uint32_t w[16];
@@ -272,10 +281,244 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(FWD_TMEM));
 }
 
+// ---- forward over many key blocks: an online softmax ----------------------
+// For T > 256 a query tile walks its key blocks of 128 (Tiki, "Write the
+// attention kernel at the algorithm level": the running max m, denominator
+// l and weighted sum a, rescaled as the max grows).  Per block j:
+//   S_j = Q K_j^T                          (tcgen05.mma -> TMEM columns 0..127)
+//   m' = max(m, max_k scale S_j), alpha = exp(m - m')
+//   P_j = exp(scale S_j - m')             (bf16, back into TMEM over the S
+//                                          columns its thread has read)
+//   l = alpha l + rowsum(P_j), O_j = P_j V_j (a fresh TMEM accumulator,
+//                                          columns 128..191)
+//   a = alpha a + O_j                      (float32, in the row threads'
+//                                          registers: 32 head-dim columns each)
+// and at the end O = a / l, L = m + log l (a query with no visible key: O = 0,
+// L = -inf).  K and V blocks come through a two-slot ring.  Roles as in the
+// one-block kernel: warp 0 TMA, warp 1 MMA, warps 2-9 two threads a query row
+// (one per 64-key half of a block, and per 32-column half of the head dim).
+constexpr int LKV_SLOT = 2 * Q_BYTES;  // a K block and a V block: 32 KB
+constexpr int LFWD_SMEM = 1024 + Q_BYTES + 2 * LKV_SLOT + 256 + 2 * 2 * QT * 4 + 2 * QT * 4;
+constexpr uint32_t LFWD_O = 128;       // TMEM: S and P in 0..127, O_j in 128..191
+
+struct LFwdBars {
+    uint64_t q_full, kv_full[2], kv_empty[2], s_full, p_ready, o_full, o_free, drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+__global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_constant__ CUtensorMap tq,
+                                                                const __grid_constant__ CUtensorMap tk,
+                                                                const __grid_constant__ CUtensorMap tv,
+                                                                const __grid_constant__ AttnParams p)
+{
+    pdl_enter();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sq = smem;                        // [128 q][64 d]
+    uint8_t* skv = sq + Q_BYTES;               // [2 slots][K block, V block]
+    LFwdBars* bars = (LFwdBars*)(skv + 2 * LKV_SLOT);
+    float* red_m = (float*)((uint8_t*)bars + 256);  // [2 blocks (parity)][2 halves][128 rows]
+    float* red_l = red_m + 2 * 2 * QT;               // [2 halves][128 rows]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * QT;
+    const int nall = (p.T + QT - 1) / QT;
+    const int nblk = p.causal ? min(qt + 1, nall) : nall;  // key blocks any query of the tile sees
+
+    if (threadIdx.x == 0) {
+        bar_init(&bars->q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            bar_init(&bars->kv_full[s], 1);
+            bar_init(&bars->kv_empty[s], 1);
+        }
+        bar_init(&bars->s_full, 1);
+        bar_init(&bars->p_ready, 8);
+        bar_init(&bars->o_full, 1);
+        bar_init(&bars->o_free, 8);
+        bar_init(&bars->drain, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&bars->tmem_base)), "r"(FWD_TMEM));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bar_expect_tx(&bars->q_full, Q_BYTES);
+            tma_load_4d(sq, &tq, &bars->q_full, 0, q0, h, b);
+            uint32_t armed = 0, armed_ph = 0;
+            for (int j = 0; j < nblk; ++j) {
+                const int s = j & 1;
+                // a slot is refilled once the products of the block before in it are done
+                if (j >= 2 && !bar_wait(&bars->kv_empty[s], (uint32_t)(((j >> 1) - 1) & 1), &bars->abort, p.status))
+                    break;
+                uint8_t* slot = skv + s * LKV_SLOT;
+                bar_expect_tx(&bars->kv_full[s], 2 * Q_BYTES);
+                tma_load_4d(slot, &tk, &bars->kv_full[s], 0, j * QT, h, b);
+                tma_load_4d(slot + Q_BYTES, &tv, &bars->kv_full[s], 0, j * QT, h, b);
+                armed |= 1u << s;
+                armed_ph = (armed_ph & ~(1u << s)) | ((uint32_t)((j >> 1) & 1) << s);
+            }
+            // every copy this CTA issued lands before it may exit
+            bar_wait_drain(&bars->q_full, 0u);
+            for (int s = 0; s < 2; ++s)
+                if (armed & (1u << s)) bar_wait_drain(&bars->kv_full[s], (armed_ph >> s) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = bar_wait(&bars->q_full, 0u, &bars->abort, p.status);
+            const uint64_t ad = sdesc(smem_u32(sq), 16u, 1024u);
+            for (int j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                ok = bar_wait(&bars->kv_full[s], (uint32_t)((j >> 1) & 1), &bars->abort, p.status);
+                // S_j goes over P_{j-1}: the product that reads it has completed
+                if (ok && j > 0) ok = bar_wait(&bars->o_full, (uint32_t)((j - 1) & 1), &bars->abort, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sk = smem_u32(skv + s * LKV_SLOT);
+                const uint64_t bd = sdesc(sk, 16u, 1024u);
+#pragma unroll
+                for (int k = 0; k < HD / 16; ++k)
+                    mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
+                mma_commit(&bars->s_full);
+                ok = bar_wait(&bars->p_ready, (uint32_t)(j & 1), &bars->abort, p.status);
+                // O_j goes where O_{j-1} was: the row threads have read it
+                if (ok && j > 0) ok = bar_wait(&bars->o_free, (uint32_t)((j - 1) & 1), &bars->abort, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                // O_j = P_j V_j: A = P from TMEM (keys 0..63 in columns 0..31, keys
+                // 64..127 in columns 64..95, 8 columns a 16-key step), B = V MN-major
+                const uint64_t vd = sdesc(sk + Q_BYTES, 8192u, 1024u);
+#pragma unroll
+                for (int ks = 0; ks < QT / 16; ++ks) {
+                    const uint32_t pa = tmem + (ks < 4 ? 8u * ks : 64u + 8u * (ks - 4));
+                    mma_f16_ts(tmem + LFWD_O, pa, vd + 128u * ks, idesc_bf16(QT, HD, true), ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->o_full);
+                mma_commit(&bars->kv_empty[s]);  // K_j and V_j read once these complete
+            }
+            mma_commit(&bars->drain);
+            bar_wait_drain(&bars->drain, 0u);
+        }
+    } else {
+        // warp w owns TMEM lanes 32 (w % 4) .. + 31 (the query rows), the keys
+        // 64 half .. + 63 of every block and head-dim columns 32 half .. + 31
+        const int half = (warp - 2) >> 2;
+        const int g = warp & 3;
+        const int r = 32 * g + lane;
+        const int i = q0 + r;
+        const uint32_t trow = tmem + ((uint32_t)(32 * g) << 16);
+        float m = -INFINITY, lh = 0.0f;
+        float a[32];
+#pragma unroll
+        for (int d = 0; d < 32; ++d) a[d] = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nblk; ++j) {
+            ok = ok && __all_sync(0xffffffffu, bar_wait(&bars->s_full, (uint32_t)(j & 1), &bars->abort, p.status));
+            tc_fence_after();
+            const int kb = j * QT + 64 * half;  // this thread's first key of the block
+            float mb = -INFINITY;
+            if (ok) {
+                // the block max, 32 columns at a time (the scores are read again below)
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 32) {
+                    uint32_t sv[32];
+                    __syncwarp();
+                    tmem_ld32(trow + 64u * half + (uint32_t)cc, sv);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int kj = kb + cc + c;
+                        if (kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj))
+                            mb = fmaxf(mb, p.scale * __uint_as_float(sv[c]));
+                    }
+                }
+            }
+            float* rm = red_m + (j & 1) * 2 * QT;
+            rm[half * QT + r] = mb;
+            rows_sync();
+            const float mn = fmaxf(m, fmaxf(rm[r], rm[QT + r]));  // the running max, the same in both halves
+            const float alpha = m == -INFINITY ? 0.0f : __expf(m - mn);
+            float lb = 0.0f;
+            if (ok) {
+                // 32 keys at a time: their 16 packed P columns go over S columns
+                // 64 half + cc / 2 .. + 15, which hold scores this thread has
+                // already read in this pass (keys 64 half .. 64 half + 31 of the
+                // first group, and cc / 2 < cc for the second)
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 32) {
+                    uint32_t sv[32], w[16];
+                    __syncwarp();
+                    tmem_ld32(trow + 64u * half + (uint32_t)cc, sv);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        float e[2];
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            const int kj = kb + cc + c + x;
+                            const bool vis = kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj);
+                            e[x] = vis ? __expf(p.scale * __uint_as_float(sv[c + x]) - mn) : 0.0f;
+                            lb += e[x];
+                        }
+                        w[c >> 1] = pack_bf16(e[0], e[1]);
+                    }
+                    tmem_st16(trow + 64u * half + (uint32_t)(cc >> 1), w);
+                }
+                tmem_wait_st();
+            }
+            lh = lh * alpha + lb;
+            m = mn;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&bars->p_ready);
+            ok = ok && __all_sync(0xffffffffu, bar_wait(&bars->o_full, (uint32_t)(j & 1), &bars->abort, p.status));
+            tc_fence_after();
+            if (ok) {
+                uint32_t o[32];
+                __syncwarp();
+                tmem_ld32(trow + LFWD_O + 32u * half, o);
+#pragma unroll
+                for (int d = 0; d < 32; ++d) a[d] = a[d] * alpha + __uint_as_float(o[d]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&bars->o_free);
+        }
+        // l: the two key halves' sums, first half then second (one order in both threads)
+        red_l[half * QT + r] = lh;
+        rows_sync();
+        const float l = red_l[r] + red_l[QT + r];
+        if (ok && i < p.T) {
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            if (half == 0) p.lse[((int64_t)b * p.H + h) * p.T + i] = l > 0.0f ? m + logf(l) : -INFINITY;
+            __nv_bfloat16* dst = (__nv_bfloat16*)p.o + p.o_off + (int64_t)b * p.o_sb + (int64_t)i * p.o_st +
+                                 (int64_t)h * p.o_sh + 32 * half;
+            uint32_t w[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) w[x] = pack_bf16(a[2 * x] * inv, a[2 * x + 1] * inv);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                ((uint4*)dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(FWD_TMEM));
+}
+
 // ---- backward ---------------------------------------------------------------
 // Both passes, one CTA per (128-row tile of its own operands, head, batch),
-// two resident a SM.  The streamed operand tiles (at most two: T <= 256) are
-// all loaded at the start and taken 64 rows (a sub-tile) at a time:
+// two resident a SM.  The streamed operand tiles come through a ring of two
+// tile slots (the producer refills a slot once the second products of the
+// tile in it have completed) and are taken 64 rows (a sub-tile) at a time:
 //   pass K/V (KV): own K, V (rows = keys); streamed Q, dO (columns = queries)
 //     S^T = K Q^T, dP^T = V dO^T, P^T = exp(scale S^T - L), dS^T = P^T (dP^T - D)
 //     dV += P^T dO, dK += dS^T Q            (dK scaled by `scale` at the end)
@@ -291,12 +534,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
 constexpr int T_BYTES = QT * ROW_BYTES;     // 16 KB: a 128-row tile of one operand
 constexpr int SUB = 64;                     // streamed rows a sub-tile
 constexpr int BWD_THREADS = 320;            // warp 0 TMA, warp 1 MMA, warps 2-9 two per row
-constexpr int BWD_SMEM = 1024 + 6 * T_BYTES + 4 * QT * 4 + 256;
+constexpr int BWD_SMEM = 1024 + 6 * T_BYTES + 256;
 constexpr int BWD_TMEM = 256;
 constexpr uint32_t BWD_DP = 64, BWD_ACC0 = 128, BWD_ACC1 = 192;
 
 struct BwdBars {
-    uint64_t full[2], mm1, ready, mm2, drain;
+    uint64_t full[2], empty[2], mm1, ready, mm2, drain;
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -363,11 +606,9 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* own0 = smem;                   // KV: K, Q: Q  [128 rows][64]
     uint8_t* own1 = own0 + T_BYTES;         // KV: V, Q: dO
-    uint8_t* st0 = own1 + T_BYTES;          // KV: Q, Q: K  [2 tiles][128 rows][64]
+    uint8_t* st0 = own1 + T_BYTES;          // KV: Q, Q: K  [2 slots][128 rows][64]
     uint8_t* st1 = st0 + 2 * T_BYTES;       // KV: dO, Q: V
-    float* sL = (float*)(st1 + 2 * T_BYTES);  // KV: L, D of the streamed queries [2 tiles][128]
-    float* sD = sL + 2 * QT;
-    BwdBars* bars = (BwdBars*)(sD + 2 * QT);
+    BwdBars* bars = (BwdBars*)(st1 + 2 * T_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ot = blockIdx.x, h = blockIdx.y;
     const int r0 = ot * QT;  // first own row (key in KV, query in Q)
@@ -380,6 +621,8 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
     if (threadIdx.x == 0) {
         bar_init(&bars->full[0], 1);
         bar_init(&bars->full[1], 1);
+        bar_init(&bars->empty[0], 1);
+        bar_init(&bars->empty[1], 1);
         bar_init(&bars->mm1, 1);
         bar_init(&bars->ready, 8);
         bar_init(&bars->mm2, 1);
@@ -403,32 +646,40 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
             const CUtensorMap* m_own1 = KV ? &tv : &tdo;
             const CUtensorMap* m_st0 = KV ? &tq : &tk;
             const CUtensorMap* m_st1 = KV ? &tdo : &tv;
+            uint32_t armed = 0, armed_ph = 0;  // slots filled, and the parity of each one's last fill
             for (int t = it0; t < it1; ++t) {
-                uint64_t* fb = &bars->full[t - it0];
-                bar_expect_tx(fb, (t == it0 ? 4u : 2u) * T_BYTES);
-                if (t == it0) {
+                const int u = t - it0, slot = u & 1;
+                // a slot is refilled once the tile before in it has been used up
+                if (u >= 2 && !bar_wait(&bars->empty[slot], (uint32_t)(((u >> 1) - 1) & 1), &bars->abort, p.status))
+                    break;
+                uint64_t* fb = &bars->full[slot];
+                bar_expect_tx(fb, (u == 0 ? 4u : 2u) * T_BYTES);
+                if (u == 0) {
                     tma_load_4d(own0, m_own0, fb, 0, r0, h, b);
                     tma_load_4d(own1, m_own1, fb, 0, r0, h, b);
                 }
-                tma_load_4d(st0 + (t - it0) * T_BYTES, m_st0, fb, 0, t * QT, h, b);
-                tma_load_4d(st1 + (t - it0) * T_BYTES, m_st1, fb, 0, t * QT, h, b);
+                tma_load_4d(st0 + slot * T_BYTES, m_st0, fb, 0, t * QT, h, b);
+                tma_load_4d(st1 + slot * T_BYTES, m_st1, fb, 0, t * QT, h, b);
+                armed |= 1u << slot;
+                armed_ph = (armed_ph & ~(1u << slot)) | ((uint32_t)((u >> 1) & 1) << slot);
             }
             // the copies land before this CTA may exit
-            for (int t = it0; t < it1; ++t) bar_wait_drain(&bars->full[t - it0], 0u);
+            for (int s = 0; s < 2; ++s)
+                if (armed & (1u << s)) bar_wait_drain(&bars->full[s], (armed_ph >> s) & 1u);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = true;
             const uint64_t a0 = sdesc(smem_u32(own0), 16u, 1024u), a1 = sdesc(smem_u32(own1), 16u, 1024u);
             for (int st = 0; st < nst && ok; ++st) {
-                const int t = st >> 1, s = st & 1;
-                if (s == 0) ok = bar_wait(&bars->full[t], 0u, &bars->abort, p.status);
+                const int t = st >> 1, s = st & 1, slot = t & 1;
+                if (s == 0) ok = bar_wait(&bars->full[slot], (uint32_t)((t >> 1) & 1), &bars->abort, p.status);
                 // the previous sub-tile's second products have read P and dS (S and dP columns)
                 if (ok && st > 0) ok = bar_wait(&bars->mm2, (uint32_t)((st - 1) & 1), &bars->abort, p.status);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sub = smem_u32(st0 + t * T_BYTES) + (uint32_t)(s * SUB * ROW_BYTES);
-                const uint32_t sub1 = smem_u32(st1 + t * T_BYTES) + (uint32_t)(s * SUB * ROW_BYTES);
+                const uint32_t sub = smem_u32(st0 + slot * T_BYTES) + (uint32_t)(s * SUB * ROW_BYTES);
+                const uint32_t sub1 = smem_u32(st1 + slot * T_BYTES) + (uint32_t)(s * SUB * ROW_BYTES);
                 const uint64_t b0 = sdesc(sub, 16u, 1024u), b1 = sdesc(sub1, 16u, 1024u);
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
@@ -450,6 +701,8 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
                     mma_f16_ts(tmem + BWD_ACC1, tmem + BWD_DP + col, n0 + 128u * ks, idesc_bf16(QT, HD, true), acc);
                 }
                 mma_commit(&bars->mm2);
+                // the tile's last products: its slot is free once they complete
+                if (s == 1) mma_commit(&bars->empty[slot]);
             }
             mma_commit(&bars->drain);
             bar_wait_drain(&bars->drain, 0u);
@@ -463,16 +716,7 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
         const uint32_t trow = tmem + ((uint32_t)(32 * g) << 16);
         const int64_t lbase = ((int64_t)b * p.H + h) * p.T;
         float Lr = 0.0f, Dr = 0.0f;
-        if (KV) {
-            // L and D of every streamed query, for all the row threads
-            const int tid = threadIdx.x - 64;
-            for (int x = tid; x < (it1 - it0) * QT; x += 256) {
-                const int i = it0 * QT + x;
-                sL[x] = i < p.T ? p.lse[lbase + i] : 0.0f;
-                sD[x] = i < p.T ? p.delta[lbase + i] : 0.0f;
-            }
-            rows_sync();
-        } else if (row < p.T) {
+        if (!KV && row < p.T) {
             Lr = p.lse[lbase + row];
             Dr = p.delta[lbase + row];
         }
@@ -496,8 +740,9 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
                             const int c = SUB * s + 32 * half + cc + u + e;  // streamed row within its tile
                             const int other = (it0 + t) * QT + c;
                             const int i = KV ? other : row, j = KV ? row : other;
-                            const bool vis = i < p.T && j < p.T && (!p.causal || j <= i);
-                            const float L = KV ? sL[t * QT + c] : Lr, D = KV ? sD[t * QT + c] : Dr;
+                            const bool vis = i < p.T && j < p.T && (!p.causal || j <= i) && key_on(p, b, j);
+                            const float L = KV ? (i < p.T ? __ldg(p.lse + lbase + i) : 0.0f) : Lr;
+                            const float D = KV ? (i < p.T ? __ldg(p.delta + lbase + i) : 0.0f) : Dr;
                             const float pe = vis ? __expf(p.scale * __uint_as_float(sv[u + e]) - L) : 0.0f;
                             pv[e] = pe;
                             dsv[e] = pe * (__uint_as_float(dp[u + e]) - D);
@@ -579,8 +824,14 @@ psg_status launch_attention_fwd(const AttnTensor& q, const AttnTensor& k, const 
     if (!make_map_attn(&mq, q, p.T, p.H, p.B, QT) || !make_map_attn(&mk, k, p.T, p.H, p.B, QT) ||
         !make_map_attn(&mv, v, p.T, p.H, p.B, QT))
         return PSG_E_CUDA;
-    if (set_max_dynamic_smem((const void*)attn_fwd, FWD_SMEM) != cudaSuccess) return PSG_E_CUDA;
     const dim3 grid((unsigned)((p.T + QT - 1) / QT), (unsigned)p.H, (unsigned)p.B);
+    if (p.T > KB) {
+        // more keys than one block: the online softmax over 128-key blocks
+        if (set_max_dynamic_smem((const void*)attn_fwd_long, LFWD_SMEM) != cudaSuccess) return PSG_E_CUDA;
+        launch(attn_fwd_long, grid, FWD_THREADS, LFWD_SMEM, (cudaStream_t)stream, mq, mk, mv, p);
+        return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
+    }
+    if (set_max_dynamic_smem((const void*)attn_fwd, FWD_SMEM) != cudaSuccess) return PSG_E_CUDA;
     launch(attn_fwd, grid, FWD_THREADS, FWD_SMEM, (cudaStream_t)stream, mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }

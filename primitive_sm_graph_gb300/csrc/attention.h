@@ -21,6 +21,8 @@ struct AttnParams {
     float* delta;      // [B, H, T] float32 (backward): rowsum(dO * O)
     void* o;           // forward output / backward dQ
     int64_t o_off, o_sb, o_st, o_sh;
+    const uint8_t* kmask;  // [B, T] per-key visibility (nonzero: visible) or null
+    int64_t km_sb;         // its batch stride (elements); token stride 1
 };
 
 psg_status launch_attention_fwd(const AttnTensor& q, const AttnTensor& k, const AttnTensor& v, const AttnParams& p,

@@ -245,6 +245,38 @@ template <> struct SV<PSG_I32> {
     }
 };
 
+// the narrow ints keep a wrapping 32-bit total too and store its low bits
+// (addition modulo 2^width gives the same bits in any grouping)
+template <> struct SV<PSG_I16> {
+    typedef uint32_t A;
+    static constexpr int ES = 2;
+    static __device__ __forceinline__ A ld(const void* p, int64_t o) { return (uint32_t)(int32_t)__ldg((const int16_t*)p + o); }
+    static __device__ __forceinline__ A add(A a, A b) { return a + b; }
+    static __device__ __forceinline__ void st(void* p, int64_t o, A v) { ((uint16_t*)p)[o] = (uint16_t)(v & 0xffffu); }
+    static __device__ __forceinline__ void unpack(const uint4 u, A (&x)[16 / ES])
+    {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = (uint32_t)(int32_t)(int16_t)(w[i] & 0xffffu);
+            x[2 * i + 1] = (uint32_t)(int32_t)(int16_t)(w[i] >> 16);
+        }
+    }
+};
+template <> struct SV<PSG_I8> {
+    typedef uint32_t A;
+    static constexpr int ES = 1;
+    static __device__ __forceinline__ A ld(const void* p, int64_t o) { return (uint32_t)(int32_t)__ldg((const int8_t*)p + o); }
+    static __device__ __forceinline__ A add(A a, A b) { return a + b; }
+    static __device__ __forceinline__ void st(void* p, int64_t o, A v) { ((uint8_t*)p)[o] = (uint8_t)(v & 0xffu); }
+    static __device__ __forceinline__ void unpack(const uint4 u, A (&x)[16 / ES])
+    {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = (uint32_t)(int32_t)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xffu);
+    }
+};
+
 constexpr int SCATTER_UNROLL = 4;  // rows of a run loaded before they are added
 
 // One warp per (run, column segment) item.  A segment is 32 * VPL columns,
@@ -912,7 +944,7 @@ template <int DT>
 static psg_status launch_owner(const ScatterLaunch& L, cudaStream_t s)
 {
     constexpr int ES = SV<DT>::ES;
-    const bool pair = ES == 2 && L.upd_cs == 1 && ((uintptr_t)L.upd + (uint64_t)L.upd_offset * ES) % 4 == 0 &&
+    const bool pair = (DT == PSG_BF16 || DT == PSG_F16) && L.upd_cs == 1 && ((uintptr_t)L.upd + (uint64_t)L.upd_offset * ES) % 4 == 0 &&
                       ((uint64_t)L.upd_rs * ES) % 4 == 0;
     const int64_t chunk = OWNER_THREADS * (pair ? 2 : 1);
     const int64_t ncb = (L.D + chunk - 1) / chunk;
@@ -937,6 +969,8 @@ psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void
         case PSG_BF16: return launch_owner<PSG_BF16>(L, s);
         case PSG_F16: return launch_owner<PSG_F16>(L, s);
         case PSG_F64: return launch_owner<PSG_F64>(L, s);
+        case PSG_I16: return launch_owner<PSG_I16>(L, s);
+        case PSG_I8: return launch_owner<PSG_I8>(L, s);
         default: return launch_owner<PSG_I32>(L, s);
         }
     }
@@ -946,6 +980,8 @@ psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void
         case PSG_BF16: return launch_planned<PSG_BF16>(L, keys, s);
         case PSG_F16: return launch_planned<PSG_F16>(L, keys, s);
         case PSG_F64: return launch_planned<PSG_F64>(L, keys, s);
+        case PSG_I16: return launch_planned<PSG_I16>(L, keys, s);
+        case PSG_I8: return launch_planned<PSG_I8>(L, keys, s);
         default: return launch_planned<PSG_I32>(L, keys, s);
         }
     }
@@ -965,6 +1001,8 @@ psg_status launch_scatter(const ScatterLaunch& L, unsigned long long* keys, void
     case PSG_BF16: launch_accumulate<PSG_BF16>(L, keys, s); break;
     case PSG_F16: launch_accumulate<PSG_F16>(L, keys, s); break;
     case PSG_F64: launch_accumulate<PSG_F64>(L, keys, s); break;
+    case PSG_I16: launch_accumulate<PSG_I16>(L, keys, s); break;
+    case PSG_I8: launch_accumulate<PSG_I8>(L, keys, s); break;
     default: launch_accumulate<PSG_I32>(L, keys, s); break;
     }
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;

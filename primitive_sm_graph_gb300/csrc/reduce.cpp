@@ -249,6 +249,13 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     const int64_t bar_bytes = ((int64_t)teams * 4 * 8 + 127) / 128 * 128;
     while (ns > 2 && bar_bytes + teams * ns * stage_bytes > RED_SMEM_PREF) --ns;
     if (bar_bytes + teams * ns * stage_bytes > RED_SMEM_MAX) staged = false;
+    // a row that one warp holds in registers (a team of at most 32 threads,
+    // the row cached in RED_CACHE_WORDS words a thread) skips the ring: the
+    // loads go out at once and nothing waits on a barrier (measured on the
+    // softmax rows of 4096 x 1024 float32: 14.3 us against 16.4 us staged
+    // for one launch, 10.2 against 12.5 back to back; the GPT block's step
+    // unchanged)
+    if (staged && tl <= 5 && ch_per * words <= RED_CACHE_WORDS) staged = false;
     if (!staged) {
         for (int k = 0; k < n_in; ++k) staged_in[k] = 0;
         stage_bytes = tx_bytes = 0;

@@ -237,30 +237,38 @@ class Tensor:
         assert idx.dtype == "i32" and idx.ndim == 1
         return Tensor("GATHER", (self, idx), (idx.shape[0],) + self.shape[1:], self.dtype)
 
-    def attention(self, k: "Tensor", v: "Tensor", scale: float, causal: bool = True):
+    def attention(self, k: "Tensor", v: "Tensor", scale: float, causal: bool = True, key_mask=None):
         """Fused scaled dot-product attention (limn, "The op set": the one
-        fused node in place of the composed T x T scores): self = Q, k, v
-        are bf16 [B, T, H, hd]; returns O [B, T, H, hd] with
-        O = softmax(scale * Q K^T, keys j > i hidden when causal) V per head."""
+        fused node in place of the composed T x T scores; masking is a flag
+        per key that composes with causal): self = Q, k, v are bf16
+        [B, T, H, hd]; returns O [B, T, H, hd] with O = softmax(scale Q K^T)
+        V per head over the keys query i sees (not j > i when causal, not
+        where key_mask [B, T] int8 is 0; a query that sees no key gets 0)."""
         assert self.shape == k.shape == v.shape and len(self.shape) == 4
         assert self.dtype == k.dtype == v.dtype == "bf16"
-        if self.shape[1] > ATTN_MAX_T or self.shape[3] != ATTN_HD:
+        if self.shape[3] != ATTN_HD:
+            if key_mask is not None:
+                raise NotImplementedError("a key mask needs the fused attention (head dim %d)" % ATTN_HD)
             return _composed_attention(self, k, v, scale, causal)
-        return Tensor("ATTN", (self, k, v), self.shape, "bf16", arg=(float(scale), bool(causal)))
+        srcs = (self, k, v) + ((_key_mask(key_mask, self.shape),) if key_mask is not None else ())
+        return Tensor("ATTN", srcs, self.shape, "bf16", arg=(float(scale), bool(causal), key_mask is not None))
 
-    def attention_packed(self, scale: float, causal: bool = True):
+    def attention_packed(self, scale: float, causal: bool = True, key_mask=None):
         """The fused attention over a packed qkv tensor [B, T, 3, H, hd] bf16
         (slot 0 Q, 1 K, 2 V: a fused projection's output): returns O
         [B, T, H, hd].  Its gradient is one tensor in the same packed
         layout, which the backward kernels write in place (no pad-and-add of
-        dQ, dK, dV back into the packed tensor)."""
+        dQ, dK, dV back into the packed tensor).  key_mask as for attention."""
         assert len(self.shape) == 5 and self.shape[2] == 3 and self.dtype == "bf16"
         B, T, _, H, hd = self.shape
-        if T > ATTN_MAX_T or hd != ATTN_HD:
+        if hd != ATTN_HD:
+            if key_mask is not None:
+                raise NotImplementedError("a key mask needs the fused attention (head dim %d)" % ATTN_HD)
             q, k, v = (self.shrink(((0, B), (0, T), (i, i + 1), (0, H), (0, hd))).reshape(B, T, H, hd)
                        for i in range(3))
             return _composed_attention(q, k, v, scale, causal)
-        return Tensor("ATTN", (self,), (B, T, H, hd), "bf16", arg=(float(scale), bool(causal)))
+        srcs = (self,) + ((_key_mask(key_mask, (B, T, H, hd)),) if key_mask is not None else ())
+        return Tensor("ATTN", srcs, (B, T, H, hd), "bf16", arg=(float(scale), bool(causal), key_mask is not None))
 
     def scatter_add(self, idx: "Tensor", upd: "Tensor"):
         """SCATTER-add along dim 0: self + rows of upd added at idx, in order."""
@@ -366,8 +374,13 @@ def _inverse(perm):
 
 # keys the fused attention kernels hold in one block, and their head dim;
 # longer sequences and other head dims take the composed form below
-ATTN_MAX_T = 256
 ATTN_HD = 64
+
+
+def _key_mask(m, shape):
+    """A per-key mask operand: int8 [B, T] (nonzero: visible)."""
+    assert isinstance(m, Tensor) and m.dtype == "i8" and m.shape == (shape[0], shape[1]), "key_mask: int8 [B, T]"
+    return m
 
 
 def _composed_attention(q, k, v, scale, causal):
@@ -1245,26 +1258,38 @@ class Executor:
             vs = slots(v)
         return buf, vs
 
+    def _attn_mask(self, fwd: Tensor):
+        """The attention node's key mask as a contiguous int8 [B, T] buffer
+        starting at its data pointer, or None."""
+        if not fwd.arg[2]:
+            return None
+        buf, v = self.realize(fwd.src[-1])
+        if v.mask is not None or v.offset != 0 or not v.contiguous():
+            buf, v = self._copy_contig(buf, v, "i8")
+        return buf
+
     def _realize_attn(self, t: Tensor):
-        scale, causal = t.arg
+        scale, causal, _ = t.arg
         B, T, H, _ = t.shape
-        if len(t.src) == 1:  # packed qkv
-            b, (vq, vk, vv) = self._attn_slots(t.src[0], t.shape)
+        ops = t.src[:-1] if t.arg[2] else t.src
+        if len(ops) == 1:  # packed qkv
+            b, (vq, vk, vv) = self._attn_slots(ops[0], t.shape)
             bq = bk = bv = b
         else:
-            (bq, vq), (bk, vk), (bv, vv) = (self._attn_operand(x) for x in t.src)
+            (bq, vq), (bk, vk), (bv, vv) = (self._attn_operand(x) for x in ops)
+        km = self._attn_mask(t)
         out = self._new(t.shape, "bf16")
         lse = self._new((B, H, T), "f32")
         self._lib("psg_attention_fwd")(bq, self._pview(bq, vq, "bf16"), bk, self._pview(bk, vk, "bf16"), bv,
-                            self._pview(bv, vv, "bf16"), out, self._pview(out, View(t.shape), "bf16"), lse, scale,
-                            causal, self._status(), stream=self._s())
+                                       self._pview(bv, vv, "bf16"), out, self._pview(out, View(t.shape), "bf16"),
+                                       lse, scale, causal, self._status(), stream=self._s(), key_mask=km)
         t._aux = lse
         self.log.append(("attention", t.shape))
         return out, View(t.shape)
 
     def _realize_attn_bwd(self, t: Tensor):
         fwd, g = t.src[-2:]
-        scale, causal = t.arg
+        scale, causal, _ = t.arg
         B, T, H, _ = fwd.shape
         bo, vo = self.realize(fwd)
         lse = fwd._aux
@@ -1282,9 +1307,10 @@ class Executor:
                   for i in range(3)]
         delta = self._new((B, H, T), "f32")
         pv = lambda bv: self._pview(bv[0], bv[1], "bf16")
-        self._lib("psg_attention_bwd")(ops[0][0], pv(ops[0]), ops[1][0], pv(ops[1]), ops[2][0], pv(ops[2]), bo, pv((bo, vo)),
-                            ops[3][0], pv(ops[3]), lse, delta, out, pv((out, gv[0])), out, pv((out, gv[1])), out,
-                            pv((out, gv[2])), scale, causal, self._status(), stream=self._s())
+        self._lib("psg_attention_bwd")(ops[0][0], pv(ops[0]), ops[1][0], pv(ops[1]), ops[2][0], pv(ops[2]), bo,
+                                       pv((bo, vo)), ops[3][0], pv(ops[3]), lse, delta, out, pv((out, gv[0])), out,
+                                       pv((out, gv[1])), out, pv((out, gv[2])), scale, causal, self._status(),
+                                       stream=self._s(), key_mask=self._attn_mask(fwd))
         self.log.append(("attention_bwd", fwd.shape))
         return out, View(t.shape)
 
@@ -1436,8 +1462,20 @@ class _Plan:
             return type(x)(self.sym(y) for y in x)
         return x
 
+    @staticmethod
+    def _has_ref(x):
+        if isinstance(x, _Ref):
+            return True
+        return isinstance(x, (list, tuple)) and any(_Plan._has_ref(y) for y in x)
+
     def call(self, name, args, kw):
-        self.calls.append((name, self.sym(args), {k: self.sym(v, k) for k, v in kw.items()}))
+        args = self.sym(args)
+        kw = {k: self.sym(v, k) for k, v in kw.items()}
+        # the arguments that name buffers, rebuilt at each replay; the rest
+        # (programs, Views, sizes) are passed as recorded
+        dyn = [i for i, x in enumerate(args) if self._has_ref(x)]
+        dkw = [k for k, v in kw.items() if self._has_ref(v)]
+        self.calls.append((name, args, kw, dyn, dkw))
 
     def run(self, ex, leaves, roots):
         status, stream = ex._status(), ex._s()
@@ -1450,8 +1488,16 @@ class _Plan:
             if isinstance(x, (list, tuple)):
                 return type(x)(val(y) for y in x)
             return x
-        for name, args, kw in self.calls:
-            getattr(A, name)(*val(args), **{k: val(v) for k, v in kw.items()})
+        for name, args, kw, dyn, dkw in self.calls:
+            if dyn:
+                args = list(args)
+                for i in dyn:
+                    args[i] = val(args[i])
+            if dkw:
+                kw = dict(kw)
+                for k in dkw:
+                    kw[k] = val(kw[k])
+            getattr(A, name)(*args, **kw)
         ex.log.extend(self.log)
         out = []
         for t, (ref, v, dt) in zip(roots, self.outs):
@@ -1468,34 +1514,42 @@ PLAN_CACHE = os.environ.get("PSG_NO_PLAN_CACHE") is None
 _PLAN_LIMIT = 256
 
 
+_PLAIN_ARG = (type(None), int, float, str, bool)
+
+
 def _structure(roots):
     """(key, leaf buffers) of the unrealized graph under roots: every node's
     op, dtype, shape, argument and operands by position, every leaf's
     layout, size, alignment and aliasing; equal keys schedule alike."""
     index, items, leaves, first_ptr = {}, [], [], {}
-    stack = [(r, False) for r in reversed(roots)]
+    stack = list(reversed(roots))
     while stack:
-        t, done = stack.pop()
+        t = stack[-1]
         if id(t) in index:
+            stack.pop()
             continue
         if t._real is not None:
+            stack.pop()
             buf, v = t._real
             p = buf.data_ptr()
-            aux = getattr(t, "_aux", None)
-            items.append(("L", t.dtype, t.shape, v.key(), str(buf.dtype), buf.numel(), p % 256,
+            aux = t._aux
+            items.append(("L", t.dtype, t.shape, v.key(), buf.dtype, buf.numel(), p % 256,
                           first_ptr.setdefault(p, len(leaves)), aux is not None))
             leaves.append(buf)
             if aux is not None:
                 leaves.append(aux)
             index[id(t)] = len(items) - 1
             continue
-        if not done:
-            stack.append((t, True))
-            stack.extend((s, False) for s in reversed(t.src) if id(s) not in index)
+        pending = [s for s in reversed(t.src) if id(s) not in index]
+        if pending:
+            stack.extend(pending)
             continue
-        items.append((t.op, t.dtype, t.shape, repr(t.arg), tuple(index[id(s)] for s in t.src)))
+        stack.pop()
+        arg = t.arg
+        items.append((t.op, t.dtype, t.shape, arg if type(arg) in _PLAIN_ARG else repr(arg),
+                      tuple([index[id(s)] for s in t.src])))
         index[id(t)] = len(items) - 1
-    return (tuple(items), tuple(index[id(r)] for r in roots)), leaves
+    return (tuple(items), tuple([index[id(r)] for r in roots])), leaves
 
 
 def realize_all(*ts):
@@ -1654,8 +1708,11 @@ def _vjp(t: Tensor, g: Tensor):
     if op == "SCATTER":
         return [(s[0], g), (s[2], g.gather(s[1]))]
     if op == "ATTN":
-        # one node computes dQ, dK, dV together (the two-pass backward)
+        # one node computes dQ, dK, dV together (the two-pass backward); the
+        # key mask (the last operand, when there is one) has no gradient
         gb = g.cast("bf16") if g.dtype != "bf16" else g
+        if t.arg[2]:
+            s = s[:-1]
         if len(s) == 1:  # packed qkv: the gradient in the same packed layout
             return [(s[0], Tensor("ATTN_BWD", (s[0], t, gb), s[0].shape, "bf16", arg=t.arg))]
         d = Tensor("ATTN_BWD", (s[0], s[1], s[2], t, gb), (3,) + t.shape, "bf16", arg=t.arg)

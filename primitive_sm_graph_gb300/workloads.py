@@ -55,9 +55,9 @@ def target_index(tok: Tensor, V: int, device) -> Tensor:
 
 
 def fused_attention_applies(T: int, D: int, H: int) -> bool:
-    """The fused attention op covers head dim 64 and one key block (T <= 256);
-    other shapes use the composed form."""
-    return D // H == 64 and T <= 256
+    """The fused attention op covers head dim 64 at any sequence length;
+    other head dims use the composed form."""
+    return D // H == 64
 
 
 def gpt_block_loss(tok: torch.Tensor, w: dict, H: int, eps: float = 1e-6,

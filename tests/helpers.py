@@ -70,39 +70,57 @@ def first_mismatches(a: np.ndarray, b: np.ndarray, k=5):
     return [(int(i), av[i], bv[i]) for i in bad[:k]], int(bad.size)
 
 
-def _visible(T, causal):
-    return np.tril(np.ones((T, T), bool)) if causal else np.ones((T, T), bool)
+def _visible(T, causal, km=None):
+    v = np.tril(np.ones((T, T), bool)) if causal else np.ones((T, T), bool)
+    return v if km is None else v & (np.asarray(km) != 0)[None, :]
 
 
-def attention_fwd_bounds(Q, K, V, O_ref, L_ref, scale, causal):
+def _probs(Q, K, L, scale, vis, h):
+    with np.errstate(invalid="ignore", over="ignore"):
+        return np.where(vis, np.exp(scale * Q[h] @ K[h].T - L[h][:, None]), 0.0)
+
+
+def attention_fwd_bounds(Q, K, V, O_ref, L_ref, scale, causal, key_mask=None):
     """Per-cell bound on the fused forward's output O (heads [BH, T, d],
     float64 oracle values): S is a float32 sum of exact bf16 products, P
     rounds to bf16 before P V, and O rounds once to bf16:
-        |O - O*| <= 2^-8 * sum_j P*_ij |V_jd| + 2^-7 |O*|."""
-    vis = _visible(Q.shape[1], causal)
+        |O - O*| <= 2^-8 * sum_j P*_ij |V_jd| + 2^-7 |O*|.
+    key_mask: None or [heads, T] (nonzero: visible)."""
     mag = np.zeros_like(O_ref)
     for h in range(Q.shape[0]):
-        P = np.where(vis, np.exp(scale * Q[h] @ K[h].T - L_ref[h][:, None]), 0.0)
+        vis = _visible(Q.shape[1], causal, None if key_mask is None else key_mask[h])
+        P = _probs(Q, K, L_ref, scale, vis, h)
         mag[h] = P @ np.abs(V[h])
     return 2.0 ** -8 * mag + 2.0 ** -7 * np.abs(O_ref)
 
 
-def attention_bwd_bounds(Q, K, V, O, dO, L, scale, causal, refs):
+def attention_bwd_bounds(Q, K, V, O, dO, L, scale, causal, refs, key_mask=None, o_err=None):
     """Per-cell bounds on the fused backward's (dQ, dK, dV) against the
     float64 oracle values refs = (dQ*, dK*, dV*): P and dS round to bf16
     before the second products and every output rounds once to bf16:
         dV:     2^-8 * sum_i P_ij |dO_id|                          + 2^-7 |dV*|
-        dQ, dK: 2^-7 * scale * sum_j P_ij (|dP_ij| + |D_i|) |K_jd|   + 2^-7 |dQ*|."""
-    vis = _visible(Q.shape[1], causal)
+        dQ, dK: 2^-7 * scale * sum_j P_ij (|dP_ij| + |D_i|) |K_jd|   + 2^-7 |dQ*|.
+    o_err: None when the backward reads the O the oracle used; else a bound
+    on |O_read - O| per cell (the forward's own bar, when refs come from the
+    exact O but the backward reads the forward's bf16 output).  Its effect on
+    D_i = sum_d dO_id O_id, e_i = sum_d |dO_id| o_err_id, reaches dS as
+    P_ij e_i and adds scale * sum_j P_ij e_i |K_jd| to dQ (and the transpose
+    to dK); dV does not read O."""
     mq, mk, mv = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    eq, ek = np.zeros_like(Q), np.zeros_like(K)
     for h in range(Q.shape[0]):
-        P = np.where(vis, np.exp(scale * Q[h] @ K[h].T - L[h][:, None]), 0.0)
+        vis = _visible(Q.shape[1], causal, None if key_mask is None else key_mask[h])
+        P = _probs(Q, K, L, scale, vis, h)
         dP = dO[h] @ V[h].T
         D = (dO[h] * O[h]).sum(1)
         G = np.abs(P) * (np.abs(dP) + np.abs(D)[:, None])
         mv[h] = P.T @ np.abs(dO[h])
         mq[h] = scale * (G @ np.abs(K[h]))
         mk[h] = scale * (G.T @ np.abs(Q[h]))
+        if o_err is not None:
+            E = np.abs(P) * (np.abs(dO[h]) * o_err[h]).sum(1)[:, None]
+            eq[h] = scale * (E @ np.abs(K[h]))
+            ek[h] = scale * (E.T @ np.abs(Q[h]))
     dq, dk, dv = refs
-    return (2.0 ** -7 * mq + 2.0 ** -7 * np.abs(dq), 2.0 ** -7 * mk + 2.0 ** -7 * np.abs(dk),
+    return (2.0 ** -7 * mq + 2.0 ** -7 * np.abs(dq) + eq, 2.0 ** -7 * mk + 2.0 ** -7 * np.abs(dk) + ek,
             2.0 ** -8 * mv + 2.0 ** -7 * np.abs(dv))

@@ -539,6 +539,14 @@ class Replayer:
         B, T, H, d = v.shape
         return v.transpose(0, 2, 1, 3).reshape(B * H, T, d)
 
+    def _key_mask(self, km, qv):
+        """A [B, T] byte key mask on the device as the oracle's [B*H, T]."""
+        if km is None:
+            return None
+        B, T, H = int(qv.shape[0]), int(qv.shape[1]), int(qv.shape[2])
+        m = snap(km, "i8", B * T).reshape(B, T)
+        return np.repeat(m, H, axis=0)
+
     def _attention_fwd(self, f):
         A, O, P = self.A, self.O, self.P
 
@@ -547,15 +555,17 @@ class Replayer:
             from oracle.attention import attention_fwd
             self.sync()
             Q, K, V = (self._heads(read_view(O, P, A, b, x)) for b, x in ((q, qv), (k, kv), (v, vv)))
+            km = self._key_mask(kw.get("key_mask"), qv)
             st = f(q, qv, k, kv, v, vv, o, ov, lse, scale, causal, *a, **kw)
             self.sync()
             rec = self._rec("attention_fwd", "heads %d T %d" % Q.shape[:2])
-            O_ref, L_ref = attention_fwd(Q, K, V, scale, causal)
+            O_ref, L_ref = attention_fwd(Q, K, V, scale, causal, key_mask=km)
             got = self._heads(read_view(O, P, A, o, ov))
-            tol = attention_fwd_bounds(Q, K, V, O_ref, L_ref, scale, causal)
+            tol = attention_fwd_bounds(Q, K, V, O_ref, L_ref, scale, causal, key_mask=km)
             L = snap(lse, "f32", Q.shape[0] * Q.shape[1]).astype(np.float64).reshape(L_ref.shape)
             ok = np.abs(got - O_ref) <= tol
-            okl = np.abs(L - L_ref) <= 1e-4 + 2.0 ** -16 * np.abs(L_ref)
+            with np.errstate(invalid="ignore"):
+                okl = (np.abs(L - L_ref) <= 1e-4 + 2.0 ** -16 * np.abs(L_ref)) | (L == L_ref)
             rec.cells = ok.size + okl.size
             rec.bad = int((~ok).sum() + (~okl).sum())
             return st
@@ -572,12 +582,13 @@ class Replayer:
             Q, K, V, Oo, dO = (self._heads(read_view(O, P, A, b, x))
                                for b, x in ((q, qv), (k, kv), (v, vv), (o, ov), (do, dov)))
             L = snap(lse, "f32", Q.shape[0] * Q.shape[1]).astype(np.float64).reshape(Q.shape[:2])
+            km = self._key_mask(kw.get("key_mask"), qv)
             st = f(q, qv, k, kv, v, vv, o, ov, do, dov, lse, delta, dq, dqv, dk, dkv, dv, dvv, scale, causal,
                    *a, **kw)
             self.sync()
             rec = self._rec("attention_bwd", "heads %d T %d" % Q.shape[:2])
-            refs = attention_bwd(Q, K, V, Oo, dO, L, scale, causal)
-            bounds = attention_bwd_bounds(Q, K, V, Oo, dO, L, scale, causal, refs)
+            refs = attention_bwd(Q, K, V, Oo, dO, L, scale, causal, key_mask=km)
+            bounds = attention_bwd_bounds(Q, K, V, Oo, dO, L, scale, causal, refs, key_mask=km)
             cells = bad = 0
             for buf, view, ref, tol in zip((dq, dk, dv), (dqv, dkv, dvv), refs, bounds):
                 got = self._heads(read_view(O, P, A, buf, view))

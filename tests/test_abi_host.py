@@ -157,8 +157,13 @@ def test_scatter_workspace_checks(A):
     assert need >= 10 * 8
     st = A.psg_scatter_add(fake, dv, fake, 10, fake, uv, fake, need - 8, fake, stream=0, check=False)
     assert st == A.E_WORKSPACE
+    # dst and upd of two dtypes, and an unknown dtype, are refused
     st = A.psg_scatter_add(fake, dv, fake, 10, fake, A.make_view("i8", (10, 2)), fake, need, fake,
                            stream=0, check=False)
+    assert st == A.E_UNSUPPORTED_DTYPE
+    bad, badu = A.make_view("i8", (4, 2)), A.make_view("i8", (10, 2))
+    bad.dtype = badu.dtype = 99
+    st = A.psg_scatter_add(fake, bad, fake, 10, fake, badu, fake, need, fake, stream=0, check=False)
     assert st == A.E_UNSUPPORTED_DTYPE
 
 

@@ -77,7 +77,7 @@ def _scatter(A, dst, idx, upd):
     return int(st.item())
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16", "f16", "i32", "f64"])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16", "i32", "i16", "i8", "f64"])
 @pytest.mark.parametrize("case", ["embedding_grad", "single_row", "permutation", "ragged", "large", "long_runs",
                                   "wide_small", "wide", "wide_max", "target_pick", "deep_keys", "one_row", "one"])
 def test_scatter_add_matches_oracle(A, O, dt, case):

@@ -319,7 +319,7 @@ def test_staged_wait_gives_up_with_timeout_status_then_recovers(A, O, PR, monkey
     the waits give up, PSG_E_TIMEOUT reaches the status word, and the kernel
     still ends, after the copies it did issue have landed, with the context
     usable.  The same call without the hook is then correct again."""
-    x = SI.softmax_input(7, 600, 1024)  # 4 KB rows: the staged ring
+    x = SI.softmax_input(7, 300, 4096)  # 16 KB rows, wider than a warp holds: the staged ring
     dx = dev(x)
     y = torch.empty_like(dx)
     st = torch.zeros((1,), dtype=torch.int32, device="cuda")
