@@ -142,7 +142,7 @@ psg_status plan_epilogue(const psg_epilogue* E, const psg_view* Cv, int dm, int 
         dl += std::to_string(k < nin ? dts[k] : 0) + (k < 7 ? ", " : "};\n");
         ml += std::to_string(k < nin ? modes[k] : 0) + (k < 7 ? ", " : "};\n");
     }
-    spec.tables = dl + ml;
+    spec.tables = dl + ml + "constexpr int kEpiN = " + std::to_string(nin) + ";\n";
     // a half-width C is rounded by the store itself (the same bits)
     spec.prog = gen_eval(nodes.data(), I, "EpiProg", "", acc, Cv->dtype != PSG_F32);
     return PSG_OK;

@@ -723,6 +723,16 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
         bool ok = true;
         for (int st = 0; st < nst; ++st) {
             const int t = st >> 1, s = st & 1;
+            // KV pass: L and D of the 32 queries this warp's columns cover,
+            // one per lane (loaded before the wait), handed out by shuffles
+            float Lq = 0.0f, Dq = 0.0f;
+            if (KV) {
+                const int iq = (it0 + t) * QT + SUB * s + 32 * half + lane;
+                if (iq < p.T) {
+                    Lq = __ldg(p.lse + lbase + iq);
+                    Dq = __ldg(p.delta + lbase + iq);
+                }
+            }
             ok = ok && __all_sync(0xffffffffu, bar_wait(&bars->mm1, (uint32_t)(st & 1), &bars->abort, p.status));
             tc_fence_after();
             if (ok) {
@@ -741,8 +751,8 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
                             const int other = (it0 + t) * QT + c;
                             const int i = KV ? other : row, j = KV ? row : other;
                             const bool vis = i < p.T && j < p.T && (!p.causal || j <= i) && key_on(p, b, j);
-                            const float L = KV ? (i < p.T ? __ldg(p.lse + lbase + i) : 0.0f) : Lr;
-                            const float D = KV ? (i < p.T ? __ldg(p.delta + lbase + i) : 0.0f) : Dr;
+                            const float L = KV ? __shfl_sync(0xffffffffu, Lq, cc + u + e) : Lr;
+                            const float D = KV ? __shfl_sync(0xffffffffu, Dq, cc + u + e) : Dr;
                             const float pe = vis ? __expf(p.scale * __uint_as_float(sv[u + e]) - L) : 0.0f;
                             pv[e] = pe;
                             dsv[e] = pe * (__uint_as_float(dp[u + e]) - D);

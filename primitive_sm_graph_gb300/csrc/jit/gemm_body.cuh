@@ -16,6 +16,7 @@
 struct EpiNone {
     static constexpr bool active = false;
     struct U {};
+    struct Raw {};
 };
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
@@ -121,10 +122,23 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, const CUtensorM
     // a fused epilogue program: its values that are uniform along the row,
     // once per row
     typename Epi::U eu;
+    // the program's inputs for a 64-column slice are fetched one slice ahead
+    // into registers, so their loads are in flight while the slice before is
+    // computed and stored (not one load latency per 8 columns)
+    // (the slice loop stays rolled: unrolled, its code no longer fits the
+    // instruction cache and every contraction's epilogue slows down)
+    typename Epi::Raw raw, next;
     if constexpr (Epi::active) {
-        if (m < p.M) eu = Epi::row_uni(p, b, m);
+        if (m < p.M) {
+            eu = Epi::row_uni(p, b, m);
+            Epi::fetch(p, b, m, n_base, raw);
+        }
     }
+#pragma unroll 1
     for (int c2 = 0; c2 < BN; c2 += 64) {
+        if constexpr (Epi::active) {
+            if (c2 + 64 < BN && m < p.M) Epi::fetch(p, b, m, n_base + c2 + 64, next);
+        }
         uint32_t rr[2][32];
         __syncwarp();  // tcgen05.ld is warp-collective: reach it converged
         tmem_ld32_nowait(tm + (uint32_t)c2, rr[0]);
@@ -133,7 +147,8 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, const CUtensorM
         // the fused epilogue replaces each float32 total by the program's
         // value (rounded as its nodes round) before the store rounds it into C
         if constexpr (Epi::active) {
-            if (m < p.M) Epi::apply(p, eu, b, m, n_base + c2, rr);
+            if (m < p.M) Epi::apply(p, eu, b, m, n_base + c2, rr, raw);
+            raw = next;
         }
         if (!p.tma_store) {
 #pragma unroll
@@ -331,11 +346,13 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap& tmap_a, const CU
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
             const int t = u / p.splits, sp = u - t * p.splits;
             const int acc = local & 1;
+            int b, mb, nb;
+            tile_coords(p.num_m, p.num_n, t, b, mb, nb);
+            // the epilogue program's inputs for this tile head for L2 while the products run
+            if constexpr (Epi::active) Epi::prefetch_l2(p, b, mb * BM + q * 32 + lane, nb * BN);
             if (!bar_wait(&bars->tfull[acc], aph[acc], &bars->abort, p.status)) break;
             aph[acc] ^= 1u;
             tc_fence_after();
-            int b, mb, nb;
-            tile_coords(p.num_m, p.num_n, t, b, mb, nb);
             epilogue_rows<Epi>(p, &tmap_c, slots, nst, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN),
                           mb * BM + q * 32, nb * BN, sp, b, lane);
             tc_fence_before();
@@ -527,11 +544,12 @@ __device__ __forceinline__ void tc_gemm2_body(const CUtensorMap& tmap_a, const C
         for (int u = cid; u < units; u += ncl, ++local) {
             const int t = u / p.splits, sp = u - t * p.splits;
             const int acc = local & 1;
+            int b, mb, nb;
+            tile_coords(p.num_m, p.num_n, t, b, mb, nb);
+            if constexpr (Epi::active) Epi::prefetch_l2(p, b, mb * P_BM + (int)rank * 128 + q * 32 + lane, nb * BN);
             if (!bar_wait(&bars->tfull[acc], aph[acc], &bars->abort, p.status)) break;
             aph[acc] ^= 1u;
             tc_fence_after();
-            int b, mb, nb;
-            tile_coords(p.num_m, p.num_n, t, b, mb, nb);
             epilogue_rows<Epi>(p, &tmap_c, slots, nst, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN),
                           mb * P_BM + (int)rank * 128 + q * 32, nb * BN, sp, b, lane);
             tc_fence_before();

@@ -270,13 +270,21 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     if (kch == 0) stash = -1;
     const int stash_node = stash >= 0 ? stages[stash].n_nodes - 1 : -1;
     // resident blocks the launch bound asks registers for: what the ring
-    // leaves room for in staged mode, else 4 (measured best for the softmax
-    // and RMSNorm rows); columnar, 512 threads an SM, so the unrolled stream
-    // keeps its loads in registers
+    // leaves room for in staged mode; with the row in registers, as many as
+    // leave each thread its cached words and stash plus about 56 working
+    // registers, so nothing spills (measured on one GB300: the 4096 x 1024
+    // float32 softmax, 104 registers estimated, 13.0 us with 2 blocks of
+    // 115 registers against 15.0 us with 4 blocks of 64 that spilled 140
+    // bytes; the GPT block's replayed step 0.565 against 0.572 ms); else 4;
+    // columnar, 512 threads an SM, so the unrolled stream keeps its loads in
+    // registers
     int min_blocks = 4;
     if (staged) {
         min_blocks = (int)((227 * 1024) / (P->smem + 1024));
         min_blocks = min_blocks < 1 ? 1 : min_blocks > 4 ? 4 : min_blocks;
+    } else if (kch > 0) {
+        const int est = kch * words + (stash >= 0 ? kch * PSG_VEC : 0) + 56;
+        min_blocks = std::max(1, std::min(4, 65536 / (RED_THREADS * est)));
     }
     // columnar: 32 rows a CTA and up to 16 members (warps), as many as keep
     // RED_COL_MIN_CHUNKS chunks each; a cluster of C CTAs (a power of two up

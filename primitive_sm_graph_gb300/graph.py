@@ -24,6 +24,7 @@ and the stream.
 """
 from __future__ import annotations
 
+import ctypes
 import os
 import sys
 from math import prod
@@ -561,9 +562,14 @@ class Executor:
             return f
 
         def call(*args, **kw):
-            st = f(*args, **kw)
+            cap = _RawCapture(A.lib)
+            A.lib = cap  # the binding's raw call is forwarded and kept for the plan
+            try:
+                st = f(*args, **kw)
+            finally:
+                A.lib = cap.lib
             if st == A.OK:
-                rec.call(name, args, kw)
+                rec.call(name, args, kw, cap.calls)
             return st
         return call
 
@@ -1433,22 +1439,113 @@ class _Ref:
         self.kind, self.i = kind, i
 
 
+class _RawCapture:
+    """Stands in for the binding's library handle while a call is recorded:
+    forwards each raw C call and keeps its function and ctypes arguments."""
+
+    def __init__(self, lib):
+        self.lib, self.calls = lib, []
+
+    def __getattr__(self, name):
+        f = getattr(self.lib, name)
+
+        def call(*cargs):
+            self.calls.append((f, cargs))
+            return f(*cargs)
+        return call
+
+
+_PTR_MIN = 1 << 32  # device addresses lie above this; smaller ints are sizes and flags
+
+
 class _Plan:
     """The library calls one graph structure was realized into, recorded
     once (limn, "Reading the schedule": the compiled devices cache execution
     plans by graph structure).  Replaying it rebinds the buffers and makes
-    the same calls: no scheduling, lowering or program building."""
+    the same calls: no scheduling, lowering or program building.
+
+    Each call is also kept in its marshalled form (the C function and its
+    ctypes arguments: node arrays, Views, sizes) with the places that hold a
+    buffer address or the stream; a replay writes the new addresses into
+    those places and calls the C function directly.  A call whose arguments
+    hold an address the plan cannot name keeps the binding-level path."""
 
     def __init__(self, ex, leaves):
         self.refs = {id(b): _Ref("leaf", i) for i, b in reversed(list(enumerate(leaves)))}
         self.refs[id(ex._status())] = _Ref("status")
+        self.ptrs = {}
+        for i, b in reversed(list(enumerate(leaves))):
+            self._name_ptr(b, _Ref("leaf", i))
+        self._name_ptr(ex._status(), _Ref("status"))
+        self.stream_handle = A._stream(ex._s())
         self.allocs, self.keep, self.calls, self.outs, self.log = [], [], [], [], []
+        self.fast = []
         self.ok = True
+
+    def _name_ptr(self, t, ref):
+        p = t.data_ptr()
+        if t.numel() == 0 or p < _PTR_MIN:
+            return
+        old = self.ptrs.get(p)
+        if old is not None and (old.kind, old.i) != (ref.kind, ref.i):
+            self.ptrs[p] = None  # two buffers at one address: not nameable
+        elif old is None and p not in self.ptrs:
+            self.ptrs[p] = ref
 
     def alloc(self, t, spec):
         self.refs[id(t)] = _Ref("tmp", len(self.allocs))
+        self._name_ptr(t, self.refs[id(t)])
         self.allocs.append(spec)
         self.keep.append(t)
+
+    def _marshalled(self, raw):
+        """(C function, argument list, slots) of one recorded raw call, or
+        None; a slot is (container, index or field, ref)."""
+        if len(raw) != 1:
+            return None
+        f, cargs = raw[0]
+        cargs = list(cargs)
+        slots = []
+
+        def name(v):
+            if v is None or v < _PTR_MIN:
+                return False, None
+            r = self.ptrs.get(v)
+            return True, r
+
+        for i, a in enumerate(cargs):
+            if isinstance(a, int):
+                big, r = name(a)
+                if not big:
+                    continue
+                if r is None:
+                    if a == self.stream_handle and i == len(cargs) - 1:
+                        slots.append((cargs, i, _Ref("stream")))
+                        continue
+                    return None
+                slots.append((cargs, i, r))
+            elif isinstance(a, ctypes.Array) and a._type_ is ctypes.c_void_p:
+                for j in range(len(a)):
+                    big, r = name(a[j])
+                    if big and r is None:
+                        return None
+                    if big:
+                        slots.append((a, j, r))
+            elif type(a).__name__ == "CArgObject" and isinstance(getattr(a, "_obj", None), A.psg_epilogue):
+                e = a._obj
+                for j in range(e.n_in):
+                    big, r = name(e.in_[j])
+                    if big and r is None:
+                        return None
+                    if big:
+                        slots.append((e.in_, j, r))
+        # the stream goes last in every launch call (0: the default stream)
+        if not slots or slots[-1][2].kind != "stream":
+            if cargs and isinstance(cargs[-1], int) and cargs[-1] == self.stream_handle:
+                slots.append((cargs, len(cargs) - 1, _Ref("stream")))
+            else:
+                return None
+        return f, cargs, slots, raw
 
     def sym(self, x, key=None):
         if key == "stream":
@@ -1468,7 +1565,7 @@ class _Plan:
             return True
         return isinstance(x, (list, tuple)) and any(_Plan._has_ref(y) for y in x)
 
-    def call(self, name, args, kw):
+    def call(self, name, args, kw, raw=()):
         args = self.sym(args)
         kw = {k: self.sym(v, k) for k, v in kw.items()}
         # the arguments that name buffers, rebuilt at each replay; the rest
@@ -1476,6 +1573,7 @@ class _Plan:
         dyn = [i for i, x in enumerate(args) if self._has_ref(x)]
         dkw = [k for k, v in kw.items() if self._has_ref(v)]
         self.calls.append((name, args, kw, dyn, dkw))
+        self.fast.append(self._marshalled(raw) if raw else None)
 
     def run(self, ex, leaves, roots):
         status, stream = ex._status(), ex._s()
@@ -1488,7 +1586,21 @@ class _Plan:
             if isinstance(x, (list, tuple)):
                 return type(x)(val(y) for y in x)
             return x
-        for name, args, kw, dyn, dkw in self.calls:
+        addr = None
+        for (name, args, kw, dyn, dkw), fast in zip(self.calls, self.fast):
+            if fast is not None:
+                if addr is None:
+                    sh = A._stream(stream)
+                    addr = {"leaf": [b.data_ptr() for b in leaves], "tmp": [b.data_ptr() for b in tmps],
+                            "status": status.data_ptr()}
+                f, cargs, slots, _ = fast
+                for box, at, r in slots:
+                    v = sh if r.kind == "stream" else addr["status"] if r.kind == "status" else addr[r.kind][r.i]
+                    box[at] = v
+                st = f(*cargs)
+                if st != A.OK:
+                    A._check(st, name)
+                continue
             if dyn:
                 args = list(args)
                 for i in dyn:
@@ -1546,7 +1658,8 @@ def _structure(roots):
             continue
         stack.pop()
         arg = t.arg
-        items.append((t.op, t.dtype, t.shape, arg if type(arg) in _PLAIN_ARG else repr(arg),
+        ta = type(arg)
+        items.append((t.op, t.dtype, t.shape, arg if ta in _PLAIN_ARG or ta is tuple else repr(arg),
                       tuple([index[id(s)] for s in t.src])))
         index[id(t)] = len(items) - 1
     return (tuple(items), tuple([index[id(r)] for r in roots])), leaves
@@ -1560,7 +1673,10 @@ def realize_all(*ts):
     key = leaves = None
     if PLAN_CACHE:
         key, leaves = _structure(ts)
-        plan = _PLANS.get(key)
+        try:
+            plan = _PLANS.get(key)
+        except TypeError:  # an argument tuple holding something unhashable: not cached
+            key = plan = None
         if plan is not None:
             return plan.run(ex, leaves, ts)
     ex.prepare(ts)

@@ -72,3 +72,19 @@ def test_full_size_transpose(A, O):
     # spot-check against the oracle's View read on a band of rows
     ref = O.view(O.T(x.numpy(), "f32"), (8192, 8192), (1, 8192)).data
     assert np.array_equal(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("shape,strides,offset,perm", [
+    ((96, 200), (200, 1), 0, [1, 0]),            # ragged 64x64 tiles both ways
+    ((260, 132), (132, 1), 0, [1, 0]),
+    ((3, 100, 68), (6800, 68, 1), 0, [0, 2, 1]),  # one batch dim
+    ((40, 52), (72, 1), 8, [1, 0]),               # a slice: row pitch 72, 32-byte offset
+    ((2, 3, 64, 16), (4096, 1024, 16, 1), 0, [0, 1, 3, 2]),  # two batch dims that do not collapse
+])
+def test_tiled_transposes_ragged_batched_and_sliced(A, O, shape, strides, offset, perm):
+    """The tiled transpose over ragged edge tiles, batch dims and a slice
+    with an offset.  Bit-exact."""
+    g = SI.gen(sum(shape) + offset)
+    n = offset + sum((s - 1) * st for s, st in zip(shape, strides)) + 1
+    base = _base(g, n, "f32")
+    _check(A, O, base, "f32", shape, strides, offset, None, perm)
