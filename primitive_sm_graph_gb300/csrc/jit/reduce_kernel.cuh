@@ -450,6 +450,14 @@ __device__ __forceinline__ typename VT<DT>::T team_fold(typename VT<DT>::T v, in
     return v;
 }
 
+// the stash's registers: its own array, or the cached row of input A
+template <int A, int NIN, int CH>
+__device__ __forceinline__ u32 (&stash_ref(u32 (&cache)[NIN][CH][PSG_VEC], u32 (&own)[A >= 0 ? 1 : CH][PSG_VEC]))[CH][PSG_VEC]
+{
+    if constexpr (A >= 0) return cache[A];
+    else return own;
+}
+
 extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUSTER_DIMS psg_reduce(
     const __grid_constant__ PsgRedParams p)
 {
@@ -564,7 +572,9 @@ extern "C" __global__ void __launch_bounds__(kBlockThreads, kMinBlocks) PSG_CLUS
             }
         }
         u32 red[PSG_MAXSTAGES] = {0u, 0u, 0u, 0u};
-        u32 stash[kCHP][PSG_VEC];
+        // the stash, or (kStashAlias >= 0) the cached row it overwrites
+        u32 stash_own[kStashAlias >= 0 ? 1 : kCHP][PSG_VEC];
+        u32 (&stash)[kCHP][PSG_VEC] = stash_ref<kStashAlias>(cache, stash_own);
         auto stage = [&](auto st) {
             constexpr int S = decltype(st)::value;
             constexpr int OP = kStageOp[S];

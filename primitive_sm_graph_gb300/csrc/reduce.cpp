@@ -269,21 +269,53 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     const int kch = columnar ? 0 : ch_per * words <= RED_CACHE_WORDS || staged ? (int)ch_per : 0;
     if (kch == 0) stash = -1;
     const int stash_node = stash >= 0 ? stages[stash].n_nodes - 1 : -1;
+    // the stash may overwrite the cached row in place when nothing reads the
+    // row after the stash stage: that stage is the last, the epilogue reads
+    // no cached input past the stash (the values only the stash needed are
+    // dropped), and the row is one 32-bit input (its words match the
+    // stash's).  The row and the stash then share one set of registers.
+    int stash_alias = -1;
+    if (stash >= 0 && stash == n_stages - 1 && !staged) {
+        int cached = -1, ncached = 0;
+        for (int k = 0; k < n_in; ++k)
+            if (cache_in[k]) { cached = k; ++ncached; }
+        if (ncached == 1 && dtype_size(dts[cached]) == 4) {
+            std::vector<char> need(n_epi, 0);
+            need[n_epi - 1] = 1;
+            bool reads = false;
+            for (int i = n_epi - 1; i >= 0; --i) {
+                if (!need[i]) continue;
+                const psg_node& x = epi[i];
+                if (i == stash_node) continue;  // read from the stash, its operands not needed
+                if (x.op == PSG_OP_LOAD) {
+                    if (x.a == cached && !E.uni[i]) reads = true;
+                    continue;
+                }
+                if (x.op == PSG_OP_CONST || x.op == PSG_OP_RED) continue;
+                const int nops = x.op == PSG_OP_WHERE ? 3 : (x.op == PSG_OP_NEG || x.op == PSG_OP_EXP ||
+                                                             x.op == PSG_OP_LOG || x.op == PSG_OP_SQRT ||
+                                                             x.op == PSG_OP_RECIP || x.op == PSG_OP_CAST) ? 1 : 2;
+                const int ops[3] = {x.a, x.b, x.c};
+                for (int o = 0; o < nops; ++o)
+                    if (ops[o] >= 0 && ops[o] < i) need[ops[o]] = 1;
+            }
+            if (!reads) stash_alias = cached;
+        }
+    }
     // resident blocks the launch bound asks registers for: what the ring
     // leaves room for in staged mode; with the row in registers, as many as
-    // leave each thread its cached words and stash plus about 56 working
-    // registers, so nothing spills (measured on one GB300: the 4096 x 1024
-    // float32 softmax, 104 registers estimated, 13.0 us with 2 blocks of
-    // 115 registers against 15.0 us with 4 blocks of 64 that spilled 140
-    // bytes; the GPT block's replayed step 0.565 against 0.572 ms); else 4;
-    // columnar, 512 threads an SM, so the unrolled stream keeps its loads in
-    // registers
+    // leave each thread its cached words and stash plus about 50 working
+    // registers, so nothing spills (the 50 fits -Xptxas -v over the GPT
+    // block's reductions and the C3a softmax; measured on one GB300, the
+    // softmax went from 15.0 us, 4 blocks of 64 registers that spilled 140
+    // bytes, to 13.0 us with 2 blocks of 115); else 4; columnar, 512 threads
+    // an SM, so the unrolled stream keeps its loads in registers
     int min_blocks = 4;
     if (staged) {
         min_blocks = (int)((227 * 1024) / (P->smem + 1024));
         min_blocks = min_blocks < 1 ? 1 : min_blocks > 4 ? 4 : min_blocks;
     } else if (kch > 0) {
-        const int est = kch * words + (stash >= 0 ? kch * PSG_VEC : 0) + 56;
+        const int est = kch * words + (stash >= 0 && stash_alias < 0 ? kch * PSG_VEC : 0) + 50;
         min_blocks = std::max(1, std::min(4, 65536 / (RED_THREADS * est)));
     }
     // columnar: 32 rows a CTA and up to 16 members (warps), as many as keep
@@ -353,6 +385,7 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
     spec += "constexpr int kCH = " + std::to_string(kch) + ";\n";
     spec += "constexpr int kCacheIn[] = " + int_list(cache_in, n_in) + ";\n";
     spec += "constexpr int kStash = " + std::to_string(stash) + ";\n";
+    spec += "constexpr int kStashAlias = " + std::to_string(stash_alias) + ";\n";
     spec += "constexpr int kMinBlocks = " + std::to_string(min_blocks) + ";\n";
     const bool exact = kch > 0 && sp.inner % PSG_VEC == 0 && sp.chunks == (int64_t)kch * T;
     spec += "constexpr bool kExact = " + std::string(exact ? "true" : "false") + ";\n";

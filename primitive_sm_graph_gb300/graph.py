@@ -873,6 +873,8 @@ class Executor:
             prog, inputs = self._lower(t, acc=top)
         except _TooBig:
             return None
+        if inputs and not FUSE_EPILOGUE_INPUTS:
+            return None
         S = s.src[0].shape
         conv = []
         for b, v, d in inputs:
@@ -1619,6 +1621,17 @@ class _Plan:
         return out
 
 
+#: Whether a contraction's epilogue program may read further tensors (a
+#: residual, a ReLU's saved pre-activation).  Off: only programs of the
+#: accumulator alone (a ReLU, a cast) fuse.  Measured on one GB300 at the GPT
+#: block's shapes, an input in the epilogue costs about 1.5-2 us per million
+#: cells (its four warps issue the loads and the node arithmetic of every
+#: cell), as much as or more than the separate elementwise launch it replaces:
+#: the residual add at 8192 x 512 x 512, 21.1 us fused against 12.3 + 9.0 us;
+#: the ReLU-mask gradient at 8192 x 2048 x 512, 49.8 us against 24.6 + 15.8 us;
+#: a ReLU alone, 29.4 us against 24.6 + 11.7 us.
+FUSE_EPILOGUE_INPUTS = False
+
 #: graph structure -> recorded plan; PLAN_CACHE = False (or PSG_NO_PLAN_CACHE
 #: in the environment) schedules every realization afresh
 _PLANS = {}
@@ -1662,7 +1675,8 @@ def _structure(roots):
         items.append((t.op, t.dtype, t.shape, arg if ta in _PLAIN_ARG or ta is tuple else repr(arg),
                       tuple([index[id(s)] for s in t.src])))
         index[id(t)] = len(items) - 1
-    return (tuple(items), tuple([index[id(r)] for r in roots])), leaves
+    # the schedule also depends on the fusion switch
+    return (tuple(items), tuple([index[id(r)] for r in roots]), FUSE_EPILOGUE_INPUTS), leaves
 
 
 def realize_all(*ts):

@@ -281,25 +281,29 @@ def test_gpt_block_full_size(O):
     _gpt_compare(O, **SI.GPT_SHAPES, seed=0, nthreads=os.cpu_count(), same_relu_mask=True)
 
 
-def test_gpt_step_contractions_write_half_width(G):
+@pytest.mark.parametrize("inputs", [False, True])
+def test_gpt_step_contractions_write_half_width(G, monkeypatch, inputs):
     """Every contraction of the GPT block step is read only through a CAST to
     bfloat16, so each one is stored in bfloat16 by its own epilogue (no
     float32 contraction output, and no contraction computed twice), unless
-    an elementwise consumer runs in its epilogue: the two residual adds of
-    the forward and the ReLU mask of the MLP's backward are computed by the
-    contraction that produces their operand (psg_contract's epilogue
-    program), whose value then never goes through memory."""
+    an elementwise consumer runs in its epilogue.  With epilogue inputs
+    allowed, the two residual adds of the forward and the ReLU mask of the
+    MLP's backward are computed by the contraction that produces their
+    operand (psg_contract's epilogue program); by default (no inputs) none
+    of the step's consumers qualifies.  The loss and gradients agree."""
     from primitive_sm_graph_gb300.workloads import gpt_step
+    monkeypatch.setattr(G, "FUSE_EPILOGUE_INPUTS", inputs)
     tok, w = SI.gpt_block(6, 2, 64, 128, 128, 2, 256)
     dev = {k: v.cuda() for k, v in w.items()}
     log = _fresh_log(G)
-    gpt_step(tok.cuda(), dev, 2)
+    loss, grads = gpt_step(tok.cuda(), dev, 2)
     torch.cuda.synchronize()
     cons = [e for e in log if e[0] == "contract"]
     assert len(cons) == 15, cons        # 5 forward, 5 input gradients, 5 weight gradients
     fused = [e for e in cons if len(e) > 4]
-    assert len(fused) == 3, cons
+    assert len(fused) == (3 if inputs else 0), cons
     assert all(e[3] == "bf16" for e in cons if len(e) == 4), cons
+    assert torch.isfinite(loss).all() and all(torch.isfinite(g.float()).all() for g in grads.values())
 
 
 _PDL_SCRIPT = r"""
