@@ -415,6 +415,32 @@ class Rows:
         fn = lambda s: A.psg_contract(a, va, b, vb, c, vc, st, stream=s)
         return fn, 2.0 * M * N * K
 
+    # The GPT block's MLP backward contraction (8192 x 2048 x 512, bf16) with
+    # its ReLU-mask program fused into the epilogue, and without: profile
+    # cases only (--profile-case), not bench rows
+    def _gemm_epilogue(self, fused):
+        A = self.A
+        g = SI.gen(41)
+        M, N, K = 8192, 2048, 512
+        a = SI.normal((M, K), 0, 1, g, torch.bfloat16).cuda()
+        b = SI.normal((K, N), 0, 1, g, torch.bfloat16).cuda()
+        u = SI.normal((M, N), 0, 1, g, torch.bfloat16).cuda()
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        va = A.view_of(a, shape=(M, N, K), strides=(K, 0, 1))
+        vb = A.view_of(b, shape=(M, N, K), strides=(0, 1, N))
+        n = lambda op, x=0, y=0, z=0, dt="bf16": A.node(op, x, y, z, dtype=dt)
+        prog = [n("CONST"), n("LOAD", 0), n("CMPLT", 0, 1), n("ACC", dt="f32"), n("CAST", 3), n("WHERE", 2, 4, 0)]
+        epi = (prog, [u], [A.view_of(u)]) if fused else None
+        st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+        fn = lambda s: A.psg_contract(a, va, b, vb, c, A.view_of(c), st, stream=s, epilogue=epi)
+        return fn, lambda ms: {"ms": round(ms, 5)}
+
+    def gemm_epilogue_mask(self):
+        return self._gemm_epilogue(True)
+
+    def gemm_epilogue_plain(self):
+        return self._gemm_epilogue(False)
+
     # C4a: bf16 A,B [8192,8192] -> bf16, f32 accumulate
     def gemm_bf16(self):
         a, b = SI.contraction_bf16(0)

@@ -82,6 +82,17 @@ __device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::
 
 // key j of batch b is not hidden by the per-key mask (limn, "The op set":
 // masking is a flag per key that composes with causal)
+// 2^x, the hardware base-2 approximation (subnormal results flush to 0, as
+// __expf's do): the score path works in the log2 domain, x = S c - m with
+// c = scale log2(e), so each score costs one FFMA and this
+__device__ __forceinline__ float ex2(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
+
 __device__ __forceinline__ bool key_on(const AttnParams& p, int b, int j)
 {
     return !p.kmask || p.kmask[(int64_t)b * p.km_sb + j] != 0;
@@ -210,15 +221,20 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
         bool ok = __all_sync(0xffffffffu, bar_wait(&bars->s_full, 0u, &bars->abort, p.status));
         tc_fence_after();
         const int kmax = p.causal ? min(i + 1, p.T) : p.T;  // keys 0 .. kmax-1 are visible
+        // the warp's smallest kmax: 32-key groups below it need no per-key tests
+        const int kmin_w = p.kmask ? 0 : (p.causal ? min(q0 + 32 * g + 1, p.T) : p.T);
+        // scores in the log2 domain: m is the max of S c, c = scale log2(e)
+        const float c2 = p.scale * LOG2E;
         float m = -INFINITY;
         if (ok) {
             for (int c = c_beg; c < c_end; c += 32) {
                 uint32_t s[32];
                 __syncwarp();
                 tmem_ld32(trow + (uint32_t)c, s);
+                const bool full = c + 32 <= kmin_w;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (c + j < kmax && key_on(p, b, c + j)) m = fmaxf(m, p.scale * __uint_as_float(s[j]));
+                    if (full || (c + j < kmax && key_on(p, b, c + j))) m = fmaxf(m, __uint_as_float(s[j]) * c2);
             }
         }
         red_m[half * QT + r] = m;
@@ -231,13 +247,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
                 __syncwarp();
                 tmem_ld32(trow + (uint32_t)c, s);
                 uint32_t w[16];
+                const bool full = c + 32 <= kmin_w;
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
-                    // l sums the float32 weights (L = m + log l is the row's
-                    // logsumexp); P is rounded to bf16 only as the MMA operand
-                    const bool v0 = c + j < kmax && key_on(p, b, c + j), v1 = c + j + 1 < kmax && key_on(p, b, c + j + 1);
-                    const float e0 = v0 ? __expf(p.scale * __uint_as_float(s[j]) - m) : 0.0f;
-                    const float e1 = v1 ? __expf(p.scale * __uint_as_float(s[j + 1]) - m) : 0.0f;
+                    // l sums the float32 weights (L = (m + log2 l) ln 2 is the
+                    // row's logsumexp); P is rounded to bf16 only as the MMA operand
+                    const bool v0 = full || (c + j < kmax && key_on(p, b, c + j));
+                    const bool v1 = full || (c + j + 1 < kmax && key_on(p, b, c + j + 1));
+                    const float e0 = v0 ? ex2(fmaf(__uint_as_float(s[j]), c2, -m)) : 0.0f;
+                    const float e1 = v1 ? ex2(fmaf(__uint_as_float(s[j + 1]), c2, -m)) : 0.0f;
                     l += e0;
                     l += e1;
                     w[j >> 1] = pack_bf16(e0, e1);
@@ -262,7 +280,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
             if (i < p.T) {
                 // a query that sees no key at all (every key masked): O = 0, L = -inf
                 const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-                if (half == 0) p.lse[((int64_t)b * p.H + h) * p.T + i] = l > 0.0f ? m + logf(l) : -INFINITY;
+                if (half == 0) p.lse[((int64_t)b * p.H + h) * p.T + i] = l > 0.0f ? m * LN2 + logf(l) : -INFINITY;
                 __nv_bfloat16* dst = (__nv_bfloat16*)p.o + p.o_off + (int64_t)b * p.o_sb + (int64_t)i * p.o_st +
                                      (int64_t)h * p.o_sh + 32 * half;
                 uint32_t w[16];
@@ -416,6 +434,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
         const int r = 32 * g + lane;
         const int i = q0 + r;
         const uint32_t trow = tmem + ((uint32_t)(32 * g) << 16);
+        // scores in the log2 domain: m is the running max of S c, c = scale log2(e)
+        const float c2 = p.scale * LOG2E;
         float m = -INFINITY, lh = 0.0f;
         float a[32];
 #pragma unroll
@@ -425,19 +445,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
             ok = ok && __all_sync(0xffffffffu, bar_wait(&bars->s_full, (uint32_t)(j & 1), &bars->abort, p.status));
             tc_fence_after();
             const int kb = j * QT + 64 * half;  // this thread's first key of the block
+            // every key of the thread's 64 visible to every row of its warp:
+            // no per-key tests (all blocks but the diagonal and the ragged last)
+            const bool full = kb + 63 < p.T && (!p.causal || kb + 63 <= q0 + 32 * g) && !p.kmask;
             float mb = -INFINITY;
             if (ok) {
-                // the block max, 32 columns at a time (the scores are read again below)
+                // the block max, 16 columns at a time (the scores are read again below)
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 32) {
-                    uint32_t sv[32];
+                for (int cc = 0; cc < 64; cc += 16) {
+                    uint32_t sv[16];
                     __syncwarp();
-                    tmem_ld32(trow + 64u * half + (uint32_t)cc, sv);
+                    tmem_ld16(trow + 64u * half + (uint32_t)cc, sv);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
+                    for (int c = 0; c < 16; ++c) {
                         const int kj = kb + cc + c;
-                        if (kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj))
-                            mb = fmaxf(mb, p.scale * __uint_as_float(sv[c]));
+                        if (full || (kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj)))
+                            mb = fmaxf(mb, __uint_as_float(sv[c]) * c2);
                     }
                 }
             }
@@ -445,31 +468,30 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
             rm[half * QT + r] = mb;
             rows_sync();
             const float mn = fmaxf(m, fmaxf(rm[r], rm[QT + r]));  // the running max, the same in both halves
-            const float alpha = m == -INFINITY ? 0.0f : __expf(m - mn);
+            const float alpha = m == -INFINITY ? 0.0f : ex2(m - mn);
             float lb = 0.0f;
             if (ok) {
-                // 32 keys at a time: their 16 packed P columns go over S columns
-                // 64 half + cc / 2 .. + 15, which hold scores this thread has
-                // already read in this pass (keys 64 half .. 64 half + 31 of the
-                // first group, and cc / 2 < cc for the second)
+                // 16 keys at a time: their 8 packed P columns go over S columns
+                // 64 half + cc / 2 .. + 7, which hold scores this thread has
+                // already read in this pass (cc / 2 + 7 < cc + 16)
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 32) {
-                    uint32_t sv[32], w[16];
+                for (int cc = 0; cc < 64; cc += 16) {
+                    uint32_t sv[16], w[8];
                     __syncwarp();
-                    tmem_ld32(trow + 64u * half + (uint32_t)cc, sv);
+                    tmem_ld16(trow + 64u * half + (uint32_t)cc, sv);
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
+                    for (int c = 0; c < 16; c += 2) {
                         float e[2];
 #pragma unroll
                         for (int x = 0; x < 2; ++x) {
                             const int kj = kb + cc + c + x;
-                            const bool vis = kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj);
-                            e[x] = vis ? __expf(p.scale * __uint_as_float(sv[c + x]) - mn) : 0.0f;
+                            const bool vis = full || (kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj));
+                            e[x] = vis ? ex2(fmaf(__uint_as_float(sv[c + x]), c2, -mn)) : 0.0f;
                             lb += e[x];
                         }
                         w[c >> 1] = pack_bf16(e[0], e[1]);
                     }
-                    tmem_st16(trow + 64u * half + (uint32_t)(cc >> 1), w);
+                    tmem_st8(trow + 64u * half + (uint32_t)(cc >> 1), w);
                 }
                 tmem_wait_st();
             }
@@ -497,7 +519,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
         const float l = red_l[r] + red_l[QT + r];
         if (ok && i < p.T) {
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            if (half == 0) p.lse[((int64_t)b * p.H + h) * p.T + i] = l > 0.0f ? m + logf(l) : -INFINITY;
+            // L = ln(sum exp(scale S)) = (m + log2 l) ln 2
+            if (half == 0) p.lse[((int64_t)b * p.H + h) * p.T + i] = l > 0.0f ? m * LN2 + logf(l) : -INFINITY;
             __nv_bfloat16* dst = (__nv_bfloat16*)p.o + p.o_off + (int64_t)b * p.o_sb + (int64_t)i * p.o_st +
                                  (int64_t)h * p.o_sh + 32 * half;
             uint32_t w[16];
@@ -715,11 +738,15 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
         const int row = r0 + r;  // KV: key j; Q: query i
         const uint32_t trow = tmem + ((uint32_t)(32 * g) << 16);
         const int64_t lbase = ((int64_t)b * p.H + h) * p.T;
+        // P = exp(scale S - L) = 2^(S c - L log2 e), c = scale log2(e): one FFMA
+        // and one base-2 step a score
+        const float c2 = p.scale * LOG2E;
         float Lr = 0.0f, Dr = 0.0f;
         if (!KV && row < p.T) {
-            Lr = p.lse[lbase + row];
+            Lr = p.lse[lbase + row] * LOG2E;
             Dr = p.delta[lbase + row];
         }
+        const int w_lo = r0 + 32 * g, w_hi = w_lo + 31;  // this warp's own rows
         bool ok = true;
         for (int st = 0; st < nst; ++st) {
             const int t = st >> 1, s = st & 1;
@@ -729,10 +756,15 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
             if (KV) {
                 const int iq = (it0 + t) * QT + SUB * s + 32 * half + lane;
                 if (iq < p.T) {
-                    Lq = __ldg(p.lse + lbase + iq);
+                    Lq = __ldg(p.lse + lbase + iq) * LOG2E;
                     Dq = __ldg(p.delta + lbase + iq);
                 }
             }
+            // the 32 streamed rows this thread's columns cover; every pair with
+            // the warp's own rows visible: no per-pair tests
+            const int o_lo = (it0 + t) * QT + SUB * s + 32 * half, o_hi = o_lo + 31;
+            const bool full = o_hi < p.T && w_hi < p.T && !p.kmask &&
+                              (!p.causal || (KV ? w_hi <= o_lo : o_hi <= w_lo));
             ok = ok && __all_sync(0xffffffffu, bar_wait(&bars->mm1, (uint32_t)(st & 1), &bars->abort, p.status));
             tc_fence_after();
             if (ok) {
@@ -750,10 +782,10 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
                             const int c = SUB * s + 32 * half + cc + u + e;  // streamed row within its tile
                             const int other = (it0 + t) * QT + c;
                             const int i = KV ? other : row, j = KV ? row : other;
-                            const bool vis = i < p.T && j < p.T && (!p.causal || j <= i) && key_on(p, b, j);
+                            const bool vis = full || (i < p.T && j < p.T && (!p.causal || j <= i) && key_on(p, b, j));
                             const float L = KV ? __shfl_sync(0xffffffffu, Lq, cc + u + e) : Lr;
                             const float D = KV ? __shfl_sync(0xffffffffu, Dq, cc + u + e) : Dr;
-                            const float pe = vis ? __expf(p.scale * __uint_as_float(sv[u + e]) - L) : 0.0f;
+                            const float pe = vis ? ex2(fmaf(__uint_as_float(sv[u + e]), c2, -L)) : 0.0f;
                             pv[e] = pe;
                             dsv[e] = pe * (__uint_as_float(dp[u + e]) - D);
                         }
