@@ -93,6 +93,18 @@ __device__ __forceinline__ float ex2(float x)
 }
 constexpr float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 __device__ __forceinline__ bool key_on(const AttnParams& p, int b, int j)
 {
     return !p.kmask || p.kmask[(int64_t)b * p.km_sb + j] != 0;
@@ -320,7 +332,7 @@ constexpr int LFWD_SMEM = 1024 + Q_BYTES + 2 * LKV_SLOT + 256 + 2 * 2 * QT * 4 +
 constexpr uint32_t LFWD_O = 128;       // TMEM: S and P in 0..127, O_j in 128..191
 
 struct LFwdBars {
-    uint64_t q_full, kv_full[2], kv_empty[2], s_full, p_ready, o_full, o_free, drain;
+    uint64_t q_full, kv_full[2], kv_empty[2], s_full, p_ready, o_full, drain;
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -353,7 +365,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
         bar_init(&bars->s_full, 1);
         bar_init(&bars->p_ready, 8);
         bar_init(&bars->o_full, 1);
-        bar_init(&bars->o_free, 8);
         bar_init(&bars->drain, 1);
         bars->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -407,18 +418,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
                 for (int k = 0; k < HD / 16; ++k)
                     mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc_bf16(QT, QT, false), k > 0 ? 1u : 0u);
                 mma_commit(&bars->s_full);
+                // P_j is written and the running O rescaled by the row threads
                 ok = bar_wait(&bars->p_ready, (uint32_t)(j & 1), &bars->abort, p.status);
-                // O_j goes where O_{j-1} was: the row threads have read it
-                if (ok && j > 0) ok = bar_wait(&bars->o_free, (uint32_t)((j - 1) & 1), &bars->abort, p.status);
                 if (!ok) break;
                 tc_fence_after();
-                // O_j = P_j V_j: A = P from TMEM (keys 0..63 in columns 0..31, keys
-                // 64..127 in columns 64..95, 8 columns a 16-key step), B = V MN-major
+                // O += P_j V_j (the first block overwrites): A = P from TMEM (keys
+                // 0..63 in columns 0..31, keys 64..127 in columns 64..95, 8
+                // columns a 16-key step), B = V MN-major
                 const uint64_t vd = sdesc(sk + Q_BYTES, 8192u, 1024u);
 #pragma unroll
                 for (int ks = 0; ks < QT / 16; ++ks) {
                     const uint32_t pa = tmem + (ks < 4 ? 8u * ks : 64u + 8u * (ks - 4));
-                    mma_f16_ts(tmem + LFWD_O, pa, vd + 128u * ks, idesc_bf16(QT, HD, true), ks > 0 ? 1u : 0u);
+                    mma_f16_ts(tmem + LFWD_O, pa, vd + 128u * ks, idesc_bf16(QT, HD, true), (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 mma_commit(&bars->o_full);
                 mma_commit(&bars->kv_empty[s]);  // K_j and V_j read once these complete
@@ -437,9 +448,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
         // scores in the log2 domain: m is the running max of S c, c = scale log2(e)
         const float c2 = p.scale * LOG2E;
         float m = -INFINITY, lh = 0.0f;
-        float a[32];
-#pragma unroll
-        for (int d = 0; d < 32; ++d) a[d] = 0.0f;
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
             ok = ok && __all_sync(0xffffffffu, bar_wait(&bars->s_full, (uint32_t)(j & 1), &bars->abort, p.status));
@@ -448,20 +456,23 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
             // every key of the thread's 64 visible to every row of its warp:
             // no per-key tests (all blocks but the diagonal and the ragged last)
             const bool full = kb + 63 < p.T && (!p.causal || kb + 63 <= q0 + 32 * g) && !p.kmask;
+            // the thread's 64 scores: two loads and one wait a pass (the
+            // softmax pass reads them again rather than hold 64 registers
+            // across the exchange of the block max)
             float mb = -INFINITY;
             if (ok) {
-                // the block max, 16 columns at a time (the scores are read again below)
+                uint32_t sv0[32], sv1[32];
+                __syncwarp();
+                tmem_ld32_nowait(trow + 64u * half, sv0);
+                tmem_ld32_nowait(trow + 64u * half + 32u, sv1);
+                tmem_ld_wait();
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 16) {
-                    uint32_t sv[16];
-                    __syncwarp();
-                    tmem_ld16(trow + 64u * half + (uint32_t)cc, sv);
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int kj = kb + cc + c;
-                        if (full || (kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj)))
-                            mb = fmaxf(mb, __uint_as_float(sv[c]) * c2);
-                    }
+                for (int c = 0; c < 32; ++c) {
+                    const int kj = kb + c, kj1 = kb + 32 + c;
+                    if (full || (kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj)))
+                        mb = fmaxf(mb, __uint_as_float(sv0[c]) * c2);
+                    if (full || (kj1 < p.T && (!p.causal || kj1 <= i) && key_on(p, b, kj1)))
+                        mb = fmaxf(mb, __uint_as_float(sv1[c]) * c2);
                 }
             }
             float* rm = red_m + (j & 1) * 2 * QT;
@@ -471,27 +482,44 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
             const float alpha = m == -INFINITY ? 0.0f : ex2(m - mn);
             float lb = 0.0f;
             if (ok) {
-                // 16 keys at a time: their 8 packed P columns go over S columns
-                // 64 half + cc / 2 .. + 7, which hold scores this thread has
-                // already read in this pass (cc / 2 + 7 < cc + 16)
+                // P over the S columns 64 half .. + 31, 32 keys at a time (the
+                // second group's scores are read before the first group's P
+                // goes over them)
+                auto p32 = [&](const uint32_t (&sx)[32], int k0, uint32_t col) {
+                    uint32_t w[16];
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 16) {
-                    uint32_t sv[16], w[8];
-                    __syncwarp();
-                    tmem_ld16(trow + 64u * half + (uint32_t)cc, sv);
-#pragma unroll
-                    for (int c = 0; c < 16; c += 2) {
+                    for (int c = 0; c < 32; c += 2) {
                         float e[2];
 #pragma unroll
                         for (int x = 0; x < 2; ++x) {
-                            const int kj = kb + cc + c + x;
+                            const int kj = k0 + c + x;
                             const bool vis = full || (kj < p.T && (!p.causal || kj <= i) && key_on(p, b, kj));
-                            e[x] = vis ? ex2(fmaf(__uint_as_float(sv[c + x]), c2, -mn)) : 0.0f;
+                            e[x] = vis ? ex2(fmaf(__uint_as_float(sx[c + x]), c2, -mn)) : 0.0f;
                             lb += e[x];
                         }
                         w[c >> 1] = pack_bf16(e[0], e[1]);
                     }
-                    tmem_st8(trow + 64u * half + (uint32_t)(cc >> 1), w);
+                    tmem_st16(trow + col, w);
+                };
+                uint32_t sv0[32], sv1[32];
+                __syncwarp();
+                tmem_ld32(trow + 64u * half, sv0);
+                tmem_ld32_nowait(trow + 64u * half + 32u, sv1);
+                p32(sv0, kb, 64u * half);
+                tmem_ld_wait();
+                p32(sv1, kb + 32, 64u * half + 16u);
+                // the running O (this thread's 32 head-dim columns) takes the
+                // new max before P_j V_j adds to it: once the product of the
+                // block before has completed, and only when some row's max moved
+                if (j > 0) ok = __all_sync(0xffffffffu, bar_wait(&bars->o_full, (uint32_t)((j - 1) & 1), &bars->abort,
+                                                                 p.status));
+                tc_fence_after();
+                if (ok && j > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
+                    uint32_t o[32];
+                    tmem_ld32(trow + LFWD_O + 32u * half, o);
+#pragma unroll
+                    for (int d = 0; d < 32; ++d) o[d] = __float_as_uint(__uint_as_float(o[d]) * alpha);
+                    tmem_st32(trow + LFWD_O + 32u * half, o);
                 }
                 tmem_wait_st();
             }
@@ -500,18 +528,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive(&bars->p_ready);
-            ok = ok && __all_sync(0xffffffffu, bar_wait(&bars->o_full, (uint32_t)(j & 1), &bars->abort, p.status));
-            tc_fence_after();
-            if (ok) {
-                uint32_t o[32];
-                __syncwarp();
-                tmem_ld32(trow + LFWD_O + 32u * half, o);
+        }
+        // the last product done: O holds sum_j P_j V_j, every block at the final max
+        float a[32];
+        if (ok && nblk > 0)
+            ok = __all_sync(0xffffffffu, bar_wait(&bars->o_full, (uint32_t)((nblk - 1) & 1), &bars->abort, p.status));
+        tc_fence_after();
+        if (ok) {
+            uint32_t o[32];
+            tmem_ld32(trow + LFWD_O + 32u * half, o);
 #pragma unroll
-                for (int d = 0; d < 32; ++d) a[d] = a[d] * alpha + __uint_as_float(o[d]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) bar_arrive(&bars->o_free);
+            for (int d = 0; d < 32; ++d) a[d] = __uint_as_float(o[d]);
         }
         // l: the two key halves' sums, first half then second (one order in both threads)
         red_l[half * QT + r] = lh;
