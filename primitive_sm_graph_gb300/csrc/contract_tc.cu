@@ -8,17 +8,18 @@
 // tcgen05.mma.cta_group::1.kind::f16 (bf16 inputs, float32 accumulate in
 // TMEM), fed by TMA.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+// Warp roles (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0  TMA producer: one elected lane streams 64-deep K slices of A and
 //           B into a 4-stage shared-memory ring (128B-swizzled tiles);
 //   warp 1  MMA issuer: allocates all 512 TMEM columns (two 128x256 f32
 //           accumulators), one lane issues 4 MMAs (K = 16 each) per stage and
 //           commits the stage back to the producer;
-//   warps 2-5 epilogue: one warp per 32 TMEM lanes (rows) over all 256
-//           columns of the tile; a warp reads 64 columns with two tcgen05.ld
-//           before one wait, rounds to the output dtype once and stores
-//           (through a 128B-swizzled staging slot and a TMA store when C's
-//           layout allows), while the MMA warp fills the other accumulator.
+//   warps 2-9 epilogue: two warps per 32 TMEM lanes (rows), each over half
+//           of the tile's 256 columns; a warp reads 64 columns with two
+//           tcgen05.ld before one wait, rounds to the output dtype once and
+//           stores (through a 128B-swizzled staging slot and a TMA store when
+//           C's layout allows), while the MMA warp fills the other
+//           accumulator.
 // The CTA-pair kernel further down keeps these roles over two SMs.
 // Every wait on an mbarrier gives up after about a second: the CTA then sets
 // PSG_E_TIMEOUT in the caller's status word, drains its own copies and MMAs,

@@ -24,13 +24,19 @@ constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
 constexpr int TMEM_COLS = 512;                   // two 128 x 256 f32 accumulators
-constexpr int EPI_WARPS = 4;                     // warps 2 .. 5
+// warps 2 .. 9: warp w reads TMEM lanes 32 (w % 4) .. + 31 (the rows it may
+// access), and the two warps of a lane quadrant take one half of the tile's
+// columns each, so eight warps issue the epilogue's instructions (with four,
+// one warp a scheduler, a fused program's per-cell work outlasted the next
+// tile's products)
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_COLS = BN / 2;                 // columns of a tile one epilogue warp takes
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-// the epilogue stages 32 rows x 128 bytes at a time, two slots a warp; the
+// the epilogue stages 32 rows x 128 bytes at a time, one slot a warp; the
 // staging area follows the operand ring (so a tensor-core operand read past
 // the last stage stays inside the allocation), the barriers follow it
 constexpr int EPI_CHUNK = 4096;
-constexpr int STAGING_BYTES = EPI_WARPS * 2 * EPI_CHUNK;
+constexpr int STAGING_BYTES = EPI_WARPS * EPI_CHUNK;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + 256;
 
 struct Bars {
@@ -104,16 +110,16 @@ __device__ __forceinline__ void epi_store32(const TcParams& p, const uint32_t (&
 }
 
 // One accumulator's rows row0 .. row0 + 31 (this warp's 32 TMEM lanes, tm
-// their first column) over the tile's BN columns, which start at column
-// n_base: 64 columns per pair of TMEM loads, rounded once into the output
-// dtype (float32 partials under split-K).  With p.tma_store every 32 x
-// 128-byte piece is written into one of the warp's two 128B-swizzled staging
-// slots and leaves in one TMA store (the tensor clips rows and columns past
-// its edge); otherwise each lane stores its own row.
+// their first column) over columns c_lo .. c_lo + EPI_COLS - 1 of the tile,
+// whose first column is n_base: 64 columns per pair of TMEM loads, rounded
+// once into the output dtype (float32 partials under split-K).  With
+// p.tma_store every 32 x 128-byte piece is written into the warp's
+// 128B-swizzled staging slot and leaves in one TMA store (the tensor clips
+// rows and columns past its edge); otherwise each lane stores its own row.
 template <class Epi>
-__device__ __forceinline__ void epilogue_rows(const TcParams& p, const CUtensorMap* tmap_c, uint8_t* slots,
-                                              uint32_t& nst, uint32_t tm, int row0, int n_base, int sp, int b,
-                                              int lane)
+__device__ __forceinline__ void epilogue_rows(const TcParams& p, const CUtensorMap* tmap_c, uint8_t* slot,
+                                              uint32_t& nst, uint32_t tm, int row0, int n_base, int c_lo, int sp,
+                                              int b, int lane)
 {
     const int m = row0 + lane;
     const int64_t crow = p.c_offset + (int64_t)b * p.c_bs + (int64_t)m * p.c_rs;
@@ -131,13 +137,13 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, const CUtensorM
     if constexpr (Epi::active) {
         if (m < p.M) {
             eu = Epi::row_uni(p, b, m);
-            Epi::fetch(p, b, m, n_base, raw);
+            Epi::fetch(p, b, m, n_base + c_lo, raw);
         }
     }
 #pragma unroll 1
-    for (int c2 = 0; c2 < BN; c2 += 64) {
+    for (int c2 = c_lo; c2 < c_lo + EPI_COLS; c2 += 64) {
         if constexpr (Epi::active) {
-            if (c2 + 64 < BN && m < p.M) Epi::fetch(p, b, m, n_base + c2 + 64, next);
+            if (c2 + 64 < c_lo + EPI_COLS && m < p.M) Epi::fetch(p, b, m, n_base + c2 + 64, next);
         }
         uint32_t rr[2][32];
         __syncwarp();  // tcgen05.ld is warp-collective: reach it converged
@@ -173,9 +179,8 @@ __device__ __forceinline__ void epilogue_rows(const TcParams& p, const CUtensorM
                     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w[j])
                         : "f"(__uint_as_float(rr[j >> 4][(2 * j + 1) & 31])), "f"(__uint_as_float(rr[j >> 4][(2 * j) & 31])));
             }
-            uint8_t* slot = slots + (nst & 1u) * EPI_CHUNK;
-            if (nst >= 2) {  // the store that last read this slot is done reading it
-                if (lane == 0) bulk_wait_read1();
+            if (nst >= 1) {  // the store that last read the slot is done reading it
+                if (lane == 0) bulk_wait_read0();
                 __syncwarp();
             }
             const uint32_t row = smem_u32(slot) + (uint32_t)lane * 128u;
@@ -339,7 +344,8 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap& tmap_a, const CU
     } else {
         // ---------------- epilogue: TMEM -> registers -> global ----------------
         const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
-        uint8_t* slots = staging + (warp - 2) * 2 * EPI_CHUNK;
+        const int c_lo = ((warp - 2) >> 2) * EPI_COLS;  // and these columns of each tile
+        uint8_t* slot = staging + (warp - 2) * EPI_CHUNK;
         uint32_t nst = 0;
         uint32_t aph[2] = {0u, 0u};
         int local = 0;
@@ -349,12 +355,12 @@ __device__ __forceinline__ void tc_gemm_body(const CUtensorMap& tmap_a, const CU
             int b, mb, nb;
             tile_coords(p.num_m, p.num_n, t, b, mb, nb);
             // the epilogue program's inputs for this tile head for L2 while the products run
-            if constexpr (Epi::active) Epi::prefetch_l2(p, b, mb * BM + q * 32 + lane, nb * BN);
+            if constexpr (Epi::active) Epi::prefetch_l2(p, b, mb * BM + q * 32 + lane, nb * BN + c_lo, EPI_COLS);
             if (!bar_wait(&bars->tfull[acc], aph[acc], &bars->abort, p.status)) break;
             aph[acc] ^= 1u;
             tc_fence_after();
-            epilogue_rows<Epi>(p, &tmap_c, slots, nst, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN),
-                          mb * BM + q * 32, nb * BN, sp, b, lane);
+            epilogue_rows<Epi>(p, &tmap_c, slot, nst, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN),
+                               mb * BM + q * 32, nb * BN, c_lo, sp, b, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive(&bars->tempty[acc]);
@@ -536,7 +542,8 @@ __device__ __forceinline__ void tc_gemm2_body(const CUtensorMap& tmap_a, const C
     } else {
         // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
         const int q = warp & 3;
-        uint8_t* slots = staging + (warp - 2) * 2 * EPI_CHUNK;
+        const int c_lo = ((warp - 2) >> 2) * EPI_COLS;
+        uint8_t* slot = staging + (warp - 2) * EPI_CHUNK;
         uint32_t nst = 0;
         const uint32_t tempty0 = smem_in_rank(&bars->tempty[0], 0);
         uint32_t aph[2] = {0u, 0u};
@@ -546,12 +553,13 @@ __device__ __forceinline__ void tc_gemm2_body(const CUtensorMap& tmap_a, const C
             const int acc = local & 1;
             int b, mb, nb;
             tile_coords(p.num_m, p.num_n, t, b, mb, nb);
-            if constexpr (Epi::active) Epi::prefetch_l2(p, b, mb * P_BM + (int)rank * 128 + q * 32 + lane, nb * BN);
+            if constexpr (Epi::active)
+                Epi::prefetch_l2(p, b, mb * P_BM + (int)rank * 128 + q * 32 + lane, nb * BN + c_lo, EPI_COLS);
             if (!bar_wait(&bars->tfull[acc], aph[acc], &bars->abort, p.status)) break;
             aph[acc] ^= 1u;
             tc_fence_after();
-            epilogue_rows<Epi>(p, &tmap_c, slots, nst, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN),
-                          mb * P_BM + (int)rank * 128 + q * 32, nb * BN, sp, b, lane);
+            epilogue_rows<Epi>(p, &tmap_c, slot, nst, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN),
+                               mb * P_BM + (int)rank * 128 + q * 32, nb * BN, c_lo, sp, b, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));

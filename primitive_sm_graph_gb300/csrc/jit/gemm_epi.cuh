@@ -101,9 +101,9 @@ struct EpiJit {
         const EpiCtx c{p, b, m, 0, nullptr, nullptr, 0};
         return Prog::uni(c);
     }
-    // an L2 prefetch of row m's contiguous (EPI_VEC) inputs over the tile's
-    // BN columns from n0, one request per 128-byte line
-    __device__ __forceinline__ static void prefetch_l2(const TcParams& p, int b, int m, int n0)
+    // an L2 prefetch of row m's contiguous (EPI_VEC) inputs over `cols`
+    // columns from n0, one request per 128-byte line
+    __device__ __forceinline__ static void prefetch_l2(const TcParams& p, int b, int m, int n0, int cols)
     {
         if (m >= p.M || n0 >= p.N) return;
 #pragma unroll
@@ -112,7 +112,7 @@ struct EpiJit {
             const TcEpiOperand& o = p.epi[k];
             const int es = kEpiDt[k] == PSG_DT_F32 ? 4 : 2;  // EPI_VEC inputs are float-typed
             const char* row = (const char*)o.ptr + ((i64)b * o.sb + (i64)m * o.sm + n0) * es;
-            const int span = (p.N - n0 < BN ? p.N - n0 : BN) * es;
+            const int span = (p.N - n0 < cols ? p.N - n0 : cols) * es;
             for (int off = 0; off < span; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
         }
     }

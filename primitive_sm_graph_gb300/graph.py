@@ -1624,12 +1624,13 @@ class _Plan:
 #: Whether a contraction's epilogue program may read further tensors (a
 #: residual, a ReLU's saved pre-activation).  Off: only programs of the
 #: accumulator alone (a ReLU, a cast) fuse.  Measured on one GB300 at the GPT
-#: block's shapes, an input in the epilogue costs about 1.5-2 us per million
-#: cells (its four warps issue the loads and the node arithmetic of every
-#: cell), as much as or more than the separate elementwise launch it replaces:
-#: the residual add at 8192 x 512 x 512, 21.1 us fused against 12.3 + 9.0 us;
-#: the ReLU-mask gradient at 8192 x 2048 x 512, 49.8 us against 24.6 + 15.8 us;
-#: a ReLU alone, 29.4 us against 24.6 + 11.7 us.
+#: block's shapes, an input in the epilogue costs about as much as the
+#: separate elementwise launch it replaces (the epilogue warps issue the
+#: loads and the node arithmetic of every cell): the residual add at 8192 x
+#: 512 x 512, 19.1 us fused against 12.3 + 9.0 us; the ReLU-mask gradient at
+#: 8192 x 2048 x 512, 43.6 us against 24.6 + 15.8 us; a ReLU alone, 27.3 us
+#: against 24.6 + 11.7 us.  The GPT block's replayed step: 0.538 ms unfused,
+#: 0.552 ms with its residual adds and ReLU-mask gradient fused.
 FUSE_EPILOGUE_INPUTS = False
 
 #: graph structure -> recorded plan; PLAN_CACHE = False (or PSG_NO_PLAN_CACHE
