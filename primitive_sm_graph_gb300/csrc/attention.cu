@@ -351,9 +351,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd_long(const __grid_con
     float* red_m = (float*)((uint8_t*)bars + 256);  // [2 blocks (parity)][2 halves][128 rows]
     float* red_l = red_m + 2 * 2 * QT;               // [2 halves][128 rows]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int q0 = qt * QT;
     const int nall = (p.T + QT - 1) / QT;
+    // a 1-D grid in order of decreasing work: rank r takes query tile
+    // nall - 1 - r (causal: the tile that walks the most key blocks first)
+    // of every head and batch, so the short tiles fill the tail
+    const int hb = blockIdx.x % (p.H * p.B), rank = blockIdx.x / (p.H * p.B);
+    const int h = hb % p.H, b = hb / p.H;
+    const int qt = p.causal ? nall - 1 - rank : rank;
+    const int q0 = qt * QT;
     const int nblk = p.causal ? min(qt + 1, nall) : nall;  // key blocks any query of the tile sees
 
     if (threadIdx.x == 0) {
@@ -650,7 +655,7 @@ __device__ __forceinline__ void store_row32(const AttnTensor& t, int b, int row,
 template <bool KV>
 __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                               const CUtensorMap& tdo, const AttnTensor& g0, const AttnTensor& g1,
-                                              const AttnParams& p, int b)
+                                              const AttnParams& p, int b, int h, int rank)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -660,9 +665,12 @@ __device__ __forceinline__ void attn_bwd_pass(const CUtensorMap& tq, const CUten
     uint8_t* st1 = st0 + 2 * T_BYTES;       // KV: dO, Q: V
     BwdBars* bars = (BwdBars*)(st1 + 2 * T_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ot = blockIdx.x, h = blockIdx.y;
-    const int r0 = ot * QT;  // first own row (key in KV, query in Q)
     const int ntile = (p.T + QT - 1) / QT;
+    // own tile by rank of decreasing work: causal, a key tile sees the query
+    // tiles from its own on (the first key tile the most), a query tile the
+    // key tiles up to its own (the last query tile the most)
+    const int ot = KV || !p.causal ? rank : ntile - 1 - rank;
+    const int r0 = ot * QT;  // first own row (key in KV, query in Q)
     // streamed tiles: KV, the query tiles that see these keys; Q, the key tiles these queries see
     const int it0 = KV ? (p.causal ? ot : 0) : 0;
     const int it1 = KV ? ntile : (p.causal ? min(ot + 1, ntile) : ntile);
@@ -863,8 +871,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 2) attn_bwd(const __grid_constant
                                                            const __grid_constant__ AttnParams p)
 {
     pdl_enter();
-    if ((int)blockIdx.z < p.B) attn_bwd_pass<true>(tq, tk, tv, tdo, dv, dk, p, (int)blockIdx.z);
-    else attn_bwd_pass<false>(tq, tk, tv, tdo, dq, dq, p, (int)blockIdx.z - p.B);
+    // a 1-D grid, rank-major: every (head, pass, batch) of rank 0 (the
+    // longest tiles) first
+    const int per = p.H * 2 * p.B;
+    const int rank = (int)blockIdx.x / per, rest = (int)blockIdx.x - rank * per;
+    const int h = rest % p.H, z = rest / p.H;
+    if (z < p.B) attn_bwd_pass<true>(tq, tk, tv, tdo, dv, dk, p, z, h, rank);
+    else attn_bwd_pass<false>(tq, tk, tv, tdo, dq, dq, p, z - p.B, h, rank);
 }
 
 // 4-D tensor map over a [B, T, H, 64] bfloat16 operand: dims {64, T, H, B},
@@ -897,7 +910,10 @@ psg_status launch_attention_fwd(const AttnTensor& q, const AttnTensor& k, const 
     if (p.T > KB) {
         // more keys than one block: the online softmax over 128-key blocks
         if (set_max_dynamic_smem((const void*)attn_fwd_long, LFWD_SMEM) != cudaSuccess) return PSG_E_CUDA;
-        launch(attn_fwd_long, grid, FWD_THREADS, LFWD_SMEM, (cudaStream_t)stream, mq, mk, mv, p);
+        const int64_t nlong = (int64_t)grid.x * p.H * p.B;
+        if (nlong > 0x7fffffffll) return PSG_E_UNSUPPORTED_LAYOUT;  // one 1-D grid holds every tile
+        const dim3 lgrid((unsigned)nlong);
+        launch(attn_fwd_long, lgrid, FWD_THREADS, LFWD_SMEM, (cudaStream_t)stream, mq, mk, mv, p);
         return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
     }
     if (set_max_dynamic_smem((const void*)attn_fwd, FWD_SMEM) != cudaSuccess) return PSG_E_CUDA;
@@ -919,8 +935,9 @@ psg_status launch_attention_bwd(const AttnTensor& q, const AttnTensor& k, const 
     const int64_t rows = (int64_t)p.B * p.T * p.H;
     const int dgrid = (int)std::min<int64_t>((rows + 31) / 32, (int64_t)num_sms() * 16);  // 32 rows a block
     launch(attn_delta, dgrid, 256, 0, s, o, dO, p);
-    const unsigned tiles = (unsigned)((p.T + QT - 1) / QT);
-    const dim3 grid(tiles, (unsigned)p.H, (unsigned)(2 * p.B));
+    const int64_t tiles = (p.T + QT - 1) / QT;
+    if (tiles * p.H * 2 * p.B > 0x7fffffffll) return PSG_E_UNSUPPORTED_LAYOUT;  // one 1-D grid holds every tile
+    const dim3 grid((unsigned)(tiles * p.H * 2 * p.B));
     launch(attn_bwd, grid, BWD_THREADS, BWD_SMEM, s, mq, mk, mv, mdo, dq, dk, dv, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
