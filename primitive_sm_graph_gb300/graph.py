@@ -1457,9 +1457,6 @@ class _RawCapture:
         return call
 
 
-_PTR_MIN = 1 << 32  # device addresses lie above this; smaller ints are sizes and flags
-
-
 class _Plan:
     """The library calls one graph structure was realized into, recorded
     once (limn, "Reading the schedule": the compiled devices cache execution
@@ -1486,11 +1483,14 @@ class _Plan:
 
     def _name_ptr(self, t, ref):
         p = t.data_ptr()
-        if t.numel() == 0 or p < _PTR_MIN:
+        if p == 0:
             return
         old = self.ptrs.get(p)
         if old is not None and (old.kind, old.i) != (ref.kind, ref.i):
-            self.ptrs[p] = None  # two buffers at one address: not nameable
+            # leaves that share an address share it in every graph of this
+            # structure (the key records the aliasing): either names it
+            if not (old.kind == "leaf" and ref.kind == "leaf"):
+                self.ptrs[p] = None  # two buffers at one address: not nameable
         elif old is None and p not in self.ptrs:
             self.ptrs[p] = ref
 
@@ -1501,52 +1501,48 @@ class _Plan:
         self.keep.append(t)
 
     def _marshalled(self, raw):
-        """(C function, argument list, slots) of one recorded raw call, or
-        None; a slot is (container, index or field, ref)."""
+        """(C function, argument list, slots, raw) of one recorded raw call,
+        or None; a slot is (container, index, ref).  Which arguments hold
+        addresses comes from the C function's declared argument types: a
+        void* argument (the last one is the stream), an array of void*
+        (input pointers), an epilogue's input array.  A NULL stays as it is;
+        any other address must be a buffer the plan names."""
         if len(raw) != 1:
             return None
         f, cargs = raw[0]
+        types = getattr(f, "argtypes", None)
         cargs = list(cargs)
+        if not types or len(types) != len(cargs):
+            return None
         slots = []
-
-        def name(v):
-            if v is None or v < _PTR_MIN:
-                return False, None
-            r = self.ptrs.get(v)
-            return True, r
-
-        for i, a in enumerate(cargs):
-            if isinstance(a, int):
-                big, r = name(a)
-                if not big:
-                    continue
-                if r is None:
-                    if a == self.stream_handle and i == len(cargs) - 1:
-                        slots.append((cargs, i, _Ref("stream")))
-                        continue
-                    return None
-                slots.append((cargs, i, r))
+        for i, (a, t) in enumerate(zip(cargs, types)):
+            if t is ctypes.c_void_p:
+                if i == len(cargs) - 1:
+                    slots.append((cargs, i, _Ref("stream")))
+                elif a:
+                    r = self.ptrs.get(a)
+                    if r is None:
+                        return None
+                    slots.append((cargs, i, r))
             elif isinstance(a, ctypes.Array) and a._type_ is ctypes.c_void_p:
                 for j in range(len(a)):
-                    big, r = name(a[j])
-                    if big and r is None:
-                        return None
-                    if big:
+                    if a[j]:
+                        r = self.ptrs.get(a[j])
+                        if r is None:
+                            return None
                         slots.append((a, j, r))
             elif type(a).__name__ == "CArgObject" and isinstance(getattr(a, "_obj", None), A.psg_epilogue):
                 e = a._obj
                 for j in range(e.n_in):
-                    big, r = name(e.in_[j])
-                    if big and r is None:
-                        return None
-                    if big:
+                    if e.in_[j]:
+                        r = self.ptrs.get(e.in_[j])
+                        if r is None:
+                            return None
                         slots.append((e.in_, j, r))
-        # the stream goes last in every launch call (0: the default stream)
-        if not slots or slots[-1][2].kind != "stream":
-            if cargs and isinstance(cargs[-1], int) and cargs[-1] == self.stream_handle:
-                slots.append((cargs, len(cargs) - 1, _Ref("stream")))
-            else:
-                return None
+            elif isinstance(a, int) and t is not None and t not in (ctypes.c_int, ctypes.c_int32, ctypes.c_int64,
+                                                                    ctypes.c_size_t, ctypes.c_float,
+                                                                    ctypes.c_double, ctypes.c_bool):
+                return None  # an address-like argument of a type not described here
         return f, cargs, slots, raw
 
     def sym(self, x, key=None):
