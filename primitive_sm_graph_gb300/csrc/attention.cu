@@ -156,7 +156,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 2) attn_fwd(const __grid_constant
     float* red_m = (float*)((uint8_t*)bars + 256);  // [2 halves][128 rows]
     float* red_l = red_m + 2 * QT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // a 1-D grid, rank-major, longest tile first (as in attn_fwd_long)
+    const int nq = (p.T + QT - 1) / QT;
+    const int hb = blockIdx.x % (p.H * p.B), rank = blockIdx.x / (p.H * p.B);
+    const int h = hb % p.H, b = hb / p.H;
+    const int qt = p.causal ? nq - 1 - rank : rank;
     const int q0 = qt * QT;
     // keys any query of this tile sees; MMA steps of 16 keys past them read zeros
     const int kv_end = p.causal ? min(p.T, q0 + QT) : p.T;
@@ -917,7 +921,9 @@ psg_status launch_attention_fwd(const AttnTensor& q, const AttnTensor& k, const 
         return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
     }
     if (set_max_dynamic_smem((const void*)attn_fwd, FWD_SMEM) != cudaSuccess) return PSG_E_CUDA;
-    launch(attn_fwd, grid, FWD_THREADS, FWD_SMEM, (cudaStream_t)stream, mq, mk, mv, p);
+    const int64_t nshort = (int64_t)grid.x * p.H * p.B;
+    if (nshort > 0x7fffffffll) return PSG_E_UNSUPPORTED_LAYOUT;
+    launch(attn_fwd, dim3((unsigned)nshort), FWD_THREADS, FWD_SMEM, (cudaStream_t)stream, mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? PSG_OK : PSG_E_CUDA;
 }
 
