@@ -17,6 +17,7 @@ namespace psg {
 
 namespace {
 constexpr int RED_THREADS = 256;      // the skeleton's launch bound (row teams)
+constexpr int RED_REG_THREADS = 128;  // rows held in registers by teams of at most this many threads
 constexpr int RED_COL_THREADS = 512;  // columnar layout: at most 16 members a CTA
 static_assert(PSG_DEV_E_TIMEOUT == PSG_E_TIMEOUT, "device status code");
 }  // namespace
@@ -302,21 +303,28 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
             if (!reads) stash_alias = cached;
         }
     }
-    // resident blocks the launch bound asks registers for: what the ring
+    // Rows held in registers by teams of at most 128 threads run in blocks of
+    // 128 (RED_REG_THREADS): the register file then divides in finer steps.
+    // Resident blocks the launch bound asks registers for: what the ring
     // leaves room for in staged mode; with the row in registers, as many as
-    // leave each thread its cached words and stash plus about 50 working
-    // registers, so nothing spills (the 50 fits -Xptxas -v over the GPT
-    // block's reductions and the C3a softmax; measured on one GB300, the
-    // softmax went from 15.0 us, 4 blocks of 64 registers that spilled 140
-    // bytes, to 13.0 us with 2 blocks of 115); else 4; columnar, 512 threads
-    // an SM, so the unrolled stream keeps its loads in registers
+    // leave each thread its cached words and stash plus about 40 working
+    // registers; else 4; columnar, 512 threads an SM, so the unrolled stream
+    // keeps its loads in registers.  Measured on one GB300 over the softmax
+    // rows of 4096 x 1024 float32 (-Xptxas -v: no spill at 72 registers):
+    // 256-thread blocks with 50 working registers (3 blocks, 76 registers)
+    // took 8.8 us a launch back to back; 128-thread blocks with 40 (7 blocks,
+    // 72 registers) 7.95 us; with 32 (8 blocks, 64 registers) 8.55 us; the
+    // GPT block's replayed step 0.538, 0.534 and 0.541 ms.  One launch after
+    // an L2 flush took 12.3-12.5 us in every case.
+    const bool reg_rows = !staged && !columnar && kch > 0 && (1 << tl) <= RED_REG_THREADS;
+    const int row_block = reg_rows ? RED_REG_THREADS : RED_THREADS;
     int min_blocks = 4;
     if (staged) {
         min_blocks = (int)((227 * 1024) / (P->smem + 1024));
         min_blocks = min_blocks < 1 ? 1 : min_blocks > 4 ? 4 : min_blocks;
     } else if (kch > 0) {
-        const int est = kch * words + (stash >= 0 && stash_alias < 0 ? kch * PSG_VEC : 0) + 50;
-        min_blocks = std::max(1, std::min(4, 65536 / (RED_THREADS * est)));
+        const int est = kch * words + (stash >= 0 && stash_alias < 0 ? kch * PSG_VEC : 0) + 40;
+        min_blocks = std::max(1, std::min(4 * RED_THREADS / row_block, 65536 / (row_block * est)));
     }
     // columnar: 32 rows a CTA and up to 16 members (warps), as many as keep
     // RED_COL_MIN_CHUNKS chunks each; a cluster of C CTAs (a power of two up
@@ -352,7 +360,8 @@ psg_status plan_reduce(const psg_reduce_stage* stages, int n_stages, const psg_n
         col_members = RED_COL_THREADS / 32;
         while (col_members > 1 && sp.inner < (int64_t)col_members * (32 / VEC_RT) * 2) col_members >>= 1;
     }
-    const int block = columnar ? 32 * col_members : RED_THREADS;
+    const int block = columnar ? 32 * col_members : row_block;
+    if (!columnar && (block >> tl) < 1) return PSG_E_INVALID_ARG;  // a block holds whole teams
     if (columnar) min_blocks = std::max(1, 512 / block);
     int cluster = 1;
     if (columnar) {
