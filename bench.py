@@ -737,7 +737,7 @@ class Rows:
         return r
 
     # C5: one forward + backward of the GPT block through the graph layer
-    def gpt(self, steps=3):
+    def gpt(self, steps=10):
         from primitive_sm_graph_gb300.workloads import gpt_step
         tok, w = SI.gpt_block(0, **SI.GPT_SHAPES)
         dtok = tok.cuda()

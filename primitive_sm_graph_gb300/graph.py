@@ -52,11 +52,16 @@ class Tensor:
 
     def __init__(self, op, src, shape, dtype, arg=None, requires_grad=False):
         self.op = op
-        self.src = tuple(src)
-        self.shape = tuple(int(s) for s in shape)
+        self.src = src = tuple(src)
+        self.shape = tuple(map(int, shape))
         self.dtype = dtype
         self.arg = arg
-        self.requires_grad = requires_grad or any(s.requires_grad for s in self.src)
+        if not requires_grad:
+            for s in src:
+                if s.requires_grad:
+                    requires_grad = True
+                    break
+        self.requires_grad = requires_grad
         self.grad = None
         self._real = None
         self._users = 0
@@ -156,6 +161,8 @@ class Tensor:
     def reshape(self, *shape):
         if len(shape) == 1 and isinstance(shape[0], (tuple, list)):
             shape = tuple(shape[0])
+        if shape == self.shape:
+            return self
         shape = list(shape)
         if -1 in shape:
             i = shape.index(-1)
@@ -339,6 +346,9 @@ class Tensor:
 # ---------------------------------------------------------------- helpers -----
 
 def broadcast_shapes(*shapes):
+    first = shapes[0]
+    if all(s == first for s in shapes):
+        return tuple(first)
     n = max(len(s) for s in shapes)
     out = []
     for d in range(n):
@@ -354,8 +364,15 @@ def _lead(t: Tensor, nd: int) -> Tensor:
 
 
 def broadcast(*ts):
+    first = ts[0].shape
+    if all(t.shape == first for t in ts):
+        return ts
     shape = broadcast_shapes(*[t.shape for t in ts])
-    return tuple(_lead(t, len(shape)).expand(shape) for t in ts)
+    # a constant broadcasts to a constant of the new shape: the same value in
+    # every cell, with no movement nodes between
+    return tuple(t if t.shape == shape else
+                 Tensor("CONST", (), shape, t.dtype, arg=t.arg) if t.op == "CONST" and t._real is None else
+                 _lead(t, len(shape)).expand(shape) for t in ts)
 
 
 def _as_torch(buf: torch.Tensor, v: View, dtype: str) -> torch.Tensor:
@@ -1645,37 +1662,44 @@ def _structure(roots):
     """(key, leaf buffers) of the unrealized graph under roots: every node's
     op, dtype, shape, argument and operands by position, every leaf's
     layout, size, alignment and aliasing; equal keys schedule alike."""
-    index, items, leaves, first_ptr = {}, [], [], {}
+    index, items, leaves, first_ptr = {}, [], [], {}  # nodes hash by identity
+    add, add_leaf = items.append, leaves.append
     stack = list(reversed(roots))
+    pop, push = stack.pop, stack.append
     while stack:
         t = stack[-1]
-        if id(t) in index:
-            stack.pop()
+        if t in index:
+            pop()
             continue
-        if t._real is not None:
-            stack.pop()
-            buf, v = t._real
+        real = t._real
+        if real is not None:
+            pop()
+            buf, v = real
             p = buf.data_ptr()
             aux = t._aux
-            items.append(("L", t.dtype, t.shape, v.key(), buf.dtype, buf.numel(), p % 256,
-                          first_ptr.setdefault(p, len(leaves)), aux is not None))
-            leaves.append(buf)
+            add(("L", t.dtype, t.shape, v.key(), buf.dtype, buf.numel(), p % 256,
+                 first_ptr.setdefault(p, len(leaves)), aux is not None))
+            add_leaf(buf)
             if aux is not None:
-                leaves.append(aux)
-            index[id(t)] = len(items) - 1
+                add_leaf(aux)
+            index[t] = len(items) - 1
             continue
-        pending = [s for s in reversed(t.src) if id(s) not in index]
-        if pending:
-            stack.extend(pending)
+        src = t.src
+        waiting = False
+        for s in reversed(src):
+            if s not in index:
+                push(s)
+                waiting = True
+        if waiting:
             continue
-        stack.pop()
+        pop()
         arg = t.arg
         ta = type(arg)
-        items.append((t.op, t.dtype, t.shape, arg if ta in _PLAIN_ARG or ta is tuple else repr(arg),
-                      tuple([index[id(s)] for s in t.src])))
-        index[id(t)] = len(items) - 1
+        add((t.op, t.dtype, t.shape, arg if ta in _PLAIN_ARG or ta is tuple else repr(arg),
+             tuple([index[s] for s in src])))
+        index[t] = len(items) - 1
     # the schedule also depends on the fusion switch
-    return (tuple(items), tuple([index[id(r)] for r in roots]), FUSE_EPILOGUE_INPUTS), leaves
+    return (tuple(items), tuple([index[r] for r in roots]), FUSE_EPILOGUE_INPUTS), leaves
 
 
 def realize_all(*ts):
