@@ -35,6 +35,12 @@
  *   never traps.  An unsupported dtype, layout or program returns its own
  *   code; no call silently runs a different implementation (Tiki, "Compile
  *   model code": unsupported contracts raise a typed error).
+ * Empty sizes: a call whose result has no cells (a zero-length dim of the
+ *   output, an empty batch, sequence or head axis, no GATHER/SCATTER rows)
+ *   returns PSG_OK and writes nothing; its pointers may then be null.  A
+ *   reduction over an empty axis gives the fold's identity: SUM 0, MAX -inf
+ *   for floats and the dtype's minimum for integers, then the epilogue.  A
+ *   contraction over K = 0 writes 0 (the empty SUM) in C's dtype.
  * Thread safety: calls may be made from several host threads at once.
  * Launches: every kernel is launched with programmatic stream serialization
  *   and waits (griddepcontrol.wait) for the kernel before it on the stream
