@@ -32,7 +32,7 @@ from math import prod
 import torch
 
 from . import _abi as A
-from .tensor_util import torch_dtype
+from .tensor_util import dtype_name, torch_dtype
 from .view import View
 
 EW_UNARY = ("NEG", "EXP", "LOG", "SQRT", "RECIP", "CAST")
@@ -73,7 +73,6 @@ class Tensor:
     # ---- sources -----------------------------------------------------------
     @staticmethod
     def from_torch(t: torch.Tensor, requires_grad=False) -> "Tensor":
-        from .tensor_util import dtype_name
         t = t.contiguous()
         x = Tensor("BUF", (), t.shape, dtype_name(t.dtype), requires_grad=requires_grad)
         x._real = (t, View(t.shape))
@@ -148,7 +147,7 @@ class Tensor:
     def __gt__(self, o): return self._coerce(o).cmplt(self)
 
     def relu(self):
-        zero = Tensor.const(0.0, (), self.dtype)
+        zero = Tensor.const(0.0, self.shape, self.dtype)
         return zero.cmplt(self).where(self, zero)
 
     def square(self):
@@ -163,6 +162,10 @@ class Tensor:
             shape = tuple(shape[0])
         if shape == self.shape:
             return self
+        if -1 not in shape:
+            shape = tuple(shape)
+            assert prod(shape) == prod(self.shape), (self.shape, shape)
+            return Tensor("MOVE", (self,), shape, self.dtype, arg=("reshape", shape))
         shape = list(shape)
         if -1 in shape:
             i = shape.index(-1)
@@ -349,14 +352,13 @@ def broadcast_shapes(*shapes):
     first = shapes[0]
     if all(s == first for s in shapes):
         return tuple(first)
-    n = max(len(s) for s in shapes)
-    out = []
-    for d in range(n):
-        dims = [s[d - (n - len(s))] for s in shapes if d - (n - len(s)) >= 0]
-        m = max(dims)
-        assert all(x in (1, m) for x in dims), shapes
-        out.append(m)
-    return tuple(out)
+    n = max(map(len, shapes))
+    cols = list(zip(*[(1,) * (n - len(s)) + tuple(s) for s in shapes]))
+    out = tuple(max(c) for c in cols)
+    for c, m in zip(cols, out):
+        for x in c:
+            assert x == 1 or x == m, shapes
+    return out
 
 
 def _lead(t: Tensor, nd: int) -> Tensor:
@@ -1496,6 +1498,7 @@ class _Plan:
         self.stream_handle = A._stream(ex._s())
         self.allocs, self.keep, self.calls, self.outs, self.log = [], [], [], [], []
         self.fast = []
+        self._flat = None  # the slots with flat address indices, made at the first replay
         self.ok = True
 
     def _name_ptr(self, t, ref):
@@ -1516,6 +1519,24 @@ class _Plan:
         self._name_ptr(t, self.refs[id(t)])
         self.allocs.append(spec)
         self.keep.append(t)
+
+    def _flat_slots(self, n_leaves):
+        """Each marshalled call's slots as (container, index, k): k indexes
+        the leaves' addresses, then the allocated buffers', then the status
+        word and the stream (computed once per plan)."""
+        flat = self._flat
+        if flat is None:
+            nt = len(self.allocs)
+
+            def k(r):
+                if r.kind == "leaf":
+                    return r.i
+                if r.kind == "tmp":
+                    return n_leaves + r.i
+                return n_leaves + nt + (0 if r.kind == "status" else 1)
+            flat = [None if f is None else [(box, at, k(r)) for box, at, r in f[2]] for f in self.fast]
+            self._flat = flat
+        return flat
 
     def _marshalled(self, raw):
         """(C function, argument list, slots, raw) of one recorded raw call,
@@ -1601,17 +1622,18 @@ class _Plan:
             if isinstance(x, (list, tuple)):
                 return type(x)(val(y) for y in x)
             return x
-        addr = None
-        for (name, args, kw, dyn, dkw), fast in zip(self.calls, self.fast):
+        vals = None
+        flat = self._flat_slots(len(leaves))
+        for (name, args, kw, dyn, dkw), fast, fslots in zip(self.calls, self.fast, flat):
             if fast is not None:
-                if addr is None:
-                    sh = A._stream(stream)
-                    addr = {"leaf": [b.data_ptr() for b in leaves], "tmp": [b.data_ptr() for b in tmps],
-                            "status": status.data_ptr()}
-                f, cargs, slots, _ = fast
-                for box, at, r in slots:
-                    v = sh if r.kind == "stream" else addr["status"] if r.kind == "status" else addr[r.kind][r.i]
-                    box[at] = v
+                if vals is None:
+                    # every address a slot can take, in the flat order of _flat_slots
+                    vals = [b.data_ptr() for b in leaves] + [b.data_ptr() for b in tmps]
+                    vals.append(status.data_ptr())
+                    vals.append(A._stream(stream))
+                f, cargs = fast[0], fast[1]
+                for box, at, k in fslots:
+                    box[at] = vals[k]
                 st = f(*cargs)
                 if st != A.OK:
                     A._check(st, name)
@@ -1647,6 +1669,9 @@ class _Plan:
 #: with the residual adds alone fused (each a win measured on its own: the
 #: step's standalone add shares its launch with the work around it).
 FUSE_EPILOGUE_INPUTS = False
+
+#: entries the executor's call log keeps (older ones are dropped)
+LOG_KEEP = 1 << 14
 
 #: graph structure -> recorded plan; PLAN_CACHE = False (or PSG_NO_PLAN_CACHE
 #: in the environment) schedules every realization afresh
@@ -1707,6 +1732,8 @@ def realize_all(*ts):
     computed once) and return them as torch tensors.  The schedule of a
     graph structure seen before is replayed from the plan cache."""
     ex = _executor()
+    if len(ex.log) > LOG_KEEP:  # keep the recent calls only: a long eager loop would grow it forever
+        del ex.log[:len(ex.log) - LOG_KEEP // 2]
     key = leaves = None
     if PLAN_CACHE:
         key, leaves = _structure(ts)
