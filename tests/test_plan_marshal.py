@@ -179,3 +179,13 @@ def test_gpt_step_replay_covers_every_call_kind(cpu_graph):
     ins = [tok2] + [w2[k] for k in sorted(w2)]
     a, b = _canon(replayed, ins, status, fake.real), _canon(fresh, ins, status, fake.real)
     assert a == b
+
+
+def test_executor_log_stays_bounded(cpu_graph, monkeypatch):
+    """A long eager loop keeps only the recent calls in the executor's log."""
+    monkeypatch.setattr(G, "LOG_KEEP", 8)
+    g = torch.Generator().manual_seed(5)
+    x, y = torch.randn((16, 8), generator=g), torch.randn((8, 4), generator=g)
+    for _ in range(40):
+        _run(x, y)
+    assert 0 < len(G._executor().log) <= 8 + 2   # one step's two calls past the trim
