@@ -1838,6 +1838,15 @@ def _sum_to(g: Tensor, shape) -> Tensor:
     return g
 
 
+def _is_relu(t: Tensor) -> bool:
+    """t = WHERE(CMPLT(0, x), x, 0), the form Tensor.relu builds."""
+    if t.op != "WHERE":
+        return False
+    c, x, y = t.src
+    return (c.op == "CMPLT" and c.src[1] is x and c.src[0].op == "CONST" and c.src[0].arg == 0.0
+            and y.op == "CONST" and y.arg == 0.0 and c.src[0]._real is None and y._real is None)
+
+
 def _vjp(t: Tensor, g: Tensor):
     op, s = t.op, t.src
     if op == "ADD":
@@ -1858,7 +1867,13 @@ def _vjp(t: Tensor, g: Tensor):
         return [(s[0], g.cast(s[0].dtype))] if s[0].dtype in FLOATS else []
     if op == "WHERE":
         z = Tensor.const(0.0, (), g.dtype)
-        return [(s[1], s[0].where(g, z)), (s[2], s[0].where(z, g))]
+        c = s[0]
+        if _is_relu(t):
+            # 0 < x and 0 < relu(x) are the same bit for every x (NaN and -0
+            # included), so the mask is taken from the output: the input is
+            # then read by nothing but the ReLU itself
+            c = Tensor.const(0.0, t.shape, t.dtype).cmplt(t)
+        return [(s[1], c.where(g, z)), (s[2], s[0].where(z, g))]
     if op == "SUM":
         return [(s[0], g.expand(s[0].shape))]
     if op == "MAX":

@@ -286,11 +286,13 @@ def test_gpt_step_contractions_write_half_width(G, monkeypatch, inputs):
     """Every contraction of the GPT block step is read only through a CAST to
     bfloat16, so each one is stored in bfloat16 by its own epilogue (no
     float32 contraction output, and no contraction computed twice), unless
-    an elementwise consumer runs in its epilogue.  With epilogue inputs
-    allowed, the two residual adds of the forward and the ReLU mask of the
-    MLP's backward are computed by the contraction that produces their
-    operand (psg_contract's epilogue program); by default (no inputs) none
-    of the step's consumers qualifies.  The loss and gradients agree."""
+    an elementwise consumer runs in its epilogue.  The MLP's ReLU reads
+    nothing but the up-projection's total (its backward takes the mask from
+    the ReLU's output), so it always runs in that contraction's epilogue
+    program.  With epilogue inputs allowed, the two residual adds of the
+    forward and the ReLU mask of the MLP's backward are also computed by the
+    contraction that produces their operand.  The loss and gradients are
+    finite."""
     from primitive_sm_graph_gb300.workloads import gpt_step
     monkeypatch.setattr(G, "FUSE_EPILOGUE_INPUTS", inputs)
     tok, w = SI.gpt_block(6, 2, 64, 128, 128, 2, 256)
@@ -301,7 +303,8 @@ def test_gpt_step_contractions_write_half_width(G, monkeypatch, inputs):
     cons = [e for e in log if e[0] == "contract"]
     assert len(cons) == 15, cons        # 5 forward, 5 input gradients, 5 weight gradients
     fused = [e for e in cons if len(e) > 4]
-    assert len(fused) == (3 if inputs else 0), cons
+    assert len(fused) == (4 if inputs else 1), cons
+    assert any(e[1] == (128, 256, 128) and e[4] == 5 for e in fused), cons   # the ReLU: ACC CAST CONST CMPLT WHERE
     assert all(e[3] == "bf16" for e in cons if len(e) == 4), cons
     assert torch.isfinite(loss).all() and all(torch.isfinite(g.float()).all() for g in grads.values())
 
