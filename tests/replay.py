@@ -347,9 +347,13 @@ class Replayer:
         self._saved = {}
 
     def __enter__(self):
+        from primitive_sm_graph_gb300 import graph as G
         self._old_threads = self.O.NTHREADS
         if self.nthreads:
             self.O.NTHREADS = self.nthreads
+        # a plan recorded earlier would replay its raw C calls past these
+        # wrappers: schedule every call afresh while the replay is active
+        self._old_plan_cache, G.PLAN_CACHE = G.PLAN_CACHE, False
         for name in self.WRAPPED:
             f = getattr(self.A, name)
             self._saved[name] = f
@@ -357,9 +361,11 @@ class Replayer:
         return self
 
     def __exit__(self, *exc):
+        from primitive_sm_graph_gb300 import graph as G
         for name, f in self._saved.items():
             setattr(self.A, name, f)
         self.O.NTHREADS = self._old_threads
+        G.PLAN_CACHE = self._old_plan_cache
         return False
 
     def failures(self):

@@ -189,3 +189,71 @@ def test_executor_log_stays_bounded(cpu_graph, monkeypatch):
     for _ in range(40):
         _run(x, y)
     assert 0 < len(G._executor().log) <= 8 + 2   # one step's two calls past the trim
+
+
+def _header_writes():
+    """Per C function, the positions of its non-const pointer parameters
+    (other than the status word and the stream): what it writes, read from
+    include/psg.h's declarations."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(__file__), "..", "include", "psg.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"psg_status\s+(psg_\w+)\s*\(([^)]*)\)\s*;", src):
+        params = [p.strip() for p in m.group(2).split(",")]
+        w = []
+        for i, p in enumerate(params):
+            name = re.split(r"[\s*]+", p)[-1]
+            if "*" in p and not p.startswith("const") and name not in ("d_status", "stream"):
+                w.append(i)
+        out[m.group(1)] = tuple(w)
+    return out
+
+
+def test_written_arguments_match_the_header():
+    hw = _header_writes()
+    for fn, pos in G._WRITES.items():
+        assert hw[fn] == pos, (fn, hw[fn], pos)
+
+
+@pytest.mark.parametrize("streams", [2, 3])
+def test_forked_schedule_orders_every_conflicting_pair(cpu_graph, monkeypatch, streams):
+    """The forked-stream schedule of the GPT block's recorded step: every
+    pair of calls that touch one buffer, one of them writing it (writes from
+    the header's non-const pointers), is ordered by stream order or by the
+    waits; the step's independent calls spread over more than one stream."""
+    import seeded_inputs as SI
+    from primitive_sm_graph_gb300.workloads import gpt_step
+    monkeypatch.setattr(G, "FORK_STREAMS", streams)
+    tok, w = SI.gpt_block(6, 2, 64, 128, 128, 2, 256)
+    gpt_step(tok, w, 2)
+    plan = next(iter(G._PLANS.values()))
+    n_leaves = 1 + max(r.i for r in plan.refs.values() if r.kind == "leaf")
+    where, waits = plan._fork_schedule(n_leaves)
+    hw = _header_writes()
+    flat = plan._flat_slots(n_leaves)
+    nb = n_leaves + len(plan.allocs)
+    acc = []
+    for fast, fs in zip(plan.fast, flat):
+        bufs = {k for _, _, k in fs if k < nb}
+        wr = {k for box, at, k in fs if k < nb and box is fast[1] and at in hw[fast[4]]} if fast[4] in hw else bufs
+        acc.append((bufs, wr))
+    n = len(acc)
+    # happens-before: stream order plus the waits, closed transitively
+    before = [set() for _ in range(n)]
+    last_on = {}
+    for c in range(n):
+        preds = set(waits[c])
+        if where[c] in last_on:
+            preds.add(last_on[where[c]])
+        for p in preds:
+            before[c] |= before[p] | {p}
+        last_on[where[c]] = c
+    for j in range(n):
+        for i in range(j):
+            bi, wi = acc[i]
+            bj, wj = acc[j]
+            if (wi & bj) or (wj & bi):
+                assert i in before[j], (i, j, plan.fast[i][4], plan.fast[j][4])
+    assert len(set(where)) > 1
