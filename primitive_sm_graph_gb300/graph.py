@@ -1480,7 +1480,9 @@ class _RawCapture:
 #: call on the capturing stream, in order).  Measured on one GB300, the GPT
 #: block's replayed step: 0.527 ms on one stream, 0.506 ms on two, 0.520 ms
 #: on three (more side streams put more contractions side by side, which
-#: then compete for the SMs).  Eager calls always run on the current stream.
+#: then compete for the SMs); keeping contractions off the side streams was
+#: slower still (0.520, 0.538 and 0.514 ms on two, three and four streams).
+#: Eager calls always run on the current stream.
 FORK_STREAMS = int(os.environ.get("PSG_FORK_STREAMS", "2"))
 
 #: The pointer arguments each library call writes, by position; every other
