@@ -61,6 +61,33 @@ def test_gpt_block_step_replay_is_bit_exact(G):
     assert not _same(got2[0], got[0])          # the loss did change with the inputs
 
 
+def test_gpt_block_full_size_replay_is_bit_exact(G):
+    """The bench's GPT block (B32, T256, d512) recorded once, its independent
+    calls on forked streams: every replay gives eager's bits, over several
+    replays and new inputs (a missing dependency edge between the streams
+    would let a call read a buffer before or after it is written)."""
+    from primitive_sm_graph_gb300.workloads import GPT_WEIGHTS, gpt_step
+    H = SI.GPT_SHAPES["H"]
+
+    def step(tok, *ws):
+        loss, grads = gpt_step(tok, dict(zip(GPT_WEIGHTS, ws)), H)
+        return (loss,) + tuple(grads[k] for k in GPT_WEIGHTS)
+
+    tok, w = SI.gpt_block(11, **SI.GPT_SHAPES)
+    ins = [tok.cuda()] + [w[k].cuda() for k in GPT_WEIGHTS]
+    rep = G.Replay(step, *ins)
+    ref = [t.clone() for t in step(*ins)]
+    for _ in range(3):
+        got = rep(*ins)
+        assert all(_same(x, y) for x, y in zip(got, ref))
+    tok2, w2 = SI.gpt_block(12, **SI.GPT_SHAPES)
+    ins2 = [tok2.cuda()] + [w2[k].cuda() for k in GPT_WEIGHTS]
+    ref2 = [t.clone() for t in step(*ins2)]
+    for _ in range(3):
+        got2 = rep(*ins2)
+        assert all(_same(x, y) for x, y in zip(got2, ref2))
+
+
 def test_gpt_train_step_replay_updates_like_eager(G):
     """Forward, backward and AdamW recorded once: replayed twice from the
     same start it gives the eager weights bit for bit."""
